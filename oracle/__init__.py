@@ -1,0 +1,170 @@
+"""CPU oracle for the stride-1, pad-1 3x3 convolution (fwd, dgrad, wgrad, dbias).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py``; never by the product path.
+
+The arithmetic lives in ``conv3x3_oracle.c`` (plain fp64 loop nests, pthreads over
+the outermost independent loop).  This module only compiles it with the host C
+compiler and marshals numpy arrays through ctypes.  It shares nothing with the
+CUDA library.
+
+The definitions follow the textbook / PyTorch ``Conv2d`` cross-correlation that
+the subject page (clu0's C++/CUDA UNet diffusion, sourcepulse.org project page,
+"How It Works" and "Highlighted Details") implies when it speaks of 3x3
+convolution kernels forward and backward that aim to match PyTorch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "conv3x3_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+_i64 = ctypes.c_int64
+_dp = ctypes.POINTER(ctypes.c_double)
+_lp = ctypes.POINTER(ctypes.c_int64)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/liboracle.so`` (gcc, -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-shared", "-fPIC",
+               "-pthread", _SRC, "-o", tmp, "-lm"]
+        subprocess.check_call(cmd)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
+        lib.oracle_get_threads.restype = ctypes.c_int
+        lib.oracle_silu_f64.argtypes = [ctypes.c_double]
+        lib.oracle_silu_f64.restype = ctypes.c_double
+        lib.oracle_conv3x3_fwd_f64.argtypes = [_dp, _dp, _dp, _dp] + [_i64] * 5 + [ctypes.c_int]
+        lib.oracle_conv3x3_fwd_at_f64.argtypes = [_dp, _dp, _dp] + [_i64] * 5 + [ctypes.c_int, _lp, _i64, _dp]
+        lib.oracle_conv3x3_dgrad_f64.argtypes = [_dp, _dp, _dp] + [_i64] * 5
+        lib.oracle_conv3x3_dgrad_at_f64.argtypes = [_dp, _dp] + [_i64] * 5 + [_lp, _i64, _dp]
+        lib.oracle_conv3x3_wgrad_f64.argtypes = [_dp, _dp, _dp, _dp] + [_i64] * 5
+        lib.oracle_conv3x3_wgrad_at_f64.argtypes = [_dp, _dp] + [_i64] * 5 + [_lp, _i64, _dp]
+        lib.oracle_conv3x3_dbias_f64.argtypes = [_dp, _dp] + [_i64] * 4
+        _lib = lib
+    return _lib
+
+
+def _d(a, shape=None):
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    if shape is not None and a.shape != tuple(shape):
+        a = a.reshape(shape)
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_dp)
+
+
+def set_threads(n: int) -> None:
+    """0 = all online cores (the default)."""
+    _load().oracle_set_threads(int(n))
+
+
+def threads() -> int:
+    return int(_load().oracle_get_threads())
+
+
+def silu(z: float) -> float:
+    return float(_load().oracle_silu_f64(float(z)))
+
+
+def conv3x3_fwd(x, w, bias=None, act: int = 0):
+    """y[n,h,w,k] = act(b[k] + sum_{r,s,c} x[n,h+r-1,w+s-1,c] w[k,r,s,c]); x NHWC, w KRSC."""
+    x = _d(x)
+    N, H, W, Cin = x.shape
+    w = _d(w)
+    Cout = w.shape[0]
+    assert w.shape == (Cout, 3, 3, Cin), w.shape
+    b = None if bias is None else _d(bias, (Cout,))
+    y = np.empty((N, H, W, Cout), np.float64)
+    _load().oracle_conv3x3_fwd_f64(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, Cin, Cout, H, W, int(act))
+    return y
+
+
+def conv3x3_fwd_at(x, w, bias, act, idx):
+    """Forward outputs at the given linear NHWC indices of y."""
+    x = _d(x)
+    N, H, W, Cin = x.shape
+    w = _d(w)
+    Cout = w.shape[0]
+    b = None if bias is None else _d(bias, (Cout,))
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    out = np.empty(idx.shape[0], np.float64)
+    _load().oracle_conv3x3_fwd_at_f64(_ptr(x), _ptr(w), _ptr(b), N, Cin, Cout, H, W, int(act),
+                                      idx.ctypes.data_as(_lp), idx.shape[0], _ptr(out))
+    return out
+
+
+def conv3x3_dgrad(dz, w):
+    """dx[n,h,w,c] = sum_{r,s,k} dz[n,h+1-r,w+1-s,k] w[k,r,s,c]."""
+    dz = _d(dz)
+    N, H, W, Cout = dz.shape
+    w = _d(w)
+    Cin = w.shape[3]
+    assert w.shape == (Cout, 3, 3, Cin), w.shape
+    dx = np.empty((N, H, W, Cin), np.float64)
+    _load().oracle_conv3x3_dgrad_f64(_ptr(dz), _ptr(w), _ptr(dx), N, Cin, Cout, H, W)
+    return dx
+
+
+def conv3x3_dgrad_at(dz, w, idx):
+    dz = _d(dz)
+    N, H, W, Cout = dz.shape
+    w = _d(w)
+    Cin = w.shape[3]
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    out = np.empty(idx.shape[0], np.float64)
+    _load().oracle_conv3x3_dgrad_at_f64(_ptr(dz), _ptr(w), N, Cin, Cout, H, W,
+                                        idx.ctypes.data_as(_lp), idx.shape[0], _ptr(out))
+    return out
+
+
+def conv3x3_wgrad(x, dz):
+    """(dw[k,r,s,c], db[k]) = (sum_p dz[p,k] x[p+(r-1,s-1),c], sum_p dz[p,k])."""
+    x = _d(x)
+    N, H, W, Cin = x.shape
+    dz = _d(dz)
+    Cout = dz.shape[3]
+    assert dz.shape[:3] == (N, H, W)
+    dw = np.empty((Cout, 3, 3, Cin), np.float64)
+    db = np.empty((Cout,), np.float64)
+    _load().oracle_conv3x3_wgrad_f64(_ptr(x), _ptr(dz), _ptr(dw), _ptr(db), N, Cin, Cout, H, W)
+    return dw, db
+
+
+def conv3x3_wgrad_at(x, dz, idx):
+    """dw at the given linear KRSC indices (each a full sum over all pixels)."""
+    x = _d(x)
+    N, H, W, Cin = x.shape
+    dz = _d(dz)
+    Cout = dz.shape[3]
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    out = np.empty(idx.shape[0], np.float64)
+    _load().oracle_conv3x3_wgrad_at_f64(_ptr(x), _ptr(dz), N, Cin, Cout, H, W,
+                                        idx.ctypes.data_as(_lp), idx.shape[0], _ptr(out))
+    return out
+
+
+def conv3x3_dbias(dz):
+    dz = _d(dz)
+    N, H, W, Cout = dz.shape
+    db = np.empty((Cout,), np.float64)
+    _load().oracle_conv3x3_dbias_f64(_ptr(dz), _ptr(db), N, Cout, H, W)
+    return db

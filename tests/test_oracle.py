@@ -1,0 +1,357 @@
+"""Pins for the CPU oracle: checks against closed forms, identities, library
+special cases and brute force -- never against the oracle itself.
+
+Each check is chosen so that a plausible slip in the oracle (flipped kernel,
+wrong padding side, transposed weight operand, dropped bias, missing tap,
+swapped dgrad tap mirror, a wgrad shifted the wrong way) fails at least one of
+them; ``test_pins_catch_planted_mistakes`` demonstrates that on mutated copies
+of the oracle's own loop nests.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+def rand(*shape):
+    return rng.standard_normal(shape)
+
+
+# ---------------------------------------------------------------------------
+# closed forms
+# ---------------------------------------------------------------------------
+def test_centre_delta_reproduces_input():
+    C = 5
+    x = rand(2, 4, 6, C)
+    w = np.zeros((C, 3, 3, C))
+    for k in range(C):
+        w[k, 1, 1, k] = 1.0
+    y = oracle.conv3x3_fwd(x, w)
+    assert np.array_equal(y, x)
+
+
+@pytest.mark.parametrize("r", [0, 1, 2])
+@pytest.mark.parametrize("s", [0, 1, 2])
+def test_off_centre_delta_shifts_with_zero_fill(r, s):
+    # y[h, w] = x[h + r - 1, w + s - 1], zero where that leaves the image
+    C = 3
+    x = rand(1, 5, 4, C)
+    w = np.zeros((C, 3, 3, C))
+    for k in range(C):
+        w[k, r, s, k] = 1.0
+    y = oracle.conv3x3_fwd(x, w)
+    xp = np.zeros((1, 7, 6, C))
+    xp[:, 1:6, 1:5] = x
+    expect = xp[:, r:r + 5, s:s + 4]
+    assert np.array_equal(y, expect)
+
+
+def test_all_ones_kernel_on_constant_input_gives_9_6_4_pattern():
+    Cin, cval = 4, 0.75
+    H, W = 5, 6
+    x = np.full((1, H, W, Cin), cval)
+    w = np.ones((2, 3, 3, Cin))
+    y = oracle.conv3x3_fwd(x, w)
+    nh = np.array([2] + [3] * (H - 2) + [2])
+    nw = np.array([2] + [3] * (W - 2) + [2])
+    taps = nh[:, None] * nw[None, :]  # 9 interior, 6 edge, 4 corner
+    assert taps[0, 0] == 4 and taps[0, 2] == 6 and taps[2, 2] == 9
+    for k in range(2):
+        assert np.array_equal(y[0, :, :, k], taps * Cin * cval)
+
+
+def test_one_by_one_special_case_is_a_gemm():
+    # only the centre tap is non-zero: y = X W1^T + b, a plain matrix product
+    N, H, W, Cin, Cout = 2, 3, 5, 7, 6
+    x = rand(N, H, W, Cin)
+    w = np.zeros((Cout, 3, 3, Cin))
+    w1 = rand(Cout, Cin)
+    w[:, 1, 1, :] = w1
+    b = rand(Cout)
+    y = oracle.conv3x3_fwd(x, w, b)
+    expect = (x.reshape(-1, Cin) @ w1.T + b).reshape(N, H, W, Cout)
+    assert np.allclose(y, expect, rtol=1e-13, atol=1e-13)
+
+
+def test_silu_special_values_and_grid():
+    assert oracle.silu(0.0) == 0.0
+    assert oracle.silu(60.0) == pytest.approx(60.0, rel=1e-15)
+    assert abs(oracle.silu(-60.0)) < 1e-20
+    assert oracle.silu(-1e4) == 0.0
+    for z in np.linspace(-12, 12, 97):
+        sig = 0.5 * (1.0 + math.tanh(0.5 * z))  # sigmoid via tanh, a different route
+        assert oracle.silu(z) == pytest.approx(z * sig, rel=1e-12, abs=1e-15)
+
+
+def test_silu_epilogue_applies_after_bias():
+    x = rand(1, 3, 3, 2)
+    w = rand(4, 3, 3, 2)
+    b = rand(4)
+    z = oracle.conv3x3_fwd(x, w, b, act=0)
+    y = oracle.conv3x3_fwd(x, w, b, act=1)
+    sig = 0.5 * (1.0 + np.tanh(0.5 * z))
+    assert np.allclose(y, z * sig, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# identities
+# ---------------------------------------------------------------------------
+def test_adjoint_identity_fwd_dgrad():
+    # <fwd(x, w), v> = <x, dgrad(v, w)> with no bias and no activation
+    x = rand(2, 5, 7, 3)
+    w = rand(4, 3, 3, 3)
+    v = rand(2, 5, 7, 4)
+    lhs = np.sum(oracle.conv3x3_fwd(x, w) * v)
+    rhs = np.sum(x * oracle.conv3x3_dgrad(v, w))
+    assert lhs == pytest.approx(rhs, rel=1e-12)
+
+
+def test_bilinear_wgrad_identity_and_dbias():
+    # <dw(x, dz), V> = <fwd(x, V), dz> for any V;  db = sum of dz over pixels
+    x = rand(2, 4, 6, 5)
+    dz = rand(2, 4, 6, 3)
+    V = rand(3, 3, 3, 5)
+    dw, db = oracle.conv3x3_wgrad(x, dz)
+    assert np.sum(dw * V) == pytest.approx(np.sum(oracle.conv3x3_fwd(x, V) * dz), rel=1e-12)
+    assert np.allclose(db, dz.sum(axis=(0, 1, 2)), rtol=1e-13)
+    assert np.allclose(oracle.conv3x3_dbias(dz), db, rtol=1e-13)
+
+
+def test_wgrad_matches_central_finite_differences():
+    # L(w) = <fwd(x, w), dz> is linear in w, so central differences are exact up to rounding
+    x = rand(1, 4, 5, 2)
+    dz = rand(1, 4, 5, 3)
+    w0 = rand(3, 3, 3, 2)
+    dw, _ = oracle.conv3x3_wgrad(x, dz)
+    eps = 1e-3
+    for e in range(w0.size):
+        wp = w0.copy().reshape(-1)
+        wm = w0.copy().reshape(-1)
+        wp[e] += eps
+        wm[e] -= eps
+        lp = np.sum(oracle.conv3x3_fwd(x, wp.reshape(w0.shape)) * dz)
+        lm = np.sum(oracle.conv3x3_fwd(x, wm.reshape(w0.shape)) * dz)
+        assert (lp - lm) / (2 * eps) == pytest.approx(dw.reshape(-1)[e], abs=1e-9)
+
+
+def test_dgrad_matches_central_finite_differences():
+    x0 = rand(1, 3, 4, 2)
+    w = rand(3, 3, 3, 2)
+    dz = rand(1, 3, 4, 3)
+    dx = oracle.conv3x3_dgrad(dz, w)
+    eps = 1e-3
+    for e in range(x0.size):
+        xp = x0.copy().reshape(-1)
+        xm = x0.copy().reshape(-1)
+        xp[e] += eps
+        xm[e] -= eps
+        lp = np.sum(oracle.conv3x3_fwd(xp.reshape(x0.shape), w) * dz)
+        lm = np.sum(oracle.conv3x3_fwd(xm.reshape(x0.shape), w) * dz)
+        assert (lp - lm) / (2 * eps) == pytest.approx(dx.reshape(-1)[e], abs=1e-9)
+
+
+# ---------------------------------------------------------------------------
+# brute force and library special cases
+# ---------------------------------------------------------------------------
+def im2col(x):
+    """Explicit [P, 9*Cin] patch matrix, column order (r, s, c)."""
+    N, H, W, C = x.shape
+    xp = np.zeros((N, H + 2, W + 2, C))
+    xp[:, 1:H + 1, 1:W + 1] = x
+    cols = [xp[:, r:r + H, s:s + W, :] for r in range(3) for s in range(3)]
+    return np.concatenate(cols, axis=-1).reshape(N * H * W, 9 * C)
+
+
+def col2im(cols, shape):
+    N, H, W, C = shape
+    xp = np.zeros((N, H + 2, W + 2, C))
+    cols = cols.reshape(N, H, W, 9, C)
+    for t in range(9):
+        r, s = divmod(t, 3)
+        xp[:, r:r + H, s:s + W, :] += cols[:, :, :, t, :]
+    return xp[:, 1:H + 1, 1:W + 1]
+
+
+def test_brute_force_im2col_all_three_passes():
+    N, H, W, Cin, Cout = 2, 5, 4, 3, 6
+    x = rand(N, H, W, Cin)
+    w = rand(Cout, 3, 3, Cin)
+    b = rand(Cout)
+    dz = rand(N, H, W, Cout)
+    A = im2col(x)
+    Wm = w.reshape(Cout, 9 * Cin)
+    y = (A @ Wm.T + b).reshape(N, H, W, Cout)
+    assert np.allclose(oracle.conv3x3_fwd(x, w, b), y, rtol=1e-12, atol=1e-12)
+    dx = col2im(dz.reshape(-1, Cout) @ Wm, x.shape)
+    assert np.allclose(oracle.conv3x3_dgrad(dz, w), dx, rtol=1e-12, atol=1e-12)
+    dw = (dz.reshape(-1, Cout).T @ A).reshape(Cout, 3, 3, Cin)
+    got_dw, got_db = oracle.conv3x3_wgrad(x, dz)
+    assert np.allclose(got_dw, dw, rtol=1e-12, atol=1e-12)
+    assert np.allclose(got_db, dz.reshape(-1, Cout).sum(0), rtol=1e-12)
+
+
+def test_torch_float64_conv2d_cross_check():
+    torch = pytest.importorskip("torch")
+    N, H, W, Cin, Cout = 2, 6, 5, 4, 3
+    x = rand(N, H, W, Cin)
+    w = rand(Cout, 3, 3, Cin)
+    b = rand(Cout)
+    dz = rand(N, H, W, Cout)
+    xt = torch.tensor(x).permute(0, 3, 1, 2).contiguous().requires_grad_(True)
+    wt = torch.tensor(w).permute(0, 3, 1, 2).contiguous().requires_grad_(True)
+    bt = torch.tensor(b).requires_grad_(True)
+    z = torch.nn.functional.conv2d(xt, wt, bt, stride=1, padding=1)
+    z.backward(torch.tensor(dz).permute(0, 3, 1, 2))
+    assert np.allclose(oracle.conv3x3_fwd(x, w, b), z.detach().permute(0, 2, 3, 1).numpy(),
+                       rtol=1e-12, atol=1e-12)
+    assert np.allclose(oracle.conv3x3_dgrad(dz, w), xt.grad.permute(0, 2, 3, 1).numpy(),
+                       rtol=1e-12, atol=1e-12)
+    dw, db = oracle.conv3x3_wgrad(x, dz)
+    assert np.allclose(dw, wt.grad.permute(0, 2, 3, 1).numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(db, bt.grad.numpy(), rtol=1e-12, atol=1e-12)
+    ys = oracle.conv3x3_fwd(x, w, b, act=1)
+    assert np.allclose(ys, torch.nn.functional.silu(z).detach().permute(0, 2, 3, 1).numpy(),
+                       rtol=1e-12, atol=1e-13)
+
+
+def test_hand_computed_fixture():
+    with open(os.path.join(GOLDEN, "hand_3x3.json")) as f:
+        g = json.load(f)
+    x, w, b = np.array(g["x"], float), np.array(g["w"], float), np.array(g["bias"], float)
+    dz = np.array(g["dz"], float)
+    assert np.array_equal(oracle.conv3x3_fwd(x, w, b), np.array(g["y"], float))
+    assert np.array_equal(oracle.conv3x3_dgrad(dz, w), np.array(g["dx"], float))
+    dw, db = oracle.conv3x3_wgrad(x, dz)
+    assert np.array_equal(dw, np.array(g["dw"], float))
+    assert np.array_equal(db, np.array(g["db"], float))
+
+
+# ---------------------------------------------------------------------------
+# invariants and internal consistency
+# ---------------------------------------------------------------------------
+def test_sampled_entry_points_equal_full_results():
+    N, H, W, Cin, Cout = 2, 5, 6, 3, 4
+    x, w, b, dz = rand(N, H, W, Cin), rand(Cout, 3, 3, Cin), rand(Cout), rand(N, H, W, Cout)
+    y = oracle.conv3x3_fwd(x, w, b, act=1)
+    idx = rng.choice(y.size, 50, replace=False)
+    assert np.array_equal(oracle.conv3x3_fwd_at(x, w, b, 1, idx), y.reshape(-1)[idx])
+    dx = oracle.conv3x3_dgrad(dz, w)
+    idx = rng.choice(dx.size, 50, replace=False)
+    assert np.array_equal(oracle.conv3x3_dgrad_at(dz, w, idx), dx.reshape(-1)[idx])
+    dw, _ = oracle.conv3x3_wgrad(x, dz)
+    idx = rng.choice(dw.size, 50, replace=False)
+    assert np.allclose(oracle.conv3x3_wgrad_at(x, dz, idx), dw.reshape(-1)[idx], rtol=1e-13, atol=1e-13)
+
+
+def test_results_do_not_depend_on_thread_count():
+    x, w, dz = rand(3, 7, 5, 4), rand(6, 3, 3, 4), rand(3, 7, 5, 6)
+    try:
+        oracle.set_threads(1)
+        a = (oracle.conv3x3_fwd(x, w), oracle.conv3x3_dgrad(dz, w), *oracle.conv3x3_wgrad(x, dz))
+        oracle.set_threads(5)
+        b = (oracle.conv3x3_fwd(x, w), oracle.conv3x3_dgrad(dz, w), *oracle.conv3x3_wgrad(x, dz))
+    finally:
+        oracle.set_threads(0)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+def test_stem_padding_channels_stay_exactly_zero():
+    L = synth.Layer("stem-small", 2, 8, 16, 6, 5, act=1, cin_real=3)
+    t = synth.make_tensors(L, seed=0)
+    assert np.all(t.x[..., 3:] == 0) and np.all(t.w[..., 3:] == 0)
+    dx = oracle.conv3x3_dgrad(t.dy, t.w)
+    dw, _ = oracle.conv3x3_wgrad(t.x, t.dy)
+    assert np.all(dx[..., 3:] == 0)
+    assert np.all(dw[..., 3:] == 0)
+    assert np.any(dx[..., :3] != 0) and np.any(dw[..., :3] != 0)
+
+
+def test_degenerate_sizes():
+    # 1x1 images: only the centre tap ever lands inside
+    x, w, b = rand(3, 1, 1, 2), rand(4, 3, 3, 2), rand(4)
+    y = oracle.conv3x3_fwd(x, w, b)
+    assert np.allclose(y[:, 0, 0, :], x[:, 0, 0, :] @ w[:, 1, 1, :].T + b, rtol=1e-13)
+    # a single row: only r = 1 taps contribute
+    x, w = rand(1, 1, 6, 2), rand(3, 3, 3, 2)
+    w2 = w.copy()
+    w2[:, [0, 2]] = 0
+    assert np.array_equal(oracle.conv3x3_fwd(x, w), oracle.conv3x3_fwd(x, w2))
+
+
+# ---------------------------------------------------------------------------
+# the pins catch planted mistakes (mutated copies of the oracle, CPU only)
+# ---------------------------------------------------------------------------
+MUTANTS = {
+    "fwd kernel flipped in h": ("int64_t hh = h + r - 1;", "int64_t hh = h - r + 1;"),
+    "fwd bias dropped": ("double acc = j->bias ? j->bias[k] : 0.0;", "double acc = 0.0;"),
+    "fwd weight taps transposed": ("const double* wp = j->wt + ((k * 3 + r) * 3 + s) * j->Cin;",
+                                   "const double* wp = j->wt + ((k * 3 + s) * 3 + r) * j->Cin;"),
+    "fwd last column of taps missing": ("for (int64_t s = 0; s < 3; ++s) {\n      int64_t ww = w + s - 1;",
+                                        "for (int64_t s = 0; s < 2; ++s) {\n      int64_t ww = w + s - 1;"),
+    "dgrad taps not mirrored": ("int64_t hh = h + 1 - r;", "int64_t hh = h + r - 1;"),
+    "dgrad weight index off by a tap": ("acc += dzp[k] * j->wt[((k * 3 + r) * 3 + s) * j->Cin + c];",
+                                        "acc += dzp[k] * j->wt[((k * 3 + s) * 3 + r) * j->Cin + c];"),
+    "wgrad shifted the wrong way": ("            int64_t ww = w + s - 1;\n            if (ww < 0 || ww >= j->W) continue;\n            const double* xp",
+                                    "            int64_t ww = w - s + 1;\n            if (ww < 0 || ww >= j->W) continue;\n            const double* xp"),
+    "dbias squares dz": ("db += d;", "db += d * d;"),
+    "silu sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+}
+
+
+def _mutant_module(tmp_path, name, old, new):
+    import importlib.util
+    src = open(oracle._SRC).read()
+    assert src.count(old) >= 1, name
+    d = tmp_path / name.replace(" ", "_")
+    d.mkdir()
+    (d / "conv3x3_oracle.c").write_text(src.replace(old, new, 1))
+    spec = importlib.util.spec_from_file_location("oracle_mutant", oracle.__file__)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod._SRC = str(d / "conv3x3_oracle.c")
+    mod._LIB = str(d / "liboracle.so")
+    mod._lib = None
+    return mod
+
+
+def _suite():
+    return [
+        test_centre_delta_reproduces_input,
+        *[(lambda r=r, s=s: test_off_centre_delta_shifts_with_zero_fill(r, s))
+          for r in range(3) for s in range(3)],
+        test_all_ones_kernel_on_constant_input_gives_9_6_4_pattern,
+        test_one_by_one_special_case_is_a_gemm,
+        test_silu_special_values_and_grid,
+        test_adjoint_identity_fwd_dgrad,
+        test_bilinear_wgrad_identity_and_dbias,
+        test_brute_force_im2col_all_three_passes,
+        test_hand_computed_fixture,
+    ]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistakes(tmp_path, name):
+    old, new = MUTANTS[name]
+    mod = _mutant_module(tmp_path, name, old, new)
+    g = globals()
+    saved = g["oracle"]
+    g["oracle"] = mod
+    caught = 0
+    try:
+        for fn in _suite():
+            try:
+                fn()
+            except AssertionError:
+                caught += 1
+    finally:
+        g["oracle"] = saved
+    assert caught > 0, "no pin caught the planted mistake: " + name
