@@ -1,0 +1,147 @@
+/*
+ * conv3x3.h -- C ABI of libconv3x3.so: stride-1, zero-pad-1 3x3 convolution
+ * forward, input gradient (dgrad) and weight gradient (wgrad) on one GB300
+ * (sm_103a).
+ *
+ * The operation is the 3x3 convolution that the subject page's custom CUDA
+ * kernels compute, forward and backward, inside a diffusion UNet training step
+ * (clu0's C++/CUDA UNet diffusion, sourcepulse.org project page, "How It Works"
+ * and "Highlighted Details").  The page does not write it down; this library
+ * computes the PyTorch Conv2d cross-correlation (no kernel flip) with stride 1,
+ * padding 1, dilation 1, groups 1:
+ *
+ *   fwd    z[n,h,w,k]  = bias[k] + sum_{r,s,c} x[n,h+r-1,w+s-1,c] * w[k,r,s,c]
+ *          y = z (act NONE) or y = z * sigmoid(z) (act SILU)
+ *   dgrad  dx[n,h,w,c] = sum_{r,s,k} dy[n,h+1-r,w+1-s,k] * w[k,r,s,c]
+ *   wgrad  dw[k,r,s,c] = sum_{n,h,w} dy[n,h,w,k] * x[n,h+r-1,w+s-1,c]
+ *          dbias[k]    = sum_{n,h,w} dy[n,h,w,k]
+ *
+ * Taps outside the image read zero.  dy is the gradient with respect to the
+ * pre-activation z (the SiLU backward, if any, is the caller's step).
+ *
+ * Layouts (all dense, no padding between rows):
+ *   activations x, y, dx, dy : NHWC, c fastest       ([N][H][W][C])
+ *   weights w, dw             : KRSC = [Cout][3][3][Cin], c fastest
+ *   bias, dbias               : [Cout]
+ * Element types: the production entry points take bf16 activations and
+ * weights, fp32 bias, fp32 dw / dbias, and accumulate in fp32.  The *_f32
+ * entry points take fp32 everywhere and accumulate with fp32 FMA on CUDA cores
+ * (never TF32).
+ *
+ * Ownership: the caller allocates every device buffer (inputs, outputs and the
+ * wgrad workspace) and keeps it alive until the work on `stream` completes.
+ * The library allocates no device memory; it keeps only host-side state (a
+ * driver entry point, per-device attributes) and one device status word.
+ *
+ * Asynchrony: every call enqueues work on `stream` (a cudaStream_t passed as
+ * void*, NULL = legacy default stream) and returns without synchronising.
+ *
+ * Errors: every call returns a conv3x3_status; nothing is thrown across the ABI.
+ * Arguments are validated on the host before anything is launched:
+ *   - N, H, W >= 1; Cin, Cout >= 8 and multiples of 8;
+ *   - every pointer non-NULL (bias / dbias may be NULL) and 16-byte aligned;
+ *   - N*H*W*max(Cin,Cout) < 2^31 elements per activation tensor, H, W <= 65535;
+ *   - act in {NONE, SILU}; out_dtype in {BF16, F32}; path in {AUTO, TENSOR, SIMT}.
+ * A launch failure returns CONV3X3_ERR_CUDA.  Kernels that wait on the
+ * hardware (mbarrier / TMA / tensor-core completion) give up after a bounded
+ * time, record CONV3X3_ERR_TIMEOUT in the device status word and exit cleanly;
+ * read it with conv3x3_device_status().
+ */
+#ifndef CONV3X3_H
+#define CONV3X3_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CONV3X3_OK = 0,
+  CONV3X3_ERR_INVALID_ARG = 1, /* bad shape, pointer, alignment or enum      */
+  CONV3X3_ERR_UNSUPPORTED = 2, /* valid arguments this build cannot run      */
+  CONV3X3_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed        */
+  CONV3X3_ERR_TIMEOUT = 4,     /* a device-side wait hit its bound           */
+  CONV3X3_ERR_WORKSPACE = 5    /* wgrad workspace missing or too small       */
+} conv3x3_status;
+
+enum { CONV3X3_ACT_NONE = 0, CONV3X3_ACT_SILU = 1 };
+enum { CONV3X3_DT_BF16 = 0, CONV3X3_DT_F32 = 1 };
+/* Kernel family: AUTO picks per shape; TENSOR = TMA-im2col + tcgen05/TMEM
+ * implicit GEMM; SIMT = CUDA-core fp32-FMA kernels with 128-bit loads. */
+enum { CONV3X3_PATH_AUTO = 0, CONV3X3_PATH_TENSOR = 1, CONV3X3_PATH_SIMT = 2 };
+
+/* Forward with fused bias + activation epilogue.
+ * x [N][H][W][Cin] bf16, w [Cout][3][3][Cin] bf16, bias [Cout] fp32 or NULL,
+ * y [N][H][W][Cout] bf16 (written, round-to-nearest-even from the fp32 result). */
+int conv3x3_fwd(const void* x, const void* w, const float* bias, void* y,
+                int N, int Cin, int Cout, int H, int W, int act, void* stream);
+
+/* Input gradient.  dy [N][H][W][Cout] bf16, w [Cout][3][3][Cin] bf16,
+ * dx [N][H][W][Cin] bf16 (written). */
+int conv3x3_dgrad(const void* dy, const void* w, void* dx,
+                  int N, int Cin, int Cout, int H, int W, void* stream);
+
+/* Weight and bias gradient.  x [N][H][W][Cin] bf16, dy [N][H][W][Cout] bf16,
+ * dw [Cout][3][3][Cin] fp32 (overwritten, not accumulated), dbias [Cout] fp32
+ * or NULL (overwritten).  The cross-CTA reduction sums fixed partial slices in
+ * a fixed order, so repeated calls give bit-identical dw and dbias.
+ * `workspace` is caller-owned device scratch of at least
+ * conv3x3_wgrad_workspace_bytes(...) bytes (may be NULL when that is 0),
+ * 256-byte aligned; its contents on entry do not matter. */
+int conv3x3_wgrad(const void* x, const void* dy, float* dw, float* dbias,
+                  int N, int Cin, int Cout, int H, int W,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Scratch bytes conv3x3_wgrad needs for this shape (0 for invalid shapes).
+ * Pure host computation; needs no GPU. */
+size_t conv3x3_wgrad_workspace_bytes(int N, int Cin, int Cout, int H, int W);
+
+/* Parity / dispatch variants of the same kernels.
+ * out_dtype = CONV3X3_DT_F32 writes the fp32 epilogue result before the bf16
+ * rounding (y or dx is then an fp32 buffer); `path` forces a kernel family.
+ * CONV3X3_ERR_UNSUPPORTED if the forced family cannot run the shape. */
+int conv3x3_fwd_ex(const void* x, const void* w, const float* bias, void* y,
+                   int N, int Cin, int Cout, int H, int W, int act,
+                   int out_dtype, int path, void* stream);
+int conv3x3_dgrad_ex(const void* dy, const void* w, void* dx,
+                     int N, int Cin, int Cout, int H, int W,
+                     int out_dtype, int path, void* stream);
+int conv3x3_wgrad_ex(const void* x, const void* dy, float* dw, float* dbias,
+                     int N, int Cin, int Cout, int H, int W,
+                     void* workspace, size_t workspace_bytes, int path, void* stream);
+size_t conv3x3_wgrad_workspace_bytes_ex(int N, int Cin, int Cout, int H, int W, int path);
+
+/* fp32 check path: every tensor fp32 (same layouts), fp32 FMA on CUDA cores,
+ * never TF32.  Any Cin, Cout >= 1; pointers 4-byte aligned.  wgrad needs no
+ * workspace (pass NULL, 0). */
+int conv3x3_fwd_f32(const float* x, const float* w, const float* bias, float* y,
+                    int N, int Cin, int Cout, int H, int W, int act, void* stream);
+int conv3x3_dgrad_f32(const float* dy, const float* w, float* dx,
+                      int N, int Cin, int Cout, int H, int W, void* stream);
+int conv3x3_wgrad_f32(const float* x, const float* dy, float* dw, float* dbias,
+                      int N, int Cin, int Cout, int H, int W,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Reads and clears the current device's status word (CONV3X3_OK or
+ * CONV3X3_ERR_TIMEOUT).  Synchronises `stream` first. */
+int conv3x3_device_status(void* stream);
+
+/* Self-test of the bounded-wait mechanism: launches one block that waits on an
+ * mbarrier nobody arrives on, with a limit of `limit_ns` nanoseconds.  The
+ * kernel gives up, records CONV3X3_ERR_TIMEOUT in the status word and returns;
+ * the CUDA context stays usable.  Returns the launch status. */
+int conv3x3_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
+
+/* Static description of a status code ("ok", "invalid argument", ...). */
+const char* conv3x3_status_string(int status);
+
+/* Which kernel family `path = AUTO` picks for this shape and pass
+ * (pass: 0 fwd, 1 dgrad, 2 wgrad).  Host-only. */
+int conv3x3_auto_path(int pass, int N, int Cin, int Cout, int H, int W);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONV3X3_H */

@@ -1,0 +1,104 @@
+"""CPU-only checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "conv3x3.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from x3_convolution_gb300 import build as b
+    b.build()
+    from x3_convolution_gb300 import _lib
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(conv3x3_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["conv3x3_fwd", "conv3x3_dgrad", "conv3x3_wgrad", "conv3x3_wgrad_workspace_bytes",
+              "conv3x3_fwd_f32", "conv3x3_dgrad_f32", "conv3x3_wgrad_f32",
+              "conv3x3_device_status", "conv3x3_status_string"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_binding_names_match_the_c_entry_points(lib):
+    from x3_convolution_gb300 import _lib
+    for n in declared_functions():
+        assert callable(getattr(_lib, n)), n
+
+
+def test_status_strings(lib):
+    from x3_convolution_gb300 import _lib
+    assert _lib.status_string(0) == "ok"
+    assert "invalid" in _lib.status_string(1)
+    assert "timed out" in _lib.status_string(4)
+    assert _lib.status_string(99) == "unknown status"
+
+
+ALIGNED = 1 << 20  # a fake 16-byte-aligned address; never dereferenced (validation fails first)
+
+
+@pytest.mark.parametrize("args", [
+    dict(N=0, Cin=64, Cout=64, H=8, W=8),     # empty batch
+    dict(N=1, Cin=3, Cout=64, H=8, W=8),      # Cin not a multiple of 8
+    dict(N=1, Cin=64, Cout=12, H=8, W=8),     # Cout not a multiple of 8
+    dict(N=1, Cin=64, Cout=64, H=0, W=8),     # empty image
+    dict(N=1, Cin=64, Cout=64, H=70000, W=1),  # H beyond 16 bits
+    dict(N=1 << 20, Cin=1024, Cout=64, H=64, W=64),  # tensor beyond 2^31 elements
+])
+def test_bad_shapes_are_rejected_without_a_gpu(lib, args):
+    a = [args[k] for k in ("N", "Cin", "Cout", "H", "W")]
+    assert lib.conv3x3_fwd(ALIGNED, ALIGNED, None, ALIGNED, *a, 0, None) == 1
+    assert lib.conv3x3_dgrad(ALIGNED, ALIGNED, ALIGNED, *a, None) == 1
+    assert lib.conv3x3_wgrad(ALIGNED, ALIGNED, ALIGNED, None, *a, ALIGNED, 1 << 30, None) == 1
+    assert lib.conv3x3_wgrad_workspace_bytes(*a) == 0
+
+
+def test_bad_pointers_and_enums_are_rejected_without_a_gpu(lib):
+    a = (2, 64, 64, 8, 8)
+    assert lib.conv3x3_fwd(None, ALIGNED, None, ALIGNED, *a, 0, None) == 1
+    assert lib.conv3x3_fwd(ALIGNED + 2, ALIGNED, None, ALIGNED, *a, 0, None) == 1  # misaligned
+    assert lib.conv3x3_fwd(ALIGNED, ALIGNED, None, ALIGNED, *a, 7, None) == 1      # bad act
+    assert lib.conv3x3_fwd_ex(ALIGNED, ALIGNED, None, ALIGNED, *a, 0, 5, 0, None) == 1  # dtype
+    assert lib.conv3x3_fwd_ex(ALIGNED, ALIGNED, None, ALIGNED, *a, 0, 0, 9, None) == 1  # path
+    assert lib.conv3x3_dgrad(ALIGNED, None, ALIGNED, *a, None) == 1
+    assert lib.conv3x3_wgrad(ALIGNED, ALIGNED, None, None, *a, ALIGNED, 1 << 30, None) == 1
+    # workspace that is required but missing / too small / misaligned
+    need = lib.conv3x3_wgrad_workspace_bytes(*a)
+    assert need > 0
+    assert lib.conv3x3_wgrad(ALIGNED, ALIGNED, ALIGNED, None, *a, None, 0, None) == 5
+    assert lib.conv3x3_wgrad(ALIGNED, ALIGNED, ALIGNED, None, *a, ALIGNED, need - 4, None) == 5
+    assert lib.conv3x3_wgrad(ALIGNED, ALIGNED, ALIGNED, None, *a, ALIGNED + 16, need, None) == 1
+    assert lib.conv3x3_fwd_f32(None, ALIGNED, None, ALIGNED, *a, 0, None) == 1
+
+
+def test_workspace_size_depends_only_on_shape(lib):
+    from synth import STACK, STEM, L1, L2, L3
+    for L in [STEM, L1, L2, L3] + STACK:
+        a = (L.N, L.Cin, L.Cout, L.H, L.W)
+        n = lib.conv3x3_wgrad_workspace_bytes(*a)
+        assert n == lib.conv3x3_wgrad_workspace_bytes(*a)
+        assert n >= 4 * (L.Cout * 9 * L.Cin + L.Cout)  # at least one full partial slice
+        assert n < 1 << 31
+
+
+def test_auto_path_is_host_only_and_valid(lib):
+    assert lib.conv3x3_auto_path(0, 64, 128, 128, 64, 64) in (1, 2)
+    assert lib.conv3x3_auto_path(0, 64, 3, 128, 64, 64) == -1

@@ -1,0 +1,230 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on
+the same seeded inputs.
+
+Tolerances (max|err| / max|ref| per output tensor):
+  * fp32 check path, all tensors fp32 ............................ <= 1e-5
+  * bf16 inputs, fp32 accumulation, fp32 result (out_dtype=F32) ... <= 2e-3
+  * bf16-stored y / dx: elementwise |y - ref| <= ulp_bf16(ref)/2 + 2e-3 max|ref|
+    and bit-identical to round-to-nearest-even of the fp32 result of the same
+    kernel (one rounding, on store)
+  * dw, dbias (fp32 outputs) ..................................... <= 2e-3
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+import synth
+from x3_convolution_gb300 import _lib as L
+from x3_convolution_gb300 import ops
+
+from gpu_util import check_bf16_store, host, rel_err, rne_bf16, to_dev_bf16, to_dev_f32
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-3
+TOL_F32 = 1e-5
+PATHS = {"tensor": L.PATH_TENSOR, "simt": L.PATH_SIMT}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    L.load()
+    yield
+    torch.cuda.synchronize()
+    assert L.conv3x3_device_status() == L.OK
+
+
+def dev_tensors(t):
+    return (to_dev_bf16(t.x), to_dev_bf16(t.w), to_dev_f32(t.bias), to_dev_bf16(t.dy))
+
+
+# ---------------------------------------------------------------------------
+# fp32 check path: the tiny workload, full tensors
+# ---------------------------------------------------------------------------
+def test_tiny_fp32_check_path_full():
+    Lr = synth.TINY
+    t = synth.make_tensors(Lr, seed=0)
+    x, w, b, dy = (to_dev_f32(a) for a in (t.x, t.w, t.bias, t.dy))
+    y = ops.fwd_f32(x, w, b, act=L.ACT_NONE)
+    dx = ops.dgrad_f32(dy, w)
+    dw, db = ops.wgrad_f32(x, dy)
+    torch.cuda.synchronize()
+    assert rel_err(host(y), oracle.conv3x3_fwd(t.x, t.w, t.bias, 0)) <= TOL_F32
+    assert rel_err(host(dx), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_F32
+    rdw, rdb = oracle.conv3x3_wgrad(t.x, t.dy)
+    assert rel_err(host(dw), rdw) <= TOL_F32
+    assert rel_err(host(db), rdb) <= TOL_F32
+    ys = ops.fwd_f32(x, w, b, act=L.ACT_SILU)
+    assert rel_err(host(ys), oracle.conv3x3_fwd(t.x, t.w, t.bias, 1)) <= TOL_F32
+
+
+def test_tiny_in_bf16_at_the_bf16_gate():
+    Lr = synth.Layer("tiny-bf16", 2, 64, 64, 32, 32, act=0)
+    t = synth.make_tensors(Lr, seed=0)
+    x, w, b, dy = dev_tensors(t)
+    y = ops.fwd(x, w, b, act=0, out_dtype=L.DT_F32)
+    dx = ops.dgrad(dy, w, out_dtype=L.DT_F32)
+    dw, db = ops.wgrad(x, dy)
+    torch.cuda.synchronize()
+    assert rel_err(host(y), oracle.conv3x3_fwd(t.x, t.w, t.bias, 0)) <= TOL_BF16
+    assert rel_err(host(dx), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
+    rdw, rdb = oracle.conv3x3_wgrad(t.x, t.dy)
+    assert rel_err(host(dw), rdw) <= TOL_BF16
+    assert rel_err(host(db), rdb) <= TOL_BF16
+
+
+# ---------------------------------------------------------------------------
+# small shapes, full tensors: several tiles, ragged tails, edge cases, both paths
+# ---------------------------------------------------------------------------
+SHAPES = [
+    # N, Cin, Cout, H, W
+    (2, 64, 64, 9, 9),        # P = 162: two 128-pixel tiles, ragged tail
+    (1, 128, 128, 16, 16),    # exact tiles
+    (3, 64, 192, 5, 7),       # P < 128, tiles cross image boundaries, N tile 192
+    (2, 256, 256, 8, 8),      # N tile 256, K = 2304
+    (1, 72, 200, 6, 11),      # ragged channel chunk (72) and ragged N tile (200)
+    (2, 8, 128, 12, 12),      # stem-like Cin = 8
+    (1, 16, 24, 3, 5),        # tiny channel counts
+    (1, 64, 64, 1, 1),        # 1x1 images: only the centre tap lands
+    (2, 64, 64, 2, 3),        # H, W in {2, 3}
+    (1, 384, 128, 4, 4),      # Cin 384 (6 chunks), dgrad N tile 384 -> 192
+    (5, 128, 64, 1, 37),      # single-row images
+    (1, 64, 512, 3, 3),       # Cout 512: two N tiles of 256
+]
+
+
+def _small(shape, act=1, seed=7):
+    N, Cin, Cout, H, W = shape
+    Lr = synth.Layer("s", N, Cin, Cout, H, W, act=act)
+    return synth.make_tensors(Lr, seed=seed)
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_small_shapes_all_passes(shape, path):
+    p = PATHS[path]
+    t = _small(shape)
+    x, w, b, dy = dev_tensors(t)
+    for act in (0, 1):
+        y32 = ops.fwd(x, w, b, act=act, out_dtype=L.DT_F32, path=p)
+        ybf = ops.fwd(x, w, b, act=act, out_dtype=L.DT_BF16, path=p)
+        torch.cuda.synchronize()
+        ref = oracle.conv3x3_fwd(t.x, t.w, t.bias, act)
+        assert rel_err(host(y32), ref) <= TOL_BF16, ("fwd", act)
+        assert check_bf16_store(host(ybf), ref) == 0, ("fwd bf16 store", act)
+        assert np.array_equal(host(ybf), rne_bf16(host(y32))), ("fwd one rounding", act)
+    dx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=p)
+    dxbf = ops.dgrad(dy, w, out_dtype=L.DT_BF16, path=p)
+    torch.cuda.synchronize()
+    ref = oracle.conv3x3_dgrad(t.dy, t.w)
+    assert rel_err(host(dx32), ref) <= TOL_BF16
+    assert check_bf16_store(host(dxbf), ref) == 0
+    assert np.array_equal(host(dxbf), rne_bf16(host(dx32)))
+    dw, db = ops.wgrad(x, dy, path=p)
+    torch.cuda.synchronize()
+    rdw, rdb = oracle.conv3x3_wgrad(t.x, t.dy)
+    assert rel_err(host(dw), rdw) <= TOL_BF16
+    assert rel_err(host(db), rdb) <= TOL_BF16
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_wgrad_is_bit_deterministic(path):
+    t = _small((4, 128, 128, 16, 16))
+    x, _, _, dy = dev_tensors(t)
+    a = ops.wgrad(x, dy, path=PATHS[path])
+    b = ops.wgrad(x, dy, path=PATHS[path])
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_wgrad_without_dbias_and_dirty_workspace():
+    t = _small((2, 64, 128, 8, 8))
+    x, _, _, dy = dev_tensors(t)
+    ws = ops.wgrad_workspace(2, 64, 128, 8, 8)
+    ws[0].fill_(0x7F)  # garbage in the scratch must not matter
+    dw, db = ops.wgrad(x, dy, with_bias=False, workspace=ws)
+    torch.cuda.synchronize()
+    assert db is None
+    assert rel_err(host(dw), oracle.conv3x3_wgrad(t.x, t.dy)[0]) <= TOL_BF16
+
+
+def test_stem_padded_channels_stay_zero():
+    Lr = synth.Layer("stem-mini", 4, 8, 128, 16, 16, act=1, cin_real=3)
+    t = synth.make_tensors(Lr, seed=3)
+    x, w, b, dy = dev_tensors(t)
+    for p in PATHS.values():
+        dx = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=p)
+        dw, _ = ops.wgrad(x, dy, path=p)
+        torch.cuda.synchronize()
+        assert torch.all(dx[..., 3:] == 0)
+        assert torch.all(dw[..., 3:] == 0)
+
+
+def test_bad_channel_count_is_rejected():
+    x = torch.zeros((1, 4, 4, 12), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((8, 3, 3, 12), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(L.Conv3x3Error) as e:
+        ops.fwd(x, w)
+    assert e.value.status == L.ERR_INVALID_ARG
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    assert L.conv3x3_device_status() == L.OK
+    L.conv3x3_selftest_wait_timeout(2_000_000)  # 2 ms, on a barrier nobody arrives at
+    assert L.conv3x3_device_status() == L.ERR_TIMEOUT
+    assert L.conv3x3_device_status() == L.OK  # read-and-clear
+    t = _small((1, 64, 64, 4, 4))
+    x, w, b, _ = dev_tensors(t)
+    y = ops.fwd(x, w, b, act=0, out_dtype=L.DT_F32)
+    torch.cuda.synchronize()
+    assert rel_err(host(y), oracle.conv3x3_fwd(t.x, t.w, t.bias, 0)) <= TOL_BF16
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled outputs, AUTO path (what the benchmark runs)
+# ---------------------------------------------------------------------------
+def _sampled_layer_check(Lr, seed, index, n_rand=4096, n_dw=192, whole_images=True):
+    t = synth.make_tensors(Lr, seed=seed, index=index)
+    x, w, b, dy = dev_tensors(t)
+    y32 = ops.fwd(x, w, b, act=Lr.act, out_dtype=L.DT_F32)
+    ybf = ops.fwd(x, w, b, act=Lr.act)
+    dx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32)
+    dw, db = ops.wgrad(x, dy)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1000 + index)
+    y32h, ybfh, dxh = host(y32).reshape(-1), host(ybf).reshape(-1), host(dx32).reshape(-1)
+    # random outputs anywhere + every output of the first and last image (all borders)
+    per_img_y = Lr.H * Lr.W * Lr.Cout
+    per_img_x = Lr.H * Lr.W * Lr.Cin
+    iy = rng.integers(0, y32h.size, n_rand)
+    ix = rng.integers(0, dxh.size, n_rand)
+    if whole_images:
+        iy = np.concatenate([iy, np.arange(per_img_y), np.arange(y32h.size - per_img_y, y32h.size)])
+        ix = np.concatenate([ix, np.arange(per_img_x), np.arange(dxh.size - per_img_x, dxh.size)])
+    ry = oracle.conv3x3_fwd_at(t.x, t.w, t.bias, Lr.act, iy)
+    scale_y = max(np.max(np.abs(ry)), 1e-30)
+    assert np.max(np.abs(y32h[iy] - ry)) / scale_y <= TOL_BF16, Lr.name
+    assert np.array_equal(ybfh[iy], rne_bf16(y32h[iy])), Lr.name
+    rx = oracle.conv3x3_dgrad_at(t.dy, t.w, ix)
+    assert np.max(np.abs(dxh[ix] - rx)) / max(np.max(np.abs(rx)), 1e-30) <= TOL_BF16, Lr.name
+    dwh = host(dw).reshape(-1)
+    iw = rng.integers(0, dwh.size, n_dw)
+    rw = oracle.conv3x3_wgrad_at(t.x, t.dy, iw)
+    rdb = oracle.conv3x3_dbias(t.dy)
+    # dw sampled: normalise by the largest magnitude among the sampled references and db
+    assert np.max(np.abs(dwh[iw] - rw)) / max(np.max(np.abs(rw)), 1e-30) <= TOL_BF16, Lr.name
+    assert rel_err(host(db), rdb) <= TOL_BF16, Lr.name
+
+
+@pytest.mark.parametrize("name", ["stem", "l1", "l2", "l3"])
+def test_full_size_configs_sampled(name):
+    Lr = synth.CONFIGS[name][0]
+    _sampled_layer_check(Lr, seed=0, index=0)
+
+
+def test_full_unet_stack_sampled():
+    for i, Lr in enumerate(synth.UNET_STEP):
+        _sampled_layer_check(Lr, seed=0, index=i, n_rand=1024, n_dw=64, whole_images=False)

@@ -1,0 +1,66 @@
+// conv3x3_internal.h -- declarations shared by the library's translation units
+// (host launchers of each kernel family).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/conv3x3.h"
+
+namespace c3 {
+
+// Problem shape as the host dispatcher sees it.
+struct Shape {
+  int N, Cin, Cout, H, W;
+  long long P() const { return (long long)N * H * W; }
+};
+
+// Per-call device context: status word and wait bound.
+struct DevCtx {
+  unsigned* status;          // device address of the status word
+  unsigned long long wait_ns;  // bound on every device-side wait
+  int num_sms;
+  int device;
+};
+
+// ---- CUDA-core kernels (simt.cu) ----
+int simt_fwd_f32(const float* x, const float* w, const float* bias, float* y, const Shape& s,
+                 int act, cudaStream_t st);
+int simt_dgrad_f32(const float* dy, const float* w, float* dx, const Shape& s, cudaStream_t st);
+int simt_wgrad_f32(const float* x, const float* dy, float* dw, float* db, const Shape& s,
+                   cudaStream_t st);
+
+int simt_fwd_bf16(const void* x, const void* w, const float* bias, void* y, const Shape& s,
+                  int act, int out_f32, cudaStream_t st);
+int simt_dgrad_bf16(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
+                    cudaStream_t st);
+size_t simt_wgrad_workspace(const Shape& s, int num_sms);
+int simt_wgrad_bf16(const void* x, const void* dy, float* dw, float* db, const Shape& s,
+                    void* ws, size_t ws_bytes, int num_sms, cudaStream_t st);
+
+// ---- tensor-core kernels (tc.cu) ----
+bool tc_supported(int pass, const Shape& s);
+int tc_fwd(const void* x, const void* w, const float* bias, void* y, const Shape& s, int act,
+           int out_f32, const DevCtx& d, cudaStream_t st);
+int tc_dgrad(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
+             const DevCtx& d, cudaStream_t st);
+size_t tc_wgrad_workspace(const Shape& s, int num_sms);
+int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s, void* ws,
+             size_t ws_bytes, const DevCtx& d, cudaStream_t st);
+
+// ---- driver entry points (api.cu) ----
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+typedef CUresult (*PFN_encodeIm2col)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                     const cuuint64_t*, const cuuint64_t*, const int*, const int*,
+                                     cuuint32_t, cuuint32_t, const cuuint32_t*,
+                                     CUtensorMapInterleave, CUtensorMapSwizzle,
+                                     CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+PFN_encodeTiled encode_tiled_fn();
+PFN_encodeIm2col encode_im2col_fn();
+
+}  // namespace c3

@@ -1,0 +1,571 @@
+// simt.cu -- CUDA-core kernels for the stride-1, pad-1 3x3 convolution.
+//
+//  * fp32 check path (fwd / dgrad / wgrad): every tensor fp32, plain fp32 FMA,
+//    one thread per output element, fixed summation order.
+//  * bf16 CUDA-core path: 128-bit (8 x bf16) vector loads and stores, fp32
+//    accumulation.  Cin == 8 (the UNet stem: RGB zero-padded to 8 channels) has
+//    specialised kernels that keep one pixel's whole 3x3x8 window in registers
+//    and the weights in shared memory; other channel counts (multiples of 8)
+//    run a generic variant.  wgrad writes fixed per-split partial sums to the
+//    caller's workspace and a second kernel adds them in split order, so the
+//    result is bit-identical run to run.
+//
+// The subject page attributes its kernels' speed to vectorised loads and
+// shared memory (clu0 C++/CUDA UNet diffusion, sourcepulse.org project page,
+// "How It Works"); this file is that style of kernel written for sm_103a.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "conv3x3_internal.h"
+
+namespace c3 {
+namespace {
+
+constexpr int kThreads = 256;
+// Split plan for wgrad partial sums: a fixed constant (not the device's SM
+// count) so that the workspace size and the summation order depend only on
+// the shape.
+constexpr int kPlanSms = 152;
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint4 v;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return v;
+}
+
+__device__ __forceinline__ float act_f(float z, int act) {
+  return act == CONV3X3_ACT_SILU ? z / (1.0f + __expf(-z)) : z;
+}
+
+__device__ __forceinline__ void store8(void* out, long long off, const float (&f)[8], int out_f32) {
+  if (out_f32) {
+    float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + off);
+    o[0] = make_float4(f[0], f[1], f[2], f[3]);
+    o[1] = make_float4(f[4], f[5], f[6], f[7]);
+  } else {
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + off) = pack8(f);
+  }
+}
+
+// ======================================================================
+// fp32 check path
+// ======================================================================
+__global__ void k_fwd_f32(const float* __restrict__ x, const float* __restrict__ w,
+                          const float* __restrict__ bias, float* __restrict__ y, int N, int H,
+                          int W, int Cin, int Cout, int act) {
+  const long long total = (long long)N * H * W * Cout;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    int k = (int)(e % Cout);
+    long long p = e / Cout;
+    int ww = (int)(p % W), hh = (int)((p / W) % H), n = (int)(p / ((long long)W * H));
+    float acc = bias ? bias[k] : 0.0f;
+    for (int r = 0; r < 3; ++r) {
+      int hi = hh + r - 1;
+      if (hi < 0 || hi >= H) continue;
+      for (int s = 0; s < 3; ++s) {
+        int wi = ww + s - 1;
+        if (wi < 0 || wi >= W) continue;
+        const float* xp = x + (((long long)n * H + hi) * W + wi) * Cin;
+        const float* wp = w + ((long long)(k * 3 + r) * 3 + s) * Cin;
+        for (int c = 0; c < Cin; ++c) acc = __fmaf_rn(xp[c], wp[c], acc);
+      }
+    }
+    y[e] = act_f(acc, act);
+  }
+}
+
+__global__ void k_dgrad_f32(const float* __restrict__ dy, const float* __restrict__ w,
+                            float* __restrict__ dx, int N, int H, int W, int Cin, int Cout) {
+  const long long total = (long long)N * H * W * Cin;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    int c = (int)(e % Cin);
+    long long p = e / Cin;
+    int ww = (int)(p % W), hh = (int)((p / W) % H), n = (int)(p / ((long long)W * H));
+    float acc = 0.0f;
+    for (int r = 0; r < 3; ++r) {
+      int hi = hh + 1 - r;
+      if (hi < 0 || hi >= H) continue;
+      for (int s = 0; s < 3; ++s) {
+        int wi = ww + 1 - s;
+        if (wi < 0 || wi >= W) continue;
+        const float* dp = dy + (((long long)n * H + hi) * W + wi) * Cout;
+        for (int k = 0; k < Cout; ++k)
+          acc = __fmaf_rn(dp[k], w[((long long)(k * 3 + r) * 3 + s) * Cin + c], acc);
+      }
+    }
+    dx[e] = acc;
+  }
+}
+
+// one thread per dw element (k, r, s, c); the sum over pixels runs in order
+__global__ void k_wgrad_f32(const float* __restrict__ x, const float* __restrict__ dy,
+                            float* __restrict__ dw, float* __restrict__ db, int N, int H, int W,
+                            int Cin, int Cout) {
+  const long long total = (long long)Cout * 9 * Cin;
+  const long long P = (long long)N * H * W;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    int c = (int)(e % Cin);
+    int rs = (int)((e / Cin) % 9);
+    int k = (int)(e / (9LL * Cin));
+    int r = rs / 3, s = rs % 3;
+    float acc = 0.0f;
+    for (long long p = 0; p < P; ++p) {
+      int ww = (int)(p % W), hh = (int)((p / W) % H);
+      int hi = hh + r - 1, wi = ww + s - 1;
+      if (hi < 0 || hi >= H || wi < 0 || wi >= W) continue;
+      acc = __fmaf_rn(dy[p * Cout + k], x[(p + (long long)(r - 1) * W + (s - 1)) * Cin + c], acc);
+    }
+    dw[e] = acc;
+  }
+  if (db) {
+    for (long long k = blockIdx.x * (long long)blockDim.x + threadIdx.x; k < Cout;
+         k += (long long)gridDim.x * blockDim.x) {
+      float acc = 0.0f;
+      for (long long p = 0; p < P; ++p) acc += dy[p * Cout + k];
+      db[k] = acc;
+    }
+  }
+}
+
+// ======================================================================
+// bf16 CUDA-core path
+// ======================================================================
+// forward, Cin == 8: one thread per output pixel; the 72-value window lives in
+// registers, weights (fp32, [Cout][72]) in shared memory.
+__global__ void __launch_bounds__(kThreads) k_fwd_bf16_c8(
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w,
+    const float* __restrict__ bias, void* __restrict__ y, int N, int H, int W, int Cout, int act,
+    int out_f32) {
+  extern __shared__ float4 smem_f4[];
+  float* ws = reinterpret_cast<float*>(smem_f4);
+  for (int i = threadIdx.x; i < Cout * 72; i += blockDim.x) ws[i] = __bfloat162float(w[i]);
+  __syncthreads();
+  const long long P = (long long)N * H * W;
+  for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < P;
+       p += (long long)gridDim.x * blockDim.x) {
+    int ww = (int)(p % W), hh = (int)((p / W) % H);
+    float in[72];
+#pragma unroll
+    for (int t = 0; t < 9; ++t) {
+      int hi = hh + t / 3 - 1, wi = ww + t % 3 - 1;
+      float f[8];
+      if (hi >= 0 && hi < H && wi >= 0 && wi < W) {
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (p + (long long)(t / 3 - 1) * W + (t % 3 - 1)) * 8));
+        unpack8(v, f);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) in[t * 8 + i] = f[i];
+    }
+#pragma unroll 1
+    for (int k0 = 0; k0 < Cout; k0 += 8) {
+      float acc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc[j] = bias ? __ldg(bias + k0 + j) : 0.0f;
+        const float4* wr = reinterpret_cast<const float4*>(ws + (k0 + j) * 72);
+#pragma unroll
+        for (int q = 0; q < 18; ++q) {
+          float4 wv = wr[q];
+          acc[j] = fmaf(in[4 * q + 0], wv.x, acc[j]);
+          acc[j] = fmaf(in[4 * q + 1], wv.y, acc[j]);
+          acc[j] = fmaf(in[4 * q + 2], wv.z, acc[j]);
+          acc[j] = fmaf(in[4 * q + 3], wv.w, acc[j]);
+        }
+        acc[j] = act_f(acc[j], act);
+      }
+      store8(y, p * Cout + k0, acc, out_f32);
+    }
+  }
+}
+
+// forward, generic Cin (multiple of 8): one thread per (pixel, 8 output channels)
+__global__ void __launch_bounds__(kThreads) k_fwd_bf16_gen(
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w,
+    const float* __restrict__ bias, void* __restrict__ y, int N, int H, int W, int Cin, int Cout,
+    int act, int out_f32) {
+  const int KG = Cout / 8;
+  const long long total = (long long)N * H * W * KG;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    int k0 = (int)(e % KG) * 8;
+    long long p = e / KG;
+    int ww = (int)(p % W), hh = (int)((p / W) % H);
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = bias ? __ldg(bias + k0 + j) : 0.0f;
+    for (int t = 0; t < 9; ++t) {
+      int hi = hh + t / 3 - 1, wi = ww + t % 3 - 1;
+      if (hi < 0 || hi >= H || wi < 0 || wi >= W) continue;
+      const __nv_bfloat16* xp = x + (p + (long long)(t / 3 - 1) * W + (t % 3 - 1)) * Cin;
+      for (int c0 = 0; c0 < Cin; c0 += 8) {
+        float xf[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(xp + c0)), xf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float wf[8];
+          unpack8(__ldg(reinterpret_cast<const uint4*>(w + ((long long)(k0 + j) * 9 + t) * Cin + c0)), wf);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[j] = fmaf(xf[i], wf[i], acc[j]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = act_f(acc[j], act);
+    store8(y, p * Cout + k0, acc, out_f32);
+  }
+}
+
+// dgrad, Cin == 8: one thread per input pixel (8 outputs); weights as fp32
+// [tap][Cout][8] in shared memory.
+__global__ void __launch_bounds__(kThreads) k_dgrad_bf16_c8(
+    const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ w,
+    void* __restrict__ dx, int N, int H, int W, int Cout, int out_f32) {
+  extern __shared__ float4 smem_f4[];
+  float* ws = reinterpret_cast<float*>(smem_f4);
+  for (int i = threadIdx.x; i < Cout * 72; i += blockDim.x) {
+    int c = i % 8, t = (i / 8) % 9, k = i / 72;  // w[k][t][c]
+    ws[(t * Cout + k) * 8 + c] = __bfloat162float(w[i]);
+  }
+  __syncthreads();
+  const long long P = (long long)N * H * W;
+  for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < P;
+       p += (long long)gridDim.x * blockDim.x) {
+    int ww = (int)(p % W), hh = (int)((p / W) % H);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll 1
+    for (int t = 0; t < 9; ++t) {
+      int r = t / 3, s = t % 3;
+      int hi = hh + 1 - r, wi = ww + 1 - s;
+      if (hi < 0 || hi >= H || wi < 0 || wi >= W) continue;
+      const __nv_bfloat16* dp = dy + (p + (long long)(1 - r) * W + (1 - s)) * Cout;
+      const float4* wt = reinterpret_cast<const float4*>(ws + t * Cout * 8);
+#pragma unroll 1
+      for (int k0 = 0; k0 < Cout; k0 += 8) {
+        float d[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(dp + k0)), d);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          float4 a = wt[(k0 + kk) * 2], b = wt[(k0 + kk) * 2 + 1];
+          acc[0] = fmaf(d[kk], a.x, acc[0]);
+          acc[1] = fmaf(d[kk], a.y, acc[1]);
+          acc[2] = fmaf(d[kk], a.z, acc[2]);
+          acc[3] = fmaf(d[kk], a.w, acc[3]);
+          acc[4] = fmaf(d[kk], b.x, acc[4]);
+          acc[5] = fmaf(d[kk], b.y, acc[5]);
+          acc[6] = fmaf(d[kk], b.z, acc[6]);
+          acc[7] = fmaf(d[kk], b.w, acc[7]);
+        }
+      }
+    }
+    store8(dx, p * 8, acc, out_f32);
+  }
+}
+
+// dgrad, generic Cin: one thread per (pixel, 8 input channels)
+__global__ void __launch_bounds__(kThreads) k_dgrad_bf16_gen(
+    const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ w,
+    void* __restrict__ dx, int N, int H, int W, int Cin, int Cout, int out_f32) {
+  const int CG = Cin / 8;
+  const long long total = (long long)N * H * W * CG;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    int c0 = (int)(e % CG) * 8;
+    long long p = e / CG;
+    int ww = (int)(p % W), hh = (int)((p / W) % H);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int t = 0; t < 9; ++t) {
+      int r = t / 3, s = t % 3;
+      int hi = hh + 1 - r, wi = ww + 1 - s;
+      if (hi < 0 || hi >= H || wi < 0 || wi >= W) continue;
+      const __nv_bfloat16* dp = dy + (p + (long long)(1 - r) * W + (1 - s)) * Cout;
+      for (int k0 = 0; k0 < Cout; k0 += 8) {
+        float d[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(dp + k0)), d);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          float wf[8];
+          unpack8(__ldg(reinterpret_cast<const uint4*>(w + ((long long)(k0 + kk) * 9 + t) * Cin + c0)), wf);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(d[kk], wf[i], acc[i]);
+        }
+      }
+    }
+    store8(dx, p * Cin + c0, acc, out_f32);
+  }
+}
+
+// wgrad partial sums.  Split `s` (blockIdx.y) owns pixels [s*chunk, (s+1)*chunk).
+// One thread per (k, tap, 8 input channels): its 8 running sums cover
+// dw[k][tap][c0..c0+8).  Threads with a block-wide index below Cout also sum
+// dbias.  partial layout: [S][Cout*9*Cin] followed by [S][Cout].
+__global__ void __launch_bounds__(kThreads) k_wgrad_bf16_partial(
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ dy,
+    float* __restrict__ part, int N, int H, int W, int Cin, int Cout, long long chunk, int S) {
+  const int CG = Cin / 8;
+  const long long E8 = (long long)Cout * 9 * CG;  // 8-wide output groups
+  const long long P = (long long)N * H * W;
+  const int split = blockIdx.y;
+  const long long p0 = split * chunk;
+  const long long p1 = p0 + chunk < P ? p0 + chunk : P;
+  const long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long dwsize = (long long)Cout * 9 * Cin;
+  if (e < E8) {
+    int c0 = (int)(e % CG) * 8;
+    int t = (int)((e / CG) % 9);
+    int k = (int)(e / (9LL * CG));
+    int r = t / 3, s = t % 3;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (long long p = p0; p < p1; ++p) {
+      int ww = (int)(p % W), hh = (int)((p / W) % H);
+      int hi = hh + r - 1, wi = ww + s - 1;
+      if (hi < 0 || hi >= H || wi < 0 || wi >= W) continue;
+      float d = __bfloat162float(dy[p * Cout + k]);
+      float xf[8];
+      unpack8(__ldg(reinterpret_cast<const uint4*>(x + (p + (long long)(r - 1) * W + (s - 1)) * Cin + c0)), xf);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(d, xf[i], acc[i]);
+    }
+    float* o = part + (long long)split * dwsize + ((long long)k * 9 + t) * Cin + c0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = acc[i];
+  }
+  if (blockIdx.x == 0) {
+    for (int k = threadIdx.x; k < Cout; k += blockDim.x) {
+      float acc = 0.0f;
+      for (long long p = p0; p < p1; ++p) acc += __bfloat162float(dy[p * Cout + k]);
+      part[(long long)S * dwsize + (long long)split * Cout + k] = acc;
+    }
+  }
+}
+
+// wgrad partial sums, Cin == 8: one block per (split, 128-channel slice of
+// Cout).  Thread (k, half): half 0 sums taps 0..4, half 1 taps 5..8 (8
+// channels each) for output channel k; half 0 also sums dbias.
+__global__ void __launch_bounds__(kThreads) k_wgrad_bf16_c8_partial(
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ dy,
+    float* __restrict__ part, int N, int H, int W, int Cout, long long chunk, int S) {
+  const long long P = (long long)N * H * W;
+  const int split = blockIdx.y;
+  const long long p0 = split * chunk;
+  const long long p1 = p0 + chunk < P ? p0 + chunk : P;
+  const int k = blockIdx.x * 128 + (threadIdx.x & 127);
+  const int half = threadIdx.x >> 7;
+  const int t0 = half ? 5 : 0, nt = half ? 4 : 5;
+  const bool active = k < Cout;
+  float acc[5][8];
+  float dbacc = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 5; ++j)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[j][i] = 0.0f;
+  if (active) {
+#pragma unroll 1
+    for (long long p = p0; p < p1; ++p) {
+      int ww = (int)(p % W), hh = (int)((p / W) % H);
+      float d = __bfloat162float(dy[p * Cout + k]);
+      dbacc += d;
+#pragma unroll
+      for (int j = 0; j < 5; ++j) {
+        if (j < nt) {
+          int t = t0 + j, r = t / 3, s = t % 3;
+          int hi = hh + r - 1, wi = ww + s - 1;
+          if (hi >= 0 && hi < H && wi >= 0 && wi < W) {
+            float xf[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(x + (p + (long long)(r - 1) * W + (s - 1)) * 8)), xf);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[j][i] = fmaf(d, xf[i], acc[j][i]);
+          }
+        }
+      }
+    }
+    const long long dwsize = (long long)Cout * 72;
+    float* o = part + (long long)split * dwsize + (long long)k * 72;
+#pragma unroll
+    for (int j = 0; j < 5; ++j)
+      if (j < nt) {
+        float4* o4 = reinterpret_cast<float4*>(o + (t0 + j) * 8);
+        o4[0] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+        o4[1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+      }
+    if (half == 0) part[(long long)S * dwsize + (long long)split * Cout + k] = dbacc;
+  }
+}
+
+// dw[e] = sum_{s=0}^{S-1} part[s][e] in increasing s; same for dbias.
+__global__ void k_wgrad_reduce(const float* __restrict__ part, float* __restrict__ dw,
+                               float* __restrict__ db, long long dwsize, int Cout, int S) {
+  const long long total = dwsize + Cout;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    if (e < dwsize) {
+      float acc = 0.0f;
+      for (int s = 0; s < S; ++s) acc += part[(long long)s * dwsize + e];
+      dw[e] = acc;
+    } else if (db) {
+      long long k = e - dwsize;
+      float acc = 0.0f;
+      for (int s = 0; s < S; ++s) acc += part[(long long)S * dwsize + (long long)s * Cout + k];
+      db[k] = acc;
+    }
+  }
+}
+
+int grid_for(long long work, int per_block = kThreads) {
+  long long g = (work + per_block - 1) / per_block;
+  if (g < 1) g = 1;
+  if (g > 65535LL * 16) g = 65535LL * 16;
+  return (int)g;
+}
+
+int launch_status() {
+  return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
+struct WgradPlan {
+  int S;
+  long long chunk;
+  bool c8;
+};
+
+WgradPlan wgrad_plan(const Shape& s) {
+  WgradPlan pl;
+  const long long P = s.P();
+  pl.c8 = (s.Cin == 8);
+  long long blocks_per_split;
+  if (pl.c8) {
+    blocks_per_split = (s.Cout + 127) / 128;
+  } else {
+    long long E8 = (long long)s.Cout * 9 * (s.Cin / 8);
+    blocks_per_split = (E8 + kThreads - 1) / kThreads;
+  }
+  long long target = 4LL * kPlanSms;  // blocks in flight across the device
+  long long S = (target + blocks_per_split - 1) / blocks_per_split;
+  if (S < 1) S = 1;
+  if (S > P) S = P;
+  if (S > 65535) S = 65535;
+  pl.chunk = (P + S - 1) / S;
+  pl.S = (int)((P + pl.chunk - 1) / pl.chunk);
+  return pl;
+}
+
+}  // namespace
+
+int launch_wgrad_reduce(const float* part, float* dw, float* db, long long dwsize, int Cout, int S,
+                        cudaStream_t st) {
+  k_wgrad_reduce<<<grid_for(dwsize + Cout), kThreads, 0, st>>>(part, dw, db, dwsize, Cout, S);
+  return launch_status();
+}
+
+// ---------------------------------------------------------------- launchers
+int simt_fwd_f32(const float* x, const float* w, const float* bias, float* y, const Shape& s,
+                 int act, cudaStream_t st) {
+  long long total = s.P() * s.Cout;
+  k_fwd_f32<<<grid_for(total), kThreads, 0, st>>>(x, w, bias, y, s.N, s.H, s.W, s.Cin, s.Cout, act);
+  return launch_status();
+}
+
+int simt_dgrad_f32(const float* dy, const float* w, float* dx, const Shape& s, cudaStream_t st) {
+  long long total = s.P() * s.Cin;
+  k_dgrad_f32<<<grid_for(total), kThreads, 0, st>>>(dy, w, dx, s.N, s.H, s.W, s.Cin, s.Cout);
+  return launch_status();
+}
+
+int simt_wgrad_f32(const float* x, const float* dy, float* dw, float* db, const Shape& s,
+                   cudaStream_t st) {
+  long long total = (long long)s.Cout * 9 * s.Cin;
+  k_wgrad_f32<<<grid_for(total), kThreads, 0, st>>>(x, dy, dw, db, s.N, s.H, s.W, s.Cin, s.Cout);
+  return launch_status();
+}
+
+int simt_fwd_bf16(const void* x, const void* w, const float* bias, void* y, const Shape& s,
+                  int act, int out_f32, cudaStream_t st) {
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
+  if (s.Cin == 8 && s.Cout <= 512) {
+    size_t sm = (size_t)s.Cout * 72 * sizeof(float);
+    if (sm > 48 * 1024 &&
+        cudaFuncSetAttribute(k_fwd_bf16_c8, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
+            cudaSuccess)
+      return CONV3X3_ERR_CUDA;
+    k_fwd_bf16_c8<<<grid_for(s.P()), kThreads, sm, st>>>(xb, wb, bias, y, s.N, s.H, s.W, s.Cout,
+                                                         act, out_f32);
+  } else {
+    k_fwd_bf16_gen<<<grid_for(s.P() * (s.Cout / 8)), kThreads, 0, st>>>(
+        xb, wb, bias, y, s.N, s.H, s.W, s.Cin, s.Cout, act, out_f32);
+  }
+  return launch_status();
+}
+
+int simt_dgrad_bf16(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
+                    cudaStream_t st) {
+  const __nv_bfloat16* db = static_cast<const __nv_bfloat16*>(dy);
+  const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
+  if (s.Cin == 8 && s.Cout <= 512) {
+    size_t sm = (size_t)s.Cout * 72 * sizeof(float);
+    if (sm > 48 * 1024 &&
+        cudaFuncSetAttribute(k_dgrad_bf16_c8, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm) != cudaSuccess)
+      return CONV3X3_ERR_CUDA;
+    k_dgrad_bf16_c8<<<grid_for(s.P()), kThreads, sm, st>>>(db, wb, dx, s.N, s.H, s.W, s.Cout,
+                                                           out_f32);
+  } else {
+    k_dgrad_bf16_gen<<<grid_for(s.P() * (s.Cin / 8)), kThreads, 0, st>>>(
+        db, wb, dx, s.N, s.H, s.W, s.Cin, s.Cout, out_f32);
+  }
+  return launch_status();
+}
+
+size_t simt_wgrad_workspace(const Shape& s, int /*num_sms*/) {
+  WgradPlan pl = wgrad_plan(s);
+  long long dwsize = (long long)s.Cout * 9 * s.Cin;
+  return (size_t)pl.S * (size_t)(dwsize + s.Cout) * sizeof(float);
+}
+
+int simt_wgrad_bf16(const void* x, const void* dy, float* dw, float* db, const Shape& s,
+                    void* ws, size_t ws_bytes, int num_sms, cudaStream_t st) {
+  if (ws_bytes < simt_wgrad_workspace(s, num_sms) || ws == nullptr) return CONV3X3_ERR_WORKSPACE;
+  WgradPlan pl = wgrad_plan(s);
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  const __nv_bfloat16* dyb = static_cast<const __nv_bfloat16*>(dy);
+  float* part = static_cast<float*>(ws);
+  if (pl.c8) {
+    dim3 grid((s.Cout + 127) / 128, pl.S);
+    k_wgrad_bf16_c8_partial<<<grid, kThreads, 0, st>>>(xb, dyb, part, s.N, s.H, s.W, s.Cout,
+                                                       pl.chunk, pl.S);
+  } else {
+    long long E8 = (long long)s.Cout * 9 * (s.Cin / 8);
+    dim3 grid((unsigned)((E8 + kThreads - 1) / kThreads), pl.S);
+    k_wgrad_bf16_partial<<<grid, kThreads, 0, st>>>(xb, dyb, part, s.N, s.H, s.W, s.Cin, s.Cout,
+                                                    pl.chunk, pl.S);
+  }
+  if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
+  long long dwsize = (long long)s.Cout * 9 * s.Cin;
+  k_wgrad_reduce<<<grid_for(dwsize + s.Cout), kThreads, 0, st>>>(part, dw, db, dwsize, s.Cout, pl.S);
+  return launch_status();
+}
+
+}  // namespace c3

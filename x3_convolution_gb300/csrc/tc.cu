@@ -1,0 +1,718 @@
+// tc.cu -- tensor-core (tcgen05 + TMEM + TMA) implicit-GEMM kernels for the
+// stride-1, pad-1 3x3 convolution on sm_103a.
+//
+// Forward and dgrad share one persistent, warp-specialised kernel:
+//   GEMM  M = N*H*W output pixels, N = output channels, K = 9 taps x channels.
+//   A tile (128 pixels x 64 channels, one tap) arrives through a TMA im2col
+//   tensor map: the hardware walks 128 consecutive output pixels, offsets each
+//   by the tap, and zero-fills the halo -- no im2col buffer ever exists.
+//   B tile comes from the KRSC weights with a tiled TMA map: K-major for the
+//   forward (w[k][tap][c] is already [N][K]), MN-major for dgrad (w[k][tap][c]
+//   read as [K=k][N=c]), so neither pass transposes anything in memory.  dgrad
+//   mirrors the taps: dx = sum over (ra, sa) of dy at offset (ra-1, sa-1) times
+//   w[:, 2-ra, 2-sa, :].
+//   Warp 0 issues TMA, warp 1 owns TMEM and issues tcgen05.mma (128 x BN x 16,
+//   fp32 accumulate), warps 2-5 drain the double-buffered TMEM accumulator:
+//   bias + SiLU in fp32, round to bf16 (or keep fp32), store.
+//
+// Weight gradient: split-K implicit GEMM  M = Cout, N = (tap, Cin), K = pixels.
+//   A = dy tile (64 pixels x 128 output channels, MN-major), B = im2col(x) for
+//   three taps (64 pixels x 128 channels each, MN-major).  Each CTA owns one
+//   (Cout block, tap row, Cin block) tile and one contiguous pixel range and
+//   writes its fp32 partial tile to the caller's workspace; a second kernel
+//   adds the partials in split order (deterministic).  dbias rides along as an
+//   extra N = 16 MMA against a block of ones.
+//
+// The subject page's kernels minimise memory transfers and avoid global
+// transposes (clu0 C++/CUDA UNet diffusion, sourcepulse.org project page,
+// "How It Works"); on sm_103a that is TMA im2col plus operand-major choices.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "conv3x3_internal.h"
+#include "ptx.cuh"
+
+namespace c3 {
+
+int launch_wgrad_reduce(const float* part, float* dw, float* db, long long dwsize, int Cout, int S,
+                        cudaStream_t st);
+
+namespace {
+
+constexpr int BM = 128;              // output pixels per tile (MMA M, TMEM lanes)
+constexpr int BKC = 64;              // channels per k-block: one 128-byte swizzle row
+constexpr int kThreads = 192;        // 6 warps
+constexpr uint32_t kABytes = BM * BKC * 2;
+constexpr int kPlanSms = 152;        // split plan constant (shape-only workspace size)
+constexpr size_t kGuardBytes = 16 * 1024;
+
+constexpr int pow2_cols(int n) { return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512; }
+
+template <int BN>
+struct IgemmCfg {
+  static constexpr uint32_t kBBytes = BN * BKC * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
+  static constexpr int kTmemCols = pow2_cols(2 * BN);
+  // + barriers, + alignment slack, + a 16 KB guard so that no descriptor
+  // arithmetic can ever address past the allocation
+  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 256 + 1024 + kGuardBytes;
+};
+
+struct IgemmParams {
+  void* out;
+  const float* bias;
+  int act, out_f32;
+  int P, H, W;
+  int kchunks;   // ceil(A channels / 64)
+  int nout;      // output channels (Cout fwd, Cin dgrad)
+  int num_m_tiles, num_n_tiles;
+  unsigned* status;
+  unsigned long long wait_ns;
+};
+
+__device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix, int col0,
+                                            const uint32_t (&v)[32]) {
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+  if (p.bias) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      if (col0 + i < p.nout) {
+        float4 b = __ldg(reinterpret_cast<const float4*>(p.bias + col0 + i));
+        f[i] += b.x;
+        f[i + 1] += b.y;
+        f[i + 2] += b.z;
+        f[i + 3] += b.w;
+      }
+    }
+  }
+  if (p.act == CONV3X3_ACT_SILU) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = silu_f32(f[i]);
+  }
+  if (p.out_f32) {
+    float* o = static_cast<float*>(p.out) + pix * p.nout + col0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (col0 + 8 * g < p.nout) {
+        reinterpret_cast<float4*>(o + 8 * g)[0] = make_float4(f[8 * g], f[8 * g + 1], f[8 * g + 2], f[8 * g + 3]);
+        reinterpret_cast<float4*>(o + 8 * g)[1] = make_float4(f[8 * g + 4], f[8 * g + 5], f[8 * g + 6], f[8 * g + 7]);
+      }
+  } else {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + pix * p.nout + col0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (col0 + 8 * g < p.nout) {
+        uint4 u;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[8 * g + 2 * i], f[8 * g + 2 * i + 1]);
+        *reinterpret_cast<uint4*>(o + 8 * g) = u;
+      }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// forward / dgrad implicit GEMM
+// ----------------------------------------------------------------------------
+template <int BN, bool kDgrad>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_igemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+            const IgemmParams p) {
+  using Cfg = IgemmCfg<BN>;
+  constexpr int S = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * Cfg::kStageBytes);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+  const int kblocks = 9 * p.kchunks;
+  const int HW = p.H * p.W;
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int mt = tile / p.num_n_tiles, nt = tile % p.num_n_tiles;
+        const int p0 = mt * BM;
+        const int n0 = p0 / HW, rem = p0 - n0 * HW;
+        const int h0 = rem / p.W, w0 = rem - (rem / p.W) * p.W;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const int tap = kb / p.kchunks, cc = kb - tap * p.kchunks;
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + (size_t)stage * Cfg::kStageBytes;
+          uint8_t* sb = sa + kABytes;
+          mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+          tma_load_im2col_4d(sa, &tmA, &full[stage], cc * BKC, w0 - 1, h0 - 1, n0,
+                             (uint16_t)(tap % 3), (uint16_t)(tap / 3));
+          if (!kDgrad) {
+            tma_load_3d(sb, &tmB, &full[stage], cc * BKC, tap, nt * BN);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_3d(sb + j * 8192, &tmB, &full[stage], nt * BN + j * 64, 8 - tap, cc * BKC);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // drain: wait (bounded) for every load still in flight before exiting
+        int n = issued < S ? issued : S;
+        int st = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < n; ++i) {
+          if (--st < 0) {
+            st = S - 1;
+            ph ^= 1;
+          }
+          mbar_wait(&full[st], ph, p.wait_ns, nullptr, nullptr);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, kDgrad ? 1 : 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      int buf = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[buf], acc_phase ^ 1, p.wait_ns, p.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + (size_t)stage * Cfg::kStageBytes);
+          const uint32_t b_base = a_base + kABytes;
+#pragma unroll
+          for (int k = 0; k < BKC / 16; ++k) {
+            const uint64_t adesc = smem_desc(a_base + k * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bdesc = kDgrad ? smem_desc(b_base + k * 2048, 8192, 1024, kSwizzle128B)
+                                          : smem_desc(b_base + k * 32, 16, 1024, kSwizzle128B);
+            tc_mma_bf16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[buf]);
+        if (++buf == 2) {
+          buf = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // make sure every issued MMA has retired before TMEM is released
+      tc_commit(drain);
+      mbar_wait(drain, 0, p.wait_ns, nullptr, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    int buf = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
+      tc_fence_after();
+      const int mt = tile / p.num_n_tiles, nt = tile % p.num_n_tiles;
+      const long long pix = (long long)mt * BM + row;
+      const bool valid = pix < p.P;
+#pragma unroll 1
+      for (int j = 0; j < BN / 32; ++j) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + j * 32), v);
+        tmem_ld_wait();
+        const int col0 = nt * BN + j * 32;
+        if (valid && col0 < p.nout) store_chunk(p, pix, col0, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (++buf == 2) {
+        buf = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+}
+
+// ----------------------------------------------------------------------------
+// wgrad split-K implicit GEMM
+// ----------------------------------------------------------------------------
+constexpr int kWgTaps = 3;                       // taps per CTA tile (one kernel row)
+constexpr int kWgPix = 64;                       // pixels per k-block
+constexpr uint32_t kWgABytes = 128 * kWgPix * 2;  // dy: 64 px x 128 Cout
+constexpr uint32_t kWgBBytes = 128 * kWgPix * 2;  // x: 64 px x 128 Cin, per tap
+constexpr uint32_t kWgStageBytes = kWgABytes + kWgTaps * kWgBBytes;
+constexpr int kWgStages = 3;
+constexpr int kWgTmemCols = 512;                 // 3 x 128 dw columns + 16 dbias columns
+constexpr int kWgBiasCol = kWgTaps * 128;
+constexpr size_t kWgSmem = (size_t)kWgStages * kWgStageBytes + 512 + 256 + 1024 + kGuardBytes;
+
+struct WgradParams {
+  float* part;  // [S][Cout][9*Cin] then [S][Cout]
+  int P, H, W, Cin, Cout;
+  int kb_total, kb_per_split, S;
+  int num_mb, num_cb;  // 128-wide blocks of Cout and Cin
+  unsigned* status;
+  unsigned long long wait_ns;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_wgrad(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmX,
+            const WgradParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* ones = smem + (size_t)kWgStages * kWgStageBytes;  // 16 x 16 bf16 ones (512 B)
+  uint64_t* full = reinterpret_cast<uint64_t*>(ones + 512);
+  uint64_t* empty = full + kWgStages;
+  uint64_t* tfull = empty + kWgStages;
+  uint64_t* drain = tfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_tiles = p.num_mb * 3 * p.num_cb;
+  const int tile = blockIdx.x % num_tiles;
+  const int split = blockIdx.x / num_tiles;
+  const int mb = tile % p.num_mb;
+  const int rest = tile / p.num_mb;
+  const int cb = rest % p.num_cb;
+  const int tr = rest / p.num_cb;  // kernel row r: taps 3r .. 3r+2
+  const bool do_bias = (tr == 0 && cb == 0);
+  const int kb0 = split * p.kb_per_split;
+  const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+  const int HW = p.H * p.W;
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < kWgStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmDY);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kWgTmemCols);
+    tmem_relinquish();
+  }
+  if (warp >= 2) {  // fill the ones block (bf16 1.0 = 0x3F80)
+    uint32_t* o = reinterpret_cast<uint32_t*>(ones);
+    for (int i = threadIdx.x - 64; i < 128; i += 128) o[i] = 0x3F803F80u;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int pk = kb * kWgPix;
+        const int n0 = pk / HW, rem = pk - n0 * HW;
+        const int h0 = rem / p.W, w0 = rem - (rem / p.W) * p.W;
+        uint8_t* sa = smem + (size_t)stage * kWgStageBytes;
+        uint8_t* sb = sa + kWgABytes;
+        mbar_arrive_expect_tx(&full[stage], kWgStageBytes);
+        tma_load_2d(sa, &tmDY, &full[stage], mb * 128, pk);
+        tma_load_2d(sa + 8192, &tmDY, &full[stage], mb * 128 + 64, pk);
+#pragma unroll
+        for (int t = 0; t < kWgTaps; ++t)
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            tma_load_im2col_4d(sb + (t * 2 + j) * 8192, &tmX, &full[stage], cb * 128 + j * 64,
+                               w0 - 1, h0 - 1, n0, (uint16_t)t, (uint16_t)tr);
+        ++issued;
+        if (++stage == kWgStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) {
+        int n = issued < kWgStages ? issued : kWgStages;
+        int st = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < n; ++i) {
+          if (--st < 0) {
+            st = kWgStages - 1;
+            ph ^= 1;
+          }
+          mbar_wait(&full[st], ph, p.wait_ns, nullptr, nullptr);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc256 = idesc_bf16_f32(128, 256, 1, 1);
+      constexpr uint32_t idesc128 = idesc_bf16_f32(128, 128, 1, 1);
+      constexpr uint32_t idesc16 = idesc_bf16_f32(128, 16, 1, 0);
+      const uint64_t ones_desc = smem_desc(smem_u32(ones), 128, 256, kSwizzleNone);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(smem + (size_t)stage * kWgStageBytes);
+        const uint32_t b_base = a_base + kWgABytes;
+#pragma unroll
+        for (int k = 0; k < kWgPix / 16; ++k) {
+          const uint32_t acc = (kb != kb0 || k != 0) ? 1u : 0u;
+          const uint64_t adesc = smem_desc(a_base + k * 2048, 8192, 1024, kSwizzle128B);
+          // taps 0 and 1: four 64-channel blocks at 8 KB stride -> one N = 256 MMA
+          tc_mma_bf16(tmem_base, adesc, smem_desc(b_base + k * 2048, 8192, 1024, kSwizzle128B),
+                      idesc256, acc);
+          tc_mma_bf16(tmem_base + 256, adesc,
+                      smem_desc(b_base + 2 * kWgBBytes + k * 2048, 8192, 1024, kSwizzle128B),
+                      idesc128, acc);
+          if (do_bias) tc_mma_bf16(tmem_base + kWgBiasCol, adesc, ones_desc, idesc16, acc);
+        }
+        tc_commit(&empty[stage]);
+        if (++stage == kWgStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (ok) tc_commit(tfull);
+      tc_commit(drain);
+      mbar_wait(drain, 0, p.wait_ns, nullptr, nullptr);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int k = mb * 128 + row;
+    if (mbar_wait(tfull, 0, p.wait_ns, p.status, abort_flag)) {
+      tc_fence_after();
+      const long long dwsize = (long long)p.Cout * 9 * p.Cin;
+      const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int t = 0; t < kWgTaps; ++t) {
+        const int tap = tr * 3 + t;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(lane_addr + (uint32_t)(t * 128 + j * 32), v);
+          tmem_ld_wait();
+          const int c0 = cb * 128 + j * 32;
+          if (k < p.Cout && c0 < p.Cin) {
+            float* o = p.part + (long long)split * dwsize + ((long long)k * 9 + tap) * p.Cin + c0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              if (c0 + 8 * g < p.Cin) {
+                reinterpret_cast<float4*>(o + 8 * g)[0] = make_float4(
+                    __uint_as_float(v[8 * g]), __uint_as_float(v[8 * g + 1]),
+                    __uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
+                reinterpret_cast<float4*>(o + 8 * g)[1] = make_float4(
+                    __uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]),
+                    __uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
+              }
+          }
+        }
+      }
+      if (do_bias) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(lane_addr + (uint32_t)kWgBiasCol, v);
+        tmem_ld_wait();
+        if (k < p.Cout)
+          p.part[(long long)p.S * dwsize + (long long)split * p.Cout + k] = __uint_as_float(v[0]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kWgTmemCols);
+}
+
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+int make_im2col_map(CUtensorMap* m, const void* base, int N, int H, int W, int C, int pixels) {
+  PFN_encodeIm2col enc = encode_im2col_fn();
+  if (!enc) return CONV3X3_ERR_CUDA;
+  cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)N};
+  cuuint64_t strides[3] = {(cuuint64_t)C * 2, (cuuint64_t)W * C * 2, (cuuint64_t)H * W * C * 2};
+  int lower[2] = {-1, -1};  // window origin = output pixel - 1 (pad 1)
+  int upper[2] = {-1, -1};  // pad 1 - (3 - 1): origins stop at size - 2
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                   lower, upper, (cuuint32_t)BKC, (cuuint32_t)pixels, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
+// KRSC weights viewed as {Cin, 9, Cout}; box {64, 1, rows}.
+int make_weight_map(CUtensorMap* m, const void* w, int Cin, int Cout, int rows) {
+  PFN_encodeTiled enc = encode_tiled_fn();
+  if (!enc) return CONV3X3_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)Cin, 9, (cuuint64_t)Cout};
+  cuuint64_t strides[2] = {(cuuint64_t)Cin * 2, (cuuint64_t)Cin * 9 * 2};
+  cuuint32_t box[3] = {(cuuint32_t)BKC, 1, (cuuint32_t)rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
+// [P][C] activations as a 2-D map, box {64 channels, 64 pixels}.
+int make_rows_map(CUtensorMap* m, const void* base, long long P, int C) {
+  PFN_encodeTiled enc = encode_tiled_fn();
+  if (!enc) return CONV3X3_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)P};
+  cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kWgPix};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
+template <typename K>
+int set_smem(K kernel, size_t bytes, int device) {
+  // cudaFuncSetAttribute once per (kernel, device); devices up to 64.
+  static std::mutex mu;
+  static uint64_t done[64] = {0};
+  static const void* keys[64] = {nullptr};
+  std::lock_guard<std::mutex> g(mu);
+  int slot = -1;
+  for (int i = 0; i < 64; ++i) {
+    if (keys[i] == (const void*)kernel) {
+      slot = i;
+      break;
+    }
+    if (keys[i] == nullptr) {
+      keys[i] = (const void*)kernel;
+      slot = i;
+      break;
+    }
+  }
+  if (slot >= 0 && device >= 0 && device < 64 && (done[slot] >> device & 1)) return CONV3X3_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+      cudaSuccess)
+    return CONV3X3_ERR_CUDA;
+  if (slot >= 0 && device >= 0 && device < 64) done[slot] |= 1ull << device;
+  return CONV3X3_OK;
+}
+
+template <int BN, bool kDgrad>
+int launch_igemm(const CUtensorMap& a, const CUtensorMap& b, const IgemmParams& prm,
+                 const DevCtx& d, cudaStream_t st) {
+  using Cfg = IgemmCfg<BN>;
+  auto kern = k_igemm<BN, kDgrad>;
+  if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+  const int tiles = prm.num_m_tiles * prm.num_n_tiles;
+  const int grid = tiles < d.num_sms ? tiles : d.num_sms;
+  kern<<<grid, kThreads, Cfg::kSmem, st>>>(a, b, prm);
+  return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
+int pick_bn(int nout) {
+  if (nout <= 64) return 64;
+  if (nout <= 128) return 128;
+  if (nout % 256 == 0) return 256;
+  if (nout % 192 == 0) return 192;
+  return 128;
+}
+
+int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const float* bias, void* out,
+              const Shape& s, int act, int out_f32, const DevCtx& d, cudaStream_t st) {
+  const int nout = dgrad ? s.Cin : s.Cout;
+  const int bn = pick_bn(nout);
+  CUtensorMap ta, tb;
+  int rc = make_im2col_map(&ta, a_src, s.N, s.H, s.W, a_ch, BM);
+  if (rc) return rc;
+  rc = make_weight_map(&tb, w, s.Cin, s.Cout, dgrad ? 64 : bn);
+  if (rc) return rc;
+  IgemmParams prm;
+  prm.out = out;
+  prm.bias = bias;
+  prm.act = act;
+  prm.out_f32 = out_f32;
+  prm.P = (int)s.P();
+  prm.H = s.H;
+  prm.W = s.W;
+  prm.kchunks = (a_ch + BKC - 1) / BKC;
+  prm.nout = nout;
+  prm.num_m_tiles = (int)((s.P() + BM - 1) / BM);
+  prm.num_n_tiles = (nout + bn - 1) / bn;
+  prm.status = d.status;
+  prm.wait_ns = d.wait_ns;
+  switch (bn) {
+    case 64: return dgrad ? launch_igemm<64, true>(ta, tb, prm, d, st) : launch_igemm<64, false>(ta, tb, prm, d, st);
+    case 128: return dgrad ? launch_igemm<128, true>(ta, tb, prm, d, st) : launch_igemm<128, false>(ta, tb, prm, d, st);
+    case 192: return dgrad ? launch_igemm<192, true>(ta, tb, prm, d, st) : launch_igemm<192, false>(ta, tb, prm, d, st);
+    default: return dgrad ? launch_igemm<256, true>(ta, tb, prm, d, st) : launch_igemm<256, false>(ta, tb, prm, d, st);
+  }
+}
+
+struct WgPlan {
+  int num_mb, num_cb, tiles, kb_total, kb_per_split, S;
+};
+
+WgPlan wg_plan(const Shape& s) {
+  WgPlan pl;
+  pl.num_mb = (s.Cout + 127) / 128;
+  pl.num_cb = (s.Cin + 127) / 128;
+  pl.tiles = pl.num_mb * 3 * pl.num_cb;
+  pl.kb_total = (int)((s.P() + kWgPix - 1) / kWgPix);
+  // minimise waves * (k-blocks per split + fixed epilogue cost)
+  long long best = -1;
+  int bestS = 1;
+  for (int S = 1; S <= pl.kb_total && S <= 1024; ++S) {
+    int per = (pl.kb_total + S - 1) / S;
+    int Sreal = (pl.kb_total + per - 1) / per;
+    if (Sreal != S) continue;
+    long long units = (long long)pl.tiles * S;
+    long long waves = (units + kPlanSms - 1) / kPlanSms;
+    long long cost = waves * (per + 6);
+    if (best < 0 || cost < best) {
+      best = cost;
+      bestS = S;
+    }
+  }
+  pl.kb_per_split = (pl.kb_total + bestS - 1) / bestS;
+  pl.S = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
+  return pl;
+}
+
+}  // namespace
+
+bool tc_supported(int pass, const Shape& s) {
+  (void)pass;
+  // im2col corner offsets and coordinates are 16/32-bit; the kernels index pixels with int.
+  if (s.P() >= (1LL << 31)) return false;
+  if (s.H > 65535 || s.W > 65535) return false;
+  return true;
+}
+
+int tc_fwd(const void* x, const void* w, const float* bias, void* y, const Shape& s, int act,
+           int out_f32, const DevCtx& d, cudaStream_t st) {
+  return run_igemm(false, x, s.Cin, w, bias, y, s, act, out_f32, d, st);
+}
+
+int tc_dgrad(const void* dy, const void* w, void* dx, const Shape& s, int out_f32, const DevCtx& d,
+             cudaStream_t st) {
+  return run_igemm(true, dy, s.Cout, w, nullptr, dx, s, CONV3X3_ACT_NONE, out_f32, d, st);
+}
+
+size_t tc_wgrad_workspace(const Shape& s, int /*num_sms*/) {
+  WgPlan pl = wg_plan(s);
+  long long dwsize = (long long)s.Cout * 9 * s.Cin;
+  return (size_t)pl.S * (size_t)(dwsize + s.Cout) * sizeof(float);
+}
+
+int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s, void* ws,
+             size_t ws_bytes, const DevCtx& d, cudaStream_t st) {
+  if (ws == nullptr || ws_bytes < tc_wgrad_workspace(s, d.num_sms)) return CONV3X3_ERR_WORKSPACE;
+  WgPlan pl = wg_plan(s);
+  CUtensorMap tdy, tx;
+  int rc = make_rows_map(&tdy, dy, s.P(), s.Cout);
+  if (rc) return rc;
+  rc = make_im2col_map(&tx, x, s.N, s.H, s.W, s.Cin, kWgPix);
+  if (rc) return rc;
+  WgradParams prm;
+  prm.part = static_cast<float*>(ws);
+  prm.P = (int)s.P();
+  prm.H = s.H;
+  prm.W = s.W;
+  prm.Cin = s.Cin;
+  prm.Cout = s.Cout;
+  prm.kb_total = pl.kb_total;
+  prm.kb_per_split = pl.kb_per_split;
+  prm.S = pl.S;
+  prm.num_mb = pl.num_mb;
+  prm.num_cb = pl.num_cb;
+  prm.status = d.status;
+  prm.wait_ns = d.wait_ns;
+  if (set_smem(k_wgrad, kWgSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+  k_wgrad<<<pl.tiles * pl.S, kThreads, kWgSmem, st>>>(tdy, tx, prm);
+  if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
+  return launch_wgrad_reduce(prm.part, dw, db, (long long)s.Cout * 9 * s.Cin, s.Cout, pl.S, st);
+}
+
+}  // namespace c3

@@ -1,0 +1,83 @@
+"""Torch-tensor convenience layer over the C ABI (allocation and marshalling only).
+
+Tensors are NHWC / KRSC and contiguous; torch only allocates device memory and
+supplies the stream.  Each call forwards to one entry point of libconv3x3.so.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib as L
+
+
+def _shape(x: torch.Tensor, w: torch.Tensor):
+    N, H, W, Cin = x.shape
+    Cout = w.shape[0]
+    return N, Cin, Cout, H, W
+
+
+def fwd(x, w, bias=None, act=L.ACT_NONE, out_dtype=L.DT_BF16, path=L.PATH_AUTO, out=None,
+        stream=None):
+    """y = act(conv3x3(x, w) + bias); x [N,H,W,Cin] bf16, w [Cout,3,3,Cin] bf16."""
+    N, Cin, Cout, H, W = _shape(x, w)
+    if out is None:
+        dt = torch.float32 if out_dtype == L.DT_F32 else torch.bfloat16
+        out = torch.empty((N, H, W, Cout), dtype=dt, device=x.device)
+    L.conv3x3_fwd_ex(x, w, bias, out, N, Cin, Cout, H, W, act, out_dtype, path, stream)
+    return out
+
+
+def dgrad(dy, w, out_dtype=L.DT_BF16, path=L.PATH_AUTO, out=None, stream=None):
+    """dx [N,H,W,Cin] from dy [N,H,W,Cout] and w [Cout,3,3,Cin]."""
+    N, H, W, Cout = dy.shape
+    Cin = w.shape[3]
+    if out is None:
+        dt = torch.float32 if out_dtype == L.DT_F32 else torch.bfloat16
+        out = torch.empty((N, H, W, Cin), dtype=dt, device=dy.device)
+    L.conv3x3_dgrad_ex(dy, w, out, N, Cin, Cout, H, W, out_dtype, path, stream)
+    return out
+
+
+def wgrad_workspace(N, Cin, Cout, H, W, path=L.PATH_AUTO, device="cuda"):
+    nbytes = L.conv3x3_wgrad_workspace_bytes_ex(N, Cin, Cout, H, W, path)
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device), nbytes
+
+
+def wgrad(x, dy, with_bias=True, path=L.PATH_AUTO, workspace=None, out=None, stream=None):
+    """(dw [Cout,3,3,Cin] fp32, dbias [Cout] fp32)."""
+    N, H, W, Cin = x.shape
+    Cout = dy.shape[3]
+    if workspace is None:
+        workspace = wgrad_workspace(N, Cin, Cout, H, W, path, x.device)
+    ws, nbytes = workspace
+    if out is None:
+        dw = torch.empty((Cout, 3, 3, Cin), dtype=torch.float32, device=x.device)
+        db = torch.empty((Cout,), dtype=torch.float32, device=x.device) if with_bias else None
+    else:
+        dw, db = out
+    L.conv3x3_wgrad_ex(x, dy, dw, db, N, Cin, Cout, H, W, ws, nbytes, path, stream)
+    return dw, db
+
+
+def fwd_f32(x, w, bias=None, act=L.ACT_NONE, stream=None):
+    N, Cin, Cout, H, W = _shape(x, w)
+    y = torch.empty((N, H, W, Cout), dtype=torch.float32, device=x.device)
+    L.conv3x3_fwd_f32(x, w, bias, y, N, Cin, Cout, H, W, act, stream)
+    return y
+
+
+def dgrad_f32(dy, w, stream=None):
+    N, H, W, Cout = dy.shape
+    Cin = w.shape[3]
+    dx = torch.empty((N, H, W, Cin), dtype=torch.float32, device=dy.device)
+    L.conv3x3_dgrad_f32(dy, w, dx, N, Cin, Cout, H, W, stream)
+    return dx
+
+
+def wgrad_f32(x, dy, stream=None):
+    N, H, W, Cin = x.shape
+    Cout = dy.shape[3]
+    dw = torch.empty((Cout, 3, 3, Cin), dtype=torch.float32, device=x.device)
+    db = torch.empty((Cout,), dtype=torch.float32, device=x.device)
+    L.conv3x3_wgrad_f32(x, dy, dw, db, N, Cin, Cout, H, W, None, 0, stream)
+    return dw, db
