@@ -1,0 +1,503 @@
+#!/usr/bin/env python3
+"""Benchmark: 3x3 conv fwd + dgrad + wgrad throughput (TFLOP/s) on GB300.
+
+One step = one training-step sweep over the UNet's 3x3 convs: every layer's
+forward (bias + SiLU epilogue) in network order, then dgrad and wgrad (+ dbias)
+in reverse order, each through the C ABI of libconv3x3.so on one stream.
+
+Default workload "unet": the stem conv (3 -> 128 channels, zero-padded to 8,
+64x64) followed by the 32 resblock convs of the 64x64 diffusion UNet (base 128,
+multipliers 1,2,3,4, two resblocks per level on the down and up paths, up-path
+inputs = concat of skip and main), batch 64, bf16 NHWC, seeded synthetic inputs.
+
+Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
+launching stream; L2 is flushed (a write of 2x the L2 size) between steps,
+outside the events.  Multi-process runs (torchrun) run one replica per GPU
+(weak scaling); the reported time is the max over ranks.
+
+--impl reference times the CPU oracle (fp64, all host cores) on a bounded
+sample of the same workload: each step runs fwd + dgrad + wgrad of one image of
+one layer, cycling through the layers.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "3x3 conv fwd+dgrad+wgrad TFLOP/s on 1 GB300 and % of roofline"
+UNIT = "TFLOP/s"
+
+
+# ---------------------------------------------------------------------------
+# accounting
+# ---------------------------------------------------------------------------
+def layer_bytes(L: synth.Layer):
+    """Algorithmic HBM bytes per pass: each ABI tensor read or written once."""
+    x = L.P * L.Cin * 2
+    dy = L.P * L.Cout * 2
+    w = L.Cout * 9 * L.Cin * 2
+    fwd = x + w + dy + L.Cout * 4           # x, w, bias in; y out
+    dgrad = dy + w + x                      # dy, w in; dx out
+    wgrad = x + dy + L.Cout * 9 * L.Cin * 4 + L.Cout * 4  # x, dy in; dw, db out
+    return {"fwd": fwd, "dgrad": dgrad, "wgrad": wgrad}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def roofline_time_s(L, peaks, tflops_key="bf16_tflops"):
+    by = layer_bytes(L)
+    f = L.flops_per_pass()
+    return {k: max(f / (peaks[tflops_key] * 1e12), by[k] / (peaks["hbm_gbs"] * 1e9)) for k in by}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+def gpu_selector(device) -> str:
+    """nvidia-smi -i argument for a torch device (its UUID when torch exposes it)."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+        if u:
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    idx = device.index or 0
+    ids = [v.strip() for v in vis.split(",") if v.strip()]
+    return ids[idx] if idx < len(ids) else str(idx)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: str):
+        self.gpu = gpu
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas; no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, ws: int, device=None) -> float:
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# the CUDA arm
+# ---------------------------------------------------------------------------
+class Workload:
+    def __init__(self, layers, seed, device, keep_host=True):
+        import torch
+        self.layers = layers
+        self.dev = []
+        self.host = []
+        ws_max = 0
+        from x3_convolution_gb300 import _lib as Lb
+        for i, L in enumerate(layers):
+            t = synth.make_tensors(L, seed=seed, index=i)
+            hx = torch.from_numpy(synth.bf16_bits(t.x).view(np.int16)).view(torch.bfloat16)
+            hw = torch.from_numpy(synth.bf16_bits(t.w).view(np.int16)).view(torch.bfloat16)
+            hb = torch.from_numpy(t.bias.copy())
+            hdy = torch.from_numpy(synth.bf16_bits(t.dy).view(np.int16)).view(torch.bfloat16)
+            del t
+            d = {
+                "x": hx.to(device), "w": hw.to(device), "b": hb.to(device), "dy": hdy.to(device),
+                "y": torch.empty((L.N, L.H, L.W, L.Cout), dtype=torch.bfloat16, device=device),
+                "dx": torch.empty((L.N, L.H, L.W, L.Cin), dtype=torch.bfloat16, device=device),
+                "dw": torch.empty((L.Cout, 3, 3, L.Cin), dtype=torch.float32, device=device),
+                "db": torch.empty((L.Cout,), dtype=torch.float32, device=device),
+            }
+            self.dev.append(d)
+            if keep_host:
+                self.host.append({"x": hx.pin_memory(), "w": hw.pin_memory(), "b": hb.pin_memory(),
+                                  "dy": hdy.pin_memory(),
+                                  "dw": torch.empty((L.Cout, 3, 3, L.Cin), dtype=torch.float32).pin_memory(),
+                                  "db": torch.empty((L.Cout,), dtype=torch.float32).pin_memory()})
+            ws_max = max(ws_max, Lb.conv3x3_wgrad_workspace_bytes(L.N, L.Cin, L.Cout, L.H, L.W))
+        self.ws_bytes = ws_max
+        self.ws = torch.empty(max(ws_max, 256), dtype=torch.uint8, device=device)
+
+    def h2d_bytes(self):
+        return sum(h[k].numel() * h[k].element_size() for h in self.host for k in ("x", "w", "b", "dy"))
+
+    def d2h_bytes(self):
+        return sum(h[k].numel() * h[k].element_size() for h in self.host for k in ("dw", "db"))
+
+
+def run_step(wl: Workload, stream_handle: int, ev=None, record=None):
+    """One sweep: fwd in order, then dgrad + wgrad in reverse order (C ABI calls)."""
+    from x3_convolution_gb300 import _lib as Lb
+    n = 0
+    for i, L in enumerate(wl.layers):
+        d = wl.dev[i]
+        if record is not None:
+            record("fwd", i, 0)
+        Lb.conv3x3_fwd(d["x"], d["w"], d["b"], d["y"], L.N, L.Cin, L.Cout, L.H, L.W, L.act,
+                       stream_handle)
+        if record is not None:
+            record("fwd", i, 1)
+        n += 1
+    for i in reversed(range(len(wl.layers))):
+        L = wl.layers[i]
+        d = wl.dev[i]
+        if record is not None:
+            record("dgrad", i, 0)
+        Lb.conv3x3_dgrad(d["dy"], d["w"], d["dx"], L.N, L.Cin, L.Cout, L.H, L.W, stream_handle)
+        if record is not None:
+            record("dgrad", i, 1)
+            record("wgrad", i, 0)
+        Lb.conv3x3_wgrad(d["x"], d["dy"], d["dw"], d["db"], L.N, L.Cin, L.Cout, L.H, L.W, wl.ws,
+                         wl.ws_bytes, stream_handle)
+        if record is not None:
+            record("wgrad", i, 1)
+        n += 3  # dgrad: 1 kernel; wgrad: partial-sum kernel + fixed-order reduction
+    return n
+
+
+def cuda_arm(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    device = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(device)
+    import __graft_entry__ as ge
+    ge.build()
+    from x3_convolution_gb300 import _lib as Lb
+
+    layers = synth.CONFIGS[args.workload]
+    peaks = load_peaks()
+    wl = Workload(layers, args.seed, device, keep_host=not args.no_e2e)
+    stream = torch.cuda.Stream(device=device)
+    sh = stream.cuda_stream
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device=device)
+
+    flops_step = sum(3 * L.flops_per_pass() for L in layers)
+    flops_padded = sum(3 * L.flops_per_pass(padded=True) for L in layers)
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            run_step(wl, sh)
+    torch.cuda.synchronize(device)
+    st = Lb.conv3x3_device_status(sh)
+    if st != Lb.OK:
+        raise RuntimeError("device status after warm-up: " + Lb.status_string(st))
+
+    # timed steps: one event pair per step, per-call events for the breakdown
+    nlay = len(layers)
+    per_call = {"fwd": [[None, None] for _ in range(nlay)], "dgrad": [[None, None] for _ in range(nlay)],
+                "wgrad": [[None, None] for _ in range(nlay)]}
+    call_ms = {k: np.zeros(nlay) for k in per_call}
+
+    def record(kind, i, which):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        per_call[kind][i][which] = e
+
+    sampler = ClockSampler(gpu_selector(device))
+    sampler.start()
+    time.sleep(0.3)
+    step_ms = []
+    launches = 0
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    for _ in range(args.steps):
+        with torch.cuda.stream(stream):
+            flush.zero_()  # same stream, before the start event: evict L2
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launches += run_step(wl, sh, record=record)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        step_ms.append(e0.elapsed_time(e1))
+        for k in per_call:
+            for i in range(nlay):
+                a, b = per_call[k][i]
+                call_ms[k][i] += a.elapsed_time(b)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    st = Lb.conv3x3_device_status(sh)
+    if st != Lb.OK:
+        raise RuntimeError("device status after timed steps: " + Lb.status_string(st))
+
+    ms = float(np.mean(step_ms))
+    ms_max = max_over_ranks(ms, ws, device)
+    value = flops_step * ws / (ms_max * 1e-3) / 1e12
+
+    # per-pass breakdown and the roofline of the dominant kernel family
+    K = args.steps
+    fam = {}
+    for k in ("fwd", "dgrad", "wgrad"):
+        t = call_ms[k].sum() / K  # ms per step
+        fl = sum(L.flops_per_pass() for L in layers)
+        fam[k] = {"ms_per_step": round(float(t), 4), "tflops": round(fl / (t * 1e-3) / 1e12, 1)}
+    dom = max(fam, key=lambda k: fam[k]["ms_per_step"])
+    dom_flops_per_step = sum(L.flops_per_pass() for L in layers)
+    achieved = dom_flops_per_step / (fam[dom]["ms_per_step"] * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    roof_s = sum(sum(roofline_time_s(L, peaks).values()) for L in layers)
+    per_layer = []
+    for i, L in enumerate(layers):
+        rt = roofline_time_s(L, peaks)
+        per_layer.append({
+            "name": L.name, "N": L.N, "Cin": L.Cin, "Cout": L.Cout, "H": L.H, "W": L.W,
+            "path": {k: ["auto", "tensor", "simt"][max(0, Lb.conv3x3_auto_path(j, L.N, L.Cin, L.Cout, L.H, L.W))]
+                     for j, k in enumerate(("fwd", "dgrad", "wgrad"))},
+            "us": {k: round(float(call_ms[k][i] / K * 1e3), 2) for k in call_ms},
+            "tflops": {k: round(L.flops_per_pass() / (call_ms[k][i] / K * 1e-3) / 1e12, 1) for k in call_ms},
+            "roofline_frac": {k: round(rt[k] / (call_ms[k][i] / K * 1e-3), 3) for k in call_ms},
+        })
+
+    # end to end through the C ABI from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for h, d in zip(wl.host, wl.dev):
+                    for k in ("x", "w", "b", "dy"):
+                        d[k].copy_(h[k], non_blocking=True)
+                run_step(wl, sh)
+                for h, d in zip(wl.host, wl.dev):
+                    h["dw"].copy_(d["dw"], non_blocking=True)
+                    h["db"].copy_(d["db"], non_blocking=True)
+            stream.synchronize()
+        e2e_step()
+        n_e2e = max(3, min(args.steps, 10))
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+        e2e_ms = max_over_ranks(e2e_ms, ws, device)
+        e2e = {"value": round(flops_step * ws / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+               "ms_per_step": round(e2e_ms, 3), "steps": n_e2e,
+               "h2d_bytes_per_step": wl.h2d_bytes(), "d2h_bytes_per_step": wl.d2h_bytes()}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(layers, args.seed, budget_s=args.cpu_budget)
+
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded splitmix64 + Box-Muller normals; no dataset, no trained weights)",
+        "config": {"workload": args.workload, "layers": len(layers), "batch": layers[0].N,
+                   "layout": "NHWC bf16 activations, KRSC bf16 weights, fp32 accumulate",
+                   "l2": "flushed between steps (write of 2x L2)",
+                   "flops_per_step": flops_step, "flops_per_step_padded_cin": flops_padded},
+        "pct_of_roofline": round(roof_s / (ms * 1e-3), 4),
+        "roofline": {"bound": "tensor", "kernel": {"fwd": "k_igemm (fwd)", "dgrad": "k_igemm (dgrad)",
+                                                   "wgrad": "k_wgrad + k_wgrad_reduce"}[dom],
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": peaks["source"] + " bf16 sustained"},
+        "passes": fam,
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "layers_detail": per_layer if args.detail else None,
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(L: synth.Layer, seed: int, index: int):
+    """fwd + dgrad + wgrad of the first image of layer L; returns (seconds, flops)."""
+    import oracle
+    L1 = synth.Layer(L.name, 1, L.Cin, L.Cout, L.H, L.W, act=L.act, cin_real=L.cin_real,
+                     dtype=L.dtype)
+    t = synth.make_tensors(L1, seed=seed, index=index)
+    x, w, b, dy = (np.asarray(a, np.float64) for a in (t.x, t.w, t.bias, t.dy))
+    t0 = time.perf_counter()
+    oracle.conv3x3_fwd(x, w, b, L.act)
+    oracle.conv3x3_dgrad(dy, w)
+    oracle.conv3x3_wgrad(x, dy)
+    dt = time.perf_counter() - t0
+    return dt, 3 * L1.flops_per_pass()
+
+
+def cpu_baseline(layers, seed, budget_s=20.0):
+    import oracle
+    tot_t, tot_f, done = 0.0, 0, []
+    order = sorted(range(len(layers)), key=lambda i: layers[i].flops_per_pass() / layers[i].N)
+    for i in order:
+        if tot_t >= budget_s:
+            break
+        dt, fl = oracle_sample(layers[i], seed, i)
+        tot_t += dt
+        tot_f += fl
+        done.append(layers[i].name)
+    return {"value": tot_f / tot_t / 1e12, "unit": UNIT, "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": "fwd+dgrad+wgrad of image 0 of %d of %d layers (fp64 loop nests), %.1f s"
+                      % (len(done), len(layers), tot_t)}
+
+
+def reference_arm(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    synth.build()
+    layers = synth.CONFIGS[args.workload]
+    for i in range(args.warmup):
+        oracle_sample(layers[i % len(layers)], args.seed, i % len(layers))
+    tt, tf = 0.0, 0
+    per = []
+    for s in range(args.steps):
+        i = s % len(layers)
+        dt, fl = oracle_sample(layers[i], args.seed, i)
+        tt += dt
+        tf += fl
+        per.append(dt)
+    value = tf / tt / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload, "layers": len(layers),
+                                        "batch": layers[0].N},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                         "sample": "each step: fwd+dgrad+wgrad of image 0 of one layer, cycling "
+                                   "through the %d layers" % len(layers)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--workload", choices=sorted(synth.CONFIGS), default="unet")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--detail", action="store_true", help="add a per-layer breakdown")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    line = reference_arm(args) if args.impl == "reference" else cuda_arm(args)
+    if line is not None:
+        if line.get("layers_detail") is None:
+            line.pop("layers_detail", None)
+        print(json.dumps(line), flush=True)
+    ws, _, _ = dist_env()
+    if ws > 1 and args.impl == "cuda":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
