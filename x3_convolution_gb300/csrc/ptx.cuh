@@ -194,6 +194,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          | ((uint32_t)(M >> 4) << 24);    // M / 16
 }
 
-__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-z)); }
+// SiLU(z) = z * sigmoid(z) = z / (1 + e^{-z}) with the hardware exponential and
+// the fast (2-ulp) divide; for z below about -87 the denominator exceeds 2^126
+// and the quotient is 0, the limit of SiLU there to well below fp32 resolution.
+__device__ __forceinline__ float silu_f32(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 }  // namespace c3

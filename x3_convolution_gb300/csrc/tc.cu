@@ -44,7 +44,9 @@ namespace {
 
 constexpr int BM = 128;              // output pixels per tile (MMA M, TMEM lanes)
 constexpr int BKC = 64;              // channels per k-block: one 128-byte swizzle row
-constexpr int kThreads = 192;        // 6 warps
+constexpr int kThreads = 192;        // wgrad: TMA warp, MMA warp, 4 epilogue warps
+constexpr int kEpiWarps = 8;         // igemm: two epilogue warps per TMEM lane quarter
+constexpr int kIgemmThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = BM * BKC * 2;
 constexpr int kPlanSms = 152;        // split plan constant (shape-only workspace size)
 constexpr size_t kGuardBytes = 16 * 1024;
@@ -121,7 +123,7 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix,
 // forward / dgrad implicit GEMM
 // ----------------------------------------------------------------------------
 template <int BN, bool kDgrad>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kIgemmThreads, 1)
     k_igemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const IgemmParams p) {
   using Cfg = IgemmCfg<BN>;
@@ -148,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
+      mbar_init(&tempty[i], kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -265,7 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // warp w may read TMEM lanes 32*(w%4) .. +31; the two warps of a lane
+    // quarter split the tile's columns in halves.
+    constexpr int kHalf = BN / 2;
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     int buf = 0;
     uint32_t acc_phase = 0;
@@ -275,12 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mt = tile / p.num_n_tiles, nt = tile % p.num_n_tiles;
       const long long pix = (long long)mt * BM + row;
       const bool valid = pix < p.P;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + half * kHalf);
 #pragma unroll 1
-      for (int j = 0; j < BN / 32; ++j) {
+      for (int j = 0; j < kHalf / 32; ++j) {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + j * 32), v);
+        tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
         tmem_ld_wait();
-        const int col0 = nt * BN + j * 32;
+        const int col0 = nt * BN + half * kHalf + j * 32;
         if (valid && col0 < p.nout) store_chunk(p, pix, col0, v);
       }
       tc_fence_before();
@@ -587,22 +594,36 @@ int launch_igemm(const CUtensorMap& a, const CUtensorMap& b, const IgemmParams& 
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
   const int grid = tiles < d.num_sms ? tiles : d.num_sms;
-  kern<<<grid, kThreads, Cfg::kSmem, st>>>(a, b, prm);
+  kern<<<grid, kIgemmThreads, Cfg::kSmem, st>>>(a, b, prm);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
-int pick_bn(int nout) {
-  if (nout <= 64) return 64;
-  if (nout <= 128) return 128;
-  if (nout % 256 == 0) return 256;
-  if (nout % 192 == 0) return 192;
-  return 128;
+// N-tile width: the candidate with the fewest persistent-tile rounds times
+// the per-tile cost (MMA work ~ BN, plus a fixed A-tile share); near-ties go
+// to the wider tile, which re-reads A less often.
+int pick_bn(int nout, long long m_tiles, int num_sms) {
+  const int cand[4] = {256, 192, 128, 64};
+  int best = 128;
+  double best_cost = -1.0;
+  for (int i = 0; i < 4; ++i) {
+    const int bn = cand[i];
+    const long long n_tiles = (nout + bn - 1) / bn;
+    const long long waste = n_tiles * bn - nout;
+    if (bn > 64 && waste * 2 > bn) continue;  // mostly-empty last tile
+    const long long rounds = (m_tiles * n_tiles + num_sms - 1) / num_sms;
+    const double cost = (double)rounds * (bn + 32);
+    if (best_cost < 0 || cost < 0.93 * best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
 }
 
 int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const float* bias, void* out,
               const Shape& s, int act, int out_f32, const DevCtx& d, cudaStream_t st) {
   const int nout = dgrad ? s.Cin : s.Cout;
-  const int bn = pick_bn(nout);
+  const int bn = pick_bn(nout, (s.P() + BM - 1) / BM, d.num_sms);
   CUtensorMap ta, tb;
   int rc = make_im2col_map(&ta, a_src, s.N, s.H, s.W, a_ch, BM);
   if (rc) return rc;
