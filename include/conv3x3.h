@@ -46,6 +46,10 @@
  * hardware (mbarrier / TMA / tensor-core completion) give up after a bounded
  * time, record CONV3X3_ERR_TIMEOUT in the device status word and exit cleanly;
  * read it with conv3x3_device_status().
+ *
+ * Tuning override: the environment variable CONV3X3_TILE="<BN>x<MT>" (BN in
+ * {64,128,192,256}, MT in {1,2}, 2*MT*BN <= 512) forces the forward / dgrad
+ * tensor-core tile to MT*128 pixels x BN channels; unset, the library picks.
  */
 #ifndef CONV3X3_H
 #define CONV3X3_H

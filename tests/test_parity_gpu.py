@@ -130,6 +130,23 @@ def test_small_shapes_all_passes(shape, path):
     assert rel_err(host(db), rdb) <= TOL_BF16
 
 
+TILES = ["64x1", "128x1", "192x1", "256x1", "64x2", "128x2"]
+
+
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("shape", [(2, 64, 64, 9, 9), (1, 72, 200, 6, 11), (3, 128, 256, 17, 13),
+                                   (2, 8, 128, 12, 12)], ids=lambda s: "x".join(map(str, s)))
+def test_every_tensor_tile_shape(shape, tile, monkeypatch):
+    monkeypatch.setenv("CONV3X3_TILE", tile)
+    t = _small(shape)
+    x, w, b, dy = dev_tensors(t)
+    y32 = ops.fwd(x, w, b, act=1, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    dx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert rel_err(host(y32), oracle.conv3x3_fwd(t.x, t.w, t.bias, 1)) <= TOL_BF16
+    assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
+
+
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_wgrad_is_bit_deterministic(path):
     t = _small((4, 128, 128, 16, 16))

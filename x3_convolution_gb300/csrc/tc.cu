@@ -30,6 +30,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "conv3x3_internal.h"
@@ -53,12 +55,16 @@ constexpr size_t kGuardBytes = 16 * 1024;
 
 constexpr int pow2_cols(int n) { return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512; }
 
-template <int BN>
+// MT = pixel sub-tiles of 128 per CTA tile (two MMAs share each B stage when
+// MT = 2, halving the B bytes per unit of tensor work).
+template <int BN, int MT>
 struct IgemmCfg {
+  static constexpr uint32_t kATileBytes = MT * kABytes;
   static constexpr uint32_t kBBytes = BN * BKC * 2;
-  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kStageBytes = kATileBytes + kBBytes;
   static constexpr int kStages = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
-  static constexpr int kTmemCols = pow2_cols(2 * BN);
+  static constexpr int kTmemCols = pow2_cols(2 * MT * BN);
+  static_assert(2 * MT * BN <= 512, "double-buffered accumulators must fit in TMEM");
   // + barriers, + alignment slack, + a 16 KB guard so that no descriptor
   // arithmetic can ever address past the allocation
   static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 256 + 1024 + kGuardBytes;
@@ -122,12 +128,13 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix,
 // ----------------------------------------------------------------------------
 // forward / dgrad implicit GEMM
 // ----------------------------------------------------------------------------
-template <int BN, bool kDgrad>
+template <int BN, int MT, bool kDgrad>
 __global__ void __launch_bounds__(kIgemmThreads, 1)
     k_igemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const IgemmParams p) {
-  using Cfg = IgemmCfg<BN>;
+  using Cfg = IgemmCfg<BN, MT>;
   constexpr int S = Cfg::kStages;
+  constexpr int TM = BM * MT;  // pixels per CTA tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * Cfg::kStageBytes);
@@ -176,9 +183,17 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         const int mt = tile / p.num_n_tiles, nt = tile % p.num_n_tiles;
-        const int p0 = mt * BM;
-        const int n0 = p0 / HW, rem = p0 - n0 * HW;
-        const int h0 = rem / p.W, w0 = rem - (rem / p.W) * p.W;
+        // window origin (pixel - 1 in h and w) of each 128-pixel sub-tile
+        int cw[MT], ch[MT], cn[MT];
+#pragma unroll
+        for (int u = 0; u < MT; ++u) {
+          const int p0 = mt * TM + u * BM;
+          const int n0 = p0 / HW, rem = p0 - n0 * HW;
+          const int h0 = rem / p.W;
+          cn[u] = n0;
+          ch[u] = h0 - 1;
+          cw[u] = rem - h0 * p.W - 1;
+        }
         for (int kb = 0; kb < kblocks; ++kb) {
           const int tap = kb / p.kchunks, cc = kb - tap * p.kchunks;
           if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
@@ -186,10 +201,12 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
             break;
           }
           uint8_t* sa = smem + (size_t)stage * Cfg::kStageBytes;
-          uint8_t* sb = sa + kABytes;
+          uint8_t* sb = sa + Cfg::kATileBytes;
           mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
-          tma_load_im2col_4d(sa, &tmA, &full[stage], cc * BKC, w0 - 1, h0 - 1, n0,
-                             (uint16_t)(tap % 3), (uint16_t)(tap / 3));
+#pragma unroll
+          for (int u = 0; u < MT; ++u)
+            tma_load_im2col_4d(sa + u * kABytes, &tmA, &full[stage], cc * BKC, cw[u], ch[u], cn[u],
+                               (uint16_t)(tap % 3), (uint16_t)(tap / 3));
           if (!kDgrad) {
             tma_load_3d(sb, &tmB, &full[stage], cc * BKC, tap, nt * BN);
           } else {
@@ -231,7 +248,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         if (!mbar_wait(&tempty[buf], acc_phase ^ 1, p.wait_ns, p.status, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * MT * BN);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) {
             ok = false;
@@ -239,13 +256,16 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
           }
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + (size_t)stage * Cfg::kStageBytes);
-          const uint32_t b_base = a_base + kABytes;
+          const uint32_t b_base = a_base + Cfg::kATileBytes;
 #pragma unroll
           for (int k = 0; k < BKC / 16; ++k) {
-            const uint64_t adesc = smem_desc(a_base + k * 32, 16, 1024, kSwizzle128B);
             const uint64_t bdesc = kDgrad ? smem_desc(b_base + k * 2048, 8192, 1024, kSwizzle128B)
                                           : smem_desc(b_base + k * 32, 16, 1024, kSwizzle128B);
-            tc_mma_bf16(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int u = 0; u < MT; ++u)
+              tc_mma_bf16(d_tmem + (uint32_t)(u * BN),
+                          smem_desc(a_base + u * kABytes + k * 32, 16, 1024, kSwizzle128B), bdesc,
+                          idesc, (kb | k) != 0 ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
           if (++stage == S) {
@@ -267,11 +287,14 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    // warp w may read TMEM lanes 32*(w%4) .. +31; the two warps of a lane
-    // quarter split the tile's columns in halves.
-    constexpr int kHalf = BN / 2;
+    // warp w may read TMEM lanes 32*(w%4) .. +31.  The two warps of a lane
+    // quarter take one 128-pixel sub-tile each (MT = 2) or half the columns
+    // of the single sub-tile (MT = 1).
+    constexpr int kCols = MT == 2 ? BN : BN / 2;
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
+    const int sub = MT == 2 ? half : 0;
+    const int col_off = MT == 2 ? 0 : half * kCols;
     const int row = q * 32 + lane;
     int buf = 0;
     uint32_t acc_phase = 0;
@@ -279,15 +302,16 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
       tc_fence_after();
       const int mt = tile / p.num_n_tiles, nt = tile % p.num_n_tiles;
-      const long long pix = (long long)mt * BM + row;
+      const long long pix = (long long)mt * TM + sub * BM + row;
       const bool valid = pix < p.P;
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + half * kHalf);
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
+                             (uint32_t)((buf * MT + sub) * BN + col_off);
 #pragma unroll 1
-      for (int j = 0; j < kHalf / 32; ++j) {
+      for (int j = 0; j < kCols / 32; ++j) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
         tmem_ld_wait();
-        const int col0 = nt * BN + half * kHalf + j * 32;
+        const int col0 = nt * BN + col_off + j * 32;
         if (valid && col0 < p.nout) store_chunk(p, pix, col0, v);
       }
       tc_fence_before();
@@ -586,11 +610,11 @@ int set_smem(K kernel, size_t bytes, int device) {
   return CONV3X3_OK;
 }
 
-template <int BN, bool kDgrad>
+template <int BN, int MT, bool kDgrad>
 int launch_igemm(const CUtensorMap& a, const CUtensorMap& b, const IgemmParams& prm,
                  const DevCtx& d, cudaStream_t st) {
-  using Cfg = IgemmCfg<BN>;
-  auto kern = k_igemm<BN, kDgrad>;
+  using Cfg = IgemmCfg<BN, MT>;
+  auto kern = k_igemm<BN, MT, kDgrad>;
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
   const int grid = tiles < d.num_sms ? tiles : d.num_sms;
@@ -598,23 +622,34 @@ int launch_igemm(const CUtensorMap& a, const CUtensorMap& b, const IgemmParams& 
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
-// N-tile width: the candidate with the fewest persistent-tile rounds times
-// the per-tile cost (MMA work ~ BN, plus a fixed A-tile share); near-ties go
-// to the wider tile, which re-reads A less often.
-int pick_bn(int nout, long long m_tiles, int num_sms) {
-  const int cand[4] = {256, 192, 128, 64};
-  int best = 128;
+struct TileShape {
+  int bn, mt;
+};
+
+// Tile choice.  Per 64-channel k-block a CTA tile of (128*MT) pixels x BN
+// channels stages (128*MT + BN) * 128 bytes into shared memory and keeps the
+// tensor core busy MT * BN / 128 * 256 cycles.  The stage ring (~200 KB) turns
+// over once per MMA-completion + TMA round trip (~2500 cycles), which caps
+// delivery near 80 B per cycle per SM; the k-block time is the larger of the
+// two.  Score = persistent-tile rounds x k-block time; near-ties go to the
+// tile listed first (larger).
+TileShape pick_tile(int nout, long long P, int num_sms) {
+  const TileShape cand[6] = {{256, 1}, {128, 2}, {192, 1}, {128, 1}, {64, 2}, {64, 1}};
+  TileShape best = {128, 1};
   double best_cost = -1.0;
-  for (int i = 0; i < 4; ++i) {
-    const int bn = cand[i];
-    const long long n_tiles = (nout + bn - 1) / bn;
-    const long long waste = n_tiles * bn - nout;
-    if (bn > 64 && waste * 2 > bn) continue;  // mostly-empty last tile
+  for (int i = 0; i < 6; ++i) {
+    const TileShape c = cand[i];
+    const long long n_tiles = (nout + c.bn - 1) / c.bn;
+    const long long waste = n_tiles * c.bn - nout;
+    if (c.bn > 64 && waste * 2 > c.bn) continue;  // mostly-empty last tile
+    const long long m_tiles = (P + 128LL * c.mt - 1) / (128LL * c.mt);
     const long long rounds = (m_tiles * n_tiles + num_sms - 1) / num_sms;
-    const double cost = (double)rounds * (bn + 32);
-    if (best_cost < 0 || cost < 0.93 * best_cost) {
+    const double mma = 256.0 * c.mt * c.bn / 128.0;
+    const double feed = (128.0 * c.mt + c.bn) * 128.0 / 80.0;
+    const double cost = (double)rounds * (mma > feed ? mma : feed);
+    if (best_cost < 0 || cost < 0.97 * best_cost) {
       best_cost = cost;
-      best = bn;
+      best = c;
     }
   }
   return best;
@@ -623,7 +658,15 @@ int pick_bn(int nout, long long m_tiles, int num_sms) {
 int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const float* bias, void* out,
               const Shape& s, int act, int out_f32, const DevCtx& d, cudaStream_t st) {
   const int nout = dgrad ? s.Cin : s.Cout;
-  const int bn = pick_bn(nout, (s.P() + BM - 1) / BM, d.num_sms);
+  TileShape ts = pick_tile(nout, s.P(), d.num_sms);
+  // CONV3X3_TILE="<BN>x<MT>" overrides the choice (tuning and tests)
+  if (const char* e = std::getenv("CONV3X3_TILE")) {
+    int bn_o = 0, mt_o = 0;
+    if (std::sscanf(e, "%dx%d", &bn_o, &mt_o) == 2 && (mt_o == 1 || mt_o == 2) &&
+        (bn_o == 64 || bn_o == 128 || bn_o == 192 || bn_o == 256) && 2 * mt_o * bn_o <= 512)
+      ts = TileShape{bn_o, mt_o};
+  }
+  const int bn = ts.bn;
   CUtensorMap ta, tb;
   int rc = make_im2col_map(&ta, a_src, s.N, s.H, s.W, a_ch, BM);
   if (rc) return rc;
@@ -639,16 +682,23 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   prm.W = s.W;
   prm.kchunks = (a_ch + BKC - 1) / BKC;
   prm.nout = nout;
-  prm.num_m_tiles = (int)((s.P() + BM - 1) / BM);
+  prm.num_m_tiles = (int)((s.P() + BM * ts.mt - 1) / (BM * ts.mt));
   prm.num_n_tiles = (nout + bn - 1) / bn;
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
-  switch (bn) {
-    case 64: return dgrad ? launch_igemm<64, true>(ta, tb, prm, d, st) : launch_igemm<64, false>(ta, tb, prm, d, st);
-    case 128: return dgrad ? launch_igemm<128, true>(ta, tb, prm, d, st) : launch_igemm<128, false>(ta, tb, prm, d, st);
-    case 192: return dgrad ? launch_igemm<192, true>(ta, tb, prm, d, st) : launch_igemm<192, false>(ta, tb, prm, d, st);
-    default: return dgrad ? launch_igemm<256, true>(ta, tb, prm, d, st) : launch_igemm<256, false>(ta, tb, prm, d, st);
+#define C3_LAUNCH(BN_, MT_) \
+  return dgrad ? launch_igemm<BN_, MT_, true>(ta, tb, prm, d, st) : launch_igemm<BN_, MT_, false>(ta, tb, prm, d, st)
+  if (ts.mt == 2) {
+    if (bn == 64) C3_LAUNCH(64, 2);
+    C3_LAUNCH(128, 2);
   }
+  switch (bn) {
+    case 64: C3_LAUNCH(64, 1);
+    case 128: C3_LAUNCH(128, 1);
+    case 192: C3_LAUNCH(192, 1);
+    default: C3_LAUNCH(256, 1);
+  }
+#undef C3_LAUNCH
 }
 
 struct WgPlan {
