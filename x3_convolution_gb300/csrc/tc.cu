@@ -46,12 +46,26 @@ namespace {
 
 constexpr int BM = 128;              // output pixels per tile (MMA M, TMEM lanes)
 constexpr int BKC = 64;              // channels per k-block: one 128-byte swizzle row
-constexpr int kThreads = 192;        // wgrad: TMA warp, MMA warp, 4 epilogue warps
+// Warp roles.  TMA copies issued by one thread do not overlap each other, so
+// every stage's boxes are spread over kProd producer warps (warps 0..3); warp
+// kProd allocates TMEM and issues the MMAs; the rest drain the accumulators.
+constexpr int kProd = 4;
+constexpr int kMmaWarp = kProd;
+constexpr int kEpiBase = kProd + 1;
 constexpr int kEpiWarps = 8;         // igemm: two epilogue warps per TMEM lane quarter
-constexpr int kIgemmThreads = 64 + 32 * kEpiWarps;
+constexpr int kIgemmThreads = 32 * (kProd + 1 + kEpiWarps);
+constexpr int kWgEpiWarps = 4;       // wgrad: one epilogue warp per lane quarter
+constexpr int kThreads = 32 * (kProd + 1 + kWgEpiWarps);
 constexpr uint32_t kABytes = BM * BKC * 2;
 constexpr int kPlanSms = 152;        // split plan constant (shape-only workspace size)
 constexpr size_t kGuardBytes = 16 * 1024;
+
+// After an abort, copies still in flight land within microseconds; a stage
+// whose other producers never issued their boxes will not complete, so the
+// drain waits are kept short.
+__device__ __forceinline__ unsigned long long drain_wait_ns(unsigned long long w) {
+  return w < 50000000ULL ? w : 50000000ULL;
+}
 
 constexpr int pow2_cols(int n) { return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512; }
 
@@ -152,7 +166,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full[i], kProd);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -165,7 +179,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, Cfg::kTmemCols);
     tmem_relinquish();
   }
@@ -174,8 +188,11 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp < kProd) {
+    // ------------------------------------------------------------ TMA producers
+    // Stage boxes: MT im2col A boxes (128 pixels x 64 channels) then BN/64
+    // weight boxes (64 rows x 64 channels); producer `warp` issues box b when
+    // b % kProd == warp and registers its own byte count on the full barrier.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -202,17 +219,25 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
           }
           uint8_t* sa = smem + (size_t)stage * Cfg::kStageBytes;
           uint8_t* sb = sa + Cfg::kATileBytes;
-          mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+          constexpr int kBoxes = MT + BN / 64;
+          uint32_t bytes = 0;
 #pragma unroll
-          for (int u = 0; u < MT; ++u)
-            tma_load_im2col_4d(sa + u * kABytes, &tmA, &full[stage], cc * BKC, cw[u], ch[u], cn[u],
-                               (uint16_t)(tap % 3), (uint16_t)(tap / 3));
-          if (!kDgrad) {
-            tma_load_3d(sb, &tmB, &full[stage], cc * BKC, tap, nt * BN);
-          } else {
+          for (int b = 0; b < kBoxes; ++b)
+            if (b % kProd == warp) bytes += b < MT ? kABytes : 8192u;
+          mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_3d(sb + j * 8192, &tmB, &full[stage], nt * BN + j * 64, 8 - tap, cc * BKC);
+          for (int b = 0; b < kBoxes; ++b) {
+            if (b % kProd != warp) continue;
+            if (b < MT) {
+              tma_load_im2col_4d(sa + b * kABytes, &tmA, &full[stage], cc * BKC, cw[b], ch[b], cn[b],
+                                 (uint16_t)(tap % 3), (uint16_t)(tap / 3));
+            } else {
+              const int j = b - MT;
+              if (!kDgrad)
+                tma_load_3d(sb + j * 8192, &tmB, &full[stage], cc * BKC, tap, nt * BN + j * 64);
+              else
+                tma_load_3d(sb + j * 8192, &tmB, &full[stage], nt * BN + j * 64, 8 - tap, cc * BKC);
+            }
           }
           ++issued;
           if (++stage == S) {
@@ -231,12 +256,12 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
             st = S - 1;
             ph ^= 1;
           }
-          mbar_wait(&full[st], ph, p.wait_ns, nullptr, nullptr);
+          mbar_wait(&full[st], ph, drain_wait_ns(p.wait_ns), nullptr, nullptr);
         }
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, kDgrad ? 1 : 0);
@@ -292,7 +317,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     // of the single sub-tile (MT = 1).
     constexpr int kCols = MT == 2 ? BN : BN / 2;
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int half = (warp - kEpiBase) >> 2;
     const int sub = MT == 2 ? half : 0;
     const int col_off = MT == 2 ? 0 : half * kCols;
     const int row = q * 32 + lane;
@@ -327,7 +352,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, Cfg::kTmemCols);
 }
 
 // ----------------------------------------------------------------------------
@@ -380,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < kWgStages; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full[i], kProd);
       mbar_init(&empty[i], 1);
     }
     mbar_init(tfull, 1);
@@ -390,13 +415,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmDY);
     tma_prefetch_desc(&tmX);
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kWgTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 2) {  // fill the ones block (bf16 1.0 = 0x3F80)
+  if (warp >= kEpiBase) {  // fill the ones block (bf16 1.0 = 0x3F80)
     uint32_t* o = reinterpret_cast<uint32_t*>(ones);
-    for (int i = threadIdx.x - 64; i < 128; i += 128) o[i] = 0x3F803F80u;
+    for (int i = threadIdx.x - 32 * kEpiBase; i < 128; i += 32 * kWgEpiWarps) o[i] = 0x3F803F80u;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   tc_fence_before();
@@ -404,7 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp < kProd) {
+    // Eight 8 KB boxes per stage: two dy boxes (64 pixels x 64 output
+    // channels) then, per tap, two im2col x boxes (64 pixels x 64 channels);
+    // producer `warp` issues boxes warp and warp + 4.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -420,15 +448,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h0 = rem / p.W, w0 = rem - (rem / p.W) * p.W;
         uint8_t* sa = smem + (size_t)stage * kWgStageBytes;
         uint8_t* sb = sa + kWgABytes;
-        mbar_arrive_expect_tx(&full[stage], kWgStageBytes);
-        tma_load_2d(sa, &tmDY, &full[stage], mb * 128, pk);
-        tma_load_2d(sa + 8192, &tmDY, &full[stage], mb * 128 + 64, pk);
+        mbar_arrive_expect_tx(&full[stage], 2 * 8192);
 #pragma unroll
-        for (int t = 0; t < kWgTaps; ++t)
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
+        for (int b = warp; b < 8; b += kProd) {
+          if (b < 2) {
+            tma_load_2d(sa + b * 8192, &tmDY, &full[stage], mb * 128 + b * 64, pk);
+          } else {
+            const int t = (b - 2) >> 1, j = (b - 2) & 1;
             tma_load_im2col_4d(sb + (t * 2 + j) * 8192, &tmX, &full[stage], cb * 128 + j * 64,
                                w0 - 1, h0 - 1, n0, (uint16_t)t, (uint16_t)tr);
+          }
+        }
         ++issued;
         if (++stage == kWgStages) {
           stage = 0;
@@ -444,12 +474,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             st = kWgStages - 1;
             ph ^= 1;
           }
-          mbar_wait(&full[st], ph, p.wait_ns, nullptr, nullptr);
+          mbar_wait(&full[st], ph, drain_wait_ns(p.wait_ns), nullptr, nullptr);
         }
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idesc256 = idesc_bf16_f32(128, 256, 1, 1);
       constexpr uint32_t idesc128 = idesc_bf16_f32(128, 128, 1, 1);
@@ -534,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, kWgTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, kWgTmemCols);
 }
 
 // ----------------------------------------------------------------------------
@@ -670,7 +700,7 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   CUtensorMap ta, tb;
   int rc = make_im2col_map(&ta, a_src, s.N, s.H, s.W, a_ch, BM);
   if (rc) return rc;
-  rc = make_weight_map(&tb, w, s.Cin, s.Cout, dgrad ? 64 : bn);
+  rc = make_weight_map(&tb, w, s.Cin, s.Cout, 64);
   if (rc) return rc;
   IgemmParams prm;
   prm.out = out;
