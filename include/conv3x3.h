@@ -47,9 +47,11 @@
  * time, record CONV3X3_ERR_TIMEOUT in the device status word and exit cleanly;
  * read it with conv3x3_device_status().
  *
- * Tuning override: the environment variable CONV3X3_TILE="<BN>x<MT>" (BN in
- * {64,128,192,256}, MT in {1,2}, 2*MT*BN <= 512) forces the forward / dgrad
- * tensor-core tile to MT*128 pixels x BN channels; unset, the library picks.
+ * Tuning override: the environment variable CONV3X3_TILE forces the forward /
+ * dgrad tensor-core tile: "<BN>x<MT>" (BN in {64,128,192,256}, MT in {1,2},
+ * 2*MT*BN <= 512) selects the im2col kernel with MT*128 pixels x BN channels,
+ * "halo<BN>" (BN in {64,128}; images of width 16, 32 or 64 whose height is a
+ * multiple of 256/W) the row-halo kernel.  Unset, the library picks.
  */
 #ifndef CONV3X3_H
 #define CONV3X3_H

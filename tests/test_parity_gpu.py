@@ -147,6 +147,31 @@ def test_every_tensor_tile_shape(shape, tile, monkeypatch):
     assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
 
 
+HALO_SHAPES = [
+    (2, 64, 64, 16, 16),    # W = 16: one tile = one whole image
+    (1, 72, 200, 8, 32),    # W = 32, ragged channel chunk and ragged N tile
+    (2, 128, 128, 4, 64),   # W = 64, tiles of 4 rows
+    (3, 8, 128, 16, 16),    # 8 input channels
+    (1, 192, 256, 32, 32),  # several tiles per image, 3 channel chunks
+]
+
+
+@pytest.mark.parametrize("tile", ["halo64", "halo128"])
+@pytest.mark.parametrize("shape", HALO_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_halo_tiles(shape, tile, monkeypatch):
+    monkeypatch.setenv("CONV3X3_TILE", tile)
+    t = _small(shape)
+    x, w, b, dy = dev_tensors(t)
+    y32 = ops.fwd(x, w, b, act=1, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    ybf = ops.fwd(x, w, b, act=1, path=L.PATH_TENSOR)
+    dx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    ref = oracle.conv3x3_fwd(t.x, t.w, t.bias, 1)
+    assert rel_err(host(y32), ref) <= TOL_BF16
+    assert np.array_equal(host(ybf), rne_bf16(host(y32)))
+    assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
+
+
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_wgrad_is_bit_deterministic(path):
     t = _small((4, 128, 128, 16, 16))

@@ -356,6 +356,270 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 }
 
 // ----------------------------------------------------------------------------
+// forward / dgrad implicit GEMM, halo variant (image widths 16, 32, 64)
+// ----------------------------------------------------------------------------
+// A CTA tile is R = 256 / W whole image rows (256 output pixels, two 128-row
+// MMAs per k-step).  For each 64-channel chunk and column shift s in {0,1,2}
+// one tiled TMA box holds the R + 2 zero-padded input rows h0-1 .. h0+R at
+// columns s-1 .. s-2+W; it serves all three row taps r, whose A operand is the
+// same box from row r*W on (a 1024-byte-aligned offset).  Every input pixel is
+// staged three times per chunk instead of nine.  A boxes and weight tiles
+// stream through separate rings; producer warps 0-1 load the two halves of
+// each A box, warps 2-3 the 64-row halves of each weight tile.
+template <int W_, int BN>
+struct HaloCfg {
+  static constexpr int R = 256 / W_;
+  static constexpr int kHalfRows = (R + 2) / 2;
+  static constexpr uint32_t kABytes = (uint32_t)(R + 2) * W_ * 128;
+  static constexpr uint32_t kAHalfBytes = kABytes / 2;
+  static constexpr uint32_t kBBytes = BN * 128;
+  static constexpr int kSA = 3;
+  static constexpr int kSBFit = (int)((208u * 1024u - kSA * kABytes) / kBBytes);
+  static constexpr int kSB = kSBFit > 8 ? 8 : kSBFit;
+  static constexpr int kTmemCols = pow2_cols(4 * BN);
+  static constexpr size_t kSmem = (size_t)kSA * kABytes + (size_t)kSB * kBBytes + 512 + 1024 + 8 * 1024;
+  static_assert((R + 2) % 2 == 0 && kAHalfBytes % 1024 == 0, "A halves must stay swizzle-atom aligned");
+  static_assert(kSB >= 3, "weight ring too shallow");
+};
+
+template <int W_, int BN, bool kDgrad>
+__global__ void __launch_bounds__(kIgemmThreads, 1)
+    k_halo(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+           const IgemmParams p) {
+  using Cfg = HaloCfg<W_, BN>;
+  constexpr int SA = Cfg::kSA, SB = Cfg::kSB, TM = 256;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* ringA = smem;
+  uint8_t* ringB = smem + (size_t)SA * Cfg::kABytes;
+  uint64_t* fullA = reinterpret_cast<uint64_t*>(ringB + (size_t)SB * Cfg::kBBytes);
+  uint64_t* emptyA = fullA + SA;
+  uint64_t* fullB = emptyA + SA;
+  uint64_t* emptyB = fullB + SB;
+  uint64_t* tfull = emptyB + SB;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+  const int HW = p.H * W_;
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < SA; ++i) {
+      mbar_init(&fullA[i], 2);
+      mbar_init(&emptyA[i], 1);
+    }
+    for (int i = 0; i < SB; ++i) {
+      mbar_init(&fullB[i], 2);
+      mbar_init(&emptyB[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp < 2) {
+    // ------------------------------------------------------------ A-box producers
+    if (lane == 0) {
+      int st = 0, issued = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int mt = tile / p.num_n_tiles;
+        const int p0 = mt * TM;
+        const int n0 = p0 / HW, h0 = (p0 - n0 * HW) / W_;
+        for (int cc = 0; cc < p.kchunks && ok; ++cc)
+          for (int s = 0; s < 3; ++s) {
+            if (!mbar_wait(&emptyA[st], ph ^ 1, p.wait_ns, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&fullA[st], Cfg::kAHalfBytes);
+            tma_load_4d(ringA + (size_t)st * Cfg::kABytes + warp * Cfg::kAHalfBytes, &tmA, &fullA[st],
+                        cc * BKC, s - 1, h0 - 1 + warp * Cfg::kHalfRows, n0);
+            ++issued;
+            if (++st == SA) {
+              st = 0;
+              ph ^= 1;
+            }
+          }
+      }
+      if (!ok) {
+        int n = issued < SA ? issued : SA;
+        for (int i = 0; i < n; ++i) {
+          if (--st < 0) {
+            st = SA - 1;
+            ph ^= 1;
+          }
+          mbar_wait(&fullA[st], ph, drain_wait_ns(p.wait_ns), nullptr, nullptr);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < kProd) {
+    // ------------------------------------------------------------ weight producers
+    if (lane == 0) {
+      const int j = warp - 2;  // 64-row half of the weight tile
+      const bool loads = j < BN / 64;
+      int st = 0, issued = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int nt = tile % p.num_n_tiles;
+        for (int cc = 0; cc < p.kchunks && ok; ++cc)
+          for (int s = 0; s < 3 && ok; ++s)
+            for (int r = 0; r < 3; ++r) {
+              if (!mbar_wait(&emptyB[st], ph ^ 1, p.wait_ns, p.status, abort_flag)) {
+                ok = false;
+                break;
+              }
+              const int tap = 3 * r + s;
+              mbar_arrive_expect_tx(&fullB[st], loads ? 8192u : 0u);
+              if (loads) {
+                uint8_t* dst = ringB + (size_t)st * Cfg::kBBytes + j * 8192;
+                if (!kDgrad)
+                  tma_load_3d(dst, &tmB, &fullB[st], cc * BKC, tap, nt * BN + j * 64);
+                else
+                  tma_load_3d(dst, &tmB, &fullB[st], nt * BN + j * 64, 8 - tap, cc * BKC);
+              }
+              ++issued;
+              if (++st == SB) {
+                st = 0;
+                ph ^= 1;
+              }
+            }
+      }
+      if (!ok) {
+        int n = issued < SB ? issued : SB;
+        for (int i = 0; i < n; ++i) {
+          if (--st < 0) {
+            st = SB - 1;
+            ph ^= 1;
+          }
+          mbar_wait(&fullB[st], ph, drain_wait_ns(p.wait_ns), nullptr, nullptr);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, kDgrad ? 1 : 0);
+      int sa = 0, sb = 0, buf = 0;
+      uint32_t pa = 0, pb = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[buf], acc_phase ^ 1, p.wait_ns, p.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * 2 * BN);
+        bool first = true;
+        for (int cc = 0; cc < p.kchunks && ok; ++cc)
+          for (int s = 0; s < 3 && ok; ++s) {
+            if (!mbar_wait(&fullA[sa], pa, p.wait_ns, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(ringA + (size_t)sa * Cfg::kABytes);
+            for (int r = 0; r < 3; ++r) {
+              if (!mbar_wait(&fullB[sb], pb, p.wait_ns, p.status, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t b_base = smem_u32(ringB + (size_t)sb * Cfg::kBBytes);
+#pragma unroll
+              for (int k = 0; k < BKC / 16; ++k) {
+                const uint64_t bdesc = kDgrad ? smem_desc(b_base + k * 2048, 8192, 1024, kSwizzle128B)
+                                              : smem_desc(b_base + k * 32, 16, 1024, kSwizzle128B);
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+                  tc_mma_bf16(d_tmem + (uint32_t)(u * BN),
+                              smem_desc(a_base + (uint32_t)(u * BM + r * W_) * 128 + k * 32, 16, 1024,
+                                        kSwizzle128B),
+                              bdesc, idesc, (first && k == 0) ? 0u : 1u);
+              }
+              first = false;
+              tc_commit(&emptyB[sb]);
+              if (++sb == SB) {
+                sb = 0;
+                pb ^= 1;
+              }
+            }
+            if (!ok) break;
+            tc_commit(&emptyA[sa]);
+            if (++sa == SA) {
+              sa = 0;
+              pa ^= 1;
+            }
+          }
+        if (!ok) break;
+        tc_commit(&tfull[buf]);
+        if (++buf == 2) {
+          buf = 0;
+          acc_phase ^= 1;
+        }
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, p.wait_ns, nullptr, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int sub = (warp - kEpiBase) >> 2;  // 128-pixel half of the tile
+    const int row = q * 32 + lane;
+    int buf = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
+      tc_fence_after();
+      const int mt = tile / p.num_n_tiles, nt = tile % p.num_n_tiles;
+      const long long pix = (long long)mt * TM + sub * BM + row;
+      const bool valid = pix < p.P;
+      const uint32_t taddr =
+          tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((buf * 2 + sub) * BN);
+#pragma unroll 1
+      for (int j = 0; j < BN / 32; ++j) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
+        tmem_ld_wait();
+        const int col0 = nt * BN + j * 32;
+        if (valid && col0 < p.nout) store_chunk(p, pix, col0, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (++buf == 2) {
+        buf = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+}
+
+// ----------------------------------------------------------------------------
 // wgrad split-K implicit GEMM
 // ----------------------------------------------------------------------------
 constexpr int kWgTaps = 3;                       // taps per CTA tile (one kernel row)
@@ -585,6 +849,22 @@ int make_im2col_map(CUtensorMap* m, const void* base, int N, int H, int W, int C
   return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
+// NHWC activations as a tiled 4-D map; box {64 channels, W, rows, 1 image}.
+// Boxes may start at w = -1 or h = -1 and run past the far edge: those
+// elements read as zero (the convolution's padding).
+int make_halo_map(CUtensorMap* m, const void* base, int N, int H, int W, int C, int rows) {
+  PFN_encodeTiled enc = encode_tiled_fn();
+  if (!enc) return CONV3X3_ERR_CUDA;
+  cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)N};
+  cuuint64_t strides[3] = {(cuuint64_t)C * 2, (cuuint64_t)W * C * 2, (cuuint64_t)H * W * C * 2};
+  cuuint32_t box[4] = {(cuuint32_t)BKC, (cuuint32_t)W, (cuuint32_t)rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
 // KRSC weights viewed as {Cin, 9, Cout}; box {64, 1, rows}.
 int make_weight_map(CUtensorMap* m, const void* w, int Cin, int Cout, int rows) {
   PFN_encodeTiled enc = encode_tiled_fn();
@@ -652,8 +932,21 @@ int launch_igemm(const CUtensorMap& a, const CUtensorMap& b, const IgemmParams& 
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
+template <int W_, int BN, bool kDgrad>
+int launch_halo(const CUtensorMap& a, const CUtensorMap& b, const IgemmParams& prm,
+                const DevCtx& d, cudaStream_t st) {
+  using Cfg = HaloCfg<W_, BN>;
+  auto kern = k_halo<W_, BN, kDgrad>;
+  if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+  const int tiles = prm.num_m_tiles * prm.num_n_tiles;
+  const int grid = tiles < d.num_sms ? tiles : d.num_sms;
+  kern<<<grid, kIgemmThreads, Cfg::kSmem, st>>>(a, b, prm);
+  return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
 struct TileShape {
   int bn, mt;
+  bool halo;
 };
 
 // Tile choice.  Per 64-channel k-block a CTA tile of (128*MT) pixels x BN
@@ -663,10 +956,27 @@ struct TileShape {
 // delivery near 80 B per cycle per SM; the k-block time is the larger of the
 // two.  Score = persistent-tile rounds x k-block time; near-ties go to the
 // tile listed first (larger).
-TileShape pick_tile(int nout, long long P, int num_sms) {
-  const TileShape cand[6] = {{256, 1}, {128, 2}, {192, 1}, {128, 1}, {64, 2}, {64, 1}};
-  TileShape best = {128, 1};
+TileShape pick_tile(int nout, const Shape& sh, int num_sms) {
+  const long long P = sh.P();
+  const TileShape cand[6] = {{256, 1, false}, {128, 2, false}, {192, 1, false},
+                             {128, 1, false}, {64, 2, false}, {64, 1, false}};
+  TileShape best = {128, 1, false};
   double best_cost = -1.0;
+  // Halo tiles (256 pixels = whole rows of one image, BN <= 128): bytes per
+  // 64-channel tap step = (3 A boxes + 9 weight tiles) / 9.
+  if ((sh.W == 16 || sh.W == 32 || sh.W == 64) && sh.H % (256 / sh.W) == 0) {
+    const int bn = nout > 64 ? 128 : 64;
+    const long long n_tiles = (nout + bn - 1) / bn;
+    const long long waste = n_tiles * bn - nout;
+    if (bn == 64 || waste * 2 <= bn) {
+      const long long rounds = (P / 256 * n_tiles + num_sms - 1) / num_sms;
+      const double mma = 512.0 * bn / 128.0;
+      const double a_bytes = 3.0 * (256 + 2 * sh.W) * 128.0;
+      const double feed = (a_bytes + 9.0 * bn * 128.0) / 9.0 / 80.0;
+      best_cost = (double)rounds * (mma > feed ? mma : feed);
+      best = {bn, 2, true};
+    }
+  }
   for (int i = 0; i < 6; ++i) {
     const TileShape c = cand[i];
     const long long n_tiles = (nout + c.bn - 1) / c.bn;
@@ -688,17 +998,21 @@ TileShape pick_tile(int nout, long long P, int num_sms) {
 int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const float* bias, void* out,
               const Shape& s, int act, int out_f32, const DevCtx& d, cudaStream_t st) {
   const int nout = dgrad ? s.Cin : s.Cout;
-  TileShape ts = pick_tile(nout, s.P(), d.num_sms);
-  // CONV3X3_TILE="<BN>x<MT>" overrides the choice (tuning and tests)
+  TileShape ts = pick_tile(nout, s, d.num_sms);
+  // CONV3X3_TILE="<BN>x<MT>" or "halo<BN>" overrides the choice (tuning and tests)
   if (const char* e = std::getenv("CONV3X3_TILE")) {
     int bn_o = 0, mt_o = 0;
-    if (std::sscanf(e, "%dx%d", &bn_o, &mt_o) == 2 && (mt_o == 1 || mt_o == 2) &&
-        (bn_o == 64 || bn_o == 128 || bn_o == 192 || bn_o == 256) && 2 * mt_o * bn_o <= 512)
-      ts = TileShape{bn_o, mt_o};
+    const bool halo_ok = (s.W == 16 || s.W == 32 || s.W == 64) && s.H % (256 / s.W) == 0;
+    if (std::sscanf(e, "halo%d", &bn_o) == 1 && halo_ok && (bn_o == 64 || bn_o == 128))
+      ts = TileShape{bn_o, 2, true};
+    else if (std::sscanf(e, "%dx%d", &bn_o, &mt_o) == 2 && (mt_o == 1 || mt_o == 2) &&
+             (bn_o == 64 || bn_o == 128 || bn_o == 192 || bn_o == 256) && 2 * mt_o * bn_o <= 512)
+      ts = TileShape{bn_o, mt_o, false};
   }
   const int bn = ts.bn;
   CUtensorMap ta, tb;
-  int rc = make_im2col_map(&ta, a_src, s.N, s.H, s.W, a_ch, BM);
+  int rc = ts.halo ? make_halo_map(&ta, a_src, s.N, s.H, s.W, a_ch, (256 / s.W + 2) / 2)
+                   : make_im2col_map(&ta, a_src, s.N, s.H, s.W, a_ch, BM);
   if (rc) return rc;
   rc = make_weight_map(&tb, w, s.Cin, s.Cout, 64);
   if (rc) return rc;
@@ -716,6 +1030,21 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   prm.num_n_tiles = (nout + bn - 1) / bn;
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
+  if (ts.halo) {
+#define C3_HALO(W_, BN_) \
+  return dgrad ? launch_halo<W_, BN_, true>(ta, tb, prm, d, st) : launch_halo<W_, BN_, false>(ta, tb, prm, d, st)
+    if (s.W == 64) {
+      if (bn == 64) C3_HALO(64, 64);
+      C3_HALO(64, 128);
+    }
+    if (s.W == 32) {
+      if (bn == 64) C3_HALO(32, 64);
+      C3_HALO(32, 128);
+    }
+    if (bn == 64) C3_HALO(16, 64);
+    C3_HALO(16, 128);
+#undef C3_HALO
+  }
 #define C3_LAUNCH(BN_, MT_) \
   return dgrad ? launch_igemm<BN_, MT_, true>(ta, tb, prm, d, st) : launch_igemm<BN_, MT_, false>(ta, tb, prm, d, st)
   if (ts.mt == 2) {
