@@ -962,9 +962,11 @@ TileShape pick_tile(int nout, const Shape& sh, int num_sms) {
                              {128, 1, false}, {64, 2, false}, {64, 1, false}};
   TileShape best = {128, 1, false};
   double best_cost = -1.0;
-  // Halo tiles (256 pixels = whole rows of one image, BN <= 128): bytes per
-  // 64-channel tap step = (3 A boxes + 9 weight tiles) / 9.
-  if ((sh.W == 16 || sh.W == 32 || sh.W == 64) && sh.H % (256 / sh.W) == 0) {
+  // Halo tiles (256 pixels = whole rows of one image, BN <= 128) stage a
+  // third of the im2col bytes, but measured slower than the im2col kernels on
+  // GB300 (the copies, not the bytes, set the pace); they stay selectable
+  // through CONV3X3_TILE and are not scored here.
+  if (false && (sh.W == 16 || sh.W == 32 || sh.W == 64) && sh.H % (256 / sh.W) == 0) {
     const int bn = nout > 64 ? 128 : 64;
     const long long n_tiles = (nout + bn - 1) / bn;
     const long long waste = n_tiles * bn - nout;
