@@ -50,6 +50,19 @@ constexpr int BKC = 64;              // channels per k-block: one 128-byte swizz
 // every stage's boxes are spread over kProd producer warps (warps 0..3); warp
 // kProd allocates TMEM and issues the MMAs; the rest drain the accumulators.
 constexpr int kProd = 4;
+// How the producers share the im2col kernel's stages: each stage's boxes
+// spread over all producers, or whole stages handed out round-robin.  The
+// forward weight tile is one BN-row box or BN/64 boxes of 64 rows.
+#ifndef C3_STAGE_PARALLEL
+#define C3_STAGE_PARALLEL 1
+#endif
+#ifndef C3_ONE_WEIGHT_BOX
+#define C3_ONE_WEIGHT_BOX 1
+#endif
+
+constexpr bool kStageParallel = C3_STAGE_PARALLEL != 0;
+constexpr bool kOneWeightBox = C3_ONE_WEIGHT_BOX != 0;
+constexpr bool kWgStageParallel = false;  // the 3-stage wgrad ring is shared box-parallel
 constexpr int kMmaWarp = kProd;
 constexpr int kEpiBase = kProd + 1;
 constexpr int kEpiWarps = 8;         // igemm: two epilogue warps per TMEM lane quarter
@@ -149,6 +162,9 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   using Cfg = IgemmCfg<BN, MT>;
   constexpr int S = Cfg::kStages;
   constexpr int TM = BM * MT;  // pixels per CTA tile
+  // A producer's parity wait on a stage is unambiguous only while no producer
+  // can run a whole ring ahead: stage-parallel mode needs S >= kProd.
+  static_assert(!kStageParallel || S >= kProd, "stage-parallel producers need S >= kProd");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * Cfg::kStageBytes);
@@ -166,7 +182,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], kProd);
+      mbar_init(&full[i], kStageParallel ? 1 : kProd);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -213,30 +229,39 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
         }
         for (int kb = 0; kb < kblocks; ++kb) {
           const int tap = kb / p.kchunks, cc = kb - tap * p.kchunks;
-          if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          uint8_t* sa = smem + (size_t)stage * Cfg::kStageBytes;
-          uint8_t* sb = sa + Cfg::kATileBytes;
-          constexpr int kBoxes = MT + BN / 64;
-          uint32_t bytes = 0;
+          // stage-parallel mode: this producer owns every kProd-th stage
+          const bool mine = kStageParallel ? (issued % kProd == warp) : true;
+          if (mine) {
+            if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            uint8_t* sa = smem + (size_t)stage * Cfg::kStageBytes;
+            uint8_t* sb = sa + Cfg::kATileBytes;
+            // boxes: MT im2col A boxes, then the weight tile as one BN-row box
+            // (forward, K-major) or BN/64 boxes of 64 rows
+            constexpr bool kOneB = !kDgrad && kOneWeightBox;
+            constexpr int kBBoxes = kOneB ? 1 : BN / 64;
+            constexpr uint32_t kBBox = kOneB ? (uint32_t)BN * 128u : 8192u;
+            constexpr int kBoxes = MT + kBBoxes;
+            uint32_t bytes = 0;
 #pragma unroll
-          for (int b = 0; b < kBoxes; ++b)
-            if (b % kProd == warp) bytes += b < MT ? kABytes : 8192u;
-          mbar_arrive_expect_tx(&full[stage], bytes);
+            for (int b = 0; b < kBoxes; ++b)
+              if (kStageParallel || b % kProd == warp) bytes += b < MT ? kABytes : kBBox;
+            mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
-          for (int b = 0; b < kBoxes; ++b) {
-            if (b % kProd != warp) continue;
-            if (b < MT) {
-              tma_load_im2col_4d(sa + b * kABytes, &tmA, &full[stage], cc * BKC, cw[b], ch[b], cn[b],
-                                 (uint16_t)(tap % 3), (uint16_t)(tap / 3));
-            } else {
-              const int j = b - MT;
-              if (!kDgrad)
-                tma_load_3d(sb + j * 8192, &tmB, &full[stage], cc * BKC, tap, nt * BN + j * 64);
-              else
-                tma_load_3d(sb + j * 8192, &tmB, &full[stage], nt * BN + j * 64, 8 - tap, cc * BKC);
+            for (int b = 0; b < kBoxes; ++b) {
+              if (!kStageParallel && b % kProd != warp) continue;
+              if (b < MT) {
+                tma_load_im2col_4d(sa + b * kABytes, &tmA, &full[stage], cc * BKC, cw[b], ch[b], cn[b],
+                                   (uint16_t)(tap % 3), (uint16_t)(tap / 3));
+              } else {
+                const int j = b - MT;
+                if (!kDgrad)
+                  tma_load_3d(sb + j * kBBox, &tmB, &full[stage], cc * BKC, tap, nt * BN + j * 64);
+                else
+                  tma_load_3d(sb + j * 8192, &tmB, &full[stage], nt * BN + j * 64, 8 - tap, cc * BKC);
+              }
             }
           }
           ++issued;
@@ -628,6 +653,7 @@ constexpr uint32_t kWgABytes = 128 * kWgPix * 2;  // dy: 64 px x 128 Cout
 constexpr uint32_t kWgBBytes = 128 * kWgPix * 2;  // x: 64 px x 128 Cin, per tap
 constexpr uint32_t kWgStageBytes = kWgABytes + kWgTaps * kWgBBytes;
 constexpr int kWgStages = 3;
+static_assert(!kWgStageParallel || kWgStages >= kProd, "stage-parallel producers need S >= kProd");
 constexpr int kWgTmemCols = 512;                 // 3 x 128 dw columns + 16 dbias columns
 constexpr int kWgBiasCol = kWgTaps * 128;
 constexpr size_t kWgSmem = (size_t)kWgStages * kWgStageBytes + 512 + 256 + 1024 + kGuardBytes;
@@ -669,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < kWgStages; ++i) {
-      mbar_init(&full[i], kProd);
+      mbar_init(&full[i], kWgStageParallel ? 1 : kProd);
       mbar_init(&empty[i], 1);
     }
     mbar_init(tfull, 1);
@@ -703,24 +729,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       bool ok = true;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const int pk = kb * kWgPix;
-        const int n0 = pk / HW, rem = pk - n0 * HW;
-        const int h0 = rem / p.W, w0 = rem - (rem / p.W) * p.W;
-        uint8_t* sa = smem + (size_t)stage * kWgStageBytes;
-        uint8_t* sb = sa + kWgABytes;
-        mbar_arrive_expect_tx(&full[stage], 2 * 8192);
+        const bool mine = kWgStageParallel ? ((kb - kb0) % kProd == warp) : true;
+        if (mine) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int pk = kb * kWgPix;
+          const int n0 = pk / HW, rem = pk - n0 * HW;
+          const int h0 = rem / p.W, w0 = rem - (rem / p.W) * p.W;
+          uint8_t* sa = smem + (size_t)stage * kWgStageBytes;
+          uint8_t* sb = sa + kWgABytes;
+          mbar_arrive_expect_tx(&full[stage], kWgStageParallel ? kWgStageBytes : 2 * 8192);
 #pragma unroll
-        for (int b = warp; b < 8; b += kProd) {
-          if (b < 2) {
-            tma_load_2d(sa + b * 8192, &tmDY, &full[stage], mb * 128 + b * 64, pk);
-          } else {
-            const int t = (b - 2) >> 1, j = (b - 2) & 1;
-            tma_load_im2col_4d(sb + (t * 2 + j) * 8192, &tmX, &full[stage], cb * 128 + j * 64,
-                               w0 - 1, h0 - 1, n0, (uint16_t)t, (uint16_t)tr);
+          for (int b = kWgStageParallel ? 0 : warp; b < 8; b += kWgStageParallel ? 1 : kProd) {
+            if (b < 2) {
+              tma_load_2d(sa + b * 8192, &tmDY, &full[stage], mb * 128 + b * 64, pk);
+            } else {
+              const int t = (b - 2) >> 1, j = (b - 2) & 1;
+              tma_load_im2col_4d(sb + (t * 2 + j) * 8192, &tmX, &full[stage], cb * 128 + j * 64,
+                                 w0 - 1, h0 - 1, n0, (uint16_t)t, (uint16_t)tr);
+            }
           }
         }
         ++issued;
@@ -1016,7 +1045,7 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   int rc = ts.halo ? make_halo_map(&ta, a_src, s.N, s.H, s.W, a_ch, (256 / s.W + 2) / 2)
                    : make_im2col_map(&ta, a_src, s.N, s.H, s.W, a_ch, BM);
   if (rc) return rc;
-  rc = make_weight_map(&tb, w, s.Cin, s.Cout, 64);
+  rc = make_weight_map(&tb, w, s.Cin, s.Cout, (kOneWeightBox && !dgrad && !ts.halo) ? bn : 64);
   if (rc) return rc;
   IgemmParams prm;
   prm.out = out;
