@@ -139,6 +139,29 @@ int conv3x3_device_status(void* stream);
  * the CUDA context stays usable.  Returns the launch status. */
 int conv3x3_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
 
+/* Weight gradient without caller-provided scratch.  The pages have no
+ * counterpart of this entry point; it exists for callers that cannot allocate
+ * device memory -- e.g. a plugin inside a host application whose memory pool
+ * it may not draw on, or a latency-critical loop that may not call cudaMalloc
+ * (which can synchronise the device) after start-up.
+ * Same arguments, layouts and results as conv3x3_wgrad minus the workspace:
+ * the split-K scratch is a fixed array of CONV3X3_WGRAD_NOALLOC_MAX_BYTES in
+ * the library's own device memory, which every GPU that loads the library
+ * holds until the process exits.  Allocates nothing.
+ *   - Shapes whose conv3x3_wgrad_workspace_bytes() exceeds the maximum return
+ *     CONV3X3_ERR_WORKSPACE before anything is launched; invalid shapes
+ *     CONV3X3_ERR_INVALID_ARG.
+ *   - The first call on a device looks up that device's copy of the array
+ *     (cudaGetSymbolAddress, with the device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the array and it keeps the previous call's
+ *     contents (nothing needs clearing: every partial read is written first).
+ *     Calls whose work overlaps on the GPU -- different streams without an
+ *     ordering between them -- race on the array; order them on one stream. */
+#define CONV3X3_WGRAD_NOALLOC_MAX_BYTES (64ull << 20)
+int conv3x3_wgrad_noalloc(const void* x, const void* dy, float* dw, float* dbias,
+                          int N, int Cin, int Cout, int H, int W, void* stream);
+
 /* Static description of a status code ("ok", "invalid argument", ...). */
 const char* conv3x3_status_string(int status);
 

@@ -39,7 +39,10 @@ _SIGS = {
     "conv3x3_selftest_wait_timeout": ([_ull, _vp], _i),
     "conv3x3_status_string": ([_i], ctypes.c_char_p),
     "conv3x3_auto_path": ([_i] * 6, _i),
+    "conv3x3_wgrad_noalloc": ([_vp, _vp, _vp, _vp] + [_i] * 5 + [_vp], _i),
 }
+
+WGRAD_NOALLOC_MAX_BYTES = 64 << 20
 
 
 class Conv3x3Error(RuntimeError):
@@ -165,3 +168,11 @@ def conv3x3_auto_path(pass_, N, Cin, Cout, H, W) -> int:
 
 def conv3x3_status_string(status) -> str:
     return status_string(status)
+
+
+def conv3x3_wgrad_noalloc(x, dy, dw, dbias, N, Cin, Cout, H, W, stream=None):
+    """conv3x3_wgrad for callers that cannot allocate device memory: the split-K
+    scratch comes from a fixed 64 MiB array inside the library (see the C header
+    for the sharing rules)."""
+    return _check(load().conv3x3_wgrad_noalloc(_p(x), _p(dy), _p(dw), _p(dbias), N, Cin, Cout, H, W,
+                                               _stream(stream)), "conv3x3_wgrad_noalloc")
