@@ -415,20 +415,38 @@ __global__ void __launch_bounds__(kThreads) k_wgrad_bf16_c8_partial(
   }
 }
 
-// dw[e] = sum_{s=0}^{S-1} part[s][e] in increasing s; same for dbias.
+// dw[e] = sum_{s=0}^{S-1} part[s][e] in increasing s (four partials loaded at a
+// time, added strictly in order), four elements per thread; dbias likewise
+// over its Sdb partial rows stored after the S dw slices.
 __global__ void k_wgrad_reduce(const float* __restrict__ part, float* __restrict__ dw,
-                               float* __restrict__ db, long long dwsize, int Cout, int S) {
-  const long long total = dwsize + Cout;
+                               float* __restrict__ db, long long dwsize, int Cout, int S, int Sdb) {
+  const long long n4 = dwsize / 4;
+  const long long total = n4 + Cout;
+  const float4* p4 = reinterpret_cast<const float4*>(part);
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
-    if (e < dwsize) {
-      float acc = 0.0f;
-      for (int s = 0; s < S; ++s) acc += part[(long long)s * dwsize + e];
-      dw[e] = acc;
+    if (e < n4) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      int s = 0;
+      for (; s + 4 <= S; s += 4) {
+        const float4 a0 = __ldg(p4 + (long long)s * n4 + e);
+        const float4 a1 = __ldg(p4 + (long long)(s + 1) * n4 + e);
+        const float4 a2 = __ldg(p4 + (long long)(s + 2) * n4 + e);
+        const float4 a3 = __ldg(p4 + (long long)(s + 3) * n4 + e);
+        acc.x += a0.x; acc.y += a0.y; acc.z += a0.z; acc.w += a0.w;
+        acc.x += a1.x; acc.y += a1.y; acc.z += a1.z; acc.w += a1.w;
+        acc.x += a2.x; acc.y += a2.y; acc.z += a2.z; acc.w += a2.w;
+        acc.x += a3.x; acc.y += a3.y; acc.z += a3.z; acc.w += a3.w;
+      }
+      for (; s < S; ++s) {
+        const float4 a = __ldg(p4 + (long long)s * n4 + e);
+        acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+      }
+      reinterpret_cast<float4*>(dw)[e] = acc;
     } else if (db) {
-      long long k = e - dwsize;
+      const long long k = e - n4;
       float acc = 0.0f;
-      for (int s = 0; s < S; ++s) acc += part[(long long)S * dwsize + (long long)s * Cout + k];
+      for (int s = 0; s < Sdb; ++s) acc += part[(long long)S * dwsize + (long long)s * Cout + k];
       db[k] = acc;
     }
   }
@@ -475,8 +493,8 @@ WgradPlan wgrad_plan(const Shape& s) {
 }  // namespace
 
 int launch_wgrad_reduce(const float* part, float* dw, float* db, long long dwsize, int Cout, int S,
-                        cudaStream_t st) {
-  k_wgrad_reduce<<<grid_for(dwsize + Cout), kThreads, 0, st>>>(part, dw, db, dwsize, Cout, S);
+                        int Sdb, cudaStream_t st) {
+  k_wgrad_reduce<<<grid_for(dwsize / 4 + Cout), kThreads, 0, st>>>(part, dw, db, dwsize, Cout, S, Sdb);
   return launch_status();
 }
 
@@ -564,7 +582,7 @@ int simt_wgrad_bf16(const void* x, const void* dy, float* dw, float* db, const S
   }
   if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
   long long dwsize = (long long)s.Cout * 9 * s.Cin;
-  k_wgrad_reduce<<<grid_for(dwsize + s.Cout), kThreads, 0, st>>>(part, dw, db, dwsize, s.Cout, pl.S);
+  k_wgrad_reduce<<<grid_for(dwsize / 4 + s.Cout), kThreads, 0, st>>>(part, dw, db, dwsize, s.Cout, pl.S, pl.S);
   return launch_status();
 }
 

@@ -20,8 +20,11 @@
 //   three taps (64 pixels x 128 channels each, MN-major).  Each CTA owns one
 //   (Cout block, tap row, Cin block) tile and one contiguous pixel range and
 //   writes its fp32 partial tile to the caller's workspace; a second kernel
-//   adds the partials in split order (deterministic).  dbias rides along as an
-//   extra N = 16 MMA against a block of ones.
+//   adds the partials in split order (deterministic).  dbias rides along: in
+//   the CTAs that own it, the third tap's MMA is widened from N = 128 to 144
+//   and its extra 16 columns read an 8 KB block of bf16 ones that sits right
+//   after that tap's x tile in every stage (a separate N = 16 MMA costs about
+//   as much as an N = 64 one).
 //
 // The subject page's kernels minimise memory transfers and avoid global
 // transposes (clu0 C++/CUDA UNet diffusion, sourcepulse.org project page,
@@ -40,7 +43,7 @@
 namespace c3 {
 
 int launch_wgrad_reduce(const float* part, float* dw, float* db, long long dwsize, int Cout, int S,
-                        cudaStream_t st);
+                        int Sdb, cudaStream_t st);
 
 namespace {
 
@@ -651,12 +654,13 @@ constexpr int kWgTaps = 3;                       // taps per CTA tile (one kerne
 constexpr int kWgPix = 64;                       // pixels per k-block
 constexpr uint32_t kWgABytes = 128 * kWgPix * 2;  // dy: 64 px x 128 Cout
 constexpr uint32_t kWgBBytes = 128 * kWgPix * 2;  // x: 64 px x 128 Cin, per tap
-constexpr uint32_t kWgStageBytes = kWgABytes + kWgTaps * kWgBBytes;
+constexpr uint32_t kWgOnesBytes = 8192;          // 64 px x 64 columns of bf16 ones
+constexpr uint32_t kWgStageBytes = kWgABytes + kWgTaps * kWgBBytes + kWgOnesBytes;
 constexpr int kWgStages = 3;
 static_assert(!kWgStageParallel || kWgStages >= kProd, "stage-parallel producers need S >= kProd");
-constexpr int kWgTmemCols = 512;                 // 3 x 128 dw columns + 16 dbias columns
+constexpr int kWgTmemCols = 512;                 // 3 x 128 dw columns + 16 dbias columns (384..399)
 constexpr int kWgBiasCol = kWgTaps * 128;
-constexpr size_t kWgSmem = (size_t)kWgStages * kWgStageBytes + 512 + 256 + 1024 + kGuardBytes;
+constexpr size_t kWgSmem = (size_t)kWgStages * kWgStageBytes + 256 + 1024 + 8 * 1024;
 
 struct WgradParams {
   float* part;  // [S][Cout][9*Cin] then [S][Cout]
@@ -672,8 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const WgradParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint8_t* ones = smem + (size_t)kWgStages * kWgStageBytes;  // 16 x 16 bf16 ones (512 B)
-  uint64_t* full = reinterpret_cast<uint64_t*>(ones + 512);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kWgStages * kWgStageBytes);
   uint64_t* empty = full + kWgStages;
   uint64_t* tfull = empty + kWgStages;
   uint64_t* drain = tfull + 1;
@@ -709,9 +712,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, kWgTmemCols);
     tmem_relinquish();
   }
-  if (warp >= kEpiBase) {  // fill the ones block (bf16 1.0 = 0x3F80)
-    uint32_t* o = reinterpret_cast<uint32_t*>(ones);
-    for (int i = threadIdx.x - 32 * kEpiBase; i < 128; i += 32 * kWgEpiWarps) o[i] = 0x3F803F80u;
+  if (warp >= kEpiBase && do_bias) {  // fill every stage's ones block (bf16 1.0 = 0x3F80)
+    for (int st = 0; st < kWgStages; ++st) {
+      uint4* o = reinterpret_cast<uint4*>(smem + (size_t)st * kWgStageBytes + kWgABytes +
+                                          kWgTaps * kWgBBytes);
+      for (int i = threadIdx.x - 32 * kEpiBase; i < (int)(kWgOnesBytes / 16); i += 32 * kWgEpiWarps)
+        o[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   tc_fence_before();
@@ -776,8 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc256 = idesc_bf16_f32(128, 256, 1, 1);
       constexpr uint32_t idesc128 = idesc_bf16_f32(128, 128, 1, 1);
-      constexpr uint32_t idesc16 = idesc_bf16_f32(128, 16, 1, 0);
-      const uint64_t ones_desc = smem_desc(smem_u32(ones), 128, 256, kSwizzleNone);
+      constexpr uint32_t idesc144 = idesc_bf16_f32(128, 144, 1, 1);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -796,10 +802,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // taps 0 and 1: four 64-channel blocks at 8 KB stride -> one N = 256 MMA
           tc_mma_bf16(tmem_base, adesc, smem_desc(b_base + k * 2048, 8192, 1024, kSwizzle128B),
                       idesc256, acc);
+          // tap 2 (+ the ones block as a third 64-column block when this CTA owns dbias)
           tc_mma_bf16(tmem_base + 256, adesc,
                       smem_desc(b_base + 2 * kWgBBytes + k * 2048, 8192, 1024, kSwizzle128B),
-                      idesc128, acc);
-          if (do_bias) tc_mma_bf16(tmem_base + kWgBiasCol, adesc, ones_desc, idesc16, acc);
+                      do_bias ? idesc144 : idesc128, acc);
         }
         tc_commit(&empty[stage]);
         if (++stage == kWgStages) {
@@ -1173,7 +1179,7 @@ int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s
   if (set_smem(k_wgrad, kWgSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   k_wgrad<<<pl.tiles * pl.S, kThreads, kWgSmem, st>>>(tdy, tx, prm);
   if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
-  return launch_wgrad_reduce(prm.part, dw, db, (long long)s.Cout * 9 * s.Cin, s.Cout, pl.S, st);
+  return launch_wgrad_reduce(prm.part, dw, db, (long long)s.Cout * 9 * s.Cin, s.Cout, pl.S, pl.S, st);
 }
 
 }  // namespace c3
