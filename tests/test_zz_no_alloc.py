@@ -68,8 +68,8 @@ def test_noalloc_after_a_different_shape():
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    # up-path concat layer 896 -> 384 @16x16, batch 64: needs ~83 MiB of partials
-    N, Cin, Cout, H, W = 64, 896, 384, 16, 16
+    # 2048 -> 2048 channels: one dw partial alone is ~151 MB
+    N, Cin, Cout, H, W = 64, 2048, 2048, 8, 8
     assert L.conv3x3_wgrad_workspace_bytes(N, Cin, Cout, H, W) > L.WGRAD_NOALLOC_MAX_BYTES
     dummy = torch.empty(16, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(L.Conv3x3Error) as e:

@@ -1107,8 +1107,11 @@ WgPlan wg_plan(const Shape& s) {
   pl.num_cb = (s.Cin + 127) / 128;
   pl.tiles = pl.num_mb * 3 * pl.num_cb;
   pl.kb_total = (int)((s.P() + kWgPix - 1) / kWgPix);
-  // minimise waves * (k-blocks per split + fixed epilogue cost)
-  long long best = -1;
+  // Cost in units of one 64-pixel k-block on one CTA, fitted to GB300 timings:
+  // waves x (k-blocks per split + ~20 for a CTA's fill, drain and partial
+  // write) + the partial-sum traffic, ~0.3 per MB of dw per split.
+  const double dw_mb = (double)s.Cout * 9.0 * s.Cin * 4.0 / 1e6;
+  double best = -1;
   int bestS = 1;
   for (int S = 1; S <= pl.kb_total && S <= 1024; ++S) {
     int per = (pl.kb_total + S - 1) / S;
@@ -1116,11 +1119,17 @@ WgPlan wg_plan(const Shape& s) {
     if (Sreal != S) continue;
     long long units = (long long)pl.tiles * S;
     long long waves = (units + kPlanSms - 1) / kPlanSms;
-    long long cost = waves * (per + 6);
+    double cost = (double)waves * (per + 20) + 0.3 * S * dw_mb;
     if (best < 0 || cost < best) {
       best = cost;
       bestS = S;
     }
+  }
+  // CONV3X3_WGRAD_SPLITS=<S> overrides the split count (tuning); the workspace
+  // size follows, so set it before querying the size.
+  if (const char* e = std::getenv("CONV3X3_WGRAD_SPLITS")) {
+    const int v = std::atoi(e);
+    if (v >= 1 && v <= pl.kb_total) bestS = v;
   }
   pl.kb_per_split = (pl.kb_total + bestS - 1) / bestS;
   pl.S = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
