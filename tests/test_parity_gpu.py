@@ -172,6 +172,29 @@ def test_halo_tiles(shape, tile, monkeypatch):
     assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
 
 
+STEM_SHAPES = [
+    (2, 8, 24, 9, 9),     # Cout 24 < 64: one mostly-empty N tile, ragged pixel tail
+    (1, 8, 64, 7, 5),
+    (2, 8, 256, 8, 8),    # the widest single N tile
+    (3, 8, 128, 1, 13),   # single-row images
+    (5, 8, 128, 16, 16),  # several 128-pixel tiles per CTA
+]
+
+
+@pytest.mark.parametrize("shape", STEM_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_eight_channel_forward_kernel(shape):
+    t = _small(shape)
+    x, w, b, _ = dev_tensors(t)
+    for act in (0, 1):
+        y32 = ops.fwd(x, w, b, act=act, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+        ybf = ops.fwd(x, w, b, act=act, path=L.PATH_TENSOR)
+        torch.cuda.synchronize()
+        ref = oracle.conv3x3_fwd(t.x, t.w, t.bias, act)
+        assert rel_err(host(y32), ref) <= TOL_BF16
+        assert check_bf16_store(host(ybf), ref) == 0
+        assert np.array_equal(host(ybf), rne_bf16(host(y32)))
+
+
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_wgrad_is_bit_deterministic(path):
     t = _small((4, 128, 128, 16, 16))

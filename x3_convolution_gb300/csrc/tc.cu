@@ -648,6 +648,203 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 }
 
 // ----------------------------------------------------------------------------
+// forward, 8 input channels (the UNet stem: RGB zero-padded to 8)
+// ----------------------------------------------------------------------------
+// With 8 channels a tap is 16 bytes per pixel, so a 64-channel SW128 k-block
+// would be seven-eighths zero fill.  Here each tap is one im2col box of 128
+// pixels x 8 channels (2 KB, no swizzle): in the K-major no-swizzle operand
+// layout that box is exactly a column of 8x16-byte core matrices, and taps
+// 2j, 2j+1 form the K = 16 of MMA j (K = 9 taps x 8 + one zero tap = 80, five
+// MMAs per tile).  The weights ([Cout][9][8], 2 KB per tap for 128 outputs) stay
+// resident in shared memory for the whole kernel.
+template <int BN>
+struct StemCfg {
+  static constexpr uint32_t kTapBytes = BM * 16;           // 128 pixels x 8 channels
+  static constexpr uint32_t kStageBytes = 10 * kTapBytes;  // 9 taps + zero tap
+  static constexpr uint32_t kBTap = BN * 16;
+  static constexpr uint32_t kBBytes = 10 * kBTap;
+  static constexpr int kStages = 8;
+  static constexpr int kTmemCols = pow2_cols(2 * BN);
+  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + kBBytes + 512 + 1024;
+  static_assert(kStages >= kProd, "stage-parallel producers need S >= kProd");
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kIgemmThreads, 1)
+    k_stem_fwd(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const IgemmParams p) {
+  using Cfg = StemCfg<BN>;
+  constexpr int S = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* wsm = smem + (size_t)S * Cfg::kStageBytes;  // resident weights
+  uint64_t* full = reinterpret_cast<uint64_t*>(wsm + Cfg::kBBytes);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint64_t* wfull = drain + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wfull + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_tiles = p.num_m_tiles;
+  const int HW = p.H * p.W;
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    mbar_init(wfull, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp >= kEpiBase) {  // zero the tenth (padding) tap of every stage and of the weights
+    const int t = threadIdx.x - 32 * kEpiBase;
+    for (int st = 0; st < S; ++st) {
+      uint4* z = reinterpret_cast<uint4*>(smem + (size_t)st * Cfg::kStageBytes + 9 * Cfg::kTapBytes);
+      for (int i = t; i < (int)(Cfg::kTapBytes / 16); i += 32 * kEpiWarps) z[i] = make_uint4(0, 0, 0, 0);
+    }
+    uint4* z = reinterpret_cast<uint4*>(wsm + 9 * Cfg::kBTap);
+    for (int i = t; i < (int)(Cfg::kBTap / 16); i += 32 * kEpiWarps) z[i] = make_uint4(0, 0, 0, 0);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp < kProd) {
+    if (lane == 0) {
+      if (warp == 0) {  // resident weights: nine boxes of BN rows x 8 channels
+        mbar_arrive_expect_tx(wfull, 9 * Cfg::kBTap);
+        for (int t = 0; t < 9; ++t) tma_load_3d(wsm + t * Cfg::kBTap, &tmB, wfull, 0, t, 0);
+      }
+      // stage-parallel: this producer owns every kProd-th tile (one stage per tile)
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (issued % kProd == warp) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int p0 = tile * BM;
+          const int n0 = p0 / HW, rem = p0 - n0 * HW;
+          const int h0 = rem / p.W, w0 = rem - h0 * p.W;
+          uint8_t* sa = smem + (size_t)stage * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], 9 * Cfg::kTapBytes);
+          for (int t = 0; t < 9; ++t)
+            tma_load_im2col_4d(sa + t * Cfg::kTapBytes, &tmA, &full[stage], 0, w0 - 1, h0 - 1, n0,
+                               (uint16_t)(t % 3), (uint16_t)(t / 3));
+        }
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) {
+        int n = issued < S ? issued : S;
+        for (int i = 0; i < n; ++i) {
+          if (--stage < 0) {
+            stage = S - 1;
+            phase ^= 1;
+          }
+          mbar_wait(&full[stage], phase, drain_wait_ns(p.wait_ns), nullptr, nullptr);
+        }
+      }
+      if (warp == 0) mbar_wait(wfull, 0, drain_wait_ns(p.wait_ns), nullptr, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 0);
+      int stage = 0, buf = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = mbar_wait(wfull, 0, p.wait_ns, p.status, abort_flag);
+      tc_fence_after();
+      const uint32_t b_base = smem_u32(wsm);
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[buf], acc_phase ^ 1, p.wait_ns, p.status, abort_flag)) break;
+        if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(smem + (size_t)stage * Cfg::kStageBytes);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+#pragma unroll
+        for (int j = 0; j < 5; ++j)
+          tc_mma_bf16(d_tmem, smem_desc(a_base + 2 * j * Cfg::kTapBytes, Cfg::kTapBytes, 128, kSwizzleNone),
+                      smem_desc(b_base + 2 * j * Cfg::kBTap, Cfg::kBTap, 128, kSwizzleNone), idesc,
+                      j ? 1u : 0u);
+        tc_commit(&empty[stage]);
+        tc_commit(&tfull[buf]);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (++buf == 2) {
+          buf = 0;
+          acc_phase ^= 1;
+        }
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, p.wait_ns, nullptr, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // epilogue: as in k_igemm with one 128-pixel sub-tile (the two warps of a
+    // lane quarter take half the columns each)
+    constexpr int kCols = BN / 2;
+    const int q = warp & 3;
+    const int half = (warp - kEpiBase) >> 2;
+    const int col_off = half * kCols;
+    const int row = q * 32 + lane;
+    int buf = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
+      tc_fence_after();
+      const long long pix = (long long)tile * BM + row;
+      const bool valid = pix < p.P;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + col_off);
+#pragma unroll 1
+      for (int j = 0; j < kCols / 32; ++j) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
+        tmem_ld_wait();
+        const int col0 = col_off + j * 32;
+        if (valid && col0 < p.nout) store_chunk(p, pix, col0, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (++buf == 2) {
+        buf = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+}
+
+// ----------------------------------------------------------------------------
 // wgrad split-K implicit GEMM
 // ----------------------------------------------------------------------------
 constexpr int kWgTaps = 3;                       // taps per CTA tile (one kernel row)
@@ -869,7 +1066,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ----------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------
-int make_im2col_map(CUtensorMap* m, const void* base, int N, int H, int W, int C, int pixels) {
+int make_im2col_map(CUtensorMap* m, const void* base, int N, int H, int W, int C, int pixels,
+                    int channels = BKC, bool swizzle = true) {
   PFN_encodeIm2col enc = encode_im2col_fn();
   if (!enc) return CONV3X3_ERR_CUDA;
   cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)N};
@@ -878,8 +1076,9 @@ int make_im2col_map(CUtensorMap* m, const void* base, int N, int H, int W, int C
   int upper[2] = {-1, -1};  // pad 1 - (3 - 1): origins stop at size - 2
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
-                   lower, upper, (cuuint32_t)BKC, (cuuint32_t)pixels, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   lower, upper, (cuuint32_t)channels, (cuuint32_t)pixels, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
@@ -901,15 +1100,17 @@ int make_halo_map(CUtensorMap* m, const void* base, int N, int H, int W, int C, 
 }
 
 // KRSC weights viewed as {Cin, 9, Cout}; box {64, 1, rows}.
-int make_weight_map(CUtensorMap* m, const void* w, int Cin, int Cout, int rows) {
+int make_weight_map(CUtensorMap* m, const void* w, int Cin, int Cout, int rows, int channels = BKC,
+                    bool swizzle = true) {
   PFN_encodeTiled enc = encode_tiled_fn();
   if (!enc) return CONV3X3_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)Cin, 9, (cuuint64_t)Cout};
   cuuint64_t strides[2] = {(cuuint64_t)Cin * 2, (cuuint64_t)Cin * 9 * 2};
-  cuuint32_t box[3] = {(cuuint32_t)BKC, 1, (cuuint32_t)rows};
+  cuuint32_t box[3] = {(cuuint32_t)channels, 1, (cuuint32_t)rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
@@ -1032,6 +1233,45 @@ TileShape pick_tile(int nout, const Shape& sh, int num_sms) {
   return best;
 }
 
+template <int BN>
+int launch_stem(const CUtensorMap& a, const CUtensorMap& b, const IgemmParams& prm, const DevCtx& d,
+                cudaStream_t st) {
+  using Cfg = StemCfg<BN>;
+  auto kern = k_stem_fwd<BN>;
+  if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+  const int grid = prm.num_m_tiles < d.num_sms ? prm.num_m_tiles : d.num_sms;
+  kern<<<grid, kIgemmThreads, Cfg::kSmem, st>>>(a, b, prm);
+  return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
+// Forward with exactly 8 input channels and at most 256 outputs (one N tile).
+int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const Shape& s, int act,
+                 int out_f32, const DevCtx& d, cudaStream_t st) {
+  const int bn = s.Cout <= 64 ? 64 : s.Cout <= 128 ? 128 : 256;
+  CUtensorMap ta, tb;
+  int rc = make_im2col_map(&ta, x, s.N, s.H, s.W, 8, BM, 8, false);
+  if (rc) return rc;
+  rc = make_weight_map(&tb, w, 8, s.Cout, bn, 8, false);
+  if (rc) return rc;
+  IgemmParams prm;
+  prm.out = y;
+  prm.bias = bias;
+  prm.act = act;
+  prm.out_f32 = out_f32;
+  prm.P = (int)s.P();
+  prm.H = s.H;
+  prm.W = s.W;
+  prm.kchunks = 1;
+  prm.nout = s.Cout;
+  prm.num_m_tiles = (int)((s.P() + BM - 1) / BM);
+  prm.num_n_tiles = 1;
+  prm.status = d.status;
+  prm.wait_ns = d.wait_ns;
+  if (bn == 64) return launch_stem<64>(ta, tb, prm, d, st);
+  if (bn == 128) return launch_stem<128>(ta, tb, prm, d, st);
+  return launch_stem<256>(ta, tb, prm, d, st);
+}
+
 int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const float* bias, void* out,
               const Shape& s, int act, int out_f32, const DevCtx& d, cudaStream_t st) {
   const int nout = dgrad ? s.Cin : s.Cout;
@@ -1148,6 +1388,7 @@ bool tc_supported(int pass, const Shape& s) {
 
 int tc_fwd(const void* x, const void* w, const float* bias, void* y, const Shape& s, int act,
            int out_f32, const DevCtx& d, cudaStream_t st) {
+  if (s.Cin == 8 && s.Cout <= 256) return run_stem_fwd(x, w, bias, y, s, act, out_f32, d, st);
   return run_igemm(false, x, s.Cin, w, bias, y, s, act, out_f32, d, st);
 }
 
