@@ -182,9 +182,16 @@ STEM_SHAPES = [
 
 
 @pytest.mark.parametrize("shape", STEM_SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_eight_channel_forward_kernel(shape):
+def test_eight_channel_kernels(shape):
     t = _small(shape)
-    x, w, b, _ = dev_tensors(t)
+    x, w, b, dy = dev_tensors(t)
+    dw, db = ops.wgrad(x, dy, path=L.PATH_TENSOR)
+    dx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    rdw, rdb = oracle.conv3x3_wgrad(t.x, t.dy)
+    assert rel_err(host(dw), rdw) <= TOL_BF16
+    assert rel_err(host(db), rdb) <= TOL_BF16
+    assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
     for act in (0, 1):
         y32 = ops.fwd(x, w, b, act=act, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
         ybf = ops.fwd(x, w, b, act=act, path=L.PATH_TENSOR)

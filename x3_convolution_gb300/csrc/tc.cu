@@ -1064,6 +1064,189 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ----------------------------------------------------------------------------
+// wgrad, 8 input channels (the UNet stem)
+// ----------------------------------------------------------------------------
+// N = all nine taps x 8 channels at once: per 64-pixel k-block, x is staged as
+// nine im2col boxes of 64 pixels x 8 channels (1 KB each, no swizzle); in the
+// MN-major no-swizzle operand layout each box is one 8-column block of core
+// matrices (8 pixels x 16 bytes), blocks 1 KB apart.  A zero block pads N to
+// 80 and two blocks of ones add 16 dbias columns: one M = 128, N = 96, K = 16
+// MMA per 16 pixels covers dw and dbias.
+constexpr uint32_t kWc8BlockBytes = kWgPix * 16;               // 64 px x 8 channels
+constexpr uint32_t kWc8BBytes = 12 * kWc8BlockBytes;           // 9 taps, zero, 2 x ones
+constexpr uint32_t kWc8StageBytes = kWgABytes + kWc8BBytes;
+constexpr int kWc8Stages = 6;
+constexpr size_t kWc8Smem = (size_t)kWc8Stages * kWc8StageBytes + 256 + 1024;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_wgrad_c8(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmX,
+               const WgradParams p) {
+  constexpr int S = kWc8Stages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * kWc8StageBytes);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* drain = tfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mb = blockIdx.x % p.num_mb;
+  const int split = blockIdx.x / p.num_mb;
+  const int kb0 = split * p.kb_per_split;
+  const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+  const int HW = p.H * p.W;
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], kProd);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmDY);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+  }
+  if (warp >= kEpiBase) {  // per stage: block 9 = zeros, blocks 10-11 = bf16 ones
+    const int t = threadIdx.x - 32 * kEpiBase;
+    for (int st = 0; st < S; ++st) {
+      uint4* b = reinterpret_cast<uint4*>(smem + (size_t)st * kWc8StageBytes + kWgABytes + 9 * kWc8BlockBytes);
+      for (int i = t; i < (int)(3 * kWc8BlockBytes / 16); i += 32 * kWgEpiWarps) {
+        const uint32_t v = i < (int)(kWc8BlockBytes / 16) ? 0u : 0x3F803F80u;
+        b[i] = make_uint4(v, v, v, v);
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp < kProd) {
+    // eleven boxes per stage: dy halves 0-1 (8 KB), x taps 2-10 (1 KB)
+    if (lane == 0) {
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int pk = kb * kWgPix;
+        const int n0 = pk / HW, rem = pk - n0 * HW;
+        const int h0 = rem / p.W, w0 = rem - h0 * p.W;
+        uint8_t* sa = smem + (size_t)stage * kWc8StageBytes;
+        uint8_t* sb = sa + kWgABytes;
+        uint32_t bytes = 0;
+        for (int b = warp; b < 11; b += kProd) bytes += b < 2 ? 8192u : kWc8BlockBytes;
+        mbar_arrive_expect_tx(&full[stage], bytes);
+        for (int b = warp; b < 11; b += kProd) {
+          if (b < 2) {
+            tma_load_2d(sa + b * 8192, &tmDY, &full[stage], mb * 128 + b * 64, pk);
+          } else {
+            const int t = b - 2;
+            tma_load_im2col_4d(sb + t * kWc8BlockBytes, &tmX, &full[stage], 0, w0 - 1, h0 - 1, n0,
+                               (uint16_t)(t % 3), (uint16_t)(t / 3));
+          }
+        }
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) {
+        int n = issued < S ? issued : S;
+        for (int i = 0; i < n; ++i) {
+          if (--stage < 0) {
+            stage = S - 1;
+            phase ^= 1;
+          }
+          mbar_wait(&full[stage], phase, drain_wait_ns(p.wait_ns), nullptr, nullptr);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 96, 1, 1);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(smem + (size_t)stage * kWc8StageBytes);
+        const uint32_t b_base = a_base + kWgABytes;
+#pragma unroll
+        for (int k = 0; k < kWgPix / 16; ++k)
+          tc_mma_bf16(tmem_base, smem_desc(a_base + k * 2048, 8192, 1024, kSwizzle128B),
+                      smem_desc(b_base + k * 256, 128, kWc8BlockBytes, kSwizzleNone), idesc,
+                      (kb != kb0 || k != 0) ? 1u : 0u);
+        tc_commit(&empty[stage]);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (ok) tc_commit(tfull);
+      tc_commit(drain);
+      mbar_wait(drain, 0, p.wait_ns, nullptr, nullptr);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int k = mb * 128 + row;
+    if (mbar_wait(tfull, 0, p.wait_ns, p.status, abort_flag)) {
+      tc_fence_after();
+      const long long dwsize = (long long)p.Cout * 72;
+      const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+      float* o = p.part + (long long)split * dwsize + (long long)k * 72;
+#pragma unroll 1
+      for (int j = 0; j < 3; ++j) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(lane_addr + (uint32_t)(j * 32), v);
+        tmem_ld_wait();
+        if (k < p.Cout) {
+          if (j < 2) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              reinterpret_cast<float4*>(o + j * 32)[g] =
+                  make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                              __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
+          } else {
+            // columns 64..71 are the last dw values, column 80 the first ones column
+            reinterpret_cast<float4*>(o + 64)[0] = make_float4(
+                __uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]), __uint_as_float(v[3]));
+            reinterpret_cast<float4*>(o + 64)[1] = make_float4(
+                __uint_as_float(v[4]), __uint_as_float(v[5]), __uint_as_float(v[6]), __uint_as_float(v[7]));
+            p.part[(long long)p.S * dwsize + (long long)split * p.Cout + k] = __uint_as_float(v[16]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, 128);
+}
+
+// ----------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------
 int make_im2col_map(CUtensorMap* m, const void* base, int N, int H, int W, int C, int pixels,
@@ -1397,15 +1580,63 @@ int tc_dgrad(const void* dy, const void* w, void* dx, const Shape& s, int out_f3
   return run_igemm(true, dy, s.Cout, w, nullptr, dx, s, CONV3X3_ACT_NONE, out_f32, d, st);
 }
 
+// Cin == 8: one tile per 128 output channels; splits fill the GPU once.
+WgPlan wg_plan_c8(const Shape& s) {
+  WgPlan pl;
+  pl.num_mb = (s.Cout + 127) / 128;
+  pl.num_cb = 1;
+  pl.tiles = pl.num_mb;
+  pl.kb_total = (int)((s.P() + kWgPix - 1) / kWgPix);
+  int S = kPlanSms / pl.tiles;
+  if (S < 1) S = 1;
+  if (S > pl.kb_total) S = pl.kb_total;
+  pl.kb_per_split = (pl.kb_total + S - 1) / S;
+  pl.S = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
+  return pl;
+}
+
 size_t tc_wgrad_workspace(const Shape& s, int /*num_sms*/) {
+  if (s.Cin == 8) {
+    WgPlan pl = wg_plan_c8(s);
+    return (size_t)pl.S * (size_t)((long long)s.Cout * 72 + s.Cout) * sizeof(float);
+  }
   WgPlan pl = wg_plan(s);
   long long dwsize = (long long)s.Cout * 9 * s.Cin;
   return (size_t)pl.S * (size_t)(dwsize + s.Cout) * sizeof(float);
 }
 
+int run_wgrad_c8(const void* x, const void* dy, float* dw, float* db, const Shape& s, void* ws,
+                 const DevCtx& d, cudaStream_t st) {
+  WgPlan pl = wg_plan_c8(s);
+  CUtensorMap tdy, tx;
+  int rc = make_rows_map(&tdy, dy, s.P(), s.Cout);
+  if (rc) return rc;
+  rc = make_im2col_map(&tx, x, s.N, s.H, s.W, 8, kWgPix, 8, false);
+  if (rc) return rc;
+  WgradParams prm;
+  prm.part = static_cast<float*>(ws);
+  prm.P = (int)s.P();
+  prm.H = s.H;
+  prm.W = s.W;
+  prm.Cin = s.Cin;
+  prm.Cout = s.Cout;
+  prm.kb_total = pl.kb_total;
+  prm.kb_per_split = pl.kb_per_split;
+  prm.S = pl.S;
+  prm.num_mb = pl.num_mb;
+  prm.num_cb = 1;
+  prm.status = d.status;
+  prm.wait_ns = d.wait_ns;
+  if (set_smem(k_wgrad_c8, kWc8Smem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+  k_wgrad_c8<<<pl.tiles * pl.S, kThreads, kWc8Smem, st>>>(tdy, tx, prm);
+  if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
+  return launch_wgrad_reduce(prm.part, dw, db, (long long)s.Cout * 72, s.Cout, pl.S, pl.S, st);
+}
+
 int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s, void* ws,
              size_t ws_bytes, const DevCtx& d, cudaStream_t st) {
   if (ws == nullptr || ws_bytes < tc_wgrad_workspace(s, d.num_sms)) return CONV3X3_ERR_WORKSPACE;
+  if (s.Cin == 8) return run_wgrad_c8(x, dy, dw, db, s, ws, d, st);
   WgPlan pl = wg_plan(s);
   CUtensorMap tdy, tx;
   int rc = make_rows_map(&tdy, dy, s.P(), s.Cout);
