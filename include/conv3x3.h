@@ -11,7 +11,8 @@
  * padding 1, dilation 1, groups 1:
  *
  *   fwd    z[n,h,w,k]  = bias[k] + sum_{r,s,c} x[n,h+r-1,w+s-1,c] * w[k,r,s,c]
- *          y = z (act NONE) or y = z * sigmoid(z) (act SILU)
+ *          y = z (act NONE), z * sigmoid(z) (act SILU) or
+ *          max(z, 0.2 z) (act LRELU)
  *   dgrad  dx[n,h,w,c] = sum_{r,s,k} dy[n,h+1-r,w+1-s,k] * w[k,r,s,c]
  *   wgrad  dw[k,r,s,c] = sum_{n,h,w} dy[n,h,w,k] * x[n,h+r-1,w+s-1,c]
  *          dbias[k]    = sum_{n,h,w} dy[n,h,w,k]
@@ -41,7 +42,7 @@
  *   - N, H, W >= 1; Cin, Cout >= 8 and multiples of 8;
  *   - every pointer non-NULL (bias / dbias may be NULL) and 16-byte aligned;
  *   - N*H*W*max(Cin,Cout) < 2^31 elements per activation tensor, H, W <= 65535;
- *   - act in {NONE, SILU}; out_dtype in {BF16, F32}; path in {AUTO, TENSOR, SIMT}.
+ *   - act in {NONE, SILU, LRELU}; out_dtype in {BF16, F32}; path in {AUTO, TENSOR, SIMT}.
  * A launch failure returns CONV3X3_ERR_CUDA.  Kernels that wait on the
  * hardware (mbarrier / TMA / tensor-core completion) give up after a bounded
  * time, record CONV3X3_ERR_TIMEOUT in the device status word and exit cleanly;
@@ -71,7 +72,12 @@ typedef enum {
   CONV3X3_ERR_WORKSPACE = 5    /* wgrad workspace missing or too small       */
 } conv3x3_status;
 
-enum { CONV3X3_ACT_NONE = 0, CONV3X3_ACT_SILU = 1 };
+/* Epilogue activations: none; SiLU z*sigmoid(z); leaky ReLU, z for z >= 0 and
+ * 0.2 z below.  The last is the bias + leaky ReLU fused op of the StyleGAN2
+ * custom-kernel blog (page titled "Dim3 grid calculation code", opening
+ * paragraphs on the two custom kernels).  That page gives no slope and no gain:
+ * the slope is taken as 0.2 and no output gain is applied. */
+enum { CONV3X3_ACT_NONE = 0, CONV3X3_ACT_SILU = 1, CONV3X3_ACT_LRELU = 2 };
 enum { CONV3X3_DT_BF16 = 0, CONV3X3_DT_F32 = 1 };
 /* Kernel family: AUTO picks per shape; TENSOR = TMA-im2col + tcgen05/TMEM
  * implicit GEMM; SIMT = CUDA-core fp32-FMA kernels with 128-bit loads. */

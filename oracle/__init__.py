@@ -50,6 +50,8 @@ def _load():
         lib.oracle_get_threads.restype = ctypes.c_int
         lib.oracle_silu_f64.argtypes = [ctypes.c_double]
         lib.oracle_silu_f64.restype = ctypes.c_double
+        lib.oracle_lrelu_f64.argtypes = [ctypes.c_double]
+        lib.oracle_lrelu_f64.restype = ctypes.c_double
         lib.oracle_conv3x3_fwd_f64.argtypes = [_dp, _dp, _dp, _dp] + [_i64] * 5 + [ctypes.c_int]
         lib.oracle_conv3x3_fwd_at_f64.argtypes = [_dp, _dp, _dp] + [_i64] * 5 + [ctypes.c_int, _lp, _i64, _dp]
         lib.oracle_conv3x3_dgrad_f64.argtypes = [_dp, _dp, _dp] + [_i64] * 5
@@ -85,8 +87,13 @@ def silu(z: float) -> float:
     return float(_load().oracle_silu_f64(float(z)))
 
 
+def lrelu(z: float) -> float:
+    return float(_load().oracle_lrelu_f64(float(z)))
+
+
 def conv3x3_fwd(x, w, bias=None, act: int = 0):
-    """y[n,h,w,k] = act(b[k] + sum_{r,s,c} x[n,h+r-1,w+s-1,c] w[k,r,s,c]); x NHWC, w KRSC."""
+    """y[n,h,w,k] = act(b[k] + sum_{r,s,c} x[n,h+r-1,w+s-1,c] w[k,r,s,c]); x NHWC, w KRSC.
+    act: 0 none, 1 SiLU, 2 leaky ReLU (slope 0.2)."""
     x = _d(x)
     N, H, W, Cin = x.shape
     w = _d(w)

@@ -16,6 +16,12 @@
  *   forward  z[n,h,w,k] = b[k] + sum_{r,s,c} x[n,h+r-1,w+s-1,c] * wt[k,r,s,c]
  *            y = z                         (act = 0)
  *            y = z * sigmoid(z)            (act = 1, SiLU)
+ *            y = z >= 0 ? z : 0.2 z        (act = 2, bias + leaky ReLU: the fused
+ *                                           bias + activation op of the StyleGAN2
+ *                                           custom-kernel blog, page titled "Dim3
+ *                                           grid calculation code", opening
+ *                                           paragraphs; it gives no slope or
+ *                                           gain, so slope 0.2 and no gain)
  *   dgrad   dx[n,h,w,c] = sum_{r,s,k} dz[n,h+1-r,w+1-s,k] * wt[k,r,s,c]
  *   wgrad   dw[k,r,s,c] = sum_{n,h,w} dz[n,h,w,k] * x[n,h+r-1,w+s-1,c]
  *   dbias   db[k]       = sum_{n,h,w} dz[n,h,w,k]
@@ -98,6 +104,15 @@ typedef struct {
  * overflows to +inf and the quotient is -0, the correct limit. */
 double oracle_silu_f64(double z) { return z / (1.0 + exp(-z)); }
 
+/* leaky ReLU with negative slope 0.2 */
+double oracle_lrelu_f64(double z) { return z >= 0.0 ? z : 0.2 * z; }
+
+static double apply_act(int act, double z) {
+  if (act == 1) return oracle_silu_f64(z);
+  if (act == 2) return oracle_lrelu_f64(z);
+  return z;
+}
+
 /* ---------------- forward ---------------- */
 static double fwd_point(const job_t* j, int64_t n, int64_t h, int64_t w, int64_t k) {
   double acc = j->bias ? j->bias[k] : 0.0;
@@ -112,7 +127,7 @@ static double fwd_point(const job_t* j, int64_t n, int64_t h, int64_t w, int64_t
       for (int64_t c = 0; c < j->Cin; ++c) acc += xp[c] * wp[c];
     }
   }
-  return j->act == 1 ? oracle_silu_f64(acc) : acc;
+  return apply_act(j->act, acc);
 }
 
 static void fwd_row(void* ctx, int64_t nh) { /* one (n, h) output row */

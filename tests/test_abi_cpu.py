@@ -76,6 +76,8 @@ def test_bad_pointers_and_enums_are_rejected_without_a_gpu(lib):
     assert lib.conv3x3_fwd(None, ALIGNED, None, ALIGNED, *a, 0, None) == 1
     assert lib.conv3x3_fwd(ALIGNED + 2, ALIGNED, None, ALIGNED, *a, 0, None) == 1  # misaligned
     assert lib.conv3x3_fwd(ALIGNED, ALIGNED, None, ALIGNED, *a, 7, None) == 1      # bad act
+    assert lib.conv3x3_fwd(ALIGNED, ALIGNED, None, ALIGNED, *a, 3, None) == 1      # one past LRELU
+    assert lib.conv3x3_fwd(ALIGNED, ALIGNED, None, ALIGNED, *a, -1, None) == 1     # negative act
     assert lib.conv3x3_fwd_ex(ALIGNED, ALIGNED, None, ALIGNED, *a, 0, 5, 0, None) == 1  # dtype
     assert lib.conv3x3_fwd_ex(ALIGNED, ALIGNED, None, ALIGNED, *a, 0, 0, 9, None) == 1  # path
     assert lib.conv3x3_dgrad(ALIGNED, None, ALIGNED, *a, None) == 1

@@ -101,6 +101,24 @@ def test_silu_epilogue_applies_after_bias():
     assert np.allclose(y, z * sig, rtol=1e-12, atol=1e-14)
 
 
+def test_leaky_relu_special_values_and_epilogue():
+    # slope 0.2 below zero, identity at and above zero (the bias + leaky ReLU op)
+    assert oracle.lrelu(0.0) == 0.0
+    assert oracle.lrelu(3.5) == 3.5
+    assert oracle.lrelu(-1.0) == -0.2
+    assert oracle.lrelu(-5.0) == -1.0
+    for z in np.linspace(-7, 7, 57):
+        assert oracle.lrelu(z) == pytest.approx(max(z, 0.2 * z), rel=1e-15, abs=0)
+    # applied after the bias: constant input, all-ones kernel, bias chosen so
+    # that the interior (9 taps) is positive and the corners (4 taps) negative
+    x = np.ones((1, 4, 4, 1))
+    w = np.ones((1, 3, 3, 1))
+    y = oracle.conv3x3_fwd(x, w, np.array([-5.0]), act=2)
+    assert y[0, 1, 1, 0] == 4.0        # 9 - 5
+    assert y[0, 0, 1, 0] == 1.0        # 6 - 5
+    assert y[0, 0, 0, 0] == -0.2       # 0.2 * (4 - 5)
+
+
 # ---------------------------------------------------------------------------
 # identities
 # ---------------------------------------------------------------------------
@@ -220,6 +238,9 @@ def test_torch_float64_conv2d_cross_check():
     ys = oracle.conv3x3_fwd(x, w, b, act=1)
     assert np.allclose(ys, torch.nn.functional.silu(z).detach().permute(0, 2, 3, 1).numpy(),
                        rtol=1e-12, atol=1e-13)
+    yl = oracle.conv3x3_fwd(x, w, b, act=2)
+    zl = torch.nn.functional.leaky_relu(z, negative_slope=0.2)
+    assert np.allclose(yl, zl.detach().permute(0, 2, 3, 1).numpy(), rtol=1e-12, atol=1e-13)
 
 
 def test_hand_computed_fixture():
@@ -304,6 +325,9 @@ MUTANTS = {
                                     "            int64_t ww = w - s + 1;\n            if (ww < 0 || ww >= j->W) continue;\n            const double* xp"),
     "dbias squares dz": ("db += d;", "db += d * d;"),
     "silu sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    "leaky relu slope": ("return z >= 0.0 ? z : 0.2 * z;", "return z >= 0.0 ? z : 0.02 * z;"),
+    "leaky relu on the wrong side": ("return z >= 0.0 ? z : 0.2 * z;", "return z >= 0.0 ? 0.2 * z : z;"),
+    "leaky relu not applied": ("if (act == 2) return oracle_lrelu_f64(z);", "if (act == 2) return z;"),
 }
 
 
@@ -331,6 +355,7 @@ def _suite():
         test_all_ones_kernel_on_constant_input_gives_9_6_4_pattern,
         test_one_by_one_special_case_is_a_gemm,
         test_silu_special_values_and_grid,
+        test_leaky_relu_special_values_and_epilogue,
         test_adjoint_identity_fwd_dgrad,
         test_bilinear_wgrad_identity_and_dbias,
         test_brute_force_im2col_all_three_passes,

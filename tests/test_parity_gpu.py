@@ -59,6 +59,8 @@ def test_tiny_fp32_check_path_full():
     assert rel_err(host(db), rdb) <= TOL_F32
     ys = ops.fwd_f32(x, w, b, act=L.ACT_SILU)
     assert rel_err(host(ys), oracle.conv3x3_fwd(t.x, t.w, t.bias, 1)) <= TOL_F32
+    yl = ops.fwd_f32(x, w, b, act=L.ACT_LRELU)
+    assert rel_err(host(yl), oracle.conv3x3_fwd(t.x, t.w, t.bias, 2)) <= TOL_F32
 
 
 def test_tiny_in_bf16_at_the_bf16_gate():
@@ -108,7 +110,7 @@ def test_small_shapes_all_passes(shape, path):
     p = PATHS[path]
     t = _small(shape)
     x, w, b, dy = dev_tensors(t)
-    for act in (0, 1):
+    for act in (0, 1, 2):
         y32 = ops.fwd(x, w, b, act=act, out_dtype=L.DT_F32, path=p)
         ybf = ops.fwd(x, w, b, act=act, out_dtype=L.DT_BF16, path=p)
         torch.cuda.synchronize()
@@ -170,6 +172,9 @@ def test_halo_tiles(shape, tile, monkeypatch):
     assert rel_err(host(y32), ref) <= TOL_BF16
     assert np.array_equal(host(ybf), rne_bf16(host(y32)))
     assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
+    yl = ops.fwd(x, w, b, act=L.ACT_LRELU, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert rel_err(host(yl), oracle.conv3x3_fwd(t.x, t.w, t.bias, 2)) <= TOL_BF16
 
 
 STEM_SHAPES = [
@@ -192,7 +197,7 @@ def test_eight_channel_kernels(shape):
     assert rel_err(host(dw), rdw) <= TOL_BF16
     assert rel_err(host(db), rdb) <= TOL_BF16
     assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
-    for act in (0, 1):
+    for act in (0, 1, 2):
         y32 = ops.fwd(x, w, b, act=act, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
         ybf = ops.fwd(x, w, b, act=act, path=L.PATH_TENSOR)
         torch.cuda.synchronize()

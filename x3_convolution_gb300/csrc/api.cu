@@ -165,7 +165,7 @@ int conv3x3_fwd_ex(const void* x, const void* w, const float* bias, void* y, int
   if (rc) return rc;
   if (!x || !w || !y || !aligned16(x) || !aligned16(w) || !aligned16(y)) return CONV3X3_ERR_INVALID_ARG;
   if (bias && !aligned16(bias)) return CONV3X3_ERR_INVALID_ARG;
-  if (act != CONV3X3_ACT_NONE && act != CONV3X3_ACT_SILU) return CONV3X3_ERR_INVALID_ARG;
+  if (act < CONV3X3_ACT_NONE || act > CONV3X3_ACT_LRELU) return CONV3X3_ERR_INVALID_ARG;
   if (out_dtype != CONV3X3_DT_BF16 && out_dtype != CONV3X3_DT_F32) return CONV3X3_ERR_INVALID_ARG;
   if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return CONV3X3_ERR_INVALID_ARG;
   Shape s{N, Cin, Cout, H, W};
@@ -252,7 +252,7 @@ int conv3x3_fwd_f32(const float* x, const float* w, const float* bias, float* y,
   if (rc) return rc;
   if (!x || !w || !y || !aligned4(x) || !aligned4(w) || !aligned4(y)) return CONV3X3_ERR_INVALID_ARG;
   if (bias && !aligned4(bias)) return CONV3X3_ERR_INVALID_ARG;
-  if (act != CONV3X3_ACT_NONE && act != CONV3X3_ACT_SILU) return CONV3X3_ERR_INVALID_ARG;
+  if (act < CONV3X3_ACT_NONE || act > CONV3X3_ACT_LRELU) return CONV3X3_ERR_INVALID_ARG;
   Shape s{N, Cin, Cout, H, W};
   return simt_fwd_f32(x, w, bias, y, s, act, as_stream(stream));
 }

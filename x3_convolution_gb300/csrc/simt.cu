@@ -46,7 +46,9 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 }
 
 __device__ __forceinline__ float act_f(float z, int act) {
-  return act == CONV3X3_ACT_SILU ? z / (1.0f + __expf(-z)) : z;
+  if (act == CONV3X3_ACT_SILU) return z / (1.0f + __expf(-z));
+  if (act == CONV3X3_ACT_LRELU) return z >= 0.0f ? z : 0.2f * z;
+  return z;
 }
 
 __device__ __forceinline__ void store8(void* out, long long off, const float (&f)[8], int out_f32) {

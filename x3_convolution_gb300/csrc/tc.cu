@@ -132,6 +132,9 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix,
   if (p.act == CONV3X3_ACT_SILU) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) f[i] = silu_f32(f[i]);
+  } else if (p.act == CONV3X3_ACT_LRELU) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = f[i] >= 0.0f ? f[i] : 0.2f * f[i];
   }
   if (p.out_f32) {
     float* o = static_cast<float*>(p.out) + pix * p.nout + col0;
