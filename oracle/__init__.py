@@ -1,4 +1,5 @@
-"""CPU oracle for the stride-1, pad-1 3x3 convolution (fwd, dgrad, wgrad, dbias).
+"""CPU oracle for the stride-1, pad-1 3x3 convolution (fwd, dgrad, dgrad through the
+input's activation, wgrad, dbias).
 
 TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()`` and
 the CPU-baseline leg of ``bench.py``; never by the product path.
@@ -54,7 +55,12 @@ def _load():
         lib.oracle_lrelu_f64.restype = ctypes.c_double
         lib.oracle_conv3x3_fwd_f64.argtypes = [_dp, _dp, _dp, _dp] + [_i64] * 5 + [ctypes.c_int]
         lib.oracle_conv3x3_fwd_at_f64.argtypes = [_dp, _dp, _dp] + [_i64] * 5 + [ctypes.c_int, _lp, _i64, _dp]
+        lib.oracle_act_grad_f64.argtypes = [ctypes.c_int, ctypes.c_double]
+        lib.oracle_act_grad_f64.restype = ctypes.c_double
         lib.oracle_conv3x3_dgrad_f64.argtypes = [_dp, _dp, _dp] + [_i64] * 5
+        lib.oracle_conv3x3_dgrad_act_f64.argtypes = [_dp, _dp, _dp, ctypes.c_int, _dp] + [_i64] * 5
+        lib.oracle_conv3x3_dgrad_act_at_f64.argtypes = ([_dp, _dp, _dp, ctypes.c_int] + [_i64] * 5
+                                                        + [_lp, _i64, _dp])
         lib.oracle_conv3x3_dgrad_at_f64.argtypes = [_dp, _dp] + [_i64] * 5 + [_lp, _i64, _dp]
         lib.oracle_conv3x3_wgrad_f64.argtypes = [_dp, _dp, _dp, _dp] + [_i64] * 5
         lib.oracle_conv3x3_wgrad_at_f64.argtypes = [_dp, _dp] + [_i64] * 5 + [_lp, _i64, _dp]
@@ -140,6 +146,39 @@ def conv3x3_dgrad_at(dz, w, idx):
     out = np.empty(idx.shape[0], np.float64)
     _load().oracle_conv3x3_dgrad_at_f64(_ptr(dz), _ptr(w), N, Cin, Cout, H, W,
                                         idx.ctypes.data_as(_lp), idx.shape[0], _ptr(out))
+    return out
+
+
+def act_grad(act: int, z: float) -> float:
+    """d act / dz at z (act 0 none, 1 SiLU, 2 leaky ReLU)."""
+    return float(_load().oracle_act_grad_f64(int(act), float(z)))
+
+
+def conv3x3_dgrad_act(dz, w, zin, act: int):
+    """Gradient with respect to zin when the convolution's input is act(zin):
+    act'(zin) * conv3x3_dgrad(dz, w); zin has the layout of the input [N,H,W,Cin]."""
+    dz = _d(dz)
+    N, H, W, Cout = dz.shape
+    w = _d(w)
+    Cin = w.shape[3]
+    assert w.shape == (Cout, 3, 3, Cin), w.shape
+    zin = _d(zin, (N, H, W, Cin))
+    dx = np.empty((N, H, W, Cin), np.float64)
+    _load().oracle_conv3x3_dgrad_act_f64(_ptr(dz), _ptr(w), _ptr(zin), int(act), _ptr(dx),
+                                         N, Cin, Cout, H, W)
+    return dx
+
+
+def conv3x3_dgrad_act_at(dz, w, zin, act: int, idx):
+    dz = _d(dz)
+    N, H, W, Cout = dz.shape
+    w = _d(w)
+    Cin = w.shape[3]
+    zin = _d(zin, (N, H, W, Cin))
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    out = np.empty(idx.shape[0], np.float64)
+    _load().oracle_conv3x3_dgrad_act_at_f64(_ptr(dz), _ptr(w), _ptr(zin), int(act), N, Cin, Cout,
+                                            H, W, idx.ctypes.data_as(_lp), idx.shape[0], _ptr(out))
     return out
 
 

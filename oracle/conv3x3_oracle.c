@@ -23,6 +23,8 @@
  *                                           paragraphs; it gives no slope or
  *                                           gain, so slope 0.2 and no gain)
  *   dgrad   dx[n,h,w,c] = sum_{r,s,k} dz[n,h+1-r,w+1-s,k] * wt[k,r,s,c]
+ *   dgrad through the input's activation, x = act(zin):
+ *           dzin[n,h,w,c] = act'(zin[n,h,w,c]) * dx[n,h,w,c]
  *   wgrad   dw[k,r,s,c] = sum_{n,h,w} dz[n,h,w,k] * x[n,h+r-1,w+s-1,c]
  *   dbias   db[k]       = sum_{n,h,w} dz[n,h,w,k]
  *
@@ -98,6 +100,7 @@ typedef struct {
   int64_t N, Cin, Cout, H, W;
   int act;
   const int64_t* idx;
+  const double* zin; /* dgrad through an activation: its pre-activation input */
 } job_t;
 
 /* SiLU(z) = z * sigmoid(z) = z / (1 + e^{-z}).  For very negative z, e^{-z}
@@ -111,6 +114,22 @@ static double apply_act(int act, double z) {
   if (act == 1) return oracle_silu_f64(z);
   if (act == 2) return oracle_lrelu_f64(z);
   return z;
+}
+
+/* Derivative of the activation at z.
+ *   SiLU:       d/dz [z s(z)] = s(z) + z s(z)(1 - s(z)) = s(z) (1 + z (1 - s(z))),
+ *               s the logistic sigmoid.
+ *   leaky ReLU: 1 for z > 0 and 0.2 otherwise; at z = 0 both one-sided
+ *               derivatives exist and the lower one is taken, as PyTorch's
+ *               leaky_relu backward does.
+ *   none:       1. */
+double oracle_act_grad_f64(int act, double z) {
+  if (act == 1) {
+    double sg = 1.0 / (1.0 + exp(-z));
+    return sg * (1.0 + z * (1.0 - sg));
+  }
+  if (act == 2) return z > 0.0 ? 1.0 : 0.2;
+  return 1.0;
 }
 
 /* ---------------- forward ---------------- */
@@ -204,6 +223,43 @@ void oracle_conv3x3_dgrad_at_f64(const double* dz, const double* wt,
                                  const int64_t* idx, int64_t count, double* out) {
   job_t j = {NULL, wt, NULL, dz, out, NULL, N, Cin, Cout, H, W, 0, idx};
   parallel_for(count, dgrad_at_item, &j);
+}
+
+/* ---------------- dgrad through the previous layer's activation ----------------
+ * When this convolution's input is x = act(zin), the chain rule gives the
+ * gradient with respect to zin as
+ *   dzin[n,h,w,c] = act'(zin[n,h,w,c]) * dx[n,h,w,c],
+ * dx the plain dgrad above; zin has the layout of dx. */
+static void dgrad_act_row(void* ctx, int64_t nh) {
+  const job_t* j = (const job_t*)ctx;
+  int64_t n = nh / j->H, h = nh % j->H;
+  for (int64_t w = 0; w < j->W; ++w)
+    for (int64_t c = 0; c < j->Cin; ++c) {
+      int64_t e = ((n * j->H + h) * j->W + w) * j->Cin + c;
+      j->out[e] = oracle_act_grad_f64(j->act, j->zin[e]) * dgrad_point(j, n, h, w, c);
+    }
+}
+
+void oracle_conv3x3_dgrad_act_f64(const double* dz, const double* wt, const double* zin, int act,
+                                  double* dx, int64_t N, int64_t Cin, int64_t Cout, int64_t H,
+                                  int64_t W) {
+  job_t j = {NULL, wt, NULL, dz, dx, NULL, N, Cin, Cout, H, W, act, NULL, zin};
+  parallel_for(N * H, dgrad_act_row, &j);
+}
+
+static void dgrad_act_at_item(void* ctx, int64_t i) {
+  const job_t* j = (const job_t*)ctx;
+  int64_t e = j->idx[i];
+  int64_t c = e % j->Cin, p = e / j->Cin;
+  int64_t w = p % j->W, h = (p / j->W) % j->H, n = p / (j->W * j->H);
+  j->out[i] = oracle_act_grad_f64(j->act, j->zin[e]) * dgrad_point(j, n, h, w, c);
+}
+
+void oracle_conv3x3_dgrad_act_at_f64(const double* dz, const double* wt, const double* zin, int act,
+                                     int64_t N, int64_t Cin, int64_t Cout, int64_t H, int64_t W,
+                                     const int64_t* idx, int64_t count, double* out) {
+  job_t j = {NULL, wt, NULL, dz, out, NULL, N, Cin, Cout, H, W, act, idx, zin};
+  parallel_for(count, dgrad_act_at_item, &j);
 }
 
 /* ---------------- wgrad + dbias ---------------- */

@@ -119,6 +119,80 @@ def test_leaky_relu_special_values_and_epilogue():
     assert y[0, 0, 0, 0] == -0.2       # 0.2 * (4 - 5)
 
 
+def test_act_grad_closed_forms_and_finite_differences():
+    # SiLU'(0) = 1/2; SiLU' -> 1 above and -> 0 below; leaky ReLU' = 1 or 0.2
+    assert oracle.act_grad(1, 0.0) == 0.5
+    assert oracle.act_grad(1, 50.0) == pytest.approx(1.0, abs=1e-15)
+    assert abs(oracle.act_grad(1, -50.0)) < 1e-18
+    assert oracle.act_grad(2, 3.0) == 1.0
+    assert oracle.act_grad(2, -3.0) == 0.2
+    assert oracle.act_grad(2, 0.0) == 0.2     # the lower one-sided derivative at the kink
+    assert oracle.act_grad(0, -7.0) == 1.0
+    # central differences of the (separately pinned) activations themselves
+    h = 1e-5
+    for z in np.linspace(-9, 9, 73):
+        fd = (oracle.silu(z + h) - oracle.silu(z - h)) / (2 * h)
+        assert oracle.act_grad(1, z) == pytest.approx(fd, rel=1e-8, abs=1e-10)
+        if abs(z) > 1e-3:
+            fd = (oracle.lrelu(z + h) - oracle.lrelu(z - h)) / (2 * h)
+            assert oracle.act_grad(2, z) == pytest.approx(fd, rel=1e-9)
+    # SiLU' has one minimum, at the root of its derivative z ~ -2.3994, value ~ -0.0998
+    zs = np.linspace(-4, -1, 3001)
+    g = np.array([oracle.act_grad(1, z) for z in zs])
+    assert zs[np.argmin(g)] == pytest.approx(-2.3994, abs=2e-3)
+    assert g.min() == pytest.approx(-0.09984, abs=2e-5)
+
+
+def _act_elementwise(act, z):
+    f = {0: float, 1: oracle.silu, 2: oracle.lrelu}[act]
+    return np.vectorize(f)(z)
+
+
+@pytest.mark.parametrize("act", [1, 2])
+def test_dgrad_through_activation_by_finite_differences(act):
+    # F(zin) = <v, conv3x3(act(zin), w)>; dF/dzin must equal dgrad_act(v, w, zin)
+    N, H, W, Cin, Cout = 1, 3, 4, 2, 3
+    zin = rand(N, H, W, Cin)
+    w = rand(Cout, 3, 3, Cin)
+    v = rand(N, H, W, Cout)
+    g = oracle.conv3x3_dgrad_act(v, w, zin, act)
+
+    def F(zz):
+        return float(np.sum(v * oracle.conv3x3_fwd(_act_elementwise(act, zz), w)))
+
+    h = 1e-6
+    for e in range(zin.size):
+        zp = zin.copy().reshape(-1)
+        zm = zin.copy().reshape(-1)
+        zp[e] += h
+        zm[e] -= h
+        fd = (F(zp.reshape(zin.shape)) - F(zm.reshape(zin.shape))) / (2 * h)
+        assert g.reshape(-1)[e] == pytest.approx(fd, rel=1e-6, abs=1e-8), e
+
+
+def test_dgrad_through_no_activation_is_plain_dgrad():
+    dz = rand(2, 5, 4, 3)
+    w = rand(3, 3, 3, 6)
+    zin = rand(2, 5, 4, 6)
+    assert np.array_equal(oracle.conv3x3_dgrad_act(dz, w, zin, 0), oracle.conv3x3_dgrad(dz, w))
+
+
+def test_dgrad_through_activation_by_torch_autograd():
+    torch = pytest.importorskip("torch")
+    N, H, W, Cin, Cout = 2, 5, 6, 4, 3
+    zin = rand(N, H, W, Cin)
+    w = rand(Cout, 3, 3, Cin)
+    dz = rand(N, H, W, Cout)
+    for act, fn in ((1, torch.nn.functional.silu),
+                    (2, lambda t: torch.nn.functional.leaky_relu(t, negative_slope=0.2))):
+        zt = torch.tensor(zin).permute(0, 3, 1, 2).contiguous().requires_grad_(True)
+        wt = torch.tensor(w).permute(0, 3, 1, 2).contiguous()
+        y = torch.nn.functional.conv2d(fn(zt), wt, stride=1, padding=1)
+        y.backward(torch.tensor(dz).permute(0, 3, 1, 2))
+        assert np.allclose(oracle.conv3x3_dgrad_act(dz, w, zin, act),
+                           zt.grad.permute(0, 2, 3, 1).numpy(), rtol=1e-12, atol=1e-13)
+
+
 # ---------------------------------------------------------------------------
 # identities
 # ---------------------------------------------------------------------------
@@ -328,6 +402,10 @@ MUTANTS = {
     "leaky relu slope": ("return z >= 0.0 ? z : 0.2 * z;", "return z >= 0.0 ? z : 0.02 * z;"),
     "leaky relu on the wrong side": ("return z >= 0.0 ? z : 0.2 * z;", "return z >= 0.0 ? 0.2 * z : z;"),
     "leaky relu not applied": ("if (act == 2) return oracle_lrelu_f64(z);", "if (act == 2) return z;"),
+    "silu grad without the (1 - s) factor": ("return sg * (1.0 + z * (1.0 - sg));", "return sg * (1.0 + z);"),
+    "leaky relu grad slope": ("return z > 0.0 ? 1.0 : 0.2;", "return z > 0.0 ? 1.0 : 0.02;"),
+    "dgrad_act reads zin of channel 0": ("j->out[e] = oracle_act_grad_f64(j->act, j->zin[e]) * dgrad_point(j, n, h, w, c);",
+                                         "j->out[e] = oracle_act_grad_f64(j->act, j->zin[e - c]) * dgrad_point(j, n, h, w, c);"),
 }
 
 
@@ -356,6 +434,9 @@ def _suite():
         test_one_by_one_special_case_is_a_gemm,
         test_silu_special_values_and_grid,
         test_leaky_relu_special_values_and_epilogue,
+        test_act_grad_closed_forms_and_finite_differences,
+        (lambda: test_dgrad_through_activation_by_finite_differences(1)),
+        (lambda: test_dgrad_through_activation_by_finite_differences(2)),
         test_adjoint_identity_fwd_dgrad,
         test_bilinear_wgrad_identity_and_dbias,
         test_brute_force_im2col_all_three_passes,
