@@ -10,6 +10,12 @@ Default workload "unet": the stem conv (3 -> 128 channels, zero-padded to 8,
 multipliers 1,2,3,4, two resblocks per level on the down and up paths, up-path
 inputs = concat of skip and main), batch 64, bf16 NHWC, seeded synthetic inputs.
 
+--fused-act runs the training step with the activation's backward fused into
+the convolutions: each forward also stores its pre-activation z
+(conv3x3_fwd_save_z) and each dgrad takes the pre-activation of the layer that
+produced its input and returns the gradient through that activation
+(conv3x3_dgrad_act), so no elementwise pass runs between the convolutions.
+
 Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
 launching stream; L2 is flushed (a write of 2x the L2 size) between steps,
 outside the events.  Multi-process runs (torchrun) run one replica per GPU
@@ -173,9 +179,10 @@ def max_over_ranks(value: float, ws: int, device=None) -> float:
 # the CUDA arm
 # ---------------------------------------------------------------------------
 class Workload:
-    def __init__(self, layers, seed, device, keep_host=True):
+    def __init__(self, layers, seed, device, keep_host=True, fused_act=False):
         import torch
         self.layers = layers
+        self.fused_act = fused_act
         self.dev = []
         self.host = []
         ws_max = 0
@@ -194,18 +201,33 @@ class Workload:
                 "dw": torch.empty((L.Cout, 3, 3, L.Cin), dtype=torch.float32, device=device),
                 "db": torch.empty((L.Cout,), dtype=torch.float32, device=device),
             }
+            if fused_act:
+                # z: this layer's pre-activation (written by the forward);
+                # zin: the pre-activation of the layer that produced x (none for
+                # the stem, whose input is the image)
+                d["z"] = torch.empty((L.N, L.H, L.W, L.Cout), dtype=torch.bfloat16, device=device)
+                d["act_in"] = L.act if i > 0 else 0
+                hz = torch.from_numpy(synth.bf16_bits(synth.make_zin(L, seed=seed, index=i))
+                                      .view(np.int16)).view(torch.bfloat16)
+                d["zin"] = hz.to(device)
             self.dev.append(d)
             if keep_host:
-                self.host.append({"x": hx.pin_memory(), "w": hw.pin_memory(), "b": hb.pin_memory(),
-                                  "dy": hdy.pin_memory(),
-                                  "dw": torch.empty((L.Cout, 3, 3, L.Cin), dtype=torch.float32).pin_memory(),
-                                  "db": torch.empty((L.Cout,), dtype=torch.float32).pin_memory()})
+                h = {"x": hx.pin_memory(), "w": hw.pin_memory(), "b": hb.pin_memory(),
+                     "dy": hdy.pin_memory(),
+                     "dw": torch.empty((L.Cout, 3, 3, L.Cin), dtype=torch.float32).pin_memory(),
+                     "db": torch.empty((L.Cout,), dtype=torch.float32).pin_memory()}
+                if fused_act:
+                    h["zin"] = hz.pin_memory()
+                self.host.append(h)
             ws_max = max(ws_max, Lb.conv3x3_wgrad_workspace_bytes(L.N, L.Cin, L.Cout, L.H, L.W))
         self.ws_bytes = ws_max
         self.ws = torch.empty(max(ws_max, 256), dtype=torch.uint8, device=device)
 
+    def inputs(self):
+        return ("x", "w", "b", "dy", "zin") if self.fused_act else ("x", "w", "b", "dy")
+
     def h2d_bytes(self):
-        return sum(h[k].numel() * h[k].element_size() for h in self.host for k in ("x", "w", "b", "dy"))
+        return sum(h[k].numel() * h[k].element_size() for h in self.host for k in self.inputs())
 
     def d2h_bytes(self):
         return sum(h[k].numel() * h[k].element_size() for h in self.host for k in ("dw", "db"))
@@ -219,8 +241,12 @@ def run_step(wl: Workload, stream_handle: int, ev=None, record=None):
         d = wl.dev[i]
         if record is not None:
             record("fwd", i, 0)
-        Lb.conv3x3_fwd(d["x"], d["w"], d["b"], d["y"], L.N, L.Cin, L.Cout, L.H, L.W, L.act,
-                       stream_handle)
+        if wl.fused_act:
+            Lb.conv3x3_fwd_save_z(d["x"], d["w"], d["b"], d["y"], d["z"], L.N, L.Cin, L.Cout, L.H,
+                                  L.W, L.act, Lb.DT_BF16, Lb.PATH_AUTO, stream_handle)
+        else:
+            Lb.conv3x3_fwd(d["x"], d["w"], d["b"], d["y"], L.N, L.Cin, L.Cout, L.H, L.W, L.act,
+                           stream_handle)
         if record is not None:
             record("fwd", i, 1)
         n += 1
@@ -229,7 +255,11 @@ def run_step(wl: Workload, stream_handle: int, ev=None, record=None):
         d = wl.dev[i]
         if record is not None:
             record("dgrad", i, 0)
-        Lb.conv3x3_dgrad(d["dy"], d["w"], d["dx"], L.N, L.Cin, L.Cout, L.H, L.W, stream_handle)
+        if wl.fused_act:
+            Lb.conv3x3_dgrad_act(d["dy"], d["w"], d["zin"], d["act_in"], d["dx"], L.N, L.Cin,
+                                 L.Cout, L.H, L.W, Lb.DT_BF16, Lb.PATH_AUTO, stream_handle)
+        else:
+            Lb.conv3x3_dgrad(d["dy"], d["w"], d["dx"], L.N, L.Cin, L.Cout, L.H, L.W, stream_handle)
         if record is not None:
             record("dgrad", i, 1)
             record("wgrad", i, 0)
@@ -256,7 +286,7 @@ def cuda_arm(args):
 
     layers = synth.CONFIGS[args.workload]
     peaks = load_peaks()
-    wl = Workload(layers, args.seed, device, keep_host=not args.no_e2e)
+    wl = Workload(layers, args.seed, device, keep_host=not args.no_e2e, fused_act=args.fused_act)
     stream = torch.cuda.Stream(device=device)
     sh = stream.cuda_stream
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -351,7 +381,7 @@ def cuda_arm(args):
         def e2e_step():
             with torch.cuda.stream(stream):
                 for h, d in zip(wl.host, wl.dev):
-                    for k in ("x", "w", "b", "dy"):
+                    for k in wl.inputs():
                         d[k].copy_(h[k], non_blocking=True)
                 run_step(wl, sh)
                 for h, d in zip(wl.host, wl.dev):
@@ -389,7 +419,8 @@ def cuda_arm(args):
         "config": {"workload": args.workload, "layers": len(layers), "batch": layers[0].N,
                    "layout": "NHWC bf16 activations, KRSC bf16 weights, fp32 accumulate",
                    "l2": "flushed between steps (write of 2x L2)",
-                   "flops_per_step": flops_step, "flops_per_step_padded_cin": flops_padded},
+                   "flops_per_step": flops_step, "flops_per_step_padded_cin": flops_padded,
+                   "fused_act_backward": bool(args.fused_act)},
         "pct_of_roofline": round(roof_s / (ms * 1e-3), 4),
         "roofline": {"bound": "tensor", "kernel": {"fwd": "k_igemm (fwd)", "dgrad": "k_igemm (dgrad)",
                                                    "wgrad": "k_wgrad + k_wgrad_reduce"}[dom],
@@ -485,6 +516,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--detail", action="store_true", help="add a per-layer breakdown")
+    ap.add_argument("--fused-act", action="store_true",
+                    help="training-step variant: forwards also store z, dgrads take the input's "
+                         "pre-activation and return the gradient through its activation")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -124,6 +124,33 @@ int conv3x3_wgrad_ex(const void* x, const void* dy, float* dw, float* dbias,
                      void* workspace, size_t workspace_bytes, int path, void* stream);
 size_t conv3x3_wgrad_workspace_bytes_ex(int N, int Cin, int Cout, int H, int W, int path);
 
+/* Backward through a layer's activation, fused into the convolutions' own
+ * epilogues.  The subject page (clu0's C++/CUDA UNet diffusion, sourcepulse.org
+ * project page, "How It Works") puts the emphasis on minimising memory
+ * transfers; these two calls remove the elementwise pass dz = dy * act'(z)
+ * that a training step otherwise runs between the convolutions.
+ *
+ * conv3x3_fwd_save_z: conv3x3_fwd_ex, and also stores the pre-activation
+ *   z = conv + bias, rounded once to bf16, in z [N][H][W][Cout] (16-byte
+ *   aligned; it must not overlap y).  y = act(z) is computed from the fp32 z,
+ *   exactly as conv3x3_fwd_ex computes it.
+ * conv3x3_dgrad_act: the input gradient of a convolution whose input was
+ *   x = act_in(z_in):  dx = act_in'(z_in) * dgrad(dy, w), the product taken in
+ *   fp32 on the accumulator and rounded once.  z_in [N][H][W][Cin] bf16,
+ *   16-byte aligned, must not overlap dx.  act_in' is SiLU' = s (1 + z (1 - s))
+ *   with s the logistic sigmoid, or leaky ReLU' = 1 for z > 0 and 0.2 for
+ *   z <= 0; act_in = CONV3X3_ACT_NONE is plain dgrad and z_in is ignored (may be
+ *   NULL).  The result is the gradient with respect to z_in: it feeds the
+ *   previous layer's conv3x3_wgrad and conv3x3_dgrad_act directly.
+ * Errors as conv3x3_fwd_ex / conv3x3_dgrad_ex, and CONV3X3_ERR_INVALID_ARG for
+ * a missing, misaligned or overlapping z / z_in or an unknown act_in. */
+int conv3x3_fwd_save_z(const void* x, const void* w, const float* bias, void* y, void* z,
+                       int N, int Cin, int Cout, int H, int W, int act,
+                       int out_dtype, int path, void* stream);
+int conv3x3_dgrad_act(const void* dy, const void* w, const void* z_in, int act_in, void* dx,
+                      int N, int Cin, int Cout, int H, int W,
+                      int out_dtype, int path, void* stream);
+
 /* fp32 check path: every tensor fp32 (same layouts), fp32 FMA on CUDA cores,
  * never TF32.  Any Cin, Cout >= 1; pointers 4-byte aligned.  wgrad needs no
  * workspace (pass NULL, 0). */

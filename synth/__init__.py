@@ -10,7 +10,9 @@ page trains (clu0's C++/CUDA UNet diffusion, sourcepulse.org project page,
 "Quick Start & Requirements": ImageNet 64x64 data); no dataset or trained
 weight is used anywhere.
 
-Stream ids: (seed << 32) | (layer << 8) | tensor, tensor = 0 x, 1 w, 2 bias, 3 dy.
+Stream ids: (seed << 32) | (layer << 8) | tensor, tensor = 0 x, 1 w, 2 bias, 3 dy,
+4 z_in (the pre-activation of the layer that produced x, for the fused backward
+through that activation; N(0, 1), laid out like x).
 Distributions: x, dy ~ N(0, 1); w ~ N(0, 2 / (9 * Cin_real)) (Kaiming normal with
 the real fan-in); bias ~ N(0, 0.02^2).  bf16 workloads round each float32 sample
 to bf16 round-to-nearest-even; the stem's three image channels are zero-padded to
@@ -31,7 +33,7 @@ _SRC = os.path.join(_HERE, "synth.c")
 _LIB = os.path.join(_HERE, "libsynth.so")
 _lib = None
 
-X, WT, BIAS, DY = 0, 1, 2, 3
+X, WT, BIAS, DY, ZIN = 0, 1, 2, 3, 4
 
 
 def build(force: bool = False) -> str:
@@ -133,6 +135,14 @@ def make_tensors(layer: Layer, seed: int = 0, index: int = 0, round_bf16: bool |
     if rb:
         x, w, dy = bf16_round(x), bf16_round(w), bf16_round(dy)
     return Tensors(x=x, w=w, bias=b, dy=dy, layer=L)
+
+
+def make_zin(layer: Layer, seed: int = 0, index: int = 0, round_bf16: bool | None = None) -> np.ndarray:
+    """Seeded z_in [N, H, W, Cin] ~ N(0, 1): the input's pre-activation."""
+    L = layer
+    rb = (L.dtype == "bf16") if round_bf16 is None else round_bf16
+    z = normal(stream_id(seed, index, ZIN), (L.N, L.H, L.W, L.Cin), 1.0)
+    return bf16_round(z) if rb else z
 
 
 # ---------------------------------------------------------------------------

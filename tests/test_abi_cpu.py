@@ -91,6 +91,31 @@ def test_bad_pointers_and_enums_are_rejected_without_a_gpu(lib):
     assert lib.conv3x3_fwd_f32(None, ALIGNED, None, ALIGNED, *a, 0, None) == 1
 
 
+def test_fused_activation_entry_points_validate_without_a_gpu(lib):
+    N, Cin, Cout, H, W = a = (2, 64, 64, 8, 8)
+    far = ALIGNED + (1 << 24)            # a second fake buffer that overlaps nothing
+    zb = N * H * W * Cout * 2            # bytes of z (bf16)
+    # forward that also stores z: z missing, misaligned, overlapping y (either side)
+    assert lib.conv3x3_fwd_save_z(ALIGNED, ALIGNED, None, far, None, *a, 1, 0, 0, None) == 1
+    assert lib.conv3x3_fwd_save_z(ALIGNED, ALIGNED, None, far, far + (1 << 22) + 8, *a, 1, 0, 0,
+                                  None) == 1
+    assert lib.conv3x3_fwd_save_z(ALIGNED, ALIGNED, None, far, far + zb - 16, *a, 1, 0, 0,
+                                  None) == 1
+    assert lib.conv3x3_fwd_save_z(ALIGNED, ALIGNED, None, far + 4096, far, *a, 1, 0, 0, None) == 1
+    # fp32 y is twice as long: z placed right after a bf16-sized y still overlaps it
+    assert lib.conv3x3_fwd_save_z(ALIGNED, ALIGNED, None, far, far + zb, *a, 1, 1, 0, None) == 1
+    # dgrad through an activation: unknown act_in, z_in missing / misaligned / overlapping dx
+    assert lib.conv3x3_dgrad_act(ALIGNED, ALIGNED, far, 3, ALIGNED, *a, 0, 0, None) == 1
+    assert lib.conv3x3_dgrad_act(ALIGNED, ALIGNED, far, -1, ALIGNED, *a, 0, 0, None) == 1
+    assert lib.conv3x3_dgrad_act(ALIGNED, ALIGNED, None, 1, ALIGNED, *a, 0, 0, None) == 1
+    assert lib.conv3x3_dgrad_act(ALIGNED, ALIGNED, far + 8, 2, ALIGNED, *a, 0, 0, None) == 1
+    assert lib.conv3x3_dgrad_act(ALIGNED, ALIGNED, far, 1, far + 256, *a, 0, 0, None) == 1
+    # bad shape and bad dgrad arguments still come back as invalid
+    assert lib.conv3x3_dgrad_act(ALIGNED, ALIGNED, far, 1, ALIGNED, 2, 60, 64, 8, 8, 0, 0,
+                                 None) == 1
+    assert lib.conv3x3_dgrad_act(None, ALIGNED, None, 0, ALIGNED, *a, 0, 0, None) == 1
+
+
 def test_workspace_size_depends_only_on_shape(lib):
     from synth import STACK, STEM, L1, L2, L3
     for L in [STEM, L1, L2, L3] + STACK:

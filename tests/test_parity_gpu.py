@@ -207,6 +207,70 @@ def test_eight_channel_kernels(shape):
         assert np.array_equal(host(ybf), rne_bf16(host(y32)))
 
 
+# ---------------------------------------------------------------------------
+# backward through the input's activation, fused into the epilogues
+# ---------------------------------------------------------------------------
+FUSED_SHAPES = [
+    (2, 64, 64, 9, 9),
+    (1, 72, 200, 6, 11),    # ragged channel chunks and N tiles
+    (2, 8, 128, 12, 12),    # eight input channels: dgrad writes 8 channels
+    (3, 128, 256, 17, 13),
+    (2, 256, 64, 5, 7),
+]
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("shape", FUSED_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_fused_activation_backward(shape, path):
+    p = PATHS[path]
+    N, Cin, Cout, H, W = shape
+    t = _small(shape)
+    zin_h = synth.make_zin(t.layer, seed=7)
+    x, w, b, dy = dev_tensors(t)
+    zin = to_dev_bf16(zin_h)
+    for act in (1, 2):
+        # forward that also keeps z: y unchanged, z = the act-free output, bit for bit
+        z = torch.empty((N, H, W, Cout), dtype=torch.bfloat16, device="cuda")
+        y = ops.fwd(x, w, b, act=act, path=p, z_out=z)
+        y_plain = ops.fwd(x, w, b, act=act, path=p)
+        z_plain = ops.fwd(x, w, b, act=0, path=p)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_plain), act
+        assert torch.equal(z, z_plain), act
+        assert check_bf16_store(host(z), oracle.conv3x3_fwd(t.x, t.w, t.bias, 0)) == 0
+        # dgrad scaled by act'(z_in)
+        dx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=p, z_in=zin, act_in=act)
+        dxbf = ops.dgrad(dy, w, path=p, z_in=zin, act_in=act)
+        torch.cuda.synchronize()
+        ref = oracle.conv3x3_dgrad_act(t.dy, t.w, zin_h, act)
+        assert rel_err(host(dx32), ref) <= TOL_BF16, act
+        assert check_bf16_store(host(dxbf), ref) == 0, act
+        assert np.array_equal(host(dxbf), rne_bf16(host(dx32))), act
+    # act_in = NONE is plain dgrad (z_in ignored)
+    dxn = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=p, z_in=zin, act_in=L.ACT_NONE)
+    dxp = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=p)
+    torch.cuda.synchronize()
+    assert torch.equal(dxn, dxp)
+
+
+@pytest.mark.parametrize("tile", ["64x2", "256x1", "halo64"])
+def test_fused_activation_backward_tiles(tile, monkeypatch):
+    monkeypatch.setenv("CONV3X3_TILE", tile)
+    shape = (2, 64, 128, 16, 16)
+    N, Cin, Cout, H, W = shape
+    t = _small(shape)
+    zin_h = synth.make_zin(t.layer, seed=7)
+    x, w, b, dy = dev_tensors(t)
+    z = torch.empty((N, H, W, Cout), dtype=torch.bfloat16, device="cuda")
+    y = ops.fwd(x, w, b, act=1, out_dtype=L.DT_F32, path=L.PATH_TENSOR, z_out=z)
+    dx = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=L.PATH_TENSOR, z_in=to_dev_bf16(zin_h),
+                   act_in=1)
+    torch.cuda.synchronize()
+    assert rel_err(host(y), oracle.conv3x3_fwd(t.x, t.w, t.bias, 1)) <= TOL_BF16
+    assert check_bf16_store(host(z), oracle.conv3x3_fwd(t.x, t.w, t.bias, 0)) == 0
+    assert rel_err(host(dx), oracle.conv3x3_dgrad_act(t.dy, t.w, zin_h, 1)) <= TOL_BF16
+
+
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_wgrad_is_bit_deterministic(path):
     t = _small((4, 128, 128, 16, 16))
@@ -300,6 +364,26 @@ def _sampled_layer_check(Lr, seed, index, n_rand=4096, n_dw=192, whole_images=Tr
 def test_full_size_configs_sampled(name):
     Lr = synth.CONFIGS[name][0]
     _sampled_layer_check(Lr, seed=0, index=0)
+
+
+def test_fused_activation_backward_full_size_sampled():
+    # the 128-channel 64x64 layer at batch 64, AUTO path, as the fused step runs it
+    Lr = synth.L1
+    t = synth.make_tensors(Lr, seed=0, index=0)
+    zin_h = synth.make_zin(Lr, seed=0, index=0)
+    x, w, b, dy = dev_tensors(t)
+    z = torch.empty((Lr.N, Lr.H, Lr.W, Lr.Cout), dtype=torch.bfloat16, device="cuda")
+    ops.fwd(x, w, b, act=1, z_out=z)
+    dx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, z_in=to_dev_bf16(zin_h), act_in=1)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(77)
+    zh, dxh = host(z).reshape(-1), host(dx32).reshape(-1)
+    iz = rng.integers(0, zh.size, 4096)
+    rz = oracle.conv3x3_fwd_at(t.x, t.w, t.bias, 0, iz)
+    assert check_bf16_store(zh[iz], rz) == 0
+    ix = rng.integers(0, dxh.size, 4096)
+    rx = oracle.conv3x3_dgrad_act_at(t.dy, t.w, zin_h, 1, ix)
+    assert np.max(np.abs(dxh[ix] - rx)) / max(np.max(np.abs(rx)), 1e-30) <= TOL_BF16
 
 
 def test_full_unet_stack_sampled():

@@ -40,6 +40,8 @@ _SIGS = {
     "conv3x3_status_string": ([_i], ctypes.c_char_p),
     "conv3x3_auto_path": ([_i] * 6, _i),
     "conv3x3_wgrad_noalloc": ([_vp, _vp, _vp, _vp] + [_i] * 5 + [_vp], _i),
+    "conv3x3_fwd_save_z": ([_vp, _vp, _vp, _vp, _vp] + [_i] * 8 + [_vp], _i),
+    "conv3x3_dgrad_act": ([_vp, _vp, _vp, _i, _vp] + [_i] * 7 + [_vp], _i),
 }
 
 WGRAD_NOALLOC_MAX_BYTES = 64 << 20
@@ -123,6 +125,18 @@ def conv3x3_fwd_ex(x, w, bias, y, N, Cin, Cout, H, W, act, out_dtype, path, stre
 def conv3x3_dgrad_ex(dy, w, dx, N, Cin, Cout, H, W, out_dtype, path, stream=None):
     return _check(load().conv3x3_dgrad_ex(_p(dy), _p(w), _p(dx), N, Cin, Cout, H, W, out_dtype,
                                           path, _stream(stream)), "conv3x3_dgrad_ex")
+
+
+def conv3x3_fwd_save_z(x, w, bias, y, z, N, Cin, Cout, H, W, act, out_dtype, path, stream=None):
+    return _check(load().conv3x3_fwd_save_z(_p(x), _p(w), _p(bias), _p(y), _p(z), N, Cin, Cout, H,
+                                            W, act, out_dtype, path, _stream(stream)),
+                  "conv3x3_fwd_save_z")
+
+
+def conv3x3_dgrad_act(dy, w, z_in, act_in, dx, N, Cin, Cout, H, W, out_dtype, path, stream=None):
+    return _check(load().conv3x3_dgrad_act(_p(dy), _p(w), _p(z_in), act_in, _p(dx), N, Cin, Cout,
+                                           H, W, out_dtype, path, _stream(stream)),
+                  "conv3x3_dgrad_act")
 
 
 def conv3x3_wgrad_ex(x, dy, dw, dbias, N, Cin, Cout, H, W, workspace, workspace_bytes, path,

@@ -137,6 +137,53 @@ __global__ void k_wait_selftest(unsigned* status, unsigned long long limit_ns) {
 
 }  // namespace c3
 
+namespace c3 {
+namespace {
+
+bool overlap(const void* a, long long abytes, const void* b, long long bbytes) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return pa < pb + (uintptr_t)bbytes && pb < pa + (uintptr_t)abytes;
+}
+
+int fwd_impl(const void* x, const void* w, const float* bias, void* y, int N, int Cin, int Cout,
+             int H, int W, int act, int out_dtype, int path, const EpiExtra& ex, void* stream) {
+  int rc = check_shape(N, Cin, Cout, H, W, true);
+  if (rc) return rc;
+  if (!x || !w || !y || !aligned16(x) || !aligned16(w) || !aligned16(y)) return CONV3X3_ERR_INVALID_ARG;
+  if (bias && !aligned16(bias)) return CONV3X3_ERR_INVALID_ARG;
+  if (act < CONV3X3_ACT_NONE || act > CONV3X3_ACT_LRELU) return CONV3X3_ERR_INVALID_ARG;
+  if (out_dtype != CONV3X3_DT_BF16 && out_dtype != CONV3X3_DT_F32) return CONV3X3_ERR_INVALID_ARG;
+  if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return CONV3X3_ERR_INVALID_ARG;
+  Shape s{N, Cin, Cout, H, W};
+  int p = choose_path(0, s, path);
+  if (p < 0) return CONV3X3_ERR_UNSUPPORTED;
+  const int of32 = out_dtype == CONV3X3_DT_F32;
+  if (p == CONV3X3_PATH_SIMT) return simt_fwd_bf16(x, w, bias, y, s, act, of32, ex, as_stream(stream));
+  DevCtx d;
+  if ((rc = get_ctx(&d))) return rc;
+  return tc_fwd(x, w, bias, y, s, act, of32, ex, d, as_stream(stream));
+}
+
+int dgrad_impl(const void* dy, const void* w, void* dx, int N, int Cin, int Cout, int H, int W,
+               int out_dtype, int path, const EpiExtra& ex, void* stream) {
+  int rc = check_shape(N, Cin, Cout, H, W, true);
+  if (rc) return rc;
+  if (!dy || !w || !dx || !aligned16(dy) || !aligned16(w) || !aligned16(dx)) return CONV3X3_ERR_INVALID_ARG;
+  if (out_dtype != CONV3X3_DT_BF16 && out_dtype != CONV3X3_DT_F32) return CONV3X3_ERR_INVALID_ARG;
+  if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return CONV3X3_ERR_INVALID_ARG;
+  Shape s{N, Cin, Cout, H, W};
+  int p = choose_path(1, s, path);
+  if (p < 0) return CONV3X3_ERR_UNSUPPORTED;
+  const int of32 = out_dtype == CONV3X3_DT_F32;
+  if (p == CONV3X3_PATH_SIMT) return simt_dgrad_bf16(dy, w, dx, s, of32, ex, as_stream(stream));
+  DevCtx d;
+  if ((rc = get_ctx(&d))) return rc;
+  return tc_dgrad(dy, w, dx, s, of32, ex, d, as_stream(stream));
+}
+
+}  // namespace
+}  // namespace c3
+
 using namespace c3;
 
 extern "C" {
@@ -159,23 +206,40 @@ int conv3x3_auto_path(int pass, int N, int Cin, int Cout, int H, int W) {
   return choose_path(pass, s, CONV3X3_PATH_AUTO);
 }
 
+
 int conv3x3_fwd_ex(const void* x, const void* w, const float* bias, void* y, int N, int Cin,
                    int Cout, int H, int W, int act, int out_dtype, int path, void* stream) {
-  int rc = check_shape(N, Cin, Cout, H, W, true);
-  if (rc) return rc;
-  if (!x || !w || !y || !aligned16(x) || !aligned16(w) || !aligned16(y)) return CONV3X3_ERR_INVALID_ARG;
-  if (bias && !aligned16(bias)) return CONV3X3_ERR_INVALID_ARG;
-  if (act < CONV3X3_ACT_NONE || act > CONV3X3_ACT_LRELU) return CONV3X3_ERR_INVALID_ARG;
-  if (out_dtype != CONV3X3_DT_BF16 && out_dtype != CONV3X3_DT_F32) return CONV3X3_ERR_INVALID_ARG;
-  if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return CONV3X3_ERR_INVALID_ARG;
-  Shape s{N, Cin, Cout, H, W};
-  int p = choose_path(0, s, path);
-  if (p < 0) return CONV3X3_ERR_UNSUPPORTED;
-  const int of32 = out_dtype == CONV3X3_DT_F32;
-  if (p == CONV3X3_PATH_SIMT) return simt_fwd_bf16(x, w, bias, y, s, act, of32, as_stream(stream));
-  DevCtx d;
-  if ((rc = get_ctx(&d))) return rc;
-  return tc_fwd(x, w, bias, y, s, act, of32, d, as_stream(stream));
+  return fwd_impl(x, w, bias, y, N, Cin, Cout, H, W, act, out_dtype, path, EpiExtra{}, stream);
+}
+
+int conv3x3_fwd_save_z(const void* x, const void* w, const float* bias, void* y, void* z, int N,
+                       int Cin, int Cout, int H, int W, int act, int out_dtype, int path,
+                       void* stream) {
+  if (!z || !aligned16(z) || !y) return CONV3X3_ERR_INVALID_ARG;
+  if (check_shape(N, Cin, Cout, H, W, true) != CONV3X3_OK) return CONV3X3_ERR_INVALID_ARG;
+  const long long elems = (long long)N * H * W * Cout;
+  if (overlap(z, elems * 2, y, elems * (out_dtype == CONV3X3_DT_F32 ? 4 : 2)))
+    return CONV3X3_ERR_INVALID_ARG;
+  EpiExtra ex;
+  ex.zout = z;
+  return fwd_impl(x, w, bias, y, N, Cin, Cout, H, W, act, out_dtype, path, ex, stream);
+}
+
+int conv3x3_dgrad_act(const void* dy, const void* w, const void* z_in, int act_in, void* dx,
+                      int N, int Cin, int Cout, int H, int W, int out_dtype, int path,
+                      void* stream) {
+  if (act_in < CONV3X3_ACT_NONE || act_in > CONV3X3_ACT_LRELU) return CONV3X3_ERR_INVALID_ARG;
+  EpiExtra ex;
+  if (act_in != CONV3X3_ACT_NONE) {
+    if (!z_in || !aligned16(z_in) || !dx) return CONV3X3_ERR_INVALID_ARG;
+    if (check_shape(N, Cin, Cout, H, W, true) != CONV3X3_OK) return CONV3X3_ERR_INVALID_ARG;
+    const long long elems = (long long)N * H * W * Cin;
+    if (overlap(z_in, elems * 2, dx, elems * (out_dtype == CONV3X3_DT_F32 ? 4 : 2)))
+      return CONV3X3_ERR_INVALID_ARG;
+    ex.zin = z_in;
+    ex.zin_act = act_in;
+  }
+  return dgrad_impl(dy, w, dx, N, Cin, Cout, H, W, out_dtype, path, ex, stream);
 }
 
 int conv3x3_fwd(const void* x, const void* w, const float* bias, void* y, int N, int Cin, int Cout,
@@ -186,19 +250,7 @@ int conv3x3_fwd(const void* x, const void* w, const float* bias, void* y, int N,
 
 int conv3x3_dgrad_ex(const void* dy, const void* w, void* dx, int N, int Cin, int Cout, int H,
                      int W, int out_dtype, int path, void* stream) {
-  int rc = check_shape(N, Cin, Cout, H, W, true);
-  if (rc) return rc;
-  if (!dy || !w || !dx || !aligned16(dy) || !aligned16(w) || !aligned16(dx)) return CONV3X3_ERR_INVALID_ARG;
-  if (out_dtype != CONV3X3_DT_BF16 && out_dtype != CONV3X3_DT_F32) return CONV3X3_ERR_INVALID_ARG;
-  if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return CONV3X3_ERR_INVALID_ARG;
-  Shape s{N, Cin, Cout, H, W};
-  int p = choose_path(1, s, path);
-  if (p < 0) return CONV3X3_ERR_UNSUPPORTED;
-  const int of32 = out_dtype == CONV3X3_DT_F32;
-  if (p == CONV3X3_PATH_SIMT) return simt_dgrad_bf16(dy, w, dx, s, of32, as_stream(stream));
-  DevCtx d;
-  if ((rc = get_ctx(&d))) return rc;
-  return tc_dgrad(dy, w, dx, s, of32, d, as_stream(stream));
+  return dgrad_impl(dy, w, dx, N, Cin, Cout, H, W, out_dtype, path, EpiExtra{}, stream);
 }
 
 int conv3x3_dgrad(const void* dy, const void* w, void* dx, int N, int Cin, int Cout, int H, int W,

@@ -25,6 +25,15 @@ struct DevCtx {
   int device;
 };
 
+// Optional extras of the fused epilogue (bf16 tensors laid out like the output):
+// zout -- forward also stores z = conv + bias before the activation;
+// zin  -- dgrad scales its result by act'(zin) for zin_act.
+struct EpiExtra {
+  void* zout = nullptr;
+  const void* zin = nullptr;
+  int zin_act = CONV3X3_ACT_NONE;
+};
+
 // ---- CUDA-core kernels (simt.cu) ----
 int simt_fwd_f32(const float* x, const float* w, const float* bias, float* y, const Shape& s,
                  int act, cudaStream_t st);
@@ -33,9 +42,9 @@ int simt_wgrad_f32(const float* x, const float* dy, float* dw, float* db, const 
                    cudaStream_t st);
 
 int simt_fwd_bf16(const void* x, const void* w, const float* bias, void* y, const Shape& s,
-                  int act, int out_f32, cudaStream_t st);
+                  int act, int out_f32, const EpiExtra& ex, cudaStream_t st);
 int simt_dgrad_bf16(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
-                    cudaStream_t st);
+                    const EpiExtra& ex, cudaStream_t st);
 size_t simt_wgrad_workspace(const Shape& s, int num_sms);
 int simt_wgrad_bf16(const void* x, const void* dy, float* dw, float* db, const Shape& s,
                     void* ws, size_t ws_bytes, int num_sms, cudaStream_t st);
@@ -43,9 +52,9 @@ int simt_wgrad_bf16(const void* x, const void* dy, float* dw, float* db, const S
 // ---- tensor-core kernels (tc.cu) ----
 bool tc_supported(int pass, const Shape& s);
 int tc_fwd(const void* x, const void* w, const float* bias, void* y, const Shape& s, int act,
-           int out_f32, const DevCtx& d, cudaStream_t st);
+           int out_f32, const EpiExtra& ex, const DevCtx& d, cudaStream_t st);
 int tc_dgrad(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
-             const DevCtx& d, cudaStream_t st);
+             const EpiExtra& ex, const DevCtx& d, cudaStream_t st);
 size_t tc_wgrad_workspace(const Shape& s, int num_sms);
 int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s, void* ws,
              size_t ws_bytes, const DevCtx& d, cudaStream_t st);

@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "act.cuh"
 #include "conv3x3_internal.h"
 
 namespace c3 {
@@ -59,6 +60,15 @@ __device__ __forceinline__ void store8(void* out, long long off, const float (&f
   } else {
     *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + off) = pack8(f);
   }
+}
+
+// acc *= act'(zin[off .. off + 8)), zin bf16
+__device__ __forceinline__ void scale_by_act_grad(float (&acc)[8], const __nv_bfloat16* zin,
+                                                  long long off, int zin_act) {
+  float z[8];
+  unpack8(__ldg(reinterpret_cast<const uint4*>(zin + off)), z);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] *= act_grad_f32(zin_act, z[i]);
 }
 
 // ======================================================================
@@ -151,8 +161,8 @@ __global__ void k_wgrad_f32(const float* __restrict__ x, const float* __restrict
 // registers, weights (fp32, [Cout][72]) in shared memory.
 __global__ void __launch_bounds__(kThreads) k_fwd_bf16_c8(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w,
-    const float* __restrict__ bias, void* __restrict__ y, int N, int H, int W, int Cout, int act,
-    int out_f32) {
+    const float* __restrict__ bias, void* __restrict__ y, __nv_bfloat16* __restrict__ zout, int N,
+    int H, int W, int Cout, int act, int out_f32) {
   extern __shared__ float4 smem_f4[];
   float* ws = reinterpret_cast<float*>(smem_f4);
   for (int i = threadIdx.x; i < Cout * 72; i += blockDim.x) ws[i] = __bfloat162float(w[i]);
@@ -191,8 +201,10 @@ __global__ void __launch_bounds__(kThreads) k_fwd_bf16_c8(
           acc[j] = fmaf(in[4 * q + 2], wv.z, acc[j]);
           acc[j] = fmaf(in[4 * q + 3], wv.w, acc[j]);
         }
-        acc[j] = act_f(acc[j], act);
       }
+      if (zout) store8(zout, p * Cout + k0, acc, 0);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = act_f(acc[j], act);
       store8(y, p * Cout + k0, acc, out_f32);
     }
   }
@@ -201,8 +213,8 @@ __global__ void __launch_bounds__(kThreads) k_fwd_bf16_c8(
 // forward, generic Cin (multiple of 8): one thread per (pixel, 8 output channels)
 __global__ void __launch_bounds__(kThreads) k_fwd_bf16_gen(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w,
-    const float* __restrict__ bias, void* __restrict__ y, int N, int H, int W, int Cin, int Cout,
-    int act, int out_f32) {
+    const float* __restrict__ bias, void* __restrict__ y, __nv_bfloat16* __restrict__ zout, int N,
+    int H, int W, int Cin, int Cout, int act, int out_f32) {
   const int KG = Cout / 8;
   const long long total = (long long)N * H * W * KG;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
@@ -229,6 +241,7 @@ __global__ void __launch_bounds__(kThreads) k_fwd_bf16_gen(
         }
       }
     }
+    if (zout) store8(zout, p * Cout + k0, acc, 0);
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = act_f(acc[j], act);
     store8(y, p * Cout + k0, acc, out_f32);
@@ -239,7 +252,8 @@ __global__ void __launch_bounds__(kThreads) k_fwd_bf16_gen(
 // [tap][Cout][8] in shared memory.
 __global__ void __launch_bounds__(kThreads) k_dgrad_bf16_c8(
     const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ w,
-    void* __restrict__ dx, int N, int H, int W, int Cout, int out_f32) {
+    void* __restrict__ dx, const __nv_bfloat16* __restrict__ zin, int zin_act, int N, int H, int W,
+    int Cout, int out_f32) {
   extern __shared__ float4 smem_f4[];
   float* ws = reinterpret_cast<float*>(smem_f4);
   for (int i = threadIdx.x; i < Cout * 72; i += blockDim.x) {
@@ -279,6 +293,7 @@ __global__ void __launch_bounds__(kThreads) k_dgrad_bf16_c8(
         }
       }
     }
+    if (zin) scale_by_act_grad(acc, zin, p * 8, zin_act);
     store8(dx, p * 8, acc, out_f32);
   }
 }
@@ -286,7 +301,8 @@ __global__ void __launch_bounds__(kThreads) k_dgrad_bf16_c8(
 // dgrad, generic Cin: one thread per (pixel, 8 input channels)
 __global__ void __launch_bounds__(kThreads) k_dgrad_bf16_gen(
     const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ w,
-    void* __restrict__ dx, int N, int H, int W, int Cin, int Cout, int out_f32) {
+    void* __restrict__ dx, const __nv_bfloat16* __restrict__ zin, int zin_act, int N, int H, int W,
+    int Cin, int Cout, int out_f32) {
   const int CG = Cin / 8;
   const long long total = (long long)N * H * W * CG;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
@@ -314,6 +330,7 @@ __global__ void __launch_bounds__(kThreads) k_dgrad_bf16_gen(
         }
       }
     }
+    if (zin) scale_by_act_grad(acc, zin, p * Cin + c0, zin_act);
     store8(dx, p * Cin + c0, acc, out_f32);
   }
 }
@@ -522,39 +539,41 @@ int simt_wgrad_f32(const float* x, const float* dy, float* dw, float* db, const 
 }
 
 int simt_fwd_bf16(const void* x, const void* w, const float* bias, void* y, const Shape& s,
-                  int act, int out_f32, cudaStream_t st) {
+                  int act, int out_f32, const EpiExtra& ex, cudaStream_t st) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
+  __nv_bfloat16* zb = static_cast<__nv_bfloat16*>(ex.zout);
   if (s.Cin == 8 && s.Cout <= 512) {
     size_t sm = (size_t)s.Cout * 72 * sizeof(float);
     if (sm > 48 * 1024 &&
         cudaFuncSetAttribute(k_fwd_bf16_c8, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
             cudaSuccess)
       return CONV3X3_ERR_CUDA;
-    k_fwd_bf16_c8<<<grid_for(s.P()), kThreads, sm, st>>>(xb, wb, bias, y, s.N, s.H, s.W, s.Cout,
-                                                         act, out_f32);
+    k_fwd_bf16_c8<<<grid_for(s.P()), kThreads, sm, st>>>(xb, wb, bias, y, zb, s.N, s.H, s.W,
+                                                         s.Cout, act, out_f32);
   } else {
     k_fwd_bf16_gen<<<grid_for(s.P() * (s.Cout / 8)), kThreads, 0, st>>>(
-        xb, wb, bias, y, s.N, s.H, s.W, s.Cin, s.Cout, act, out_f32);
+        xb, wb, bias, y, zb, s.N, s.H, s.W, s.Cin, s.Cout, act, out_f32);
   }
   return launch_status();
 }
 
 int simt_dgrad_bf16(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
-                    cudaStream_t st) {
+                    const EpiExtra& ex, cudaStream_t st) {
   const __nv_bfloat16* db = static_cast<const __nv_bfloat16*>(dy);
   const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
+  const __nv_bfloat16* zb = static_cast<const __nv_bfloat16*>(ex.zin);
   if (s.Cin == 8 && s.Cout <= 512) {
     size_t sm = (size_t)s.Cout * 72 * sizeof(float);
     if (sm > 48 * 1024 &&
         cudaFuncSetAttribute(k_dgrad_bf16_c8, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sm) != cudaSuccess)
       return CONV3X3_ERR_CUDA;
-    k_dgrad_bf16_c8<<<grid_for(s.P()), kThreads, sm, st>>>(db, wb, dx, s.N, s.H, s.W, s.Cout,
-                                                           out_f32);
+    k_dgrad_bf16_c8<<<grid_for(s.P()), kThreads, sm, st>>>(db, wb, dx, zb, ex.zin_act, s.N, s.H,
+                                                           s.W, s.Cout, out_f32);
   } else {
     k_dgrad_bf16_gen<<<grid_for(s.P() * (s.Cin / 8)), kThreads, 0, st>>>(
-        db, wb, dx, s.N, s.H, s.W, s.Cin, s.Cout, out_f32);
+        db, wb, dx, zb, ex.zin_act, s.N, s.H, s.W, s.Cin, s.Cout, out_f32);
   }
   return launch_status();
 }

@@ -37,6 +37,7 @@
 #include <cstdlib>
 #include <mutex>
 
+#include "act.cuh"
 #include "conv3x3_internal.h"
 #include "ptx.cuh"
 
@@ -110,10 +111,48 @@ struct IgemmParams {
   int num_m_tiles, num_n_tiles;
   unsigned* status;
   unsigned long long wait_ns;
+  // forward: also store z = conv + bias, rounded once to bf16, laid out like out
+  __nv_bfloat16* zout = nullptr;
+  // dgrad: scale by act'(zin) (the input's pre-activation, laid out like out)
+  const __nv_bfloat16* zin = nullptr;
+  int zin_act = CONV3X3_ACT_NONE;
 };
 
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* o, int col0, int nout, const float (&f)[32]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    if (col0 + 8 * g < nout) {
+      uint4 u;
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[8 * g + 2 * i], f[8 * g + 2 * i + 1]);
+      *reinterpret_cast<uint4*>(o + 8 * g) = u;
+    }
+}
+
+// The 32 z_in values (bf16) of one output chunk, fetched before the
+// accumulator so that their latency overlaps the TMEM load.
+__device__ __forceinline__ void load_zin(const IgemmParams& p, long long pix, int col0,
+                                         uint4 (&zr)[4]) {
+  const __nv_bfloat16* zp = p.zin + pix * p.nout + col0;
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    zr[g] = col0 + 8 * g < p.nout ? __ldg(reinterpret_cast<const uint4*>(zp + 8 * g))
+                                  : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// L2 prefetch of one output row's z_in span [col0, col0 + ncols), issued while
+// the tile's MMAs still run.
+__device__ __forceinline__ void prefetch_zin_row(const IgemmParams& p, long long pix, int col0,
+                                                 int ncols) {
+  const int n = min(ncols, p.nout - col0);
+  const char* base = reinterpret_cast<const char*>(p.zin + pix * p.nout + col0);
+  for (int b = 0; b < 2 * n; b += 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(base + b));
+}
+
 __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix, int col0,
-                                            const uint32_t (&v)[32]) {
+                                            const uint32_t (&v)[32], const uint4 (&zr)[4]) {
   float f[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
@@ -129,12 +168,25 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix,
       }
     }
   }
+  if (p.zout) store_bf16x32(p.zout + pix * p.nout + col0, col0, p.nout, f);
   if (p.act == CONV3X3_ACT_SILU) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) f[i] = silu_f32(f[i]);
   } else if (p.act == CONV3X3_ACT_LRELU) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) f[i] = f[i] >= 0.0f ? f[i] : 0.2f * f[i];
+  }
+  if (p.zin) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&zr[g]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 z = __bfloat1622float2(h[i]);
+        f[8 * g + 2 * i] *= act_grad_f32(p.zin_act, z.x);
+        f[8 * g + 2 * i + 1] *= act_grad_f32(p.zin_act, z.y);
+      }
+    }
   }
   if (p.out_f32) {
     float* o = static_cast<float*>(p.out) + pix * p.nout + col0;
@@ -145,17 +197,15 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix,
         reinterpret_cast<float4*>(o + 8 * g)[1] = make_float4(f[8 * g + 4], f[8 * g + 5], f[8 * g + 6], f[8 * g + 7]);
       }
   } else {
-    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + pix * p.nout + col0;
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-      if (col0 + 8 * g < p.nout) {
-        uint4 u;
-        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[8 * g + 2 * i], f[8 * g + 2 * i + 1]);
-        *reinterpret_cast<uint4*>(o + 8 * g) = u;
-      }
+    store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + pix * p.nout + col0, col0, p.nout, f);
   }
+}
+
+__device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix, int col0,
+                                            const uint32_t (&v)[32]) {
+  uint4 zr[4] = {};
+  if (p.zin) load_zin(p, pix, col0, zr);
+  store_chunk(p, pix, col0, v, zr);
 }
 
 // ----------------------------------------------------------------------------
@@ -355,20 +405,25 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     int buf = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
-      tc_fence_after();
       const int mt = tile / p.num_n_tiles, nt = tile % p.num_n_tiles;
       const long long pix = (long long)mt * TM + sub * BM + row;
       const bool valid = pix < p.P;
+      if (p.zin && valid && nt * BN + col_off < p.nout)
+        prefetch_zin_row(p, pix, nt * BN + col_off, kCols);
+      if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
+      tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
                              (uint32_t)((buf * MT + sub) * BN + col_off);
 #pragma unroll 1
       for (int j = 0; j < kCols / 32; ++j) {
+        const int col0 = nt * BN + col_off + j * 32;
+        const bool live = valid && col0 < p.nout;
+        uint4 zr[4] = {};
+        if (p.zin && live) load_zin(p, pix, col0, zr);
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
         tmem_ld_wait();
-        const int col0 = nt * BN + col_off + j * 32;
-        if (valid && col0 < p.nout) store_chunk(p, pix, col0, v);
+        if (live) store_chunk(p, pix, col0, v, zr);
       }
       tc_fence_before();
       __syncwarp();
@@ -1432,7 +1487,7 @@ int launch_stem(const CUtensorMap& a, const CUtensorMap& b, const IgemmParams& p
 
 // Forward with exactly 8 input channels and at most 256 outputs (one N tile).
 int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const Shape& s, int act,
-                 int out_f32, const DevCtx& d, cudaStream_t st) {
+                 int out_f32, const EpiExtra& ex, const DevCtx& d, cudaStream_t st) {
   const int bn = s.Cout <= 64 ? 64 : s.Cout <= 128 ? 128 : 256;
   CUtensorMap ta, tb;
   int rc = make_im2col_map(&ta, x, s.N, s.H, s.W, 8, BM, 8, false);
@@ -1453,13 +1508,15 @@ int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const
   prm.num_n_tiles = 1;
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
+  prm.zout = static_cast<__nv_bfloat16*>(ex.zout);
   if (bn == 64) return launch_stem<64>(ta, tb, prm, d, st);
   if (bn == 128) return launch_stem<128>(ta, tb, prm, d, st);
   return launch_stem<256>(ta, tb, prm, d, st);
 }
 
 int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const float* bias, void* out,
-              const Shape& s, int act, int out_f32, const DevCtx& d, cudaStream_t st) {
+              const Shape& s, int act, int out_f32, const EpiExtra& ex, const DevCtx& d,
+              cudaStream_t st) {
   const int nout = dgrad ? s.Cin : s.Cout;
   TileShape ts = pick_tile(nout, s, d.num_sms);
   // CONV3X3_TILE="<BN>x<MT>" or "halo<BN>" overrides the choice (tuning and tests)
@@ -1493,6 +1550,9 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   prm.num_n_tiles = (nout + bn - 1) / bn;
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
+  prm.zout = static_cast<__nv_bfloat16*>(ex.zout);
+  prm.zin = static_cast<const __nv_bfloat16*>(ex.zin);
+  prm.zin_act = ex.zin ? ex.zin_act : CONV3X3_ACT_NONE;
   if (ts.halo) {
 #define C3_HALO(W_, BN_) \
   return dgrad ? launch_halo<W_, BN_, true>(ta, tb, prm, d, st) : launch_halo<W_, BN_, false>(ta, tb, prm, d, st)
@@ -1573,14 +1633,14 @@ bool tc_supported(int pass, const Shape& s) {
 }
 
 int tc_fwd(const void* x, const void* w, const float* bias, void* y, const Shape& s, int act,
-           int out_f32, const DevCtx& d, cudaStream_t st) {
-  if (s.Cin == 8 && s.Cout <= 256) return run_stem_fwd(x, w, bias, y, s, act, out_f32, d, st);
-  return run_igemm(false, x, s.Cin, w, bias, y, s, act, out_f32, d, st);
+           int out_f32, const EpiExtra& ex, const DevCtx& d, cudaStream_t st) {
+  if (s.Cin == 8 && s.Cout <= 256) return run_stem_fwd(x, w, bias, y, s, act, out_f32, ex, d, st);
+  return run_igemm(false, x, s.Cin, w, bias, y, s, act, out_f32, ex, d, st);
 }
 
-int tc_dgrad(const void* dy, const void* w, void* dx, const Shape& s, int out_f32, const DevCtx& d,
-             cudaStream_t st) {
-  return run_igemm(true, dy, s.Cout, w, nullptr, dx, s, CONV3X3_ACT_NONE, out_f32, d, st);
+int tc_dgrad(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
+             const EpiExtra& ex, const DevCtx& d, cudaStream_t st) {
+  return run_igemm(true, dy, s.Cout, w, nullptr, dx, s, CONV3X3_ACT_NONE, out_f32, ex, d, st);
 }
 
 // Cin == 8: one tile per 128 output channels; splits fill the GPU once.

@@ -17,24 +17,34 @@ def _shape(x: torch.Tensor, w: torch.Tensor):
 
 
 def fwd(x, w, bias=None, act=L.ACT_NONE, out_dtype=L.DT_BF16, path=L.PATH_AUTO, out=None,
-        stream=None):
-    """y = act(conv3x3(x, w) + bias); x [N,H,W,Cin] bf16, w [Cout,3,3,Cin] bf16."""
+        stream=None, z_out=None):
+    """y = act(conv3x3(x, w) + bias); x [N,H,W,Cin] bf16, w [Cout,3,3,Cin] bf16.
+    With z_out (bf16 [N,H,W,Cout]) the pre-activation is stored there too."""
     N, Cin, Cout, H, W = _shape(x, w)
     if out is None:
         dt = torch.float32 if out_dtype == L.DT_F32 else torch.bfloat16
         out = torch.empty((N, H, W, Cout), dtype=dt, device=x.device)
-    L.conv3x3_fwd_ex(x, w, bias, out, N, Cin, Cout, H, W, act, out_dtype, path, stream)
+    if z_out is None:
+        L.conv3x3_fwd_ex(x, w, bias, out, N, Cin, Cout, H, W, act, out_dtype, path, stream)
+    else:
+        L.conv3x3_fwd_save_z(x, w, bias, out, z_out, N, Cin, Cout, H, W, act, out_dtype, path,
+                             stream)
     return out
 
 
-def dgrad(dy, w, out_dtype=L.DT_BF16, path=L.PATH_AUTO, out=None, stream=None):
-    """dx [N,H,W,Cin] from dy [N,H,W,Cout] and w [Cout,3,3,Cin]."""
+def dgrad(dy, w, out_dtype=L.DT_BF16, path=L.PATH_AUTO, out=None, stream=None, z_in=None,
+          act_in=L.ACT_NONE):
+    """dx [N,H,W,Cin] from dy [N,H,W,Cout] and w [Cout,3,3,Cin].
+    With z_in (bf16 [N,H,W,Cin]) and act_in, returns act_in'(z_in) * dx instead."""
     N, H, W, Cout = dy.shape
     Cin = w.shape[3]
     if out is None:
         dt = torch.float32 if out_dtype == L.DT_F32 else torch.bfloat16
         out = torch.empty((N, H, W, Cin), dtype=dt, device=dy.device)
-    L.conv3x3_dgrad_ex(dy, w, out, N, Cin, Cout, H, W, out_dtype, path, stream)
+    if z_in is None:
+        L.conv3x3_dgrad_ex(dy, w, out, N, Cin, Cout, H, W, out_dtype, path, stream)
+    else:
+        L.conv3x3_dgrad_act(dy, w, z_in, act_in, out, N, Cin, Cout, H, W, out_dtype, path, stream)
     return out
 
 
