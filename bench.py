@@ -10,6 +10,10 @@ Default workload "unet": the stem conv (3 -> 128 channels, zero-padded to 8,
 multipliers 1,2,3,4, two resblocks per level on the down and up paths, up-path
 inputs = concat of skip and main), batch 64, bf16 NHWC, seeded synthetic inputs.
 
+--concat-free gives each up-path conv its main branch and its skip as two
+tensors (conv3x3_fwd_cat / conv3x3_dgrad_cat / conv3x3_wgrad_cat): no
+concatenated input is built and dx comes back already split.
+
 --fused-act runs the training step with the activation's backward fused into
 the convolutions: each forward also stores its pre-activation z
 (conv3x3_fwd_save_z) and each dgrad takes the pre-activation of the layer that
@@ -179,10 +183,11 @@ def max_over_ranks(value: float, ws: int, device=None) -> float:
 # the CUDA arm
 # ---------------------------------------------------------------------------
 class Workload:
-    def __init__(self, layers, seed, device, keep_host=True, fused_act=False):
+    def __init__(self, layers, seed, device, keep_host=True, fused_act=False, concat_free=False):
         import torch
         self.layers = layers
         self.fused_act = fused_act
+        self.concat_free = concat_free
         self.dev = []
         self.host = []
         ws_max = 0
@@ -201,6 +206,17 @@ class Workload:
                 "dw": torch.empty((L.Cout, 3, 3, L.Cin), dtype=torch.float32, device=device),
                 "db": torch.empty((L.Cout,), dtype=torch.float32, device=device),
             }
+            cat = concat_free and L.cat_a > 0
+            d["cat_a"] = L.cat_a if cat else 0
+            if cat:
+                # up-path conv: main and skip stay two tensors; no concat buffer
+                ca = L.cat_a
+                d["xa"] = d["x"][..., :ca].contiguous()
+                d["xb"] = d["x"][..., ca:].contiguous()
+                d["dxa"] = torch.empty((L.N, L.H, L.W, ca), dtype=torch.bfloat16, device=device)
+                d["dxb"] = torch.empty((L.N, L.H, L.W, L.Cin - ca), dtype=torch.bfloat16,
+                                       device=device)
+                del d["x"], d["dx"]
             if fused_act:
                 # z: this layer's pre-activation (written by the forward);
                 # zin: the pre-activation of the layer that produced x (none for
@@ -210,6 +226,10 @@ class Workload:
                 hz = torch.from_numpy(synth.bf16_bits(synth.make_zin(L, seed=seed, index=i))
                                       .view(np.int16)).view(torch.bfloat16)
                 d["zin"] = hz.to(device)
+                if cat:
+                    d["za"] = d["zin"][..., :L.cat_a].contiguous()
+                    d["zb"] = d["zin"][..., L.cat_a:].contiguous()
+                    del d["zin"]
             self.dev.append(d)
             if keep_host:
                 h = {"x": hx.pin_memory(), "w": hw.pin_memory(), "b": hb.pin_memory(),
@@ -218,16 +238,30 @@ class Workload:
                      "db": torch.empty((L.Cout,), dtype=torch.float32).pin_memory()}
                 if fused_act:
                     h["zin"] = hz.pin_memory()
+                if cat:
+                    ca = L.cat_a
+                    h["xa"] = h["x"][..., :ca].contiguous().pin_memory()
+                    h["xb"] = h["x"][..., ca:].contiguous().pin_memory()
+                    del h["x"]
+                    if fused_act:
+                        h["za"] = h["zin"][..., :ca].contiguous().pin_memory()
+                        h["zb"] = h["zin"][..., ca:].contiguous().pin_memory()
+                        del h["zin"]
                 self.host.append(h)
-            ws_max = max(ws_max, Lb.conv3x3_wgrad_workspace_bytes(L.N, L.Cin, L.Cout, L.H, L.W))
+            if cat:
+                ws_max = max(ws_max, Lb.conv3x3_wgrad_cat_workspace_bytes(
+                    L.N, L.Cin, L.cat_a, L.Cout, L.H, L.W, Lb.PATH_AUTO))
+            else:
+                ws_max = max(ws_max, Lb.conv3x3_wgrad_workspace_bytes(L.N, L.Cin, L.Cout, L.H, L.W))
         self.ws_bytes = ws_max
         self.ws = torch.empty(max(ws_max, 256), dtype=torch.uint8, device=device)
 
-    def inputs(self):
-        return ("x", "w", "b", "dy", "zin") if self.fused_act else ("x", "w", "b", "dy")
+    def inputs(self, h):
+        keys = ("x", "xa", "xb", "w", "b", "dy", "zin", "za", "zb")
+        return [k for k in keys if k in h]
 
     def h2d_bytes(self):
-        return sum(h[k].numel() * h[k].element_size() for h in self.host for k in self.inputs())
+        return sum(h[k].numel() * h[k].element_size() for h in self.host for k in self.inputs(h))
 
     def d2h_bytes(self):
         return sum(h[k].numel() * h[k].element_size() for h in self.host for k in ("dw", "db"))
@@ -241,7 +275,11 @@ def run_step(wl: Workload, stream_handle: int, ev=None, record=None):
         d = wl.dev[i]
         if record is not None:
             record("fwd", i, 0)
-        if wl.fused_act:
+        if d["cat_a"]:
+            Lb.conv3x3_fwd_cat(d["xa"], d["xb"], d["cat_a"], d["w"], d["b"], d["y"], d.get("z"),
+                               L.N, L.Cin, L.Cout, L.H, L.W, L.act, Lb.DT_BF16, Lb.PATH_AUTO,
+                               stream_handle)
+        elif wl.fused_act:
             Lb.conv3x3_fwd_save_z(d["x"], d["w"], d["b"], d["y"], d["z"], L.N, L.Cin, L.Cout, L.H,
                                   L.W, L.act, Lb.DT_BF16, Lb.PATH_AUTO, stream_handle)
         else:
@@ -255,7 +293,11 @@ def run_step(wl: Workload, stream_handle: int, ev=None, record=None):
         d = wl.dev[i]
         if record is not None:
             record("dgrad", i, 0)
-        if wl.fused_act:
+        if d["cat_a"]:
+            Lb.conv3x3_dgrad_cat(d["dy"], d["w"], d["dxa"], d["dxb"], d["cat_a"], d.get("za"),
+                                 d.get("zb"), d.get("act_in", 0), L.N, L.Cin, L.Cout, L.H, L.W,
+                                 Lb.DT_BF16, Lb.PATH_AUTO, stream_handle)
+        elif wl.fused_act:
             Lb.conv3x3_dgrad_act(d["dy"], d["w"], d["zin"], d["act_in"], d["dx"], L.N, L.Cin,
                                  L.Cout, L.H, L.W, Lb.DT_BF16, Lb.PATH_AUTO, stream_handle)
         else:
@@ -263,8 +305,13 @@ def run_step(wl: Workload, stream_handle: int, ev=None, record=None):
         if record is not None:
             record("dgrad", i, 1)
             record("wgrad", i, 0)
-        Lb.conv3x3_wgrad(d["x"], d["dy"], d["dw"], d["db"], L.N, L.Cin, L.Cout, L.H, L.W, wl.ws,
-                         wl.ws_bytes, stream_handle)
+        if d["cat_a"]:
+            Lb.conv3x3_wgrad_cat(d["xa"], d["xb"], d["cat_a"], d["dy"], d["dw"], d["db"], L.N,
+                                 L.Cin, L.Cout, L.H, L.W, wl.ws, wl.ws_bytes, Lb.PATH_AUTO,
+                                 stream_handle)
+        else:
+            Lb.conv3x3_wgrad(d["x"], d["dy"], d["dw"], d["db"], L.N, L.Cin, L.Cout, L.H, L.W, wl.ws,
+                             wl.ws_bytes, stream_handle)
         if record is not None:
             record("wgrad", i, 1)
         n += 3  # dgrad: 1 kernel; wgrad: partial-sum kernel + fixed-order reduction
@@ -286,7 +333,8 @@ def cuda_arm(args):
 
     layers = synth.CONFIGS[args.workload]
     peaks = load_peaks()
-    wl = Workload(layers, args.seed, device, keep_host=not args.no_e2e, fused_act=args.fused_act)
+    wl = Workload(layers, args.seed, device, keep_host=not args.no_e2e, fused_act=args.fused_act,
+                  concat_free=args.concat_free)
     stream = torch.cuda.Stream(device=device)
     sh = stream.cuda_stream
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -381,7 +429,7 @@ def cuda_arm(args):
         def e2e_step():
             with torch.cuda.stream(stream):
                 for h, d in zip(wl.host, wl.dev):
-                    for k in wl.inputs():
+                    for k in wl.inputs(h):
                         d[k].copy_(h[k], non_blocking=True)
                 run_step(wl, sh)
                 for h, d in zip(wl.host, wl.dev):
@@ -420,7 +468,8 @@ def cuda_arm(args):
                    "layout": "NHWC bf16 activations, KRSC bf16 weights, fp32 accumulate",
                    "l2": "flushed between steps (write of 2x L2)",
                    "flops_per_step": flops_step, "flops_per_step_padded_cin": flops_padded,
-                   "fused_act_backward": bool(args.fused_act)},
+                   "fused_act_backward": bool(args.fused_act),
+                   "concat_free_up_path": bool(args.concat_free)},
         "pct_of_roofline": round(roof_s / (ms * 1e-3), 4),
         "roofline": {"bound": "tensor", "kernel": {"fwd": "k_igemm (fwd)", "dgrad": "k_igemm (dgrad)",
                                                    "wgrad": "k_wgrad + k_wgrad_reduce"}[dom],
@@ -516,6 +565,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--detail", action="store_true", help="add a per-layer breakdown")
+    ap.add_argument("--concat-free", action="store_true",
+                    help="up-path convs take main and skip as two tensors (no concat buffer)")
     ap.add_argument("--fused-act", action="store_true",
                     help="training-step variant: forwards also store z, dgrads take the input's "
                          "pre-activation and return the gradient through its activation")

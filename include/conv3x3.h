@@ -195,6 +195,41 @@ int conv3x3_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
 int conv3x3_wgrad_noalloc(const void* x, const void* dy, float* dw, float* dbias,
                           int N, int Cin, int Cout, int H, int W, void* stream);
 
+/* Convolution of a channel-concatenated input without the concatenation.
+ * A UNet (the architecture of the subject page, clu0's C++/CUDA UNet diffusion,
+ * sourcepulse.org project page, "How It Works") feeds each up-path conv the
+ * concatenation of its main branch and a skip from the down path.  These calls
+ * take the two parts as separate tensors, so the concatenated copy is never
+ * built (forward, weight gradient) and the input gradient comes back already
+ * split (dgrad).  The results are those of the plain calls on
+ * x = concat(xa, xb) along channels:
+ *   xa [N][H][W][Ca], xb [N][H][W][Cin - Ca], both bf16, 16-byte aligned;
+ *   w [Cout][3][3][Cin] (channels [0, Ca) act on xa, [Ca, Cin) on xb).
+ *   0 < Ca < Cin, Ca a multiple of 8 (and of 64 for the tensor-core path:
+ *   path = AUTO then falls back to the CUDA-core kernels, TENSOR returns
+ *   CONV3X3_ERR_UNSUPPORTED).
+ * conv3x3_fwd_cat:   as conv3x3_fwd_save_z; z may be NULL (no z stored).
+ * conv3x3_dgrad_cat: dxa [N][H][W][Ca] and dxb [N][H][W][Cin - Ca] receive the
+ *   two parts of dx (they must not overlap).  With act_in != NONE each part is
+ *   scaled by act_in' of its pre-activation (za_in / zb_in, laid out like
+ *   dxa / dxb), as conv3x3_dgrad_act does; with NONE both z pointers are ignored.
+ * conv3x3_wgrad_cat: as conv3x3_wgrad_ex; the workspace size comes from
+ *   conv3x3_wgrad_cat_workspace_bytes (0 for invalid arguments).
+ * Errors as the plain calls, and CONV3X3_ERR_INVALID_ARG for a bad Ca, a
+ * missing or misaligned part, or overlapping outputs. */
+int conv3x3_fwd_cat(const void* xa, const void* xb, int Ca, const void* w, const float* bias,
+                    void* y, void* z, int N, int Cin, int Cout, int H, int W, int act,
+                    int out_dtype, int path, void* stream);
+int conv3x3_dgrad_cat(const void* dy, const void* w, void* dxa, void* dxb, int Ca,
+                      const void* za_in, const void* zb_in, int act_in,
+                      int N, int Cin, int Cout, int H, int W, int out_dtype, int path,
+                      void* stream);
+int conv3x3_wgrad_cat(const void* xa, const void* xb, int Ca, const void* dy, float* dw,
+                      float* dbias, int N, int Cin, int Cout, int H, int W,
+                      void* workspace, size_t workspace_bytes, int path, void* stream);
+size_t conv3x3_wgrad_cat_workspace_bytes(int N, int Cin, int Ca, int Cout, int H, int W,
+                                         int path);
+
 /* Static description of a status code ("ok", "invalid argument", ...). */
 const char* conv3x3_status_string(int status);
 

@@ -182,6 +182,40 @@ def conv3x3_dgrad_act_at(dz, w, zin, act: int, idx):
     return out
 
 
+# ---------------------------------------------------------------------------
+# channel-concatenated input: x = concat(xa, xb) along channels (a UNet up-path
+# conv reads its main branch and its skip this way).  The definition is the
+# plain convolution of the concatenated tensor; the weight's channels [0, Ca)
+# act on xa and [Ca, Ca + Cb) on xb.
+# ---------------------------------------------------------------------------
+def _cat(xa, xb):
+    xa, xb = _d(xa), _d(xb)
+    assert xa.shape[:3] == xb.shape[:3], (xa.shape, xb.shape)
+    return np.concatenate([xa, xb], axis=-1)
+
+
+def conv3x3_fwd_cat(xa, xb, w, bias=None, act: int = 0):
+    return conv3x3_fwd(_cat(xa, xb), w, bias, act)
+
+
+def conv3x3_fwd_cat_at(xa, xb, w, bias, act, idx):
+    return conv3x3_fwd_at(_cat(xa, xb), w, bias, act, idx)
+
+
+def conv3x3_dgrad_cat(dz, w, Ca: int):
+    """(dxa, dxb): the input gradient split at channel Ca."""
+    dx = conv3x3_dgrad(dz, w)
+    return np.ascontiguousarray(dx[..., :Ca]), np.ascontiguousarray(dx[..., Ca:])
+
+
+def conv3x3_wgrad_cat(xa, xb, dz):
+    return conv3x3_wgrad(_cat(xa, xb), dz)
+
+
+def conv3x3_wgrad_cat_at(xa, xb, dz, idx):
+    return conv3x3_wgrad_at(_cat(xa, xb), dz, idx)
+
+
 def conv3x3_wgrad(x, dz):
     """(dw[k,r,s,c], db[k]) = (sum_p dz[p,k] x[p+(r-1,s-1),c], sum_p dz[p,k])."""
     x = _d(x)

@@ -92,6 +92,7 @@ class Layer:
     act: int = 1      # 0 none, 1 SiLU (fwd epilogue)
     cin_real: int = 0  # channels that carry data (stem: 3); 0 means Cin
     dtype: str = "bf16"
+    cat_a: int = 0     # up-path conv1: x = concat(main, skip) and main has cat_a channels; 0 = one tensor
 
     @property
     def P(self) -> int:
@@ -182,7 +183,7 @@ def unet_stack(N: int = 64, base: int = 128, mult=(1, 2, 3, 4), res0: int = 64,
         c, r = base * mult[l], res0 >> l
         for b in range(blocks):
             s = skips.pop()
-            layers.append(Layer(f"up{l}.rb{b}.conv1", N, main + s, c, r, r))
+            layers.append(Layer(f"up{l}.rb{b}.conv1", N, main + s, c, r, r, cat_a=main))
             layers.append(Layer(f"up{l}.rb{b}.conv2", N, c, c, r, r))
             main = c
     return layers

@@ -116,6 +116,39 @@ def test_fused_activation_entry_points_validate_without_a_gpu(lib):
     assert lib.conv3x3_dgrad_act(None, ALIGNED, None, 0, ALIGNED, *a, 0, 0, None) == 1
 
 
+def test_concat_free_entry_points_validate_without_a_gpu(lib):
+    N, Cin, Cout, H, W = 2, 128, 64, 8, 8
+    far = ALIGNED + (1 << 24)
+    sh = (N, Cin, Cout, H, W)
+    # bad split points, missing or misaligned second part
+    for ca in (0, Cin, -8, 12):
+        assert lib.conv3x3_fwd_cat(ALIGNED, far, ca, ALIGNED, None, ALIGNED, None, *sh, 1, 0, 0,
+                                   None) == 1, ca
+        assert lib.conv3x3_wgrad_cat(ALIGNED, far, ca, ALIGNED, ALIGNED, None, *sh, ALIGNED,
+                                     1 << 30, 0, None) == 1, ca
+        assert lib.conv3x3_wgrad_cat_workspace_bytes(N, Cin, ca, Cout, H, W, 0) == 0, ca
+    assert lib.conv3x3_fwd_cat(ALIGNED, None, 64, ALIGNED, None, ALIGNED, None, *sh, 1, 0, 0,
+                               None) == 1
+    assert lib.conv3x3_fwd_cat(ALIGNED, far + 8, 64, ALIGNED, None, ALIGNED, None, *sh, 1, 0, 0,
+                               None) == 1
+    # z overlapping y
+    assert lib.conv3x3_fwd_cat(ALIGNED, far, 64, ALIGNED, None, far + 4096, far + 4096 + 16, *sh,
+                               1, 0, 0, None) == 1
+    # dgrad: the two output parts overlap; z parts missing with an activation
+    assert lib.conv3x3_dgrad_cat(ALIGNED, ALIGNED, far, far + 64, 64, None, None, 0, *sh, 0, 0,
+                                 None) == 1
+    assert lib.conv3x3_dgrad_cat(ALIGNED, ALIGNED, far, far + (1 << 22), 64, None, None, 1, *sh, 0,
+                                 0, None) == 1
+    assert lib.conv3x3_dgrad_cat(ALIGNED, ALIGNED, far, far + (1 << 22), 64, ALIGNED, ALIGNED, 5,
+                                 *sh, 0, 0, None) == 1
+    # a split that is not a whole 64-channel chunk cannot be forced onto the tensor cores
+    assert lib.conv3x3_wgrad_cat_workspace_bytes(N, Cin, 32, Cout, H, W, 1) == 0
+    assert lib.conv3x3_wgrad_cat_workspace_bytes(N, Cin, 32, Cout, H, W, 0) > 0
+    # a tensor-core split needs the same scratch as the unsplit call
+    assert (lib.conv3x3_wgrad_cat_workspace_bytes(N, Cin, 64, Cout, H, W, 0)
+            == lib.conv3x3_wgrad_workspace_bytes(N, Cin, Cout, H, W))
+
+
 def test_workspace_size_depends_only_on_shape(lib):
     from synth import STACK, STEM, L1, L2, L3
     for L in [STEM, L1, L2, L3] + STACK:

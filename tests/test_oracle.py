@@ -193,6 +193,30 @@ def test_dgrad_through_activation_by_torch_autograd():
                            zt.grad.permute(0, 2, 3, 1).numpy(), rtol=1e-12, atol=1e-13)
 
 
+def test_concatenated_input_splits_into_two_convolutions():
+    # conv over concat(xa, xb) = conv(xa, w[..., :Ca]) + conv(xb, w[..., Ca:]) (linearity in x);
+    # dgrad's channel c and wgrad's channel c involve only w[..., c] and x[..., c]
+    N, H, W, Ca, Cb, Cout = 2, 5, 4, 3, 2, 4
+    xa, xb = rand(N, H, W, Ca), rand(N, H, W, Cb)
+    w, b, dz = rand(Cout, 3, 3, Ca + Cb), rand(Cout), rand(N, H, W, Cout)
+    y = oracle.conv3x3_fwd_cat(xa, xb, w, b)
+    ya = oracle.conv3x3_fwd(xa, np.ascontiguousarray(w[..., :Ca]), b)
+    yb = oracle.conv3x3_fwd(xb, np.ascontiguousarray(w[..., Ca:]))
+    assert np.allclose(y, ya + yb, rtol=1e-12, atol=1e-12)
+    dxa, dxb = oracle.conv3x3_dgrad_cat(dz, w, Ca)
+    assert np.array_equal(dxa, oracle.conv3x3_dgrad(dz, np.ascontiguousarray(w[..., :Ca])))
+    assert np.array_equal(dxb, oracle.conv3x3_dgrad(dz, np.ascontiguousarray(w[..., Ca:])))
+    dw, db = oracle.conv3x3_wgrad_cat(xa, xb, dz)
+    dwa, dba = oracle.conv3x3_wgrad(xa, dz)
+    dwb, _ = oracle.conv3x3_wgrad(xb, dz)
+    assert np.array_equal(dw[..., :Ca], dwa) and np.array_equal(dw[..., Ca:], dwb)
+    assert np.array_equal(db, dba)
+    idx = np.arange(0, y.size, 7)
+    assert np.array_equal(oracle.conv3x3_fwd_cat_at(xa, xb, w, b, 0, idx), y.reshape(-1)[idx])
+    iw = np.arange(0, dw.size, 5)
+    assert np.array_equal(oracle.conv3x3_wgrad_cat_at(xa, xb, dz, iw), dw.reshape(-1)[iw])
+
+
 # ---------------------------------------------------------------------------
 # identities
 # ---------------------------------------------------------------------------

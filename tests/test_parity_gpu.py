@@ -389,3 +389,105 @@ def test_fused_activation_backward_full_size_sampled():
 def test_full_unet_stack_sampled():
     for i, Lr in enumerate(synth.UNET_STEP):
         _sampled_layer_check(Lr, seed=0, index=i, n_rand=1024, n_dw=64, whole_images=False)
+
+
+# ---------------------------------------------------------------------------
+# channel-concatenated input passed as two tensors (UNet up-path convs)
+# ---------------------------------------------------------------------------
+CAT_SHAPES = [
+    # N, Ca, Cb, Cout, H, W
+    (2, 64, 64, 64, 9, 9),
+    (1, 128, 72, 200, 6, 11),   # ragged second part and N tiles
+    (2, 256, 128, 128, 8, 8),
+    (1, 64, 192, 96, 5, 7),
+    (2, 24, 40, 64, 6, 6),      # Ca not a whole 64-channel chunk: CUDA-core kernels only
+]
+
+
+def _cat_case(shape, seed=11):
+    N, Ca, Cb, Cout, H, W = shape
+    t = _small((N, Ca + Cb, Cout, H, W), seed=seed)
+    zin = synth.make_zin(t.layer, seed=seed)
+    return t, zin, Ca
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("shape", CAT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_concat_free_convs(shape, path):
+    p = PATHS[path]
+    N, Ca, Cb, Cout, H, W = shape
+    Cin = Ca + Cb
+    t, zin_h, _ = _cat_case(shape)
+    x, w, b, dy = dev_tensors(t)
+    xa, xb = x[..., :Ca].contiguous(), x[..., Ca:].contiguous()
+    if p == L.PATH_TENSOR and Ca % 64:
+        with pytest.raises(L.Conv3x3Error) as e:
+            ops.fwd_cat(xa, xb, w, b, act=1, path=p)
+        assert e.value.status == L.ERR_UNSUPPORTED
+        return
+    # forward: equals the oracle on the concatenation, and the plain kernel on
+    # the materialised concatenation bit for bit (same tiles, same K order)
+    z = torch.empty((N, H, W, Cout), dtype=torch.bfloat16, device="cuda")
+    y32 = ops.fwd_cat(xa, xb, w, b, act=1, out_dtype=L.DT_F32, path=p, z_out=z)
+    y32_plain = ops.fwd(x, w, b, act=1, out_dtype=L.DT_F32, path=p)
+    z_plain = ops.fwd(x, w, b, act=0, path=p)
+    torch.cuda.synchronize()
+    ta, tb = t.x[..., :Ca], t.x[..., Ca:]
+    assert rel_err(host(y32), oracle.conv3x3_fwd_cat(ta, tb, t.w, t.bias, 1)) <= TOL_BF16
+    assert torch.equal(y32, y32_plain)
+    assert torch.equal(z, z_plain)
+    # input gradient, split; plain and through the activation
+    dxa, dxb = ops.dgrad_cat(dy, w, Ca, out_dtype=L.DT_F32, path=p)
+    dx_plain = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=p)
+    torch.cuda.synchronize()
+    ra, rb = oracle.conv3x3_dgrad_cat(t.dy, t.w, Ca)
+    scale = max(np.max(np.abs(ra)), np.max(np.abs(rb)))
+    assert np.max(np.abs(host(dxa) - ra)) / scale <= TOL_BF16
+    assert np.max(np.abs(host(dxb) - rb)) / scale <= TOL_BF16
+    assert torch.equal(dxa, dx_plain[..., :Ca]) and torch.equal(dxb, dx_plain[..., Ca:])
+    zin = to_dev_bf16(zin_h)
+    za, zb = zin[..., :Ca].contiguous(), zin[..., Ca:].contiguous()
+    gxa, gxb = ops.dgrad_cat(dy, w, Ca, path=p, za_in=za, zb_in=zb, act_in=1)
+    gx_plain = ops.dgrad(dy, w, path=p, z_in=zin, act_in=1)
+    torch.cuda.synchronize()
+    assert torch.equal(gxa, gx_plain[..., :Ca]) and torch.equal(gxb, gx_plain[..., Ca:])
+    ref = oracle.conv3x3_dgrad_act(t.dy, t.w, zin_h, 1)
+    assert check_bf16_store(np.concatenate([host(gxa), host(gxb)], axis=-1), ref) == 0
+    # weight gradient: oracle, and bit-identical to the plain call on the concatenation
+    dw, db = ops.wgrad_cat(xa, xb, dy, path=p)
+    dw_plain, db_plain = ops.wgrad(x, dy, path=p)
+    torch.cuda.synchronize()
+    rdw, rdb = oracle.conv3x3_wgrad_cat(ta, tb, t.dy)
+    assert rel_err(host(dw), rdw) <= TOL_BF16
+    assert rel_err(host(db), rdb) <= TOL_BF16
+    assert torch.equal(dw, dw_plain) and torch.equal(db, db_plain)
+
+
+def test_concat_free_up_path_layer_full_size_sampled():
+    # up1.rb0.conv1 of the UNet: main 384 + skip 256 channels at 32x32, batch 64
+    i, Lr = next((i, Lr) for i, Lr in enumerate(synth.UNET_STEP) if Lr.name == "up1.rb0.conv1")
+    Ca = Lr.cat_a
+    assert Ca == 384
+    t = synth.make_tensors(Lr, seed=0, index=i)
+    x, w, b, dy = dev_tensors(t)
+    xa, xb = x[..., :Ca].contiguous(), x[..., Ca:].contiguous()
+    del x
+    y32 = ops.fwd_cat(xa, xb, w, b, act=Lr.act, out_dtype=L.DT_F32)
+    dxa, dxb = ops.dgrad_cat(dy, w, Ca, out_dtype=L.DT_F32)
+    dw, db = ops.wgrad_cat(xa, xb, dy)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    ta, tb = t.x[..., :Ca], t.x[..., Ca:]
+    yh = host(y32).reshape(-1)
+    iy = rng.integers(0, yh.size, 2048)
+    ry = oracle.conv3x3_fwd_cat_at(ta, tb, t.w, t.bias, Lr.act, iy)
+    assert np.max(np.abs(yh[iy] - ry)) / np.max(np.abs(ry)) <= TOL_BF16
+    dxh = np.concatenate([host(dxa), host(dxb)], axis=-1).reshape(-1)
+    ix = rng.integers(0, dxh.size, 2048)
+    rx = oracle.conv3x3_dgrad_at(t.dy, t.w, ix)
+    assert np.max(np.abs(dxh[ix] - rx)) / np.max(np.abs(rx)) <= TOL_BF16
+    dwh = host(dw).reshape(-1)
+    iw = rng.integers(0, dwh.size, 64)
+    rw = oracle.conv3x3_wgrad_cat_at(ta, tb, t.dy, iw)
+    assert np.max(np.abs(dwh[iw] - rw)) / np.max(np.abs(rw)) <= TOL_BF16
+    assert rel_err(host(db), oracle.conv3x3_dbias(t.dy)) <= TOL_BF16

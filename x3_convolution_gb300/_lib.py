@@ -42,6 +42,10 @@ _SIGS = {
     "conv3x3_wgrad_noalloc": ([_vp, _vp, _vp, _vp] + [_i] * 5 + [_vp], _i),
     "conv3x3_fwd_save_z": ([_vp, _vp, _vp, _vp, _vp] + [_i] * 8 + [_vp], _i),
     "conv3x3_dgrad_act": ([_vp, _vp, _vp, _i, _vp] + [_i] * 7 + [_vp], _i),
+    "conv3x3_fwd_cat": ([_vp, _vp, _i, _vp, _vp, _vp, _vp] + [_i] * 8 + [_vp], _i),
+    "conv3x3_dgrad_cat": ([_vp, _vp, _vp, _vp, _i, _vp, _vp, _i] + [_i] * 7 + [_vp], _i),
+    "conv3x3_wgrad_cat": ([_vp, _vp, _i, _vp, _vp, _vp] + [_i] * 5 + [_vp, _sz, _i, _vp], _i),
+    "conv3x3_wgrad_cat_workspace_bytes": ([_i] * 7, _sz),
 }
 
 WGRAD_NOALLOC_MAX_BYTES = 64 << 20
@@ -137,6 +141,31 @@ def conv3x3_dgrad_act(dy, w, z_in, act_in, dx, N, Cin, Cout, H, W, out_dtype, pa
     return _check(load().conv3x3_dgrad_act(_p(dy), _p(w), _p(z_in), act_in, _p(dx), N, Cin, Cout,
                                            H, W, out_dtype, path, _stream(stream)),
                   "conv3x3_dgrad_act")
+
+
+def conv3x3_fwd_cat(xa, xb, Ca, w, bias, y, z, N, Cin, Cout, H, W, act, out_dtype, path,
+                    stream=None):
+    return _check(load().conv3x3_fwd_cat(_p(xa), _p(xb), Ca, _p(w), _p(bias), _p(y), _p(z), N, Cin,
+                                         Cout, H, W, act, out_dtype, path, _stream(stream)),
+                  "conv3x3_fwd_cat")
+
+
+def conv3x3_dgrad_cat(dy, w, dxa, dxb, Ca, za_in, zb_in, act_in, N, Cin, Cout, H, W, out_dtype,
+                      path, stream=None):
+    return _check(load().conv3x3_dgrad_cat(_p(dy), _p(w), _p(dxa), _p(dxb), Ca, _p(za_in),
+                                           _p(zb_in), act_in, N, Cin, Cout, H, W, out_dtype, path,
+                                           _stream(stream)), "conv3x3_dgrad_cat")
+
+
+def conv3x3_wgrad_cat(xa, xb, Ca, dy, dw, dbias, N, Cin, Cout, H, W, workspace, workspace_bytes,
+                      path, stream=None):
+    return _check(load().conv3x3_wgrad_cat(_p(xa), _p(xb), Ca, _p(dy), _p(dw), _p(dbias), N, Cin,
+                                           Cout, H, W, _p(workspace), int(workspace_bytes), path,
+                                           _stream(stream)), "conv3x3_wgrad_cat")
+
+
+def conv3x3_wgrad_cat_workspace_bytes(N, Cin, Ca, Cout, H, W, path) -> int:
+    return int(load().conv3x3_wgrad_cat_workspace_bytes(N, Cin, Ca, Cout, H, W, path))
 
 
 def conv3x3_wgrad_ex(x, dy, dw, dbias, N, Cin, Cout, H, W, workspace, workspace_bytes, path,

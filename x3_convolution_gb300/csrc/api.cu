@@ -98,10 +98,11 @@ int check_shape(int N, int Cin, int Cout, int H, int W, bool need8) {
   return CONV3X3_OK;
 }
 
-int choose_path(int pass, const Shape& s, int path) {
+int choose_path(int pass, const Shape& s, int path, const CatSplit& cat = CatSplit{}) {
+  const bool tc = tc_supported(pass, s) && tc_supports_cat(s, cat);
   if (path == CONV3X3_PATH_SIMT) return CONV3X3_PATH_SIMT;
-  if (path == CONV3X3_PATH_TENSOR) return tc_supported(pass, s) ? CONV3X3_PATH_TENSOR : -1;
-  return tc_supported(pass, s) ? CONV3X3_PATH_TENSOR : CONV3X3_PATH_SIMT;
+  if (path == CONV3X3_PATH_TENSOR) return tc ? CONV3X3_PATH_TENSOR : -1;
+  return tc ? CONV3X3_PATH_TENSOR : CONV3X3_PATH_SIMT;
 }
 
 inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
@@ -145,8 +146,14 @@ bool overlap(const void* a, long long abytes, const void* b, long long bbytes) {
   return pa < pb + (uintptr_t)bbytes && pb < pa + (uintptr_t)abytes;
 }
 
+// A channel split: 0 < Ca < Cin, Ca a multiple of 8, second part 16-byte aligned.
+bool cat_ok(const CatSplit& cat, int Cin) {
+  return !cat.on() || (cat.Ca > 0 && cat.Ca < Cin && cat.Ca % 8 == 0 && aligned16(cat.b));
+}
+
 int fwd_impl(const void* x, const void* w, const float* bias, void* y, int N, int Cin, int Cout,
-             int H, int W, int act, int out_dtype, int path, const EpiExtra& ex, void* stream) {
+             int H, int W, int act, int out_dtype, int path, const EpiExtra& ex,
+             const CatSplit& cat, void* stream) {
   int rc = check_shape(N, Cin, Cout, H, W, true);
   if (rc) return rc;
   if (!x || !w || !y || !aligned16(x) || !aligned16(w) || !aligned16(y)) return CONV3X3_ERR_INVALID_ARG;
@@ -154,31 +161,68 @@ int fwd_impl(const void* x, const void* w, const float* bias, void* y, int N, in
   if (act < CONV3X3_ACT_NONE || act > CONV3X3_ACT_LRELU) return CONV3X3_ERR_INVALID_ARG;
   if (out_dtype != CONV3X3_DT_BF16 && out_dtype != CONV3X3_DT_F32) return CONV3X3_ERR_INVALID_ARG;
   if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return CONV3X3_ERR_INVALID_ARG;
+  if (!cat_ok(cat, Cin)) return CONV3X3_ERR_INVALID_ARG;
   Shape s{N, Cin, Cout, H, W};
-  int p = choose_path(0, s, path);
+  int p = choose_path(0, s, path, cat);
   if (p < 0) return CONV3X3_ERR_UNSUPPORTED;
   const int of32 = out_dtype == CONV3X3_DT_F32;
-  if (p == CONV3X3_PATH_SIMT) return simt_fwd_bf16(x, w, bias, y, s, act, of32, ex, as_stream(stream));
+  if (p == CONV3X3_PATH_SIMT)
+    return simt_fwd_bf16(x, w, bias, y, s, act, of32, ex, cat, as_stream(stream));
   DevCtx d;
   if ((rc = get_ctx(&d))) return rc;
-  return tc_fwd(x, w, bias, y, s, act, of32, ex, d, as_stream(stream));
+  return tc_fwd(x, w, bias, y, s, act, of32, ex, cat, d, as_stream(stream));
 }
 
 int dgrad_impl(const void* dy, const void* w, void* dx, int N, int Cin, int Cout, int H, int W,
-               int out_dtype, int path, const EpiExtra& ex, void* stream) {
+               int out_dtype, int path, const EpiExtra& ex, const CatSplit& cat, void* stream) {
   int rc = check_shape(N, Cin, Cout, H, W, true);
   if (rc) return rc;
   if (!dy || !w || !dx || !aligned16(dy) || !aligned16(w) || !aligned16(dx)) return CONV3X3_ERR_INVALID_ARG;
   if (out_dtype != CONV3X3_DT_BF16 && out_dtype != CONV3X3_DT_F32) return CONV3X3_ERR_INVALID_ARG;
   if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return CONV3X3_ERR_INVALID_ARG;
+  if (!cat_ok(cat, Cin)) return CONV3X3_ERR_INVALID_ARG;
   Shape s{N, Cin, Cout, H, W};
-  int p = choose_path(1, s, path);
+  int p = choose_path(1, s, path, cat);
   if (p < 0) return CONV3X3_ERR_UNSUPPORTED;
   const int of32 = out_dtype == CONV3X3_DT_F32;
-  if (p == CONV3X3_PATH_SIMT) return simt_dgrad_bf16(dy, w, dx, s, of32, ex, as_stream(stream));
+  if (p == CONV3X3_PATH_SIMT)
+    return simt_dgrad_bf16(dy, w, dx, s, of32, ex, cat, as_stream(stream));
   DevCtx d;
   if ((rc = get_ctx(&d))) return rc;
-  return tc_dgrad(dy, w, dx, s, of32, ex, d, as_stream(stream));
+  return tc_dgrad(dy, w, dx, s, of32, ex, cat, d, as_stream(stream));
+}
+
+size_t wgrad_ws_impl(int N, int Cin, int Cout, int H, int W, int path, const CatSplit& cat) {
+  if (check_shape(N, Cin, Cout, H, W, true) != CONV3X3_OK) return 0;
+  if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return 0;
+  if (cat.Ca != 0 && (cat.Ca < 0 || cat.Ca >= Cin || cat.Ca % 8 != 0)) return 0;
+  Shape s{N, Cin, Cout, H, W};
+  int p = choose_path(2, s, path, cat);
+  if (p < 0) return 0;
+  return p == CONV3X3_PATH_SIMT ? simt_wgrad_workspace(s, 0) : tc_wgrad_workspace(s, 0);
+}
+
+int wgrad_impl(const void* x, const void* dy, float* dw, float* dbias, int N, int Cin, int Cout,
+               int H, int W, void* workspace, size_t workspace_bytes, int path,
+               const CatSplit& cat, void* stream) {
+  int rc = check_shape(N, Cin, Cout, H, W, true);
+  if (rc) return rc;
+  if (!x || !dy || !dw || !aligned16(x) || !aligned16(dy) || !aligned16(dw)) return CONV3X3_ERR_INVALID_ARG;
+  if (dbias && !aligned4(dbias)) return CONV3X3_ERR_INVALID_ARG;
+  if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return CONV3X3_ERR_INVALID_ARG;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return CONV3X3_ERR_INVALID_ARG;
+  if (!cat_ok(cat, Cin)) return CONV3X3_ERR_INVALID_ARG;
+  Shape s{N, Cin, Cout, H, W};
+  int p = choose_path(2, s, path, cat);
+  if (p < 0) return CONV3X3_ERR_UNSUPPORTED;
+  size_t need = p == CONV3X3_PATH_SIMT ? simt_wgrad_workspace(s, 0) : tc_wgrad_workspace(s, 0);
+  if (need && (!workspace || workspace_bytes < need)) return CONV3X3_ERR_WORKSPACE;
+  if (p == CONV3X3_PATH_SIMT)
+    return simt_wgrad_bf16(x, dy, dw, dbias, s, workspace, workspace_bytes, 0, cat,
+                           as_stream(stream));
+  DevCtx d;
+  if ((rc = get_ctx(&d))) return rc;
+  return tc_wgrad(x, dy, dw, dbias, s, workspace, workspace_bytes, cat, d, as_stream(stream));
 }
 
 }  // namespace
@@ -209,7 +253,8 @@ int conv3x3_auto_path(int pass, int N, int Cin, int Cout, int H, int W) {
 
 int conv3x3_fwd_ex(const void* x, const void* w, const float* bias, void* y, int N, int Cin,
                    int Cout, int H, int W, int act, int out_dtype, int path, void* stream) {
-  return fwd_impl(x, w, bias, y, N, Cin, Cout, H, W, act, out_dtype, path, EpiExtra{}, stream);
+  return fwd_impl(x, w, bias, y, N, Cin, Cout, H, W, act, out_dtype, path, EpiExtra{}, CatSplit{},
+                  stream);
 }
 
 int conv3x3_fwd_save_z(const void* x, const void* w, const float* bias, void* y, void* z, int N,
@@ -222,7 +267,7 @@ int conv3x3_fwd_save_z(const void* x, const void* w, const float* bias, void* y,
     return CONV3X3_ERR_INVALID_ARG;
   EpiExtra ex;
   ex.zout = z;
-  return fwd_impl(x, w, bias, y, N, Cin, Cout, H, W, act, out_dtype, path, ex, stream);
+  return fwd_impl(x, w, bias, y, N, Cin, Cout, H, W, act, out_dtype, path, ex, CatSplit{}, stream);
 }
 
 int conv3x3_dgrad_act(const void* dy, const void* w, const void* z_in, int act_in, void* dx,
@@ -239,7 +284,7 @@ int conv3x3_dgrad_act(const void* dy, const void* w, const void* z_in, int act_i
     ex.zin = z_in;
     ex.zin_act = act_in;
   }
-  return dgrad_impl(dy, w, dx, N, Cin, Cout, H, W, out_dtype, path, ex, stream);
+  return dgrad_impl(dy, w, dx, N, Cin, Cout, H, W, out_dtype, path, ex, CatSplit{}, stream);
 }
 
 int conv3x3_fwd(const void* x, const void* w, const float* bias, void* y, int N, int Cin, int Cout,
@@ -250,7 +295,7 @@ int conv3x3_fwd(const void* x, const void* w, const float* bias, void* y, int N,
 
 int conv3x3_dgrad_ex(const void* dy, const void* w, void* dx, int N, int Cin, int Cout, int H,
                      int W, int out_dtype, int path, void* stream) {
-  return dgrad_impl(dy, w, dx, N, Cin, Cout, H, W, out_dtype, path, EpiExtra{}, stream);
+  return dgrad_impl(dy, w, dx, N, Cin, Cout, H, W, out_dtype, path, EpiExtra{}, CatSplit{}, stream);
 }
 
 int conv3x3_dgrad(const void* dy, const void* w, void* dx, int N, int Cin, int Cout, int H, int W,
@@ -259,12 +304,7 @@ int conv3x3_dgrad(const void* dy, const void* w, void* dx, int N, int Cin, int C
 }
 
 size_t conv3x3_wgrad_workspace_bytes_ex(int N, int Cin, int Cout, int H, int W, int path) {
-  if (check_shape(N, Cin, Cout, H, W, true) != CONV3X3_OK) return 0;
-  if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return 0;
-  Shape s{N, Cin, Cout, H, W};
-  int p = choose_path(2, s, path);
-  if (p < 0) return 0;
-  return p == CONV3X3_PATH_SIMT ? simt_wgrad_workspace(s, 0) : tc_wgrad_workspace(s, 0);
+  return wgrad_ws_impl(N, Cin, Cout, H, W, path, CatSplit{});
 }
 
 size_t conv3x3_wgrad_workspace_bytes(int N, int Cin, int Cout, int H, int W) {
@@ -274,22 +314,75 @@ size_t conv3x3_wgrad_workspace_bytes(int N, int Cin, int Cout, int H, int W) {
 int conv3x3_wgrad_ex(const void* x, const void* dy, float* dw, float* dbias, int N, int Cin,
                      int Cout, int H, int W, void* workspace, size_t workspace_bytes, int path,
                      void* stream) {
-  int rc = check_shape(N, Cin, Cout, H, W, true);
-  if (rc) return rc;
-  if (!x || !dy || !dw || !aligned16(x) || !aligned16(dy) || !aligned16(dw)) return CONV3X3_ERR_INVALID_ARG;
-  if (dbias && !aligned4(dbias)) return CONV3X3_ERR_INVALID_ARG;
-  if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return CONV3X3_ERR_INVALID_ARG;
-  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return CONV3X3_ERR_INVALID_ARG;
-  Shape s{N, Cin, Cout, H, W};
-  int p = choose_path(2, s, path);
-  if (p < 0) return CONV3X3_ERR_UNSUPPORTED;
-  size_t need = p == CONV3X3_PATH_SIMT ? simt_wgrad_workspace(s, 0) : tc_wgrad_workspace(s, 0);
-  if (need && (!workspace || workspace_bytes < need)) return CONV3X3_ERR_WORKSPACE;
-  if (p == CONV3X3_PATH_SIMT)
-    return simt_wgrad_bf16(x, dy, dw, dbias, s, workspace, workspace_bytes, 0, as_stream(stream));
-  DevCtx d;
-  if ((rc = get_ctx(&d))) return rc;
-  return tc_wgrad(x, dy, dw, dbias, s, workspace, workspace_bytes, d, as_stream(stream));
+  return wgrad_impl(x, dy, dw, dbias, N, Cin, Cout, H, W, workspace, workspace_bytes, path,
+                    CatSplit{}, stream);
+}
+
+int conv3x3_fwd_cat(const void* xa, const void* xb, int Ca, const void* w, const float* bias,
+                    void* y, void* z, int N, int Cin, int Cout, int H, int W, int act,
+                    int out_dtype, int path, void* stream) {
+  if (!xb || !y) return CONV3X3_ERR_INVALID_ARG;
+  if (check_shape(N, Cin, Cout, H, W, true) != CONV3X3_OK) return CONV3X3_ERR_INVALID_ARG;
+  EpiExtra ex;
+  if (z) {
+    if (!aligned16(z)) return CONV3X3_ERR_INVALID_ARG;
+    const long long elems = (long long)N * H * W * Cout;
+    if (overlap(z, elems * 2, y, elems * (out_dtype == CONV3X3_DT_F32 ? 4 : 2)))
+      return CONV3X3_ERR_INVALID_ARG;
+    ex.zout = z;
+  }
+  CatSplit cat;
+  cat.b = const_cast<void*>(xb);
+  cat.Ca = Ca;
+  return fwd_impl(xa, w, bias, y, N, Cin, Cout, H, W, act, out_dtype, path, ex, cat, stream);
+}
+
+int conv3x3_dgrad_cat(const void* dy, const void* w, void* dxa, void* dxb, int Ca,
+                      const void* za_in, const void* zb_in, int act_in, int N, int Cin, int Cout,
+                      int H, int W, int out_dtype, int path, void* stream) {
+  if (!dxa || !dxb) return CONV3X3_ERR_INVALID_ARG;
+  if (check_shape(N, Cin, Cout, H, W, true) != CONV3X3_OK) return CONV3X3_ERR_INVALID_ARG;
+  if (Ca <= 0 || Ca >= Cin || Ca % 8 != 0) return CONV3X3_ERR_INVALID_ARG;
+  if (act_in < CONV3X3_ACT_NONE || act_in > CONV3X3_ACT_LRELU) return CONV3X3_ERR_INVALID_ARG;
+  const long long P = (long long)N * H * W;
+  const int esz = out_dtype == CONV3X3_DT_F32 ? 4 : 2;
+  const long long ba = P * Ca * esz, bb = P * (Cin - Ca) * esz;
+  if (overlap(dxa, ba, dxb, bb)) return CONV3X3_ERR_INVALID_ARG;
+  EpiExtra ex;
+  if (act_in != CONV3X3_ACT_NONE) {
+    if (!za_in || !zb_in || !aligned16(za_in) || !aligned16(zb_in)) return CONV3X3_ERR_INVALID_ARG;
+    const long long za = P * Ca * 2, zb = P * (Cin - Ca) * 2;
+    if (overlap(za_in, za, dxa, ba) || overlap(za_in, za, dxb, bb) ||
+        overlap(zb_in, zb, dxa, ba) || overlap(zb_in, zb, dxb, bb))
+      return CONV3X3_ERR_INVALID_ARG;
+    ex.zin = za_in;
+    ex.zin_b = zb_in;
+    ex.zin_act = act_in;
+  }
+  CatSplit cat;
+  cat.b = dxb;
+  cat.Ca = Ca;
+  return dgrad_impl(dy, w, dxa, N, Cin, Cout, H, W, out_dtype, path, ex, cat, stream);
+}
+
+size_t conv3x3_wgrad_cat_workspace_bytes(int N, int Cin, int Ca, int Cout, int H, int W,
+                                         int path) {
+  if (Ca <= 0) return 0;
+  CatSplit cat;
+  cat.b = reinterpret_cast<void*>(uintptr_t(16));  // marks the split; never dereferenced
+  cat.Ca = Ca;
+  return wgrad_ws_impl(N, Cin, Cout, H, W, path, cat);
+}
+
+int conv3x3_wgrad_cat(const void* xa, const void* xb, int Ca, const void* dy, float* dw,
+                      float* dbias, int N, int Cin, int Cout, int H, int W, void* workspace,
+                      size_t workspace_bytes, int path, void* stream) {
+  if (!xb) return CONV3X3_ERR_INVALID_ARG;
+  CatSplit cat;
+  cat.b = const_cast<void*>(xb);
+  cat.Ca = Ca;
+  return wgrad_impl(xa, dy, dw, dbias, N, Cin, Cout, H, W, workspace, workspace_bytes, path, cat,
+                    stream);
 }
 
 int conv3x3_wgrad(const void* x, const void* dy, float* dw, float* dbias, int N, int Cin, int Cout,

@@ -31,7 +31,17 @@ struct DevCtx {
 struct EpiExtra {
   void* zout = nullptr;
   const void* zin = nullptr;
+  const void* zin_b = nullptr;  // z_in of channels [Ca, Cin) when the input is split (CatSplit)
   int zin_act = CONV3X3_ACT_NONE;
+};
+
+// A channel-split input (fwd, wgrad) or input gradient (dgrad): channels
+// [0, Ca) live in the primary tensor ([P][Ca]), channels [Ca, Cin) in `b`
+// ([P][Cin - Ca]).  b == nullptr: one tensor of Cin channels.
+struct CatSplit {
+  void* b = nullptr;
+  int Ca = 0;
+  bool on() const { return b != nullptr; }
 };
 
 // ---- CUDA-core kernels (simt.cu) ----
@@ -42,22 +52,23 @@ int simt_wgrad_f32(const float* x, const float* dy, float* dw, float* db, const 
                    cudaStream_t st);
 
 int simt_fwd_bf16(const void* x, const void* w, const float* bias, void* y, const Shape& s,
-                  int act, int out_f32, const EpiExtra& ex, cudaStream_t st);
+                  int act, int out_f32, const EpiExtra& ex, const CatSplit& cat, cudaStream_t st);
 int simt_dgrad_bf16(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
-                    const EpiExtra& ex, cudaStream_t st);
+                    const EpiExtra& ex, const CatSplit& cat, cudaStream_t st);
 size_t simt_wgrad_workspace(const Shape& s, int num_sms);
 int simt_wgrad_bf16(const void* x, const void* dy, float* dw, float* db, const Shape& s,
-                    void* ws, size_t ws_bytes, int num_sms, cudaStream_t st);
+                    void* ws, size_t ws_bytes, int num_sms, const CatSplit& cat, cudaStream_t st);
 
 // ---- tensor-core kernels (tc.cu) ----
 bool tc_supported(int pass, const Shape& s);
+bool tc_supports_cat(const Shape& s, const CatSplit& cat);
 int tc_fwd(const void* x, const void* w, const float* bias, void* y, const Shape& s, int act,
-           int out_f32, const EpiExtra& ex, const DevCtx& d, cudaStream_t st);
+           int out_f32, const EpiExtra& ex, const CatSplit& cat, const DevCtx& d, cudaStream_t st);
 int tc_dgrad(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
-             const EpiExtra& ex, const DevCtx& d, cudaStream_t st);
+             const EpiExtra& ex, const CatSplit& cat, const DevCtx& d, cudaStream_t st);
 size_t tc_wgrad_workspace(const Shape& s, int num_sms);
 int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s, void* ws,
-             size_t ws_bytes, const DevCtx& d, cudaStream_t st);
+             size_t ws_bytes, const CatSplit& cat, const DevCtx& d, cudaStream_t st);
 
 // ---- driver entry points (api.cu) ----
 typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,

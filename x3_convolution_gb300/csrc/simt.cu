@@ -211,10 +211,13 @@ __global__ void __launch_bounds__(kThreads) k_fwd_bf16_c8(
 }
 
 // forward, generic Cin (multiple of 8): one thread per (pixel, 8 output channels)
+// A channel-split input keeps channels [0, Ca) in x (row stride Ca) and
+// [Ca, Cin) in x2 (row stride Cin - Ca); Ca = Cin when there is no split.
 __global__ void __launch_bounds__(kThreads) k_fwd_bf16_gen(
-    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w,
-    const float* __restrict__ bias, void* __restrict__ y, __nv_bfloat16* __restrict__ zout, int N,
-    int H, int W, int Cin, int Cout, int act, int out_f32) {
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ x2, int Ca,
+    const __nv_bfloat16* __restrict__ w, const float* __restrict__ bias, void* __restrict__ y,
+    __nv_bfloat16* __restrict__ zout, int N, int H, int W, int Cin, int Cout, int act,
+    int out_f32) {
   const int KG = Cout / 8;
   const long long total = (long long)N * H * W * KG;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
@@ -228,10 +231,11 @@ __global__ void __launch_bounds__(kThreads) k_fwd_bf16_gen(
     for (int t = 0; t < 9; ++t) {
       int hi = hh + t / 3 - 1, wi = ww + t % 3 - 1;
       if (hi < 0 || hi >= H || wi < 0 || wi >= W) continue;
-      const __nv_bfloat16* xp = x + (p + (long long)(t / 3 - 1) * W + (t % 3 - 1)) * Cin;
+      const long long q = p + (long long)(t / 3 - 1) * W + (t % 3 - 1);
       for (int c0 = 0; c0 < Cin; c0 += 8) {
+        const __nv_bfloat16* xp = c0 < Ca ? x + q * Ca + c0 : x2 + q * (Cin - Ca) + (c0 - Ca);
         float xf[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(xp + c0)), xf);
+        unpack8(__ldg(reinterpret_cast<const uint4*>(xp)), xf);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           float wf[8];
@@ -299,10 +303,13 @@ __global__ void __launch_bounds__(kThreads) k_dgrad_bf16_c8(
 }
 
 // dgrad, generic Cin: one thread per (pixel, 8 input channels)
+// dx channels [0, Ca) go to dx (row stride Ca, z_in from zin), [Ca, Cin) to
+// dx2 (row stride Cin - Ca, z_in from zin2); Ca = Cin when there is no split.
 __global__ void __launch_bounds__(kThreads) k_dgrad_bf16_gen(
     const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ w,
-    void* __restrict__ dx, const __nv_bfloat16* __restrict__ zin, int zin_act, int N, int H, int W,
-    int Cin, int Cout, int out_f32) {
+    void* __restrict__ dx, void* __restrict__ dx2, int Ca, const __nv_bfloat16* __restrict__ zin,
+    const __nv_bfloat16* __restrict__ zin2, int zin_act, int N, int H, int W, int Cin, int Cout,
+    int out_f32) {
   const int CG = Cin / 8;
   const long long total = (long long)N * H * W * CG;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
@@ -330,8 +337,10 @@ __global__ void __launch_bounds__(kThreads) k_dgrad_bf16_gen(
         }
       }
     }
-    if (zin) scale_by_act_grad(acc, zin, p * Cin + c0, zin_act);
-    store8(dx, p * Cin + c0, acc, out_f32);
+    const bool second = c0 >= Ca;
+    const long long off = second ? p * (Cin - Ca) + (c0 - Ca) : p * Ca + c0;
+    if (zin) scale_by_act_grad(acc, second ? zin2 : zin, off, zin_act);
+    store8(second ? dx2 : dx, off, acc, out_f32);
   }
 }
 
@@ -340,8 +349,9 @@ __global__ void __launch_bounds__(kThreads) k_dgrad_bf16_gen(
 // dw[k][tap][c0..c0+8).  Threads with a block-wide index below Cout also sum
 // dbias.  partial layout: [S][Cout*9*Cin] followed by [S][Cout].
 __global__ void __launch_bounds__(kThreads) k_wgrad_bf16_partial(
-    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ dy,
-    float* __restrict__ part, int N, int H, int W, int Cin, int Cout, long long chunk, int S) {
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ x2, int Ca,
+    const __nv_bfloat16* __restrict__ dy, float* __restrict__ part, int N, int H, int W, int Cin,
+    int Cout, long long chunk, int S) {
   const int CG = Cin / 8;
   const long long E8 = (long long)Cout * 9 * CG;  // 8-wide output groups
   const long long P = (long long)N * H * W;
@@ -355,6 +365,9 @@ __global__ void __launch_bounds__(kThreads) k_wgrad_bf16_partial(
     int t = (int)((e / CG) % 9);
     int k = (int)(e / (9LL * CG));
     int r = t / 3, s = t % 3;
+    // channel-split input: this thread's 8 channels lie in one part
+    const __nv_bfloat16* xs = c0 < Ca ? x + c0 : x2 + (c0 - Ca);
+    const int xstride = c0 < Ca ? Ca : Cin - Ca;
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
@@ -364,7 +377,7 @@ __global__ void __launch_bounds__(kThreads) k_wgrad_bf16_partial(
       if (hi < 0 || hi >= H || wi < 0 || wi >= W) continue;
       float d = __bfloat162float(dy[p * Cout + k]);
       float xf[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(x + (p + (long long)(r - 1) * W + (s - 1)) * Cin + c0)), xf);
+      unpack8(__ldg(reinterpret_cast<const uint4*>(xs + (p + (long long)(r - 1) * W + (s - 1)) * xstride)), xf);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(d, xf[i], acc[i]);
     }
@@ -539,11 +552,11 @@ int simt_wgrad_f32(const float* x, const float* dy, float* dw, float* db, const 
 }
 
 int simt_fwd_bf16(const void* x, const void* w, const float* bias, void* y, const Shape& s,
-                  int act, int out_f32, const EpiExtra& ex, cudaStream_t st) {
+                  int act, int out_f32, const EpiExtra& ex, const CatSplit& cat, cudaStream_t st) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
   __nv_bfloat16* zb = static_cast<__nv_bfloat16*>(ex.zout);
-  if (s.Cin == 8 && s.Cout <= 512) {
+  if (s.Cin == 8 && s.Cout <= 512 && !cat.on()) {
     size_t sm = (size_t)s.Cout * 72 * sizeof(float);
     if (sm > 48 * 1024 &&
         cudaFuncSetAttribute(k_fwd_bf16_c8, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
@@ -553,17 +566,18 @@ int simt_fwd_bf16(const void* x, const void* w, const float* bias, void* y, cons
                                                          s.Cout, act, out_f32);
   } else {
     k_fwd_bf16_gen<<<grid_for(s.P() * (s.Cout / 8)), kThreads, 0, st>>>(
-        xb, wb, bias, y, zb, s.N, s.H, s.W, s.Cin, s.Cout, act, out_f32);
+        xb, static_cast<const __nv_bfloat16*>(cat.b), cat.on() ? cat.Ca : s.Cin, wb, bias, y, zb,
+        s.N, s.H, s.W, s.Cin, s.Cout, act, out_f32);
   }
   return launch_status();
 }
 
 int simt_dgrad_bf16(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
-                    const EpiExtra& ex, cudaStream_t st) {
+                    const EpiExtra& ex, const CatSplit& cat, cudaStream_t st) {
   const __nv_bfloat16* db = static_cast<const __nv_bfloat16*>(dy);
   const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
   const __nv_bfloat16* zb = static_cast<const __nv_bfloat16*>(ex.zin);
-  if (s.Cin == 8 && s.Cout <= 512) {
+  if (s.Cin == 8 && s.Cout <= 512 && !cat.on()) {
     size_t sm = (size_t)s.Cout * 72 * sizeof(float);
     if (sm > 48 * 1024 &&
         cudaFuncSetAttribute(k_dgrad_bf16_c8, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -573,7 +587,9 @@ int simt_dgrad_bf16(const void* dy, const void* w, void* dx, const Shape& s, int
                                                            s.W, s.Cout, out_f32);
   } else {
     k_dgrad_bf16_gen<<<grid_for(s.P() * (s.Cin / 8)), kThreads, 0, st>>>(
-        db, wb, dx, zb, ex.zin_act, s.N, s.H, s.W, s.Cin, s.Cout, out_f32);
+        db, wb, dx, cat.b, cat.on() ? cat.Ca : s.Cin, zb,
+        static_cast<const __nv_bfloat16*>(ex.zin_b), ex.zin_act, s.N, s.H, s.W, s.Cin, s.Cout,
+        out_f32);
   }
   return launch_status();
 }
@@ -585,7 +601,7 @@ size_t simt_wgrad_workspace(const Shape& s, int /*num_sms*/) {
 }
 
 int simt_wgrad_bf16(const void* x, const void* dy, float* dw, float* db, const Shape& s,
-                    void* ws, size_t ws_bytes, int num_sms, cudaStream_t st) {
+                    void* ws, size_t ws_bytes, int num_sms, const CatSplit& cat, cudaStream_t st) {
   if (ws_bytes < simt_wgrad_workspace(s, num_sms) || ws == nullptr) return CONV3X3_ERR_WORKSPACE;
   WgradPlan pl = wgrad_plan(s);
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
@@ -598,8 +614,9 @@ int simt_wgrad_bf16(const void* x, const void* dy, float* dw, float* db, const S
   } else {
     long long E8 = (long long)s.Cout * 9 * (s.Cin / 8);
     dim3 grid((unsigned)((E8 + kThreads - 1) / kThreads), pl.S);
-    k_wgrad_bf16_partial<<<grid, kThreads, 0, st>>>(xb, dyb, part, s.N, s.H, s.W, s.Cin, s.Cout,
-                                                    pl.chunk, pl.S);
+    k_wgrad_bf16_partial<<<grid, kThreads, 0, st>>>(
+        xb, static_cast<const __nv_bfloat16*>(cat.b), cat.on() ? cat.Ca : s.Cin, dyb, part, s.N,
+        s.H, s.W, s.Cin, s.Cout, pl.chunk, pl.S);
   }
   if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
   long long dwsize = (long long)s.Cout * 9 * s.Cin;

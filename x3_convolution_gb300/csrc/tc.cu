@@ -106,22 +106,42 @@ struct IgemmParams {
   const float* bias;
   int act, out_f32;
   int P, H, W;
-  int kchunks;   // ceil(A channels / 64)
-  int nout;      // output channels (Cout fwd, Cin dgrad)
+  int kchunks;    // ceil(A channels / 64)
+  int kchunks_a;  // forward, channel-split input: chunks [0, kchunks_a) come from tmA, the rest from tmA2
+  int nout;       // output channels (Cout fwd, Cin dgrad)
+  int nsplit;     // output columns [0, nsplit) go to out (row stride nsplit), [nsplit, nout) to out2
   int num_m_tiles, num_n_tiles;
   unsigned* status;
   unsigned long long wait_ns;
+  void* out2 = nullptr;
   // forward: also store z = conv + bias, rounded once to bf16, laid out like out
   __nv_bfloat16* zout = nullptr;
-  // dgrad: scale by act'(zin) (the input's pre-activation, laid out like out)
+  // dgrad: scale by act'(zin) (the input's pre-activation, split like the output)
   const __nv_bfloat16* zin = nullptr;
+  const __nv_bfloat16* zin2 = nullptr;
   int zin_act = CONV3X3_ACT_NONE;
 };
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* o, int col0, int nout, const float (&f)[32]) {
+// Where output column col0 of pixel `pix` lives.  Columns [0, nsplit) are in
+// the primary tensor (row stride nsplit); columns [nsplit, nout) -- the second
+// part of a channel-split input gradient -- in the second one (row stride
+// nout - nsplit).  nsplit is a multiple of 32, so a 32-column chunk never
+// straddles the two.  `lim` = columns left in that tensor's row from col0.
+struct OutPos {
+  long long off;
+  int lim;
+  bool second;
+};
+
+__device__ __forceinline__ OutPos out_pos(const IgemmParams& p, long long pix, int col0) {
+  if (col0 < p.nsplit) return OutPos{pix * p.nsplit + col0, p.nsplit - col0, false};
+  return OutPos{pix * (p.nout - p.nsplit) + (col0 - p.nsplit), p.nout - col0, true};
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* o, int lim, const float (&f)[32]) {
 #pragma unroll
   for (int g = 0; g < 4; ++g)
-    if (col0 + 8 * g < nout) {
+    if (8 * g < lim) {
       uint4 u;
       __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
@@ -134,21 +154,24 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* o, int col0, int no
 // accumulator so that their latency overlaps the TMEM load.
 __device__ __forceinline__ void load_zin(const IgemmParams& p, long long pix, int col0,
                                          uint4 (&zr)[4]) {
-  const __nv_bfloat16* zp = p.zin + pix * p.nout + col0;
+  const OutPos o = out_pos(p, pix, col0);
+  const __nv_bfloat16* zp = (o.second ? p.zin2 : p.zin) + o.off;
 #pragma unroll
   for (int g = 0; g < 4; ++g)
-    zr[g] = col0 + 8 * g < p.nout ? __ldg(reinterpret_cast<const uint4*>(zp + 8 * g))
-                                  : make_uint4(0u, 0u, 0u, 0u);
+    zr[g] = 8 * g < o.lim ? __ldg(reinterpret_cast<const uint4*>(zp + 8 * g))
+                          : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// L2 prefetch of one output row's z_in span [col0, col0 + ncols), issued while
-// the tile's MMAs still run.
+// L2 prefetch of one output row's z_in over columns [col0, col0 + ncols),
+// issued while the tile's MMAs still run: one prefetch at the start of each
+// 32-column chunk (an address that chunk itself reads).
 __device__ __forceinline__ void prefetch_zin_row(const IgemmParams& p, long long pix, int col0,
                                                  int ncols) {
-  const int n = min(ncols, p.nout - col0);
-  const char* base = reinterpret_cast<const char*>(p.zin + pix * p.nout + col0);
-  for (int b = 0; b < 2 * n; b += 128)
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(base + b));
+  const int end = min(col0 + ncols, p.nout);
+  for (int c = col0; c < end; c += 32) {
+    const OutPos o = out_pos(p, pix, c);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"((o.second ? p.zin2 : p.zin) + o.off));
+  }
 }
 
 __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix, int col0,
@@ -168,7 +191,7 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix,
       }
     }
   }
-  if (p.zout) store_bf16x32(p.zout + pix * p.nout + col0, col0, p.nout, f);
+  if (p.zout) store_bf16x32(p.zout + pix * p.nout + col0, p.nout - col0, f);
   if (p.act == CONV3X3_ACT_SILU) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) f[i] = silu_f32(f[i]);
@@ -188,16 +211,18 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix,
       }
     }
   }
+  const OutPos o = out_pos(p, pix, col0);
+  void* base = o.second ? p.out2 : p.out;
   if (p.out_f32) {
-    float* o = static_cast<float*>(p.out) + pix * p.nout + col0;
+    float* op = static_cast<float*>(base) + o.off;
 #pragma unroll
     for (int g = 0; g < 4; ++g)
-      if (col0 + 8 * g < p.nout) {
-        reinterpret_cast<float4*>(o + 8 * g)[0] = make_float4(f[8 * g], f[8 * g + 1], f[8 * g + 2], f[8 * g + 3]);
-        reinterpret_cast<float4*>(o + 8 * g)[1] = make_float4(f[8 * g + 4], f[8 * g + 5], f[8 * g + 6], f[8 * g + 7]);
+      if (8 * g < o.lim) {
+        reinterpret_cast<float4*>(op + 8 * g)[0] = make_float4(f[8 * g], f[8 * g + 1], f[8 * g + 2], f[8 * g + 3]);
+        reinterpret_cast<float4*>(op + 8 * g)[1] = make_float4(f[8 * g + 4], f[8 * g + 5], f[8 * g + 6], f[8 * g + 7]);
       }
   } else {
-    store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + pix * p.nout + col0, col0, p.nout, f);
+    store_bf16x32(static_cast<__nv_bfloat16*>(base) + o.off, o.lim, f);
   }
 }
 
@@ -213,8 +238,8 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix,
 // ----------------------------------------------------------------------------
 template <int BN, int MT, bool kDgrad>
 __global__ void __launch_bounds__(kIgemmThreads, 1)
-    k_igemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-            const IgemmParams p) {
+    k_igemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+            const __grid_constant__ CUtensorMap tmB, const IgemmParams p) {
   using Cfg = IgemmCfg<BN, MT>;
   constexpr int S = Cfg::kStages;
   constexpr int TM = BM * MT;  // pixels per CTA tile
@@ -249,6 +274,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
+    if (p.kchunks_a < p.kchunks) tma_prefetch_desc(&tmA2);
     tma_prefetch_desc(&tmB);
   }
   if (warp == kMmaWarp) {
@@ -309,7 +335,10 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
             for (int b = 0; b < kBoxes; ++b) {
               if (!kStageParallel && b % kProd != warp) continue;
               if (b < MT) {
-                tma_load_im2col_4d(sa + b * kABytes, &tmA, &full[stage], cc * BKC, cw[b], ch[b], cn[b],
+                // channel-split input: chunks past kchunks_a read the second tensor
+                const bool second = cc >= p.kchunks_a;
+                tma_load_im2col_4d(sa + b * kABytes, second ? &tmA2 : &tmA, &full[stage],
+                                   (second ? cc - p.kchunks_a : cc) * BKC, cw[b], ch[b], cn[b],
                                    (uint16_t)(tap % 3), (uint16_t)(tap / 3));
               } else {
                 const int j = b - MT;
@@ -920,6 +949,7 @@ constexpr size_t kWgSmem = (size_t)kWgStages * kWgStageBytes + 256 + 1024 + 8 * 
 struct WgradParams {
   float* part;  // [S][Cout][9*Cin] then [S][Cout]
   int P, H, W, Cin, Cout;
+  int ca;       // channel-split input: channels [0, ca) from tmX, [ca, Cin) from tmX2 (ca % 64 == 0)
   int kb_total, kb_per_split, S;
   int num_mb, num_cb;  // 128-wide blocks of Cout and Cin
   unsigned* status;
@@ -928,7 +958,7 @@ struct WgradParams {
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_wgrad(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmX,
-            const WgradParams p) {
+            const __grid_constant__ CUtensorMap tmX2, const WgradParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kWgStages * kWgStageBytes);
@@ -962,6 +992,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmDY);
     tma_prefetch_desc(&tmX);
+    if (p.ca < p.Cin) tma_prefetch_desc(&tmX2);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, kWgTmemCols);
@@ -1009,8 +1040,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d(sa + b * 8192, &tmDY, &full[stage], mb * 128 + b * 64, pk);
             } else {
               const int t = (b - 2) >> 1, j = (b - 2) & 1;
-              tma_load_im2col_4d(sb + (t * 2 + j) * 8192, &tmX, &full[stage], cb * 128 + j * 64,
-                                 w0 - 1, h0 - 1, n0, (uint16_t)t, (uint16_t)tr);
+              const int c = cb * 128 + j * 64;  // a 64-channel box lies in one part
+              const bool second = c >= p.ca;
+              tma_load_im2col_4d(sb + (t * 2 + j) * 8192, second ? &tmX2 : &tmX, &full[stage],
+                                 second ? c - p.ca : c, w0 - 1, h0 - 1, n0, (uint16_t)t, (uint16_t)tr);
             }
           }
         }
@@ -1398,14 +1431,14 @@ int set_smem(K kernel, size_t bytes, int device) {
 }
 
 template <int BN, int MT, bool kDgrad>
-int launch_igemm(const CUtensorMap& a, const CUtensorMap& b, const IgemmParams& prm,
-                 const DevCtx& d, cudaStream_t st) {
+int launch_igemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
+                 const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
   using Cfg = IgemmCfg<BN, MT>;
   auto kern = k_igemm<BN, MT, kDgrad>;
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
   const int grid = tiles < d.num_sms ? tiles : d.num_sms;
-  kern<<<grid, kIgemmThreads, Cfg::kSmem, st>>>(a, b, prm);
+  kern<<<grid, kIgemmThreads, Cfg::kSmem, st>>>(a, a2, b, prm);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
@@ -1503,7 +1536,9 @@ int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const
   prm.H = s.H;
   prm.W = s.W;
   prm.kchunks = 1;
+  prm.kchunks_a = 1;
   prm.nout = s.Cout;
+  prm.nsplit = s.Cout;
   prm.num_m_tiles = (int)((s.P() + BM - 1) / BM);
   prm.num_n_tiles = 1;
   prm.status = d.status;
@@ -1514,9 +1549,12 @@ int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const
   return launch_stem<256>(ta, tb, prm, d, st);
 }
 
+// Forward (a_src = x, a_ch = Cin) or dgrad (a_src = dy, a_ch = Cout).  With a
+// channel split the forward reads x's channels [Ca, Cin) from cat.b and the
+// dgrad writes dx's channels [Ca, Cin) to cat.b.
 int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const float* bias, void* out,
-              const Shape& s, int act, int out_f32, const EpiExtra& ex, const DevCtx& d,
-              cudaStream_t st) {
+              const Shape& s, int act, int out_f32, const EpiExtra& ex, const CatSplit& cat,
+              const DevCtx& d, cudaStream_t st) {
   const int nout = dgrad ? s.Cin : s.Cout;
   TileShape ts = pick_tile(nout, s, d.num_sms);
   // CONV3X3_TILE="<BN>x<MT>" or "halo<BN>" overrides the choice (tuning and tests)
@@ -1529,11 +1567,20 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
              (bn_o == 64 || bn_o == 128 || bn_o == 192 || bn_o == 256) && 2 * mt_o * bn_o <= 512)
       ts = TileShape{bn_o, mt_o, false};
   }
+  if (ts.halo && cat.on()) ts = pick_tile(nout, s, d.num_sms);  // the halo kernel reads one tensor
   const int bn = ts.bn;
-  CUtensorMap ta, tb;
+  const bool split_a = cat.on() && !dgrad;  // forward: A comes from two tensors
+  const int a_ch1 = split_a ? cat.Ca : a_ch;
+  CUtensorMap ta, ta2, tb;
   int rc = ts.halo ? make_halo_map(&ta, a_src, s.N, s.H, s.W, a_ch, (256 / s.W + 2) / 2)
-                   : make_im2col_map(&ta, a_src, s.N, s.H, s.W, a_ch, BM);
+                   : make_im2col_map(&ta, a_src, s.N, s.H, s.W, a_ch1, BM);
   if (rc) return rc;
+  if (split_a) {
+    rc = make_im2col_map(&ta2, cat.b, s.N, s.H, s.W, a_ch - cat.Ca, BM);
+    if (rc) return rc;
+  } else {
+    ta2 = ta;
+  }
   rc = make_weight_map(&tb, w, s.Cin, s.Cout, (kOneWeightBox && !dgrad && !ts.halo) ? bn : 64);
   if (rc) return rc;
   IgemmParams prm;
@@ -1544,14 +1591,18 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   prm.P = (int)s.P();
   prm.H = s.H;
   prm.W = s.W;
-  prm.kchunks = (a_ch + BKC - 1) / BKC;
+  prm.kchunks_a = split_a ? cat.Ca / BKC : (a_ch + BKC - 1) / BKC;
+  prm.kchunks = split_a ? prm.kchunks_a + (a_ch - cat.Ca + BKC - 1) / BKC : prm.kchunks_a;
   prm.nout = nout;
+  prm.nsplit = (cat.on() && dgrad) ? cat.Ca : nout;
+  prm.out2 = (cat.on() && dgrad) ? cat.b : nullptr;
   prm.num_m_tiles = (int)((s.P() + BM * ts.mt - 1) / (BM * ts.mt));
   prm.num_n_tiles = (nout + bn - 1) / bn;
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
   prm.zout = static_cast<__nv_bfloat16*>(ex.zout);
   prm.zin = static_cast<const __nv_bfloat16*>(ex.zin);
+  prm.zin2 = static_cast<const __nv_bfloat16*>(ex.zin_b);
   prm.zin_act = ex.zin ? ex.zin_act : CONV3X3_ACT_NONE;
   if (ts.halo) {
 #define C3_HALO(W_, BN_) \
@@ -1569,7 +1620,8 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
 #undef C3_HALO
   }
 #define C3_LAUNCH(BN_, MT_) \
-  return dgrad ? launch_igemm<BN_, MT_, true>(ta, tb, prm, d, st) : launch_igemm<BN_, MT_, false>(ta, tb, prm, d, st)
+  return dgrad ? launch_igemm<BN_, MT_, true>(ta, ta2, tb, prm, d, st) \
+               : launch_igemm<BN_, MT_, false>(ta, ta2, tb, prm, d, st)
   if (ts.mt == 2) {
     if (bn == 64) C3_LAUNCH(64, 2);
     C3_LAUNCH(128, 2);
@@ -1632,15 +1684,25 @@ bool tc_supported(int pass, const Shape& s) {
   return true;
 }
 
+// A channel split runs on the tensor cores when the first part is a whole
+// number of 64-channel K chunks (every TMA box then lies in one part).
+bool tc_supports_cat(const Shape& s, const CatSplit& cat) {
+  return !cat.on() || (cat.Ca % BKC == 0 && cat.Ca > 0 && cat.Ca < s.Cin);
+}
+
 int tc_fwd(const void* x, const void* w, const float* bias, void* y, const Shape& s, int act,
-           int out_f32, const EpiExtra& ex, const DevCtx& d, cudaStream_t st) {
-  if (s.Cin == 8 && s.Cout <= 256) return run_stem_fwd(x, w, bias, y, s, act, out_f32, ex, d, st);
-  return run_igemm(false, x, s.Cin, w, bias, y, s, act, out_f32, ex, d, st);
+           int out_f32, const EpiExtra& ex, const CatSplit& cat, const DevCtx& d,
+           cudaStream_t st) {
+  if (!tc_supports_cat(s, cat)) return CONV3X3_ERR_UNSUPPORTED;
+  if (s.Cin == 8 && s.Cout <= 256 && !cat.on())
+    return run_stem_fwd(x, w, bias, y, s, act, out_f32, ex, d, st);
+  return run_igemm(false, x, s.Cin, w, bias, y, s, act, out_f32, ex, cat, d, st);
 }
 
 int tc_dgrad(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
-             const EpiExtra& ex, const DevCtx& d, cudaStream_t st) {
-  return run_igemm(true, dy, s.Cout, w, nullptr, dx, s, CONV3X3_ACT_NONE, out_f32, ex, d, st);
+             const EpiExtra& ex, const CatSplit& cat, const DevCtx& d, cudaStream_t st) {
+  if (!tc_supports_cat(s, cat)) return CONV3X3_ERR_UNSUPPORTED;
+  return run_igemm(true, dy, s.Cout, w, nullptr, dx, s, CONV3X3_ACT_NONE, out_f32, ex, cat, d, st);
 }
 
 // Cin == 8: one tile per 128 output channels; splits fill the GPU once.
@@ -1683,6 +1745,7 @@ int run_wgrad_c8(const void* x, const void* dy, float* dw, float* db, const Shap
   prm.W = s.W;
   prm.Cin = s.Cin;
   prm.Cout = s.Cout;
+  prm.ca = s.Cin;
   prm.kb_total = pl.kb_total;
   prm.kb_per_split = pl.kb_per_split;
   prm.S = pl.S;
@@ -1697,15 +1760,22 @@ int run_wgrad_c8(const void* x, const void* dy, float* dw, float* db, const Shap
 }
 
 int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s, void* ws,
-             size_t ws_bytes, const DevCtx& d, cudaStream_t st) {
+             size_t ws_bytes, const CatSplit& cat, const DevCtx& d, cudaStream_t st) {
+  if (!tc_supports_cat(s, cat)) return CONV3X3_ERR_UNSUPPORTED;
   if (ws == nullptr || ws_bytes < tc_wgrad_workspace(s, d.num_sms)) return CONV3X3_ERR_WORKSPACE;
-  if (s.Cin == 8) return run_wgrad_c8(x, dy, dw, db, s, ws, d, st);
+  if (s.Cin == 8 && !cat.on()) return run_wgrad_c8(x, dy, dw, db, s, ws, d, st);
   WgPlan pl = wg_plan(s);
-  CUtensorMap tdy, tx;
+  CUtensorMap tdy, tx, tx2;
   int rc = make_rows_map(&tdy, dy, s.P(), s.Cout);
   if (rc) return rc;
-  rc = make_im2col_map(&tx, x, s.N, s.H, s.W, s.Cin, kWgPix);
+  rc = make_im2col_map(&tx, x, s.N, s.H, s.W, cat.on() ? cat.Ca : s.Cin, kWgPix);
   if (rc) return rc;
+  if (cat.on()) {
+    rc = make_im2col_map(&tx2, cat.b, s.N, s.H, s.W, s.Cin - cat.Ca, kWgPix);
+    if (rc) return rc;
+  } else {
+    tx2 = tx;
+  }
   WgradParams prm;
   prm.part = static_cast<float*>(ws);
   prm.P = (int)s.P();
@@ -1713,6 +1783,7 @@ int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s
   prm.W = s.W;
   prm.Cin = s.Cin;
   prm.Cout = s.Cout;
+  prm.ca = cat.on() ? cat.Ca : s.Cin;
   prm.kb_total = pl.kb_total;
   prm.kb_per_split = pl.kb_per_split;
   prm.S = pl.S;
@@ -1721,7 +1792,7 @@ int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
   if (set_smem(k_wgrad, kWgSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
-  k_wgrad<<<pl.tiles * pl.S, kThreads, kWgSmem, st>>>(tdy, tx, prm);
+  k_wgrad<<<pl.tiles * pl.S, kThreads, kWgSmem, st>>>(tdy, tx, tx2, prm);
   if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
   return launch_wgrad_reduce(prm.part, dw, db, (long long)s.Cout * 9 * s.Cin, s.Cout, pl.S, pl.S, st);
 }

@@ -91,3 +91,49 @@ def wgrad_f32(x, dy, stream=None):
     db = torch.empty((Cout,), dtype=torch.float32, device=x.device)
     L.conv3x3_wgrad_f32(x, dy, dw, db, N, Cin, Cout, H, W, None, 0, stream)
     return dw, db
+
+
+# ---------------------------------------------------------------------------
+# channel-concatenated input, passed as its two parts
+# ---------------------------------------------------------------------------
+def fwd_cat(xa, xb, w, bias=None, act=L.ACT_NONE, out_dtype=L.DT_BF16, path=L.PATH_AUTO,
+            out=None, z_out=None, stream=None):
+    """act(conv3x3(concat(xa, xb), w) + bias) without building the concatenation."""
+    N, H, W, Ca = xa.shape
+    Cin, Cout = Ca + xb.shape[3], w.shape[0]
+    if out is None:
+        dt = torch.float32 if out_dtype == L.DT_F32 else torch.bfloat16
+        out = torch.empty((N, H, W, Cout), dtype=dt, device=xa.device)
+    L.conv3x3_fwd_cat(xa, xb, Ca, w, bias, out, z_out, N, Cin, Cout, H, W, act, out_dtype, path,
+                      stream)
+    return out
+
+
+def dgrad_cat(dy, w, Ca, out_dtype=L.DT_BF16, path=L.PATH_AUTO, out=None, za_in=None, zb_in=None,
+              act_in=L.ACT_NONE, stream=None):
+    """(dxa, dxb): the input gradient of a conv over concat(xa, xb), split at channel Ca."""
+    N, H, W, Cout = dy.shape
+    Cin = w.shape[3]
+    if out is None:
+        dt = torch.float32 if out_dtype == L.DT_F32 else torch.bfloat16
+        out = (torch.empty((N, H, W, Ca), dtype=dt, device=dy.device),
+               torch.empty((N, H, W, Cin - Ca), dtype=dt, device=dy.device))
+    dxa, dxb = out
+    L.conv3x3_dgrad_cat(dy, w, dxa, dxb, Ca, za_in, zb_in, act_in, N, Cin, Cout, H, W, out_dtype,
+                        path, stream)
+    return dxa, dxb
+
+
+def wgrad_cat(xa, xb, dy, with_bias=True, path=L.PATH_AUTO, out=None, stream=None):
+    """(dw [Cout,3,3,Cin] fp32, dbias [Cout] fp32) of a conv over concat(xa, xb)."""
+    N, H, W, Ca = xa.shape
+    Cin, Cout = Ca + xb.shape[3], dy.shape[3]
+    nbytes = L.conv3x3_wgrad_cat_workspace_bytes(N, Cin, Ca, Cout, H, W, path)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=xa.device)
+    if out is None:
+        dw = torch.empty((Cout, 3, 3, Cin), dtype=torch.float32, device=xa.device)
+        db = torch.empty((Cout,), dtype=torch.float32, device=xa.device) if with_bias else None
+    else:
+        dw, db = out
+    L.conv3x3_wgrad_cat(xa, xb, Ca, dy, dw, db, N, Cin, Cout, H, W, ws, nbytes, path, stream)
+    return dw, db
