@@ -426,15 +426,44 @@ def cuda_arm(args):
     # end to end through the C ABI from pinned host buffers
     e2e = None
     if not args.no_e2e:
+        # Pipelined through the public calls: one stream uploads every layer's
+        # forward inputs (network order) and then its dy (reverse order, the
+        # order the backward consumes them); the compute stream waits only for
+        # the layer it is about to run; a third stream downloads each layer's
+        # dw and dbias as soon as its wgrad is done.
+        up = torch.cuda.Stream(device=device)
+        down = torch.cuda.Stream(device=device)
+        nl = len(wl.layers)
+        ev_fwd_in = [torch.cuda.Event() for _ in range(nl)]
+        ev_dy_in = [torch.cuda.Event() for _ in range(nl)]
+        ev_grads = [torch.cuda.Event() for _ in range(nl)]
+
+        def hook(kind, i, which):
+            if kind == "fwd" and which == 0:
+                stream.wait_event(ev_fwd_in[i])
+            elif kind == "dgrad" and which == 0:
+                stream.wait_event(ev_dy_in[i])
+            elif kind == "wgrad" and which == 1:
+                ev_grads[i].record(stream)
+                down.wait_event(ev_grads[i])
+                with torch.cuda.stream(down):
+                    wl.host[i]["dw"].copy_(wl.dev[i]["dw"], non_blocking=True)
+                    wl.host[i]["db"].copy_(wl.dev[i]["db"], non_blocking=True)
+
         def e2e_step():
-            with torch.cuda.stream(stream):
-                for h, d in zip(wl.host, wl.dev):
+            up.wait_stream(stream)     # the previous step no longer reads the inputs
+            with torch.cuda.stream(up):
+                for i, (h, d) in enumerate(zip(wl.host, wl.dev)):
                     for k in wl.inputs(h):
-                        d[k].copy_(h[k], non_blocking=True)
-                run_step(wl, sh)
-                for h, d in zip(wl.host, wl.dev):
-                    h["dw"].copy_(d["dw"], non_blocking=True)
-                    h["db"].copy_(d["db"], non_blocking=True)
+                        if k != "dy":
+                            d[k].copy_(h[k], non_blocking=True)
+                    ev_fwd_in[i].record(up)
+                for i in reversed(range(nl)):
+                    wl.dev[i]["dy"].copy_(wl.host[i]["dy"], non_blocking=True)
+                    ev_dy_in[i].record(up)
+            with torch.cuda.stream(stream):
+                run_step(wl, sh, record=hook)
+            down.synchronize()
             stream.synchronize()
         e2e_step()
         n_e2e = max(3, min(args.steps, 10))

@@ -65,6 +65,13 @@ def _load():
         lib.oracle_conv3x3_wgrad_f64.argtypes = [_dp, _dp, _dp, _dp] + [_i64] * 5
         lib.oracle_conv3x3_wgrad_at_f64.argtypes = [_dp, _dp] + [_i64] * 5 + [_lp, _i64, _dp]
         lib.oracle_conv3x3_dbias_f64.argtypes = [_dp, _dp] + [_i64] * 4
+        lib.oracle_conv3x3_fwd_strided_f64.argtypes = [_dp, _dp, _dp, _dp] + [_i64] * 6 + [ctypes.c_int]
+        lib.oracle_conv3x3_fwd_strided_at_f64.argtypes = ([_dp, _dp, _dp] + [_i64] * 6
+                                                          + [ctypes.c_int, _lp, _i64, _dp])
+        lib.oracle_conv3x3_dgrad_strided_f64.argtypes = [_dp, _dp, _dp] + [_i64] * 6
+        lib.oracle_conv3x3_dgrad_strided_at_f64.argtypes = [_dp, _dp] + [_i64] * 6 + [_lp, _i64, _dp]
+        lib.oracle_conv3x3_wgrad_strided_f64.argtypes = [_dp, _dp, _dp] + [_i64] * 6
+        lib.oracle_conv3x3_wgrad_strided_at_f64.argtypes = [_dp, _dp] + [_i64] * 6 + [_lp, _i64, _dp]
         _lib = lib
     return _lib
 
@@ -248,3 +255,89 @@ def conv3x3_dbias(dz):
     db = np.empty((Cout,), np.float64)
     _load().oracle_conv3x3_dbias_f64(_ptr(dz), _ptr(db), N, Cout, H, W)
     return db
+
+
+# ---------------------------------------------------------------------------
+# strided convolution (stride u, zero padding 1): the UNet's downsampling conv
+# ---------------------------------------------------------------------------
+def strided_out(length: int, u: int) -> int:
+    return (length - 1) // u + 1
+
+
+def conv3x3_fwd_strided(x, w, bias=None, act: int = 0, u: int = 2):
+    """y[n,ho,wo,k] = act(b[k] + sum x[n, u ho + r - 1, u wo + s - 1, c] w[k,r,s,c])."""
+    x = _d(x)
+    N, H, W, Cin = x.shape
+    w = _d(w)
+    Cout = w.shape[0]
+    assert w.shape == (Cout, 3, 3, Cin), w.shape
+    b = None if bias is None else _d(bias, (Cout,))
+    y = np.empty((N, strided_out(H, u), strided_out(W, u), Cout), np.float64)
+    _load().oracle_conv3x3_fwd_strided_f64(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, Cin, Cout, H, W,
+                                           int(u), int(act))
+    return y
+
+
+def conv3x3_fwd_strided_at(x, w, bias, act, u, idx):
+    x = _d(x)
+    N, H, W, Cin = x.shape
+    w = _d(w)
+    Cout = w.shape[0]
+    b = None if bias is None else _d(bias, (Cout,))
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    out = np.empty(idx.shape[0], np.float64)
+    _load().oracle_conv3x3_fwd_strided_at_f64(_ptr(x), _ptr(w), _ptr(b), N, Cin, Cout, H, W,
+                                              int(u), int(act), idx.ctypes.data_as(_lp),
+                                              idx.shape[0], _ptr(out))
+    return out
+
+
+def conv3x3_dgrad_strided(dz, w, H: int, W: int, u: int = 2):
+    """dx [N,H,W,Cin]: the adjoint of the strided forward applied to dz [N,Ho,Wo,Cout]."""
+    dz = _d(dz)
+    N, Ho, Wo, Cout = dz.shape
+    assert (Ho, Wo) == (strided_out(H, u), strided_out(W, u)), (dz.shape, H, W, u)
+    w = _d(w)
+    Cin = w.shape[3]
+    dx = np.empty((N, H, W, Cin), np.float64)
+    _load().oracle_conv3x3_dgrad_strided_f64(_ptr(dz), _ptr(w), _ptr(dx), N, Cin, Cout, H, W,
+                                             int(u))
+    return dx
+
+
+def conv3x3_dgrad_strided_at(dz, w, H, W, u, idx):
+    dz = _d(dz)
+    N, Ho, Wo, Cout = dz.shape
+    w = _d(w)
+    Cin = w.shape[3]
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    out = np.empty(idx.shape[0], np.float64)
+    _load().oracle_conv3x3_dgrad_strided_at_f64(_ptr(dz), _ptr(w), N, Cin, Cout, H, W, int(u),
+                                                idx.ctypes.data_as(_lp), idx.shape[0], _ptr(out))
+    return out
+
+
+def conv3x3_wgrad_strided(x, dz, u: int = 2):
+    """(dw [Cout,3,3,Cin], db [Cout]) of the strided convolution."""
+    x = _d(x)
+    N, H, W, Cin = x.shape
+    dz = _d(dz)
+    Cout = dz.shape[3]
+    assert dz.shape[:3] == (N, strided_out(H, u), strided_out(W, u)), (x.shape, dz.shape)
+    out = np.empty(9 * Cin * Cout + Cout, np.float64)
+    _load().oracle_conv3x3_wgrad_strided_f64(_ptr(x), _ptr(dz), _ptr(out), N, Cin, Cout, H, W,
+                                             int(u))
+    return out[:9 * Cin * Cout].reshape(Cout, 3, 3, Cin), out[9 * Cin * Cout:].copy()
+
+
+def conv3x3_wgrad_strided_at(x, dz, u, idx):
+    """dw at linear KRSC indices (an index 9*Cin*Cout + k gives db[k])."""
+    x = _d(x)
+    N, H, W, Cin = x.shape
+    dz = _d(dz)
+    Cout = dz.shape[3]
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    out = np.empty(idx.shape[0], np.float64)
+    _load().oracle_conv3x3_wgrad_strided_at_f64(_ptr(x), _ptr(dz), N, Cin, Cout, H, W, int(u),
+                                                idx.ctypes.data_as(_lp), idx.shape[0], _ptr(out))
+    return out

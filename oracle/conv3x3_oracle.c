@@ -101,6 +101,7 @@ typedef struct {
   int act;
   const int64_t* idx;
   const double* zin; /* dgrad through an activation: its pre-activation input */
+  int64_t u;         /* strided convolution: stride (output Ho = (H-1)/u + 1, Wo likewise) */
 } job_t;
 
 /* SiLU(z) = z * sigmoid(z) = z / (1 + e^{-z}).  For very negative z, e^{-z}
@@ -336,4 +337,141 @@ void oracle_conv3x3_dbias_f64(const double* dz, double* db, int64_t N, int64_t C
                               int64_t W) {
   job_t j = {NULL, NULL, NULL, dz, db, NULL, N, 0, Cout, H, W, 0, NULL};
   parallel_for(Cout, dbias_k, &j);
+}
+
+/* ---------------- strided convolution (stride u, zero padding 1) ----------------
+ * A UNet's downsampling conv: the same 3x3 window, moved u pixels at a time.
+ *   Ho = (H - 1) / u + 1,  Wo = (W - 1) / u + 1
+ *   forward  z[n,ho,wo,k] = b[k] + sum_{r,s,c} x[n, u ho + r - 1, u wo + s - 1, c] wt[k,r,s,c]
+ *            y = act(z)
+ *   dgrad    dx[n,h,w,c] = sum over (ho, wo, r, s) with u ho + r - 1 = h and
+ *            u wo + s - 1 = w of dz[n,ho,wo,k] wt[k,r,s,c]   (the adjoint of the forward)
+ *   wgrad    dw[k,r,s,c] = sum_{n,ho,wo} dz[n,ho,wo,k] x[n, u ho + r - 1, u wo + s - 1, c]
+ *   dbias    db[k]       = sum_{n,ho,wo} dz[n,ho,wo,k]
+ * x, dx: [N][H][W][Cin]; y, dz: [N][Ho][Wo][Cout]; out-of-range taps contribute zero. */
+static int64_t s_out(int64_t len, int64_t u) { return (len - 1) / u + 1; }
+
+static double sfwd_point(const job_t* j, int64_t n, int64_t ho, int64_t wo, int64_t k) {
+  double acc = j->bias ? j->bias[k] : 0.0;
+  for (int64_t r = 0; r < 3; ++r) {
+    int64_t hh = j->u * ho + r - 1;
+    if (hh < 0 || hh >= j->H) continue;
+    for (int64_t s = 0; s < 3; ++s) {
+      int64_t ww = j->u * wo + s - 1;
+      if (ww < 0 || ww >= j->W) continue;
+      const double* xp = j->x + ((n * j->H + hh) * j->W + ww) * j->Cin;
+      const double* wp = j->wt + ((k * 3 + r) * 3 + s) * j->Cin;
+      for (int64_t c = 0; c < j->Cin; ++c) acc += xp[c] * wp[c];
+    }
+  }
+  return apply_act(j->act, acc);
+}
+
+static void sfwd_item(void* ctx, int64_t i) { /* one output element, linear [N][Ho][Wo][Cout] index */
+  const job_t* j = (const job_t*)ctx;
+  const int64_t Ho = s_out(j->H, j->u), Wo = s_out(j->W, j->u);
+  int64_t e = j->idx ? j->idx[i] : i;
+  int64_t k = e % j->Cout, p = e / j->Cout;
+  int64_t wo = p % Wo, ho = (p / Wo) % Ho, n = p / (Wo * Ho);
+  j->out[i] = sfwd_point(j, n, ho, wo, k);
+}
+
+void oracle_conv3x3_fwd_strided_f64(const double* x, const double* wt, const double* bias,
+                                    double* y, int64_t N, int64_t Cin, int64_t Cout, int64_t H,
+                                    int64_t W, int64_t u, int act) {
+  job_t j = {x, wt, bias, NULL, y, NULL, N, Cin, Cout, H, W, act, NULL, NULL, u};
+  parallel_for(N * s_out(H, u) * s_out(W, u) * Cout, sfwd_item, &j);
+}
+
+void oracle_conv3x3_fwd_strided_at_f64(const double* x, const double* wt, const double* bias,
+                                       int64_t N, int64_t Cin, int64_t Cout, int64_t H, int64_t W,
+                                       int64_t u, int act, const int64_t* idx, int64_t count,
+                                       double* out) {
+  job_t j = {x, wt, bias, NULL, out, NULL, N, Cin, Cout, H, W, act, idx, NULL, u};
+  parallel_for(count, sfwd_item, &j);
+}
+
+static double sdgrad_point(const job_t* j, int64_t n, int64_t h, int64_t w, int64_t c) {
+  const int64_t Ho = s_out(j->H, j->u), Wo = s_out(j->W, j->u);
+  double acc = 0.0;
+  for (int64_t r = 0; r < 3; ++r) {
+    int64_t th = h + 1 - r; /* = u ho */
+    if (th < 0 || th % j->u != 0 || th / j->u >= Ho) continue;
+    int64_t ho = th / j->u;
+    for (int64_t s = 0; s < 3; ++s) {
+      int64_t tw = w + 1 - s; /* = u wo */
+      if (tw < 0 || tw % j->u != 0 || tw / j->u >= Wo) continue;
+      int64_t wo = tw / j->u;
+      const double* dzp = j->dz + ((n * Ho + ho) * Wo + wo) * j->Cout;
+      for (int64_t k = 0; k < j->Cout; ++k)
+        acc += dzp[k] * j->wt[((k * 3 + r) * 3 + s) * j->Cin + c];
+    }
+  }
+  return acc;
+}
+
+static void sdgrad_item(void* ctx, int64_t i) { /* one element of dx, linear [N][H][W][Cin] index */
+  const job_t* j = (const job_t*)ctx;
+  int64_t e = j->idx ? j->idx[i] : i;
+  int64_t c = e % j->Cin, p = e / j->Cin;
+  int64_t w = p % j->W, h = (p / j->W) % j->H, n = p / (j->W * j->H);
+  j->out[i] = sdgrad_point(j, n, h, w, c);
+}
+
+void oracle_conv3x3_dgrad_strided_f64(const double* dz, const double* wt, double* dx, int64_t N,
+                                      int64_t Cin, int64_t Cout, int64_t H, int64_t W, int64_t u) {
+  job_t j = {NULL, wt, NULL, dz, dx, NULL, N, Cin, Cout, H, W, 0, NULL, NULL, u};
+  parallel_for(N * H * W * Cin, sdgrad_item, &j);
+}
+
+void oracle_conv3x3_dgrad_strided_at_f64(const double* dz, const double* wt, int64_t N,
+                                         int64_t Cin, int64_t Cout, int64_t H, int64_t W,
+                                         int64_t u, const int64_t* idx, int64_t count,
+                                         double* out) {
+  job_t j = {NULL, wt, NULL, dz, out, NULL, N, Cin, Cout, H, W, 0, idx, NULL, u};
+  parallel_for(count, sdgrad_item, &j);
+}
+
+/* one element of dw (linear KRSC index), or db[k] when the index is 9*Cin*Cout + k;
+ * the pixel sum runs in increasing (n, ho, wo) order */
+static void swgrad_item(void* ctx, int64_t i) {
+  const job_t* j = (const job_t*)ctx;
+  const int64_t Ho = s_out(j->H, j->u), Wo = s_out(j->W, j->u);
+  int64_t e = j->idx ? j->idx[i] : i;
+  double acc = 0.0;
+  if (e >= 9 * j->Cin * j->Cout) {
+    int64_t k = e - 9 * j->Cin * j->Cout;
+    for (int64_t p = 0; p < j->N * Ho * Wo; ++p) acc += j->dz[p * j->Cout + k];
+    j->out[i] = acc;
+    return;
+  }
+  int64_t c = e % j->Cin, rs = (e / j->Cin) % 9, k = e / (9 * j->Cin);
+  int64_t r = rs / 3, s = rs % 3;
+  for (int64_t n = 0; n < j->N; ++n)
+    for (int64_t ho = 0; ho < Ho; ++ho) {
+      int64_t hh = j->u * ho + r - 1;
+      if (hh < 0 || hh >= j->H) continue;
+      for (int64_t wo = 0; wo < Wo; ++wo) {
+        int64_t ww = j->u * wo + s - 1;
+        if (ww < 0 || ww >= j->W) continue;
+        acc += j->dz[((n * Ho + ho) * Wo + wo) * j->Cout + k] *
+               j->x[((n * j->H + hh) * j->W + ww) * j->Cin + c];
+      }
+    }
+  j->out[i] = acc;
+}
+
+/* dwdb: 9*Cin*Cout dw values (KRSC) followed by Cout db values */
+void oracle_conv3x3_wgrad_strided_f64(const double* x, const double* dz, double* dwdb, int64_t N,
+                                      int64_t Cin, int64_t Cout, int64_t H, int64_t W, int64_t u) {
+  job_t j = {x, NULL, NULL, dz, dwdb, NULL, N, Cin, Cout, H, W, 0, NULL, NULL, u};
+  parallel_for(9 * Cin * Cout + Cout, swgrad_item, &j);
+}
+
+void oracle_conv3x3_wgrad_strided_at_f64(const double* x, const double* dz, int64_t N,
+                                         int64_t Cin, int64_t Cout, int64_t H, int64_t W,
+                                         int64_t u, const int64_t* idx, int64_t count,
+                                         double* out) {
+  job_t j = {x, NULL, NULL, dz, out, NULL, N, Cin, Cout, H, W, 0, idx, NULL, u};
+  parallel_for(count, swgrad_item, &j);
 }

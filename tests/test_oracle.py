@@ -218,6 +218,77 @@ def test_concatenated_input_splits_into_two_convolutions():
 
 
 # ---------------------------------------------------------------------------
+# strided (downsampling) convolution
+# ---------------------------------------------------------------------------
+def test_strided_with_stride_one_is_the_plain_convolution():
+    x, w, b, dz = rand(2, 5, 6, 3), rand(4, 3, 3, 3), rand(4), rand(2, 5, 6, 4)
+    assert np.array_equal(oracle.conv3x3_fwd_strided(x, w, b, 1, u=1), oracle.conv3x3_fwd(x, w, b, 1))
+    assert np.array_equal(oracle.conv3x3_dgrad_strided(dz, w, 5, 6, u=1), oracle.conv3x3_dgrad(dz, w))
+    dw, db = oracle.conv3x3_wgrad_strided(x, dz, u=1)
+    rdw, rdb = oracle.conv3x3_wgrad(x, dz)
+    assert np.array_equal(dw, rdw) and np.array_equal(db, rdb)
+
+
+@pytest.mark.parametrize("H,W", [(6, 8), (7, 5), (1, 4), (2, 3)])
+def test_stride_two_forward_is_the_plain_output_at_even_positions(H, W):
+    x, w, b = rand(2, H, W, 3), rand(4, 3, 3, 3), rand(4)
+    y = oracle.conv3x3_fwd_strided(x, w, b, 0, u=2)
+    assert y.shape == (2, (H + 1) // 2, (W + 1) // 2, 4)
+    assert np.array_equal(y, oracle.conv3x3_fwd(x, w, b)[:, ::2, ::2])
+
+
+@pytest.mark.parametrize("H,W", [(6, 8), (7, 5), (3, 3)])
+def test_stride_two_backward_identities(H, W):
+    N, Cin, Cout = 2, 3, 4
+    Ho, Wo = (H + 1) // 2, (W + 1) // 2
+    x, w, v = rand(N, H, W, Cin), rand(Cout, 3, 3, Cin), rand(N, Ho, Wo, Cout)
+    # adjoint: <fwd(x, w), v> = <x, dgrad(v, w)>
+    lhs = np.sum(oracle.conv3x3_fwd_strided(x, w, None, 0, u=2) * v)
+    rhs = np.sum(x * oracle.conv3x3_dgrad_strided(v, w, H, W, u=2))
+    assert lhs == pytest.approx(rhs, rel=1e-12)
+    # dgrad = the plain dgrad of v spread onto the even positions of an H x W grid
+    up = np.zeros((N, H, W, Cout))
+    up[:, ::2, ::2] = v
+    assert np.allclose(oracle.conv3x3_dgrad_strided(v, w, H, W, u=2), oracle.conv3x3_dgrad(up, w),
+                       rtol=1e-13, atol=1e-13)
+    # bilinear: <dw(x, v), V> = <fwd(x, V), v>;  db = sum of v
+    dw, db = oracle.conv3x3_wgrad_strided(x, v, u=2)
+    V = rand(Cout, 3, 3, Cin)
+    assert np.sum(dw * V) == pytest.approx(np.sum(oracle.conv3x3_fwd_strided(x, V, None, 0, u=2) * v),
+                                           rel=1e-12)
+    assert np.allclose(db, v.sum(axis=(0, 1, 2)), rtol=1e-13, atol=1e-13)
+    # sampled variants agree with the full ones
+    dx = oracle.conv3x3_dgrad_strided(v, w, H, W, u=2)
+    i = np.arange(0, dx.size, 3)
+    assert np.array_equal(oracle.conv3x3_dgrad_strided_at(v, w, H, W, 2, i), dx.reshape(-1)[i])
+    iw = np.concatenate([np.arange(0, dw.size, 4), dw.size + np.arange(Cout)])
+    assert np.array_equal(oracle.conv3x3_wgrad_strided_at(x, v, 2, iw),
+                          np.concatenate([dw.reshape(-1), db])[iw])
+    y = oracle.conv3x3_fwd_strided(x, w, None, 1, u=2)
+    iy = np.arange(0, y.size, 2)
+    assert np.array_equal(oracle.conv3x3_fwd_strided_at(x, w, None, 1, 2, iy), y.reshape(-1)[iy])
+
+
+def test_stride_two_against_torch_float64():
+    torch = pytest.importorskip("torch")
+    N, H, W, Cin, Cout = 2, 7, 6, 4, 3
+    x, w, b = rand(N, H, W, Cin), rand(Cout, 3, 3, Cin), rand(Cout)
+    xt = torch.tensor(x).permute(0, 3, 1, 2).contiguous().requires_grad_(True)
+    wt = torch.tensor(w).permute(0, 3, 1, 2).contiguous().requires_grad_(True)
+    bt = torch.tensor(b).requires_grad_(True)
+    z = torch.nn.functional.conv2d(xt, wt, bt, stride=2, padding=1)
+    dz = rand(*z.permute(0, 2, 3, 1).shape)
+    z.backward(torch.tensor(dz).permute(0, 3, 1, 2))
+    assert np.allclose(oracle.conv3x3_fwd_strided(x, w, b, 0, u=2),
+                       z.detach().permute(0, 2, 3, 1).numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(oracle.conv3x3_dgrad_strided(dz, w, H, W, u=2),
+                       xt.grad.permute(0, 2, 3, 1).numpy(), rtol=1e-12, atol=1e-12)
+    dw, db = oracle.conv3x3_wgrad_strided(x, dz, u=2)
+    assert np.allclose(dw, wt.grad.permute(0, 2, 3, 1).numpy(), rtol=1e-12, atol=1e-12)
+    assert np.allclose(db, bt.grad.numpy(), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
 # identities
 # ---------------------------------------------------------------------------
 def test_adjoint_identity_fwd_dgrad():
@@ -428,6 +499,12 @@ MUTANTS = {
     "leaky relu not applied": ("if (act == 2) return oracle_lrelu_f64(z);", "if (act == 2) return z;"),
     "silu grad without the (1 - s) factor": ("return sg * (1.0 + z * (1.0 - sg));", "return sg * (1.0 + z);"),
     "leaky relu grad slope": ("return z > 0.0 ? 1.0 : 0.2;", "return z > 0.0 ? 1.0 : 0.02;"),
+    "strided forward ignores the row stride": ("    int64_t hh = j->u * ho + r - 1;", "    int64_t hh = ho + r - 1;"),
+    "strided dgrad skips the parity test": ("if (th < 0 || th % j->u != 0 || th / j->u >= Ho) continue;",
+                                            "if (th < 0 || th / j->u >= Ho) continue;"),
+    "strided wgrad column off by one": ("        int64_t ww = j->u * wo + s - 1;", "        int64_t ww = j->u * wo + s;"),
+    "strided dbias drops the last image": ("for (int64_t p = 0; p < j->N * Ho * Wo; ++p)",
+                                           "for (int64_t p = 0; p < (j->N - 1) * Ho * Wo; ++p)"),
     "dgrad_act reads zin of channel 0": ("j->out[e] = oracle_act_grad_f64(j->act, j->zin[e]) * dgrad_point(j, n, h, w, c);",
                                          "j->out[e] = oracle_act_grad_f64(j->act, j->zin[e - c]) * dgrad_point(j, n, h, w, c);"),
 }
@@ -459,6 +536,9 @@ def _suite():
         test_silu_special_values_and_grid,
         test_leaky_relu_special_values_and_epilogue,
         test_act_grad_closed_forms_and_finite_differences,
+        test_strided_with_stride_one_is_the_plain_convolution,
+        (lambda: test_stride_two_forward_is_the_plain_output_at_even_positions(7, 5)),
+        (lambda: test_stride_two_backward_identities(7, 5)),
         (lambda: test_dgrad_through_activation_by_finite_differences(1)),
         (lambda: test_dgrad_through_activation_by_finite_differences(2)),
         test_adjoint_identity_fwd_dgrad,
