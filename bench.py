@@ -57,7 +57,7 @@ UNIT = "TFLOP/s"
 def layer_bytes(L: synth.Layer):
     """Algorithmic HBM bytes per pass: each ABI tensor read or written once."""
     x = L.P * L.Cin * 2
-    dy = L.P * L.Cout * 2
+    dy = L.Po * L.Cout * 2                  # y and dy live on the output grid
     w = L.Cout * 9 * L.Cin * 2
     fwd = x + w + dy + L.Cout * 4           # x, w, bias in; y out
     dgrad = dy + w + x                      # dy, w in; dx out
@@ -201,7 +201,7 @@ class Workload:
             del t
             d = {
                 "x": hx.to(device), "w": hw.to(device), "b": hb.to(device), "dy": hdy.to(device),
-                "y": torch.empty((L.N, L.H, L.W, L.Cout), dtype=torch.bfloat16, device=device),
+                "y": torch.empty((L.N, L.Ho, L.Wo, L.Cout), dtype=torch.bfloat16, device=device),
                 "dx": torch.empty((L.N, L.H, L.W, L.Cin), dtype=torch.bfloat16, device=device),
                 "dw": torch.empty((L.Cout, 3, 3, L.Cin), dtype=torch.float32, device=device),
                 "db": torch.empty((L.Cout,), dtype=torch.float32, device=device),
@@ -221,7 +221,7 @@ class Workload:
                 # z: this layer's pre-activation (written by the forward);
                 # zin: the pre-activation of the layer that produced x (none for
                 # the stem, whose input is the image)
-                d["z"] = torch.empty((L.N, L.H, L.W, L.Cout), dtype=torch.bfloat16, device=device)
+                d["z"] = torch.empty((L.N, L.Ho, L.Wo, L.Cout), dtype=torch.bfloat16, device=device)
                 d["act_in"] = L.act if i > 0 else 0
                 hz = torch.from_numpy(synth.bf16_bits(synth.make_zin(L, seed=seed, index=i))
                                       .view(np.int16)).view(torch.bfloat16)
@@ -248,7 +248,10 @@ class Workload:
                         h["zb"] = h["zin"][..., ca:].contiguous().pin_memory()
                         del h["zin"]
                 self.host.append(h)
-            if cat:
+            if L.stride != 1:
+                ws_max = max(ws_max, Lb.conv3x3_wgrad_strided_workspace_bytes(
+                    L.N, L.Cin, L.Cout, L.H, L.W, L.stride, Lb.PATH_AUTO))
+            elif cat:
                 ws_max = max(ws_max, Lb.conv3x3_wgrad_cat_workspace_bytes(
                     L.N, L.Cin, L.cat_a, L.Cout, L.H, L.W, Lb.PATH_AUTO))
             else:
@@ -275,7 +278,11 @@ def run_step(wl: Workload, stream_handle: int, ev=None, record=None):
         d = wl.dev[i]
         if record is not None:
             record("fwd", i, 0)
-        if d["cat_a"]:
+        if L.stride != 1:
+            Lb.conv3x3_fwd_strided(d["x"], d["w"], d["b"], d["y"], d.get("z"), L.N, L.Cin, L.Cout,
+                                   L.H, L.W, L.stride, L.act, Lb.DT_BF16, Lb.PATH_AUTO,
+                                   stream_handle)
+        elif d["cat_a"]:
             Lb.conv3x3_fwd_cat(d["xa"], d["xb"], d["cat_a"], d["w"], d["b"], d["y"], d.get("z"),
                                L.N, L.Cin, L.Cout, L.H, L.W, L.act, Lb.DT_BF16, Lb.PATH_AUTO,
                                stream_handle)
@@ -293,7 +300,11 @@ def run_step(wl: Workload, stream_handle: int, ev=None, record=None):
         d = wl.dev[i]
         if record is not None:
             record("dgrad", i, 0)
-        if d["cat_a"]:
+        if L.stride != 1:
+            Lb.conv3x3_dgrad_strided(d["dy"], d["w"], d["dx"], d.get("zin"), d.get("act_in", 0),
+                                     L.N, L.Cin, L.Cout, L.H, L.W, L.stride, Lb.DT_BF16,
+                                     Lb.PATH_AUTO, stream_handle)
+        elif d["cat_a"]:
             Lb.conv3x3_dgrad_cat(d["dy"], d["w"], d["dxa"], d["dxb"], d["cat_a"], d.get("za"),
                                  d.get("zb"), d.get("act_in", 0), L.N, L.Cin, L.Cout, L.H, L.W,
                                  Lb.DT_BF16, Lb.PATH_AUTO, stream_handle)
@@ -305,7 +316,11 @@ def run_step(wl: Workload, stream_handle: int, ev=None, record=None):
         if record is not None:
             record("dgrad", i, 1)
             record("wgrad", i, 0)
-        if d["cat_a"]:
+        if L.stride != 1:
+            Lb.conv3x3_wgrad_strided(d["x"], d["dy"], d["dw"], d["db"], L.N, L.Cin, L.Cout, L.H,
+                                     L.W, L.stride, wl.ws, wl.ws_bytes, Lb.PATH_AUTO,
+                                     stream_handle)
+        elif d["cat_a"]:
             Lb.conv3x3_wgrad_cat(d["xa"], d["xb"], d["cat_a"], d["dy"], d["dw"], d["db"], L.N,
                                  L.Cin, L.Cout, L.H, L.W, wl.ws, wl.ws_bytes, Lb.PATH_AUTO,
                                  stream_handle)
@@ -416,6 +431,7 @@ def cuda_arm(args):
         rt = roofline_time_s(L, peaks)
         per_layer.append({
             "name": L.name, "N": L.N, "Cin": L.Cin, "Cout": L.Cout, "H": L.H, "W": L.W,
+            "stride": L.stride,
             "path": {k: ["auto", "tensor", "simt"][max(0, Lb.conv3x3_auto_path(j, L.N, L.Cin, L.Cout, L.H, L.W))]
                      for j, k in enumerate(("fwd", "dgrad", "wgrad"))},
             "us": {k: round(float(call_ms[k][i] / K * 1e3), 2) for k in call_ms},
@@ -522,13 +538,18 @@ def oracle_sample(L: synth.Layer, seed: int, index: int):
     """fwd + dgrad + wgrad of the first image of layer L; returns (seconds, flops)."""
     import oracle
     L1 = synth.Layer(L.name, 1, L.Cin, L.Cout, L.H, L.W, act=L.act, cin_real=L.cin_real,
-                     dtype=L.dtype)
+                     dtype=L.dtype, stride=L.stride)
     t = synth.make_tensors(L1, seed=seed, index=index)
     x, w, b, dy = (np.asarray(a, np.float64) for a in (t.x, t.w, t.bias, t.dy))
     t0 = time.perf_counter()
-    oracle.conv3x3_fwd(x, w, b, L.act)
-    oracle.conv3x3_dgrad(dy, w)
-    oracle.conv3x3_wgrad(x, dy)
+    if L.stride == 1:
+        oracle.conv3x3_fwd(x, w, b, L.act)
+        oracle.conv3x3_dgrad(dy, w)
+        oracle.conv3x3_wgrad(x, dy)
+    else:
+        oracle.conv3x3_fwd_strided(x, w, b, L.act, u=L.stride)
+        oracle.conv3x3_dgrad_strided(dy, w, L.H, L.W, u=L.stride)
+        oracle.conv3x3_wgrad_strided(x, dy, u=L.stride)
     dt = time.perf_counter() - t0
     return dt, 3 * L1.flops_per_pass()
 

@@ -230,6 +230,36 @@ int conv3x3_wgrad_cat(const void* xa, const void* xb, int Ca, const void* dy, fl
 size_t conv3x3_wgrad_cat_workspace_bytes(int N, int Cin, int Ca, int Cout, int H, int W,
                                          int path);
 
+/* Strided (downsampling) convolution: the same 3x3 window and zero padding of
+ * 1, moved `stride` input pixels per output pixel (stride 1 or 2).  The pages
+ * reach downsampling only through the StyleGAN2 custom-kernel blog (page
+ * titled "Dim3 grid calculation code", on up/downsampling); a UNet's down path
+ * (the subject page's architecture) halves the resolution with a stride-2
+ * 3x3 conv.  With Ho = (H - 1) / stride + 1 and Wo likewise:
+ *   y[n,ho,wo,k] = act(b[k] + sum_{r,s,c} x[n, stride*ho + r - 1, stride*wo + s - 1, c] w[k,r,s,c])
+ *   x, dx [N][H][W][Cin];  y, z, dy [N][Ho][Wo][Cout];  w KRSC as everywhere.
+ * conv3x3_fwd_strided:   as conv3x3_fwd_save_z (z may be NULL).
+ * conv3x3_dgrad_strided: dx = the adjoint of the forward applied to dy, scaled
+ *   by act_in'(z_in) as in conv3x3_dgrad_act (act_in NONE: plain, z_in ignored).
+ * conv3x3_wgrad_strided: as conv3x3_wgrad_ex; scratch size from
+ *   conv3x3_wgrad_strided_workspace_bytes.
+ * The tensor-core kernels take stride 2 when Cin >= 64 and Cout >= 64 (the
+ * stride-2 dgrad runs as four output-parity classes with 1, 2, 2 and 4 taps);
+ * other shapes use the CUDA-core kernels (path AUTO) or return
+ * CONV3X3_ERR_UNSUPPORTED (path TENSOR).  Any other stride:
+ * CONV3X3_ERR_INVALID_ARG. */
+int conv3x3_fwd_strided(const void* x, const void* w, const float* bias, void* y, void* z,
+                        int N, int Cin, int Cout, int H, int W, int stride, int act,
+                        int out_dtype, int path, void* stream);
+int conv3x3_dgrad_strided(const void* dy, const void* w, void* dx, const void* z_in, int act_in,
+                          int N, int Cin, int Cout, int H, int W, int stride,
+                          int out_dtype, int path, void* stream);
+int conv3x3_wgrad_strided(const void* x, const void* dy, float* dw, float* dbias,
+                          int N, int Cin, int Cout, int H, int W, int stride,
+                          void* workspace, size_t workspace_bytes, int path, void* stream);
+size_t conv3x3_wgrad_strided_workspace_bytes(int N, int Cin, int Cout, int H, int W, int stride,
+                                             int path);
+
 /* Static description of a status code ("ok", "invalid argument", ...). */
 const char* conv3x3_status_string(int status);
 

@@ -93,19 +93,32 @@ class Layer:
     cin_real: int = 0  # channels that carry data (stem: 3); 0 means Cin
     dtype: str = "bf16"
     cat_a: int = 0     # up-path conv1: x = concat(main, skip) and main has cat_a channels; 0 = one tensor
+    stride: int = 1    # 2: downsampling conv (y and dy on the (H-1)//2+1 x (W-1)//2+1 grid)
 
     @property
     def P(self) -> int:
         return self.N * self.H * self.W
 
     @property
+    def Ho(self) -> int:
+        return (self.H - 1) // self.stride + 1
+
+    @property
+    def Wo(self) -> int:
+        return (self.W - 1) // self.stride + 1
+
+    @property
+    def Po(self) -> int:
+        return self.N * self.Ho * self.Wo
+
+    @property
     def real_cin(self) -> int:
         return self.cin_real or self.Cin
 
     def flops_per_pass(self, padded: bool = False) -> int:
-        """2 * N*H*W * Cin * Cout * 9 (real Cin unless padded=True)."""
+        """2 * N*Ho*Wo * Cin * Cout * 9 (real Cin unless padded=True)."""
         cin = self.Cin if padded else self.real_cin
-        return 2 * self.P * cin * self.Cout * 9
+        return 2 * self.Po * cin * self.Cout * 9
 
 
 @dataclass
@@ -126,7 +139,7 @@ def make_tensors(layer: Layer, seed: int = 0, index: int = 0, round_bf16: bool |
     x = normal(stream_id(seed, index, X), (L.N, L.H, L.W, cr), 1.0)
     w = normal(stream_id(seed, index, WT), (L.Cout, 3, 3, cr), math.sqrt(2.0 / (9 * cr)))
     b = normal(stream_id(seed, index, BIAS), (L.Cout,), 0.02)
-    dy = normal(stream_id(seed, index, DY), (L.N, L.H, L.W, L.Cout), 1.0)
+    dy = normal(stream_id(seed, index, DY), (L.N, L.Ho, L.Wo, L.Cout), 1.0)
     if cr != L.Cin:  # zero-pad the channel dimension (stem: 3 -> 8)
         xp = np.zeros((L.N, L.H, L.W, L.Cin), np.float32)
         xp[..., :cr] = x
@@ -191,8 +204,13 @@ def unet_stack(N: int = 64, base: int = 128, mult=(1, 2, 3, 4), res0: int = 64,
 
 STACK = unet_stack()
 
+# The UNet's downsampling convs between levels (stride 2, channels kept):
+# 128 @64x64 -> 32x32, 256 @32x32 -> 16x16, 384 @16x16 -> 8x8.
+DOWNSAMPLE = [Layer(f"down{l}.downsample", 64, c, c, r, r, stride=2)
+              for l, (c, r) in enumerate([(128, 64), (256, 32), (384, 16)])]
+
 # The benchmark's training-step sweep: the stem conv followed by the 32 resblock convs.
 UNET_STEP = [STEM] + STACK
 
 CONFIGS = {"tiny": [TINY], "stem": [STEM], "l1": [L1], "l2": [L2], "l3": [L3], "stack": STACK,
-           "unet": UNET_STEP}
+           "unet": UNET_STEP, "downsample": DOWNSAMPLE}

@@ -149,6 +149,30 @@ def test_concat_free_entry_points_validate_without_a_gpu(lib):
             == lib.conv3x3_wgrad_workspace_bytes(N, Cin, Cout, H, W))
 
 
+def test_strided_entry_points_validate_without_a_gpu(lib):
+    sh = (2, 64, 64, 8, 8)
+    far = ALIGNED + (1 << 24)
+    for bad in (0, 3, -1):
+        assert lib.conv3x3_fwd_strided(ALIGNED, ALIGNED, None, far, None, *sh, bad, 0, 0, 0,
+                                       None) == 1, bad
+        assert lib.conv3x3_dgrad_strided(ALIGNED, ALIGNED, far, None, 0, *sh, bad, 0, 0,
+                                         None) == 1, bad
+        assert lib.conv3x3_wgrad_strided(ALIGNED, ALIGNED, ALIGNED, None, *sh, bad, ALIGNED,
+                                         1 << 30, 0, None) == 1, bad
+        assert lib.conv3x3_wgrad_strided_workspace_bytes(*sh, bad, 0) == 0
+    # z overlapping y (y is [2][4][4][64] bf16 = 4 KB); z_in missing with an activation
+    assert lib.conv3x3_fwd_strided(ALIGNED, ALIGNED, None, far, far + 2048, *sh, 2, 1, 0, 0,
+                                   None) == 1
+    assert lib.conv3x3_dgrad_strided(ALIGNED, ALIGNED, far, None, 1, *sh, 2, 0, 0, None) == 1
+    # stride 2 on the tensor cores needs 64 channels each side; the split plan runs over dy's grid
+    assert lib.conv3x3_wgrad_strided_workspace_bytes(2, 32, 64, 8, 8, 2, 1) == 0
+    assert lib.conv3x3_wgrad_strided_workspace_bytes(2, 32, 64, 8, 8, 2, 0) > 0
+    assert (lib.conv3x3_wgrad_strided_workspace_bytes(64, 128, 128, 64, 64, 2, 0)
+            == lib.conv3x3_wgrad_workspace_bytes(64, 128, 128, 32, 32))
+    assert (lib.conv3x3_wgrad_strided_workspace_bytes(*sh, 1, 0)
+            == lib.conv3x3_wgrad_workspace_bytes(*sh))
+
+
 def test_workspace_size_depends_only_on_shape(lib):
     from synth import STACK, STEM, L1, L2, L3
     for L in [STEM, L1, L2, L3] + STACK:

@@ -491,3 +491,118 @@ def test_concat_free_up_path_layer_full_size_sampled():
     rw = oracle.conv3x3_wgrad_cat_at(ta, tb, t.dy, iw)
     assert np.max(np.abs(dwh[iw] - rw)) / np.max(np.abs(rw)) <= TOL_BF16
     assert rel_err(host(db), oracle.conv3x3_dbias(t.dy)) <= TOL_BF16
+
+
+# ---------------------------------------------------------------------------
+# strided (downsampling) convolution
+# ---------------------------------------------------------------------------
+STRIDE_SHAPES = [
+    # N, Cin, Cout, H, W
+    (2, 64, 64, 8, 8),
+    (1, 72, 200, 7, 9),     # odd grid, ragged channel chunk and N tiles
+    (2, 128, 128, 16, 16),
+    (3, 64, 96, 5, 6),
+    (1, 64, 64, 1, 5),      # single-row images
+    (2, 16, 32, 6, 7),      # fewer than 64 channels: CUDA-core kernels only
+]
+
+
+def _strided_case(shape, seed=13):
+    N, Cin, Cout, H, W = shape
+    Lr = synth.Layer("s2", N, Cin, Cout, H, W, act=1, stride=2)
+    return synth.make_tensors(Lr, seed=seed), synth.make_zin(Lr, seed=seed)
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("shape", STRIDE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_stride_two_convs(shape, path):
+    p = PATHS[path]
+    N, Cin, Cout, H, W = shape
+    Ho, Wo = (H + 1) // 2, (W + 1) // 2
+    t, zin_h = _strided_case(shape)
+    x, w, b, dy = dev_tensors(t)
+    assert tuple(dy.shape) == (N, Ho, Wo, Cout)
+    if p == L.PATH_TENSOR and min(Cin, Cout) < 64:
+        with pytest.raises(L.Conv3x3Error) as e:
+            ops.fwd_strided(x, w, b, act=1, path=p)
+        assert e.value.status == L.ERR_UNSUPPORTED
+        return
+    for act in (0, 1):
+        z = torch.empty((N, Ho, Wo, Cout), dtype=torch.bfloat16, device="cuda")
+        y32 = ops.fwd_strided(x, w, b, act=act, out_dtype=L.DT_F32, path=p)
+        ybf = ops.fwd_strided(x, w, b, act=act, path=p, z_out=z)
+        torch.cuda.synchronize()
+        ref = oracle.conv3x3_fwd_strided(t.x, t.w, t.bias, act, u=2)
+        assert rel_err(host(y32), ref) <= TOL_BF16, act
+        assert check_bf16_store(host(ybf), ref) == 0, act
+        assert np.array_equal(host(ybf), rne_bf16(host(y32))), act
+        assert check_bf16_store(host(z), oracle.conv3x3_fwd_strided(t.x, t.w, t.bias, 0, u=2)) == 0
+    dx32 = ops.dgrad_strided(dy, w, H, W, out_dtype=L.DT_F32, path=p)
+    dxbf = ops.dgrad_strided(dy, w, H, W, path=p)
+    torch.cuda.synchronize()
+    ref = oracle.conv3x3_dgrad_strided(t.dy, t.w, H, W, u=2)
+    assert rel_err(host(dx32), ref) <= TOL_BF16
+    assert check_bf16_store(host(dxbf), ref) == 0
+    assert np.array_equal(host(dxbf), rne_bf16(host(dx32)))
+    ga = ops.dgrad_strided(dy, w, H, W, out_dtype=L.DT_F32, path=p, z_in=to_dev_bf16(zin_h),
+                           act_in=1)
+    torch.cuda.synchronize()
+    grad = oracle.act_grad
+    ref_a = ref * np.vectorize(lambda z: grad(1, z))(zin_h.astype(np.float64))
+    assert rel_err(host(ga), ref_a) <= TOL_BF16
+    dw, db = ops.wgrad_strided(x, dy, path=p)
+    torch.cuda.synchronize()
+    rdw, rdb = oracle.conv3x3_wgrad_strided(t.x, t.dy, u=2)
+    assert rel_err(host(dw), rdw) <= TOL_BF16
+    assert rel_err(host(db), rdb) <= TOL_BF16
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_stride_one_through_the_strided_calls_is_the_plain_call(path):
+    p = PATHS[path]
+    t = _small((2, 64, 64, 9, 7))
+    x, w, b, dy = dev_tensors(t)
+    assert torch.equal(ops.fwd_strided(x, w, b, stride=1, act=1, path=p), ops.fwd(x, w, b, act=1, path=p))
+    assert torch.equal(ops.dgrad_strided(dy, w, 9, 7, stride=1, path=p), ops.dgrad(dy, w, path=p))
+    dw1, db1 = ops.wgrad_strided(x, dy, stride=1, path=p)
+    dw0, db0 = ops.wgrad(x, dy, path=p)
+    assert torch.equal(dw1, dw0) and torch.equal(db1, db0)
+
+
+@pytest.mark.parametrize("tile", ["64x1", "128x2", "256x1"])
+def test_stride_two_tiles(tile, monkeypatch):
+    monkeypatch.setenv("CONV3X3_TILE", tile)
+    shape = (2, 64, 128, 13, 10)
+    N, Cin, Cout, H, W = shape
+    t, _ = _strided_case(shape)
+    x, w, b, dy = dev_tensors(t)
+    y32 = ops.fwd_strided(x, w, b, act=1, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    dx32 = ops.dgrad_strided(dy, w, H, W, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert rel_err(host(y32), oracle.conv3x3_fwd_strided(t.x, t.w, t.bias, 1, u=2)) <= TOL_BF16
+    assert rel_err(host(dx32), oracle.conv3x3_dgrad_strided(t.dy, t.w, H, W, u=2)) <= TOL_BF16
+
+
+@pytest.mark.parametrize("index", [0, 2])
+def test_downsampling_layers_full_size_sampled(index):
+    Lr = synth.DOWNSAMPLE[index]
+    t = synth.make_tensors(Lr, seed=0, index=index)
+    x, w, b, dy = dev_tensors(t)
+    y32 = ops.fwd_strided(x, w, b, act=Lr.act, out_dtype=L.DT_F32)
+    dx32 = ops.dgrad_strided(dy, w, Lr.H, Lr.W, out_dtype=L.DT_F32)
+    dw, db = ops.wgrad_strided(x, dy)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(21 + index)
+    yh, dxh, dwh = host(y32).reshape(-1), host(dx32).reshape(-1), host(dw).reshape(-1)
+    iy = rng.integers(0, yh.size, 2048)
+    ry = oracle.conv3x3_fwd_strided_at(t.x, t.w, t.bias, Lr.act, 2, iy)
+    assert np.max(np.abs(yh[iy] - ry)) / np.max(np.abs(ry)) <= TOL_BF16
+    per_img = Lr.H * Lr.W * Lr.Cin   # every dx of the first image (all four parity classes, borders)
+    ix = np.concatenate([rng.integers(0, dxh.size, 2048), np.arange(min(per_img, 65536))])
+    rx = oracle.conv3x3_dgrad_strided_at(t.dy, t.w, Lr.H, Lr.W, 2, ix)
+    assert np.max(np.abs(dxh[ix] - rx)) / np.max(np.abs(rx)) <= TOL_BF16
+    iw = rng.integers(0, dwh.size, 64)
+    rw = oracle.conv3x3_wgrad_strided_at(t.x, t.dy, 2, iw)
+    assert np.max(np.abs(dwh[iw] - rw)) / np.max(np.abs(rw)) <= TOL_BF16
+    rdb = oracle.conv3x3_wgrad_strided_at(t.x, t.dy, 2, dwh.size + np.arange(Lr.Cout))
+    assert rel_err(host(db), rdb) <= TOL_BF16

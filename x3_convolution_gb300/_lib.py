@@ -46,6 +46,10 @@ _SIGS = {
     "conv3x3_dgrad_cat": ([_vp, _vp, _vp, _vp, _i, _vp, _vp, _i] + [_i] * 7 + [_vp], _i),
     "conv3x3_wgrad_cat": ([_vp, _vp, _i, _vp, _vp, _vp] + [_i] * 5 + [_vp, _sz, _i, _vp], _i),
     "conv3x3_wgrad_cat_workspace_bytes": ([_i] * 7, _sz),
+    "conv3x3_fwd_strided": ([_vp, _vp, _vp, _vp, _vp] + [_i] * 9 + [_vp], _i),
+    "conv3x3_dgrad_strided": ([_vp, _vp, _vp, _vp, _i] + [_i] * 8 + [_vp], _i),
+    "conv3x3_wgrad_strided": ([_vp, _vp, _vp, _vp] + [_i] * 6 + [_vp, _sz, _i, _vp], _i),
+    "conv3x3_wgrad_strided_workspace_bytes": ([_i] * 7, _sz),
 }
 
 WGRAD_NOALLOC_MAX_BYTES = 64 << 20
@@ -166,6 +170,31 @@ def conv3x3_wgrad_cat(xa, xb, Ca, dy, dw, dbias, N, Cin, Cout, H, W, workspace, 
 
 def conv3x3_wgrad_cat_workspace_bytes(N, Cin, Ca, Cout, H, W, path) -> int:
     return int(load().conv3x3_wgrad_cat_workspace_bytes(N, Cin, Ca, Cout, H, W, path))
+
+
+def conv3x3_fwd_strided(x, w, bias, y, z, N, Cin, Cout, H, W, stride, act, out_dtype, path,
+                        stream=None):
+    return _check(load().conv3x3_fwd_strided(_p(x), _p(w), _p(bias), _p(y), _p(z), N, Cin, Cout, H,
+                                             W, stride, act, out_dtype, path, _stream(stream)),
+                  "conv3x3_fwd_strided")
+
+
+def conv3x3_dgrad_strided(dy, w, dx, z_in, act_in, N, Cin, Cout, H, W, stride, out_dtype, path,
+                          stream=None):
+    return _check(load().conv3x3_dgrad_strided(_p(dy), _p(w), _p(dx), _p(z_in), act_in, N, Cin,
+                                               Cout, H, W, stride, out_dtype, path,
+                                               _stream(stream)), "conv3x3_dgrad_strided")
+
+
+def conv3x3_wgrad_strided(x, dy, dw, dbias, N, Cin, Cout, H, W, stride, workspace,
+                          workspace_bytes, path, stream=None):
+    return _check(load().conv3x3_wgrad_strided(_p(x), _p(dy), _p(dw), _p(dbias), N, Cin, Cout, H,
+                                               W, stride, _p(workspace), int(workspace_bytes),
+                                               path, _stream(stream)), "conv3x3_wgrad_strided")
+
+
+def conv3x3_wgrad_strided_workspace_bytes(N, Cin, Cout, H, W, stride, path) -> int:
+    return int(load().conv3x3_wgrad_strided_workspace_bytes(N, Cin, Cout, H, W, stride, path))
 
 
 def conv3x3_wgrad_ex(x, dy, dw, dbias, N, Cin, Cout, H, W, workspace, workspace_bytes, path,

@@ -153,7 +153,7 @@ bool cat_ok(const CatSplit& cat, int Cin) {
 
 int fwd_impl(const void* x, const void* w, const float* bias, void* y, int N, int Cin, int Cout,
              int H, int W, int act, int out_dtype, int path, const EpiExtra& ex,
-             const CatSplit& cat, void* stream) {
+             const CatSplit& cat, void* stream, int u = 1) {
   int rc = check_shape(N, Cin, Cout, H, W, true);
   if (rc) return rc;
   if (!x || !w || !y || !aligned16(x) || !aligned16(w) || !aligned16(y)) return CONV3X3_ERR_INVALID_ARG;
@@ -162,7 +162,9 @@ int fwd_impl(const void* x, const void* w, const float* bias, void* y, int N, in
   if (out_dtype != CONV3X3_DT_BF16 && out_dtype != CONV3X3_DT_F32) return CONV3X3_ERR_INVALID_ARG;
   if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return CONV3X3_ERR_INVALID_ARG;
   if (!cat_ok(cat, Cin)) return CONV3X3_ERR_INVALID_ARG;
+  if (u != 1 && u != 2) return CONV3X3_ERR_INVALID_ARG;
   Shape s{N, Cin, Cout, H, W};
+  s.u = u;
   int p = choose_path(0, s, path, cat);
   if (p < 0) return CONV3X3_ERR_UNSUPPORTED;
   const int of32 = out_dtype == CONV3X3_DT_F32;
@@ -174,14 +176,17 @@ int fwd_impl(const void* x, const void* w, const float* bias, void* y, int N, in
 }
 
 int dgrad_impl(const void* dy, const void* w, void* dx, int N, int Cin, int Cout, int H, int W,
-               int out_dtype, int path, const EpiExtra& ex, const CatSplit& cat, void* stream) {
+               int out_dtype, int path, const EpiExtra& ex, const CatSplit& cat, void* stream,
+               int u = 1) {
   int rc = check_shape(N, Cin, Cout, H, W, true);
   if (rc) return rc;
   if (!dy || !w || !dx || !aligned16(dy) || !aligned16(w) || !aligned16(dx)) return CONV3X3_ERR_INVALID_ARG;
   if (out_dtype != CONV3X3_DT_BF16 && out_dtype != CONV3X3_DT_F32) return CONV3X3_ERR_INVALID_ARG;
   if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return CONV3X3_ERR_INVALID_ARG;
   if (!cat_ok(cat, Cin)) return CONV3X3_ERR_INVALID_ARG;
+  if (u != 1 && u != 2) return CONV3X3_ERR_INVALID_ARG;
   Shape s{N, Cin, Cout, H, W};
+  s.u = u;
   int p = choose_path(1, s, path, cat);
   if (p < 0) return CONV3X3_ERR_UNSUPPORTED;
   const int of32 = out_dtype == CONV3X3_DT_F32;
@@ -192,11 +197,14 @@ int dgrad_impl(const void* dy, const void* w, void* dx, int N, int Cin, int Cout
   return tc_dgrad(dy, w, dx, s, of32, ex, cat, d, as_stream(stream));
 }
 
-size_t wgrad_ws_impl(int N, int Cin, int Cout, int H, int W, int path, const CatSplit& cat) {
+size_t wgrad_ws_impl(int N, int Cin, int Cout, int H, int W, int path, const CatSplit& cat,
+                     int u = 1) {
   if (check_shape(N, Cin, Cout, H, W, true) != CONV3X3_OK) return 0;
   if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return 0;
   if (cat.Ca != 0 && (cat.Ca < 0 || cat.Ca >= Cin || cat.Ca % 8 != 0)) return 0;
+  if (u != 1 && u != 2) return 0;
   Shape s{N, Cin, Cout, H, W};
+  s.u = u;
   int p = choose_path(2, s, path, cat);
   if (p < 0) return 0;
   return p == CONV3X3_PATH_SIMT ? simt_wgrad_workspace(s, 0) : tc_wgrad_workspace(s, 0);
@@ -204,7 +212,7 @@ size_t wgrad_ws_impl(int N, int Cin, int Cout, int H, int W, int path, const Cat
 
 int wgrad_impl(const void* x, const void* dy, float* dw, float* dbias, int N, int Cin, int Cout,
                int H, int W, void* workspace, size_t workspace_bytes, int path,
-               const CatSplit& cat, void* stream) {
+               const CatSplit& cat, void* stream, int u = 1) {
   int rc = check_shape(N, Cin, Cout, H, W, true);
   if (rc) return rc;
   if (!x || !dy || !dw || !aligned16(x) || !aligned16(dy) || !aligned16(dw)) return CONV3X3_ERR_INVALID_ARG;
@@ -212,7 +220,9 @@ int wgrad_impl(const void* x, const void* dy, float* dw, float* dbias, int N, in
   if (path < CONV3X3_PATH_AUTO || path > CONV3X3_PATH_SIMT) return CONV3X3_ERR_INVALID_ARG;
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return CONV3X3_ERR_INVALID_ARG;
   if (!cat_ok(cat, Cin)) return CONV3X3_ERR_INVALID_ARG;
+  if (u != 1 && u != 2) return CONV3X3_ERR_INVALID_ARG;
   Shape s{N, Cin, Cout, H, W};
+  s.u = u;
   int p = choose_path(2, s, path, cat);
   if (p < 0) return CONV3X3_ERR_UNSUPPORTED;
   size_t need = p == CONV3X3_PATH_SIMT ? simt_wgrad_workspace(s, 0) : tc_wgrad_workspace(s, 0);
@@ -372,6 +382,53 @@ size_t conv3x3_wgrad_cat_workspace_bytes(int N, int Cin, int Ca, int Cout, int H
   cat.b = reinterpret_cast<void*>(uintptr_t(16));  // marks the split; never dereferenced
   cat.Ca = Ca;
   return wgrad_ws_impl(N, Cin, Cout, H, W, path, cat);
+}
+
+int conv3x3_fwd_strided(const void* x, const void* w, const float* bias, void* y, void* z, int N,
+                        int Cin, int Cout, int H, int W, int stride, int act, int out_dtype,
+                        int path, void* stream) {
+  if (stride != 1 && stride != 2) return CONV3X3_ERR_INVALID_ARG;
+  if (check_shape(N, Cin, Cout, H, W, true) != CONV3X3_OK) return CONV3X3_ERR_INVALID_ARG;
+  EpiExtra ex;
+  if (z) {
+    if (!aligned16(z) || !y) return CONV3X3_ERR_INVALID_ARG;
+    const long long elems = (long long)N * ((H - 1) / stride + 1) * ((W - 1) / stride + 1) * Cout;
+    if (overlap(z, elems * 2, y, elems * (out_dtype == CONV3X3_DT_F32 ? 4 : 2)))
+      return CONV3X3_ERR_INVALID_ARG;
+    ex.zout = z;
+  }
+  return fwd_impl(x, w, bias, y, N, Cin, Cout, H, W, act, out_dtype, path, ex, CatSplit{}, stream,
+                  stride);
+}
+
+int conv3x3_dgrad_strided(const void* dy, const void* w, void* dx, const void* z_in, int act_in,
+                          int N, int Cin, int Cout, int H, int W, int stride, int out_dtype,
+                          int path, void* stream) {
+  if (stride != 1 && stride != 2) return CONV3X3_ERR_INVALID_ARG;
+  if (act_in < CONV3X3_ACT_NONE || act_in > CONV3X3_ACT_LRELU) return CONV3X3_ERR_INVALID_ARG;
+  EpiExtra ex;
+  if (act_in != CONV3X3_ACT_NONE) {
+    if (!z_in || !aligned16(z_in) || !dx) return CONV3X3_ERR_INVALID_ARG;
+    if (check_shape(N, Cin, Cout, H, W, true) != CONV3X3_OK) return CONV3X3_ERR_INVALID_ARG;
+    const long long elems = (long long)N * H * W * Cin;
+    if (overlap(z_in, elems * 2, dx, elems * (out_dtype == CONV3X3_DT_F32 ? 4 : 2)))
+      return CONV3X3_ERR_INVALID_ARG;
+    ex.zin = z_in;
+    ex.zin_act = act_in;
+  }
+  return dgrad_impl(dy, w, dx, N, Cin, Cout, H, W, out_dtype, path, ex, CatSplit{}, stream, stride);
+}
+
+size_t conv3x3_wgrad_strided_workspace_bytes(int N, int Cin, int Cout, int H, int W, int stride,
+                                             int path) {
+  return wgrad_ws_impl(N, Cin, Cout, H, W, path, CatSplit{}, stride);
+}
+
+int conv3x3_wgrad_strided(const void* x, const void* dy, float* dw, float* dbias, int N, int Cin,
+                          int Cout, int H, int W, int stride, void* workspace,
+                          size_t workspace_bytes, int path, void* stream) {
+  return wgrad_impl(x, dy, dw, dbias, N, Cin, Cout, H, W, workspace, workspace_bytes, path,
+                    CatSplit{}, stream, stride);
 }
 
 int conv3x3_wgrad_cat(const void* xa, const void* xb, int Ca, const void* dy, float* dw,

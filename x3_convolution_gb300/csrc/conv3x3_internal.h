@@ -13,8 +13,12 @@ namespace c3 {
 
 // Problem shape as the host dispatcher sees it.
 struct Shape {
-  int N, Cin, Cout, H, W;
+  int N, Cin, Cout, H, W;  // H, W: the input's (x's, dx's) grid
+  int u = 1;               // stride: 1, or 2 for a downsampling conv (pad 1 either way)
   long long P() const { return (long long)N * H * W; }
+  int Ho() const { return (H - 1) / u + 1; }  // output (y's, dy's) grid
+  int Wo() const { return (W - 1) / u + 1; }
+  long long Po() const { return (long long)N * Ho() * Wo(); }
 };
 
 // Per-call device context: status word and wait bound.

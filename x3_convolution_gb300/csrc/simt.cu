@@ -213,25 +213,30 @@ __global__ void __launch_bounds__(kThreads) k_fwd_bf16_c8(
 // forward, generic Cin (multiple of 8): one thread per (pixel, 8 output channels)
 // A channel-split input keeps channels [0, Ca) in x (row stride Ca) and
 // [Ca, Cin) in x2 (row stride Cin - Ca); Ca = Cin when there is no split.
+// Stride u: output pixel (ho, wo) of the (Ho, Wo) grid reads input pixels
+// (u*ho + r - 1, u*wo + s - 1).
 __global__ void __launch_bounds__(kThreads) k_fwd_bf16_gen(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ x2, int Ca,
     const __nv_bfloat16* __restrict__ w, const float* __restrict__ bias, void* __restrict__ y,
     __nv_bfloat16* __restrict__ zout, int N, int H, int W, int Cin, int Cout, int act,
-    int out_f32) {
+    int out_f32, int u) {
   const int KG = Cout / 8;
-  const long long total = (long long)N * H * W * KG;
+  const int Ho = (H - 1) / u + 1, Wo = (W - 1) / u + 1;
+  const long long total = (long long)N * Ho * Wo * KG;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
     int k0 = (int)(e % KG) * 8;
     long long p = e / KG;
-    int ww = (int)(p % W), hh = (int)((p / W) % H);
+    const int wo = (int)(p % Wo), ho = (int)((p / Wo) % Ho);
+    const long long n = p / ((long long)Wo * Ho);
+    const int ww = u * wo, hh = u * ho;
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = bias ? __ldg(bias + k0 + j) : 0.0f;
     for (int t = 0; t < 9; ++t) {
       int hi = hh + t / 3 - 1, wi = ww + t % 3 - 1;
       if (hi < 0 || hi >= H || wi < 0 || wi >= W) continue;
-      const long long q = p + (long long)(t / 3 - 1) * W + (t % 3 - 1);
+      const long long q = (n * H + hi) * W + wi;
       for (int c0 = 0; c0 < Cin; c0 += 8) {
         const __nv_bfloat16* xp = c0 < Ca ? x + q * Ca + c0 : x2 + q * (Cin - Ca) + (c0 - Ca);
         float xf[8];
@@ -309,8 +314,9 @@ __global__ void __launch_bounds__(kThreads) k_dgrad_bf16_gen(
     const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ w,
     void* __restrict__ dx, void* __restrict__ dx2, int Ca, const __nv_bfloat16* __restrict__ zin,
     const __nv_bfloat16* __restrict__ zin2, int zin_act, int N, int H, int W, int Cin, int Cout,
-    int out_f32) {
+    int out_f32, int u) {
   const int CG = Cin / 8;
+  const int Ho = (H - 1) / u + 1, Wo = (W - 1) / u + 1;
   const long long total = (long long)N * H * W * CG;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
@@ -320,11 +326,15 @@ __global__ void __launch_bounds__(kThreads) k_dgrad_bf16_gen(
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    const long long n = p / ((long long)W * H);
     for (int t = 0; t < 9; ++t) {
       int r = t / 3, s = t % 3;
-      int hi = hh + 1 - r, wi = ww + 1 - s;
-      if (hi < 0 || hi >= H || wi < 0 || wi >= W) continue;
-      const __nv_bfloat16* dp = dy + (p + (long long)(1 - r) * W + (1 - s)) * Cout;
+      // dy pixel (ho, wo) with u*ho + r - 1 = hh and u*wo + s - 1 = ww
+      int th = hh + 1 - r, tw = ww + 1 - s;
+      if (th < 0 || tw < 0 || th % u != 0 || tw % u != 0) continue;
+      int hi = th / u, wi = tw / u;
+      if (hi >= Ho || wi >= Wo) continue;
+      const __nv_bfloat16* dp = dy + ((n * Ho + hi) * Wo + wi) * Cout;
       for (int k0 = 0; k0 < Cout; k0 += 8) {
         float d[8];
         unpack8(__ldg(reinterpret_cast<const uint4*>(dp + k0)), d);
@@ -351,10 +361,11 @@ __global__ void __launch_bounds__(kThreads) k_dgrad_bf16_gen(
 __global__ void __launch_bounds__(kThreads) k_wgrad_bf16_partial(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ x2, int Ca,
     const __nv_bfloat16* __restrict__ dy, float* __restrict__ part, int N, int H, int W, int Cin,
-    int Cout, long long chunk, int S) {
+    int Cout, long long chunk, int S, int u) {
   const int CG = Cin / 8;
   const long long E8 = (long long)Cout * 9 * CG;  // 8-wide output groups
-  const long long P = (long long)N * H * W;
+  const int Ho = (H - 1) / u + 1, Wo = (W - 1) / u + 1;
+  const long long P = (long long)N * Ho * Wo;     // dy's pixels
   const int split = blockIdx.y;
   const long long p0 = split * chunk;
   const long long p1 = p0 + chunk < P ? p0 + chunk : P;
@@ -372,12 +383,13 @@ __global__ void __launch_bounds__(kThreads) k_wgrad_bf16_partial(
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
     for (long long p = p0; p < p1; ++p) {
-      int ww = (int)(p % W), hh = (int)((p / W) % H);
-      int hi = hh + r - 1, wi = ww + s - 1;
+      const int wo = (int)(p % Wo), ho = (int)((p / Wo) % Ho);
+      const long long n = p / ((long long)Wo * Ho);
+      int hi = u * ho + r - 1, wi = u * wo + s - 1;
       if (hi < 0 || hi >= H || wi < 0 || wi >= W) continue;
       float d = __bfloat162float(dy[p * Cout + k]);
       float xf[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(xs + (p + (long long)(r - 1) * W + (s - 1)) * xstride)), xf);
+      unpack8(__ldg(reinterpret_cast<const uint4*>(xs + ((n * H + hi) * W + wi) * xstride)), xf);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(d, xf[i], acc[i]);
     }
@@ -503,8 +515,8 @@ struct WgradPlan {
 
 WgradPlan wgrad_plan(const Shape& s) {
   WgradPlan pl;
-  const long long P = s.P();
-  pl.c8 = (s.Cin == 8);
+  const long long P = s.Po();  // splits run over dy's pixels
+  pl.c8 = (s.Cin == 8 && s.u == 1);
   long long blocks_per_split;
   if (pl.c8) {
     blocks_per_split = (s.Cout + 127) / 128;
@@ -556,7 +568,7 @@ int simt_fwd_bf16(const void* x, const void* w, const float* bias, void* y, cons
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
   __nv_bfloat16* zb = static_cast<__nv_bfloat16*>(ex.zout);
-  if (s.Cin == 8 && s.Cout <= 512 && !cat.on()) {
+  if (s.Cin == 8 && s.Cout <= 512 && !cat.on() && s.u == 1) {
     size_t sm = (size_t)s.Cout * 72 * sizeof(float);
     if (sm > 48 * 1024 &&
         cudaFuncSetAttribute(k_fwd_bf16_c8, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) !=
@@ -565,9 +577,9 @@ int simt_fwd_bf16(const void* x, const void* w, const float* bias, void* y, cons
     k_fwd_bf16_c8<<<grid_for(s.P()), kThreads, sm, st>>>(xb, wb, bias, y, zb, s.N, s.H, s.W,
                                                          s.Cout, act, out_f32);
   } else {
-    k_fwd_bf16_gen<<<grid_for(s.P() * (s.Cout / 8)), kThreads, 0, st>>>(
+    k_fwd_bf16_gen<<<grid_for(s.Po() * (s.Cout / 8)), kThreads, 0, st>>>(
         xb, static_cast<const __nv_bfloat16*>(cat.b), cat.on() ? cat.Ca : s.Cin, wb, bias, y, zb,
-        s.N, s.H, s.W, s.Cin, s.Cout, act, out_f32);
+        s.N, s.H, s.W, s.Cin, s.Cout, act, out_f32, s.u);
   }
   return launch_status();
 }
@@ -577,7 +589,7 @@ int simt_dgrad_bf16(const void* dy, const void* w, void* dx, const Shape& s, int
   const __nv_bfloat16* db = static_cast<const __nv_bfloat16*>(dy);
   const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
   const __nv_bfloat16* zb = static_cast<const __nv_bfloat16*>(ex.zin);
-  if (s.Cin == 8 && s.Cout <= 512 && !cat.on()) {
+  if (s.Cin == 8 && s.Cout <= 512 && !cat.on() && s.u == 1) {
     size_t sm = (size_t)s.Cout * 72 * sizeof(float);
     if (sm > 48 * 1024 &&
         cudaFuncSetAttribute(k_dgrad_bf16_c8, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -589,7 +601,7 @@ int simt_dgrad_bf16(const void* dy, const void* w, void* dx, const Shape& s, int
     k_dgrad_bf16_gen<<<grid_for(s.P() * (s.Cin / 8)), kThreads, 0, st>>>(
         db, wb, dx, cat.b, cat.on() ? cat.Ca : s.Cin, zb,
         static_cast<const __nv_bfloat16*>(ex.zin_b), ex.zin_act, s.N, s.H, s.W, s.Cin, s.Cout,
-        out_f32);
+        out_f32, s.u);
   }
   return launch_status();
 }
@@ -616,7 +628,7 @@ int simt_wgrad_bf16(const void* x, const void* dy, float* dw, float* db, const S
     dim3 grid((unsigned)((E8 + kThreads - 1) / kThreads), pl.S);
     k_wgrad_bf16_partial<<<grid, kThreads, 0, st>>>(
         xb, static_cast<const __nv_bfloat16*>(cat.b), cat.on() ? cat.Ca : s.Cin, dyb, part, s.N,
-        s.H, s.W, s.Cin, s.Cout, pl.chunk, pl.S);
+        s.H, s.W, s.Cin, s.Cout, pl.chunk, pl.S, s.u);
   }
   if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
   long long dwsize = (long long)s.Cout * 9 * s.Cin;

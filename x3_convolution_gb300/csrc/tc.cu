@@ -107,6 +107,11 @@ struct IgemmParams {
   int act, out_f32;
   int P, H, W;
   int kchunks;    // ceil(A channels / 64)
+  // Pixel traversal: P pixels of an (N, H, W) grid -- the output grid of the
+  // forward, dx's grid of a stride-1 dgrad, dy's grid of a stride-2 dgrad.
+  int ustride;    // forward: input row/column step per output pixel (1 or 2)
+  int s2;         // dgrad of a stride-2 conv, run as four output-parity classes
+  int oh, ow;     // s2: dx's H and W
   int kchunks_a;  // forward, channel-split input: chunks [0, kchunks_a) come from tmA, the rest from tmA2
   int nout;       // output channels (Cout fwd, Cin dgrad)
   int nsplit;     // output columns [0, nsplit) go to out (row stride nsplit), [nsplit, nout) to out2
@@ -236,6 +241,39 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix,
 // ----------------------------------------------------------------------------
 // forward / dgrad implicit GEMM
 // ----------------------------------------------------------------------------
+// Stride-2 dgrad by output parity.  dx[h][w] collects dy[ho][wo] w[r][s] over
+// 2 ho + r - 1 = h, 2 wo + s - 1 = w.  For h = 2i + ph only rows r = ph + 1
+// (mod 2) contribute, from dy row i + (ph + 1 - r) / 2: one tap row (r = 1)
+// for even h, two (r = 0 -> i + 1, r = 2 -> i) for odd h; columns likewise.
+// Each class (ph, pw) is a stride-1 implicit GEMM over dy's pixel grid with
+// 1, 2, 2 or 4 taps, all of them reading a 2x2 window at (i, j): the nine
+// taps are each used once, as in the stride-1 dgrad.
+struct TileInfo {
+  int mt, nt, cls, kblocks;
+};
+
+__device__ __forceinline__ int igemm_num_tiles(const IgemmParams& p) {
+  return (p.s2 ? 4 : 1) * p.num_m_tiles * p.num_n_tiles;
+}
+
+__device__ __forceinline__ TileInfo tile_info(const IgemmParams& p, int tile) {
+  if (!p.s2) return TileInfo{tile / p.num_n_tiles, tile % p.num_n_tiles, 0, 9 * p.kchunks};
+  const int per = p.num_m_tiles * p.num_n_tiles;
+  const int ci = tile / per, rest = tile - ci * per;
+  const int cls = 3 - ci;  // cls = 2 ph + pw; the 4-tap class first
+  const int ntaps = (1 + (cls >> 1)) * (1 + (cls & 1));
+  return TileInfo{rest / p.num_n_tiles, rest % p.num_n_tiles, cls, ntaps * p.kchunks};
+}
+
+// Tap `t` of class `cls`: weight tap r*3+s and the A window offsets (dj, di).
+__device__ __forceinline__ void s2_tap(int cls, int t, int& wtap, int& dj, int& di) {
+  const int ph = cls >> 1, pw = cls & 1, ns = 1 + pw;
+  const int ri = t / ns, si = t - ri * ns;
+  const int r = ph ? 2 * ri : 1, s = pw ? 2 * si : 1;
+  wtap = r * 3 + s;
+  di = (ph + 1 - r) >> 1;
+  dj = (pw + 1 - s) >> 1;
+}
 template <int BN, int MT, bool kDgrad>
 __global__ void __launch_bounds__(kIgemmThreads, 1)
     k_igemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
@@ -257,8 +295,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
-  const int kblocks = 9 * p.kchunks;
+  const int num_tiles = igemm_num_tiles(p);
   const int HW = p.H * p.W;
 
   if (warp == 0 && lane == 0) {
@@ -297,8 +334,11 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       int issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int mt = tile / p.num_n_tiles, nt = tile % p.num_n_tiles;
-        // window origin (pixel - 1 in h and w) of each 128-pixel sub-tile
+        const TileInfo ti = tile_info(p, tile);
+        const int mt = ti.mt, nt = ti.nt;
+        // window origin of each 128-pixel sub-tile: the input pixel (u*h - 1,
+        // u*w - 1) of the first output pixel (stride u, pad 1), or dy's pixel
+        // itself for the parity classes of a stride-2 dgrad
         int cw[MT], ch[MT], cn[MT];
 #pragma unroll
         for (int u = 0; u < MT; ++u) {
@@ -306,11 +346,20 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
           const int n0 = p0 / HW, rem = p0 - n0 * HW;
           const int h0 = rem / p.W;
           cn[u] = n0;
-          ch[u] = h0 - 1;
-          cw[u] = rem - h0 * p.W - 1;
+          ch[u] = p.s2 ? h0 : p.ustride * h0 - 1;
+          cw[u] = p.s2 ? rem - h0 * p.W : p.ustride * (rem - h0 * p.W) - 1;
         }
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = 0; kb < ti.kblocks; ++kb) {
           const int tap = kb / p.kchunks, cc = kb - tap * p.kchunks;
+          // A window offsets and weight tap of this k-block
+          int wtap, off_w, off_h;
+          if (p.s2) {
+            s2_tap(ti.cls, tap, wtap, off_w, off_h);
+          } else {
+            off_w = tap % 3;
+            off_h = tap / 3;
+            wtap = kDgrad ? 8 - tap : tap;
+          }
           // stage-parallel mode: this producer owns every kProd-th stage
           const bool mine = kStageParallel ? (issued % kProd == warp) : true;
           if (mine) {
@@ -339,13 +388,13 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
                 const bool second = cc >= p.kchunks_a;
                 tma_load_im2col_4d(sa + b * kABytes, second ? &tmA2 : &tmA, &full[stage],
                                    (second ? cc - p.kchunks_a : cc) * BKC, cw[b], ch[b], cn[b],
-                                   (uint16_t)(tap % 3), (uint16_t)(tap / 3));
+                                   (uint16_t)off_w, (uint16_t)off_h);
               } else {
                 const int j = b - MT;
                 if (!kDgrad)
-                  tma_load_3d(sb + j * kBBox, &tmB, &full[stage], cc * BKC, tap, nt * BN + j * 64);
+                  tma_load_3d(sb + j * kBBox, &tmB, &full[stage], cc * BKC, wtap, nt * BN + j * 64);
                 else
-                  tma_load_3d(sb + j * 8192, &tmB, &full[stage], nt * BN + j * 64, 8 - tap, cc * BKC);
+                  tma_load_3d(sb + j * 8192, &tmB, &full[stage], nt * BN + j * 64, wtap, cc * BKC);
               }
             }
           }
@@ -384,6 +433,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
         if (!mbar_wait(&tempty[buf], acc_phase ^ 1, p.wait_ns, p.status, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * MT * BN);
+        const int kblocks = tile_info(p, tile).kblocks;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) {
             ok = false;
@@ -434,9 +484,18 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     int buf = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int mt = tile / p.num_n_tiles, nt = tile % p.num_n_tiles;
-      const long long pix = (long long)mt * TM + sub * BM + row;
-      const bool valid = pix < p.P;
+      const TileInfo ti = tile_info(p, tile);
+      const int mt = ti.mt, nt = ti.nt;
+      long long pix = (long long)mt * TM + sub * BM + row;
+      bool valid = pix < p.P;
+      if (p.s2 && valid) {
+        // dy pixel (n, i, j) of class (ph, pw) -> dx pixel (n, 2i + ph, 2j + pw)
+        const int n = (int)(pix / HW), rem = (int)(pix - (long long)n * HW);
+        const int i = rem / p.W, j = rem - i * p.W;
+        const int h = 2 * i + (ti.cls >> 1), w = 2 * j + (ti.cls & 1);
+        valid = h < p.oh && w < p.ow;
+        pix = ((long long)n * p.oh + h) * p.ow + w;
+      }
       if (p.zin && valid && nt * BN + col_off < p.nout)
         prefetch_zin_row(p, pix, nt * BN + col_off, kCols);
       if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
@@ -950,6 +1009,7 @@ struct WgradParams {
   float* part;  // [S][Cout][9*Cin] then [S][Cout]
   int P, H, W, Cin, Cout;
   int ca;       // channel-split input: channels [0, ca) from tmX, [ca, Cin) from tmX2 (ca % 64 == 0)
+  int ustride;  // conv stride: output pixel (h, w) reads x around (u*h, u*w); P, H, W are dy's grid
   int kb_total, kb_per_split, S;
   int num_mb, num_cb;  // 128-wide blocks of Cout and Cin
   unsigned* status;
@@ -1043,7 +1103,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int c = cb * 128 + j * 64;  // a 64-channel box lies in one part
               const bool second = c >= p.ca;
               tma_load_im2col_4d(sb + (t * 2 + j) * 8192, second ? &tmX2 : &tmX, &full[stage],
-                                 second ? c - p.ca : c, w0 - 1, h0 - 1, n0, (uint16_t)t, (uint16_t)tr);
+                                 second ? c - p.ca : c, p.ustride * w0 - 1, p.ustride * h0 - 1, n0,
+                                 (uint16_t)t, (uint16_t)tr);
             }
           }
         }
@@ -1340,15 +1401,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ----------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------
+// NHWC activations as an im2col map.  Default: window origins run over
+// [-1, size - 2] (pad 1, 3 taps) in steps of `ustride` (1, or 2 for a
+// stride-2 conv: origins -1, 1, 3, ...).  corner = 0: origins over
+// [0, size - 1] with offsets 0..1 (the 2x2 windows of the stride-2 dgrad).
 int make_im2col_map(CUtensorMap* m, const void* base, int N, int H, int W, int C, int pixels,
-                    int channels = BKC, bool swizzle = true) {
+                    int channels = BKC, bool swizzle = true, int ustride = 1, int corner = -1) {
   PFN_encodeIm2col enc = encode_im2col_fn();
   if (!enc) return CONV3X3_ERR_CUDA;
   cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)N};
   cuuint64_t strides[3] = {(cuuint64_t)C * 2, (cuuint64_t)W * C * 2, (cuuint64_t)H * W * C * 2};
-  int lower[2] = {-1, -1};  // window origin = output pixel - 1 (pad 1)
-  int upper[2] = {-1, -1};  // pad 1 - (3 - 1): origins stop at size - 2
-  cuuint32_t estr[4] = {1, 1, 1, 1};
+  int lower[2] = {corner, corner};
+  int upper[2] = {corner, corner};
+  cuuint32_t estr[4] = {1, (cuuint32_t)ustride, (cuuint32_t)ustride, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
                    lower, upper, (cuuint32_t)channels, (cuuint32_t)pixels, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1436,7 +1501,7 @@ int launch_igemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap&
   using Cfg = IgemmCfg<BN, MT>;
   auto kern = k_igemm<BN, MT, kDgrad>;
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
-  const int tiles = prm.num_m_tiles * prm.num_n_tiles;
+  const int tiles = (prm.s2 ? 4 : 1) * prm.num_m_tiles * prm.num_n_tiles;
   const int grid = tiles < d.num_sms ? tiles : d.num_sms;
   kern<<<grid, kIgemmThreads, Cfg::kSmem, st>>>(a, a2, b, prm);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
@@ -1537,6 +1602,10 @@ int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const
   prm.W = s.W;
   prm.kchunks = 1;
   prm.kchunks_a = 1;
+  prm.ustride = 1;
+  prm.s2 = 0;
+  prm.oh = s.H;
+  prm.ow = s.W;
   prm.nout = s.Cout;
   prm.nsplit = s.Cout;
   prm.num_m_tiles = (int)((s.P() + BM - 1) / BM);
@@ -1556,7 +1625,16 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
               const Shape& s, int act, int out_f32, const EpiExtra& ex, const CatSplit& cat,
               const DevCtx& d, cudaStream_t st) {
   const int nout = dgrad ? s.Cin : s.Cout;
-  TileShape ts = pick_tile(nout, s, d.num_sms);
+  // pixel grid the tiles traverse: y's (forward), dx's (stride-1 dgrad) or
+  // dy's (stride-2 dgrad, four parity classes over it)
+  const bool s2 = dgrad && s.u == 2;
+  Shape g = s;
+  if (!dgrad || s2) {
+    g.H = s.Ho();
+    g.W = s.Wo();
+  }
+  g.u = 1;
+  TileShape ts = pick_tile(nout, dgrad ? s : g, d.num_sms);
   // CONV3X3_TILE="<BN>x<MT>" or "halo<BN>" overrides the choice (tuning and tests)
   if (const char* e = std::getenv("CONV3X3_TILE")) {
     int bn_o = 0, mt_o = 0;
@@ -1567,16 +1645,21 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
              (bn_o == 64 || bn_o == 128 || bn_o == 192 || bn_o == 256) && 2 * mt_o * bn_o <= 512)
       ts = TileShape{bn_o, mt_o, false};
   }
-  if (ts.halo && cat.on()) ts = pick_tile(nout, s, d.num_sms);  // the halo kernel reads one tensor
+  if (ts.halo && (cat.on() || s.u != 1))  // the halo kernel reads one stride-1 tensor
+    ts = pick_tile(nout, dgrad ? s : g, d.num_sms);
   const int bn = ts.bn;
   const bool split_a = cat.on() && !dgrad;  // forward: A comes from two tensors
   const int a_ch1 = split_a ? cat.Ca : a_ch;
   CUtensorMap ta, ta2, tb;
+  // A: x over its own grid with the conv's stride (forward), dy over dx's grid
+  // (stride-1 dgrad) or over its own grid in 2x2 windows (stride-2 dgrad)
+  const int a_h = dgrad ? g.H : s.H, a_w = dgrad ? g.W : s.W;
+  const int a_u = dgrad ? 1 : s.u, a_corner = s2 ? 0 : -1;
   int rc = ts.halo ? make_halo_map(&ta, a_src, s.N, s.H, s.W, a_ch, (256 / s.W + 2) / 2)
-                   : make_im2col_map(&ta, a_src, s.N, s.H, s.W, a_ch1, BM);
+                   : make_im2col_map(&ta, a_src, s.N, a_h, a_w, a_ch1, BM, BKC, true, a_u, a_corner);
   if (rc) return rc;
   if (split_a) {
-    rc = make_im2col_map(&ta2, cat.b, s.N, s.H, s.W, a_ch - cat.Ca, BM);
+    rc = make_im2col_map(&ta2, cat.b, s.N, s.H, s.W, a_ch - cat.Ca, BM, BKC, true, a_u, a_corner);
     if (rc) return rc;
   } else {
     ta2 = ta;
@@ -1588,15 +1671,19 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   prm.bias = bias;
   prm.act = act;
   prm.out_f32 = out_f32;
-  prm.P = (int)s.P();
-  prm.H = s.H;
-  prm.W = s.W;
+  prm.P = (int)g.P();
+  prm.H = g.H;
+  prm.W = g.W;
+  prm.ustride = dgrad ? 1 : s.u;
+  prm.s2 = s2 ? 1 : 0;
+  prm.oh = s.H;
+  prm.ow = s.W;
   prm.kchunks_a = split_a ? cat.Ca / BKC : (a_ch + BKC - 1) / BKC;
   prm.kchunks = split_a ? prm.kchunks_a + (a_ch - cat.Ca + BKC - 1) / BKC : prm.kchunks_a;
   prm.nout = nout;
   prm.nsplit = (cat.on() && dgrad) ? cat.Ca : nout;
   prm.out2 = (cat.on() && dgrad) ? cat.b : nullptr;
-  prm.num_m_tiles = (int)((s.P() + BM * ts.mt - 1) / (BM * ts.mt));
+  prm.num_m_tiles = (int)((g.P() + BM * ts.mt - 1) / (BM * ts.mt));
   prm.num_n_tiles = (nout + bn - 1) / bn;
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
@@ -1681,6 +1768,8 @@ bool tc_supported(int pass, const Shape& s) {
   // im2col corner offsets and coordinates are 16/32-bit; the kernels index pixels with int.
   if (s.P() >= (1LL << 31)) return false;
   if (s.H > 65535 || s.W > 65535) return false;
+  // stride 2: TMA boxes of 64 channels over tensors at least that wide
+  if (s.u != 1 && (s.u != 2 || s.Cin < BKC || s.Cout < BKC)) return false;
   return true;
 }
 
@@ -1694,7 +1783,7 @@ int tc_fwd(const void* x, const void* w, const float* bias, void* y, const Shape
            int out_f32, const EpiExtra& ex, const CatSplit& cat, const DevCtx& d,
            cudaStream_t st) {
   if (!tc_supports_cat(s, cat)) return CONV3X3_ERR_UNSUPPORTED;
-  if (s.Cin == 8 && s.Cout <= 256 && !cat.on())
+  if (s.Cin == 8 && s.Cout <= 256 && !cat.on() && s.u == 1)
     return run_stem_fwd(x, w, bias, y, s, act, out_f32, ex, d, st);
   return run_igemm(false, x, s.Cin, w, bias, y, s, act, out_f32, ex, cat, d, st);
 }
@@ -1720,12 +1809,21 @@ WgPlan wg_plan_c8(const Shape& s) {
   return pl;
 }
 
+// The split plan runs over dy's pixel grid.
+Shape wg_grid(const Shape& s) {
+  Shape g = s;
+  g.H = s.Ho();
+  g.W = s.Wo();
+  g.u = 1;
+  return g;
+}
+
 size_t tc_wgrad_workspace(const Shape& s, int /*num_sms*/) {
-  if (s.Cin == 8) {
+  if (s.Cin == 8 && s.u == 1) {
     WgPlan pl = wg_plan_c8(s);
     return (size_t)pl.S * (size_t)((long long)s.Cout * 72 + s.Cout) * sizeof(float);
   }
-  WgPlan pl = wg_plan(s);
+  WgPlan pl = wg_plan(wg_grid(s));
   long long dwsize = (long long)s.Cout * 9 * s.Cin;
   return (size_t)pl.S * (size_t)(dwsize + s.Cout) * sizeof(float);
 }
@@ -1746,6 +1844,7 @@ int run_wgrad_c8(const void* x, const void* dy, float* dw, float* db, const Shap
   prm.Cin = s.Cin;
   prm.Cout = s.Cout;
   prm.ca = s.Cin;
+  prm.ustride = 1;
   prm.kb_total = pl.kb_total;
   prm.kb_per_split = pl.kb_per_split;
   prm.S = pl.S;
@@ -1763,27 +1862,29 @@ int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s
              size_t ws_bytes, const CatSplit& cat, const DevCtx& d, cudaStream_t st) {
   if (!tc_supports_cat(s, cat)) return CONV3X3_ERR_UNSUPPORTED;
   if (ws == nullptr || ws_bytes < tc_wgrad_workspace(s, d.num_sms)) return CONV3X3_ERR_WORKSPACE;
-  if (s.Cin == 8 && !cat.on()) return run_wgrad_c8(x, dy, dw, db, s, ws, d, st);
-  WgPlan pl = wg_plan(s);
+  if (s.Cin == 8 && !cat.on() && s.u == 1) return run_wgrad_c8(x, dy, dw, db, s, ws, d, st);
+  const Shape g = wg_grid(s);
+  WgPlan pl = wg_plan(g);
   CUtensorMap tdy, tx, tx2;
-  int rc = make_rows_map(&tdy, dy, s.P(), s.Cout);
+  int rc = make_rows_map(&tdy, dy, g.P(), s.Cout);
   if (rc) return rc;
-  rc = make_im2col_map(&tx, x, s.N, s.H, s.W, cat.on() ? cat.Ca : s.Cin, kWgPix);
+  rc = make_im2col_map(&tx, x, s.N, s.H, s.W, cat.on() ? cat.Ca : s.Cin, kWgPix, BKC, true, s.u);
   if (rc) return rc;
   if (cat.on()) {
-    rc = make_im2col_map(&tx2, cat.b, s.N, s.H, s.W, s.Cin - cat.Ca, kWgPix);
+    rc = make_im2col_map(&tx2, cat.b, s.N, s.H, s.W, s.Cin - cat.Ca, kWgPix, BKC, true, s.u);
     if (rc) return rc;
   } else {
     tx2 = tx;
   }
   WgradParams prm;
   prm.part = static_cast<float*>(ws);
-  prm.P = (int)s.P();
-  prm.H = s.H;
-  prm.W = s.W;
+  prm.P = (int)g.P();
+  prm.H = g.H;
+  prm.W = g.W;
   prm.Cin = s.Cin;
   prm.Cout = s.Cout;
   prm.ca = cat.on() ? cat.Ca : s.Cin;
+  prm.ustride = s.u;
   prm.kb_total = pl.kb_total;
   prm.kb_per_split = pl.kb_per_split;
   prm.S = pl.S;

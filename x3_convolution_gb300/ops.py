@@ -137,3 +137,50 @@ def wgrad_cat(xa, xb, dy, with_bias=True, path=L.PATH_AUTO, out=None, stream=Non
         dw, db = out
     L.conv3x3_wgrad_cat(xa, xb, Ca, dy, dw, db, N, Cin, Cout, H, W, ws, nbytes, path, stream)
     return dw, db
+
+
+# ---------------------------------------------------------------------------
+# strided (downsampling) convolution
+# ---------------------------------------------------------------------------
+def strided_out(length, stride):
+    return (length - 1) // stride + 1
+
+
+def fwd_strided(x, w, bias=None, stride=2, act=L.ACT_NONE, out_dtype=L.DT_BF16,
+                path=L.PATH_AUTO, out=None, z_out=None, stream=None):
+    """y [N, Ho, Wo, Cout] of the stride-`stride`, pad-1 3x3 convolution."""
+    N, Cin, Cout, H, W = _shape(x, w)
+    Ho, Wo = strided_out(H, stride), strided_out(W, stride)
+    if out is None:
+        dt = torch.float32 if out_dtype == L.DT_F32 else torch.bfloat16
+        out = torch.empty((N, Ho, Wo, Cout), dtype=dt, device=x.device)
+    L.conv3x3_fwd_strided(x, w, bias, out, z_out, N, Cin, Cout, H, W, stride, act, out_dtype, path,
+                          stream)
+    return out
+
+
+def dgrad_strided(dy, w, H, W, stride=2, out_dtype=L.DT_BF16, path=L.PATH_AUTO, out=None,
+                  z_in=None, act_in=L.ACT_NONE, stream=None):
+    """dx [N, H, W, Cin] from dy [N, Ho, Wo, Cout]."""
+    N = dy.shape[0]
+    Cout, Cin = w.shape[0], w.shape[3]
+    if out is None:
+        dt = torch.float32 if out_dtype == L.DT_F32 else torch.bfloat16
+        out = torch.empty((N, H, W, Cin), dtype=dt, device=dy.device)
+    L.conv3x3_dgrad_strided(dy, w, out, z_in, act_in, N, Cin, Cout, H, W, stride, out_dtype, path,
+                            stream)
+    return out
+
+
+def wgrad_strided(x, dy, stride=2, with_bias=True, path=L.PATH_AUTO, out=None, stream=None):
+    N, H, W, Cin = x.shape
+    Cout = dy.shape[3]
+    nbytes = L.conv3x3_wgrad_strided_workspace_bytes(N, Cin, Cout, H, W, stride, path)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=x.device)
+    if out is None:
+        dw = torch.empty((Cout, 3, 3, Cin), dtype=torch.float32, device=x.device)
+        db = torch.empty((Cout,), dtype=torch.float32, device=x.device) if with_bias else None
+    else:
+        dw, db = out
+    L.conv3x3_wgrad_strided(x, dy, dw, db, N, Cin, Cout, H, W, stride, ws, nbytes, path, stream)
+    return dw, db
