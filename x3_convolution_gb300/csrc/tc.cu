@@ -179,24 +179,36 @@ __device__ __forceinline__ void prefetch_zin_row(const IgemmParams& p, long long
   }
 }
 
+// The 32 bias values of one output chunk (zero past nout), loaded ahead of the
+// accumulator: with the loads issued before the TMEM load, the bias add does
+// not wait on them.
+__device__ __forceinline__ void load_bias(const IgemmParams& p, int col0, float (&bv)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    const float4 b = col0 + i < p.nout ? __ldg(reinterpret_cast<const float4*>(p.bias + col0 + i))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    bv[i] = b.x;
+    bv[i + 1] = b.y;
+    bv[i + 2] = b.z;
+    bv[i + 3] = b.w;
+  }
+}
+
+// Epilogue of one 32-column chunk: (+ bias) -> [store z] -> activation ->
+// [* act'(z_in)] -> fp32 or bf16 store.  kExt = false compiles out the fused
+// extras (z store, z_in scaling, split output) for the plain calls.
+template <bool kExt>
 __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix, int col0,
-                                            const uint32_t (&v)[32], const uint4 (&zr)[4]) {
+                                            const uint32_t (&v)[32], const float (&bv)[32],
+                                            const uint4 (&zr)[4]) {
   float f[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
   if (p.bias) {
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      if (col0 + i < p.nout) {
-        float4 b = __ldg(reinterpret_cast<const float4*>(p.bias + col0 + i));
-        f[i] += b.x;
-        f[i + 1] += b.y;
-        f[i + 2] += b.z;
-        f[i + 3] += b.w;
-      }
-    }
+    for (int i = 0; i < 32; ++i) f[i] += bv[i];
   }
-  if (p.zout) store_bf16x32(p.zout + pix * p.nout + col0, p.nout - col0, f);
+  if (kExt && p.zout) store_bf16x32(p.zout + pix * p.nout + col0, p.nout - col0, f);
   if (p.act == CONV3X3_ACT_SILU) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) f[i] = silu_f32(f[i]);
@@ -204,7 +216,7 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix,
 #pragma unroll
     for (int i = 0; i < 32; ++i) f[i] = f[i] >= 0.0f ? f[i] : 0.2f * f[i];
   }
-  if (p.zin) {
+  if (kExt && p.zin) {
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&zr[g]);
@@ -216,8 +228,8 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix,
       }
     }
   }
-  const OutPos o = out_pos(p, pix, col0);
-  void* base = o.second ? p.out2 : p.out;
+  const OutPos o = kExt ? out_pos(p, pix, col0) : OutPos{pix * p.nout + col0, p.nout - col0, false};
+  void* base = (kExt && o.second) ? p.out2 : p.out;
   if (p.out_f32) {
     float* op = static_cast<float*>(base) + o.off;
 #pragma unroll
@@ -231,11 +243,14 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix,
   }
 }
 
+// All features, operands fetched here (the halo and 8-channel kernels).
 __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix, int col0,
                                             const uint32_t (&v)[32]) {
+  float bv[32];
+  if (p.bias) load_bias(p, col0, bv);
   uint4 zr[4] = {};
   if (p.zin) load_zin(p, pix, col0, zr);
-  store_chunk(p, pix, col0, v, zr);
+  store_chunk<true>(p, pix, col0, v, bv, zr);
 }
 
 // ----------------------------------------------------------------------------
@@ -252,12 +267,12 @@ struct TileInfo {
   int mt, nt, cls, kblocks;
 };
 
-__device__ __forceinline__ int igemm_num_tiles(const IgemmParams& p) {
-  return (p.s2 ? 4 : 1) * p.num_m_tiles * p.num_n_tiles;
+__device__ __forceinline__ int igemm_num_tiles(const IgemmParams& p, bool s2) {
+  return (s2 ? 4 : 1) * p.num_m_tiles * p.num_n_tiles;
 }
 
-__device__ __forceinline__ TileInfo tile_info(const IgemmParams& p, int tile) {
-  if (!p.s2) return TileInfo{tile / p.num_n_tiles, tile % p.num_n_tiles, 0, 9 * p.kchunks};
+__device__ __forceinline__ TileInfo tile_info(const IgemmParams& p, int tile, bool s2) {
+  if (!s2) return TileInfo{tile / p.num_n_tiles, tile % p.num_n_tiles, 0, 9 * p.kchunks};
   const int per = p.num_m_tiles * p.num_n_tiles;
   const int ci = tile / per, rest = tile - ci * per;
   const int cls = 3 - ci;  // cls = 2 ph + pw; the 4-tap class first
@@ -274,7 +289,9 @@ __device__ __forceinline__ void s2_tap(int cls, int t, int& wtap, int& dj, int& 
   di = (ph + 1 - r) >> 1;
   dj = (pw + 1 - s) >> 1;
 }
-template <int BN, int MT, bool kDgrad>
+// kExt = false: no fused extras and no stride-2 dgrad (p.s2, p.zout, p.zin
+// and the split output are ignored).
+template <int BN, int MT, bool kDgrad, bool kExt>
 __global__ void __launch_bounds__(kIgemmThreads, 1)
     k_igemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
             const __grid_constant__ CUtensorMap tmB, const IgemmParams p) {
@@ -295,7 +312,8 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_tiles = igemm_num_tiles(p);
+  const bool s2 = kExt && kDgrad && p.s2;  // stride-2 dgrad by output parity
+  const int num_tiles = igemm_num_tiles(p, s2);
   const int HW = p.H * p.W;
 
   if (warp == 0 && lane == 0) {
@@ -334,7 +352,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       int issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const TileInfo ti = tile_info(p, tile);
+        const TileInfo ti = tile_info(p, tile, s2);
         const int mt = ti.mt, nt = ti.nt;
         // window origin of each 128-pixel sub-tile: the input pixel (u*h - 1,
         // u*w - 1) of the first output pixel (stride u, pad 1), or dy's pixel
@@ -346,14 +364,14 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
           const int n0 = p0 / HW, rem = p0 - n0 * HW;
           const int h0 = rem / p.W;
           cn[u] = n0;
-          ch[u] = p.s2 ? h0 : p.ustride * h0 - 1;
-          cw[u] = p.s2 ? rem - h0 * p.W : p.ustride * (rem - h0 * p.W) - 1;
+          ch[u] = s2 ? h0 : p.ustride * h0 - 1;
+          cw[u] = s2 ? rem - h0 * p.W : p.ustride * (rem - h0 * p.W) - 1;
         }
         for (int kb = 0; kb < ti.kblocks; ++kb) {
           const int tap = kb / p.kchunks, cc = kb - tap * p.kchunks;
           // A window offsets and weight tap of this k-block
           int wtap, off_w, off_h;
-          if (p.s2) {
+          if (s2) {
             s2_tap(ti.cls, tap, wtap, off_w, off_h);
           } else {
             off_w = tap % 3;
@@ -433,7 +451,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
         if (!mbar_wait(&tempty[buf], acc_phase ^ 1, p.wait_ns, p.status, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * MT * BN);
-        const int kblocks = tile_info(p, tile).kblocks;
+        const int kblocks = tile_info(p, tile, s2).kblocks;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) {
             ok = false;
@@ -484,11 +502,11 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     int buf = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const TileInfo ti = tile_info(p, tile);
+      const TileInfo ti = tile_info(p, tile, s2);
       const int mt = ti.mt, nt = ti.nt;
       long long pix = (long long)mt * TM + sub * BM + row;
       bool valid = pix < p.P;
-      if (p.s2 && valid) {
+      if (s2 && valid) {
         // dy pixel (n, i, j) of class (ph, pw) -> dx pixel (n, 2i + ph, 2j + pw)
         const int n = (int)(pix / HW), rem = (int)(pix - (long long)n * HW);
         const int i = rem / p.W, j = rem - i * p.W;
@@ -496,7 +514,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
         valid = h < p.oh && w < p.ow;
         pix = ((long long)n * p.oh + h) * p.ow + w;
       }
-      if (p.zin && valid && nt * BN + col_off < p.nout)
+      if (kExt && p.zin && valid && nt * BN + col_off < p.nout)
         prefetch_zin_row(p, pix, nt * BN + col_off, kCols);
       if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
       tc_fence_after();
@@ -506,12 +524,15 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       for (int j = 0; j < kCols / 32; ++j) {
         const int col0 = nt * BN + col_off + j * 32;
         const bool live = valid && col0 < p.nout;
+        // operands that do not depend on the accumulator are loaded first
+        float bv[32];
+        if (p.bias && live) load_bias(p, col0, bv);
         uint4 zr[4] = {};
-        if (p.zin && live) load_zin(p, pix, col0, zr);
+        if (kExt && p.zin && live) load_zin(p, pix, col0, zr);
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
         tmem_ld_wait();
-        if (live) store_chunk(p, pix, col0, v, zr);
+        if (live) store_chunk<kExt>(p, pix, col0, v, bv, zr);
       }
       tc_fence_before();
       __syncwarp();
@@ -1499,7 +1520,9 @@ template <int BN, int MT, bool kDgrad>
 int launch_igemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
                  const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
   using Cfg = IgemmCfg<BN, MT>;
-  auto kern = k_igemm<BN, MT, kDgrad>;
+  // the fused extras, a split output or a stride-2 dgrad need the full epilogue
+  const bool ext = prm.zout || prm.zin || prm.out2 || prm.s2;
+  auto kern = ext ? k_igemm<BN, MT, kDgrad, true> : k_igemm<BN, MT, kDgrad, false>;
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int tiles = (prm.s2 ? 4 : 1) * prm.num_m_tiles * prm.num_n_tiles;
   const int grid = tiles < d.num_sms ? tiles : d.num_sms;
