@@ -169,6 +169,12 @@ def dist_env():
     return ws, rank, local
 
 
+def whole_job_tflops(flops_per_rank_step: float, ws: int, ms_max: float) -> float:
+    """Weak scaling: every rank runs the same step; the job's throughput is all ranks'
+    FLOPs over the slowest rank's time."""
+    return flops_per_rank_step * ws / (ms_max * 1e-3) / 1e12
+
+
 def max_over_ranks(value: float, ws: int, device=None) -> float:
     if ws <= 1:
         return value
@@ -412,7 +418,7 @@ def cuda_arm(args):
 
     ms = float(np.mean(step_ms))
     ms_max = max_over_ranks(ms, ws, device)
-    value = flops_step * ws / (ms_max * 1e-3) / 1e12
+    value = whole_job_tflops(flops_step, ws, ms_max)
 
     # per-pass breakdown and the roofline of the dominant kernel family
     K = args.steps
