@@ -2,8 +2,10 @@
 """Benchmark: 3x3 conv fwd + dgrad + wgrad throughput (TFLOP/s) on GB300.
 
 One step = one training-step sweep over the UNet's 3x3 convs: every layer's
-forward (bias + SiLU epilogue) in network order, then dgrad and wgrad (+ dbias)
-in reverse order, each through the C ABI of libconv3x3.so on one stream.
+forward (bias + SiLU epilogue) in network order, then every dgrad in reverse
+order, then every wgrad (+ dbias) in reverse order, each through the C ABI of
+libconv3x3.so on one stream.  CUDA events at the step's start and at the end of
+each pass give the step time and the per-pass times.
 
 Default workload "unet": the stem conv (3 -> 128 channels, zero-padded to 8,
 64x64) followed by the 32 resblock convs of the 64x64 diffusion UNet (base 128,
@@ -276,66 +278,91 @@ class Workload:
         return sum(h[k].numel() * h[k].element_size() for h in self.host for k in ("dw", "db"))
 
 
-def run_step(wl: Workload, stream_handle: int, ev=None, record=None):
-    """One sweep: fwd in order, then dgrad + wgrad in reverse order (C ABI calls)."""
+def _fwd(wl, i, sh):
     from x3_convolution_gb300 import _lib as Lb
+    L, d = wl.layers[i], wl.dev[i]
+    if L.stride != 1:
+        Lb.conv3x3_fwd_strided(d["x"], d["w"], d["b"], d["y"], d.get("z"), L.N, L.Cin, L.Cout, L.H,
+                               L.W, L.stride, L.act, Lb.DT_BF16, Lb.PATH_AUTO, sh)
+    elif d["cat_a"]:
+        Lb.conv3x3_fwd_cat(d["xa"], d["xb"], d["cat_a"], d["w"], d["b"], d["y"], d.get("z"), L.N,
+                           L.Cin, L.Cout, L.H, L.W, L.act, Lb.DT_BF16, Lb.PATH_AUTO, sh)
+    elif wl.fused_act:
+        Lb.conv3x3_fwd_save_z(d["x"], d["w"], d["b"], d["y"], d["z"], L.N, L.Cin, L.Cout, L.H, L.W,
+                              L.act, Lb.DT_BF16, Lb.PATH_AUTO, sh)
+    else:
+        Lb.conv3x3_fwd(d["x"], d["w"], d["b"], d["y"], L.N, L.Cin, L.Cout, L.H, L.W, L.act, sh)
+    return 1
+
+
+def _dgrad(wl, i, sh):
+    from x3_convolution_gb300 import _lib as Lb
+    L, d = wl.layers[i], wl.dev[i]
+    if L.stride != 1:
+        Lb.conv3x3_dgrad_strided(d["dy"], d["w"], d["dx"], d.get("zin"), d.get("act_in", 0), L.N,
+                                 L.Cin, L.Cout, L.H, L.W, L.stride, Lb.DT_BF16, Lb.PATH_AUTO, sh)
+    elif d["cat_a"]:
+        Lb.conv3x3_dgrad_cat(d["dy"], d["w"], d["dxa"], d["dxb"], d["cat_a"], d.get("za"),
+                             d.get("zb"), d.get("act_in", 0), L.N, L.Cin, L.Cout, L.H, L.W,
+                             Lb.DT_BF16, Lb.PATH_AUTO, sh)
+    elif wl.fused_act:
+        Lb.conv3x3_dgrad_act(d["dy"], d["w"], d["zin"], d["act_in"], d["dx"], L.N, L.Cin, L.Cout,
+                             L.H, L.W, Lb.DT_BF16, Lb.PATH_AUTO, sh)
+    else:
+        Lb.conv3x3_dgrad(d["dy"], d["w"], d["dx"], L.N, L.Cin, L.Cout, L.H, L.W, sh)
+    return 1
+
+
+def _wgrad(wl, i, sh):
+    from x3_convolution_gb300 import _lib as Lb
+    L, d = wl.layers[i], wl.dev[i]
+    if L.stride != 1:
+        Lb.conv3x3_wgrad_strided(d["x"], d["dy"], d["dw"], d["db"], L.N, L.Cin, L.Cout, L.H, L.W,
+                                 L.stride, wl.ws, wl.ws_bytes, Lb.PATH_AUTO, sh)
+    elif d["cat_a"]:
+        Lb.conv3x3_wgrad_cat(d["xa"], d["xb"], d["cat_a"], d["dy"], d["dw"], d["db"], L.N, L.Cin,
+                             L.Cout, L.H, L.W, wl.ws, wl.ws_bytes, Lb.PATH_AUTO, sh)
+    else:
+        Lb.conv3x3_wgrad(d["x"], d["dy"], d["dw"], d["db"], L.N, L.Cin, L.Cout, L.H, L.W, wl.ws,
+                         wl.ws_bytes, sh)
+    return 2  # partial-sum kernel + fixed-order reduction
+
+
+def run_step(wl: Workload, stream_handle: int, record=None, mark=None, interleave=False):
+    """One sweep through the C ABI: every layer's forward in network order, then
+    the backward in reverse order -- by default every dgrad, then every wgrad (a
+    wgrad needs only its layer's x and dy); with `interleave` each layer's
+    dgrad and wgrad back to back.  `record(kind, i, 0|1)` brackets each call,
+    `mark(pass)` the end of each pass.  Returns the number of kernel launches."""
+    def call(kind, fn, i):
+        if record is not None:
+            record(kind, i, 0)
+        k = fn(wl, i, stream_handle)
+        if record is not None:
+            record(kind, i, 1)
+        return k
+
     n = 0
-    for i, L in enumerate(wl.layers):
-        d = wl.dev[i]
-        if record is not None:
-            record("fwd", i, 0)
-        if L.stride != 1:
-            Lb.conv3x3_fwd_strided(d["x"], d["w"], d["b"], d["y"], d.get("z"), L.N, L.Cin, L.Cout,
-                                   L.H, L.W, L.stride, L.act, Lb.DT_BF16, Lb.PATH_AUTO,
-                                   stream_handle)
-        elif d["cat_a"]:
-            Lb.conv3x3_fwd_cat(d["xa"], d["xb"], d["cat_a"], d["w"], d["b"], d["y"], d.get("z"),
-                               L.N, L.Cin, L.Cout, L.H, L.W, L.act, Lb.DT_BF16, Lb.PATH_AUTO,
-                               stream_handle)
-        elif wl.fused_act:
-            Lb.conv3x3_fwd_save_z(d["x"], d["w"], d["b"], d["y"], d["z"], L.N, L.Cin, L.Cout, L.H,
-                                  L.W, L.act, Lb.DT_BF16, Lb.PATH_AUTO, stream_handle)
-        else:
-            Lb.conv3x3_fwd(d["x"], d["w"], d["b"], d["y"], L.N, L.Cin, L.Cout, L.H, L.W, L.act,
-                           stream_handle)
-        if record is not None:
-            record("fwd", i, 1)
-        n += 1
-    for i in reversed(range(len(wl.layers))):
-        L = wl.layers[i]
-        d = wl.dev[i]
-        if record is not None:
-            record("dgrad", i, 0)
-        if L.stride != 1:
-            Lb.conv3x3_dgrad_strided(d["dy"], d["w"], d["dx"], d.get("zin"), d.get("act_in", 0),
-                                     L.N, L.Cin, L.Cout, L.H, L.W, L.stride, Lb.DT_BF16,
-                                     Lb.PATH_AUTO, stream_handle)
-        elif d["cat_a"]:
-            Lb.conv3x3_dgrad_cat(d["dy"], d["w"], d["dxa"], d["dxb"], d["cat_a"], d.get("za"),
-                                 d.get("zb"), d.get("act_in", 0), L.N, L.Cin, L.Cout, L.H, L.W,
-                                 Lb.DT_BF16, Lb.PATH_AUTO, stream_handle)
-        elif wl.fused_act:
-            Lb.conv3x3_dgrad_act(d["dy"], d["w"], d["zin"], d["act_in"], d["dx"], L.N, L.Cin,
-                                 L.Cout, L.H, L.W, Lb.DT_BF16, Lb.PATH_AUTO, stream_handle)
-        else:
-            Lb.conv3x3_dgrad(d["dy"], d["w"], d["dx"], L.N, L.Cin, L.Cout, L.H, L.W, stream_handle)
-        if record is not None:
-            record("dgrad", i, 1)
-            record("wgrad", i, 0)
-        if L.stride != 1:
-            Lb.conv3x3_wgrad_strided(d["x"], d["dy"], d["dw"], d["db"], L.N, L.Cin, L.Cout, L.H,
-                                     L.W, L.stride, wl.ws, wl.ws_bytes, Lb.PATH_AUTO,
-                                     stream_handle)
-        elif d["cat_a"]:
-            Lb.conv3x3_wgrad_cat(d["xa"], d["xb"], d["cat_a"], d["dy"], d["dw"], d["db"], L.N,
-                                 L.Cin, L.Cout, L.H, L.W, wl.ws, wl.ws_bytes, Lb.PATH_AUTO,
-                                 stream_handle)
-        else:
-            Lb.conv3x3_wgrad(d["x"], d["dy"], d["dw"], d["db"], L.N, L.Cin, L.Cout, L.H, L.W, wl.ws,
-                             wl.ws_bytes, stream_handle)
-        if record is not None:
-            record("wgrad", i, 1)
-        n += 3  # dgrad: 1 kernel; wgrad: partial-sum kernel + fixed-order reduction
+    if mark is not None:
+        mark("start")
+    for i in range(len(wl.layers)):
+        n += call("fwd", _fwd, i)
+    if mark is not None:
+        mark("fwd")
+    back = list(reversed(range(len(wl.layers))))
+    if interleave:
+        for i in back:
+            n += call("dgrad", _dgrad, i)
+            n += call("wgrad", _wgrad, i)
+        return n
+    for i in back:
+        n += call("dgrad", _dgrad, i)
+    if mark is not None:
+        mark("dgrad")
+    for i in back:
+        n += call("wgrad", _wgrad, i)
+    if mark is not None:
+        mark("wgrad")
     return n
 
 
@@ -373,16 +400,17 @@ def cuda_arm(args):
     if st != Lb.OK:
         raise RuntimeError("device status after warm-up: " + Lb.status_string(st))
 
-    # timed steps: one event pair per step, per-call events for the breakdown
-    nlay = len(layers)
-    per_call = {"fwd": [[None, None] for _ in range(nlay)], "dgrad": [[None, None] for _ in range(nlay)],
-                "wgrad": [[None, None] for _ in range(nlay)]}
-    call_ms = {k: np.zeros(nlay) for k in per_call}
+    # Timed steps: CUDA events on the launching stream at the step's start and
+    # at the end of each pass (forward, dgrad, wgrad): four events per step,
+    # so the breakdown costs the step nothing measurable.  Per-call events
+    # (--detail) are recorded in extra steps after the timed region.
+    fam_ms = {"fwd": 0.0, "dgrad": 0.0, "wgrad": 0.0}
+    marks = {}
 
-    def record(kind, i, which):
+    def mark(name):
         e = torch.cuda.Event(enable_timing=True)
         e.record(stream)
-        per_call[kind][i][which] = e
+        marks[name] = e
 
     sampler = ClockSampler(gpu_selector(device))
     sampler.start()
@@ -396,17 +424,12 @@ def cuda_arm(args):
     for _ in range(args.steps):
         with torch.cuda.stream(stream):
             flush.zero_()  # same stream, before the start event: evict L2
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        launches += run_step(wl, sh, record=record)
-        e1.record(stream)
+        launches += run_step(wl, sh, mark=mark)
         torch.cuda.synchronize(device)
-        step_ms.append(e0.elapsed_time(e1))
-        for k in per_call:
-            for i in range(nlay):
-                a, b = per_call[k][i]
-                call_ms[k][i] += a.elapsed_time(b)
+        step_ms.append(marks["start"].elapsed_time(marks["wgrad"]))
+        fam_ms["fwd"] += marks["start"].elapsed_time(marks["fwd"])
+        fam_ms["dgrad"] += marks["fwd"].elapsed_time(marks["dgrad"])
+        fam_ms["wgrad"] += marks["dgrad"].elapsed_time(marks["wgrad"])
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -423,27 +446,49 @@ def cuda_arm(args):
     # per-pass breakdown and the roofline of the dominant kernel family
     K = args.steps
     fam = {}
+    fl = sum(L.flops_per_pass() for L in layers)
     for k in ("fwd", "dgrad", "wgrad"):
-        t = call_ms[k].sum() / K  # ms per step
-        fl = sum(L.flops_per_pass() for L in layers)
+        t = fam_ms[k] / K  # ms per step
         fam[k] = {"ms_per_step": round(float(t), 4), "tflops": round(fl / (t * 1e-3) / 1e12, 1)}
     dom = max(fam, key=lambda k: fam[k]["ms_per_step"])
-    dom_flops_per_step = sum(L.flops_per_pass() for L in layers)
-    achieved = dom_flops_per_step / (fam[dom]["ms_per_step"] * 1e-3) / 1e12
+    achieved = fl / (fam[dom]["ms_per_step"] * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
     roof_s = sum(sum(roofline_time_s(L, peaks).values()) for L in layers)
-    per_layer = []
-    for i, L in enumerate(layers):
-        rt = roofline_time_s(L, peaks)
-        per_layer.append({
-            "name": L.name, "N": L.N, "Cin": L.Cin, "Cout": L.Cout, "H": L.H, "W": L.W,
-            "stride": L.stride,
-            "path": {k: ["auto", "tensor", "simt"][max(0, Lb.conv3x3_auto_path(j, L.N, L.Cin, L.Cout, L.H, L.W))]
-                     for j, k in enumerate(("fwd", "dgrad", "wgrad"))},
-            "us": {k: round(float(call_ms[k][i] / K * 1e3), 2) for k in call_ms},
-            "tflops": {k: round(L.flops_per_pass() / (call_ms[k][i] / K * 1e-3) / 1e12, 1) for k in call_ms},
-            "roofline_frac": {k: round(rt[k] / (call_ms[k][i] / K * 1e-3), 3) for k in call_ms},
-        })
+
+    # per-layer detail: extra (untimed) steps with an event pair around every call
+    per_layer = None
+    if args.detail:
+        nlay = len(layers)
+        per_call = {k: [[None, None] for _ in range(nlay)] for k in fam}
+        call_ms = {k: np.zeros(nlay) for k in fam}
+
+        def record(kind, i, which):
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            per_call[kind][i][which] = e
+
+        nd = max(3, min(K, 10))
+        for _ in range(nd):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+            run_step(wl, sh, record=record)
+            torch.cuda.synchronize(device)
+            for k in per_call:
+                for i in range(nlay):
+                    a, b = per_call[k][i]
+                    call_ms[k][i] += a.elapsed_time(b)
+        per_layer = []
+        for i, L in enumerate(layers):
+            rt = roofline_time_s(L, peaks)
+            per_layer.append({
+                "name": L.name, "N": L.N, "Cin": L.Cin, "Cout": L.Cout, "H": L.H, "W": L.W,
+                "stride": L.stride,
+                "path": {k: ["auto", "tensor", "simt"][max(0, Lb.conv3x3_auto_path(j, L.N, L.Cin, L.Cout, L.H, L.W))]
+                         for j, k in enumerate(("fwd", "dgrad", "wgrad"))},
+                "us": {k: round(float(call_ms[k][i] / nd * 1e3), 2) for k in call_ms},
+                "tflops": {k: round(L.flops_per_pass() / (call_ms[k][i] / nd * 1e-3) / 1e12, 1) for k in call_ms},
+                "roofline_frac": {k: round(rt[k] / (call_ms[k][i] / nd * 1e-3), 3) for k in call_ms},
+            })
 
     # end to end through the C ABI from pinned host buffers
     e2e = None
@@ -451,8 +496,9 @@ def cuda_arm(args):
         # Pipelined through the public calls: one stream uploads every layer's
         # forward inputs (network order) and then its dy (reverse order, the
         # order the backward consumes them); the compute stream waits only for
-        # the layer it is about to run; a third stream downloads each layer's
-        # dw and dbias as soon as its wgrad is done.
+        # the layer it is about to run, and runs each layer's dgrad and wgrad
+        # back to back so that the backward trails the uploads closely; a third
+        # stream downloads each layer's dw and dbias as soon as its wgrad is done.
         up = torch.cuda.Stream(device=device)
         down = torch.cuda.Stream(device=device)
         nl = len(wl.layers)
@@ -484,7 +530,7 @@ def cuda_arm(args):
                     wl.dev[i]["dy"].copy_(wl.host[i]["dy"], non_blocking=True)
                     ev_dy_in[i].record(up)
             with torch.cuda.stream(stream):
-                run_step(wl, sh, record=hook)
+                run_step(wl, sh, record=hook, interleave=True)
             down.synchronize()
             stream.synchronize()
         e2e_step()
@@ -532,7 +578,7 @@ def cuda_arm(args):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clocks,
-        "layers_detail": per_layer if args.detail else None,
+        "layers_detail": per_layer,
     }
     return line
 
