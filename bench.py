@@ -401,9 +401,12 @@ def cuda_arm(args):
         raise RuntimeError("device status after warm-up: " + Lb.status_string(st))
 
     # Timed steps: CUDA events on the launching stream at the step's start and
-    # at the end of each pass (forward, dgrad, wgrad): four events per step,
-    # so the breakdown costs the step nothing measurable.  Per-call events
-    # (--detail) are recorded in extra steps after the timed region.
+    # at the end of each pass (forward, dgrad, wgrad).  By default the step's
+    # C ABI calls and these events are captured once into a CUDA graph that
+    # each timed step replays on the same stream (the launches of 132 kernels
+    # then cost the GPU no gaps); --no-graph launches them one by one.
+    # Per-call events (--detail) are recorded in extra steps after the timed
+    # region.
     fam_ms = {"fwd": 0.0, "dgrad": 0.0, "wgrad": 0.0}
     marks = {}
 
@@ -411,6 +414,24 @@ def cuda_arm(args):
         e = torch.cuda.Event(enable_timing=True)
         e.record(stream)
         marks[name] = e
+
+    def mark_in_graph(name):
+        # an event record node of the graph (re-recorded at every replay)
+        e = torch.cuda.Event(enable_timing=True, external=True)
+        e.record(stream)
+        marks[name] = e
+
+    graph = None
+    launches_per_step = 0
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            launches_per_step = run_step(wl, sh, mark=mark_in_graph)
+        torch.cuda.synchronize(device)
+        for _ in range(args.warmup):
+            with torch.cuda.stream(stream):
+                graph.replay()
+        torch.cuda.synchronize(device)
 
     sampler = ClockSampler(gpu_selector(device))
     sampler.start()
@@ -424,7 +445,11 @@ def cuda_arm(args):
     for _ in range(args.steps):
         with torch.cuda.stream(stream):
             flush.zero_()  # same stream, before the start event: evict L2
-        launches += run_step(wl, sh, mark=mark)
+            if graph is not None:
+                graph.replay()
+                launches += launches_per_step
+        if graph is None:
+            launches += run_step(wl, sh, mark=mark)
         torch.cuda.synchronize(device)
         step_ms.append(marks["start"].elapsed_time(marks["wgrad"]))
         fam_ms["fwd"] += marks["start"].elapsed_time(marks["fwd"])
@@ -518,8 +543,10 @@ def cuda_arm(args):
                     wl.host[i]["dw"].copy_(wl.dev[i]["dw"], non_blocking=True)
                     wl.host[i]["db"].copy_(wl.dev[i]["db"], non_blocking=True)
 
-        def e2e_step():
-            up.wait_stream(stream)     # the previous step no longer reads the inputs
+        def e2e_body():
+            # fork: the copy streams start after everything already on `stream`
+            up.wait_stream(stream)
+            down.wait_stream(stream)
             with torch.cuda.stream(up):
                 for i, (h, d) in enumerate(zip(wl.host, wl.dev)):
                     for k in wl.inputs(h):
@@ -531,7 +558,26 @@ def cuda_arm(args):
                     ev_dy_in[i].record(up)
             with torch.cuda.stream(stream):
                 run_step(wl, sh, record=hook, interleave=True)
-            down.synchronize()
+            # join: `stream` ends after the last download
+            stream.wait_stream(down)
+            stream.wait_stream(up)
+
+        # The same step, host copies included, as one CUDA graph (memcpy nodes
+        # from the pinned host buffers, the C ABI kernels, cross-stream event
+        # edges) so that host-side launch overhead does not pace it.
+        e2e_graph = None
+        if graph is not None:
+            e2e_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(e2e_graph, stream=stream):
+                e2e_body()
+            torch.cuda.synchronize(device)
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                if e2e_graph is not None:
+                    e2e_graph.replay()
+                else:
+                    e2e_body()
             stream.synchronize()
         e2e_step()
         n_e2e = max(3, min(args.steps, 10))
@@ -545,6 +591,7 @@ def cuda_arm(args):
         e2e_ms = max_over_ranks(e2e_ms, ws, device)
         e2e = {"value": round(flops_step * ws / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                "ms_per_step": round(e2e_ms, 3), "steps": n_e2e,
+               "launch": "stream" if e2e_graph is None else "CUDA graph (copies + C ABI calls)",
                "h2d_bytes_per_step": wl.h2d_bytes(), "d2h_bytes_per_step": wl.d2h_bytes()}
 
     cpu = None
@@ -565,6 +612,7 @@ def cuda_arm(args):
                    "layout": "NHWC bf16 activations, KRSC bf16 weights, fp32 accumulate",
                    "l2": "flushed between steps (write of 2x L2)",
                    "flops_per_step": flops_step, "flops_per_step_padded_cin": flops_padded,
+                   "launch": "stream" if graph is None else "CUDA graph of the step's C ABI calls",
                    "fused_act_backward": bool(args.fused_act),
                    "concat_free_up_path": bool(args.concat_free)},
         "pct_of_roofline": round(roof_s / (ms * 1e-3), 4),
@@ -667,6 +715,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--detail", action="store_true", help="add a per-layer breakdown")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the timed steps call by call instead of replaying a CUDA graph")
     ap.add_argument("--concat-free", action="store_true",
                     help="up-path convs take main and skip as two tensors (no concat buffer)")
     ap.add_argument("--fused-act", action="store_true",
