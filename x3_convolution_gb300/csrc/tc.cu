@@ -442,8 +442,21 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, kDgrad ? 1 : 0);
+      // One thread issues every MMA, and its instruction path per k-block
+      // sets the pace when the MMAs are short (N = 128: 64 cycles each), so
+      // the descriptors are built once: a stage, a sub-tile or a K step only
+      // moves the start-address field (bits 0-13, 16-byte units), and no
+      // offset inside the shared-memory allocation carries out of it.
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
+      const uint64_t b_desc0 = kDgrad ? smem_desc(sbase + Cfg::kATileBytes, 8192, 1024, kSwizzle128B)
+                                      : smem_desc(sbase + Cfg::kATileBytes, 16, 1024, kSwizzle128B);
+      constexpr uint32_t kStageStep = Cfg::kStageBytes >> 4;
+      constexpr uint32_t kBKStep = (kDgrad ? 2048u : 32u) >> 4;  // per K step of 16
+      constexpr uint32_t kAKStep = 32u >> 4;
+      constexpr uint32_t kSubStep = kABytes >> 4;
       int stage = 0;
-      uint32_t phase = 0;
+      uint32_t phase = 0, stage_off = 0;
       int buf = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
@@ -458,21 +471,19 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(smem + (size_t)stage * Cfg::kStageBytes);
-          const uint32_t b_base = a_base + Cfg::kATileBytes;
+          const uint64_t ad = a_desc0 + stage_off, bd = b_desc0 + stage_off;
+          const uint32_t acc0 = kb != 0 ? 1u : 0u;  // the tile's first K step starts the sum
 #pragma unroll
-          for (int k = 0; k < BKC / 16; ++k) {
-            const uint64_t bdesc = kDgrad ? smem_desc(b_base + k * 2048, 8192, 1024, kSwizzle128B)
-                                          : smem_desc(b_base + k * 32, 16, 1024, kSwizzle128B);
+          for (int k = 0; k < BKC / 16; ++k)
 #pragma unroll
             for (int u = 0; u < MT; ++u)
-              tc_mma_bf16(d_tmem + (uint32_t)(u * BN),
-                          smem_desc(a_base + u * kABytes + k * 32, 16, 1024, kSwizzle128B), bdesc,
-                          idesc, (kb | k) != 0 ? 1u : 0u);
-          }
+              tc_mma_bf16(d_tmem + (uint32_t)(u * BN), ad + (uint64_t)(u * kSubStep + k * kAKStep),
+                          bd + (uint64_t)(k * kBKStep), idesc, k == 0 ? acc0 : 1u);
           tc_commit(&empty[stage]);
+          stage_off += kStageStep;
           if (++stage == S) {
             stage = 0;
+            stage_off = 0;
             phase ^= 1;
           }
         }
@@ -1154,8 +1165,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc256 = idesc_bf16_f32(128, 256, 1, 1);
       constexpr uint32_t idesc128 = idesc_bf16_f32(128, 128, 1, 1);
       constexpr uint32_t idesc144 = idesc_bf16_f32(128, 144, 1, 1);
+      const uint32_t idesc_t2 = do_bias ? idesc144 : idesc128;
+      // descriptors built once; stages and K steps move the start address only
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t a_desc0 = smem_desc(sbase, 8192, 1024, kSwizzle128B);
+      const uint64_t b_desc0 = smem_desc(sbase + kWgABytes, 8192, 1024, kSwizzle128B);
+      constexpr uint32_t kStageStep = kWgStageBytes >> 4;
+      constexpr uint32_t kKStep = 2048u >> 4;
+      constexpr uint32_t kTap2 = (2 * kWgBBytes) >> 4;
       int stage = 0;
-      uint32_t phase = 0;
+      uint32_t phase = 0, stage_off = 0;
       bool ok = true;
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) {
@@ -1163,23 +1182,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a_base = smem_u32(smem + (size_t)stage * kWgStageBytes);
-        const uint32_t b_base = a_base + kWgABytes;
+        const uint64_t ad = a_desc0 + stage_off, bd = b_desc0 + stage_off;
+        const uint32_t acc0 = kb != kb0 ? 1u : 0u;
 #pragma unroll
         for (int k = 0; k < kWgPix / 16; ++k) {
-          const uint32_t acc = (kb != kb0 || k != 0) ? 1u : 0u;
-          const uint64_t adesc = smem_desc(a_base + k * 2048, 8192, 1024, kSwizzle128B);
+          const uint32_t acc = k == 0 ? acc0 : 1u;
           // taps 0 and 1: four 64-channel blocks at 8 KB stride -> one N = 256 MMA
-          tc_mma_bf16(tmem_base, adesc, smem_desc(b_base + k * 2048, 8192, 1024, kSwizzle128B),
-                      idesc256, acc);
+          tc_mma_bf16(tmem_base, ad + (uint64_t)(k * kKStep), bd + (uint64_t)(k * kKStep), idesc256,
+                      acc);
           // tap 2 (+ the ones block as a third 64-column block when this CTA owns dbias)
-          tc_mma_bf16(tmem_base + 256, adesc,
-                      smem_desc(b_base + 2 * kWgBBytes + k * 2048, 8192, 1024, kSwizzle128B),
-                      do_bias ? idesc144 : idesc128, acc);
+          tc_mma_bf16(tmem_base + 256, ad + (uint64_t)(k * kKStep),
+                      bd + (uint64_t)(kTap2 + k * kKStep), idesc_t2, acc);
         }
         tc_commit(&empty[stage]);
+        stage_off += kStageStep;
         if (++stage == kWgStages) {
           stage = 0;
+          stage_off = 0;
           phase ^= 1;
         }
       }
