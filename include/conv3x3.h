@@ -53,6 +53,9 @@
  * 2*MT*BN <= 512) selects the im2col kernel with MT*128 pixels x BN channels,
  * "halo<BN>" (BN in {64,128}; images of width 16, 32 or 64 whose height is a
  * multiple of 256/W) the row-halo kernel.  Unset, the library picks.
+ * CONV3X3_KC=1|2 forces the 64-channel chunks per pipeline stage of the im2col
+ * kernel (2 for 128x1 tiles unless set).  CONV3X3_WGRAD_SPLITS=<S> forces the
+ * weight gradient's split count (set it before querying the workspace size).
  */
 #ifndef CONV3X3_H
 #define CONV3X3_H

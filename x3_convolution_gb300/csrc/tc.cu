@@ -87,13 +87,22 @@ __device__ __forceinline__ unsigned long long drain_wait_ns(unsigned long long w
 constexpr int pow2_cols(int n) { return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512; }
 
 // MT = pixel sub-tiles of 128 per CTA tile (two MMAs share each B stage when
-// MT = 2, halving the B bytes per unit of tensor work).
-template <int BN, int MT>
+// MT = 2, halving the B bytes per unit of tensor work).  KC = 64-channel chunks
+// per stage: KC = 2 doubles the tensor work per pipeline round trip, which the
+// single issuing thread needs when each chunk holds only 4 x N = 128 MMAs.
+// Stage layout: KC chunks of A (MT boxes each), then KC chunks of B.
+template <int BN, int MT, int KC = 1>
 struct IgemmCfg {
-  static constexpr uint32_t kATileBytes = MT * kABytes;
-  static constexpr uint32_t kBBytes = BN * BKC * 2;
+  static constexpr uint32_t kChunkA = MT * kABytes;
+  static constexpr uint32_t kChunkB = BN * BKC * 2;
+  static constexpr uint32_t kATileBytes = KC * kChunkA;
+  static constexpr uint32_t kBBytes = KC * kChunkB;
   static constexpr uint32_t kStageBytes = kATileBytes + kBBytes;
   static constexpr int kStages = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
+  // producers take whole stages in turn when the ring is deep enough for that
+  // (a parity wait is unambiguous only while S >= kProd); otherwise they split
+  // each stage's boxes
+  static constexpr bool kStagePar = kStageParallel && kStages >= kProd;
   static constexpr int kTmemCols = pow2_cols(2 * MT * BN);
   static_assert(2 * MT * BN <= 512, "double-buffered accumulators must fit in TMEM");
   // + barriers, + alignment slack, + a 16 KB guard so that no descriptor
@@ -107,6 +116,7 @@ struct IgemmParams {
   int act, out_f32;
   int P, H, W;
   int kchunks;    // ceil(A channels / 64)
+  int kgroups;    // k-blocks per tap: ceil(kchunks / KC)
   // Pixel traversal: P pixels of an (N, H, W) grid -- the output grid of the
   // forward, dx's grid of a stride-1 dgrad, dy's grid of a stride-2 dgrad.
   int ustride;    // forward: input row/column step per output pixel (1 or 2)
@@ -272,12 +282,12 @@ __device__ __forceinline__ int igemm_num_tiles(const IgemmParams& p, bool s2) {
 }
 
 __device__ __forceinline__ TileInfo tile_info(const IgemmParams& p, int tile, bool s2) {
-  if (!s2) return TileInfo{tile / p.num_n_tiles, tile % p.num_n_tiles, 0, 9 * p.kchunks};
+  if (!s2) return TileInfo{tile / p.num_n_tiles, tile % p.num_n_tiles, 0, 9 * p.kgroups};
   const int per = p.num_m_tiles * p.num_n_tiles;
   const int ci = tile / per, rest = tile - ci * per;
   const int cls = 3 - ci;  // cls = 2 ph + pw; the 4-tap class first
   const int ntaps = (1 + (cls >> 1)) * (1 + (cls & 1));
-  return TileInfo{rest / p.num_n_tiles, rest % p.num_n_tiles, cls, ntaps * p.kchunks};
+  return TileInfo{rest / p.num_n_tiles, rest % p.num_n_tiles, cls, ntaps * p.kgroups};
 }
 
 // Tap `t` of class `cls`: weight tap r*3+s and the A window offsets (dj, di).
@@ -291,16 +301,17 @@ __device__ __forceinline__ void s2_tap(int cls, int t, int& wtap, int& dj, int& 
 }
 // kExt = false: no fused extras and no stride-2 dgrad (p.s2, p.zout, p.zin
 // and the split output are ignored).
-template <int BN, int MT, bool kDgrad, bool kExt>
+template <int BN, int MT, bool kDgrad, bool kExt, int KC>
 __global__ void __launch_bounds__(kIgemmThreads, 1)
     k_igemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
             const __grid_constant__ CUtensorMap tmB, const IgemmParams p) {
-  using Cfg = IgemmCfg<BN, MT>;
+  using Cfg = IgemmCfg<BN, MT, KC>;
   constexpr int S = Cfg::kStages;
   constexpr int TM = BM * MT;  // pixels per CTA tile
   // A producer's parity wait on a stage is unambiguous only while no producer
   // can run a whole ring ahead: stage-parallel mode needs S >= kProd.
-  static_assert(!kStageParallel || S >= kProd, "stage-parallel producers need S >= kProd");
+  constexpr bool kSP = Cfg::kStagePar;
+  static_assert(!kSP || S >= kProd, "stage-parallel producers need S >= kProd");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * Cfg::kStageBytes);
@@ -318,7 +329,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], kStageParallel ? 1 : kProd);
+      mbar_init(&full[i], kSP ? 1 : kProd);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -368,7 +379,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
           cw[u] = s2 ? rem - h0 * p.W : p.ustride * (rem - h0 * p.W) - 1;
         }
         for (int kb = 0; kb < ti.kblocks; ++kb) {
-          const int tap = kb / p.kchunks, cc = kb - tap * p.kchunks;
+          const int tap = kb / p.kgroups, cg = (kb - tap * p.kgroups) * KC;
           // A window offsets and weight tap of this k-block
           int wtap, off_w, off_h;
           if (s2) {
@@ -379,7 +390,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
             wtap = kDgrad ? 8 - tap : tap;
           }
           // stage-parallel mode: this producer owns every kProd-th stage
-          const bool mine = kStageParallel ? (issued % kProd == warp) : true;
+          const bool mine = kSP ? (issued % kProd == warp) : true;
           if (mine) {
             if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
               ok = false;
@@ -392,27 +403,31 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
             constexpr bool kOneB = !kDgrad && kOneWeightBox;
             constexpr int kBBoxes = kOneB ? 1 : BN / 64;
             constexpr uint32_t kBBox = kOneB ? (uint32_t)BN * 128u : 8192u;
-            constexpr int kBoxes = MT + kBBoxes;
+            constexpr int kPer = MT + kBBoxes;  // boxes per chunk
+            constexpr int kBoxes = KC * kPer;
             uint32_t bytes = 0;
 #pragma unroll
             for (int b = 0; b < kBoxes; ++b)
-              if (kStageParallel || b % kProd == warp) bytes += b < MT ? kABytes : kBBox;
+              if (kSP || b % kProd == warp) bytes += b % kPer < MT ? kABytes : kBBox;
             mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
             for (int b = 0; b < kBoxes; ++b) {
-              if (!kStageParallel && b % kProd != warp) continue;
-              if (b < MT) {
+              if (!kSP && b % kProd != warp) continue;
+              // chunk cc of the stage (a chunk past the channels reads zeros)
+              const int c = b / kPer, r = b - c * kPer, cc = cg + c;
+              if (r < MT) {
                 // channel-split input: chunks past kchunks_a read the second tensor
                 const bool second = cc >= p.kchunks_a;
-                tma_load_im2col_4d(sa + b * kABytes, second ? &tmA2 : &tmA, &full[stage],
-                                   (second ? cc - p.kchunks_a : cc) * BKC, cw[b], ch[b], cn[b],
-                                   (uint16_t)off_w, (uint16_t)off_h);
+                tma_load_im2col_4d(sa + c * Cfg::kChunkA + r * kABytes, second ? &tmA2 : &tmA,
+                                   &full[stage], (second ? cc - p.kchunks_a : cc) * BKC, cw[r],
+                                   ch[r], cn[r], (uint16_t)off_w, (uint16_t)off_h);
               } else {
-                const int j = b - MT;
+                const int j = r - MT;
+                uint8_t* dst = sb + c * Cfg::kChunkB;
                 if (!kDgrad)
-                  tma_load_3d(sb + j * kBBox, &tmB, &full[stage], cc * BKC, wtap, nt * BN + j * 64);
+                  tma_load_3d(dst + j * kBBox, &tmB, &full[stage], cc * BKC, wtap, nt * BN + j * 64);
                 else
-                  tma_load_3d(sb + j * 8192, &tmB, &full[stage], nt * BN + j * 64, wtap, cc * BKC);
+                  tma_load_3d(dst + j * 8192, &tmB, &full[stage], nt * BN + j * 64, wtap, cc * BKC);
               }
             }
           }
@@ -474,11 +489,15 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
           const uint64_t ad = a_desc0 + stage_off, bd = b_desc0 + stage_off;
           const uint32_t acc0 = kb != 0 ? 1u : 0u;  // the tile's first K step starts the sum
 #pragma unroll
-          for (int k = 0; k < BKC / 16; ++k)
+          for (int c = 0; c < KC; ++c)
 #pragma unroll
-            for (int u = 0; u < MT; ++u)
-              tc_mma_bf16(d_tmem + (uint32_t)(u * BN), ad + (uint64_t)(u * kSubStep + k * kAKStep),
-                          bd + (uint64_t)(k * kBKStep), idesc, k == 0 ? acc0 : 1u);
+            for (int k = 0; k < BKC / 16; ++k)
+#pragma unroll
+              for (int u = 0; u < MT; ++u)
+                tc_mma_bf16(d_tmem + (uint32_t)(u * BN),
+                            ad + (uint64_t)(c * (Cfg::kChunkA >> 4) + u * kSubStep + k * kAKStep),
+                            bd + (uint64_t)(c * (Cfg::kChunkB >> 4) + k * kBKStep), idesc,
+                            (c == 0 && k == 0) ? acc0 : 1u);
           tc_commit(&empty[stage]);
           stage_off += kStageStep;
           if (++stage == S) {
@@ -1535,13 +1554,13 @@ int set_smem(K kernel, size_t bytes, int device) {
   return CONV3X3_OK;
 }
 
-template <int BN, int MT, bool kDgrad>
+template <int BN, int MT, bool kDgrad, int KC = 1>
 int launch_igemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
                  const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
-  using Cfg = IgemmCfg<BN, MT>;
+  using Cfg = IgemmCfg<BN, MT, KC>;
   // the fused extras, a split output or a stride-2 dgrad need the full epilogue
   const bool ext = prm.zout || prm.zin || prm.out2 || prm.s2;
-  auto kern = ext ? k_igemm<BN, MT, kDgrad, true> : k_igemm<BN, MT, kDgrad, false>;
+  auto kern = ext ? k_igemm<BN, MT, kDgrad, true, KC> : k_igemm<BN, MT, kDgrad, false, KC>;
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int tiles = (prm.s2 ? 4 : 1) * prm.num_m_tiles * prm.num_n_tiles;
   const int grid = tiles < d.num_sms ? tiles : d.num_sms;
@@ -1643,6 +1662,7 @@ int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const
   prm.H = s.H;
   prm.W = s.W;
   prm.kchunks = 1;
+  prm.kgroups = 1;
   prm.kchunks_a = 1;
   prm.ustride = 1;
   prm.s2 = 0;
@@ -1722,6 +1742,7 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   prm.ow = s.W;
   prm.kchunks_a = split_a ? cat.Ca / BKC : (a_ch + BKC - 1) / BKC;
   prm.kchunks = split_a ? prm.kchunks_a + (a_ch - cat.Ca + BKC - 1) / BKC : prm.kchunks_a;
+  prm.kgroups = prm.kchunks;
   prm.nout = nout;
   prm.nsplit = (cat.on() && dgrad) ? cat.Ca : nout;
   prm.out2 = (cat.on() && dgrad) ? cat.b : nullptr;
@@ -1748,18 +1769,34 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
     C3_HALO(16, 128);
 #undef C3_HALO
   }
-#define C3_LAUNCH(BN_, MT_) \
-  return dgrad ? launch_igemm<BN_, MT_, true>(ta, ta2, tb, prm, d, st) \
-               : launch_igemm<BN_, MT_, false>(ta, ta2, tb, prm, d, st)
+  // Two 64-channel chunks per k-block where the tile's MMAs are short (see
+  // IgemmCfg); CONV3X3_KC=1|2 overrides the choice (tuning).
+  int kc = (ts.mt == 1 && bn == 128) ? 2 : 1;
+  if (const char* e = std::getenv("CONV3X3_KC")) {
+    const int v = std::atoi(e);
+    if (v == 1 || v == 2) kc = v;
+  }
+  if (kc == 2 && !((ts.mt == 1 && (bn == 128 || bn == 192 || bn == 256)) || (ts.mt == 2 && bn == 128)))
+    kc = 1;
+  prm.kgroups = (prm.kchunks + kc - 1) / kc;
+#define C3_LAUNCH(BN_, MT_, KC_) \
+  return dgrad ? launch_igemm<BN_, MT_, true, KC_>(ta, ta2, tb, prm, d, st) \
+               : launch_igemm<BN_, MT_, false, KC_>(ta, ta2, tb, prm, d, st)
+  if (kc == 2) {
+    if (ts.mt == 2) C3_LAUNCH(128, 2, 2);
+    if (bn == 128) C3_LAUNCH(128, 1, 2);
+    if (bn == 192) C3_LAUNCH(192, 1, 2);
+    C3_LAUNCH(256, 1, 2);
+  }
   if (ts.mt == 2) {
-    if (bn == 64) C3_LAUNCH(64, 2);
-    C3_LAUNCH(128, 2);
+    if (bn == 64) C3_LAUNCH(64, 2, 1);
+    C3_LAUNCH(128, 2, 1);
   }
   switch (bn) {
-    case 64: C3_LAUNCH(64, 1);
-    case 128: C3_LAUNCH(128, 1);
-    case 192: C3_LAUNCH(192, 1);
-    default: C3_LAUNCH(256, 1);
+    case 64: C3_LAUNCH(64, 1, 1);
+    case 128: C3_LAUNCH(128, 1, 1);
+    case 192: C3_LAUNCH(192, 1, 1);
+    default: C3_LAUNCH(256, 1, 1);
   }
 #undef C3_LAUNCH
 }
