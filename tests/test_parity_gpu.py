@@ -271,6 +271,32 @@ def test_fused_activation_backward_tiles(tile, monkeypatch):
     assert rel_err(host(dx), oracle.conv3x3_dgrad_act(t.dy, t.w, zin_h, 1)) <= TOL_BF16
 
 
+# dgrad with 8 output channels and whole-row tiles of 128 pixels (the stem's
+# input gradient): T = dy x Wt on the tensor cores, then the nine-tap sum
+STEM_DGRAD_SHAPES = [
+    (2, 8, 128, 64, 64),   # two dx rows per tile
+    (3, 8, 64, 8, 32),     # 64 dy channels, four rows per tile
+    (4, 8, 128, 16, 8),    # sixteen rows of width 8 per tile
+    (2, 8, 128, 2, 64),    # one tile per image: both halo rows outside it
+]
+
+
+@pytest.mark.parametrize("shape", STEM_DGRAD_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_eight_output_channel_dgrad(shape):
+    t = _small(shape)
+    zin_h = synth.make_zin(t.layer, seed=7)
+    x, w, b, dy = dev_tensors(t)
+    dx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    dxbf = ops.dgrad(dy, w, path=L.PATH_TENSOR)
+    ga = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=L.PATH_TENSOR, z_in=to_dev_bf16(zin_h), act_in=1)
+    torch.cuda.synchronize()
+    ref = oracle.conv3x3_dgrad(t.dy, t.w)
+    assert rel_err(host(dx32), ref) <= TOL_BF16
+    assert check_bf16_store(host(dxbf), ref) == 0
+    assert np.array_equal(host(dxbf), rne_bf16(host(dx32)))
+    assert rel_err(host(ga), oracle.conv3x3_dgrad_act(t.dy, t.w, zin_h, 1)) <= TOL_BF16
+
+
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_wgrad_is_bit_deterministic(path):
     t = _small((4, 128, 128, 16, 16))

@@ -1042,6 +1042,281 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 }
 
 // ----------------------------------------------------------------------------
+// input gradient with 8 output channels (the stem): dy's 3x3 window folded in
+// after a single pass over dy
+// ----------------------------------------------------------------------------
+// dx[h][w][c] = sum_{r,s} T[h + 1 - r][w + 1 - s][(3 r + s) * 8 + c], where
+// T = dy x Wt is a plain GEMM over dy's K channels: Wt[(3 r + s) * 8 + c][k] =
+// w[k][r][s][c], 72 columns (padded to N = 80).  A CTA tile is R = 128 / W
+// rows of dx of one image; the tensor cores produce T for the R + 2 dy rows
+// around them (one TMA box per 64 channels: rows above the image or below it
+// read as zero), the epilogue warps stage T in shared memory and sum the nine
+// shifted slices.  dy is read about (R + 2) / R times instead of nine times.
+constexpr int kSdEpiWarps = 8;
+constexpr int kSdThreads = 32 * (kProd + 1 + kSdEpiWarps);
+constexpr int kSdN = 80;                  // MMA N: 72 used columns of T
+constexpr int kSdTPitch = 72;             // floats per staged T row
+constexpr uint32_t kSdChunkBytes = 256u * 128u;  // room for 256 dy pixels x 64 channels
+constexpr int kSdStages = 2;
+
+struct StemDgradParams {
+  void* out;
+  int out_f32;
+  const __nv_bfloat16* zin;  // optional act'(z_in) scaling (laid out like dx)
+  int zin_act;
+  int P, H, W, K, R;         // dx pixels, image height / width, dy channels, dx rows per tile
+  int num_tiles;
+  unsigned* status;
+  unsigned long long wait_ns;
+};
+
+__host__ __device__ constexpr size_t stem_dgrad_smem(int K) {
+  return (size_t)kSdStages * (K / 64) * kSdChunkBytes  // dy stages
+         + (size_t)(K / 8) * kSdN * 16                   // Wt, no-swizzle K-major
+         + (size_t)256 * kSdTPitch * 4                   // staged T
+         + 1024 + 256;                                   // alignment, barriers
+}
+
+__global__ void __launch_bounds__(kSdThreads, 1)
+    k_stem_dgrad(const __grid_constant__ CUtensorMap tmDY, const __nv_bfloat16* __restrict__ w,
+                 const StemDgradParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const int kchunks = p.K / 64;
+  const uint32_t stage_bytes = (uint32_t)kchunks * kSdChunkBytes;
+  uint8_t* wsm = smem + (size_t)kSdStages * stage_bytes;
+  const uint32_t wgroup_bytes = kSdN * 16;  // one 8-channel K group of Wt: 80 rows x 16 B
+  float* tsm = reinterpret_cast<float*>(wsm + (size_t)(p.K / 8) * wgroup_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(tsm + 256 * kSdTPitch);
+  uint64_t* empty = full + kSdStages;
+  uint64_t* tfull = empty + kSdStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* tready = tempty + 2;  // every epilogue warp has staged its T rows
+  uint64_t* tdone = tready + 1;   // every epilogue warp has finished reading them
+  uint64_t* drain = tdone + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows_per_img = p.H / p.R;
+  const int tpix = (p.R + 2) * p.W;  // T pixels of a tile (<= 256)
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < kSdStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kSdEpiWarps);
+    }
+    mbar_init(tready, kSdEpiWarps);
+    mbar_init(tdone, kSdEpiWarps);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmDY);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  // Wt from w [K][3][3][8]: element (n = 8 t + c, k) at group k/8, row n, 2 (k % 8) bytes;
+  // rows 72..79 are zero
+  for (int e = threadIdx.x; e < (p.K / 8) * kSdN; e += kSdThreads) {
+    const int g = e / kSdN, n = e - g * kSdN;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (n < 72) {
+      __nv_bfloat16 h[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) h[i] = w[(size_t)(g * 8 + i) * 72 + n];
+      v = *reinterpret_cast<const uint4*>(h);
+    }
+    *reinterpret_cast<uint4*>(wsm + (size_t)g * wgroup_bytes + n * 16) = v;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp < kProd) {
+    // ------------------------------------------------------------ TMA producer (warp 0)
+    if (warp == 0 && lane == 0) {
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const uint32_t box_bytes = (uint32_t)tpix * 128u;
+      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int n0 = tile / rows_per_img, h0 = (tile - n0 * rows_per_img) * p.R;
+        uint8_t* sa = smem + (size_t)stage * stage_bytes;
+        mbar_arrive_expect_tx(&full[stage], (uint32_t)kchunks * box_bytes);
+        for (int c = 0; c < kchunks; ++c)
+          tma_load_4d(sa + (size_t)c * kSdChunkBytes, &tmDY, &full[stage], c * 64, 0, h0 - 1, n0);
+        ++issued;
+        if (++stage == kSdStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) {
+        int n = issued < kSdStages ? issued : kSdStages;
+        for (int i = 0; i < n; ++i) {
+          if (--stage < 0) {
+            stage = kSdStages - 1;
+            phase ^= 1;
+          }
+          mbar_wait(&full[stage], phase, drain_wait_ns(p.wait_ns), nullptr, nullptr);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, kSdN, 0, 0);
+      const uint32_t sbase = smem_u32(smem), wbase = smem_u32(wsm);
+      int stage = 0, buf = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[buf], acc_phase ^ 1, p.wait_ns, p.status, abort_flag)) break;
+        if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t a0 = sbase + (uint32_t)stage * stage_bytes;
+        const uint32_t d0 = tmem_base + (uint32_t)(buf * 2 * kSdN);
+        for (int c = 0; c < kchunks; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // A: 128 dy pixels x 16 channels (SW128 K-major); B: 16 channels of Wt
+            // (no swizzle, K groups 1280 bytes apart, 8-row groups 128 bytes apart)
+            const uint64_t bdesc =
+                smem_desc(wbase + (uint32_t)((c * 4 + kk) * 2) * (kSdN * 16), kSdN * 16, 128, kSwizzleNone);
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+              tc_mma_bf16(d0 + (uint32_t)(u * kSdN),
+                          smem_desc(a0 + (uint32_t)c * kSdChunkBytes + (uint32_t)u * 16384u + kk * 32, 16,
+                                    1024, kSwizzle128B),
+                          bdesc, idesc, (c | kk) != 0 ? 1u : 0u);
+          }
+        tc_commit(&empty[stage]);
+        tc_commit(&tfull[buf]);
+        if (++stage == kSdStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (++buf == 2) {
+          buf = 0;
+          acc_phase ^= 1;
+        }
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, p.wait_ns, nullptr, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // warp (q = lane quarter, u = half): T pixel u*128 + 32 q + lane, staged in
+    // shared memory; then every thread sums four channels of one dx pixel.
+    const int ew = warp - (kProd + 1);
+    const int q = warp & 3, u = ew >> 2;
+    const int tp = u * 128 + q * 32 + lane;
+    const int e = ew * 32 + lane;  // 0..255
+    const int o = e >> 1, ch = (e & 1) * 4;
+    const int orow = o / p.W, ocol = o - orow * p.W;
+    int buf = 0;
+    uint32_t acc_phase = 0, tph = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
+      // the previous tile's gather must be done before T is overwritten
+      if (!mbar_wait(tdone, tph ^ 1, p.wait_ns, p.status, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 2 * kSdN + u * kSdN);
+      uint32_t v0[32], v1[32], v2[32];
+      tmem_ld_32x32b_x32(taddr, v0);
+      tmem_ld_32x32b_x32(taddr + 32, v1);
+      tmem_ld_32x32b_x32(taddr + 48, v2);  // columns 48..79 (72..79 unused)
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (tp < tpix) {
+        float4* trow = reinterpret_cast<float4*>(tsm + (size_t)tp * kSdTPitch);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          trow[i] = make_float4(__uint_as_float(v0[4 * i]), __uint_as_float(v0[4 * i + 1]),
+                                __uint_as_float(v0[4 * i + 2]), __uint_as_float(v0[4 * i + 3]));
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          trow[8 + i] = make_float4(__uint_as_float(v1[4 * i]), __uint_as_float(v1[4 * i + 1]),
+                                    __uint_as_float(v1[4 * i + 2]), __uint_as_float(v1[4 * i + 3]));
+        // columns 64..71 = v2[16..23]
+        trow[16] = make_float4(__uint_as_float(v2[16]), __uint_as_float(v2[17]), __uint_as_float(v2[18]),
+                               __uint_as_float(v2[19]));
+        trow[17] = make_float4(__uint_as_float(v2[20]), __uint_as_float(v2[21]), __uint_as_float(v2[22]),
+                               __uint_as_float(v2[23]));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tready);
+      if (!mbar_wait(tready, tph, p.wait_ns, p.status, abort_flag)) break;
+      // gather: dx(orow, ocol) channels ch..ch+3
+      const int n0 = tile / rows_per_img, h0 = (tile - n0 * rows_per_img) * p.R;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int r = 0; r < 3; ++r)
+#pragma unroll
+        for (int s = 0; s < 3; ++s) {
+          const int wc = ocol + 1 - s;
+          if (wc >= 0 && wc < p.W) {
+            const float4 t = *reinterpret_cast<const float4*>(
+                tsm + (size_t)((orow + 2 - r) * p.W + wc) * kSdTPitch + (r * 3 + s) * 8 + ch);
+            acc[0] += t.x;
+            acc[1] += t.y;
+            acc[2] += t.z;
+            acc[3] += t.w;
+          }
+        }
+      const long long pix = ((long long)n0 * p.H + h0 + orow) * p.W + ocol;
+      if (p.zin) {
+        const uint2 zz = *reinterpret_cast<const uint2*>(p.zin + pix * 8 + ch);
+        const __nv_bfloat162* zh = reinterpret_cast<const __nv_bfloat162*>(&zz);
+        const float2 z0 = __bfloat1622float2(zh[0]), z1 = __bfloat1622float2(zh[1]);
+        acc[0] *= act_grad_f32(p.zin_act, z0.x);
+        acc[1] *= act_grad_f32(p.zin_act, z0.y);
+        acc[2] *= act_grad_f32(p.zin_act, z1.x);
+        acc[3] *= act_grad_f32(p.zin_act, z1.y);
+      }
+      if (p.out_f32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + pix * 8 + ch) =
+            make_float4(acc[0], acc[1], acc[2], acc[3]);
+      } else {
+        uint2 o2;
+        __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o2);
+        oh[0] = __floats2bfloat162_rn(acc[0], acc[1]);
+        oh[1] = __floats2bfloat162_rn(acc[2], acc[3]);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + pix * 8 + ch) = o2;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tdone);
+      tph ^= 1;
+      if (++buf == 2) {
+        buf = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, 512);
+}
+
+// ----------------------------------------------------------------------------
 // wgrad split-K implicit GEMM
 // ----------------------------------------------------------------------------
 constexpr int kWgTaps = 3;                       // taps per CTA tile (one kernel row)
@@ -1680,6 +1955,50 @@ int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const
   return launch_stem<256>(ta, tb, prm, d, st);
 }
 
+// dgrad with 8 output channels (k_stem_dgrad): whole-row tiles of 128 dx
+// pixels, dy channels a multiple of 64 up to 128.
+bool stem_dgrad_fits(const Shape& s) {
+  if (s.Cin != 8 || s.u != 1 || s.Cout % 64 != 0 || s.Cout > 128) return false;
+  if (s.W > 64 || BM % s.W != 0) return false;
+  const int R = BM / s.W;
+  return R <= s.H && s.H % R == 0;
+}
+
+int run_stem_dgrad(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
+                   const EpiExtra& ex, const DevCtx& d, cudaStream_t st) {
+  PFN_encodeTiled enc = encode_tiled_fn();
+  if (!enc) return CONV3X3_ERR_CUDA;
+  const int R = BM / s.W;
+  CUtensorMap tdy;
+  cuuint64_t dims[4] = {(cuuint64_t)s.Cout, (cuuint64_t)s.W, (cuuint64_t)s.H, (cuuint64_t)s.N};
+  cuuint64_t strides[3] = {(cuuint64_t)s.Cout * 2, (cuuint64_t)s.W * s.Cout * 2,
+                           (cuuint64_t)s.H * s.W * s.Cout * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)s.W, (cuuint32_t)(R + 2), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (enc(&tdy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(dy), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return CONV3X3_ERR_CUDA;
+  StemDgradParams prm;
+  prm.out = dx;
+  prm.out_f32 = out_f32;
+  prm.zin = static_cast<const __nv_bfloat16*>(ex.zin);
+  prm.zin_act = ex.zin ? ex.zin_act : CONV3X3_ACT_NONE;
+  prm.P = (int)s.P();
+  prm.H = s.H;
+  prm.W = s.W;
+  prm.K = s.Cout;
+  prm.R = R;
+  prm.num_tiles = s.N * (s.H / R);
+  prm.status = d.status;
+  prm.wait_ns = d.wait_ns;
+  const size_t smem = stem_dgrad_smem(s.Cout);
+  if (set_smem(k_stem_dgrad, smem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+  const int grid = prm.num_tiles < d.num_sms ? prm.num_tiles : d.num_sms;
+  k_stem_dgrad<<<grid, kSdThreads, smem, st>>>(tdy, static_cast<const __nv_bfloat16*>(w), prm);
+  return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
 // Forward (a_src = x, a_ch = Cin) or dgrad (a_src = dy, a_ch = Cout).  With a
 // channel split the forward reads x's channels [Ca, Cin) from cat.b and the
 // dgrad writes dx's channels [Ca, Cin) to cat.b.
@@ -1870,6 +2189,9 @@ int tc_fwd(const void* x, const void* w, const float* bias, void* y, const Shape
 int tc_dgrad(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
              const EpiExtra& ex, const CatSplit& cat, const DevCtx& d, cudaStream_t st) {
   if (!tc_supports_cat(s, cat)) return CONV3X3_ERR_UNSUPPORTED;
+  // a forced im2col tile (CONV3X3_TILE) keeps the 8-channel dgrad on k_igemm
+  if (!cat.on() && stem_dgrad_fits(s) && std::getenv("CONV3X3_TILE") == nullptr)
+    return run_stem_dgrad(dy, w, dx, s, out_f32, ex, d, st);
   return run_igemm(true, dy, s.Cout, w, nullptr, dx, s, CONV3X3_ACT_NONE, out_f32, ex, cat, d, st);
 }
 
