@@ -132,7 +132,8 @@ def test_small_shapes_all_passes(shape, path):
     assert rel_err(host(db), rdb) <= TOL_BF16
 
 
-TILES = ["64x1", "128x1", "192x1", "256x1", "64x2", "128x2"]
+# "128x2" runs transposed (channels on TMEM lanes), "128x2n" is the same tile untransposed
+TILES = ["64x1", "128x1", "192x1", "256x1", "64x2", "128x2", "128x2n"]
 
 
 @pytest.mark.parametrize("tile", TILES)
@@ -253,7 +254,7 @@ def test_fused_activation_backward(shape, path):
     assert torch.equal(dxn, dxp)
 
 
-@pytest.mark.parametrize("tile", ["64x2", "256x1", "halo64"])
+@pytest.mark.parametrize("tile", ["64x2", "256x1", "halo64", "128x2", "128x2n"])
 def test_fused_activation_backward_tiles(tile, monkeypatch):
     monkeypatch.setenv("CONV3X3_TILE", tile)
     shape = (2, 64, 128, 16, 16)
@@ -487,6 +488,30 @@ def test_concat_free_convs(shape, path):
     assert rel_err(host(dw), rdw) <= TOL_BF16
     assert rel_err(host(db), rdb) <= TOL_BF16
     assert torch.equal(dw, dw_plain) and torch.equal(db, db_plain)
+
+
+@pytest.mark.parametrize("tile", ["128x2", "128x2n"])
+@pytest.mark.parametrize("shape", [(1, 128, 72, 200, 6, 11), (2, 128, 128, 128, 16, 16)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_concat_free_256_pixel_tiles(shape, tile, monkeypatch):
+    """Split input and split input gradient on the 256-pixel tiles, transposed
+    (one channel per epilogue thread) and not."""
+    monkeypatch.setenv("CONV3X3_TILE", tile)
+    N, Ca, Cb, Cout, H, W = shape
+    t, zin_h, _ = _cat_case(shape)
+    x, w, b, dy = dev_tensors(t)
+    xa, xb = x[..., :Ca].contiguous(), x[..., Ca:].contiguous()
+    y32 = ops.fwd_cat(xa, xb, w, b, act=1, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert rel_err(host(y32), oracle.conv3x3_fwd_cat(t.x[..., :Ca], t.x[..., Ca:], t.w, t.bias, 1)) <= TOL_BF16
+    zin = to_dev_bf16(zin_h)
+    za, zb = zin[..., :Ca].contiguous(), zin[..., Ca:].contiguous()
+    gxa, gxb = ops.dgrad_cat(dy, w, Ca, out_dtype=L.DT_F32, path=L.PATH_TENSOR, za_in=za, zb_in=zb,
+                             act_in=1)
+    torch.cuda.synchronize()
+    ref = oracle.conv3x3_dgrad_act(t.dy, t.w, zin_h, 1)
+    got = np.concatenate([host(gxa), host(gxb)], axis=-1)
+    assert rel_err(got, ref) <= TOL_BF16
 
 
 def test_concat_free_up_path_layer_full_size_sampled():

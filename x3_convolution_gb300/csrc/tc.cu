@@ -35,6 +35,7 @@
 
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "act.cuh"
@@ -301,10 +302,20 @@ __device__ __forceinline__ void s2_tap(int cls, int t, int& wtap, int& dj, int& 
 }
 // kExt = false: no fused extras and no stride-2 dgrad (p.s2, p.zout, p.zin
 // and the split output are ignored).
-template <int BN, int MT, bool kDgrad, bool kExt, int KC>
+//
+// kT (128-channel x 256-pixel tiles only): the transposed product.  The weight
+// tile is the MMA's A operand (M = 128 output channels) and the two im2col
+// boxes, contiguous in the stage, are one N = 256 B operand, so each K step
+// is one 128 x 256 x 16 MMA instead of two 128 x 128 x 16 ones sharing B:
+// the same tensor work with a third fewer operand bytes read from shared
+// memory per MMA and half the instructions for the issuing thread.  The
+// accumulator then holds channels on TMEM lanes and pixels on columns, and
+// the epilogue stores one channel per thread.  No stride-2 dgrad.
+template <int BN, int MT, bool kDgrad, bool kExt, int KC, bool kT = false>
 __global__ void __launch_bounds__(kIgemmThreads, 1)
     k_igemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
             const __grid_constant__ CUtensorMap tmB, const IgemmParams p) {
+  static_assert(!kT || (MT == 2 && BN == BM && KC == 1), "transposed tiles are 128 channels x 256 pixels");
   using Cfg = IgemmCfg<BN, MT, KC>;
   constexpr int S = Cfg::kStages;
   constexpr int TM = BM * MT;  // pixels per CTA tile
@@ -323,7 +334,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool s2 = kExt && kDgrad && p.s2;  // stride-2 dgrad by output parity
+  const bool s2 = kExt && kDgrad && !kT && p.s2;  // stride-2 dgrad by output parity
   const int num_tiles = igemm_num_tiles(p, s2);
   const int HW = p.H * p.W;
 
@@ -457,6 +468,8 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, kDgrad ? 1 : 0);
+      // transposed: the weight tile (K-major forward, MN-major dgrad) is A
+      constexpr uint32_t idesc_t = idesc_bf16_f32(BM, MT * BM, kDgrad ? 1 : 0, 0);
       // One thread issues every MMA, and its instruction path per k-block
       // sets the pace when the MMAs are short (N = 128: 64 cycles each), so
       // the descriptors are built once: a stage, a sub-tile or a K step only
@@ -488,16 +501,24 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
           tc_fence_after();
           const uint64_t ad = a_desc0 + stage_off, bd = b_desc0 + stage_off;
           const uint32_t acc0 = kb != 0 ? 1u : 0u;  // the tile's first K step starts the sum
-#pragma unroll
-          for (int c = 0; c < KC; ++c)
+          if constexpr (kT) {
+            // weights (M = 128 channels) x both pixel boxes (N = 256)
 #pragma unroll
             for (int k = 0; k < BKC / 16; ++k)
+              tc_mma_bf16(d_tmem, bd + (uint64_t)(k * kBKStep), ad + (uint64_t)(k * kAKStep), idesc_t,
+                          k == 0 ? acc0 : 1u);
+          } else {
 #pragma unroll
-              for (int u = 0; u < MT; ++u)
-                tc_mma_bf16(d_tmem + (uint32_t)(u * BN),
-                            ad + (uint64_t)(c * (Cfg::kChunkA >> 4) + u * kSubStep + k * kAKStep),
-                            bd + (uint64_t)(c * (Cfg::kChunkB >> 4) + k * kBKStep), idesc,
-                            (c == 0 && k == 0) ? acc0 : 1u);
+            for (int c = 0; c < KC; ++c)
+#pragma unroll
+              for (int k = 0; k < BKC / 16; ++k)
+#pragma unroll
+                for (int u = 0; u < MT; ++u)
+                  tc_mma_bf16(d_tmem + (uint32_t)(u * BN),
+                              ad + (uint64_t)(c * (Cfg::kChunkA >> 4) + u * kSubStep + k * kAKStep),
+                              bd + (uint64_t)(c * (Cfg::kChunkB >> 4) + k * kBKStep), idesc,
+                              (c == 0 && k == 0) ? acc0 : 1u);
+          }
           tc_commit(&empty[stage]);
           stage_off += kStageStep;
           if (++stage == S) {
@@ -518,6 +539,88 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       mbar_wait(drain, 0, p.wait_ns, nullptr, nullptr);
     }
     __syncwarp();
+  } else if constexpr (kT) {
+    // ------------------------------------------------------------ epilogue (transposed)
+    // TMEM lane = output channel, column = pixel of the 256-pixel tile.  Warp
+    // w reads lanes 32*(w%4) .. +31 (32 channels); the two warps of a lane
+    // quarter take 128 pixels each.  A thread owns one channel, so a 32-pixel
+    // chunk leaves as 32 scalar stores, each a 64-byte (bf16) or 128-byte
+    // (fp32) contiguous run across the warp.
+    const int q = warp & 3;
+    const int half = (warp - kEpiBase) >> 2;
+    int buf = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const TileInfo ti = tile_info(p, tile, false);
+      const int ch = ti.nt * BN + q * 32 + lane;
+      const bool ch_ok = ch < p.nout;
+      const float bc = (p.bias && ch_ok) ? __ldg(p.bias + ch) : 0.0f;
+      // this channel's tensor, row stride and column (the split output of a
+      // channel-split dgrad puts channels [nsplit, nout) in the second tensor)
+      const bool second = kExt && ch >= p.nsplit;
+      void* obase = second ? p.out2 : p.out;
+      const __nv_bfloat16* zbase = second ? p.zin2 : p.zin;
+      const long long ostride = !kExt ? p.nout : second ? p.nout - p.nsplit : p.nsplit;
+      const int ocol = second ? ch - p.nsplit : ch;
+      const long long pix_base = (long long)ti.mt * TM + half * BM;
+      if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
+                             (uint32_t)(buf * MT * BN + half * BM);
+#pragma unroll 1
+      for (int j = 0; j < BM / 32; ++j) {
+        const long long pix0 = pix_base + j * 32;
+        const int npix = p.P - pix0 < 32 ? (int)(p.P - pix0) : 32;  // <= 0 past the end
+        float zg[32];
+        if (kExt && p.zin) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            zg[i] = (ch_ok && i < npix) ? __bfloat162float(zbase[(pix0 + i) * ostride + ocol]) : 0.0f;
+        }
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
+        tmem_ld_wait();
+        if (ch_ok && npix > 0) {
+          float f[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]) + bc;
+          if (kExt && p.zout) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < npix) p.zout[(pix0 + i) * p.nout + ch] = __float2bfloat16_rn(f[i]);
+          }
+          if (p.act == CONV3X3_ACT_SILU) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = silu_f32(f[i]);
+          } else if (p.act == CONV3X3_ACT_LRELU) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = f[i] >= 0.0f ? f[i] : 0.2f * f[i];
+          }
+          if (kExt && p.zin) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] *= act_grad_f32(p.zin_act, zg[i]);
+          }
+          if (p.out_f32) {
+            float* op = static_cast<float*>(obase) + pix0 * ostride + ocol;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < npix) op[i * ostride] = f[i];
+          } else {
+            __nv_bfloat16* op = static_cast<__nv_bfloat16*>(obase) + pix0 * ostride + ocol;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < npix) op[i * ostride] = __float2bfloat16_rn(f[i]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (++buf == 2) {
+        buf = 0;
+        acc_phase ^= 1;
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     // warp w may read TMEM lanes 32*(w%4) .. +31.  The two warps of a lane
@@ -1829,13 +1932,13 @@ int set_smem(K kernel, size_t bytes, int device) {
   return CONV3X3_OK;
 }
 
-template <int BN, int MT, bool kDgrad, int KC = 1>
+template <int BN, int MT, bool kDgrad, int KC = 1, bool kT = false>
 int launch_igemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
                  const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
   using Cfg = IgemmCfg<BN, MT, KC>;
   // the fused extras, a split output or a stride-2 dgrad need the full epilogue
   const bool ext = prm.zout || prm.zin || prm.out2 || prm.s2;
-  auto kern = ext ? k_igemm<BN, MT, kDgrad, true, KC> : k_igemm<BN, MT, kDgrad, false, KC>;
+  auto kern = ext ? k_igemm<BN, MT, kDgrad, true, KC, kT> : k_igemm<BN, MT, kDgrad, false, KC, kT>;
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int tiles = (prm.s2 ? 4 : 1) * prm.num_m_tiles * prm.num_n_tiles;
   const int grid = tiles < d.num_sms ? tiles : d.num_sms;
@@ -2016,8 +2119,12 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   }
   g.u = 1;
   TileShape ts = pick_tile(nout, dgrad ? s : g, d.num_sms);
+  // 128-channel x 256-pixel tiles run transposed (k_igemm kT) unless the
+  // override names "128x2n"
+  bool trans = true;
   // CONV3X3_TILE="<BN>x<MT>" or "halo<BN>" overrides the choice (tuning and tests)
   if (const char* e = std::getenv("CONV3X3_TILE")) {
+    trans = std::strcmp(e, "128x2n") != 0;
     int bn_o = 0, mt_o = 0;
     const bool halo_ok = (s.W == 16 || s.W == 32 || s.W == 64) && s.H % (256 / s.W) == 0;
     if (std::sscanf(e, "halo%d", &bn_o) == 1 && halo_ok && (bn_o == 64 || bn_o == 128))
@@ -2109,6 +2216,9 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   }
   if (ts.mt == 2) {
     if (bn == 64) C3_LAUNCH(64, 2, 1);
+    if (trans && !s2)
+      return dgrad ? launch_igemm<128, 2, true, 1, true>(ta, ta2, tb, prm, d, st)
+                   : launch_igemm<128, 2, false, 1, true>(ta, ta2, tb, prm, d, st);
     C3_LAUNCH(128, 2, 1);
   }
   switch (bn) {
