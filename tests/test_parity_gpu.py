@@ -132,8 +132,10 @@ def test_small_shapes_all_passes(shape, path):
     assert rel_err(host(db), rdb) <= TOL_BF16
 
 
-# "128x2" runs transposed (channels on TMEM lanes), "128x2n" is the same tile untransposed
-TILES = ["64x1", "128x1", "192x1", "256x1", "64x2", "128x2", "128x2n"]
+# "128x2" runs transposed (channels on TMEM lanes), "128x2n" is the same tile untransposed;
+# "256x1" runs on two-CTA clusters (one 256-pixel x 256-channel tile per pair), "256x1n" on
+# one CTA
+TILES = ["64x1", "128x1", "192x1", "256x1", "256x1n", "64x2", "128x2", "128x2n"]
 
 
 @pytest.mark.parametrize("tile", TILES)
@@ -254,7 +256,7 @@ def test_fused_activation_backward(shape, path):
     assert torch.equal(dxn, dxp)
 
 
-@pytest.mark.parametrize("tile", ["64x2", "256x1", "halo64", "128x2", "128x2n"])
+@pytest.mark.parametrize("tile", ["64x2", "256x1", "256x1n", "halo64", "128x2", "128x2n"])
 def test_fused_activation_backward_tiles(tile, monkeypatch):
     monkeypatch.setenv("CONV3X3_TILE", tile)
     shape = (2, 64, 128, 16, 16)
@@ -490,12 +492,12 @@ def test_concat_free_convs(shape, path):
     assert torch.equal(dw, dw_plain) and torch.equal(db, db_plain)
 
 
-@pytest.mark.parametrize("tile", ["128x2", "128x2n"])
+@pytest.mark.parametrize("tile", ["128x2", "128x2n", "256x1", "256x1n"])
 @pytest.mark.parametrize("shape", [(1, 128, 72, 200, 6, 11), (2, 128, 128, 128, 16, 16)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_concat_free_256_pixel_tiles(shape, tile, monkeypatch):
-    """Split input and split input gradient on the 256-pixel tiles, transposed
-    (one channel per epilogue thread) and not."""
+    """Split input and split input gradient on the 256-pixel tiles: transposed
+    (one channel per epilogue thread) and not, on CTA pairs and on one CTA."""
     monkeypatch.setenv("CONV3X3_TILE", tile)
     N, Ca, Cb, Cout, H, W = shape
     t, zin_h, _ = _cat_case(shape)
@@ -620,7 +622,7 @@ def test_stride_one_through_the_strided_calls_is_the_plain_call(path):
     assert torch.equal(dw1, dw0) and torch.equal(db1, db0)
 
 
-@pytest.mark.parametrize("tile", ["64x1", "128x2", "256x1"])
+@pytest.mark.parametrize("tile", ["64x1", "128x2", "256x1", "256x1n"])
 def test_stride_two_tiles(tile, monkeypatch):
     monkeypatch.setenv("CONV3X3_TILE", tile)
     shape = (2, 64, 128, 13, 10)

@@ -310,7 +310,8 @@ __device__ __forceinline__ void s2_tap(int cls, int t, int& wtap, int& dj, int& 
 // the same tensor work with a third fewer operand bytes read from shared
 // memory per MMA and half the instructions for the issuing thread.  The
 // accumulator then holds channels on TMEM lanes and pixels on columns, and
-// the epilogue stores one channel per thread.  No stride-2 dgrad.
+// the epilogue stores one channel per thread.  No stride-2 dgrad and no z_in
+// (the dispatch sends those to the untransposed tile).
 template <int BN, int MT, bool kDgrad, bool kExt, int KC, bool kT = false>
 __global__ void __launch_bounds__(kIgemmThreads, 1)
     k_igemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
@@ -559,7 +560,6 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       // channel-split dgrad puts channels [nsplit, nout) in the second tensor)
       const bool second = kExt && ch >= p.nsplit;
       void* obase = second ? p.out2 : p.out;
-      const __nv_bfloat16* zbase = second ? p.zin2 : p.zin;
       const long long ostride = !kExt ? p.nout : second ? p.nout - p.nsplit : p.nsplit;
       const int ocol = second ? ch - p.nsplit : ch;
       const long long pix_base = (long long)ti.mt * TM + half * BM;
@@ -571,12 +571,6 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       for (int j = 0; j < BM / 32; ++j) {
         const long long pix0 = pix_base + j * 32;
         const int npix = p.P - pix0 < 32 ? (int)(p.P - pix0) : 32;  // <= 0 past the end
-        float zg[32];
-        if (kExt && p.zin) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            zg[i] = (ch_ok && i < npix) ? __bfloat162float(zbase[(pix0 + i) * ostride + ocol]) : 0.0f;
-        }
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
         tmem_ld_wait();
@@ -595,10 +589,6 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
           } else if (p.act == CONV3X3_ACT_LRELU) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = f[i] >= 0.0f ? f[i] : 0.2f * f[i];
-          }
-          if (kExt && p.zin) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] *= act_grad_f32(p.zin_act, zg[i]);
           }
           if (p.out_f32) {
             float* op = static_cast<float*>(obase) + pix0 * ostride + ocol;
@@ -681,6 +671,254 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+}
+
+// ----------------------------------------------------------------------------
+// forward / dgrad implicit GEMM on CTA pairs (tcgen05 cta_group::2)
+// ----------------------------------------------------------------------------
+// A cluster of two CTAs on two SMs owns one tile of 256 pixels x 256 output
+// channels.  Each CTA stages its own 128 pixels (one im2col A box) and half of
+// the weight tile (128 of the 256 channels); one thread of rank 0 issues
+// M = 256, N = 256 MMAs that read A and B from both CTAs' shared memory, and
+// each CTA's TMEM accumulates its 128 pixels x 256 channels.  Per SM that is
+// the tensor work of a 128 x 256 tile for two thirds of its operand bytes
+// (32 KB per 64-channel k-block instead of 48), so six stages fit where four
+// did and the ring covers 50 % more load and MMA latency.
+//
+// Barriers.  full[s] of rank 0 counts both CTAs' bytes (each CTA's loads
+// signal it through the cluster window, rank 0's producer registers the
+// pair's total); empty[s] and tfull[b] exist in both CTAs and are signalled by
+// rank 0's multicast commits; tempty[b] of rank 0 collects the epilogue warps
+// of both CTAs.  Every wait is bounded; the two cluster barriers (after setup,
+// before the TMEM release) are reached by every thread on every path.
+constexpr int kPairBN = 256;                           // output channels per pair tile
+constexpr uint32_t kPairBHalf = 128 * BKC * 2;         // 128 weight rows x 64 channels
+constexpr uint32_t kPairStage = kABytes + kPairBHalf;  // per CTA
+constexpr int kPairStages = 6;
+constexpr size_t kPairSmem = (size_t)kPairStages * kPairStage + 256 + 1024 + kGuardBytes;
+
+template <bool kDgrad, bool kExt>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
+    k_igemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                 const __grid_constant__ CUtensorMap tmB, const IgemmParams p) {
+  constexpr int S = kPairStages;
+  static_assert(S >= kProd, "stage-parallel producers need S >= kProd");
+  extern __shared__ uint8_t smem_raw[];
+  // same offset in both CTAs: the MMAs address the peer's operands at the
+  // offsets of rank 0's
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * kPairStage);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+  const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+  const int HW = p.H * p.W;
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 2 * kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    if (p.kchunks_a < p.kchunks) tma_prefetch_desc(&tmA2);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // rank 0's full and tempty barriers in the cluster window
+  const uint32_t full0 = cluster_addr(full, 0);
+  const uint32_t tempty0 = cluster_addr(tempty, 0);
+
+  if (warp < kProd) {
+    // ------------------------------------------------------------ TMA producers
+    // Whole stages in turn: producer `warp` fills stage k-blocks issued % kProd
+    // == warp with this CTA's A box and weight half.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      constexpr uint32_t kPairBytes = 2 * kPairStage;
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+        const int mt = tile / p.num_n_tiles, nt = tile - mt * p.num_n_tiles;
+        const int p0 = mt * 2 * BM + (int)rank * BM;  // this CTA's 128 pixels
+        const int n0 = p0 / HW, rem = p0 - n0 * HW;
+        const int h0 = rem / p.W;
+        const int cn = n0, ch = p.ustride * h0 - 1, cw = p.ustride * (rem - h0 * p.W) - 1;
+        const int c0 = nt * kPairBN + (int)rank * 128;  // this CTA's weight rows (output channels)
+        const int kblocks = 9 * p.kchunks;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const int tap = kb / p.kchunks, cc = kb - tap * p.kchunks;
+          if (issued % kProd == warp) {
+            if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            uint8_t* sa = smem + (size_t)stage * kPairStage;
+            uint8_t* sb = sa + kABytes;
+            const uint32_t fb = full0 + (uint32_t)stage * 8u;
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], kPairBytes);
+            const bool second = cc >= p.kchunks_a;
+            tma_load_im2col_4d_pair(sa, second ? &tmA2 : &tmA, fb,
+                                    (second ? cc - p.kchunks_a : cc) * BKC, cw, ch, cn,
+                                    (uint16_t)(tap % 3), (uint16_t)(tap / 3));
+            const int wtap = kDgrad ? 8 - tap : tap;
+            if (!kDgrad) {
+              tma_load_3d_pair(sb, &tmB, fb, cc * BKC, wtap, c0);
+            } else {
+              tma_load_3d_pair(sb, &tmB, fb, c0, wtap, cc * BKC);
+              tma_load_3d_pair(sb + 8192, &tmB, fb, c0 + 64, wtap, cc * BKC);
+            }
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        if (rank == 0) {
+          // wait (bounded) for the loads still in flight
+          int n = issued < S ? issued : S;
+          int st = stage;
+          uint32_t ph = phase;
+          for (int i = 0; i < n; ++i) {
+            if (--st < 0) {
+              st = S - 1;
+              ph ^= 1;
+            }
+            mbar_wait(&full[st], ph, drain_wait_ns(p.wait_ns), nullptr, nullptr);
+          }
+        } else {
+          // rank 1's loads complete on rank 0's barriers: give them time to land
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, kPairBN, 0, kDgrad ? 1 : 0);
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
+      const uint64_t b_desc0 = kDgrad ? smem_desc(sbase + kABytes, 8192, 1024, kSwizzle128B)
+                                      : smem_desc(sbase + kABytes, 16, 1024, kSwizzle128B);
+      constexpr uint32_t kStageStep = kPairStage >> 4;
+      constexpr uint32_t kBKStep = (kDgrad ? 2048u : 32u) >> 4;
+      constexpr uint32_t kAKStep = 32u >> 4;
+      int stage = 0;
+      uint32_t phase = 0, stage_off = 0;
+      int buf = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+        if (!mbar_wait(&tempty[buf], acc_phase ^ 1, p.wait_ns, p.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kPairBN);
+        const int kblocks = 9 * p.kchunks;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = a_desc0 + stage_off, bd = b_desc0 + stage_off;
+#pragma unroll
+          for (int k = 0; k < BKC / 16; ++k)
+            tc_mma_bf16_pair(d_tmem, ad + (uint64_t)(k * kAKStep), bd + (uint64_t)(k * kBKStep), idesc,
+                             (kb != 0 || k != 0) ? 1u : 0u);
+          tc_commit_pair_mc(&empty[stage], (uint16_t)0x3);
+          stage_off += kStageStep;
+          if (++stage == S) {
+            stage = 0;
+            stage_off = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(&tfull[buf], (uint16_t)0x3);
+        if (++buf == 2) {
+          buf = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // every issued MMA (which reads both CTAs' shared memory and writes both
+      // TMEMs) retires before either CTA releases anything
+      tc_commit_pair(drain);
+      mbar_wait(drain, 0, p.wait_ns, nullptr, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    // TMEM lane = this CTA's pixel, column = output channel of the 256-wide
+    // tile; the two warps of a lane quarter take 128 columns each.
+    constexpr int kCols = kPairBN / 2;
+    const int q = warp & 3;
+    const int half = (warp - kEpiBase) >> 2;
+    const int col_off = half * kCols;
+    const int row = q * 32 + lane;
+    int buf = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = pair; tile < num_tiles; tile += num_pairs) {
+      const int mt = tile / p.num_n_tiles, nt = tile - mt * p.num_n_tiles;
+      const long long pix = (long long)mt * 2 * BM + rank * BM + row;
+      const bool valid = pix < p.P;
+      if (kExt && p.zin && valid && nt * kPairBN + col_off < p.nout)
+        prefetch_zin_row(p, pix, nt * kPairBN + col_off, kCols);
+      if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kPairBN + col_off);
+#pragma unroll 1
+      for (int j = 0; j < kCols / 32; ++j) {
+        const int col0 = nt * kPairBN + col_off + j * 32;
+        const bool live = valid && col0 < p.nout;
+        float bv[32];
+        if (p.bias && live) load_bias(p, col0, bv);
+        uint4 zr[4] = {};
+        if (kExt && p.zin && live) load_zin(p, pix, col0, zr);
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
+        tmem_ld_wait();
+        if (live) store_chunk<kExt>(p, pix, col0, v, bv, zr);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0 + (uint32_t)buf * 8u);
+      if (++buf == 2) {
+        buf = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc_pair(tmem_base, 512);
 }
 
 // ----------------------------------------------------------------------------
@@ -1946,6 +2184,48 @@ int launch_igemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap&
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
+// Resident two-CTA clusters of k_igemm_pair (a GPC with an odd number of free
+// SMs leaves one idle), cached per kernel and device.
+template <typename K>
+int pair_slots(K kernel, const DevCtx& d) {
+  static std::mutex mu;
+  static int cache[4][64] = {};
+  static const void* keys[4] = {nullptr, nullptr, nullptr, nullptr};
+  std::lock_guard<std::mutex> g(mu);
+  int slot = 0;
+  while (slot < 4 && keys[slot] != nullptr && keys[slot] != (const void*)kernel) ++slot;
+  const bool cacheable = slot < 4 && d.device >= 0 && d.device < 64;
+  if (cacheable && keys[slot] == (const void*)kernel && cache[slot][d.device] > 0)
+    return cache[slot][d.device];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (d.num_sms / 2), 1, 1);
+  cfg.blockDim = dim3(kIgemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairSmem;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    n = d.num_sms / 2;
+  }
+  if (cacheable) {
+    keys[slot] = (const void*)kernel;
+    cache[slot][d.device] = n;
+  }
+  return n;
+}
+
+template <bool kDgrad>
+int launch_igemm_pair(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
+                      const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
+  const bool ext = prm.zout || prm.zin || prm.out2;
+  auto kern = ext ? k_igemm_pair<kDgrad, true> : k_igemm_pair<kDgrad, false>;
+  if (set_smem(kern, kPairSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+  const int tiles = prm.num_m_tiles * prm.num_n_tiles;
+  const int pairs = pair_slots(kern, d);
+  const int grid = 2 * (tiles < pairs ? tiles : pairs);
+  kern<<<grid, kIgemmThreads, kPairSmem, st>>>(a, a2, b, prm);
+  return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
 template <int W_, int BN, bool kDgrad>
 int launch_halo(const CUtensorMap& a, const CUtensorMap& b, const IgemmParams& prm,
                 const DevCtx& d, cudaStream_t st) {
@@ -2120,11 +2400,19 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   g.u = 1;
   TileShape ts = pick_tile(nout, dgrad ? s : g, d.num_sms);
   // 128-channel x 256-pixel tiles run transposed (k_igemm kT) unless the
-  // override names "128x2n"
+  // override names "128x2n".  256-channel tiles run on CTA pairs
+  // (k_igemm_pair) where that measured faster: dgrad, or a forward with a long
+  // K (at least eight 64-channel chunks), and at least two rounds of pair
+  // tiles (a 256-pixel pair tile halves the tile count, so small grids lose).
+  // CONV3X3_PAIR=0|1 or the override "256x1" / "256x1n" forces the choice.
   bool trans = true;
+  int pair_force = -1;
+  if (const char* e = std::getenv("CONV3X3_PAIR")) pair_force = std::strcmp(e, "0") != 0 ? 1 : 0;
   // CONV3X3_TILE="<BN>x<MT>" or "halo<BN>" overrides the choice (tuning and tests)
   if (const char* e = std::getenv("CONV3X3_TILE")) {
     trans = std::strcmp(e, "128x2n") != 0;
+    if (std::strcmp(e, "256x1n") == 0) pair_force = 0;
+    if (std::strcmp(e, "256x1") == 0) pair_force = 1;
     int bn_o = 0, mt_o = 0;
     const bool halo_ok = (s.W == 16 || s.W == 32 || s.W == 64) && s.H % (256 / s.W) == 0;
     if (std::sscanf(e, "halo%d", &bn_o) == 1 && halo_ok && (bn_o == 64 || bn_o == 128))
@@ -2195,6 +2483,20 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
     C3_HALO(16, 128);
 #undef C3_HALO
   }
+  const long long pair_tiles = (g.P() + 2 * BM - 1) / (2 * BM) * prm.num_n_tiles;
+  const bool pair = pair_force >= 0 ? pair_force == 1
+                                    : ((dgrad || prm.kchunks >= 8) && pair_tiles >= d.num_sms);
+  if (pair && bn == 256 && ts.mt == 1 && !s2) {
+    // a pair tile is 256 pixels (128 per CTA) x 256 channels, each CTA
+    // loading 128 weight rows
+    prm.num_m_tiles = (int)((g.P() + 2 * BM - 1) / (2 * BM));
+    if (!dgrad) {
+      rc = make_weight_map(&tb, w, s.Cin, s.Cout, 128);
+      if (rc) return rc;
+    }
+    return dgrad ? launch_igemm_pair<true>(ta, ta2, tb, prm, d, st)
+                 : launch_igemm_pair<false>(ta, ta2, tb, prm, d, st);
+  }
   // Two 64-channel chunks per k-block where the tile's MMAs are short (see
   // IgemmCfg); CONV3X3_KC=1|2 overrides the choice (tuning).
   int kc = (ts.mt == 1 && bn == 128) ? 2 : 1;
@@ -2216,7 +2518,9 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   }
   if (ts.mt == 2) {
     if (bn == 64) C3_LAUNCH(64, 2, 1);
-    if (trans && !s2)
+    // (not with z_in: one channel per thread turns its loads into 2-byte
+    // gathers, eight times the requests of the row-per-thread epilogue)
+    if (trans && !s2 && !prm.zin)
       return dgrad ? launch_igemm<128, 2, true, 1, true>(ta, ta2, tb, prm, d, st)
                    : launch_igemm<128, 2, false, 1, true>(ta, ta2, tb, prm, d, st);
     C3_LAUNCH(128, 2, 1);
