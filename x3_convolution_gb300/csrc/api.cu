@@ -7,6 +7,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "conv3x3_internal.h"
@@ -134,6 +135,14 @@ __global__ void k_wait_selftest(unsigned* status, unsigned long long limit_ns) {
     mbar_wait(&bar, 0, limit_ns, status, &abort_flag);
   }
   __syncthreads();
+}
+
+bool pdl_enabled() {
+  static const bool v = [] {
+    const char* e = std::getenv("CONV3X3_PDL");
+    return !(e && std::strcmp(e, "0") == 0);
+  }();
+  return v;
 }
 
 }  // namespace c3

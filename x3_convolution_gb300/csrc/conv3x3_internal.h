@@ -21,6 +21,38 @@ struct Shape {
   long long Po() const { return (long long)N * Ho() * Wo(); }
 };
 
+// Programmatic dependent launch.  The tensor-path kernels start with
+// pdl_trigger() (their dependents may begin launching; the wgrad mainloops
+// skip it, see there) and execute pdl_wait() -- which returns once the previous
+// kernel in the stream has completed and its writes are visible -- before
+// their first access to global memory, so only set-up (barrier init, TMEM
+// allocation, descriptor prefetch) overlaps the previous kernel's tail.
+// Launched without the attribute, both are no-ops.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Whether launches carry the programmatic-serialization attribute
+// (CONV3X3_PDL=0 turns it off).
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Per-call device context: status word and wait bound.
 struct DevCtx {
   unsigned* status;          // device address of the status word

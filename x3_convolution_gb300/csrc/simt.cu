@@ -464,6 +464,8 @@ __global__ void __launch_bounds__(kThreads) k_wgrad_bf16_c8_partial(
 // over its Sdb partial rows stored after the S dw slices.
 __global__ void k_wgrad_reduce(const float* __restrict__ part, float* __restrict__ dw,
                                float* __restrict__ db, long long dwsize, int Cout, int S, int Sdb) {
+  pdl_trigger();
+  pdl_wait();  // the partials of the kernel before
   const long long n4 = dwsize / 4;
   const long long total = n4 + Cout;
   const float4* p4 = reinterpret_cast<const float4*>(part);
@@ -538,7 +540,8 @@ WgradPlan wgrad_plan(const Shape& s) {
 
 int launch_wgrad_reduce(const float* part, float* dw, float* db, long long dwsize, int Cout, int S,
                         int Sdb, cudaStream_t st) {
-  k_wgrad_reduce<<<grid_for(dwsize / 4 + Cout), kThreads, 0, st>>>(part, dw, db, dwsize, Cout, S, Sdb);
+  launch_pdl(k_wgrad_reduce, dim3(grid_for(dwsize / 4 + Cout)), dim3(kThreads), 0, st, part, dw, db,
+             dwsize, Cout, S, Sdb);
   return launch_status();
 }
 

@@ -335,6 +335,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   const bool s2 = kExt && kDgrad && !kT && p.s2;  // stride-2 dgrad by output parity
   const int num_tiles = igemm_num_tiles(p, s2);
   const int HW = p.H * p.W;
@@ -363,6 +364,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the previous kernel's writes are visible from here on
 
   if (warp < kProd) {
     // ------------------------------------------------------------ TMA producers
@@ -716,6 +718,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   const uint32_t rank = cluster_ctarank();
   const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
   const int num_tiles = p.num_m_tiles * p.num_n_tiles;
@@ -745,6 +748,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the previous kernel's writes are visible from here on
   // rank 0's full and tempty barriers in the cluster window
   const uint32_t full0 = cluster_addr(full, 0);
   const uint32_t tempty0 = cluster_addr(tempty, 0);
@@ -969,6 +973,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   const int num_tiles = p.num_m_tiles * p.num_n_tiles;
   const int HW = p.H * W_;
 
@@ -999,6 +1004,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the previous kernel's writes are visible from here on
 
   if (warp < 2) {
     // ------------------------------------------------------------ A-box producers
@@ -1226,6 +1232,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   const int num_tiles = p.num_m_tiles;
   const int HW = p.H * p.W;
 
@@ -1263,6 +1270,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the previous kernel's writes are visible from here on
 
   if (warp < kProd) {
     if (lane == 0) {
@@ -1439,6 +1447,7 @@ __global__ void __launch_bounds__(kSdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   const int rows_per_img = p.H / p.R;
   const int tpix = (p.R + 2) * p.W;  // T pixels of a tile (<= 256)
 
@@ -1462,6 +1471,7 @@ __global__ void __launch_bounds__(kSdThreads, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
+  pdl_wait();  // w is read below
   // Wt from w [K][3][3][8]: element (n = 8 t + c, k) at group k/8, row n, 2 (k % 8) bytes;
   // rows 72..79 are zero
   for (int e = threadIdx.x; e < (p.K / 8) * kSdN; e += kSdThreads) {
@@ -1480,6 +1490,7 @@ __global__ void __launch_bounds__(kSdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the previous kernel's writes are visible from here on
 
   if (warp < kProd) {
     // ------------------------------------------------------------ TMA producer (warp 0)
@@ -1696,6 +1707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // no early trigger: the dependent is the partials' reduction, whose blocks
+  // would otherwise sit on the SMs (waiting) while this kernel runs
   const int num_tiles = p.num_mb * 3 * p.num_cb;
   const int tile = blockIdx.x % num_tiles;
   const int split = blockIdx.x / num_tiles;
@@ -1738,6 +1751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the previous kernel's writes are visible from here on
 
   if (warp < kProd) {
     // Eight 8 KB boxes per stage: two dy boxes (64 pixels x 64 output
@@ -1919,6 +1933,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // no early trigger: the dependent is the partials' reduction, whose blocks
+  // would otherwise sit on the SMs (waiting) while this kernel runs
   const int mb = blockIdx.x % p.num_mb;
   const int split = blockIdx.x / p.num_mb;
   const int kb0 = split * p.kb_per_split;
@@ -1956,6 +1972,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the previous kernel's writes are visible from here on
 
   if (warp < kProd) {
     // eleven boxes per stage: dy halves 0-1 (8 KB), x taps 2-10 (1 KB)
@@ -2180,7 +2197,7 @@ int launch_igemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap&
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int tiles = (prm.s2 ? 4 : 1) * prm.num_m_tiles * prm.num_n_tiles;
   const int grid = tiles < d.num_sms ? tiles : d.num_sms;
-  kern<<<grid, kIgemmThreads, Cfg::kSmem, st>>>(a, a2, b, prm);
+  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, a2, b, prm);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
@@ -2222,7 +2239,7 @@ int launch_igemm_pair(const CUtensorMap& a, const CUtensorMap& a2, const CUtenso
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
   const int pairs = pair_slots(kern, d);
   const int grid = 2 * (tiles < pairs ? tiles : pairs);
-  kern<<<grid, kIgemmThreads, kPairSmem, st>>>(a, a2, b, prm);
+  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), kPairSmem, st, a, a2, b, prm);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
@@ -2234,7 +2251,7 @@ int launch_halo(const CUtensorMap& a, const CUtensorMap& b, const IgemmParams& p
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
   const int grid = tiles < d.num_sms ? tiles : d.num_sms;
-  kern<<<grid, kIgemmThreads, Cfg::kSmem, st>>>(a, b, prm);
+  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, b, prm);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
@@ -2298,7 +2315,7 @@ int launch_stem(const CUtensorMap& a, const CUtensorMap& b, const IgemmParams& p
   auto kern = k_stem_fwd<BN>;
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int grid = prm.num_m_tiles < d.num_sms ? prm.num_m_tiles : d.num_sms;
-  kern<<<grid, kIgemmThreads, Cfg::kSmem, st>>>(a, b, prm);
+  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, b, prm);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
@@ -2378,7 +2395,8 @@ int run_stem_dgrad(const void* dy, const void* w, void* dx, const Shape& s, int 
   const size_t smem = stem_dgrad_smem(s.Cout);
   if (set_smem(k_stem_dgrad, smem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int grid = prm.num_tiles < d.num_sms ? prm.num_tiles : d.num_sms;
-  k_stem_dgrad<<<grid, kSdThreads, smem, st>>>(tdy, static_cast<const __nv_bfloat16*>(w), prm);
+  launch_pdl(k_stem_dgrad, dim3(grid), dim3(kSdThreads), smem, st, tdy,
+             static_cast<const __nv_bfloat16*>(w), prm);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
@@ -2668,7 +2686,7 @@ int run_wgrad_c8(const void* x, const void* dy, float* dw, float* db, const Shap
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
   if (set_smem(k_wgrad_c8, kWc8Smem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
-  k_wgrad_c8<<<pl.tiles * pl.S, kThreads, kWc8Smem, st>>>(tdy, tx, prm);
+  launch_pdl(k_wgrad_c8, dim3(pl.tiles * pl.S), dim3(kThreads), kWc8Smem, st, tdy, tx, prm);
   if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
   return launch_wgrad_reduce(prm.part, dw, db, (long long)s.Cout * 72, s.Cout, pl.S, pl.S, st);
 }
@@ -2708,7 +2726,7 @@ int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
   if (set_smem(k_wgrad, kWgSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
-  k_wgrad<<<pl.tiles * pl.S, kThreads, kWgSmem, st>>>(tdy, tx, tx2, prm);
+  launch_pdl(k_wgrad, dim3(pl.tiles * pl.S), dim3(kThreads), kWgSmem, st, tdy, tx, tx2, prm);
   if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
   return launch_wgrad_reduce(prm.part, dw, db, (long long)s.Cout * 9 * s.Cin, s.Cout, pl.S, pl.S, st);
 }
