@@ -266,6 +266,16 @@ class Workload:
                 ws_max = max(ws_max, Lb.conv3x3_wgrad_workspace_bytes(L.N, L.Cin, L.Cout, L.H, L.W))
         self.ws_bytes = ws_max
         self.ws = torch.empty(max(ws_max, 256), dtype=torch.uint8, device=device)
+        # one more split-K workspace per extra wgrad stream (see run_step)
+        self.ws_side = []
+        self.device = device
+
+    def side_workspace(self, k):
+        import torch
+        while len(self.ws_side) <= k:
+            self.ws_side.append(torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8,
+                                            device=self.device))
+        return self.ws_side[k]
 
     def inputs(self, h):
         keys = ("x", "xa", "xb", "w", "b", "dy", "zin", "za", "zb")
@@ -313,27 +323,35 @@ def _dgrad(wl, i, sh):
     return 1
 
 
-def _wgrad(wl, i, sh):
+def _wgrad(wl, i, sh, side=-1):
     from x3_convolution_gb300 import _lib as Lb
     L, d = wl.layers[i], wl.dev[i]
+    ws = wl.side_workspace(side) if side >= 0 else wl.ws
     if L.stride != 1:
         Lb.conv3x3_wgrad_strided(d["x"], d["dy"], d["dw"], d["db"], L.N, L.Cin, L.Cout, L.H, L.W,
-                                 L.stride, wl.ws, wl.ws_bytes, Lb.PATH_AUTO, sh)
+                                 L.stride, ws, wl.ws_bytes, Lb.PATH_AUTO, sh)
     elif d["cat_a"]:
         Lb.conv3x3_wgrad_cat(d["xa"], d["xb"], d["cat_a"], d["dy"], d["dw"], d["db"], L.N, L.Cin,
-                             L.Cout, L.H, L.W, wl.ws, wl.ws_bytes, Lb.PATH_AUTO, sh)
+                             L.Cout, L.H, L.W, ws, wl.ws_bytes, Lb.PATH_AUTO, sh)
     else:
-        Lb.conv3x3_wgrad(d["x"], d["dy"], d["dw"], d["db"], L.N, L.Cin, L.Cout, L.H, L.W, wl.ws,
+        Lb.conv3x3_wgrad(d["x"], d["dy"], d["dw"], d["db"], L.N, L.Cin, L.Cout, L.H, L.W, ws,
                          wl.ws_bytes, sh)
     return 2  # partial-sum kernel + fixed-order reduction
 
 
-def run_step(wl: Workload, stream_handle: int, record=None, mark=None, interleave=False):
+def run_step(wl: Workload, stream_handle: int, record=None, mark=None, interleave=False,
+             streams=None):
     """One sweep through the C ABI: every layer's forward in network order, then
     the backward in reverse order -- by default every dgrad, then every wgrad (a
     wgrad needs only its layer's x and dy); with `interleave` each layer's
     dgrad and wgrad back to back.  `record(kind, i, 0|1)` brackets each call,
-    `mark(pass)` the end of each pass.  Returns the number of kernel launches."""
+    `mark(pass)` the end of each pass.  With `streams` = (main, side, ...) torch
+    streams (main being the stream of `stream_handle`), the wgrad calls -- which
+    depend on no other wgrad -- go round-robin over the streams (fork and join
+    by events, each stream with its own workspace), so that one layer's
+    reduction and last tile round overlap the next layer's wgrad.  The forward
+    and dgrad calls stay in order on one stream: in a network each depends on
+    the one before.  Returns the number of kernel launches."""
     def call(kind, fn, i):
         if record is not None:
             record(kind, i, 0)
@@ -359,8 +377,22 @@ def run_step(wl: Workload, stream_handle: int, record=None, mark=None, interleav
         n += call("dgrad", _dgrad, i)
     if mark is not None:
         mark("dgrad")
-    for i in back:
-        n += call("wgrad", _wgrad, i)
+    if streams is None:
+        for i in back:
+            n += call("wgrad", _wgrad, i)
+    else:
+        import torch
+        main, sides = streams[0], streams[1:]
+        for sd in sides:
+            sd.wait_stream(main)
+        for j, i in enumerate(back):
+            k = j % len(streams)
+            if k:
+                n += _wgrad(wl, i, sides[k - 1].cuda_stream, side=k - 1)
+            else:
+                n += call("wgrad", _wgrad, i)
+        for sd in sides:
+            main.wait_stream(sd)
     if mark is not None:
         mark("wgrad")
     return n
@@ -385,6 +417,11 @@ def cuda_arm(args):
                   concat_free=args.concat_free)
     stream = torch.cuda.Stream(device=device)
     sh = stream.cuda_stream
+    # the wgrad pass runs on --wgrad-streams streams (1: in order on one)
+    wstreams = None
+    if args.wgrad_streams > 1:
+        wstreams = (stream,) + tuple(torch.cuda.Stream(device=device)
+                                     for _ in range(args.wgrad_streams - 1))
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device=device)
 
@@ -394,7 +431,7 @@ def cuda_arm(args):
     # warm-up
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            run_step(wl, sh)
+            run_step(wl, sh, streams=wstreams)
     torch.cuda.synchronize(device)
     st = Lb.conv3x3_device_status(sh)
     if st != Lb.OK:
@@ -426,7 +463,7 @@ def cuda_arm(args):
     if not args.no_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
-            launches_per_step = run_step(wl, sh, mark=mark_in_graph)
+            launches_per_step = run_step(wl, sh, mark=mark_in_graph, streams=wstreams)
         torch.cuda.synchronize(device)
         for _ in range(args.warmup):
             with torch.cuda.stream(stream):
@@ -449,7 +486,7 @@ def cuda_arm(args):
                 graph.replay()
                 launches += launches_per_step
         if graph is None:
-            launches += run_step(wl, sh, mark=mark)
+            launches += run_step(wl, sh, mark=mark, streams=wstreams)
         torch.cuda.synchronize(device)
         step_ms.append(marks["start"].elapsed_time(marks["wgrad"]))
         fam_ms["fwd"] += marks["start"].elapsed_time(marks["fwd"])
@@ -619,7 +656,8 @@ def cuda_arm(args):
                    "flops_per_step": flops_step, "flops_per_step_padded_cin": flops_padded,
                    "launch": "stream" if graph is None else "CUDA graph of the step's C ABI calls",
                    "fused_act_backward": bool(args.fused_act),
-                   "concat_free_up_path": bool(args.concat_free)},
+                   "concat_free_up_path": bool(args.concat_free),
+                   "wgrad_streams": 1 if wstreams is None else len(wstreams)},
         "pct_of_roofline": round(roof_s / (ms * 1e-3), 4),
         "roofline": {"bound": "tensor", "kernel": {"fwd": "k_igemm (fwd)", "dgrad": "k_igemm (dgrad)",
                                                    "wgrad": "k_wgrad + k_wgrad_reduce"}[dom],
@@ -720,6 +758,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--detail", action="store_true", help="add a per-layer breakdown")
+    ap.add_argument("--wgrad-streams", type=int, default=2,
+                    help="streams the wgrad calls go round-robin over (1 = one stream)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps call by call instead of replaying a CUDA graph")
     ap.add_argument("--concat-free", action="store_true",
@@ -730,6 +770,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.wgrad_streams < 1:
+        ap.error("--wgrad-streams must be >= 1")
     line = reference_arm(args) if args.impl == "reference" else cuda_arm(args)
     if line is not None:
         if line.get("layers_detail") is None:
