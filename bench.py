@@ -339,6 +339,33 @@ def _wgrad(wl, i, sh, side=-1):
     return 2  # partial-sum kernel + fixed-order reduction
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the wgrad family
+# (k_wgrad, k_wgrad_c8, k_wgrad_reduce) over one UNet step, from one ncu capture
+# (profiles/wgrad_traffic_unet_step.md), and the SHA-256 of the kernel sources it
+# was taken on: the bench reports it only while those sources are unchanged.
+WGRAD_TRAFFIC_BYTES = 3275.3e6
+WGRAD_TRAFFIC_SOURCES = ("tc.cu", "simt.cu", "ptx.cuh", "conv3x3_internal.h")
+WGRAD_TRAFFIC_SHA256 = "d722612076bd50819393c739856f08c633aee6ea9fe179944f7a9cd4a2961351"
+
+
+def recorded_traffic(args, dom):
+    """Bytes per step of the dominant family from the recorded capture, or None
+    when it does not apply (another family, workload or variant) or the kernels
+    changed since it was taken."""
+    import hashlib
+    if dom != "wgrad" or args.workload != "unet" or args.fused_act or args.concat_free:
+        return None
+    h = hashlib.sha256()
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "x3_convolution_gb300", "csrc")
+    try:
+        for f in WGRAD_TRAFFIC_SOURCES:
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    except OSError:
+        return None
+    return WGRAD_TRAFFIC_BYTES if h.hexdigest() == WGRAD_TRAFFIC_SHA256 else None
+
+
 def run_step(wl: Workload, stream_handle: int, record=None, mark=None, interleave=False,
              streams=None):
     """One sweep through the C ABI: every layer's forward in network order, then
@@ -662,7 +689,8 @@ def cuda_arm(args):
         "roofline": {"bound": "tensor", "kernel": {"fwd": "k_igemm (fwd)", "dgrad": "k_igemm (dgrad)",
                                                    "wgrad": "k_wgrad + k_wgrad_reduce"}[dom],
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic(args, dom),
+                     "traffic_unit": "bytes per step (DRAM read + write, ncu)",
                      "peak_source": peaks["source"] + " bf16 sustained"},
         "passes": fam,
         "gpu_launches": launches,
