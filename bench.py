@@ -339,31 +339,31 @@ def _wgrad(wl, i, sh, side=-1):
     return 2  # partial-sum kernel + fixed-order reduction
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the wgrad family
-# (k_wgrad, k_wgrad_c8, k_wgrad_reduce) over one UNet step, from one ncu capture
-# (profiles/wgrad_traffic_unet_step.md), and the SHA-256 of the kernel sources it
-# was taken on: the bench reports it only while those sources are unchanged.
-WGRAD_TRAFFIC_BYTES = 3275.3e6
-WGRAD_TRAFFIC_SOURCES = ("tc.cu", "simt.cu", "ptx.cuh", "conv3x3_internal.h")
-WGRAD_TRAFFIC_SHA256 = "d722612076bd50819393c739856f08c633aee6ea9fe179944f7a9cd4a2961351"
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of each pass's
+# kernels over one UNet step, from one ncu capture of every launch
+# (profiles/traffic_unet_step.md), and the SHA-256 of the kernel sources it was
+# taken on: the bench reports it only while those sources are unchanged.
+TRAFFIC_BYTES = {"fwd": 2361.6e6, "dgrad": 2370.1e6, "wgrad": 3275.5e6}
+TRAFFIC_SOURCES = ("tc.cu", "simt.cu", "ptx.cuh", "conv3x3_internal.h")
+TRAFFIC_SHA256 = "d722612076bd50819393c739856f08c633aee6ea9fe179944f7a9cd4a2961351"
 
 
 def recorded_traffic(args, dom):
     """Bytes per step of the dominant family from the recorded capture, or None
-    when it does not apply (another family, workload or variant) or the kernels
-    changed since it was taken."""
+    when it does not apply (another workload or variant) or the kernels changed
+    since it was taken."""
     import hashlib
-    if dom != "wgrad" or args.workload != "unet" or args.fused_act or args.concat_free:
+    if args.workload != "unet" or args.fused_act or args.concat_free:
         return None
     h = hashlib.sha256()
     csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "x3_convolution_gb300", "csrc")
     try:
-        for f in WGRAD_TRAFFIC_SOURCES:
+        for f in TRAFFIC_SOURCES:
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(fh.read())
     except OSError:
         return None
-    return WGRAD_TRAFFIC_BYTES if h.hexdigest() == WGRAD_TRAFFIC_SHA256 else None
+    return TRAFFIC_BYTES[dom] if h.hexdigest() == TRAFFIC_SHA256 else None
 
 
 def run_step(wl: Workload, stream_handle: int, record=None, mark=None, interleave=False,
@@ -686,8 +686,10 @@ def cuda_arm(args):
                    "concat_free_up_path": bool(args.concat_free),
                    "wgrad_streams": 1 if wstreams is None else len(wstreams)},
         "pct_of_roofline": round(roof_s / (ms * 1e-3), 4),
-        "roofline": {"bound": "tensor", "kernel": {"fwd": "k_igemm (fwd)", "dgrad": "k_igemm (dgrad)",
-                                                   "wgrad": "k_wgrad + k_wgrad_reduce"}[dom],
+        "roofline": {"bound": "tensor",
+                     "kernel": {"fwd": "k_igemm + k_igemm_pair + k_stem_fwd (forward pass)",
+                                "dgrad": "k_igemm + k_igemm_pair + k_stem_dgrad (dgrad pass)",
+                                "wgrad": "k_wgrad + k_wgrad_c8 + k_wgrad_reduce (wgrad pass)"}[dom],
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic(args, dom),
                      "traffic_unit": "bytes per step (DRAM read + write, ncu)",
