@@ -1368,11 +1368,17 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + col_off);
 #pragma unroll 1
       for (int j = 0; j < kCols / 32; ++j) {
+        const int col0 = col_off + j * 32;
+        const bool live = valid && col0 < p.nout;
+        // the bias is loaded ahead of the accumulator, so that the add does not
+        // wait on it (a forward has no z_in)
+        float bv[32];
+        if (p.bias && live) load_bias(p, col0, bv);
+        const uint4 zr[4] = {};
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
         tmem_ld_wait();
-        const int col0 = col_off + j * 32;
-        if (valid && col0 < p.nout) store_chunk(p, pix, col0, v);
+        if (live) store_chunk<true>(p, pix, col0, v, bv, zr);
       }
       tc_fence_before();
       __syncwarp();
