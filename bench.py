@@ -342,10 +342,11 @@ def _wgrad(wl, i, sh, side=-1):
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of each pass's
 # kernels over one UNet step, from one ncu capture of every launch
 # (profiles/traffic_unet_step.md), and the SHA-256 of the kernel sources it was
-# taken on: the bench reports it only while those sources are unchanged.
+# taken on (re-pinned after comment-only edits): the bench reports it only while
+# those sources are unchanged.
 TRAFFIC_BYTES = {"fwd": 2360.8e6, "dgrad": 2368.9e6, "wgrad": 3275.7e6}
 TRAFFIC_SOURCES = ("tc.cu", "simt.cu", "ptx.cuh", "conv3x3_internal.h")
-TRAFFIC_SHA256 = "c295e7ae201d659813e74cdbb66a8708b5d1630f5a746796af8c4fb6d7a55de7"
+TRAFFIC_SHA256 = "98a1ac22625c33a53d784c3db73dee04e10dc7d2a160d1c61829932317d09063"
 
 
 def recorded_traffic(args, dom):

@@ -1,5 +1,5 @@
 // tc.cu -- tensor-core (tcgen05 + TMEM + TMA) implicit-GEMM kernels for the
-// stride-1, pad-1 3x3 convolution on sm_103a.
+// pad-1 3x3 convolution on sm_103a (stride 1, and stride 2 for downsampling).
 //
 // Forward and dgrad share one persistent, warp-specialised kernel:
 //   GEMM  M = N*H*W output pixels, N = output channels, K = 9 taps x channels.
@@ -11,9 +11,12 @@
 //   read as [K=k][N=c]), so neither pass transposes anything in memory.  dgrad
 //   mirrors the taps: dx = sum over (ra, sa) of dy at offset (ra-1, sa-1) times
 //   w[:, 2-ra, 2-sa, :].
-//   Warp 0 issues TMA, warp 1 owns TMEM and issues tcgen05.mma (128 x BN x 16,
-//   fp32 accumulate), warps 2-5 drain the double-buffered TMEM accumulator:
-//   bias + SiLU in fp32, round to bf16 (or keep fp32), store.
+//   Warps 0-3 issue TMA, warp 4 owns TMEM and issues tcgen05.mma (128 x BN x 16,
+//   fp32 accumulate), warps 5-12 drain the double-buffered TMEM accumulator:
+//   bias + SiLU in fp32, round to bf16 (or keep fp32), store.  The 256-pixel x
+//   128-channel tile can run transposed (weights as the M operand, both pixel
+//   boxes as one N = 256 operand), and 256-channel tiles can run on two-CTA
+//   clusters (k_igemm_pair: tcgen05 cta_group::2, M = 256 pixels per pair).
 //
 // Weight gradient: split-K implicit GEMM  M = Cout, N = (tap, Cin), K = pixels.
 //   A = dy tile (64 pixels x 128 output channels, MN-major), B = im2col(x) for
