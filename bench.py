@@ -27,6 +27,13 @@ launching stream; L2 is flushed (a write of 2x the L2 size) between steps,
 outside the events.  Multi-process runs (torchrun) run one replica per GPU
 (weak scaling); the reported time is the max over ranks.
 
+Beside the step, the line carries the per-layer breakdown of the step
+(layers_detail: extra untimed steps with an event pair around every call) and
+the gates block: each pass of the per-layer workloads (stem, l1, l2, l3) timed
+alone with L2 flushed before every call, as a fraction of its roofline (HBM for
+the 8-input-channel stem, the dense bf16 tensor peak for the others) against
+its target, and the tiny fp32 check workload (launch-bound, no target).
+
 --impl reference times the CPU oracle (fp64, all host cores) on a bounded
 sample of the same workload: each step runs fwd + dgrad + wgrad of one image of
 one layer, cycling through the layers.
@@ -339,32 +346,119 @@ def _wgrad(wl, i, sh, side=-1):
     return 2  # partial-sum kernel + fixed-order reduction
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of each pass's
-# kernels over one UNet step, from one ncu capture of every launch
-# (profiles/traffic_unet_step.md), and the SHA-256 of the kernel sources it was
-# taken on (re-pinned after comment-only edits): the bench reports it only while
-# those sources are unchanged.
-TRAFFIC_BYTES = {"fwd": 2360.8e6, "dgrad": 2368.9e6, "wgrad": 3275.7e6}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one call of
+# each pass on the per-layer configs (stem, l1, l2, l3), from scoped ncu
+# captures -- one workload of one layer, the three calls of one step, DRAM
+# counters only -- and the SHA-256 of the kernel sources they were taken on: a
+# figure is reported only while those sources are unchanged.
+RECORDED_TRAFFIC: dict = {}   # {(config, pass): bytes per call}
 TRAFFIC_SOURCES = ("tc.cu", "simt.cu", "ptx.cuh", "conv3x3_internal.h")
-TRAFFIC_SHA256 = "98a1ac22625c33a53d784c3db73dee04e10dc7d2a160d1c61829932317d09063"
+TRAFFIC_SHA256 = None
 
 
-def recorded_traffic(args, dom):
-    """Bytes per step of the dominant family from the recorded capture, or None
-    when it does not apply (another workload or variant) or the kernels changed
-    since it was taken."""
+def sources_sha256():
     import hashlib
-    if args.workload != "unet" or args.fused_act or args.concat_free:
-        return None
     h = hashlib.sha256()
-    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "x3_convolution_gb300", "csrc")
+    csrc = os.path.join(ROOT, "x3_convolution_gb300", "csrc")
     try:
         for f in TRAFFIC_SOURCES:
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(fh.read())
     except OSError:
         return None
-    return TRAFFIC_BYTES[dom] if h.hexdigest() == TRAFFIC_SHA256 else None
+    return h.hexdigest()
+
+
+def recorded_traffic(config, pas):
+    """Bytes per call of `pas` on per-layer config `config` from the recorded
+    capture, or None when there is none or the kernels changed since."""
+    if TRAFFIC_SHA256 is None or (config, pas) not in RECORDED_TRAFFIC:
+        return None
+    return RECORDED_TRAFFIC[(config, pas)] if sources_sha256() == TRAFFIC_SHA256 else None
+
+
+def pick_peak(peaks, clocks, timed_s):
+    """The tensor peak the step is held to: the burst figure (cuBLAS timed in
+    isolation) when the timed region is short and the SM clock stayed near its
+    maximum, else the sustained one (cuBLAS held for seconds under the power cap)."""
+    burst = clocks is not None and timed_s < 1.0 and \
+        clocks.get("sm_mhz", 0.0) >= 0.95 * clocks.get("sm_max_mhz", 1e9)
+    key = "bf16_tflops" if burst else "bf16_tflops_sustained"
+    return key, peaks[key]
+
+
+# The per-layer workloads and the gate each is held to: the small-channel stem
+# against the HBM roofline, the large-channel layers against the dense bf16
+# tensor peak (burst: each call is timed alone).
+GATES = (("stem", "hbm", 0.70), ("l1", "tensor", 0.60), ("l2", "tensor", 0.60),
+         ("l3", "tensor", 0.60))
+
+
+def call_us(stream, flush, fn, warm=3, reps=15):
+    """Median device time of fn() (one C ABI call) in microseconds: CUDA events
+    on the launching stream around the call only, L2 flushed before each run."""
+    import torch
+    evs = []
+    for r in range(warm + reps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        if r >= warm:
+            evs.append((a, b))
+    stream.synchronize()
+    return float(np.median([a.elapsed_time(b) * 1e3 for a, b in evs]))
+
+
+def config_gates(seed, device, stream, flush, peaks):
+    """Each pass of each per-layer workload timed alone, as a fraction of its
+    roofline, against its target; and the tiny fp32 check workload (launch-bound,
+    no target)."""
+    import torch
+    from x3_convolution_gb300 import _lib as Lb
+    sh = stream.cuda_stream
+    out = {}
+    for name, bound, target in GATES:
+        L = synth.CONFIGS[name][0]
+        wl = Workload([L], seed, device, keep_host=False)
+        rt = roofline_time_s(L, peaks)
+        rs = roofline_time_s(L, peaks, "bf16_tflops_sustained")
+        by = layer_bytes(L)
+        ent = {"bound": bound, "target": target, "shape": [L.N, L.Cin, L.Cout, L.H, L.W]}
+        for k, fn in (("fwd", _fwd), ("dgrad", _dgrad), ("wgrad", _wgrad)):
+            us = call_us(stream, flush, lambda: fn(wl, 0, sh))
+            frac = rt[k] / (us * 1e-6)
+            e = {"us": round(us, 2), "tflops": round(L.flops_per_pass() / (us * 1e-6) / 1e12, 1),
+                 "gbs": round(by[k] / (us * 1e-6) / 1e9, 1), "frac": round(frac, 3),
+                 "pass": bool(frac >= target), "traffic": recorded_traffic(name, k),
+                 "algorithmic_bytes": by[k]}
+            if bound == "tensor":
+                e["frac_sustained"] = round(rs[k] / (us * 1e-6), 3)
+            ent[k] = e
+        out[name] = ent
+        del wl
+        torch.cuda.empty_cache()
+    # tiny: the fp32 check path (CUDA-core fp32 FMA); launch-bound, parity only
+    T = synth.TINY
+    t = synth.make_tensors(T, seed=seed)
+    x, w, b, dy = (torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+                   for a in (t.x, t.w, t.bias, t.dy))
+    y = torch.empty((T.N, T.H, T.W, T.Cout), dtype=torch.float32, device=device)
+    dx = torch.empty_like(x)
+    dw = torch.empty((T.Cout, 3, 3, T.Cin), dtype=torch.float32, device=device)
+    db = torch.empty((T.Cout,), dtype=torch.float32, device=device)
+    tiny = {"bound": "launch", "target": None, "shape": [T.N, T.Cin, T.Cout, T.H, T.W],
+            "dtype": "f32"}
+    for k, fn in (("fwd", lambda: Lb.conv3x3_fwd_f32(x, w, b, y, T.N, T.Cin, T.Cout, T.H, T.W, 0, sh)),
+                  ("dgrad", lambda: Lb.conv3x3_dgrad_f32(dy, w, dx, T.N, T.Cin, T.Cout, T.H, T.W, sh)),
+                  ("wgrad", lambda: Lb.conv3x3_wgrad_f32(x, dy, dw, db, T.N, T.Cin, T.Cout, T.H,
+                                                        T.W, None, 0, sh))):
+        tiny[k] = {"us": round(call_us(stream, flush, fn), 2)}
+    out["tiny"] = tiny
+    return out
 
 
 def run_step(wl: Workload, stream_handle: int, record=None, mark=None, interleave=False,
@@ -470,7 +564,7 @@ def cuda_arm(args):
     # C ABI calls and these events are captured once into a CUDA graph that
     # each timed step replays on the same stream (the launches of 132 kernels
     # then cost the GPU no gaps); --no-graph launches them one by one.
-    # Per-call events (--detail) are recorded in extra steps after the timed
+    # Per-call events (the per-layer detail) are recorded in extra steps after the timed
     # region.
     fam_ms = {"fwd": 0.0, "dgrad": 0.0, "wgrad": 0.0}
     marks = {}
@@ -542,12 +636,12 @@ def cuda_arm(args):
         fam[k] = {"ms_per_step": round(float(t), 4), "tflops": round(fl / (t * 1e-3) / 1e12, 1)}
     dom = max(fam, key=lambda k: fam[k]["ms_per_step"])
     achieved = fl / (fam[dom]["ms_per_step"] * 1e-3) / 1e12
-    peak = peaks["bf16_tflops_sustained"]
+    peak_key, peak = pick_peak(peaks, clocks, sum(step_ms) * 1e-3)
     roof_s = sum(sum(roofline_time_s(L, peaks).values()) for L in layers)
 
     # per-layer detail: extra (untimed) steps with an event pair around every call
     per_layer = None
-    if args.detail:
+    if not args.no_detail:
         nlay = len(layers)
         per_call = {k: [[None, None] for _ in range(nlay)] for k in fam}
         call_ms = {k: np.zeros(nlay) for k in fam}
@@ -664,6 +758,10 @@ def cuda_arm(args):
                "launch": "stream" if e2e_graph is None else "CUDA graph (copies + C ABI calls)",
                "h2d_bytes_per_step": wl.h2d_bytes(), "d2h_bytes_per_step": wl.d2h_bytes()}
 
+    gates = None
+    if not args.no_gates:
+        gates = config_gates(args.seed, device, stream, flush, peaks)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(layers, args.seed, budget_s=args.cpu_budget)
@@ -692,15 +790,23 @@ def cuda_arm(args):
                                 "dgrad": "k_igemm + k_igemm_pair + k_stem_dgrad (dgrad pass)",
                                 "wgrad": "k_wgrad + k_wgrad_c8 + k_wgrad_reduce (wgrad pass)"}[dom],
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic(args, dom),
-                     "traffic_unit": "bytes per step (DRAM read + write, ncu)",
-                     "peak_source": peaks["source"] + " bf16 sustained"},
+                     "frac": round(achieved / peak, 4),
+                     "frac_burst": round(achieved / peaks["bf16_tflops"], 4),
+                     "frac_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                     "peak_source": "%s %s (%s)" % (
+                         peaks["source"], "bf16 burst" if peak_key == "bf16_tflops" else
+                         "bf16 sustained", "short timed region at full SM clock"
+                         if peak_key == "bf16_tflops" else "long or throttled timed region"),
+                     "traffic": None,
+                     "traffic_note": "per-call DRAM bytes of the per-layer configs are in gates "
+                                     "(scoped ncu captures); the step's 33 layers are not captured"},
         "passes": fam,
         "gpu_launches": launches,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clocks,
         "layers_detail": per_layer,
+        "gates": gates,
     }
     return line
 
@@ -788,7 +894,10 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
-    ap.add_argument("--detail", action="store_true", help="add a per-layer breakdown")
+    ap.add_argument("--no-detail", action="store_true",
+                    help="omit the per-layer breakdown of the step (extra untimed steps)")
+    ap.add_argument("--no-gates", action="store_true",
+                    help="omit the per-config calls timed alone against their targets")
     ap.add_argument("--wgrad-streams", type=int, default=2,
                     help="streams the wgrad calls go round-robin over (1 = one stream)")
     ap.add_argument("--no-graph", action="store_true",

@@ -43,7 +43,9 @@
  *   - every pointer non-NULL (bias / dbias may be NULL) and 16-byte aligned;
  *   - N*H*W*max(Cin,Cout) < 2^31 elements per activation tensor, H, W <= 65535;
  *   - act in {NONE, SILU, LRELU}; out_dtype in {BF16, F32}; path in {AUTO, TENSOR, SIMT}.
- * A launch failure returns CONV3X3_ERR_CUDA.  Kernels that wait on the
+ * A launch failure returns CONV3X3_ERR_CUDA.  The library keeps per-device
+ * state for device ordinals 0..63; a call made with a higher ordinal current
+ * returns CONV3X3_ERR_UNSUPPORTED.  Kernels that wait on the
  * hardware (mbarrier / TMA / tensor-core completion) give up after a bounded
  * time, record CONV3X3_ERR_TIMEOUT in the device status word and exit cleanly;
  * read it with conv3x3_device_status().
@@ -198,7 +200,8 @@ int conv3x3_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
  *     CONV3X3_ERR_INVALID_ARG.
  *   - The first call on a device looks up that device's copy of the array
  *     (cudaGetSymbolAddress, with the device current); make that first call
- *     before any stream capture.
+ *     before any stream capture.  Device ordinals 0..63 only (higher:
+ *     CONV3X3_ERR_UNSUPPORTED).
  *   - All calls on a device share the array and it keeps the previous call's
  *     contents (nothing needs clearing: every partial read is written first).
  *     Calls whose work overlaps on the GPU -- different streams without an

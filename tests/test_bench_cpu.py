@@ -1,7 +1,6 @@
 """Host logic of bench.py that needs no GPU: the step's call schedule (including
-the wgrad calls spread over several streams) and the guard on the recorded DRAM
-traffic."""
-import hashlib
+the wgrad calls spread over several streams), the guard on the recorded DRAM
+traffic, the choice of the tensor peak and the gate targets."""
 import os
 import sys
 import types
@@ -80,26 +79,36 @@ def test_interleaved_schedule(monkeypatch):
     assert back == [(k, i) for i in reversed(range(4)) for k in ("dgrad", "wgrad")]
 
 
-def _sources_sha256():
-    h = hashlib.sha256()
-    for f in bench.TRAFFIC_SOURCES:
-        with open(os.path.join(ROOT, "x3_convolution_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    return h.hexdigest()
-
-
 def test_recorded_traffic_guard(monkeypatch):
-    args = types.SimpleNamespace(workload="unet", fused_act=False, concat_free=False)
-    monkeypatch.setattr(bench, "TRAFFIC_SHA256", _sources_sha256())
-    for dom in ("fwd", "dgrad", "wgrad"):
-        assert bench.recorded_traffic(args, dom) == bench.TRAFFIC_BYTES[dom]
-    # another workload or variant: the capture does not apply
-    for other in (dict(workload="l1"), dict(fused_act=True), dict(concat_free=True)):
-        a = types.SimpleNamespace(**dict(vars(args), **other))
-        assert bench.recorded_traffic(a, "fwd") is None
+    monkeypatch.setattr(bench, "RECORDED_TRAFFIC", {("l1", "fwd"): 1.5e8})
+    monkeypatch.setattr(bench, "TRAFFIC_SHA256", bench.sources_sha256())
+    assert bench.sources_sha256() is not None
+    assert bench.recorded_traffic("l1", "fwd") == 1.5e8
+    # no capture for this config or pass
+    assert bench.recorded_traffic("l2", "fwd") is None
+    assert bench.recorded_traffic("l1", "wgrad") is None
     # kernel sources changed since the capture: no figure
     monkeypatch.setattr(bench, "TRAFFIC_SHA256", "0" * 64)
-    assert bench.recorded_traffic(args, "wgrad") is None
+    assert bench.recorded_traffic("l1", "fwd") is None
+
+
+def test_peak_choice():
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0}
+    assert bench.pick_peak(peaks, full, 0.3) == ("bf16_tflops", 1900.0)
+    # a long timed region, a clock well below its maximum, or no clock record:
+    # the sustained figure
+    assert bench.pick_peak(peaks, full, 3.0) == ("bf16_tflops_sustained", 1700.0)
+    assert bench.pick_peak(peaks, {"sm_mhz": 1500.0, "sm_max_mhz": 2070.0}, 0.3)[0] == \
+        "bf16_tflops_sustained"
+    assert bench.pick_peak(peaks, None, 0.3)[0] == "bf16_tflops_sustained"
+
+
+def test_gate_targets():
+    # the small-channel stem is held to the HBM roofline, the others to the tensor peak
+    g = {name: (bound, target) for name, bound, target in bench.GATES}
+    assert g == {"stem": ("hbm", 0.70), "l1": ("tensor", 0.60), "l2": ("tensor", 0.60),
+                 "l3": ("tensor", 0.60)}
 
 
 def test_wgrad_streams_validated():

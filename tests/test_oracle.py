@@ -439,6 +439,16 @@ def test_sampled_entry_points_equal_full_results():
     dw, _ = oracle.conv3x3_wgrad(x, dz)
     idx = rng.choice(dw.size, 50, replace=False)
     assert np.allclose(oracle.conv3x3_wgrad_at(x, dz, idx), dw.reshape(-1)[idx], rtol=1e-13, atol=1e-13)
+    # the sampled dgrad through the input's activation: every element of a
+    # shape whose sizes are all distinct (a slip in the index decode cannot
+    # land on a value that happens to be equal), both activations
+    zin = 3.0 * rand(N, H, W, Cin)
+    every = np.arange(N * H * W * Cin)
+    for act in (1, 2):
+        full = oracle.conv3x3_dgrad_act(dz, w, zin, act)
+        assert np.array_equal(oracle.conv3x3_dgrad_act_at(dz, w, zin, act, every), full.reshape(-1))
+        idx = rng.choice(full.size, 50, replace=False)
+        assert np.array_equal(oracle.conv3x3_dgrad_act_at(dz, w, zin, act, idx), full.reshape(-1)[idx])
 
 
 def test_results_do_not_depend_on_thread_count():
@@ -505,6 +515,13 @@ MUTANTS = {
     "strided wgrad column off by one": ("        int64_t ww = j->u * wo + s - 1;", "        int64_t ww = j->u * wo + s;"),
     "strided dbias drops the last image": ("for (int64_t p = 0; p < j->N * Ho * Wo; ++p)",
                                            "for (int64_t p = 0; p < (j->N - 1) * Ho * Wo; ++p)"),
+    "sampled dgrad_act reads zin at the pixel, not the element": (
+        "j->out[i] = oracle_act_grad_f64(j->act, j->zin[e])", "j->out[i] = oracle_act_grad_f64(j->act, j->zin[p])"),
+    "sampled dgrad_act decodes the row one off": (
+        "int64_t w = p % j->W, h = (p / j->W) % j->H, n = p / (j->W * j->H);\n  j->out[i] = oracle_act_grad_f64",
+        "int64_t w = p % j->W, h = (p / j->W) % j->H, n = p / (j->W * j->H);\n  h = (h + 1) % j->H;\n"
+        "  j->out[i] = oracle_act_grad_f64"),
+    "sampled wgrad decodes the tap transposed": ("int64_t r = rs / 3, s = rs % 3;", "int64_t r = rs % 3, s = rs / 3;"),
     "dgrad_act reads zin of channel 0": ("j->out[e] = oracle_act_grad_f64(j->act, j->zin[e]) * dgrad_point(j, n, h, w, c);",
                                          "j->out[e] = oracle_act_grad_f64(j->act, j->zin[e - c]) * dgrad_point(j, n, h, w, c);"),
 }
@@ -545,6 +562,7 @@ def _suite():
         test_bilinear_wgrad_identity_and_dbias,
         test_brute_force_im2col_all_three_passes,
         test_hand_computed_fixture,
+        test_sampled_entry_points_equal_full_results,
     ]
 
 

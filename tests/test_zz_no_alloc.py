@@ -67,6 +67,24 @@ def test_noalloc_after_a_different_shape():
         assert rel_err(db.double().cpu().numpy(), ref_db.double().cpu().numpy()) <= TOL
 
 
+def test_noalloc_allocates_no_device_memory():
+    # after a first call (which loads the kernels and looks up the array), a
+    # call leaves the device's free memory exactly where it was
+    N, Cin, Cout, H, W = 16, 128, 128, 32, 32
+    x, dy = _inputs((N, Cin, Cout, H, W), seed=3)
+    dw = torch.empty((Cout, 3, 3, Cin), device="cuda")
+    db = torch.empty((Cout,), device="cuda")
+    L.conv3x3_wgrad_noalloc(x, dy, dw, db, N, Cin, Cout, H, W)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        L.conv3x3_wgrad_noalloc(x, dy, dw, db, N, Cin, Cout, H, W)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert L.conv3x3_device_status() == L.OK
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     # 2048 -> 2048 channels: one dw partial alone is ~151 MB
     N, Cin, Cout, H, W = 64, 2048, 2048, 8, 8

@@ -65,7 +65,8 @@ unsigned long long wait_limit_ns() {
 // Device context for the current device; set-up happens on first use per device.
 int get_ctx(DevCtx* out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CONV3X3_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return CONV3X3_ERR_CUDA;
+  if (dev >= kMaxDevices) return CONV3X3_ERR_UNSUPPORTED;  // beyond the per-device table
   std::lock_guard<std::mutex> g(g_mu);
   load_entry_points();
   DeviceInfo& di = g_dev[dev];

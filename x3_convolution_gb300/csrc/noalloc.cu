@@ -26,7 +26,7 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_wgrad_scratch[CONV3X3_WGRAD_NOALLOC_MAX_BYTES];
 
-constexpr int kMaxDevices = 64;
+constexpr int kMaxDevices = 64;  // device ordinals 0..63
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
 
@@ -35,7 +35,8 @@ void* g_scratch_ptr[kMaxDevices] = {nullptr};
 // cudaGetSymbolAddress with the device current; done once per device.
 int scratch_for_current_device(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CONV3X3_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return CONV3X3_ERR_CUDA;
+  if (dev >= kMaxDevices) return CONV3X3_ERR_UNSUPPORTED;  // beyond the per-device cache
   std::lock_guard<std::mutex> g(g_mu);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
