@@ -24,6 +24,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "conv3x3_oracle.c")
+_SRC_UFD = os.path.join(_HERE, "upfirdn2d_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
@@ -34,10 +35,12 @@ _lp = ctypes.POINTER(ctypes.c_int64)
 
 def build(force: bool = False) -> str:
     """Compile the oracle into ``oracle/liboracle.so`` (gcc, -O2, no fast-math)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    srcs = [_SRC, _SRC_UFD]
+    if force or not os.path.exists(_LIB) or any(os.path.getmtime(_LIB) < os.path.getmtime(f)
+                                                for f in srcs):
         tmp = _LIB + ".tmp%d" % os.getpid()
         cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-shared", "-fPIC",
-               "-pthread", _SRC, "-o", tmp, "-lm"]
+               "-pthread"] + srcs + ["-o", tmp, "-lm"]
         subprocess.check_call(cmd)
         os.replace(tmp, _LIB)
     return _LIB
@@ -72,6 +75,10 @@ def _load():
         lib.oracle_conv3x3_dgrad_strided_at_f64.argtypes = [_dp, _dp] + [_i64] * 6 + [_lp, _i64, _dp]
         lib.oracle_conv3x3_wgrad_strided_f64.argtypes = [_dp, _dp, _dp] + [_i64] * 6
         lib.oracle_conv3x3_wgrad_strided_at_f64.argtypes = [_dp, _dp] + [_i64] * 6 + [_lp, _i64, _dp]
+        lib.oracle_upfirdn2d_f64.argtypes = [_dp, _dp, _dp] + [_i64] * 12
+        lib.oracle_upfirdn2d_at_f64.argtypes = [_dp, _dp] + [_i64] * 12 + [_lp, _i64, _dp]
+        lib.oracle_upfirdn2d_out_len.argtypes = [_i64] * 6
+        lib.oracle_upfirdn2d_out_len.restype = _i64
         _lib = lib
     return _lib
 
@@ -340,4 +347,56 @@ def conv3x3_wgrad_strided_at(x, dz, u, idx):
     out = np.empty(idx.shape[0], np.float64)
     _load().oracle_conv3x3_wgrad_strided_at_f64(_ptr(x), _ptr(dz), N, Cin, Cout, H, W, int(u),
                                                 idx.ctypes.data_as(_lp), idx.shape[0], _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# upfirdn2d: upsample (zeros after each pixel), zero-pad, FIR filter
+# (convolution), downsample -- the StyleGAN2 custom-kernel blog's filtered
+# up/downsampling (page titled "Dim3 grid calculation code", first paragraph).
+# The arithmetic is in upfirdn2d_oracle.c.
+# ---------------------------------------------------------------------------
+def _pads(pad):
+    """(pad_x0, pad_x1, pad_y0, pad_y1) from an int, a pair (x, y) or a 4-tuple."""
+    if isinstance(pad, int):
+        return pad, pad, pad, pad
+    pad = tuple(int(p) for p in pad)
+    if len(pad) == 2:
+        return pad[0], pad[0], pad[1], pad[1]
+    assert len(pad) == 4, pad
+    return pad
+
+
+def upfirdn2d_out_len(length, up, down, p0, p1, k):
+    return int(_load().oracle_upfirdn2d_out_len(length, up, down, p0, p1, k))
+
+
+def upfirdn2d(x, f, up: int = 1, down: int = 1, pad=0):
+    """x [N,H,W,C], f [kh,kw]; pad = (pad_x0, pad_x1, pad_y0, pad_y1).  Returns
+    y [N,Ho,Wo,C]: every channel upsampled, padded, convolved with f and
+    downsampled, in that order."""
+    x = _d(x)
+    N, H, W, C = x.shape
+    f = _d(f)
+    kh, kw = f.shape
+    px0, px1, py0, py1 = _pads(pad)
+    Ho = upfirdn2d_out_len(H, up, down, py0, py1, kh)
+    Wo = upfirdn2d_out_len(W, up, down, px0, px1, kw)
+    y = np.empty((N, Ho, Wo, C), np.float64)
+    _load().oracle_upfirdn2d_f64(_ptr(x), _ptr(f), _ptr(y), N, H, W, C, up, down, px0, px1, py0,
+                                 py1, kh, kw)
+    return y
+
+
+def upfirdn2d_at(x, f, up, down, pad, idx):
+    """y at the given linear NHWC indices of the output."""
+    x = _d(x)
+    N, H, W, C = x.shape
+    f = _d(f)
+    kh, kw = f.shape
+    px0, px1, py0, py1 = _pads(pad)
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    out = np.empty(idx.shape[0], np.float64)
+    _load().oracle_upfirdn2d_at_f64(_ptr(x), _ptr(f), N, H, W, C, up, down, px0, px1, py0, py1,
+                                    kh, kw, idx.ctypes.data_as(_lp), idx.shape[0], _ptr(out))
     return out
