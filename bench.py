@@ -198,11 +198,13 @@ def max_over_ranks(value: float, ws: int, device=None) -> float:
 # the CUDA arm
 # ---------------------------------------------------------------------------
 class Workload:
-    def __init__(self, layers, seed, device, keep_host=True, fused_act=False, concat_free=False):
+    def __init__(self, layers, seed, device, keep_host=True, fused_act=False, concat_free=False,
+                 path=0):
         import torch
         self.layers = layers
         self.fused_act = fused_act
         self.concat_free = concat_free
+        self.path = path  # kernel family of the plain calls (0 = AUTO)
         self.dev = []
         self.host = []
         ws_max = 0
@@ -270,7 +272,8 @@ class Workload:
                 ws_max = max(ws_max, Lb.conv3x3_wgrad_cat_workspace_bytes(
                     L.N, L.Cin, L.cat_a, L.Cout, L.H, L.W, Lb.PATH_AUTO))
             else:
-                ws_max = max(ws_max, Lb.conv3x3_wgrad_workspace_bytes(L.N, L.Cin, L.Cout, L.H, L.W))
+                ws_max = max(ws_max, Lb.conv3x3_wgrad_workspace_bytes_ex(L.N, L.Cin, L.Cout, L.H, L.W,
+                                                                         path))
         self.ws_bytes = ws_max
         self.ws = torch.empty(max(ws_max, 256), dtype=torch.uint8, device=device)
         # one more split-K workspace per extra wgrad stream (see run_step)
@@ -307,6 +310,9 @@ def _fwd(wl, i, sh):
     elif wl.fused_act:
         Lb.conv3x3_fwd_save_z(d["x"], d["w"], d["b"], d["y"], d["z"], L.N, L.Cin, L.Cout, L.H, L.W,
                               L.act, Lb.DT_BF16, Lb.PATH_AUTO, sh)
+    elif getattr(wl, "path", 0):
+        Lb.conv3x3_fwd_ex(d["x"], d["w"], d["b"], d["y"], L.N, L.Cin, L.Cout, L.H, L.W, L.act,
+                          Lb.DT_BF16, wl.path, sh)
     else:
         Lb.conv3x3_fwd(d["x"], d["w"], d["b"], d["y"], L.N, L.Cin, L.Cout, L.H, L.W, L.act, sh)
     return 1
@@ -325,6 +331,9 @@ def _dgrad(wl, i, sh):
     elif wl.fused_act:
         Lb.conv3x3_dgrad_act(d["dy"], d["w"], d["zin"], d["act_in"], d["dx"], L.N, L.Cin, L.Cout,
                              L.H, L.W, Lb.DT_BF16, Lb.PATH_AUTO, sh)
+    elif getattr(wl, "path", 0):
+        Lb.conv3x3_dgrad_ex(d["dy"], d["w"], d["dx"], L.N, L.Cin, L.Cout, L.H, L.W, Lb.DT_BF16,
+                            wl.path, sh)
     else:
         Lb.conv3x3_dgrad(d["dy"], d["w"], d["dx"], L.N, L.Cin, L.Cout, L.H, L.W, sh)
     return 1
@@ -340,6 +349,9 @@ def _wgrad(wl, i, sh, side=-1):
     elif d["cat_a"]:
         Lb.conv3x3_wgrad_cat(d["xa"], d["xb"], d["cat_a"], d["dy"], d["dw"], d["db"], L.N, L.Cin,
                              L.Cout, L.H, L.W, ws, wl.ws_bytes, Lb.PATH_AUTO, sh)
+    elif getattr(wl, "path", 0):
+        Lb.conv3x3_wgrad_ex(d["x"], d["dy"], d["dw"], d["db"], L.N, L.Cin, L.Cout, L.H, L.W, ws,
+                            wl.ws_bytes, wl.path, sh)
     else:
         Lb.conv3x3_wgrad(d["x"], d["dy"], d["dw"], d["db"], L.N, L.Cin, L.Cout, L.H, L.W, ws,
                          wl.ws_bytes, sh)
@@ -535,8 +547,9 @@ def cuda_arm(args):
 
     layers = synth.CONFIGS[args.workload]
     peaks = load_peaks()
+    path = {"auto": Lb.PATH_AUTO, "tensor": Lb.PATH_TENSOR, "simt": Lb.PATH_SIMT}[args.path]
     wl = Workload(layers, args.seed, device, keep_host=not args.no_e2e, fused_act=args.fused_act,
-                  concat_free=args.concat_free)
+                  concat_free=args.concat_free, path=path)
     stream = torch.cuda.Stream(device=device)
     sh = stream.cuda_stream
     # the wgrad pass runs on --wgrad-streams streams (1: in order on one)
@@ -781,6 +794,7 @@ def cuda_arm(args):
                    "l2": "flushed between steps (write of 2x L2)",
                    "flops_per_step": flops_step, "flops_per_step_padded_cin": flops_padded,
                    "launch": "stream" if graph is None else "CUDA graph of the step's C ABI calls",
+                   "kernel_family": args.path,
                    "fused_act_backward": bool(args.fused_act),
                    "concat_free_up_path": bool(args.concat_free),
                    "wgrad_streams": 1 if wstreams is None else len(wstreams)},
@@ -809,6 +823,154 @@ def cuda_arm(args):
         "gates": gates,
     }
     return line
+
+
+# ---------------------------------------------------------------------------
+# filtered resampling (upfirdn2d) between the UNet's levels
+# ---------------------------------------------------------------------------
+UFD_METRIC = "upfirdn2d UNet 2x resampling throughput (GB/s of algorithmic HBM traffic) on 1 GB300 and % of HBM roofline"
+
+
+def upfirdn2d_arm(args):
+    """One step = the six resampling ops between the UNet's levels (2x down at
+    64, 32, 16; 2x up at 8, 16, 32), batch 64, bf16 NHWC, each through the
+    upfirdn2d C ABI call.  The metric is algorithmic bytes (x read once, y
+    written once) per second against the measured HBM copy bandwidth."""
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    device = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(device)
+    import __graft_entry__ as ge
+    ge.build()
+    from x3_convolution_gb300 import _lib as Lb
+    ops_ = synth.UPFIRDN2D
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(device=device)
+    sh = stream.cuda_stream
+    xs, ys, fs, hx, hy = [], [], [], [], []
+    for i, op in enumerate(ops_):
+        x = synth.make_resample_input(op, seed=args.seed, index=i)
+        t = torch.from_numpy(synth.bf16_bits(x).view(np.int16)).view(torch.bfloat16)
+        xs.append(t.to(device))
+        ys.append(torch.empty((op.N, op.Ho, op.Wo, op.C), dtype=torch.bfloat16, device=device))
+        fs.append(op.filter())
+        if not args.no_e2e:
+            hx.append(t.pin_memory())
+            hy.append(torch.empty((op.N, op.Ho, op.Wo, op.C), dtype=torch.bfloat16).pin_memory())
+    bytes_step = sum(op.bytes() for op in ops_)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device=device)
+
+    def call(i, x=None, y=None):
+        op = ops_[i]
+        Lb.upfirdn2d(xs[i] if x is None else x, fs[i], ys[i] if y is None else y, op.N, op.C, op.H,
+                     op.W, op.up, op.down, *op.pad, 4, 4, Lb.DT_BF16, sh)
+
+    def step():
+        for i in range(len(ops_)):
+            call(i)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(gpu_selector(device))
+    sampler.start()
+    time.sleep(0.3)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    evs = []
+    for _ in range(args.steps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step()
+            b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    ms_max = max_over_ranks(ms, ws, device)
+    value = bytes_step * ws / (ms_max * 1e-3) / 1e9
+    # each op timed alone (L2 flushed before every call)
+    detail = []
+    for i, op in enumerate(ops_):
+        us = call_us(stream, flush, lambda i=i: call(i))
+        detail.append({"name": op.name, "C": op.C, "H": op.H, "Ho": op.Ho, "up": op.up, "down": op.down,
+                       "us": round(us, 2), "gbs": round(op.bytes() / (us * 1e-6) / 1e9, 1),
+                       "frac": round(op.bytes() / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3)})
+    dom = max(detail, key=lambda d: d["us"])
+    e2e = None
+    if not args.no_e2e:
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for i in range(len(ops_)):
+                    xs[i].copy_(hx[i], non_blocking=True)
+                    call(i)
+                    hy[i].copy_(ys[i], non_blocking=True)
+            stream.synchronize()
+        e2e_step()
+        t = []
+        for _ in range(max(3, min(args.steps, 10))):
+            t0 = time.perf_counter()
+            e2e_step()
+            t.append((time.perf_counter() - t0) * 1e3)
+        e_ms = max_over_ranks(float(np.median(t)), ws, device)
+        e2e = {"value": round(bytes_step * ws / (e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+               "ms_per_step": round(e_ms, 3), "statistic": "median step",
+               "h2d_bytes_per_step": sum(h.numel() * 2 for h in hx),
+               "d2h_bytes_per_step": sum(h.numel() * 2 for h in hy)}
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = upfirdn2d_cpu_baseline(args.seed, budget_s=min(args.cpu_budget, 15.0))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if rank != 0:
+        return None
+    achieved = value / ws
+    return {
+        "metric": UFD_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded splitmix64 + Box-Muller normals)",
+        "config": {"workload": "upfirdn2d", "ops": len(ops_), "batch": ops_[0].N,
+                   "filter": "binomial [1,3,3,1] x [1,3,3,1] / 64 (x up^2 when upsampling)",
+                   "bytes_per_step": bytes_step, "l2": "flushed between steps (write of 2x L2)"},
+        "roofline": {"bound": "hbm", "kernel": "k_upfirdn2d (all six ops)",
+                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": None, "peak_source": peaks["source"] + " HBM copy"},
+        "ops_detail": detail, "slowest_op": dom["name"],
+        "gpu_launches": len(ops_) * args.steps, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
+    }
+
+
+def upfirdn2d_cpu_baseline(seed, budget_s=None):
+    """The oracle on one image of each op (fp64, all host cores), in bytes/s;
+    with a budget, the ops after the one that crosses it are skipped."""
+    import oracle
+    tot_t, tot_b, done = 0.0, 0, 0
+    for i, op in enumerate(synth.UPFIRDN2D):
+        if budget_s is not None and tot_t >= budget_s:
+            break
+        one = synth.Resample(op.name, 1, op.C, op.H, op.W, op.up, op.down, op.pad)
+        x = synth.make_resample_input(one, seed=seed, index=i)
+        t0 = time.perf_counter()
+        oracle.upfirdn2d(x, one.filter().astype(np.float64), one.up, one.down, one.pad)
+        tot_t += time.perf_counter() - t0
+        tot_b += one.bytes()
+        done += 1
+    return {"value": tot_b / tot_t / 1e9, "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": "image 0 of %d of %d ops (fp64, four materialised steps), %.3f s"
+                      % (done, len(synth.UPFIRDN2D), tot_t)}
 
 
 # ---------------------------------------------------------------------------
@@ -858,6 +1020,21 @@ def reference_arm(args):
     import oracle
     oracle.build()
     synth.build()
+    if args.workload == "upfirdn2d":
+        steps = []
+        for _ in range(args.warmup):
+            upfirdn2d_cpu_baseline(args.seed)
+        for _ in range(args.steps):
+            steps.append(upfirdn2d_cpu_baseline(args.seed))
+        value = float(np.mean([c["value"] for c in steps]))
+        return {
+            "impl": "reference", "metric": UFD_METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "upfirdn2d", "ops": len(synth.UPFIRDN2D)},
+            "cpu_baseline": dict(steps[-1], value=value),
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
     layers = synth.CONFIGS[args.workload]
     for i in range(args.warmup):
         oracle_sample(layers[i % len(layers)], args.seed, i % len(layers))
@@ -889,7 +1066,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
-    ap.add_argument("--workload", choices=sorted(synth.CONFIGS), default="unet")
+    ap.add_argument("--workload", choices=sorted(synth.CONFIGS) + ["upfirdn2d"], default="unet")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -900,6 +1077,8 @@ def main(argv=None):
                     help="omit the per-config calls timed alone against their targets")
     ap.add_argument("--wgrad-streams", type=int, default=2,
                     help="streams the wgrad calls go round-robin over (1 = one stream)")
+    ap.add_argument("--path", choices=["auto", "tensor", "simt"], default="auto",
+                    help="kernel family of the plain calls (auto: the library picks)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps call by call instead of replaying a CUDA graph")
     ap.add_argument("--concat-free", action="store_true",
@@ -912,7 +1091,12 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.wgrad_streams < 1:
         ap.error("--wgrad-streams must be >= 1")
-    line = reference_arm(args) if args.impl == "reference" else cuda_arm(args)
+    if args.impl == "reference":
+        line = reference_arm(args)
+    elif args.workload == "upfirdn2d":
+        line = upfirdn2d_arm(args)
+    else:
+        line = cuda_arm(args)
     if line is not None:
         if line.get("layers_detail") is None:
             line.pop("layers_detail", None)

@@ -214,3 +214,52 @@ UNET_STEP = [STEM] + STACK
 
 CONFIGS = {"tiny": [TINY], "stem": [STEM], "l1": [L1], "l2": [L2], "l3": [L3], "stack": STACK,
            "unet": UNET_STEP, "downsample": DOWNSAMPLE}
+
+
+# ---------------------------------------------------------------------------
+# filtered resampling (upfirdn2d) between the UNet's levels
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class Resample:
+    """One upfirdn2d op: x [N, H, W, C] resampled by `up` / `down` with the
+    binomial [1,3,3,1] (x) [1,3,3,1] / 64 filter (times up^2 when upsampling,
+    so that a constant keeps its value) and pads (pad_x0, pad_x1, pad_y0,
+    pad_y1) that make the output exactly 2x or 1/2x the input."""
+    name: str
+    N: int
+    C: int
+    H: int
+    W: int
+    up: int = 1
+    down: int = 1
+    pad: tuple = (0, 0, 0, 0)
+
+    def filter(self) -> np.ndarray:
+        a = np.array([1.0, 3.0, 3.0, 1.0], np.float64)
+        return (np.outer(a, a) / 64.0 * self.up * self.up).astype(np.float32)
+
+    @property
+    def Ho(self) -> int:
+        return (self.H * self.up + self.pad[2] + self.pad[3] - 4) // self.down + 1
+
+    @property
+    def Wo(self) -> int:
+        return (self.W * self.up + self.pad[0] + self.pad[1] - 4) // self.down + 1
+
+    def bytes(self) -> int:
+        """Algorithmic HBM bytes: x read once, y written once (bf16)."""
+        return 2 * self.C * self.N * (self.H * self.W + self.Ho * self.Wo)
+
+
+def make_resample_input(op: Resample, seed: int = 0, index: int = 0) -> np.ndarray:
+    """Seeded x [N, H, W, C] ~ N(0, 1), rounded to bf16."""
+    return bf16_round(normal(stream_id(seed, 64 + index, X), (op.N, op.H, op.W, op.C), 1.0))
+
+
+# The resampling between the UNet's levels (base 128, multipliers 1,2,3,4,
+# 64 -> 8 and back), batch 64: 2x downsampling (pads 1, 1) on the way down,
+# 2x upsampling (pads 2, 1) on the way up.
+UPFIRDN2D = ([Resample(f"down{l}.blur_down", 64, c, r, r, down=2, pad=(1, 1, 1, 1))
+              for l, (c, r) in enumerate([(128, 64), (256, 32), (384, 16)])]
+             + [Resample(f"up{l}.blur_up", 64, c, r, r, up=2, pad=(2, 1, 2, 1))
+                for l, (c, r) in zip((3, 2, 1), [(512, 8), (384, 16), (256, 32)])])

@@ -7,7 +7,7 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "conv3x3.h")
+INCLUDE = os.path.join(ROOT, "include")
 
 
 @pytest.fixture(scope="module")
@@ -19,10 +19,14 @@ def lib():
 
 
 def declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    names = re.findall(r"\b(conv3x3_\w+)\s*\(", src)
-    return sorted(set(names))
+    """Every function declared in include/*.h."""
+    names = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            src = open(os.path.join(INCLUDE, h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names.update(re.findall(r"\b((?:conv3x3|upfirdn2d)\w*)\s*\(", src))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
@@ -31,6 +35,25 @@ def test_header_declares_the_boundary():
               "conv3x3_fwd_f32", "conv3x3_dgrad_f32", "conv3x3_wgrad_f32",
               "conv3x3_device_status", "conv3x3_status_string"]:
         assert n in names
+
+
+def test_upfirdn2d_is_declared_and_validates_without_a_gpu(lib):
+    assert "upfirdn2d" in declared_functions() and "upfirdn2d_out_size" in declared_functions()
+    assert lib.upfirdn2d_out_size(64, 2, 1, 2, 1, 4) == 128
+    assert lib.upfirdn2d_out_size(64, 1, 2, 1, 1, 4) == 32
+    assert lib.upfirdn2d_out_size(64, 9, 1, 0, 0, 4) == 0     # factor beyond the limit
+    assert lib.upfirdn2d_out_size(64, 1, 1, -1, 0, 4) == 0    # cropping is not a pad
+    assert lib.upfirdn2d_out_size(2, 1, 1, 0, 0, 4) == 0      # kernel longer than the plane
+    f = (ctypes.c_float * 16)(*([1.0 / 16] * 16))
+    ok = (ALIGNED, f, ALIGNED, 2, 64, 8, 8, 1, 2, 1, 1, 1, 1, 4, 4, 0, None)
+    bad = [dict(C=12), dict(C=0), dict(up=0), dict(down=9), dict(kh=9), dict(px0=-1),
+           dict(dtype=2), dict(x=ALIGNED + 4), dict(f=None)]
+    keys = ["x", "f", "y", "N", "C", "H", "W", "up", "down", "px0", "px1", "py0", "py1", "kh", "kw",
+            "dtype", "stream"]
+    for b in bad:
+        a = dict(zip(keys, ok))
+        a.update(b)
+        assert lib.upfirdn2d(*[a[k] for k in keys]) == 1, b
 
 
 def test_every_declared_symbol_is_exported(lib):

@@ -186,6 +186,8 @@ STEM_SHAPES = [
     (2, 8, 256, 8, 8),    # the widest single N tile
     (3, 8, 128, 1, 13),   # single-row images
     (5, 8, 128, 16, 16),  # several 128-pixel tiles per CTA
+    (2, 8, 72, 9, 11),    # 128-channel tile, second 64-channel store box clipped to 8 channels
+    (1, 8, 104, 13, 10),  # clipped store box and a ragged pixel tail
 ]
 
 

@@ -50,6 +50,8 @@ _SIGS = {
     "conv3x3_dgrad_strided": ([_vp, _vp, _vp, _vp, _i] + [_i] * 8 + [_vp], _i),
     "conv3x3_wgrad_strided": ([_vp, _vp, _vp, _vp] + [_i] * 6 + [_vp, _sz, _i, _vp], _i),
     "conv3x3_wgrad_strided_workspace_bytes": ([_i] * 7, _sz),
+    "upfirdn2d": ([_vp, ctypes.POINTER(ctypes.c_float), _vp] + [_i] * 13 + [_vp], _i),
+    "upfirdn2d_out_size": ([_i] * 6, _i),
 }
 
 WGRAD_NOALLOC_MAX_BYTES = 64 << 20
@@ -248,3 +250,23 @@ def conv3x3_wgrad_noalloc(x, dy, dw, dbias, N, Cin, Cout, H, W, stream=None):
     for the sharing rules)."""
     return _check(load().conv3x3_wgrad_noalloc(_p(x), _p(dy), _p(dw), _p(dbias), N, Cin, Cout, H, W,
                                                _stream(stream)), "conv3x3_wgrad_noalloc")
+
+
+def _host_f32(a):
+    """A host fp32 array (filter taps) as a ctypes pointer, and its keep-alive."""
+    import numpy as np
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.float32).reshape(-1))
+    return arr.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), arr
+
+
+def upfirdn2d(x, f, y, N, C, H, W, up, down, pad_x0, pad_x1, pad_y0, pad_y1, kh, kw,
+              out_dtype=DT_BF16, stream=None):
+    fp, keep = _host_f32(f)
+    rc = load().upfirdn2d(_p(x), fp, _p(y), N, C, H, W, up, down, pad_x0, pad_x1, pad_y0, pad_y1,
+                          kh, kw, out_dtype, _stream(stream))
+    del keep
+    return _check(rc, "upfirdn2d")
+
+
+def upfirdn2d_out_size(length, up, down, pad0, pad1, k) -> int:
+    return int(load().upfirdn2d_out_size(length, up, down, pad0, pad1, k))

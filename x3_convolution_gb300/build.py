@@ -18,7 +18,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(os.path.dirname(PKG), "_build")
 LIB = os.path.join(PKG, "libconv3x3.so")
-SOURCES = ["api.cu", "simt.cu", "tc.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "simt.cu", "tc.cu", "noalloc.cu", "upfirdn2d.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xcompiler", "-Wall"]
@@ -30,8 +30,9 @@ def nvcc() -> str:
 
 
 def _deps():
+    inc = os.path.join(os.path.dirname(PKG), "include")
     return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [
-        os.path.join(os.path.dirname(PKG), "include", "conv3x3.h")]
+        os.path.join(inc, f) for f in os.listdir(inc)]
 
 
 def _stale() -> bool:

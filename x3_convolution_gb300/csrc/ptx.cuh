@@ -130,6 +130,31 @@ __device__ __forceinline__ void tma_prefetch_im2col_4d(const CUtensorMap* m, int
       : "memory");
 }
 
+// TMA store of a 2-D box from shared memory (bulk-group completion).  The box
+// is clipped to the tensor: rows or columns past its end are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most N committed bulk groups of this thread still reading shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// at most N committed bulk groups of this thread not yet complete
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// this thread's generic-proxy shared-memory writes become visible to TMA
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -303,5 +328,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
 // the fast (2-ulp) divide; for z below about -87 the denominator exceeds 2^126
 // and the quotient is 0, the limit of SiLU there to well below fp32 resolution.
 __device__ __forceinline__ float silu_f32(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// SiLU through tanh: z * sigmoid(z) = h + h * tanh(h) with h = z / 2, since
+// sigmoid(z) = (1 + tanh(z / 2)) / 2.  One special-function op (the hardware
+// tanh approximation, relative error near 2^-11) where silu_f32 takes two; the
+// 8-input-channel forward, whose epilogue is its bottleneck, uses it.  At
+// large |z| tanh saturates to +-1 and the result to z or -0.
+__device__ __forceinline__ float silu_tanh_f32(float z) {
+  const float h = 0.5f * z;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+  return fmaf(h, t, h);
+}
 
 }  // namespace c3

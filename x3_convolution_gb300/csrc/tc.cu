@@ -210,8 +210,9 @@ __device__ __forceinline__ void load_bias(const IgemmParams& p, int col0, float 
 
 // Epilogue of one 32-column chunk: (+ bias) -> [store z] -> activation ->
 // [* act'(z_in)] -> fp32 or bf16 store.  kExt = false compiles out the fused
-// extras (z store, z_in scaling, split output) for the plain calls.
-template <bool kExt>
+// extras (z store, z_in scaling, split output) for the plain calls; kTanh
+// takes SiLU through tanh (silu_tanh_f32).
+template <bool kExt, bool kTanh = false>
 __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix, int col0,
                                             const uint32_t (&v)[32], const float (&bv)[32],
                                             const uint4 (&zr)[4]) {
@@ -225,7 +226,7 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix,
   if (kExt && p.zout) store_bf16x32(p.zout + pix * p.nout + col0, p.nout - col0, f);
   if (p.act == CONV3X3_ACT_SILU) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) f[i] = silu_f32(f[i]);
+    for (int i = 0; i < 32; ++i) f[i] = kTanh ? silu_tanh_f32(f[i]) : silu_f32(f[i]);
   } else if (p.act == CONV3X3_ACT_LRELU) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) f[i] = f[i] >= 0.0f ? f[i] : 0.2f * f[i];
@@ -1204,28 +1205,49 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 // 2j, 2j+1 form the K = 16 of MMA j (K = 9 taps x 8 + one zero tap = 80, five
 // MMAs per tile).  The weights ([Cout][9][8], 2 KB per tap for 128 outputs) stay
 // resident in shared memory for the whole kernel.
-template <int BN>
+//
+// The bias rides in the padding tap: its A block holds 1.0 in channels 0 and 1
+// for every pixel, its weight row k holds bias[k] split into two bf16 parts
+// (hi = RNE(bias), lo = RNE(bias - hi), together exact to 2^-18 relative), so
+// the accumulator comes out of the tensor core as conv + bias and the epilogue
+// -- this kernel's bottleneck -- only applies the activation (SiLU through
+// tanh, one special-function op) and rounds.
+//
+// kTS (BN = 128, bf16 y, no z store): the output leaves through TMA stores.
+// Each epilogue warp owns 32 pixels x 64 channels of a tile -- 32 rows of
+// 128 bytes, contiguous rows of y -- which it stages in shared memory in the
+// 128-byte-swizzled layout of a {64 channels, 32 pixels} box (16-byte chunk c
+// of row r at chunk c ^ (r % 8): the eight rows a store phase covers hit all
+// 32 banks) and hands to one TMA tensor store; two staging buffers per warp let
+// a tile's stores overlap the next tile's epilogue.  The direct path writes the
+// same bytes as per-thread 16-byte stores spread over 32 pixel rows.
+template <int BN, bool kTS = false>
 struct StemCfg {
   static constexpr uint32_t kTapBytes = BM * 16;           // 128 pixels x 8 channels
   static constexpr uint32_t kStageBytes = 10 * kTapBytes;  // 9 taps + zero tap
   static constexpr uint32_t kBTap = BN * 16;
   static constexpr uint32_t kBBytes = 10 * kBTap;
-  static constexpr int kStages = 8;
+  static constexpr int kStages = kTS ? 6 : 8;
+  static constexpr uint32_t kStageOutBytes = 32 * 128;     // one warp's 32 x 64 bf16 box
+  static constexpr uint32_t kOutBytes = kTS ? 2 * kEpiWarps * kStageOutBytes : 0;
   static constexpr int kTmemCols = pow2_cols(2 * BN);
-  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + kBBytes + 512 + 1024;
+  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + kBBytes + kOutBytes + 512 + 1024;
   static_assert(kStages >= kProd, "stage-parallel producers need S >= kProd");
+  static_assert(!kTS || BN == 128, "the TMA-store epilogue covers 128-channel tiles");
+  static_assert(((size_t)kStages * kStageBytes + kBBytes) % 1024 == 0, "staging must be 1 KB aligned");
 };
 
-template <int BN>
+template <int BN, bool kTS = false>
 __global__ void __launch_bounds__(kIgemmThreads, 1)
     k_stem_fwd(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const IgemmParams p) {
-  using Cfg = StemCfg<BN>;
+               const __grid_constant__ CUtensorMap tmY, const IgemmParams p) {
+  using Cfg = StemCfg<BN, kTS>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* wsm = smem + (size_t)S * Cfg::kStageBytes;  // resident weights
-  uint64_t* full = reinterpret_cast<uint64_t*>(wsm + Cfg::kBBytes);
+  uint8_t* osm = wsm + Cfg::kBBytes;                   // output staging (kTS)
+  uint64_t* full = reinterpret_cast<uint64_t*>(osm + Cfg::kOutBytes);
   uint64_t* empty = full + S;
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 2;
@@ -1254,19 +1276,28 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (kTS) tma_prefetch_desc(&tmY);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, Cfg::kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= kEpiBase) {  // zero the tenth (padding) tap of every stage and of the weights
+  if (warp >= kEpiBase) {
+    // the tenth (padding) tap: ones in A channels 0-1 of every stage, the
+    // bias (hi, lo) in the weights' channels 0-1
+    pdl_wait();  // the bias is read below
     const int t = threadIdx.x - 32 * kEpiBase;
     for (int st = 0; st < S; ++st) {
       uint4* z = reinterpret_cast<uint4*>(smem + (size_t)st * Cfg::kStageBytes + 9 * Cfg::kTapBytes);
-      for (int i = t; i < (int)(Cfg::kTapBytes / 16); i += 32 * kEpiWarps) z[i] = make_uint4(0, 0, 0, 0);
+      for (int i = t; i < (int)(Cfg::kTapBytes / 16); i += 32 * kEpiWarps) z[i] = make_uint4(0x3F803F80u, 0, 0, 0);
     }
     uint4* z = reinterpret_cast<uint4*>(wsm + 9 * Cfg::kBTap);
-    for (int i = t; i < (int)(Cfg::kBTap / 16); i += 32 * kEpiWarps) z[i] = make_uint4(0, 0, 0, 0);
+    for (int i = t; i < BN; i += 32 * kEpiWarps) {
+      const float b = (p.bias && i < p.nout) ? __ldg(p.bias + i) : 0.0f;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(b);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(b - __bfloat162float(hi));
+      z[i] = make_uint4((uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(lo) << 16), 0, 0, 0);
+    }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   tc_fence_before();
@@ -1353,10 +1384,78 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       mbar_wait(drain, 0, p.wait_ns, nullptr, nullptr);
     }
     __syncwarp();
+  } else if constexpr (kTS) {
+    // epilogue, TMA-store path: warp (q, half) owns pixels 32q.. of the tile
+    // and channels 64 half..; bias + activation in fp32, one bf16 rounding,
+    // staged swizzled, one TMA store per tile
+    const int q = warp & 3;
+    const int half = (warp - kEpiBase) >> 2;
+    const int col_off = half * 64;
+    const int ew = warp - kEpiBase;
+    int buf = 0, sb = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
+      tc_fence_after();
+      // the store issued from this buffer two tiles ago has read it
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+      uint8_t* stg = osm + (size_t)(ew * 2 + sb) * Cfg::kStageOutBytes + lane * 128;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + col_off);
+      uint32_t v[2][32];
+      tmem_ld_32x32b_x32(taddr, v[0]);
+      tmem_ld_32x32b_x32(taddr + 32u, v[1]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint4 u;
+          __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float f0 = __uint_as_float(v[j][8 * g + 2 * i]);  // conv + bias
+            float f1 = __uint_as_float(v[j][8 * g + 2 * i + 1]);
+            if (p.act == CONV3X3_ACT_SILU) {
+              f0 = silu_tanh_f32(f0);
+              f1 = silu_tanh_f32(f1);
+            } else if (p.act == CONV3X3_ACT_LRELU) {
+              f0 = f0 >= 0.0f ? f0 : 0.2f * f0;
+              f1 = f1 >= 0.0f ? f1 : 0.2f * f1;
+            }
+            h[i] = __floats2bfloat162_rn(f0, f1);
+          }
+          const int chunk = (4 * j + g) ^ (lane & 7);
+          *reinterpret_cast<uint4*>(stg + chunk * 16) = u;
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&tempty[buf]);
+        // one bulk group per tile (empty past the last pixel), so that
+        // "all but the newest group" is always the store two tiles back
+        const int row0 = tile * BM + q * 32;
+        if (row0 < p.P && col_off < p.nout)
+          tma_store_2d(&tmY, osm + (size_t)(ew * 2 + sb) * Cfg::kStageOutBytes, col_off, row0);
+        bulk_commit();
+      }
+      sb ^= 1;
+      if (++buf == 2) {
+        buf = 0;
+        acc_phase ^= 1;
+      }
+    }
+    // every store has completed before the CTA's shared memory goes away
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
   } else {
     // epilogue: as in k_igemm with one 128-pixel sub-tile (the two warps of a
-    // lane quarter take half the columns each)
+    // lane quarter take half the columns each); the bias is in the accumulator
     constexpr int kCols = BN / 2;
+    IgemmParams pe = p;
+    pe.bias = nullptr;
     const int q = warp & 3;
     const int half = (warp - kEpiBase) >> 2;
     const int col_off = half * kCols;
@@ -1373,15 +1472,13 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       for (int j = 0; j < kCols / 32; ++j) {
         const int col0 = col_off + j * 32;
         const bool live = valid && col0 < p.nout;
-        // the bias is loaded ahead of the accumulator, so that the add does not
-        // wait on it (a forward has no z_in)
-        float bv[32];
-        if (p.bias && live) load_bias(p, col0, bv);
+        // the accumulator already holds conv + bias (the padding tap)
+        const float bv[32] = {};
         const uint4 zr[4] = {};
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
         tmem_ld_wait();
-        if (live) store_chunk<true>(p, pix, col0, v, bv, zr);
+        if (live) store_chunk<true, true>(pe, pix, col0, v, bv, zr);
       }
       tc_fence_before();
       __syncwarp();
@@ -2317,15 +2414,30 @@ TileShape pick_tile(int nout, const Shape& sh, int num_sms) {
   return best;
 }
 
-template <int BN>
-int launch_stem(const CUtensorMap& a, const CUtensorMap& b, const IgemmParams& prm, const DevCtx& d,
-                cudaStream_t st) {
-  using Cfg = StemCfg<BN>;
-  auto kern = k_stem_fwd<BN>;
+template <int BN, bool kTS = false>
+int launch_stem(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y,
+                const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
+  using Cfg = StemCfg<BN, kTS>;
+  auto kern = k_stem_fwd<BN, kTS>;
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int grid = prm.num_m_tiles < d.num_sms ? prm.num_m_tiles : d.num_sms;
-  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, b, prm);
+  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, b, y, prm);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
+// [P][C] bf16 output as a 2-D map for TMA stores: box {64 channels, 32 pixels},
+// 128-byte swizzle (the staging layout of the TMA-store epilogues).
+int make_store_map(CUtensorMap* m, void* base, long long P, int C) {
+  PFN_encodeTiled enc = encode_tiled_fn();
+  if (!enc) return CONV3X3_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)P};
+  cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
 // Forward with exactly 8 input channels and at most 256 outputs (one N tile).
@@ -2359,9 +2471,16 @@ int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
   prm.zout = static_cast<__nv_bfloat16*>(ex.zout);
-  if (bn == 64) return launch_stem<64>(ta, tb, prm, d, st);
-  if (bn == 128) return launch_stem<128>(ta, tb, prm, d, st);
-  return launch_stem<256>(ta, tb, prm, d, st);
+  if (bn == 128 && !out_f32 && !ex.zout) {
+    // bf16 output with no z store leaves through TMA stores
+    CUtensorMap ty;
+    rc = make_store_map(&ty, y, s.P(), s.Cout);
+    if (rc) return rc;
+    return launch_stem<128, true>(ta, tb, ty, prm, d, st);
+  }
+  if (bn == 64) return launch_stem<64>(ta, tb, tb, prm, d, st);
+  if (bn == 128) return launch_stem<128>(ta, tb, tb, prm, d, st);
+  return launch_stem<256>(ta, tb, tb, prm, d, st);
 }
 
 // dgrad with 8 output channels (k_stem_dgrad): whole-row tiles of 128 dx

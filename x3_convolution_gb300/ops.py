@@ -184,3 +184,21 @@ def wgrad_strided(x, dy, stride=2, with_bias=True, path=L.PATH_AUTO, out=None, s
         dw, db = out
     L.conv3x3_wgrad_strided(x, dy, dw, db, N, Cin, Cout, H, W, stride, ws, nbytes, path, stream)
     return dw, db
+
+
+def upfirdn2d(x, f, up=1, down=1, pad=(0, 0, 0, 0), out_dtype=L.DT_BF16, out=None, stream=None):
+    """Filtered resampling of x [N,H,W,C] bf16 with the host filter f [kh,kw]:
+    upsample (zeros after each pixel), zero-pad (pad_x0, pad_x1, pad_y0,
+    pad_y1), convolve with f, keep every down-th pixel.  Returns y [N,Ho,Wo,C]."""
+    import numpy as np
+    N, H, W, C = x.shape
+    f = np.asarray(f, dtype=np.float32)
+    kh, kw = f.shape
+    px0, px1, py0, py1 = pad
+    Ho = L.upfirdn2d_out_size(H, up, down, py0, py1, kh)
+    Wo = L.upfirdn2d_out_size(W, up, down, px0, px1, kw)
+    if out is None:
+        dt = torch.float32 if out_dtype == L.DT_F32 else torch.bfloat16
+        out = torch.empty((N, max(Ho, 1), max(Wo, 1), C), dtype=dt, device=x.device)
+    L.upfirdn2d(x, f, out, N, C, H, W, up, down, px0, px1, py0, py1, kh, kw, out_dtype, stream)
+    return out
