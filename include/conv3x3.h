@@ -57,12 +57,18 @@
  * multiple of 256/W) the row-halo kernel.  Unset, the library picks.
  * "128x2" runs transposed (weights as the M = 128 operand, 256 pixels as N) and
  * "128x2n" untransposed; "256x1" runs on two-CTA clusters (one 256-pixel x
- * 256-channel tile per pair, tcgen05 cta_group::2) and "256x1n" on one CTA.
+ * 256-channel tile per pair, tcgen05 cta_group::2) and "256x1n" on one CTA;
+ * "pair128", "pair192", "pair256" run 256-pixel x 128/192/256-channel tiles on
+ * two-CTA clusters.
  * CONV3X3_PAIR=0|1 forces the two-CTA choice for 256-channel tiles (unset: dgrad
  * and forwards of at least 512 input channels, with two rounds of pair tiles).
  * CONV3X3_KC=1|2 forces the 64-channel chunks per pipeline stage of the im2col
  * kernel (2 for 128x1 tiles unless set).  CONV3X3_WGRAD_SPLITS=<S> forces the
  * weight gradient's split count (set it before querying the workspace size).
+ * CONV3X3_WGRAD_ROWS=0|1 chooses how the weight gradient stages x: im2col
+ * boxes per tap (0), or one zero-padded box per image row that all three taps
+ * of a kernel row read (1; stride 1, width 16, 32 or 64).  Unset: the latter
+ * for width 64 only.
  * CONV3X3_PDL=0 launches without programmatic dependent launch (by default a
  * kernel's set-up overlaps the end of the previous kernel in the stream; each
  * kernel still waits for that kernel to complete before touching memory).

@@ -134,8 +134,9 @@ def test_small_shapes_all_passes(shape, path):
 
 # "128x2" runs transposed (channels on TMEM lanes), "128x2n" is the same tile untransposed;
 # "256x1" runs on two-CTA clusters (one 256-pixel x 256-channel tile per pair), "256x1n" on
-# one CTA
-TILES = ["64x1", "128x1", "192x1", "256x1", "256x1n", "64x2", "128x2", "128x2n"]
+# one CTA; "pair<BN>" runs 256-pixel x BN-channel tiles on two-CTA clusters
+TILES = ["64x1", "128x1", "192x1", "256x1", "256x1n", "64x2", "128x2", "128x2n",
+         "pair128", "pair192", "pair256"]
 
 
 @pytest.mark.parametrize("tile", TILES)
@@ -258,7 +259,8 @@ def test_fused_activation_backward(shape, path):
     assert torch.equal(dxn, dxp)
 
 
-@pytest.mark.parametrize("tile", ["64x2", "256x1", "256x1n", "halo64", "128x2", "128x2n"])
+@pytest.mark.parametrize("tile", ["64x2", "256x1", "256x1n", "halo64", "128x2", "128x2n", "pair128",
+                                  "pair192"])
 def test_fused_activation_backward_tiles(tile, monkeypatch):
     monkeypatch.setenv("CONV3X3_TILE", tile)
     shape = (2, 64, 128, 16, 16)
@@ -310,6 +312,34 @@ def test_wgrad_is_bit_deterministic(path):
     b = ops.wgrad(x, dy, path=PATHS[path])
     torch.cuda.synchronize()
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+# The weight gradient's two x layouts: im2col boxes per tap, and (stride 1,
+# width 16, 32 or 64) one zero-padded box of W + 2 columns per image row that
+# all three taps of a kernel row read, shifted by a row each.
+WGRAD_ROW_SHAPES = [
+    (1, 128, 128, 4, 16),   # 16-wide rows, four per k-block
+    (2, 64, 128, 2, 32),    # 32-wide rows, two per k-block
+    (1, 128, 64, 1, 64),    # one 64-wide row: kernel rows 0 and 2 read only padding
+    (2, 256, 256, 4, 16),   # several channel blocks and tiles
+    (1, 72, 200, 8, 16),    # ragged channel box and ragged Cout block
+    (3, 64, 64, 6, 32),     # several splits over several images
+]
+
+
+@pytest.mark.parametrize("rows", ["1", "0"], ids=["row_shifted", "im2col"])
+@pytest.mark.parametrize("shape", WGRAD_ROW_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_wgrad_x_layouts(shape, rows, monkeypatch):
+    monkeypatch.setenv("CONV3X3_WGRAD_ROWS", rows)
+    t = _small(shape, seed=13)
+    x, _, _, dy = dev_tensors(t)
+    dw, db = ops.wgrad(x, dy, path=L.PATH_TENSOR)
+    dw2, db2 = ops.wgrad(x, dy, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    rdw, rdb = oracle.conv3x3_wgrad(t.x, t.dy)
+    assert rel_err(host(dw), rdw) <= TOL_BF16
+    assert rel_err(host(db), rdb) <= TOL_BF16
+    assert torch.equal(dw, dw2) and torch.equal(db, db2)
 
 
 def test_wgrad_without_dbias_and_dirty_workspace():
@@ -513,6 +543,8 @@ CAT_SHAPES = [
     (2, 256, 128, 128, 8, 8),
     (1, 64, 192, 96, 5, 7),
     (2, 24, 40, 64, 6, 6),      # Ca not a whole 64-channel chunk: CUDA-core kernels only
+    (1, 64, 128, 128, 4, 16),   # wgrad with row-shifted x boxes from both parts
+    (2, 128, 64, 64, 2, 32),
 ]
 
 
@@ -575,7 +607,7 @@ def test_concat_free_convs(shape, path):
     assert torch.equal(dw, dw_plain) and torch.equal(db, db_plain)
 
 
-@pytest.mark.parametrize("tile", ["128x2", "128x2n", "256x1", "256x1n"])
+@pytest.mark.parametrize("tile", ["128x2", "128x2n", "256x1", "256x1n", "pair192"])
 @pytest.mark.parametrize("shape", [(1, 128, 72, 200, 6, 11), (2, 128, 128, 128, 16, 16)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_concat_free_256_pixel_tiles(shape, tile, monkeypatch):

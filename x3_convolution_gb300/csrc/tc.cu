@@ -697,18 +697,33 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 // rank 0's multicast commits; tempty[b] of rank 0 collects the epilogue warps
 // of both CTAs.  Every wait is bounded; the two cluster barriers (after setup,
 // before the TMEM release) are reached by every thread on every path.
-constexpr int kPairBN = 256;                           // output channels per pair tile
-constexpr uint32_t kPairBHalf = 128 * BKC * 2;         // 128 weight rows x 64 channels
-constexpr uint32_t kPairStage = kABytes + kPairBHalf;  // per CTA
-constexpr int kPairStages = 6;
-constexpr size_t kPairSmem = (size_t)kPairStages * kPairStage + 256 + 1024 + kGuardBytes;
+//
+// The pair tile is 256 pixels x BN output channels, BN in {128, 192, 256}:
+// each CTA stages BN / 2 weight rows (the forward's K-major box of BN / 2 rows;
+// dgrad's MN-major boxes of 64 channels, the last one partly unused when
+// BN / 2 = 96), the MMA is M = 256, N = BN.
+template <int BN, bool kDgrad>
+struct PairCfg {
+  static constexpr int kHalf = BN / 2;                  // weight rows (output channels) per CTA
+  static constexpr int kDgradBoxes = (kHalf + 63) / 64;  // dgrad: 64-channel MN-major boxes
+  static constexpr uint32_t kBHalf = kDgrad ? (uint32_t)kDgradBoxes * 8192u : (uint32_t)kHalf * 128u;
+  static constexpr uint32_t kStage = kABytes + kBHalf;  // per CTA
+  static constexpr int kStagesFit = (int)((200u * 1024u) / kStage);
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr size_t kSmem = (size_t)kStages * kStage + 256 + 1024 + kGuardBytes;
+  static_assert(BN == 128 || BN == 192 || BN == 256, "pair tiles are 128, 192 or 256 channels wide");
+  static_assert(kStage % 1024 == 0, "stages must keep 1 KB swizzle alignment");
+  static_assert(kStages >= kProd, "stage-parallel producers need S >= kProd");
+};
 
-template <bool kDgrad, bool kExt>
+template <bool kDgrad, bool kExt, int BN = 256>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
     k_igemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                  const __grid_constant__ CUtensorMap tmB, const IgemmParams p) {
-  constexpr int S = kPairStages;
-  static_assert(S >= kProd, "stage-parallel producers need S >= kProd");
+  using Cfg = PairCfg<BN, kDgrad>;
+  constexpr int S = Cfg::kStages;
+  constexpr int kPairBN = BN;
+  constexpr uint32_t kPairStage = Cfg::kStage;
   extern __shared__ uint8_t smem_raw[];
   // same offset in both CTAs: the MMAs address the peer's operands at the
   // offsets of rank 0's
@@ -773,7 +788,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
         const int n0 = p0 / HW, rem = p0 - n0 * HW;
         const int h0 = rem / p.W;
         const int cn = n0, ch = p.ustride * h0 - 1, cw = p.ustride * (rem - h0 * p.W) - 1;
-        const int c0 = nt * kPairBN + (int)rank * 128;  // this CTA's weight rows (output channels)
+        const int c0 = nt * kPairBN + (int)rank * Cfg::kHalf;  // this CTA's weight rows (output channels)
         const int kblocks = 9 * p.kchunks;
         for (int kb = 0; kb < kblocks; ++kb) {
           const int tap = kb / p.kchunks, cc = kb - tap * p.kchunks;
@@ -794,8 +809,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
             if (!kDgrad) {
               tma_load_3d_pair(sb, &tmB, fb, cc * BKC, wtap, c0);
             } else {
-              tma_load_3d_pair(sb, &tmB, fb, c0, wtap, cc * BKC);
-              tma_load_3d_pair(sb + 8192, &tmB, fb, c0 + 64, wtap, cc * BKC);
+#pragma unroll
+              for (int j = 0; j < Cfg::kDgradBoxes; ++j)
+                tma_load_3d_pair(sb + j * 8192, &tmB, fb, c0 + j * 64, wtap, cc * BKC);
             }
           }
           ++issued;
@@ -1782,12 +1798,31 @@ constexpr int kWgPix = 64;                       // pixels per k-block
 constexpr uint32_t kWgABytes = 128 * kWgPix * 2;  // dy: 64 px x 128 Cout
 constexpr uint32_t kWgBBytes = 128 * kWgPix * 2;  // x: 64 px x 128 Cin, per tap
 constexpr uint32_t kWgOnesBytes = 8192;          // 64 px x 64 columns of bf16 ones
-constexpr uint32_t kWgStageBytes = kWgABytes + kWgTaps * kWgBBytes + kWgOnesBytes;
-constexpr int kWgStages = 3;
-static_assert(!kWgStageParallel || kWgStages >= kProd, "stage-parallel producers need S >= kProd");
 constexpr int kWgTmemCols = 512;                 // 3 x 128 dw columns + 16 dbias columns (384..399)
 constexpr int kWgBiasCol = kWgTaps * 128;
-constexpr size_t kWgSmem = (size_t)kWgStages * kWgStageBytes + 256 + 1024 + 8 * 1024;
+static_assert(!kWgStageParallel, "the wgrad stages are shared box-parallel by the producers");
+
+// Stage layout of k_wgrad.  kHW = 0 (im2col x): dy (two 64-pixel x 64-channel
+// boxes), then per tap two 64-pixel x 64-channel im2col boxes of x, then the
+// ones block.  kHW = image width 16, 32 or 64 (row-shifted x): a k-block is
+// R = 64 / kHW whole image rows; per 64-channel half j and image row i one
+// tiled box holds x[h][-1 .. kHW][64 channels] (the columns outside the image
+// read zero), in a slot of kSlot bytes, slots ordered [j][i]; tap s of the
+// kernel row reads that box from row s on, so one box serves all three taps.
+// Slot half j = 2 is all ones (the dbias block, at the same offsets).
+template <int kHW>
+struct WgCfg {
+  static constexpr int R = kHW ? kWgPix / kHW : 0;
+  static constexpr uint32_t kSlot = kHW ? (uint32_t)((kHW + 2) * 128 + 1023) / 1024 * 1024 : 0;
+  static constexpr uint32_t kXBytes = kHW ? 3u * R * kSlot : kWgTaps * kWgBBytes + kWgOnesBytes;
+  static constexpr uint32_t kStageBytes = kWgABytes + kXBytes;
+  static constexpr int kStagesFit = (int)((220u * 1024u) / kStageBytes);
+  static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
+  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 256 + 1024 + 8 * 1024;
+  static_assert(kHW == 0 || kHW == 16 || kHW == 32 || kHW == 64, "row-shifted x for widths 16, 32, 64");
+  static_assert(kStages >= 3, "wgrad stage ring too shallow");
+  static_assert(kStageBytes % 1024 == 0 && kSlot % 1024 == 0, "swizzle atoms must stay 1 KB aligned");
+};
 
 struct WgradParams {
   float* part;  // [S][Cout][9*Cin] then [S][Cout]
@@ -1800,14 +1835,17 @@ struct WgradParams {
   unsigned long long wait_ns;
 };
 
+template <int kHW>
 __global__ void __launch_bounds__(kThreads, 1)
     k_wgrad(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmX,
             const __grid_constant__ CUtensorMap tmX2, const WgradParams p) {
+  using Cfg = WgCfg<kHW>;
+  constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kWgStages * kWgStageBytes);
-  uint64_t* empty = full + kWgStages;
-  uint64_t* tfull = empty + kWgStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * Cfg::kStageBytes);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
   uint64_t* drain = tfull + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -1828,8 +1866,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int HW = p.H * p.W;
 
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < kWgStages; ++i) {
-      mbar_init(&full[i], kWgStageParallel ? 1 : kProd);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], kProd);
       mbar_init(&empty[i], 1);
     }
     mbar_init(tfull, 1);
@@ -1845,10 +1883,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp >= kEpiBase && do_bias) {  // fill every stage's ones block (bf16 1.0 = 0x3F80)
-    for (int st = 0; st < kWgStages; ++st) {
-      uint4* o = reinterpret_cast<uint4*>(smem + (size_t)st * kWgStageBytes + kWgABytes +
-                                          kWgTaps * kWgBBytes);
-      for (int i = threadIdx.x - 32 * kEpiBase; i < (int)(kWgOnesBytes / 16); i += 32 * kWgEpiWarps)
+    constexpr uint32_t kOnesOff = kHW ? kWgABytes + 2u * Cfg::R * Cfg::kSlot : kWgABytes + kWgTaps * kWgBBytes;
+    constexpr uint32_t kOnes = kHW ? Cfg::R * Cfg::kSlot : kWgOnesBytes;
+    for (int st = 0; st < S; ++st) {
+      uint4* o = reinterpret_cast<uint4*>(smem + (size_t)st * Cfg::kStageBytes + kOnesOff);
+      for (int i = threadIdx.x - 32 * kEpiBase; i < (int)(kOnes / 16); i += 32 * kWgEpiWarps)
         o[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1860,54 +1899,61 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();  // the previous kernel's writes are visible from here on
 
   if (warp < kProd) {
-    // Eight 8 KB boxes per stage: two dy boxes (64 pixels x 64 output
-    // channels) then, per tap, two im2col x boxes (64 pixels x 64 channels);
-    // producer `warp` issues boxes warp and warp + 4.
+    // Boxes per stage: two dy boxes (64 pixels x 64 output channels), then x:
+    // im2col, per tap two 64-pixel x 64-channel boxes; row-shifted, per
+    // channel half and image row one (kHW + 2)-pixel box.  Producer `warp`
+    // issues boxes warp, warp + 4, ...
     if (lane == 0) {
+      constexpr int kXBoxes = kHW ? 2 * Cfg::R : 2 * kWgTaps;
+      constexpr uint32_t kXBox = kHW ? (uint32_t)(kHW + 2) * 128u : 8192u;
+      uint32_t bytes = 0;
+      for (int b = warp; b < 2 + kXBoxes; b += kProd) bytes += b < 2 ? 8192u : kXBox;
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
       for (int kb = kb0; kb < kb1; ++kb) {
-        const bool mine = kWgStageParallel ? ((kb - kb0) % kProd == warp) : true;
-        if (mine) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const int pk = kb * kWgPix;
-          const int n0 = pk / HW, rem = pk - n0 * HW;
-          const int h0 = rem / p.W, w0 = rem - (rem / p.W) * p.W;
-          uint8_t* sa = smem + (size_t)stage * kWgStageBytes;
-          uint8_t* sb = sa + kWgABytes;
-          mbar_arrive_expect_tx(&full[stage], kWgStageParallel ? kWgStageBytes : 2 * 8192);
-#pragma unroll
-          for (int b = kWgStageParallel ? 0 : warp; b < 8; b += kWgStageParallel ? 1 : kProd) {
-            if (b < 2) {
-              tma_load_2d(sa + b * 8192, &tmDY, &full[stage], mb * 128 + b * 64, pk);
-            } else {
-              const int t = (b - 2) >> 1, j = (b - 2) & 1;
-              const int c = cb * 128 + j * 64;  // a 64-channel box lies in one part
-              const bool second = c >= p.ca;
-              tma_load_im2col_4d(sb + (t * 2 + j) * 8192, second ? &tmX2 : &tmX, &full[stage],
-                                 second ? c - p.ca : c, p.ustride * w0 - 1, p.ustride * h0 - 1, n0,
-                                 (uint16_t)t, (uint16_t)tr);
-            }
+        if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int pk = kb * kWgPix;
+        const int n0 = pk / HW, rem = pk - n0 * HW;
+        const int h0 = rem / p.W, w0 = rem - h0 * p.W;
+        uint8_t* sa = smem + (size_t)stage * Cfg::kStageBytes;
+        uint8_t* sb = sa + kWgABytes;
+        mbar_arrive_expect_tx(&full[stage], bytes);
+        for (int b = warp; b < 2 + kXBoxes; b += kProd) {
+          if (b < 2) {
+            tma_load_2d(sa + b * 8192, &tmDY, &full[stage], mb * 128 + b * 64, pk);
+          } else if constexpr (kHW != 0) {
+            const int j = (b - 2) / Cfg::R, i = (b - 2) - j * Cfg::R;
+            const int c = cb * 128 + j * 64;  // a 64-channel box lies in one part
+            const bool second = c >= p.ca;
+            tma_load_4d(sb + (size_t)(j * Cfg::R + i) * Cfg::kSlot, second ? &tmX2 : &tmX, &full[stage],
+                        second ? c - p.ca : c, -1, h0 + i + tr - 1, n0);
+          } else {
+            const int t = (b - 2) >> 1, j = (b - 2) & 1;
+            const int c = cb * 128 + j * 64;
+            const bool second = c >= p.ca;
+            tma_load_im2col_4d(sb + (t * 2 + j) * 8192, second ? &tmX2 : &tmX, &full[stage],
+                               second ? c - p.ca : c, p.ustride * w0 - 1, p.ustride * h0 - 1, n0,
+                               (uint16_t)t, (uint16_t)tr);
           }
         }
         ++issued;
-        if (++stage == kWgStages) {
+        if (++stage == S) {
           stage = 0;
           phase ^= 1;
         }
       }
       if (!ok) {
-        int n = issued < kWgStages ? issued : kWgStages;
+        int n = issued < S ? issued : S;
         int st = stage;
         uint32_t ph = phase;
         for (int i = 0; i < n; ++i) {
           if (--st < 0) {
-            st = kWgStages - 1;
+            st = S - 1;
             ph ^= 1;
           }
           mbar_wait(&full[st], ph, drain_wait_ns(p.wait_ns), nullptr, nullptr);
@@ -1924,10 +1970,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // descriptors built once; stages and K steps move the start address only
       const uint32_t sbase = smem_u32(smem);
       const uint64_t a_desc0 = smem_desc(sbase, 8192, 1024, kSwizzle128B);
-      const uint64_t b_desc0 = smem_desc(sbase + kWgABytes, 8192, 1024, kSwizzle128B);
-      constexpr uint32_t kStageStep = kWgStageBytes >> 4;
+      constexpr uint32_t kStageStep = Cfg::kStageBytes >> 4;
       constexpr uint32_t kKStep = 2048u >> 4;
-      constexpr uint32_t kTap2 = (2 * kWgBBytes) >> 4;
       int stage = 0;
       uint32_t phase = 0, stage_off = 0;
       bool ok = true;
@@ -1937,21 +1981,46 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint64_t ad = a_desc0 + stage_off, bd = b_desc0 + stage_off;
+        const uint64_t ad = a_desc0 + stage_off;
         const uint32_t acc0 = kb != kb0 ? 1u : 0u;
+        if constexpr (kHW) {
+          // K step k covers pixels 16k .. 16k + 15 of the k-block: image row
+          // i = 16k / kHW, columns w0 .. w0 + 15 with w0 = 16k mod kHW; tap s
+          // reads rows w0 + s .. of slot (j, i) (the box starts at column -1),
+          // the two channel halves Cfg::R slots apart.  The swizzle follows the
+          // absolute shared-memory address, so a start that is s rows into a
+          // 1 KB swizzle atom needs no base offset.
+          const uint32_t xbase = sbase + (uint32_t)stage * Cfg::kStageBytes + kWgABytes;
 #pragma unroll
-        for (int k = 0; k < kWgPix / 16; ++k) {
-          const uint32_t acc = k == 0 ? acc0 : 1u;
-          // taps 0 and 1: four 64-channel blocks at 8 KB stride -> one N = 256 MMA
-          tc_mma_bf16(tmem_base, ad + (uint64_t)(k * kKStep), bd + (uint64_t)(k * kKStep), idesc256,
-                      acc);
-          // tap 2 (+ the ones block as a third 64-column block when this CTA owns dbias)
-          tc_mma_bf16(tmem_base + 256, ad + (uint64_t)(k * kKStep),
-                      bd + (uint64_t)(kTap2 + k * kKStep), idesc_t2, acc);
+          for (int k = 0; k < kWgPix / 16; ++k) {
+            const uint32_t acc = k == 0 ? acc0 : 1u;
+            constexpr int kW = kHW ? kHW : 16;  // (kHW = 0 never reaches here)
+            const int i = (16 * k) / kW, w0 = (16 * k) % kW;
+            const uint32_t row0 = xbase + (uint32_t)i * Cfg::kSlot + (uint32_t)w0 * 128u;
+#pragma unroll
+            for (int t = 0; t < kWgTaps; ++t)
+              tc_mma_bf16(tmem_base + (uint32_t)(t * 128), ad + (uint64_t)(k * kKStep),
+                          smem_desc(row0 + (uint32_t)t * 128u, Cfg::R * Cfg::kSlot, 1024, kSwizzle128B),
+                          t == 2 ? idesc_t2 : idesc128, acc);
+          }
+        } else {
+          const uint64_t b_desc0 = smem_desc(sbase + kWgABytes, 8192, 1024, kSwizzle128B);
+          const uint64_t bd = b_desc0 + stage_off;
+          constexpr uint32_t kTap2 = (2 * kWgBBytes) >> 4;
+#pragma unroll
+          for (int k = 0; k < kWgPix / 16; ++k) {
+            const uint32_t acc = k == 0 ? acc0 : 1u;
+            // taps 0 and 1: four 64-channel blocks at 8 KB stride -> one N = 256 MMA
+            tc_mma_bf16(tmem_base, ad + (uint64_t)(k * kKStep), bd + (uint64_t)(k * kKStep), idesc256,
+                        acc);
+            // tap 2 (+ the ones block as a third 64-column block when this CTA owns dbias)
+            tc_mma_bf16(tmem_base + 256, ad + (uint64_t)(k * kKStep),
+                        bd + (uint64_t)(kTap2 + k * kKStep), idesc_t2, acc);
+          }
         }
         tc_commit(&empty[stage]);
         stage_off += kStageStep;
-        if (++stage == kWgStages) {
+        if (++stage == S) {
           stage = 0;
           stage_off = 0;
           phase ^= 1;
@@ -2220,15 +2289,17 @@ int make_im2col_map(CUtensorMap* m, const void* base, int N, int H, int W, int C
   return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
-// NHWC activations as a tiled 4-D map; box {64 channels, W, rows, 1 image}.
+// NHWC activations as a tiled 4-D map; box {64 channels, box_w (default W)
+// columns, rows, 1 image}.
 // Boxes may start at w = -1 or h = -1 and run past the far edge: those
 // elements read as zero (the convolution's padding).
-int make_halo_map(CUtensorMap* m, const void* base, int N, int H, int W, int C, int rows) {
+int make_halo_map(CUtensorMap* m, const void* base, int N, int H, int W, int C, int rows,
+                  int box_w = 0) {
   PFN_encodeTiled enc = encode_tiled_fn();
   if (!enc) return CONV3X3_ERR_CUDA;
   cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)N};
   cuuint64_t strides[3] = {(cuuint64_t)C * 2, (cuuint64_t)W * C * 2, (cuuint64_t)H * W * C * 2};
-  cuuint32_t box[4] = {(cuuint32_t)BKC, (cuuint32_t)W, (cuuint32_t)rows, 1};
+  cuuint32_t box[4] = {(cuuint32_t)BKC, (cuuint32_t)(box_w ? box_w : W), (cuuint32_t)rows, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -2310,20 +2381,21 @@ int launch_igemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap&
 // Resident two-CTA clusters of k_igemm_pair (a GPC with an odd number of free
 // SMs leaves one idle), cached per kernel and device.
 template <typename K>
-int pair_slots(K kernel, const DevCtx& d) {
+int pair_slots(K kernel, size_t smem, const DevCtx& d) {
+  constexpr int kKeys = 16;
   static std::mutex mu;
-  static int cache[4][64] = {};
-  static const void* keys[4] = {nullptr, nullptr, nullptr, nullptr};
+  static int cache[kKeys][64] = {};
+  static const void* keys[kKeys] = {};
   std::lock_guard<std::mutex> g(mu);
   int slot = 0;
-  while (slot < 4 && keys[slot] != nullptr && keys[slot] != (const void*)kernel) ++slot;
-  const bool cacheable = slot < 4 && d.device >= 0 && d.device < 64;
+  while (slot < kKeys && keys[slot] != nullptr && keys[slot] != (const void*)kernel) ++slot;
+  const bool cacheable = slot < kKeys && d.device >= 0 && d.device < 64;
   if (cacheable && keys[slot] == (const void*)kernel && cache[slot][d.device] > 0)
     return cache[slot][d.device];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (d.num_sms / 2), 1, 1);
   cfg.blockDim = dim3(kIgemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.dynamicSmemBytes = smem;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
     (void)cudaGetLastError();
@@ -2336,16 +2408,17 @@ int pair_slots(K kernel, const DevCtx& d) {
   return n;
 }
 
-template <bool kDgrad>
+template <bool kDgrad, int BN>
 int launch_igemm_pair(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
                       const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
+  using Cfg = PairCfg<BN, kDgrad>;
   const bool ext = prm.zout || prm.zin || prm.out2;
-  auto kern = ext ? k_igemm_pair<kDgrad, true> : k_igemm_pair<kDgrad, false>;
-  if (set_smem(kern, kPairSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+  auto kern = ext ? k_igemm_pair<kDgrad, true, BN> : k_igemm_pair<kDgrad, false, BN>;
+  if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
-  const int pairs = pair_slots(kern, d);
+  const int pairs = pair_slots(kern, Cfg::kSmem, d);
   const int grid = 2 * (tiles < pairs ? tiles : pairs);
-  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), kPairSmem, st, a, a2, b, prm);
+  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, a2, b, prm);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
@@ -2552,13 +2625,15 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   // tiles (a 256-pixel pair tile halves the tile count, so small grids lose).
   // CONV3X3_PAIR=0|1 or the override "256x1" / "256x1n" forces the choice.
   bool trans = true;
-  int pair_force = -1;
+  int pair_force = -1, pair_bn = 0;
   if (const char* e = std::getenv("CONV3X3_PAIR")) pair_force = std::strcmp(e, "0") != 0 ? 1 : 0;
-  // CONV3X3_TILE="<BN>x<MT>" or "halo<BN>" overrides the choice (tuning and tests)
+  // CONV3X3_TILE="<BN>x<MT>", "halo<BN>" or "pair<BN>" overrides the choice (tuning and tests)
   if (const char* e = std::getenv("CONV3X3_TILE")) {
     trans = std::strcmp(e, "128x2n") != 0;
     if (std::strcmp(e, "256x1n") == 0) pair_force = 0;
     if (std::strcmp(e, "256x1") == 0) pair_force = 1;
+    int pb = 0;
+    if (std::sscanf(e, "pair%d", &pb) == 1 && (pb == 128 || pb == 192 || pb == 256)) pair_bn = pb;
     int bn_o = 0, mt_o = 0;
     const bool halo_ok = (s.W == 16 || s.W == 32 || s.W == 64) && s.H % (256 / s.W) == 0;
     if (std::sscanf(e, "halo%d", &bn_o) == 1 && halo_ok && (bn_o == 64 || bn_o == 128))
@@ -2632,16 +2707,23 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   const long long pair_tiles = (g.P() + 2 * BM - 1) / (2 * BM) * prm.num_n_tiles;
   const bool pair = pair_force >= 0 ? pair_force == 1
                                     : ((dgrad || prm.kchunks >= 8) && pair_tiles >= d.num_sms);
-  if (pair && bn == 256 && ts.mt == 1 && !s2) {
-    // a pair tile is 256 pixels (128 per CTA) x 256 channels, each CTA
-    // loading 128 weight rows
+  if (pair_bn == 0 && pair && bn == 256 && ts.mt == 1) pair_bn = 256;
+  if (pair_bn && !s2) {
+    // a pair tile is 256 pixels (128 per CTA) x pair_bn channels, each CTA
+    // loading pair_bn / 2 weight rows
     prm.num_m_tiles = (int)((g.P() + 2 * BM - 1) / (2 * BM));
-    if (!dgrad) {
-      rc = make_weight_map(&tb, w, s.Cin, s.Cout, 128);
+    prm.num_n_tiles = (nout + pair_bn - 1) / pair_bn;
+    if (!dgrad) {  // (dgrad's map already has 64-row boxes)
+      rc = make_weight_map(&tb, w, s.Cin, s.Cout, pair_bn / 2);
       if (rc) return rc;
     }
-    return dgrad ? launch_igemm_pair<true>(ta, ta2, tb, prm, d, st)
-                 : launch_igemm_pair<false>(ta, ta2, tb, prm, d, st);
+#define C3_PAIR(BN_)                                                                   \
+  return dgrad ? launch_igemm_pair<true, BN_>(ta, ta2, tb, prm, d, st)                 \
+               : launch_igemm_pair<false, BN_>(ta, ta2, tb, prm, d, st)
+    if (pair_bn == 128) C3_PAIR(128);
+    if (pair_bn == 192) C3_PAIR(192);
+    C3_PAIR(256);
+#undef C3_PAIR
   }
   // Two 64-channel chunks per k-block where the tile's MMAs are short (see
   // IgemmCfg); CONV3X3_KC=1|2 overrides the choice (tuning).
@@ -2770,6 +2852,22 @@ WgPlan wg_plan_c8(const Shape& s) {
   return pl;
 }
 
+// Image width for the row-shifted x layout of k_wgrad, or 0 for im2col: stride
+// 1, a width of 16, 32 or 64 and images of a whole number of 64-pixel
+// k-blocks (every k-block is whole image rows of one image).  By default only
+// width 64 takes it: measured on GB300 (CUDA events, batch 64) it ran the
+// 128-channel 64x64 layer in 68 instead of 72 us, while at widths 32 and 16 --
+// two and four image rows per k-block, three MMAs per K step where im2col
+// needs two -- it ran 3-12 % slower.  CONV3X3_WGRAD_ROWS=0 forces im2col,
+// =1 the row-shifted layout wherever it applies (tuning and tests).
+int wg_row_width(const Shape& s) {
+  int mode = -1;
+  if (const char* e = std::getenv("CONV3X3_WGRAD_ROWS")) mode = std::strcmp(e, "0") == 0 ? 0 : 1;
+  if (mode == 0 || s.u != 1 || !(s.W == 16 || s.W == 32 || s.W == 64)) return 0;
+  if (mode < 0 && s.W != 64) return 0;
+  return ((long long)s.H * s.W) % kWgPix == 0 ? s.W : 0;
+}
+
 // The split plan runs over dy's pixel grid.
 Shape wg_grid(const Shape& s) {
   Shape g = s;
@@ -2853,8 +2951,34 @@ int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s
   prm.num_cb = pl.num_cb;
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
-  if (set_smem(k_wgrad, kWgSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
-  launch_pdl(k_wgrad, dim3(pl.tiles * pl.S), dim3(kThreads), kWgSmem, st, tdy, tx, tx2, prm);
+  const int hw = wg_row_width(s);
+  if (hw) {
+    // row-shifted x: per image row one box of (W + 2) pixels x 64 channels
+    rc = make_halo_map(&tx, x, s.N, s.H, s.W, cat.on() ? cat.Ca : s.Cin, 1, s.W + 2);
+    if (rc) return rc;
+    if (cat.on()) {
+      rc = make_halo_map(&tx2, cat.b, s.N, s.H, s.W, s.Cin - cat.Ca, 1, s.W + 2);
+      if (rc) return rc;
+    } else {
+      tx2 = tx;
+    }
+  }
+#define C3_WG(HW_)                                                                               \
+  do {                                                                                           \
+    using Cfg = WgCfg<HW_>;                                                                      \
+    if (set_smem(k_wgrad<HW_>, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;     \
+    launch_pdl(k_wgrad<HW_>, dim3(pl.tiles * pl.S), dim3(kThreads), Cfg::kSmem, st, tdy, tx, tx2, \
+               prm);                                                                             \
+  } while (0)
+  if (hw == 64)
+    C3_WG(64);
+  else if (hw == 32)
+    C3_WG(32);
+  else if (hw == 16)
+    C3_WG(16);
+  else
+    C3_WG(0);
+#undef C3_WG
   if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
   return launch_wgrad_reduce(prm.part, dw, db, (long long)s.Cout * 9 * s.Cin, s.Cout, pl.S, pl.S, st);
 }
