@@ -189,11 +189,19 @@ STEM_SHAPES = [
     (5, 8, 128, 16, 16),  # several 128-pixel tiles per CTA
     (2, 8, 72, 9, 11),    # 128-channel tile, second 64-channel store box clipped to 8 channels
     (1, 8, 104, 13, 10),  # clipped store box and a ragged pixel tail
+    # widths 64 and 32 with whole-row tiles: the forward stages x as image rows
+    (2, 8, 128, 4, 64),
+    (1, 8, 72, 8, 32),
+    (2, 8, 256, 2, 64),   # 256-channel tile
+    (3, 8, 40, 4, 32),    # 64-channel tile
 ]
 
 
+@pytest.mark.parametrize("rows", ["auto", "0"], ids=["rows_auto", "im2col"])
 @pytest.mark.parametrize("shape", STEM_SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_eight_channel_kernels(shape):
+def test_eight_channel_kernels(shape, rows, monkeypatch):
+    if rows == "0":
+        monkeypatch.setenv("CONV3X3_STEM_ROWS", "0")
     t = _small(shape)
     x, w, b, dy = dev_tensors(t)
     dw, db = ops.wgrad(x, dy, path=L.PATH_TENSOR)
@@ -340,6 +348,23 @@ def test_wgrad_x_layouts(shape, rows, monkeypatch):
     assert rel_err(host(dw), rdw) <= TOL_BF16
     assert rel_err(host(db), rdb) <= TOL_BF16
     assert torch.equal(dw, dw2) and torch.equal(db, db2)
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_wgrad_dbias_only_four_byte_aligned(path):
+    # dbias may sit 4 bytes past a 16-byte boundary (the ABI asks for 4)
+    t = _small((2, 64, 136, 8, 8), seed=17)
+    x, _, _, dy = dev_tensors(t)
+    dw = torch.empty((136, 3, 3, 64), dtype=torch.float32, device="cuda")
+    buf = torch.full((137 + 3,), float("nan"), dtype=torch.float32, device="cuda")
+    db = buf[1:137]
+    assert db.data_ptr() % 16 == 4
+    ops.wgrad(x, dy, path=PATHS[path], out=(dw, db))
+    torch.cuda.synchronize()
+    rdw, rdb = oracle.conv3x3_wgrad(t.x, t.dy)
+    assert rel_err(host(dw), rdw) <= TOL_BF16
+    assert rel_err(host(db), rdb) <= TOL_BF16
+    assert torch.isnan(buf[0]) and torch.all(torch.isnan(buf[137:]))  # nothing written outside
 
 
 def test_wgrad_without_dbias_and_dirty_workspace():

@@ -461,7 +461,8 @@ __global__ void __launch_bounds__(kThreads) k_wgrad_bf16_c8_partial(
 
 // dw[e] = sum_{s=0}^{S-1} part[s][e] in increasing s (four partials loaded at a
 // time, added strictly in order), four elements per thread; dbias likewise
-// over its Sdb partial rows stored after the S dw slices.
+// over its Sdb partial rows stored after the S dw slices.  For layers whose
+// split count is small (a few partials of a large dw).
 __global__ void k_wgrad_reduce(const float* __restrict__ part, float* __restrict__ dw,
                                float* __restrict__ db, long long dwsize, int Cout, int S, int Sdb) {
   pdl_trigger();
@@ -494,6 +495,65 @@ __global__ void k_wgrad_reduce(const float* __restrict__ part, float* __restrict
       float acc = 0.0f;
       for (int s = 0; s < Sdb; ++s) acc += part[(long long)S * dwsize + (long long)s * Cout + k];
       db[k] = acc;
+    }
+  }
+}
+
+// The same sum for wide splits (a layer with few output tiles has up to
+// hundreds of splits of a small dw), in another fixed order: split group
+// g = 0..7 (in order) of the sums over s = g, g + 8, g + 16, ... (each in
+// increasing s).  A block covers 32 float4 columns with 8 warps, one per split
+// group, so the splits are read by eight warps at once instead of one thread
+// per column walking all of them; the result depends only on S, never on
+// timing, and is bit-identical run to run.  dbias rides along as Cout / 4 more
+// float4 columns over its Sdb partial rows stored after the S dw slices.
+constexpr int kRedGroups = 8;
+
+__global__ void __launch_bounds__(32 * kRedGroups)
+    k_wgrad_reduce_wide(const float* __restrict__ part, float* __restrict__ dw, float* __restrict__ db,
+                        long long dwsize, int Cout, int S, int Sdb) {
+  __shared__ float4 red[kRedGroups][32];
+  pdl_trigger();
+  pdl_wait();  // the partials of the kernel before
+  const int x = threadIdx.x, g = threadIdx.y;
+  const long long n4 = dwsize / 4;
+  const long long col = blockIdx.x * 32LL + x;
+  const bool bias_col = col >= n4;
+  const long long total = n4 + (db ? Cout / 4 : 0);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (col < total) {
+    const float4* src = reinterpret_cast<const float4*>(bias_col ? part + (long long)S * dwsize : part);
+    const long long c = bias_col ? col - n4 : col;
+    const long long stride = bias_col ? Cout / 4 : n4;
+    const int n = bias_col ? Sdb : S;
+    for (int sp = g; sp < n; sp += kRedGroups) {
+      const float4 a = __ldg(src + (long long)sp * stride + c);
+      acc.x += a.x;
+      acc.y += a.y;
+      acc.z += a.z;
+      acc.w += a.w;
+    }
+  }
+  red[g][x] = acc;
+  __syncthreads();
+  if (g == 0 && col < total) {
+    float4 t = red[0][x];
+#pragma unroll
+    for (int i = 1; i < kRedGroups; ++i) {
+      const float4 a = red[i][x];
+      t.x += a.x;
+      t.y += a.y;
+      t.z += a.z;
+      t.w += a.w;
+    }
+    if (bias_col) {  // dbias need only be 4-byte aligned: scalar stores
+      float* o = db + (col - n4) * 4;
+      o[0] = t.x;
+      o[1] = t.y;
+      o[2] = t.z;
+      o[3] = t.w;
+    } else {
+      reinterpret_cast<float4*>(dw)[col] = t;
     }
   }
 }
@@ -538,10 +598,21 @@ WgradPlan wgrad_plan(const Shape& s) {
 
 }  // namespace
 
+// Partial sums of S splits -> dw, dbias.  Which fixed summation order is used
+// depends only on S: per column in split order below kWideSplits splits,
+// eight split groups per column from there on.
+constexpr int kWideSplits = 16;
+
 int launch_wgrad_reduce(const float* part, float* dw, float* db, long long dwsize, int Cout, int S,
                         int Sdb, cudaStream_t st) {
-  launch_pdl(k_wgrad_reduce, dim3(grid_for(dwsize / 4 + Cout)), dim3(kThreads), 0, st, part, dw, db,
-             dwsize, Cout, S, Sdb);
+  if (S >= kWideSplits) {
+    const long long cols = dwsize / 4 + (db ? Cout / 4 : 0);
+    launch_pdl(k_wgrad_reduce_wide, dim3((unsigned)((cols + 31) / 32)), dim3(32, kRedGroups), 0, st,
+               part, dw, db, dwsize, Cout, S, Sdb);
+  } else {
+    launch_pdl(k_wgrad_reduce, dim3(grid_for(dwsize / 4 + Cout)), dim3(kThreads), 0, st, part, dw, db,
+               dwsize, Cout, S, Sdb);
+  }
   return launch_status();
 }
 
@@ -635,8 +706,7 @@ int simt_wgrad_bf16(const void* x, const void* dy, float* dw, float* db, const S
   }
   if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
   long long dwsize = (long long)s.Cout * 9 * s.Cin;
-  k_wgrad_reduce<<<grid_for(dwsize / 4 + s.Cout), kThreads, 0, st>>>(part, dw, db, dwsize, s.Cout, pl.S, pl.S);
-  return launch_status();
+  return launch_wgrad_reduce(part, dw, db, dwsize, s.Cout, pl.S, pl.S, st);
 }
 
 }  // namespace c3

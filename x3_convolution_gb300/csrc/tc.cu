@@ -1237,13 +1237,31 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 // 32 banks) and hands to one TMA tensor store; two staging buffers per warp let
 // a tile's stores overlap the next tile's epilogue.  The direct path writes the
 // same bytes as per-thread 16-byte stores spread over 32 pixel rows.
-template <int BN, bool kTS = false>
+//
+// kRW (image width 32 or 64, whole-row tiles): x staged in long rows instead
+// of im2col boxes.  An im2col box of 8 channels moves 128 rows of 16 bytes, and
+// the copy engine's row rate -- not bytes -- set this kernel's pace.  Viewing x
+// as [N][H][W * 8], an image row is one run of W * 16 bytes; for each column
+// shift s the stage holds a slot of the tile's R = 128 / W image rows plus the
+// row above and below, shifted by s - 1 pixels (the columns and rows outside
+// the image read zero), in 512-byte boxes.  Tap (r, s) -- K slot q = 3 s + r --
+// is then the 128 pixels that start r rows into slot s: 24 (W = 64) or 18
+// (W = 32) copy rows per tile instead of 1152.  The weights sit in the same
+// slot order.
+template <int BN, bool kTS = false, int kRW = 0>
 struct StemCfg {
   static constexpr uint32_t kTapBytes = BM * 16;           // 128 pixels x 8 channels
-  static constexpr uint32_t kStageBytes = 10 * kTapBytes;  // 9 taps + zero tap
+  static constexpr int kRowsPerTile = kRW ? BM / kRW : 0;  // image rows of a tile (kRW)
+  static constexpr uint32_t kRowBytes = (uint32_t)kRW * 16;  // one image row of x (kRW)
+  static constexpr uint32_t kSlotBytes = (uint32_t)(kRowsPerTile + 2) * kRowBytes;
+  static constexpr int kBoxElems = kRW * 8 < 256 ? kRW * 8 : 256;  // elements per row box
+  static constexpr int kRowParts = kRW ? kRW * 8 / kBoxElems : 0;  // boxes per image row
+  // A offset of the tenth (padding) K slot: after the 9 taps, or the 3 slots
+  static constexpr uint32_t kPadOff = kRW ? 3 * kSlotBytes : 9 * kTapBytes;
+  static constexpr uint32_t kStageBytes = kPadOff + kTapBytes;  // + padding tap
   static constexpr uint32_t kBTap = BN * 16;
   static constexpr uint32_t kBBytes = 10 * kBTap;
-  static constexpr int kStages = kTS ? 6 : 8;
+  static constexpr int kStages = kTS ? (kRW ? 8 : 6) : 8;
   static constexpr uint32_t kStageOutBytes = 32 * 128;     // one warp's 32 x 64 bf16 box
   static constexpr uint32_t kOutBytes = kTS ? 2 * kEpiWarps * kStageOutBytes : 0;
   static constexpr int kTmemCols = pow2_cols(2 * BN);
@@ -1251,13 +1269,25 @@ struct StemCfg {
   static_assert(kStages >= kProd, "stage-parallel producers need S >= kProd");
   static_assert(!kTS || BN == 128, "the TMA-store epilogue covers 128-channel tiles");
   static_assert(((size_t)kStages * kStageBytes + kBBytes) % 1024 == 0, "staging must be 1 KB aligned");
+  static_assert(kRW == 0 || kRW == 32 || kRW == 64, "row staging for widths 32 and 64");
 };
 
-template <int BN, bool kTS = false>
+// Byte offset in the A stage of K slot q (0..8: taps in the stage's order,
+// 9: the padding tap).  im2col: slot q holds tap q; row staging: slot q holds
+// tap (q % 3) * 3 + q / 3 (r = q % 3 rows into the slot of shift s = q / 3).
+template <int BN, bool kTS, int kRW>
+__host__ __device__ constexpr uint32_t stem_a_off(int q) {
+  using Cfg = StemCfg<BN, kTS, kRW>;
+  return q == 9 ? Cfg::kPadOff
+                : kRW ? (uint32_t)(q / 3) * Cfg::kSlotBytes + (uint32_t)(q % 3) * Cfg::kRowBytes
+                      : (uint32_t)q * Cfg::kTapBytes;
+}
+
+template <int BN, bool kTS = false, int kRW = 0>
 __global__ void __launch_bounds__(kIgemmThreads, 1)
     k_stem_fwd(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmY, const IgemmParams p) {
-  using Cfg = StemCfg<BN, kTS>;
+  using Cfg = StemCfg<BN, kTS, kRW>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -1304,7 +1334,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     pdl_wait();  // the bias is read below
     const int t = threadIdx.x - 32 * kEpiBase;
     for (int st = 0; st < S; ++st) {
-      uint4* z = reinterpret_cast<uint4*>(smem + (size_t)st * Cfg::kStageBytes + 9 * Cfg::kTapBytes);
+      uint4* z = reinterpret_cast<uint4*>(smem + (size_t)st * Cfg::kStageBytes + Cfg::kPadOff);
       for (int i = t; i < (int)(Cfg::kTapBytes / 16); i += 32 * kEpiWarps) z[i] = make_uint4(0x3F803F80u, 0, 0, 0);
     }
     uint4* z = reinterpret_cast<uint4*>(wsm + 9 * Cfg::kBTap);
@@ -1324,9 +1354,10 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 
   if (warp < kProd) {
     if (lane == 0) {
-      if (warp == 0) {  // resident weights: nine boxes of BN rows x 8 channels
+      if (warp == 0) {  // resident weights: nine boxes of BN rows x 8 channels, in K slot order
         mbar_arrive_expect_tx(wfull, 9 * Cfg::kBTap);
-        for (int t = 0; t < 9; ++t) tma_load_3d(wsm + t * Cfg::kBTap, &tmB, wfull, 0, t, 0);
+        for (int q = 0; q < 9; ++q)
+          tma_load_3d(wsm + q * Cfg::kBTap, &tmB, wfull, 0, kRW ? (q % 3) * 3 + q / 3 : q, 0);
       }
       // stage-parallel: this producer owns every kProd-th tile (one stage per tile)
       int stage = 0, issued = 0;
@@ -1342,10 +1373,21 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
           const int n0 = p0 / HW, rem = p0 - n0 * HW;
           const int h0 = rem / p.W, w0 = rem - h0 * p.W;
           uint8_t* sa = smem + (size_t)stage * Cfg::kStageBytes;
-          mbar_arrive_expect_tx(&full[stage], 9 * Cfg::kTapBytes);
-          for (int t = 0; t < 9; ++t)
-            tma_load_im2col_4d(sa + t * Cfg::kTapBytes, &tmA, &full[stage], 0, w0 - 1, h0 - 1, n0,
-                               (uint16_t)(t % 3), (uint16_t)(t / 3));
+          if constexpr (kRW != 0) {
+            // slot s: image rows h0 - 1 .. h0 + R, columns s - 1 .. s - 2 + W
+            mbar_arrive_expect_tx(&full[stage], 3 * Cfg::kSlotBytes);
+            for (int sh = 0; sh < 3; ++sh)
+              for (int rho = 0; rho < Cfg::kRowsPerTile + 2; ++rho)
+#pragma unroll
+                for (int part = 0; part < Cfg::kRowParts; ++part)
+                  tma_load_3d(sa + sh * Cfg::kSlotBytes + rho * Cfg::kRowBytes + part * 2 * Cfg::kBoxElems,
+                              &tmA, &full[stage], (sh - 1) * 8 + part * Cfg::kBoxElems, h0 - 1 + rho, n0);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], 9 * Cfg::kTapBytes);
+            for (int t = 0; t < 9; ++t)
+              tma_load_im2col_4d(sa + t * Cfg::kTapBytes, &tmA, &full[stage], 0, w0 - 1, h0 - 1, n0,
+                                 (uint16_t)(t % 3), (uint16_t)(t / 3));
+          }
         }
         ++issued;
         if (++stage == S) {
@@ -1381,10 +1423,17 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
         const uint32_t a_base = smem_u32(smem + (size_t)stage * Cfg::kStageBytes);
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
 #pragma unroll
-        for (int j = 0; j < 5; ++j)
-          tc_mma_bf16(d_tmem, smem_desc(a_base + 2 * j * Cfg::kTapBytes, Cfg::kTapBytes, 128, kSwizzleNone),
+        for (int j = 0; j < 5; ++j) {
+          // K slots 2j, 2j + 1: the second's distance from the first is the LBO
+          constexpr uint32_t kOff[10] = {stem_a_off<BN, kTS, kRW>(0), stem_a_off<BN, kTS, kRW>(1),
+                                         stem_a_off<BN, kTS, kRW>(2), stem_a_off<BN, kTS, kRW>(3),
+                                         stem_a_off<BN, kTS, kRW>(4), stem_a_off<BN, kTS, kRW>(5),
+                                         stem_a_off<BN, kTS, kRW>(6), stem_a_off<BN, kTS, kRW>(7),
+                                         stem_a_off<BN, kTS, kRW>(8), stem_a_off<BN, kTS, kRW>(9)};
+          tc_mma_bf16(d_tmem, smem_desc(a_base + kOff[2 * j], kOff[2 * j + 1] - kOff[2 * j], 128, kSwizzleNone),
                       smem_desc(b_base + 2 * j * Cfg::kBTap, Cfg::kBTap, 128, kSwizzleNone), idesc,
                       j ? 1u : 0u);
+        }
         tc_commit(&empty[stage]);
         tc_commit(&tfull[buf]);
         if (++stage == S) {
@@ -2094,9 +2143,18 @@ constexpr uint32_t kWc8StageBytes = kWgABytes + kWc8BBytes;
 constexpr int kWc8Stages = 6;
 constexpr size_t kWc8Smem = (size_t)kWc8Stages * kWc8StageBytes + 256 + 1024;
 
+//
+// kRW = 64 (image width 64: a k-block is one image row): x staged in long rows,
+// as in k_stem_fwd.  Column block q = 3 s + r of the B operand (64 pixels x 8
+// channels, 1 KB) holds tap (r, s): image row h + r - 1 shifted by s - 1
+// pixels, as two 512-byte boxes of [N][H][W * 8] -- 18 copy rows per k-block
+// where nine im2col boxes move 576 rows of 16 bytes.  The epilogue writes
+// block q to tap 3 r + s of dw.
+template <int kRW = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     k_wgrad_c8(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmX,
                const WgradParams p) {
+  static_assert(kRW == 0 || kRW == 64, "row staging for width 64");
   constexpr int S = kWc8Stages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -2150,11 +2208,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();  // the previous kernel's writes are visible from here on
 
   if (warp < kProd) {
-    // eleven boxes per stage: dy halves 0-1 (8 KB), x taps 2-10 (1 KB)
+    // boxes per stage: dy halves 0-1 (8 KB); x taps 2-10 (1 KB im2col boxes),
+    // or with row staging 2-19 (512-byte row boxes, two per tap)
     if (lane == 0) {
+      constexpr int kBoxes = kRW ? 2 + 18 : 11;
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
+      uint32_t bytes = 0;
+      for (int b = warp; b < kBoxes; b += kProd) bytes += b < 2 ? 8192u : kRW ? 512u : kWc8BlockBytes;
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
           ok = false;
@@ -2165,12 +2227,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h0 = rem / p.W, w0 = rem - h0 * p.W;
         uint8_t* sa = smem + (size_t)stage * kWc8StageBytes;
         uint8_t* sb = sa + kWgABytes;
-        uint32_t bytes = 0;
-        for (int b = warp; b < 11; b += kProd) bytes += b < 2 ? 8192u : kWc8BlockBytes;
         mbar_arrive_expect_tx(&full[stage], bytes);
-        for (int b = warp; b < 11; b += kProd) {
+        for (int b = warp; b < kBoxes; b += kProd) {
           if (b < 2) {
             tma_load_2d(sa + b * 8192, &tmDY, &full[stage], mb * 128 + b * 64, pk);
+          } else if constexpr (kRW != 0) {
+            const int q = (b - 2) >> 1, part = (b - 2) & 1;  // block q = 3 s + r
+            const int sh = q / 3, r = q - 3 * sh;
+            tma_load_3d(sb + q * kWc8BlockBytes + part * 512, &tmX, &full[stage], (sh - 1) * 8 + part * 256,
+                        h0 + r - 1, n0);
           } else {
             const int t = b - 2;
             tma_load_im2col_4d(sb + t * kWc8BlockBytes, &tmX, &full[stage], 0, w0 - 1, h0 - 1, n0,
@@ -2240,20 +2305,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x32(lane_addr + (uint32_t)(j * 32), v);
         tmem_ld_wait();
         if (k < p.Cout) {
-          if (j < 2) {
+          // column block qb (8 columns) holds tap qb (im2col) or tap 3 (qb % 3) +
+          // qb / 3 (row staging); blocks 9-11 are the zero and ones blocks
 #pragma unroll
-            for (int g = 0; g < 8; ++g)
-              reinterpret_cast<float4*>(o + j * 32)[g] =
-                  make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
-                              __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
-          } else {
-            // columns 64..71 are the last dw values, column 80 the first ones column
-            reinterpret_cast<float4*>(o + 64)[0] = make_float4(
-                __uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]), __uint_as_float(v[3]));
-            reinterpret_cast<float4*>(o + 64)[1] = make_float4(
-                __uint_as_float(v[4]), __uint_as_float(v[5]), __uint_as_float(v[6]), __uint_as_float(v[7]));
-            p.part[(long long)p.S * dwsize + (long long)split * p.Cout + k] = __uint_as_float(v[16]);
+          for (int g = 0; g < 4; ++g) {
+            const int qb = 4 * j + g;
+            if (qb < 9) {
+              const int tap = kRW ? (qb % 3) * 3 + qb / 3 : qb;
+              reinterpret_cast<float4*>(o + tap * 8)[0] =
+                  make_float4(__uint_as_float(v[8 * g]), __uint_as_float(v[8 * g + 1]),
+                              __uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
+              reinterpret_cast<float4*>(o + tap * 8)[1] =
+                  make_float4(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]),
+                              __uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
+            }
           }
+          // column 80 (block 10) is the first ones column: dbias
+          if (j == 2) p.part[(long long)p.S * dwsize + (long long)split * p.Cout + k] = __uint_as_float(v[16]);
         }
       }
     }
@@ -2487,11 +2555,11 @@ TileShape pick_tile(int nout, const Shape& sh, int num_sms) {
   return best;
 }
 
-template <int BN, bool kTS = false>
+template <int BN, bool kTS = false, int kRW = 0>
 int launch_stem(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y,
                 const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
-  using Cfg = StemCfg<BN, kTS>;
-  auto kern = k_stem_fwd<BN, kTS>;
+  using Cfg = StemCfg<BN, kTS, kRW>;
+  auto kern = k_stem_fwd<BN, kTS, kRW>;
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int grid = prm.num_m_tiles < d.num_sms ? prm.num_m_tiles : d.num_sms;
   launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, b, y, prm);
@@ -2513,12 +2581,38 @@ int make_store_map(CUtensorMap* m, void* base, long long P, int C) {
   return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
+// x [N][H][W][8] viewed as [N][H][W * 8]: boxes of `elems` consecutive
+// elements of one image row (no swizzle), for the row-staged 8-channel kernels.
+int make_row_map(CUtensorMap* m, const void* base, int N, int H, int W, int elems) {
+  PFN_encodeTiled enc = encode_tiled_fn();
+  if (!enc) return CONV3X3_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)W * 8, (cuuint64_t)H, (cuuint64_t)N};
+  cuuint64_t strides[2] = {(cuuint64_t)W * 16, (cuuint64_t)H * W * 16};
+  cuuint32_t box[3] = {(cuuint32_t)elems, 1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
+// Row staging for the 8-channel forward: width 32 or 64 and 128-pixel tiles of
+// whole image rows of one image.  CONV3X3_STEM_ROWS=0 keeps im2col boxes.
+int stem_row_width(const Shape& s) {
+  if (const char* e = std::getenv("CONV3X3_STEM_ROWS"))
+    if (std::strcmp(e, "0") == 0) return 0;
+  if (s.u != 1 || !(s.W == 32 || s.W == 64)) return 0;
+  return ((long long)s.H * s.W) % BM == 0 ? s.W : 0;
+}
+
 // Forward with exactly 8 input channels and at most 256 outputs (one N tile).
 int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const Shape& s, int act,
                  int out_f32, const EpiExtra& ex, const DevCtx& d, cudaStream_t st) {
   const int bn = s.Cout <= 64 ? 64 : s.Cout <= 128 ? 128 : 256;
+  const int rw = stem_row_width(s);
   CUtensorMap ta, tb;
-  int rc = make_im2col_map(&ta, x, s.N, s.H, s.W, 8, BM, 8, false);
+  int rc = rw ? make_row_map(&ta, x, s.N, s.H, s.W, rw * 8 < 256 ? rw * 8 : 256)
+              : make_im2col_map(&ta, x, s.N, s.H, s.W, 8, BM, 8, false);
   if (rc) return rc;
   rc = make_weight_map(&tb, w, 8, s.Cout, bn, 8, false);
   if (rc) return rc;
@@ -2544,16 +2638,21 @@ int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
   prm.zout = static_cast<__nv_bfloat16*>(ex.zout);
+#define C3_STEM(BN_, TS_, Y_)                                                  \
+  return rw == 64   ? launch_stem<BN_, TS_, 64>(ta, tb, Y_, prm, d, st)          \
+         : rw == 32 ? launch_stem<BN_, TS_, 32>(ta, tb, Y_, prm, d, st)          \
+                    : launch_stem<BN_, TS_, 0>(ta, tb, Y_, prm, d, st)
   if (bn == 128 && !out_f32 && !ex.zout) {
     // bf16 output with no z store leaves through TMA stores
     CUtensorMap ty;
     rc = make_store_map(&ty, y, s.P(), s.Cout);
     if (rc) return rc;
-    return launch_stem<128, true>(ta, tb, ty, prm, d, st);
+    C3_STEM(128, true, ty);
   }
-  if (bn == 64) return launch_stem<64>(ta, tb, tb, prm, d, st);
-  if (bn == 128) return launch_stem<128>(ta, tb, tb, prm, d, st);
-  return launch_stem<256>(ta, tb, tb, prm, d, st);
+  if (bn == 64) C3_STEM(64, false, tb);
+  if (bn == 128) C3_STEM(128, false, tb);
+  C3_STEM(256, false, tb);
+#undef C3_STEM
 }
 
 // dgrad with 8 output channels (k_stem_dgrad): whole-row tiles of 128 dx
@@ -2890,10 +2989,15 @@ size_t tc_wgrad_workspace(const Shape& s, int /*num_sms*/) {
 int run_wgrad_c8(const void* x, const void* dy, float* dw, float* db, const Shape& s, void* ws,
                  const DevCtx& d, cudaStream_t st) {
   WgPlan pl = wg_plan_c8(s);
+  // row staging at width 64 (each 64-pixel k-block is one image row);
+  // CONV3X3_STEM_ROWS=0 keeps im2col boxes
+  bool rows = s.W == 64;
+  if (const char* e = std::getenv("CONV3X3_STEM_ROWS"))
+    if (std::strcmp(e, "0") == 0) rows = false;
   CUtensorMap tdy, tx;
   int rc = make_rows_map(&tdy, dy, s.P(), s.Cout);
   if (rc) return rc;
-  rc = make_im2col_map(&tx, x, s.N, s.H, s.W, 8, kWgPix, 8, false);
+  rc = rows ? make_row_map(&tx, x, s.N, s.H, s.W, 256) : make_im2col_map(&tx, x, s.N, s.H, s.W, 8, kWgPix, 8, false);
   if (rc) return rc;
   WgradParams prm;
   prm.part = static_cast<float*>(ws);
@@ -2911,8 +3015,9 @@ int run_wgrad_c8(const void* x, const void* dy, float* dw, float* db, const Shap
   prm.num_cb = 1;
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
-  if (set_smem(k_wgrad_c8, kWc8Smem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
-  launch_pdl(k_wgrad_c8, dim3(pl.tiles * pl.S), dim3(kThreads), kWc8Smem, st, tdy, tx, prm);
+  auto kern = rows ? k_wgrad_c8<64> : k_wgrad_c8<0>;
+  if (set_smem(kern, kWc8Smem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+  launch_pdl(kern, dim3(pl.tiles * pl.S), dim3(kThreads), kWc8Smem, st, tdy, tx, prm);
   if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
   return launch_wgrad_reduce(prm.part, dw, db, (long long)s.Cout * 72, s.Cout, pl.S, pl.S, st);
 }
