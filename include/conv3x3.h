@@ -69,8 +69,10 @@
  * boxes per tap (0), or one zero-padded box per image row that all three taps
  * of a kernel row read (1; stride 1, width 16, 32 or 64).  Unset: the latter
  * for width 64 only.  CONV3X3_STEM_ROWS=0 makes the 8-input-channel forward
- * stage x as im2col boxes even where it would stage whole image rows (widths
- * 32 and 64).
+ * and weight gradient stage x as im2col boxes even where they would stage
+ * whole image rows (forward: widths 32 and 64; weight gradient: width 64).
+ * CONV3X3_STEM_DGRAD=rows runs the 8-output-channel input gradient of width 64
+ * as row bands instead of tiles.
  * CONV3X3_PDL=0 launches without programmatic dependent launch (by default a
  * kernel's set-up overlaps the end of the previous kernel in the stream; each
  * kernel still waits for that kernel to complete before touching memory).

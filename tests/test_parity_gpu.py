@@ -230,6 +230,7 @@ FUSED_SHAPES = [
     (2, 8, 128, 12, 12),    # eight input channels: dgrad writes 8 channels
     (3, 128, 256, 17, 13),
     (2, 256, 64, 5, 7),
+    (3, 8, 128, 5, 64),     # eight input channels, width 64: the row-band dgrad
 ]
 
 
@@ -288,16 +289,23 @@ def test_fused_activation_backward_tiles(tile, monkeypatch):
 
 # dgrad with 8 output channels and whole-row tiles of 128 pixels (the stem's
 # input gradient): T = dy x Wt on the tensor cores, then the nine-tap sum
+# CONV3X3_STEM_DGRAD=rows runs width 64 as row bands (T formed once per dy row,
+# a ring of staged T rows; bands cross image boundaries); by default, tiles.
 STEM_DGRAD_SHAPES = [
-    (2, 8, 128, 64, 64),   # two dx rows per tile
+    (2, 8, 128, 64, 64),   # two dx rows per tile / bands of one row (128 rows, 128+ SMs)
     (3, 8, 64, 8, 32),     # 64 dy channels, four rows per tile
     (4, 8, 128, 16, 8),    # sixteen rows of width 8 per tile
     (2, 8, 128, 2, 64),    # one tile per image: both halo rows outside it
+    (64, 8, 128, 7, 64),   # 448 rows: bands of three rows crossing image boundaries
+    (5, 8, 64, 3, 64),     # 64 dy channels, odd image height, one-row bands
 ]
 
 
+@pytest.mark.parametrize("kernel", ["tiles", "rows"])
 @pytest.mark.parametrize("shape", STEM_DGRAD_SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_eight_output_channel_dgrad(shape):
+def test_eight_output_channel_dgrad(shape, kernel, monkeypatch):
+    if kernel == "rows":
+        monkeypatch.setenv("CONV3X3_STEM_DGRAD", "rows")
     t = _small(shape)
     zin_h = synth.make_zin(t.layer, seed=7)
     x, w, b, dy = dev_tensors(t)

@@ -1840,6 +1840,278 @@ __global__ void __launch_bounds__(kSdThreads, 1)
 }
 
 // ----------------------------------------------------------------------------
+// input gradient with 8 output channels, image width 64: row bands
+// ----------------------------------------------------------------------------
+// The same T = dy x Wt formulation as k_stem_dgrad, but each CTA owns a band of
+// consecutive image rows (rows of all images in one sequence, n * H + h) and
+// forms T once per dy row: chunks of two dy rows (128 pixels, one M = 128 MMA
+// per 16 channels) stream through four stages, the epilogue stages each
+// chunk's two T rows in a ring of four T rows in shared memory, and dx row r is
+// summed as soon as T rows r - 1 .. r + 1 are staged (T rows of another image,
+// or outside the batch, count as zero).  dy crosses the copy engine and the
+// tensor cores about once (plus two halo rows per band) instead of twice.
+constexpr int kSrW = 64;                             // image width
+constexpr int kSrTPitch = 76;                        // floats per staged T pixel (72 used)
+constexpr uint32_t kSrTRow = kSrW * kSrTPitch * 4;   // one staged T row
+constexpr int kSrRing = 4;                           // staged T rows
+constexpr int kSrStages = 4;
+constexpr uint32_t kSrChunkBytes = 2u * kSrW * 128u;  // two dy rows x 64 channels
+static_assert(kSrTPitch % 4 == 0, "T pixels must stay 16-byte aligned");
+
+struct StemDgradRowsParams {
+  void* out;
+  int out_f32;
+  const __nv_bfloat16* zin;  // optional act'(z_in) scaling (laid out like dx)
+  int zin_act;
+  int NH, H, K;              // image rows of the batch, rows per image, dy channels
+  int band;                  // dx rows per CTA
+  unsigned* status;
+  unsigned long long wait_ns;
+};
+
+__host__ __device__ constexpr size_t stem_dgrad_rows_smem(int K) {
+  return (size_t)kSrStages * (K / 64) * kSrChunkBytes  // dy stages
+         + (size_t)(K / 8) * kSdN * 16                   // Wt, no-swizzle K-major
+         + (size_t)kSrRing * kSrTRow                     // staged T rows
+         + 1024 + 256;                                   // alignment, barriers
+}
+
+__global__ void __launch_bounds__(kSdThreads, 1)
+    k_stem_dgrad_rows(const __grid_constant__ CUtensorMap tmDY, const __nv_bfloat16* __restrict__ w,
+                      const StemDgradRowsParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const int kchunks = p.K / 64;
+  const uint32_t stage_bytes = (uint32_t)kchunks * kSrChunkBytes;
+  uint8_t* wsm = smem + (size_t)kSrStages * stage_bytes;
+  const uint32_t wgroup_bytes = kSdN * 16;  // one 8-channel K group of Wt: 80 rows x 16 B
+  uint8_t* ring = wsm + (size_t)(p.K / 8) * wgroup_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)kSrRing * kSrTRow);
+  uint64_t* empty = full + kSrStages;
+  uint64_t* tfull = empty + kSrStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* tready = tempty + 2;  // every epilogue warp has staged its part of a chunk
+  uint64_t* tdone = tready + 1;   // every epilogue warp has finished the gather after it
+  uint64_t* drain = tdone + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  // this CTA's dx rows [g0, g1) and the T rows [t0, t1) they read
+  const int g0 = blockIdx.x * p.band;
+  const int g1 = min(p.NH, g0 + p.band);
+  const int t0 = max(g0 - 1, 0), t1 = min(g1 + 1, p.NH);
+  const int nchunks = (t1 - t0 + 1) / 2;
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < kSrStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kSdEpiWarps);
+    }
+    mbar_init(tready, kSdEpiWarps);
+    mbar_init(tdone, kSdEpiWarps);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmDY);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  pdl_wait();  // w is read below
+  // Wt from w [K][3][3][8]: element (n = 8 t + c, k) at group k/8, row n, 2 (k % 8) bytes;
+  // rows 72..79 are zero
+  for (int e = threadIdx.x; e < (p.K / 8) * kSdN; e += kSdThreads) {
+    const int g = e / kSdN, n = e - g * kSdN;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (n < 72) {
+      __nv_bfloat16 h[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) h[i] = w[(size_t)(g * 8 + i) * 72 + n];
+      v = *reinterpret_cast<const uint4*>(h);
+    }
+    *reinterpret_cast<uint4*>(wsm + (size_t)g * wgroup_bytes + n * 16) = v;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp < kProd) {
+    // ------------------------------------------------------------ TMA producer (warp 0)
+    if (warp == 0 && lane == 0) {
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int j = 0; j < nchunks && ok; ++j) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sa = smem + (size_t)stage * stage_bytes;
+        mbar_arrive_expect_tx(&full[stage], stage_bytes);
+        for (int c = 0; c < kchunks; ++c)  // rows past the batch read as zero
+          tma_load_3d(sa + (size_t)c * kSrChunkBytes, &tmDY, &full[stage], c * 64, 0, t0 + 2 * j);
+        ++issued;
+        if (++stage == kSrStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) {
+        int n = issued < kSrStages ? issued : kSrStages;
+        for (int i = 0; i < n; ++i) {
+          if (--stage < 0) {
+            stage = kSrStages - 1;
+            phase ^= 1;
+          }
+          mbar_wait(&full[stage], phase, drain_wait_ns(p.wait_ns), nullptr, nullptr);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, kSdN, 0, 0);
+      const uint32_t sbase = smem_u32(smem), wbase = smem_u32(wsm);
+      int stage = 0, buf = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int j = 0; j < nchunks && ok; ++j) {
+        if (!mbar_wait(&tempty[buf], acc_phase ^ 1, p.wait_ns, p.status, abort_flag)) break;
+        if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t a0 = sbase + (uint32_t)stage * stage_bytes;
+        const uint32_t d0 = tmem_base + (uint32_t)(buf * 128);
+        for (int c = 0; c < kchunks; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            // A: 128 dy pixels x 16 channels (SW128 K-major); B: 16 channels of Wt
+            tc_mma_bf16(d0, smem_desc(a0 + (uint32_t)c * kSrChunkBytes + kk * 32, 16, 1024, kSwizzle128B),
+                        smem_desc(wbase + (uint32_t)((c * 4 + kk) * 2) * (kSdN * 16), kSdN * 16, 128,
+                                  kSwizzleNone),
+                        idesc, (c | kk) != 0 ? 1u : 0u);
+        tc_commit(&empty[stage]);
+        tc_commit(&tfull[buf]);
+        if (++stage == kSrStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (++buf == 2) {
+          buf = 0;
+          acc_phase ^= 1;
+        }
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, p.wait_ns, nullptr, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // warp (q = lane quarter, h = half): T pixel 32 q + lane of the chunk;
+    // half 0 stages columns 0..31 and 64..71, half 1 columns 32..63
+    const int ew = warp - (kProd + 1);
+    const int q = warp & 3, h = ew >> 2;
+    const int tp = q * 32 + lane;  // pixel of the chunk: row tp / 64, column tp % 64
+    const int et = ew * 32 + lane;  // 0..255: gather thread
+    const int gpx = et >> 2, gc = (et & 3) * 2;  // gather: pixel, channel pair
+    int buf = 0;
+    uint32_t acc_phase = 0, tph = 0;
+    int next = g0;  // next dx row to sum
+    bool ok = true;
+    for (int j = 0; j <= nchunks && ok; ++j) {
+      const bool staging = j < nchunks;
+      // the previous gather has read the ring slots this chunk overwrites
+      if (!mbar_wait(tdone, tph ^ 1, p.wait_ns, p.status, abort_flag)) break;
+      if (staging) {
+        if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 128);
+        uint32_t v[32], v8[8];
+        tmem_ld_32x32b_x32(taddr + (h ? 32u : 0u), v);
+        if (h == 0) tmem_ld_32x32b_x8(taddr + 64u, v8);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+        const int slot = (2 * j + (tp >> 6)) & (kSrRing - 1);
+        float4* trow = reinterpret_cast<float4*>(ring + (size_t)slot * kSrTRow + (size_t)(tp & 63) * kSrTPitch * 4);
+        const int c4 = h ? 8 : 0;  // first float4 of this warp's 32 columns
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          trow[c4 + i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+        if (h == 0) {
+          trow[16] = make_float4(__uint_as_float(v8[0]), __uint_as_float(v8[1]), __uint_as_float(v8[2]),
+                                 __uint_as_float(v8[3]));
+          trow[17] = make_float4(__uint_as_float(v8[4]), __uint_as_float(v8[5]), __uint_as_float(v8[6]),
+                                 __uint_as_float(v8[7]));
+        }
+        if (++buf == 2) {
+          buf = 0;
+          acc_phase ^= 1;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tready);
+      if (!mbar_wait(tready, tph, p.wait_ns, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      // T rows t0 .. t0 + 2 j + 1 are staged: sum every dx row r whose T rows
+      // r - 1 .. r + 1 are (after the last chunk: every remaining row -- the
+      // rows past the staged ones are past the batch and read as zero)
+      const int hi = staging ? t0 + 2 * j : p.NH;
+      for (; next < g1 && next <= hi; ++next) {
+        const int r = next, img = r / p.H;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int rk = 0; rk < 3; ++rk) {
+          const int tr = r + 1 - rk;  // T row
+          if (tr < 0 || tr >= p.NH || tr / p.H != img) continue;
+          const float* tb = reinterpret_cast<const float*>(ring + (size_t)((tr - t0) & (kSrRing - 1)) * kSrTRow);
+#pragma unroll
+          for (int s = 0; s < 3; ++s) {
+            const int px = gpx + 1 - s;
+            if (px < 0 || px >= kSrW) continue;
+            const float2 t = *reinterpret_cast<const float2*>(tb + px * kSrTPitch + (rk * 3 + s) * 8 + gc);
+            a0 += t.x;
+            a1 += t.y;
+          }
+        }
+        const long long pix = (long long)r * kSrW + gpx;
+        if (p.zin) {
+          const float2 z = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p.zin + pix * 8 + gc));
+          a0 *= act_grad_f32(p.zin_act, z.x);
+          a1 *= act_grad_f32(p.zin_act, z.y);
+        }
+        if (p.out_f32)
+          *reinterpret_cast<float2*>(static_cast<float*>(p.out) + pix * 8 + gc) = make_float2(a0, a1);
+        else
+          *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + pix * 8 + gc) =
+              __floats2bfloat162_rn(a0, a1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tdone);
+      tph ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, 256);
+}
+
+// ----------------------------------------------------------------------------
 // wgrad split-K implicit GEMM
 // ----------------------------------------------------------------------------
 constexpr int kWgTaps = 3;                       // taps per CTA tile (one kernel row)
@@ -2664,8 +2936,52 @@ bool stem_dgrad_fits(const Shape& s) {
   return R <= s.H && s.H % R == 0;
 }
 
+// Width 64, row bands (k_stem_dgrad_rows): selected by CONV3X3_STEM_DGRAD=rows.
+// Measured on GB300 (batch 64, 64x64, 128 dy channels) it ran in 32.8 us
+// against 28.7 us for the tile kernel: both are bound by the epilogue's
+// per-chunk round trip (stage T, synchronise, sum, synchronise), and a band
+// walked in order gives each round trip one or two dx rows where a tile gives
+// two, so the halved tensor and copy work did not pay.
+int run_stem_dgrad_rows(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
+                        const EpiExtra& ex, const DevCtx& d, cudaStream_t st) {
+  PFN_encodeTiled enc = encode_tiled_fn();
+  if (!enc) return CONV3X3_ERR_CUDA;
+  // dy as [N * H][64][K]: boxes of 64 channels x 64 pixels x 2 rows
+  CUtensorMap tdy;
+  const int NH = s.N * s.H;
+  cuuint64_t dims[3] = {(cuuint64_t)s.Cout, (cuuint64_t)kSrW, (cuuint64_t)NH};
+  cuuint64_t strides[2] = {(cuuint64_t)s.Cout * 2, (cuuint64_t)kSrW * s.Cout * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kSrW, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(&tdy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(dy), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return CONV3X3_ERR_CUDA;
+  StemDgradRowsParams prm;
+  prm.out = dx;
+  prm.out_f32 = out_f32;
+  prm.zin = static_cast<const __nv_bfloat16*>(ex.zin);
+  prm.zin_act = ex.zin ? ex.zin_act : CONV3X3_ACT_NONE;
+  prm.NH = NH;
+  prm.H = s.H;
+  prm.K = s.Cout;
+  const int grid0 = NH < d.num_sms ? NH : d.num_sms;
+  prm.band = (NH + grid0 - 1) / grid0;
+  const int grid = (NH + prm.band - 1) / prm.band;
+  prm.status = d.status;
+  prm.wait_ns = d.wait_ns;
+  const size_t smem = stem_dgrad_rows_smem(s.Cout);
+  if (set_smem(k_stem_dgrad_rows, smem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+  launch_pdl(k_stem_dgrad_rows, dim3(grid), dim3(kSdThreads), smem, st, tdy,
+             static_cast<const __nv_bfloat16*>(w), prm);
+  return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
 int run_stem_dgrad(const void* dy, const void* w, void* dx, const Shape& s, int out_f32,
                    const EpiExtra& ex, const DevCtx& d, cudaStream_t st) {
+  const char* e = std::getenv("CONV3X3_STEM_DGRAD");
+  if (s.W == kSrW && e && std::strcmp(e, "rows") == 0)
+    return run_stem_dgrad_rows(dy, w, dx, s, out_f32, ex, d, st);
   PFN_encodeTiled enc = encode_tiled_fn();
   if (!enc) return CONV3X3_ERR_CUDA;
   const int R = BM / s.W;
