@@ -358,6 +358,45 @@ def test_wgrad_x_layouts(shape, rows, monkeypatch):
     assert torch.equal(dw, dw2) and torch.equal(db, db2)
 
 
+WGRAD_PAIR_SHAPES = [
+    # N, Cin, Cout, H, W: Cout a multiple of 256 takes the two-CTA tiles
+    (2, 128, 256, 8, 8),     # one pair block
+    (1, 64, 512, 5, 7),      # ragged pixel tail, half a channel block, two pair blocks
+    (2, 192, 256, 6, 10),    # ragged channel block (128 + 64)
+    (1, 72, 256, 9, 9),      # ragged 64-channel box
+    (3, 256, 256, 16, 16),   # several channel blocks and splits
+]
+
+
+@pytest.mark.parametrize("pair", ["1", "0"], ids=["pair", "one_cta"])
+@pytest.mark.parametrize("shape", WGRAD_PAIR_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_wgrad_pair_tiles(shape, pair, monkeypatch):
+    monkeypatch.setenv("CONV3X3_WGRAD_PAIR", pair)
+    t = _small(shape, seed=19)
+    x, _, _, dy = dev_tensors(t)
+    dw, db = ops.wgrad(x, dy, path=L.PATH_TENSOR)
+    dw2, db2 = ops.wgrad(x, dy, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    rdw, rdb = oracle.conv3x3_wgrad(t.x, t.dy)
+    assert rel_err(host(dw), rdw) <= TOL_BF16
+    assert rel_err(host(db), rdb) <= TOL_BF16
+    assert torch.equal(dw, dw2) and torch.equal(db, db2)
+
+
+@pytest.mark.parametrize("splits", ["1", "3", "10"])
+def test_wgrad_pair_split_counts(splits, monkeypatch):
+    # 624 pixels = 10 k-blocks, the last one 48 pixels: one split, splits of
+    # 4 + 4 + 2 k-blocks, one k-block per split
+    monkeypatch.setenv("CONV3X3_WGRAD_SPLITS", splits)
+    t = _small((3, 128, 256, 13, 16), seed=23)
+    x, _, _, dy = dev_tensors(t)
+    dw, db = ops.wgrad(x, dy, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    rdw, rdb = oracle.conv3x3_wgrad(t.x, t.dy)
+    assert rel_err(host(dw), rdw) <= TOL_BF16
+    assert rel_err(host(db), rdb) <= TOL_BF16
+
+
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_wgrad_dbias_only_four_byte_aligned(path):
     # dbias may sit 4 bytes past a 16-byte boundary (the ABI asks for 4)
@@ -578,6 +617,7 @@ CAT_SHAPES = [
     (2, 24, 40, 64, 6, 6),      # Ca not a whole 64-channel chunk: CUDA-core kernels only
     (1, 64, 128, 128, 4, 16),   # wgrad with row-shifted x boxes from both parts
     (2, 128, 64, 64, 2, 32),
+    (2, 128, 64, 256, 6, 6),    # wgrad on two-CTA tiles, x from both parts
 ]
 
 
@@ -705,6 +745,7 @@ STRIDE_SHAPES = [
     (3, 64, 96, 5, 6),
     (1, 64, 64, 1, 5),      # single-row images
     (2, 16, 32, 6, 7),      # fewer than 64 channels: CUDA-core kernels only
+    (2, 64, 256, 9, 9),     # wgrad on two-CTA tiles
 ]
 
 

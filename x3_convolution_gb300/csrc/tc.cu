@@ -2401,6 +2401,252 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ----------------------------------------------------------------------------
+// wgrad on two-CTA clusters (tcgen05.mma.cta_group::2)
+// ----------------------------------------------------------------------------
+// A pair tile is 256 output channels (128 per CTA: the MMA's M = 256 rows, dy
+// MN-major) x one kernel row (three taps) x 128 input channels, over a pixel
+// range.  The pair shares the x operand, each CTA staging half of its columns:
+// rank 0 tap 0 and input channels 0-63 of tap 2, rank 1 tap 1 and channels
+// 64-127 of tap 2.  Per 16 pixels one M = 256, N = 256 MMA covers taps 0-1
+// (accumulator columns 0-127 from rank 0's half, 128-255 from rank 1's) and
+// one M = 256, N = 128 MMA tap 2 (columns 256-319 and 320-383); in the pair
+// that owns dbias the tap-2 MMA is N = 144 and each half ends with 8 columns
+// of the static ones block, so tap 2's second half moves to columns 328-391
+// and column 320 holds dbias.  Each CTA stages 40 KB per 64-pixel k-block
+// where the one-CTA tile stages 64 KB for the same accumulator work, and the
+// tensor core reads half the x operand from each shared memory.
+constexpr uint32_t kWpX0 = kWgABytes;                      // this CTA's tap (0 or 1), two 64-channel boxes
+constexpr uint32_t kWpX2 = kWgABytes + kWgBBytes;          // this CTA's 64 channels of tap 2
+constexpr uint32_t kWpOnes = kWpX2 + kWgBBytes / 2;        // ones block (follows tap 2 at one box stride)
+constexpr uint32_t kWpStage = kWpOnes + kWgOnesBytes;      // 48 KB
+constexpr uint32_t kWpLoadBytes = kWpOnes;                 // bytes each CTA loads per k-block
+constexpr int kWpBiasCol = 256 + 64;                     // rank 0's first ones column
+constexpr int kWpStages = 4;
+constexpr size_t kWpSmem = (size_t)kWpStages * kWpStage + 256 + 1024 + 8 * 1024;
+static_assert(kWpStages >= kProd, "stage-parallel producers need S >= kProd");
+static_assert(kWpStage % 1024 == 0 && kWpX2 % 1024 == 0, "swizzle atoms must stay 1 KB aligned");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_wgrad_pair(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmX,
+                 const __grid_constant__ CUtensorMap tmX2, const WgradParams p) {
+  constexpr int S = kWpStages;
+  extern __shared__ uint8_t smem_raw[];
+  // same offsets in both CTAs: the MMAs address the peer's operands at rank 0's
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * kWpStage);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* drain = tfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  // num_mb counts 256-channel pair blocks here
+  const int num_tiles = p.num_mb * 3 * p.num_cb;
+  const int pair = blockIdx.x >> 1;
+  const int tile = pair % num_tiles;
+  const int split = pair / num_tiles;
+  const int mb = tile % p.num_mb;
+  const int rest = tile / p.num_mb;
+  const int cb = rest % p.num_cb;
+  const int tr = rest / p.num_cb;  // kernel row r: taps 3r .. 3r+2
+  const bool do_bias = (tr == 0 && cb == 0);
+  const int kb0 = split * p.kb_per_split;
+  const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+  const int HW = p.H * p.W;
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmDY);
+    tma_prefetch_desc(&tmX);
+    if (p.ca < p.Cin) tma_prefetch_desc(&tmX2);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc_pair(tmem_slot, kWgTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp >= kEpiBase && do_bias) {  // every stage's ones block (bf16 1.0 = 0x3F80)
+    for (int st = 0; st < S; ++st) {
+      uint4* o = reinterpret_cast<uint4*>(smem + (size_t)st * kWpStage + kWpOnes);
+      for (int i = threadIdx.x - 32 * kEpiBase; i < (int)(kWgOnesBytes / 16); i += 32 * kWgEpiWarps)
+        o[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the previous kernel's writes are visible from here on
+  const uint32_t full0 = cluster_addr(full, 0);  // rank 0's full barriers count both CTAs' bytes
+
+  if (warp < kProd) {
+    // Whole stages in turn: producer `warp` fills the k-blocks issued % kProd
+    // == warp with this CTA's dy half (two 64-channel boxes), its x tap (two
+    // im2col boxes) and its 64 channels of tap 2.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (issued % kProd == warp) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int pk = kb * kWgPix;
+          const int n0 = pk / HW, rem = pk - n0 * HW;
+          const int h0 = rem / p.W, w0 = rem - h0 * p.W;
+          const int cw = p.ustride * w0 - 1, chh = p.ustride * h0 - 1;
+          uint8_t* sa = smem + (size_t)stage * kWpStage;
+          const uint32_t fb = full0 + (uint32_t)stage * 8u;
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kWpLoadBytes);
+          const int k0 = mb * 256 + (int)rank * 128;
+          tma_load_2d_pair(sa, &tmDY, fb, k0, pk);
+          tma_load_2d_pair(sa + 8192, &tmDY, fb, k0 + 64, pk);
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            // j = 0, 1: this CTA's tap, channel halves; j = 2: its half of tap 2
+            const int t = j < 2 ? (int)rank : 2;
+            const int c = cb * 128 + (j < 2 ? j * 64 : (int)rank * 64);  // a 64-channel box lies in one part
+            const bool second = c >= p.ca;
+            tma_load_im2col_4d_pair(sa + kWpX0 + j * 8192, second ? &tmX2 : &tmX, fb, second ? c - p.ca : c, cw,
+                                    chh, n0, (uint16_t)t, (uint16_t)tr);
+          }
+        }
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) {
+        if (rank == 0) {
+          // wait (bounded) for the loads still in flight
+          int n = issued < S ? issued : S;
+          int st = stage;
+          uint32_t ph = phase;
+          for (int i = 0; i < n; ++i) {
+            if (--st < 0) {
+              st = S - 1;
+              ph ^= 1;
+            }
+            mbar_wait(&full[st], ph, drain_wait_ns(p.wait_ns), nullptr, nullptr);
+          }
+        } else {
+          // rank 1's loads complete on rank 0's barriers: give them time to land
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t idesc256 = idesc_bf16_f32(256, 256, 1, 1);
+      const uint32_t idesc_t2 = idesc_bf16_f32(256, do_bias ? 144 : 128, 1, 1);
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t a_desc0 = smem_desc(sbase, 8192, 1024, kSwizzle128B);
+      const uint64_t b01_desc0 = smem_desc(sbase + kWpX0, 8192, 1024, kSwizzle128B);
+      const uint64_t b2_desc0 = smem_desc(sbase + kWpX2, 8192, 1024, kSwizzle128B);
+      constexpr uint32_t kStageStep = kWpStage >> 4;
+      constexpr uint32_t kKStep = 2048u >> 4;  // 16 pixels of an MN-major operand
+      int stage = 0;
+      uint32_t phase = 0, stage_off = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc0 = kb != kb0 ? 1u : 0u;
+#pragma unroll
+        for (int k = 0; k < kWgPix / 16; ++k) {
+          const uint32_t acc = k == 0 ? acc0 : 1u;
+          const uint64_t off = (uint64_t)(stage_off + k * kKStep);
+          tc_mma_bf16_pair(tmem_base, a_desc0 + off, b01_desc0 + off, idesc256, acc);
+          tc_mma_bf16_pair(tmem_base + 256, a_desc0 + off, b2_desc0 + off, idesc_t2, acc);
+        }
+        tc_commit_pair_mc(&empty[stage], (uint16_t)0x3);
+        stage_off += kStageStep;
+        if (++stage == S) {
+          stage = 0;
+          stage_off = 0;
+          phase ^= 1;
+        }
+      }
+      if (ok) tc_commit_pair_mc(tfull, (uint16_t)0x3);
+      // every issued MMA (which reads both CTAs' shared memory and writes both
+      // TMEMs) retires before either CTA releases anything
+      tc_commit_pair(drain);
+      mbar_wait(drain, 0, p.wait_ns, nullptr, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    // TMEM lane = this CTA's output channel; column c of tap t as described
+    // above the kernel.
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int k = mb * 256 + (int)rank * 128 + row;
+    if (mbar_wait(tfull, 0, p.wait_ns, p.status, abort_flag)) {
+      tc_fence_after();
+      const long long dwsize = (long long)p.Cout * 9 * p.Cin;
+      const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+      const uint32_t gap = do_bias ? 8u : 0u;  // the ones columns between tap 2's halves
+#pragma unroll 1
+      for (int t = 0; t < kWgTaps; ++t) {
+        const int tap = tr * 3 + t;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t col = (uint32_t)(t * 128 + j * 32) + (t == 2 && j >= 2 ? gap : 0u);
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(lane_addr + col, v);
+          tmem_ld_wait();
+          const int c0 = cb * 128 + j * 32;
+          if (k < p.Cout && c0 < p.Cin) {
+            float* o = p.part + (long long)split * dwsize + ((long long)k * 9 + tap) * p.Cin + c0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              if (c0 + 8 * g < p.Cin) {
+                reinterpret_cast<float4*>(o + 8 * g)[0] = make_float4(
+                    __uint_as_float(v[8 * g]), __uint_as_float(v[8 * g + 1]),
+                    __uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
+                reinterpret_cast<float4*>(o + 8 * g)[1] = make_float4(
+                    __uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]),
+                    __uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
+              }
+          }
+        }
+      }
+      if (do_bias) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(lane_addr + (uint32_t)kWpBiasCol, v);
+        tmem_ld_wait();
+        if (k < p.Cout)
+          p.part[(long long)p.S * dwsize + (long long)split * p.Cout + k] = __uint_as_float(v[0]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc_pair(tmem_base, kWgTmemCols);
+}
+
+// ----------------------------------------------------------------------------
 // wgrad, 8 input channels (the UNet stem)
 // ----------------------------------------------------------------------------
 // N = all nine taps x 8 channels at once: per 64-pixel k-block, x is staged as
@@ -3216,6 +3462,42 @@ WgPlan wg_plan(const Shape& s) {
   return pl;
 }
 
+// Two-CTA wgrad: Cout a multiple of 256 (pair tiles of 256 output channels).
+bool wg_pair_shape(const Shape& s) { return s.Cout % 256 == 0; }
+
+// Split plan of k_wgrad_pair: the same cost model over pair tiles and the
+// kPlanSms / 2 cluster slots.
+WgPlan wg_plan_pair(const Shape& s) {
+  WgPlan pl;
+  pl.num_mb = s.Cout / 256;
+  pl.num_cb = (s.Cin + 127) / 128;
+  pl.tiles = pl.num_mb * 3 * pl.num_cb;
+  pl.kb_total = (int)((s.P() + kWgPix - 1) / kWgPix);
+  const double dw_mb = (double)s.Cout * 9.0 * s.Cin * 4.0 / 1e6;
+  const int slots = kPlanSms / 2;
+  double best = -1;
+  int bestS = 1;
+  for (int S = 1; S <= pl.kb_total && S <= 1024; ++S) {
+    int per = (pl.kb_total + S - 1) / S;
+    int Sreal = (pl.kb_total + per - 1) / per;
+    if (Sreal != S) continue;
+    long long units = (long long)pl.tiles * S;
+    long long waves = (units + slots - 1) / slots;
+    double cost = (double)waves * (per + 20) + 0.3 * S * dw_mb;
+    if (best < 0 || cost < best) {
+      best = cost;
+      bestS = S;
+    }
+  }
+  if (const char* e = std::getenv("CONV3X3_WGRAD_SPLITS")) {
+    const int v = std::atoi(e);
+    if (v >= 1 && v <= pl.kb_total) bestS = v;
+  }
+  pl.kb_per_split = (pl.kb_total + bestS - 1) / bestS;
+  pl.S = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
+  return pl;
+}
+
 }  // namespace
 
 bool tc_supported(int pass, const Shape& s) {
@@ -3297,9 +3579,15 @@ size_t tc_wgrad_workspace(const Shape& s, int /*num_sms*/) {
     WgPlan pl = wg_plan_c8(s);
     return (size_t)pl.S * (size_t)((long long)s.Cout * 72 + s.Cout) * sizeof(float);
   }
-  WgPlan pl = wg_plan(wg_grid(s));
+  const Shape g = wg_grid(s);
+  int S = wg_plan(g).S;
+  // room for either kernel's splits, whichever the call takes
+  if (wg_pair_shape(g)) {
+    const int Sp = wg_plan_pair(g).S;
+    if (Sp > S) S = Sp;
+  }
   long long dwsize = (long long)s.Cout * 9 * s.Cin;
-  return (size_t)pl.S * (size_t)(dwsize + s.Cout) * sizeof(float);
+  return (size_t)S * (size_t)(dwsize + s.Cout) * sizeof(float);
 }
 
 int run_wgrad_c8(const void* x, const void* dy, float* dw, float* db, const Shape& s, void* ws,
@@ -3373,6 +3661,23 @@ int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
   const int hw = wg_row_width(s);
+  // Two-CTA tiles for Cout a multiple of 256 with im2col x;
+  // CONV3X3_WGRAD_PAIR=0 keeps the one-CTA kernel, =1 is the default.
+  bool pair = hw == 0 && wg_pair_shape(g);
+  if (const char* e = std::getenv("CONV3X3_WGRAD_PAIR"))
+    if (std::strcmp(e, "0") == 0) pair = false;
+  if (pair) {
+    const WgPlan pp = wg_plan_pair(g);
+    prm.kb_total = pp.kb_total;
+    prm.kb_per_split = pp.kb_per_split;
+    prm.S = pp.S;
+    prm.num_mb = pp.num_mb;  // 256-channel pair blocks
+    prm.num_cb = pp.num_cb;
+    if (set_smem(k_wgrad_pair, kWpSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+    launch_pdl(k_wgrad_pair, dim3(2 * pp.tiles * pp.S), dim3(kThreads), kWpSmem, st, tdy, tx, tx2, prm);
+    if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
+    return launch_wgrad_reduce(prm.part, dw, db, (long long)s.Cout * 9 * s.Cin, s.Cout, pp.S, pp.S, st);
+  }
   if (hw) {
     // row-shifted x: per image row one box of (W + 2) pixels x 64 channels
     rc = make_halo_map(&tx, x, s.N, s.H, s.W, cat.on() ? cat.Ca : s.Cin, 1, s.W + 2);
