@@ -68,7 +68,10 @@
  * CONV3X3_WGRAD_ROWS=0|1 chooses how the weight gradient stages x: im2col
  * boxes per tap (0), or one zero-padded box per image row that all three taps
  * of a kernel row read (1; stride 1, width 16, 32 or 64).  Unset: the latter
- * for width 64 only.  CONV3X3_STEM_ROWS=0 makes the 8-input-channel forward
+ * for width 64 only.  CONV3X3_WGRAD_PAIR=0 keeps the weight gradient of Cout a
+ * multiple of 256 on one-CTA tiles (by default, where x is staged as im2col
+ * boxes, it runs on two-CTA clusters with 256-output-channel tiles; the
+ * workspace size covers either).  CONV3X3_STEM_ROWS=0 makes the 8-input-channel forward
  * and weight gradient stage x as im2col boxes even where they would stage
  * whole image rows (forward: widths 32 and 64; weight gradient: width 64).
  * CONV3X3_STEM_DGRAD=rows runs the 8-output-channel input gradient of width 64
