@@ -73,7 +73,8 @@
  * boxes, it runs on two-CTA clusters with 256-output-channel tiles; the
  * workspace size covers either).  CONV3X3_STEM_ROWS=0 makes the 8-input-channel forward
  * and weight gradient stage x as im2col boxes even where they would stage
- * whole image rows (forward: widths 32 and 64; weight gradient: width 64).
+ * whole image rows (forward: widths 32 and 64; weight gradient: width 64, one
+ * box of three zero-padded image rows per 64-pixel k-block).
  * CONV3X3_STEM_DGRAD=rows runs the 8-output-channel input gradient of width 64
  * as row bands instead of tiles.
  * CONV3X3_PDL=0 launches without programmatic dependent launch (by default a

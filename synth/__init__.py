@@ -167,6 +167,8 @@ STEM = Layer("stem", 64, 8, 128, 64, 64, act=1, cin_real=3)
 L1 = Layer("l1", 64, 128, 128, 64, 64, act=1)
 L2 = Layer("l2", 64, 256, 256, 32, 32, act=1)
 L3 = Layer("l3", 64, 384, 384, 16, 16, act=1)
+# the UNet's deepest level (not a gate config): 512 channels at 8x8
+L4 = Layer("l4", 64, 512, 512, 8, 8, act=1)
 
 
 def unet_stack(N: int = 64, base: int = 128, mult=(1, 2, 3, 4), res0: int = 64,
@@ -212,7 +214,7 @@ DOWNSAMPLE = [Layer(f"down{l}.downsample", 64, c, c, r, r, stride=2)
 # The benchmark's training-step sweep: the stem conv followed by the 32 resblock convs.
 UNET_STEP = [STEM] + STACK
 
-CONFIGS = {"tiny": [TINY], "stem": [STEM], "l1": [L1], "l2": [L2], "l3": [L3], "stack": STACK,
+CONFIGS = {"tiny": [TINY], "stem": [STEM], "l1": [L1], "l2": [L2], "l3": [L3], "l4": [L4], "stack": STACK,
            "unet": UNET_STEP, "downsample": DOWNSAMPLE}
 
 

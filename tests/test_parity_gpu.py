@@ -221,6 +221,32 @@ def test_eight_channel_kernels(shape, rows, monkeypatch):
         assert np.array_equal(host(ybf), rne_bf16(host(y32)))
 
 
+STEM_WGRAD_SHAPES = [
+    # width 64: each 64-pixel k-block is one image row
+    (2, 8, 128, 4, 64),
+    (2, 8, 256, 2, 64),   # two 128-channel tiles
+    (1, 8, 24, 3, 64),    # Cout 24: a mostly empty tile
+    (3, 8, 200, 5, 64),   # ragged second tile
+    (2, 8, 128, 1, 64),   # single-row images: both halo rows are padding
+]
+
+
+@pytest.mark.parametrize("mode", ["halo", "im2col"])
+@pytest.mark.parametrize("shape", STEM_WGRAD_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_eight_channel_wgrad_x_layouts(shape, mode, monkeypatch):
+    if mode == "im2col":
+        monkeypatch.setenv("CONV3X3_STEM_ROWS", "0")
+    t = _small(shape, seed=29)
+    x, _, _, dy = dev_tensors(t)
+    dw, db = ops.wgrad(x, dy, path=L.PATH_TENSOR)
+    dw2, db2 = ops.wgrad(x, dy, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    rdw, rdb = oracle.conv3x3_wgrad(t.x, t.dy)
+    assert rel_err(host(dw), rdw) <= TOL_BF16
+    assert rel_err(host(db), rdb) <= TOL_BF16
+    assert torch.equal(dw, dw2) and torch.equal(db, db2)
+
+
 # ---------------------------------------------------------------------------
 # backward through the input's activation, fused into the epilogues
 # ---------------------------------------------------------------------------

@@ -2661,18 +2661,9 @@ constexpr uint32_t kWc8StageBytes = kWgABytes + kWc8BBytes;
 constexpr int kWc8Stages = 6;
 constexpr size_t kWc8Smem = (size_t)kWc8Stages * kWc8StageBytes + 256 + 1024;
 
-//
-// kRW = 64 (image width 64: a k-block is one image row): x staged in long rows,
-// as in k_stem_fwd.  Column block q = 3 s + r of the B operand (64 pixels x 8
-// channels, 1 KB) holds tap (r, s): image row h + r - 1 shifted by s - 1
-// pixels, as two 512-byte boxes of [N][H][W * 8] -- 18 copy rows per k-block
-// where nine im2col boxes move 576 rows of 16 bytes.  The epilogue writes
-// block q to tap 3 r + s of dw.
-template <int kRW = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     k_wgrad_c8(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmX,
                const WgradParams p) {
-  static_assert(kRW == 0 || kRW == 64, "row staging for width 64");
   constexpr int S = kWc8Stages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -2726,15 +2717,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();  // the previous kernel's writes are visible from here on
 
   if (warp < kProd) {
-    // boxes per stage: dy halves 0-1 (8 KB); x taps 2-10 (1 KB im2col boxes),
-    // or with row staging 2-19 (512-byte row boxes, two per tap)
+    // boxes per stage: dy halves 0-1 (8 KB); x taps 2-10 (1 KB im2col boxes)
     if (lane == 0) {
-      constexpr int kBoxes = kRW ? 2 + 18 : 11;
+      constexpr int kBoxes = 11;
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
       uint32_t bytes = 0;
-      for (int b = warp; b < kBoxes; b += kProd) bytes += b < 2 ? 8192u : kRW ? 512u : kWc8BlockBytes;
+      for (int b = warp; b < kBoxes; b += kProd) bytes += b < 2 ? 8192u : kWc8BlockBytes;
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
           ok = false;
@@ -2749,11 +2739,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = warp; b < kBoxes; b += kProd) {
           if (b < 2) {
             tma_load_2d(sa + b * 8192, &tmDY, &full[stage], mb * 128 + b * 64, pk);
-          } else if constexpr (kRW != 0) {
-            const int q = (b - 2) >> 1, part = (b - 2) & 1;  // block q = 3 s + r
-            const int sh = q / 3, r = q - 3 * sh;
-            tma_load_3d(sb + q * kWc8BlockBytes + part * 512, &tmX, &full[stage], (sh - 1) * 8 + part * 256,
-                        h0 + r - 1, n0);
           } else {
             const int t = b - 2;
             tma_load_im2col_4d(sb + t * kWc8BlockBytes, &tmX, &full[stage], 0, w0 - 1, h0 - 1, n0,
@@ -2823,13 +2808,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x32(lane_addr + (uint32_t)(j * 32), v);
         tmem_ld_wait();
         if (k < p.Cout) {
-          // column block qb (8 columns) holds tap qb (im2col) or tap 3 (qb % 3) +
-          // qb / 3 (row staging); blocks 9-11 are the zero and ones blocks
+          // column block qb (8 columns) holds tap qb; blocks 9-11 are the zero
+          // and ones blocks
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             const int qb = 4 * j + g;
             if (qb < 9) {
-              const int tap = kRW ? (qb % 3) * 3 + qb / 3 : qb;
+              const int tap = qb;
               reinterpret_cast<float4*>(o + tap * 8)[0] =
                   make_float4(__uint_as_float(v[8 * g]), __uint_as_float(v[8 * g + 1]),
                               __uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
@@ -2840,6 +2825,190 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // column 80 (block 10) is the first ones column: dbias
           if (j == 2) p.part[(long long)p.S * dwsize + (long long)split * p.Cout + k] = __uint_as_float(v[16]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, 128);
+}
+
+// Width 64, x staged as halo rows: x [N][H][64][8] viewed as [N][H][32][16]
+// (pixel pairs), one 4-D box per 64-pixel k-block (one image row h) brings
+// rows h - 1 .. h + 1 at pixels -2 .. 65 (34 pairs; outside the image reads
+// zero) as three contiguous 1088-byte rows, pixel p of row r at r * 1088 +
+// (p + 2) * 16.  In the MN-major no-swizzle layout (8-pixel x 16-byte core
+// matrices) the operand for column shift s starts (s + 1) * 16 bytes into the
+// rows, and its four 8-column blocks are rows 0, 1, 2 and a static ones block
+// one row further: per 16 pixels one M = 128, N = 32 MMA per shift s writes
+// accumulator columns 32 s + 8 r + c for tap (r, s), and column 24 (ones) is
+// dbias.  Three copies per k-block where the 512-byte row boxes take twenty.
+constexpr uint32_t kWhRow = 34 * 32;                          // one staged row of 68 pixels
+constexpr uint32_t kWhX = kWgABytes;                          // x rows after dy
+constexpr uint32_t kWhOnes = kWhX + 3 * kWhRow;               // the ones block, as row 3
+constexpr uint32_t kWhStage = (kWhOnes + kWhRow + 1023) / 1024 * 1024;
+constexpr uint32_t kWhLoad = kWgABytes + 3 * kWhRow;          // bytes copied per k-block
+constexpr int kWhStages = 8;
+constexpr size_t kWhSmem = (size_t)kWhStages * kWhStage + 256 + 1024;
+static_assert(kWhStages >= kProd, "stage-parallel producers need S >= kProd");
+static_assert(kWhX % 128 == 0, "TMA destinations stay 128-byte aligned");
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_wgrad_c8h(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmX,
+                const WgradParams p) {
+  constexpr int S = kWhStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * kWhStage);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* drain = tfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // no early trigger: the dependent is the partials' reduction
+  const int mb = blockIdx.x % p.num_mb;
+  const int split = blockIdx.x / p.num_mb;
+  const int kb0 = split * p.kb_per_split;
+  const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+  const int HW = p.H * p.W;
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmDY);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+  }
+  if (warp >= kEpiBase) {  // every stage's ones block (bf16 1.0 = 0x3F80)
+    const int t = threadIdx.x - 32 * kEpiBase;
+    for (int st = 0; st < S; ++st) {
+      uint4* b = reinterpret_cast<uint4*>(smem + (size_t)st * kWhStage + kWhOnes);
+      for (int i = t; i < (int)(kWhRow / 16); i += 32 * kWgEpiWarps)
+        b[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the previous kernel's writes are visible from here on
+
+  if (warp < kProd) {
+    // whole stages in turn: two dy boxes (64 pixels x 64 channels) and the
+    // three x rows of k-block kb (image row h0 of image n0)
+    if (lane == 0) {
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (issued % kProd == warp) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int pk = kb * kWgPix;
+          const int n0 = pk / HW, h0 = (pk - n0 * HW) / p.W;
+          uint8_t* sa = smem + (size_t)stage * kWhStage;
+          mbar_arrive_expect_tx(&full[stage], kWhLoad);
+          tma_load_2d(sa, &tmDY, &full[stage], mb * 128, pk);
+          tma_load_2d(sa + 8192, &tmDY, &full[stage], mb * 128 + 64, pk);
+          tma_load_4d(sa + kWhX, &tmX, &full[stage], 0, -1, h0 - 1, n0);
+        }
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) {
+        // wait (bounded) for the loads still in flight
+        const int n = issued < S ? issued : S;
+        for (int i = 0; i < n; ++i) {
+          if (--stage < 0) {
+            stage = S - 1;
+            phase ^= 1;
+          }
+          mbar_wait(&full[stage], phase, drain_wait_ns(p.wait_ns), nullptr, nullptr);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 32, 1, 1);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(smem + (size_t)stage * kWhStage);
+        const uint32_t x_base = a_base + kWhX;
+#pragma unroll
+        for (int k = 0; k < kWgPix / 16; ++k) {
+          const uint64_t ad = smem_desc(a_base + k * 2048, 8192, 1024, kSwizzle128B);
+#pragma unroll
+          for (int s = 0; s < 3; ++s)
+            tc_mma_bf16(tmem_base + (uint32_t)(32 * s), ad,
+                        smem_desc(x_base + (uint32_t)((s + 1) * 16 + k * 256), 128, kWhRow, kSwizzleNone),
+                        idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+        }
+        tc_commit(&empty[stage]);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (ok) tc_commit(tfull);
+      tc_commit(drain);
+      mbar_wait(drain, 0, p.wait_ns, nullptr, nullptr);
+    }
+    __syncwarp();
+  } else {
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int k = mb * 128 + row;
+    if (mbar_wait(tfull, 0, p.wait_ns, p.status, abort_flag)) {
+      tc_fence_after();
+      const long long dwsize = (long long)p.Cout * 72;
+      const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+      float* o = p.part + (long long)split * dwsize + (long long)k * 72;
+#pragma unroll 1
+      for (int s = 0; s < 3; ++s) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(lane_addr + (uint32_t)(32 * s), v);
+        tmem_ld_wait();
+        if (k < p.Cout) {
+#pragma unroll
+          for (int r = 0; r < 3; ++r) {
+            const int tap = 3 * r + s;
+            reinterpret_cast<float4*>(o + tap * 8)[0] =
+                make_float4(__uint_as_float(v[8 * r]), __uint_as_float(v[8 * r + 1]),
+                            __uint_as_float(v[8 * r + 2]), __uint_as_float(v[8 * r + 3]));
+            reinterpret_cast<float4*>(o + tap * 8)[1] =
+                make_float4(__uint_as_float(v[8 * r + 4]), __uint_as_float(v[8 * r + 5]),
+                            __uint_as_float(v[8 * r + 6]), __uint_as_float(v[8 * r + 7]));
+          }
+          // column 24 of shift 0 is the first ones column: dbias
+          if (s == 0) p.part[(long long)p.S * dwsize + (long long)split * p.Cout + k] = __uint_as_float(v[24]);
         }
       }
     }
@@ -3109,6 +3278,21 @@ int make_row_map(CUtensorMap* m, const void* base, int N, int H, int W, int elem
   cuuint32_t box[3] = {(cuuint32_t)elems, 1, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
+// 8 channels viewed as pixel pairs, [N][H][W/2][16], for k_wgrad_c8h: one box
+// holds three image rows of W/2 + 2 pairs (a pair of zero pixels each side).
+int make_pair_row_map(CUtensorMap* m, const void* base, int N, int H, int W) {
+  PFN_encodeTiled enc = encode_tiled_fn();
+  if (!enc) return CONV3X3_ERR_CUDA;
+  cuuint64_t dims[4] = {16, (cuuint64_t)W / 2, (cuuint64_t)H, (cuuint64_t)N};
+  cuuint64_t strides[3] = {32, (cuuint64_t)W * 16, (cuuint64_t)H * W * 16};
+  cuuint32_t box[4] = {16, (cuuint32_t)W / 2 + 2, 3, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
@@ -3593,15 +3777,19 @@ size_t tc_wgrad_workspace(const Shape& s, int /*num_sms*/) {
 int run_wgrad_c8(const void* x, const void* dy, float* dw, float* db, const Shape& s, void* ws,
                  const DevCtx& d, cudaStream_t st) {
   WgPlan pl = wg_plan_c8(s);
-  // row staging at width 64 (each 64-pixel k-block is one image row);
-  // CONV3X3_STEM_ROWS=0 keeps im2col boxes
-  bool rows = s.W == 64;
+  // width 64 (each 64-pixel k-block is one image row): x staged as three
+  // halo rows per k-block, one copy; otherwise (or with CONV3X3_STEM_ROWS=0)
+  // as nine im2col boxes.  Measured on the 64x64 batch-64 stem: 28.7 us for
+  // the call against 33.3 us with two 512-byte row boxes per tap and 43 us
+  // with im2col boxes.
+  bool halo = s.W == 64;
   if (const char* e = std::getenv("CONV3X3_STEM_ROWS"))
-    if (std::strcmp(e, "0") == 0) rows = false;
+    if (std::strcmp(e, "0") == 0) halo = false;
   CUtensorMap tdy, tx;
   int rc = make_rows_map(&tdy, dy, s.P(), s.Cout);
   if (rc) return rc;
-  rc = rows ? make_row_map(&tx, x, s.N, s.H, s.W, 256) : make_im2col_map(&tx, x, s.N, s.H, s.W, 8, kWgPix, 8, false);
+  rc = halo ? make_pair_row_map(&tx, x, s.N, s.H, s.W)
+            : make_im2col_map(&tx, x, s.N, s.H, s.W, 8, kWgPix, 8, false);
   if (rc) return rc;
   WgradParams prm;
   prm.part = static_cast<float*>(ws);
@@ -3619,9 +3807,13 @@ int run_wgrad_c8(const void* x, const void* dy, float* dw, float* db, const Shap
   prm.num_cb = 1;
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
-  auto kern = rows ? k_wgrad_c8<64> : k_wgrad_c8<0>;
-  if (set_smem(kern, kWc8Smem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
-  launch_pdl(kern, dim3(pl.tiles * pl.S), dim3(kThreads), kWc8Smem, st, tdy, tx, prm);
+  if (halo) {
+    if (set_smem(k_wgrad_c8h, kWhSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+    launch_pdl(k_wgrad_c8h, dim3(pl.tiles * pl.S), dim3(kThreads), kWhSmem, st, tdy, tx, prm);
+  } else {
+    if (set_smem(k_wgrad_c8, kWc8Smem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+    launch_pdl(k_wgrad_c8, dim3(pl.tiles * pl.S), dim3(kThreads), kWc8Smem, st, tdy, tx, prm);
+  }
   if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
   return launch_wgrad_reduce(prm.part, dw, db, (long long)s.Cout * 72, s.Cout, pl.S, pl.S, st);
 }
