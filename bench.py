@@ -23,8 +23,10 @@ produced its input and returns the gradient through that activation
 (conv3x3_dgrad_act), so no elementwise pass runs between the convolutions.
 
 Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
-launching stream; L2 is flushed (a write of 2x the L2 size) between steps,
-outside the events.  Multi-process runs (torchrun) run one replica per GPU
+launching stream; L2 is flushed between steps, outside the events: a write of
+a buffer twice the L2 size, then a read of a second such buffer, so that the
+dirty lines the write leaves are written back before the timed region starts
+(the timed kernels find L2 cold and clean).  Multi-process runs (torchrun) run one replica per GPU
 (weak scaling); the reported time is the max over ranks.
 
 Beside the step, the line carries the per-layer breakdown of the step
@@ -406,6 +408,27 @@ GATES = (("stem", "hbm", 0.70), ("l1", "tensor", 0.60), ("l2", "tensor", 0.60),
          ("l3", "tensor", 0.60))
 
 
+class L2Flush:
+    """Evicts L2 on the current stream: writes a buffer twice the L2 size, then
+    reads a second one, so that the write's dirty lines reach DRAM here and not
+    inside the next timed region."""
+
+    def __init__(self, device):
+        import torch
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        n = max(2 * l2, 64 << 20) // 4
+        self.w = torch.empty(n, dtype=torch.float32, device=device)
+        self.r = torch.zeros(n, dtype=torch.float32, device=device)
+        self.bytes = 2 * 4 * n
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
+FLUSH_NOTE = "flushed between steps (write of 2x L2, then a read of another 2x L2)"
+
+
 def call_us(stream, flush, fn, warm=3, reps=15):
     """Median device time of fn() (one C ABI call) in microseconds: CUDA events
     on the launching stream around the call only, L2 flushed before each run."""
@@ -413,7 +436,7 @@ def call_us(stream, flush, fn, warm=3, reps=15):
     evs = []
     for r in range(warm + reps):
         with torch.cuda.stream(stream):
-            flush.zero_()
+            flush()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -557,8 +580,7 @@ def cuda_arm(args):
     if args.wgrad_streams > 1:
         wstreams = (stream,) + tuple(torch.cuda.Stream(device=device)
                                      for _ in range(args.wgrad_streams - 1))
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device=device)
+    flush = L2Flush(device)
 
     flops_step = sum(3 * L.flops_per_pass() for L in layers)
     flops_padded = sum(3 * L.flops_per_pass(padded=True) for L in layers)
@@ -616,7 +638,7 @@ def cuda_arm(args):
     torch.cuda.synchronize(device)
     for _ in range(args.steps):
         with torch.cuda.stream(stream):
-            flush.zero_()  # same stream, before the start event: evict L2
+            flush()  # same stream, before the start event: evict L2
             if graph is not None:
                 graph.replay()
                 launches += launches_per_step
@@ -667,7 +689,7 @@ def cuda_arm(args):
         nd = max(3, min(K, 10))
         for _ in range(nd):
             with torch.cuda.stream(stream):
-                flush.zero_()
+                flush()
             run_step(wl, sh, record=record)
             torch.cuda.synchronize(device)
             for k in per_call:
@@ -791,7 +813,7 @@ def cuda_arm(args):
         "data": "synthetic (seeded splitmix64 + Box-Muller normals; no dataset, no trained weights)",
         "config": {"workload": args.workload, "layers": len(layers), "batch": layers[0].N,
                    "layout": "NHWC bf16 activations, KRSC bf16 weights, fp32 accumulate",
-                   "l2": "flushed between steps (write of 2x L2)",
+                   "l2": FLUSH_NOTE,
                    "flops_per_step": flops_step, "flops_per_step_padded_cin": flops_padded,
                    "launch": "stream" if graph is None else "CUDA graph of the step's C ABI calls",
                    "kernel_family": args.path,
@@ -862,8 +884,7 @@ def upfirdn2d_arm(args):
             hx.append(t.pin_memory())
             hy.append(torch.empty((op.N, op.Ho, op.Wo, op.C), dtype=torch.bfloat16).pin_memory())
     bytes_step = sum(op.bytes() for op in ops_)
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device=device)
+    flush = L2Flush(device)
 
     def call(i, x=None, y=None):
         op = ops_[i]
@@ -888,7 +909,7 @@ def upfirdn2d_arm(args):
     evs = []
     for _ in range(args.steps):
         with torch.cuda.stream(stream):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             step()
@@ -943,7 +964,7 @@ def upfirdn2d_arm(args):
         "data": "synthetic (seeded splitmix64 + Box-Muller normals)",
         "config": {"workload": "upfirdn2d", "ops": len(ops_), "batch": ops_[0].N,
                    "filter": "binomial [1,3,3,1] x [1,3,3,1] / 64 (x up^2 when upsampling)",
-                   "bytes_per_step": bytes_step, "l2": "flushed between steps (write of 2x L2)"},
+                   "bytes_per_step": bytes_step, "l2": FLUSH_NOTE},
         "roofline": {"bound": "hbm", "kernel": "k_upfirdn2d (all six ops)",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
