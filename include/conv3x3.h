@@ -61,9 +61,11 @@
  * "pair128", "pair192", "pair256" run 256-pixel x 128/192/256-channel tiles on
  * two-CTA clusters.
  * CONV3X3_PAIR=0|1 forces the two-CTA choice for 256-channel tiles (unset: dgrad
- * and forwards of at least 512 input channels, with two rounds of pair tiles).
+ * and forwards of at least 256 input channels, with two rounds of pair tiles).
  * CONV3X3_KC=1|2 forces the 64-channel chunks per pipeline stage of the im2col
- * kernel (2 for 128x1 tiles unless set).  CONV3X3_WGRAD_SPLITS=<S> forces the
+ * kernel (2 for 128x1 tiles unless set); CONV3X3_PAIR_KC=1 keeps one chunk per
+ * stage in the 256-channel two-CTA tiles (unset: two where the input channels
+ * are a whole number of 128).  CONV3X3_WGRAD_SPLITS=<S> forces the
  * weight gradient's split count (set it before querying the workspace size).
  * CONV3X3_WGRAD_ROWS=0|1 chooses how the weight gradient stages x: im2col
  * boxes per tap (0), or one zero-padded box per image row that all three taps

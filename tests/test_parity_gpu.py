@@ -153,6 +153,23 @@ def test_every_tensor_tile_shape(shape, tile, monkeypatch):
     assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
 
 
+@pytest.mark.parametrize("kc", ["2", "1"], ids=["two_chunks", "one_chunk"])
+@pytest.mark.parametrize("shape", [(1, 72, 200, 6, 11), (2, 256, 256, 8, 8), (1, 192, 320, 5, 7)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_pair_chunks_per_stage(shape, kc, monkeypatch):
+    # CTA-pair tiles with one or two 64-channel chunks per stage (two only where
+    # the chunk count is even: 192 input channels keep one in the forward)
+    monkeypatch.setenv("CONV3X3_TILE", "pair256")
+    monkeypatch.setenv("CONV3X3_PAIR_KC", kc)
+    t = _small(shape, seed=37)
+    x, w, b, dy = dev_tensors(t)
+    y32 = ops.fwd(x, w, b, act=1, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    dx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert rel_err(host(y32), oracle.conv3x3_fwd(t.x, t.w, t.bias, 1)) <= TOL_BF16
+    assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
+
+
 HALO_SHAPES = [
     (2, 64, 64, 16, 16),    # W = 16: one tile = one whole image
     (1, 72, 200, 8, 32),    # W = 32, ragged channel chunk and ragged N tile
@@ -707,7 +724,8 @@ def test_concat_free_convs(shape, path):
 
 
 @pytest.mark.parametrize("tile", ["128x2", "128x2n", "256x1", "256x1n", "pair192"])
-@pytest.mark.parametrize("shape", [(1, 128, 72, 200, 6, 11), (2, 128, 128, 128, 16, 16)],
+@pytest.mark.parametrize("shape", [(1, 128, 72, 200, 6, 11), (2, 128, 128, 128, 16, 16),
+                                   (1, 192, 64, 256, 6, 7)],  # a two-chunk stage across the split
                          ids=lambda s: "x".join(map(str, s)))
 def test_concat_free_256_pixel_tiles(shape, tile, monkeypatch):
     """Split input and split input gradient on the 256-pixel tiles: transposed

@@ -701,27 +701,33 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 // The pair tile is 256 pixels x BN output channels, BN in {128, 192, 256}:
 // each CTA stages BN / 2 weight rows (the forward's K-major box of BN / 2 rows;
 // dgrad's MN-major boxes of 64 channels, the last one partly unused when
-// BN / 2 = 96), the MMA is M = 256, N = BN.
-template <int BN, bool kDgrad>
+// BN / 2 = 96), the MMA is M = 256, N = BN.  KC = 64-channel chunks per stage:
+// with KC = 2 a barrier round trip of the issuing thread covers eight MMAs
+// (1024 cycles of tensor work at N = 256) instead of four; the three 64 KB
+// stages are then filled box-parallel by all producers.
+template <int BN, bool kDgrad, int KC = 1>
 struct PairCfg {
   static constexpr int kHalf = BN / 2;                  // weight rows (output channels) per CTA
   static constexpr int kDgradBoxes = (kHalf + 63) / 64;  // dgrad: 64-channel MN-major boxes
   static constexpr uint32_t kBHalf = kDgrad ? (uint32_t)kDgradBoxes * 8192u : (uint32_t)kHalf * 128u;
-  static constexpr uint32_t kStage = kABytes + kBHalf;  // per CTA
+  static constexpr uint32_t kStage = KC * (kABytes + kBHalf);  // per CTA: KC A boxes, then KC B halves
   static constexpr int kStagesFit = (int)((200u * 1024u) / kStage);
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr bool kSP = kStages >= kProd;  // whole stages per producer, else boxes
   static constexpr size_t kSmem = (size_t)kStages * kStage + 256 + 1024 + kGuardBytes;
   static_assert(BN == 128 || BN == 192 || BN == 256, "pair tiles are 128, 192 or 256 channels wide");
+  static_assert(KC == 1 || KC == 2, "one or two chunks per stage");
   static_assert(kStage % 1024 == 0, "stages must keep 1 KB swizzle alignment");
-  static_assert(kStages >= kProd, "stage-parallel producers need S >= kProd");
+  static_assert(kStages >= 2, "pair stage ring too shallow");
 };
 
-template <bool kDgrad, bool kExt, int BN = 256>
+template <bool kDgrad, bool kExt, int BN = 256, int KC = 1>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
     k_igemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                  const __grid_constant__ CUtensorMap tmB, const IgemmParams p) {
-  using Cfg = PairCfg<BN, kDgrad>;
+  using Cfg = PairCfg<BN, kDgrad, KC>;
   constexpr int S = Cfg::kStages;
+  constexpr bool kSP = Cfg::kSP;
   constexpr int kPairBN = BN;
   constexpr uint32_t kPairStage = Cfg::kStage;
   extern __shared__ uint8_t smem_raw[];
@@ -745,7 +751,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
 
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full[i], kSP ? 1 : kProd);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -774,14 +780,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
 
   if (warp < kProd) {
     // ------------------------------------------------------------ TMA producers
-    // Whole stages in turn: producer `warp` fills stage k-blocks issued % kProd
-    // == warp with this CTA's A box and weight half.
+    // Whole stages in turn (producer `warp` fills the k-blocks issued % kProd
+    // == warp), or with KC = 2 every stage's boxes spread over the producers
+    // (box b by producer b % kProd): per chunk this CTA's A box, then its
+    // weight half.  Rank 0's full barrier counts both CTAs' bytes.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      constexpr uint32_t kPairBytes = 2 * kPairStage;
+      constexpr int kBPer = kDgrad ? Cfg::kDgradBoxes : 1;  // weight boxes per chunk
+      constexpr int kPer = 1 + kBPer;
+      constexpr int kBoxes = KC * kPer;
+      constexpr uint32_t kBBox = kDgrad ? 8192u : Cfg::kBHalf;
+      uint32_t my_bytes = 0;  // box-parallel: this producer's share of a stage
+      for (int b = warp; b < kBoxes; b += kProd) my_bytes += b % kPer == 0 ? kABytes : kBBox;
+      const int kgroups = p.kchunks / KC;
       for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
         const int mt = tile / p.num_n_tiles, nt = tile - mt * p.num_n_tiles;
         const int p0 = mt * 2 * BM + (int)rank * BM;  // this CTA's 128 pixels
@@ -789,29 +803,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
         const int h0 = rem / p.W;
         const int cn = n0, ch = p.ustride * h0 - 1, cw = p.ustride * (rem - h0 * p.W) - 1;
         const int c0 = nt * kPairBN + (int)rank * Cfg::kHalf;  // this CTA's weight rows (output channels)
-        const int kblocks = 9 * p.kchunks;
+        const int kblocks = 9 * kgroups;
         for (int kb = 0; kb < kblocks; ++kb) {
-          const int tap = kb / p.kchunks, cc = kb - tap * p.kchunks;
-          if (issued % kProd == warp) {
+          const int tap = kb / kgroups, cg = (kb - tap * kgroups) * KC;
+          if (!kSP || issued % kProd == warp) {
             if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
               ok = false;
               break;
             }
             uint8_t* sa = smem + (size_t)stage * kPairStage;
-            uint8_t* sb = sa + kABytes;
+            uint8_t* sb = sa + KC * kABytes;
             const uint32_t fb = full0 + (uint32_t)stage * 8u;
-            if (rank == 0) mbar_arrive_expect_tx(&full[stage], kPairBytes);
-            const bool second = cc >= p.kchunks_a;
-            tma_load_im2col_4d_pair(sa, second ? &tmA2 : &tmA, fb,
-                                    (second ? cc - p.kchunks_a : cc) * BKC, cw, ch, cn,
-                                    (uint16_t)(tap % 3), (uint16_t)(tap / 3));
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], kSP ? 2 * kPairStage : 2 * my_bytes);
             const int wtap = kDgrad ? 8 - tap : tap;
-            if (!kDgrad) {
-              tma_load_3d_pair(sb, &tmB, fb, cc * BKC, wtap, c0);
-            } else {
 #pragma unroll
-              for (int j = 0; j < Cfg::kDgradBoxes; ++j)
-                tma_load_3d_pair(sb + j * 8192, &tmB, fb, c0 + j * 64, wtap, cc * BKC);
+            for (int b = 0; b < kBoxes; ++b) {
+              if (!kSP && b % kProd != warp) continue;
+              const int c = b / kPer, r = b - c * kPer, cc = cg + c;
+              if (r == 0) {
+                const bool second = cc >= p.kchunks_a;
+                tma_load_im2col_4d_pair(sa + c * kABytes, second ? &tmA2 : &tmA, fb,
+                                        (second ? cc - p.kchunks_a : cc) * BKC, cw, ch, cn,
+                                        (uint16_t)(tap % 3), (uint16_t)(tap / 3));
+              } else if (!kDgrad) {
+                tma_load_3d_pair(sb + c * Cfg::kBHalf, &tmB, fb, cc * BKC, wtap, c0);
+              } else {
+                const int j = r - 1;
+                tma_load_3d_pair(sb + c * Cfg::kBHalf + j * 8192, &tmB, fb, c0 + j * 64, wtap, cc * BKC);
+              }
             }
           }
           ++issued;
@@ -848,8 +867,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, kPairBN, 0, kDgrad ? 1 : 0);
       const uint32_t sbase = smem_u32(smem);
       const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
-      const uint64_t b_desc0 = kDgrad ? smem_desc(sbase + kABytes, 8192, 1024, kSwizzle128B)
-                                      : smem_desc(sbase + kABytes, 16, 1024, kSwizzle128B);
+      const uint64_t b_desc0 = kDgrad ? smem_desc(sbase + KC * kABytes, 8192, 1024, kSwizzle128B)
+                                      : smem_desc(sbase + KC * kABytes, 16, 1024, kSwizzle128B);
       constexpr uint32_t kStageStep = kPairStage >> 4;
       constexpr uint32_t kBKStep = (kDgrad ? 2048u : 32u) >> 4;
       constexpr uint32_t kAKStep = 32u >> 4;
@@ -862,7 +881,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
         if (!mbar_wait(&tempty[buf], acc_phase ^ 1, p.wait_ns, p.status, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kPairBN);
-        const int kblocks = 9 * p.kchunks;
+        const int kblocks = 9 * (p.kchunks / KC);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) {
             ok = false;
@@ -871,9 +890,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
           tc_fence_after();
           const uint64_t ad = a_desc0 + stage_off, bd = b_desc0 + stage_off;
 #pragma unroll
-          for (int k = 0; k < BKC / 16; ++k)
-            tc_mma_bf16_pair(d_tmem, ad + (uint64_t)(k * kAKStep), bd + (uint64_t)(k * kBKStep), idesc,
-                             (kb != 0 || k != 0) ? 1u : 0u);
+          for (int c = 0; c < KC; ++c)
+#pragma unroll
+            for (int k = 0; k < BKC / 16; ++k)
+              tc_mma_bf16_pair(d_tmem, ad + (uint64_t)(c * (kABytes >> 4) + k * kAKStep),
+                               bd + (uint64_t)(c * (Cfg::kBHalf >> 4) + k * kBKStep), idesc,
+                               (kb != 0 || c != 0 || k != 0) ? 1u : 0u);
           tc_commit_pair_mc(&empty[stage], (uint16_t)0x3);
           stage_off += kStageStep;
           if (++stage == S) {
@@ -3163,12 +3185,12 @@ int pair_slots(K kernel, size_t smem, const DevCtx& d) {
   return n;
 }
 
-template <bool kDgrad, int BN>
+template <bool kDgrad, int BN, int KC = 1>
 int launch_igemm_pair(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
                       const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
-  using Cfg = PairCfg<BN, kDgrad>;
+  using Cfg = PairCfg<BN, kDgrad, KC>;
   const bool ext = prm.zout || prm.zin || prm.out2;
-  auto kern = ext ? k_igemm_pair<kDgrad, true, BN> : k_igemm_pair<kDgrad, false, BN>;
+  auto kern = ext ? k_igemm_pair<kDgrad, true, BN, KC> : k_igemm_pair<kDgrad, false, BN, KC>;
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
   const int pairs = pair_slots(kern, Cfg::kSmem, d);
@@ -3465,9 +3487,10 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   TileShape ts = pick_tile(nout, dgrad ? s : g, d.num_sms);
   // 128-channel x 256-pixel tiles run transposed (k_igemm kT) unless the
   // override names "128x2n".  256-channel tiles run on CTA pairs
-  // (k_igemm_pair) where that measured faster: dgrad, or a forward with a long
-  // K (at least eight 64-channel chunks), and at least two rounds of pair
-  // tiles (a 256-pixel pair tile halves the tile count, so small grids lose).
+  // (k_igemm_pair) where that measured faster: dgrad, or a forward of at least
+  // four 64-channel chunks (256 -> 256 channels at 32x32: 61 instead of 65 us
+  // with two chunks per pair stage), and at least two rounds of pair tiles (a
+  // 256-pixel pair tile halves the tile count, so small grids lose).
   // CONV3X3_PAIR=0|1 or the override "256x1" / "256x1n" forces the choice.
   bool trans = true;
   int pair_force = -1, pair_bn = 0;
@@ -3551,7 +3574,7 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   }
   const long long pair_tiles = (g.P() + 2 * BM - 1) / (2 * BM) * prm.num_n_tiles;
   const bool pair = pair_force >= 0 ? pair_force == 1
-                                    : ((dgrad || prm.kchunks >= 8) && pair_tiles >= d.num_sms);
+                                    : ((dgrad || prm.kchunks >= 4) && pair_tiles >= d.num_sms);
   if (pair_bn == 0 && pair && bn == 256 && ts.mt == 1) pair_bn = 256;
   if (pair_bn && !s2) {
     // a pair tile is 256 pixels (128 per CTA) x pair_bn channels, each CTA
@@ -3562,12 +3585,18 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
       rc = make_weight_map(&tb, w, s.Cin, s.Cout, pair_bn / 2);
       if (rc) return rc;
     }
-#define C3_PAIR(BN_)                                                                   \
-  return dgrad ? launch_igemm_pair<true, BN_>(ta, ta2, tb, prm, d, st)                 \
-               : launch_igemm_pair<false, BN_>(ta, ta2, tb, prm, d, st)
-    if (pair_bn == 128) C3_PAIR(128);
-    if (pair_bn == 192) C3_PAIR(192);
-    C3_PAIR(256);
+#define C3_PAIR(BN_, KC_)                                                              \
+  return dgrad ? launch_igemm_pair<true, BN_, KC_>(ta, ta2, tb, prm, d, st)            \
+               : launch_igemm_pair<false, BN_, KC_>(ta, ta2, tb, prm, d, st)
+    if (pair_bn == 128) C3_PAIR(128, 1);
+    if (pair_bn == 192) C3_PAIR(192, 1);
+    // two 64-channel chunks per stage where K is a whole number of them;
+    // CONV3X3_PAIR_KC=1 keeps one
+    int pkc = prm.kchunks % 2 == 0 ? 2 : 1;
+    if (const char* e = std::getenv("CONV3X3_PAIR_KC"))
+      if (std::strcmp(e, "1") == 0) pkc = 1;
+    if (pkc == 2) C3_PAIR(256, 2);
+    C3_PAIR(256, 1);
 #undef C3_PAIR
   }
   // Two 64-channel chunks per k-block where the tile's MMAs are short (see
