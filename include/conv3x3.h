@@ -58,8 +58,10 @@
  * "128x2" runs transposed (weights as the M = 128 operand, 256 pixels as N) and
  * "128x2n" untransposed; "256x1" runs on two-CTA clusters (one 256-pixel x
  * 256-channel tile per pair, tcgen05 cta_group::2) and "256x1n" on one CTA;
- * "pair128", "pair192", "pair256" run 256-pixel x 128/192/256-channel tiles on
- * two-CTA clusters.
+ * "pair128", "pair192", "pair256", "pair384" run 256-pixel x 128/192/256/384-
+ * channel tiles on two-CTA clusters.  CONV3X3_PAIR384=0 keeps 384-channel
+ * outputs off the 384-wide two-CTA tile (unset: taken with at least six input
+ * chunks and enough 256-pixel tiles to fill 3/8 of the GPU in one round).
  * CONV3X3_PAIR=0|1 forces the two-CTA choice for 256-channel tiles (unset: dgrad
  * and forwards of at least 256 input channels, with two rounds of pair tiles).
  * CONV3X3_KC=1|2 forces the 64-channel chunks per pipeline stage of the im2col

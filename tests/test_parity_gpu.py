@@ -136,7 +136,7 @@ def test_small_shapes_all_passes(shape, path):
 # "256x1" runs on two-CTA clusters (one 256-pixel x 256-channel tile per pair), "256x1n" on
 # one CTA; "pair<BN>" runs 256-pixel x BN-channel tiles on two-CTA clusters
 TILES = ["64x1", "128x1", "192x1", "256x1", "256x1n", "64x2", "128x2", "128x2n",
-         "pair128", "pair192", "pair256"]
+         "pair128", "pair192", "pair256", "pair384"]
 
 
 @pytest.mark.parametrize("tile", TILES)
@@ -167,6 +167,31 @@ def test_pair_chunks_per_stage(shape, kc, monkeypatch):
     dx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
     torch.cuda.synchronize()
     assert rel_err(host(y32), oracle.conv3x3_fwd(t.x, t.w, t.bias, 1)) <= TOL_BF16
+    assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
+
+
+@pytest.mark.parametrize("pair384", ["auto", "0"], ids=["pair384", "one_cta"])
+@pytest.mark.parametrize("shape", [(2, 384, 384, 16, 16), (1, 256, 384, 16, 16), (3, 128, 384, 9, 13),
+                                   (1, 896, 384, 8, 8)], ids=lambda s: "x".join(map(str, s)))
+def test_384_channel_tiles(shape, pair384, monkeypatch):
+    # 256 x 384 two-CTA tiles (which the full-size 16x16 layers take by
+    # default; forced here) against the one-CTA tiles
+    if pair384 == "0":
+        monkeypatch.setenv("CONV3X3_PAIR384", "0")
+    else:
+        monkeypatch.setenv("CONV3X3_TILE", "pair384")
+    t = _small(shape, seed=41)
+    x, w, b, dy = dev_tensors(t)
+    for act in (1, 2):
+        y32 = ops.fwd(x, w, b, act=act, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+        ybf = ops.fwd(x, w, b, act=act, path=L.PATH_TENSOR)
+        torch.cuda.synchronize()
+        ref = oracle.conv3x3_fwd(t.x, t.w, t.bias, act)
+        assert rel_err(host(y32), ref) <= TOL_BF16
+        assert np.array_equal(host(ybf), rne_bf16(host(y32)))
+    # dgrad: 384 outputs where Cin = 384
+    dx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
     assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
 
 
@@ -312,7 +337,7 @@ def test_fused_activation_backward(shape, path):
 
 
 @pytest.mark.parametrize("tile", ["64x2", "256x1", "256x1n", "halo64", "128x2", "128x2n", "pair128",
-                                  "pair192"])
+                                  "pair192", "pair384"])
 def test_fused_activation_backward_tiles(tile, monkeypatch):
     monkeypatch.setenv("CONV3X3_TILE", tile)
     shape = (2, 64, 128, 16, 16)
@@ -723,7 +748,7 @@ def test_concat_free_convs(shape, path):
     assert torch.equal(dw, dw_plain) and torch.equal(db, db_plain)
 
 
-@pytest.mark.parametrize("tile", ["128x2", "128x2n", "256x1", "256x1n", "pair192"])
+@pytest.mark.parametrize("tile", ["128x2", "128x2n", "256x1", "256x1n", "pair192", "pair384"])
 @pytest.mark.parametrize("shape", [(1, 128, 72, 200, 6, 11), (2, 128, 128, 128, 16, 16),
                                    (1, 192, 64, 256, 6, 7)],  # a two-chunk stage across the split
                          ids=lambda s: "x".join(map(str, s)))

@@ -705,17 +705,27 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 // with KC = 2 a barrier round trip of the issuing thread covers eight MMAs
 // (1024 cycles of tensor work at N = 256) instead of four; the three 64 KB
 // stages are then filled box-parallel by all producers.
+//
+// BN = 384 (one accumulator, 384 of the 512 TMEM columns): two M = 256,
+// N = 192 MMAs per K step.  CTA r stages output channels [96 r, 96 r + 96) as
+// its weight rows 0-95 and [192 + 96 r, 192 + 96 r + 96) as rows 96-191, so
+// the first MMA (rows 0-95 of both CTAs) writes accumulator columns 0-191 and
+// the second (rows 96-191) columns 192-383: column = channel of the tile.  The
+// forward loads two 96-row K-major boxes, dgrad two pairs of 64-channel
+// MN-major boxes (the second of each pair half used).
 template <int BN, bool kDgrad, int KC = 1>
 struct PairCfg {
   static constexpr int kHalf = BN / 2;                  // weight rows (output channels) per CTA
-  static constexpr int kDgradBoxes = (kHalf + 63) / 64;  // dgrad: 64-channel MN-major boxes
+  static constexpr int kDgradBoxes = BN == 384 ? 4 : (kHalf + 63) / 64;  // dgrad: MN-major boxes
   static constexpr uint32_t kBHalf = kDgrad ? (uint32_t)kDgradBoxes * 8192u : (uint32_t)kHalf * 128u;
+  static constexpr int kBufs = 2 * BN <= 512 ? 2 : 1;    // TMEM accumulators
   static constexpr uint32_t kStage = KC * (kABytes + kBHalf);  // per CTA: KC A boxes, then KC B halves
   static constexpr int kStagesFit = (int)((200u * 1024u) / kStage);
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr bool kSP = kStages >= kProd;  // whole stages per producer, else boxes
   static constexpr size_t kSmem = (size_t)kStages * kStage + 256 + 1024 + kGuardBytes;
-  static_assert(BN == 128 || BN == 192 || BN == 256, "pair tiles are 128, 192 or 256 channels wide");
+  static_assert(BN == 128 || BN == 192 || BN == 256 || BN == 384, "pair tiles are 128 .. 384 channels wide");
+  static_assert(BN != 384 || KC == 1, "384-channel pair tiles take one chunk per stage");
   static_assert(KC == 1 || KC == 2, "one or two chunks per stage");
   static_assert(kStage % 1024 == 0, "stages must keep 1 KB swizzle alignment");
   static_assert(kStages >= 2, "pair stage ring too shallow");
@@ -825,6 +835,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
                 tma_load_im2col_4d_pair(sa + c * kABytes, second ? &tmA2 : &tmA, fb,
                                         (second ? cc - p.kchunks_a : cc) * BKC, cw, ch, cn,
                                         (uint16_t)(tap % 3), (uint16_t)(tap / 3));
+              } else if constexpr (BN == 384) {
+                // rows [96 rank, +96) then [192 + 96 rank, +96) of the tile's channels
+                const int cb = nt * kPairBN + (int)rank * 96;
+                if (!kDgrad) {
+                  tma_load_3d_pair(sb, &tmB, fb, cc * BKC, wtap, cb);
+                  tma_load_3d_pair(sb + 96 * 128, &tmB, fb, cc * BKC, wtap, cb + 192);
+                } else {
+                  const int j = r - 1;  // boxes at cb, cb + 64, cb + 192, cb + 256
+                  tma_load_3d_pair(sb + j * 8192, &tmB, fb, cb + (j >> 1) * 192 + (j & 1) * 64, wtap, cc * BKC);
+                }
               } else if (!kDgrad) {
                 tma_load_3d_pair(sb + c * Cfg::kBHalf, &tmB, fb, cc * BKC, wtap, c0);
               } else {
@@ -864,7 +884,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer (rank 0)
     if (rank == 0 && lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, kPairBN, 0, kDgrad ? 1 : 0);
+      constexpr int kMmaN = BN == 384 ? 192 : kPairBN;  // two N = 192 MMAs per K step at BN = 384
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, kMmaN, 0, kDgrad ? 1 : 0);
+      // the second MMA's weight rows: 96 K-major rows on, or two 8 KB boxes on
+      constexpr uint32_t kB2 = (kDgrad ? 2u * 8192u : 96u * 128u) >> 4;
       const uint32_t sbase = smem_u32(smem);
       const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
       const uint64_t b_desc0 = kDgrad ? smem_desc(sbase + KC * kABytes, 8192, 1024, kSwizzle128B)
@@ -892,10 +915,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
 #pragma unroll
           for (int c = 0; c < KC; ++c)
 #pragma unroll
-            for (int k = 0; k < BKC / 16; ++k)
+            for (int k = 0; k < BKC / 16; ++k) {
+              const uint32_t acc = (kb != 0 || c != 0 || k != 0) ? 1u : 0u;
               tc_mma_bf16_pair(d_tmem, ad + (uint64_t)(c * (kABytes >> 4) + k * kAKStep),
-                               bd + (uint64_t)(c * (Cfg::kBHalf >> 4) + k * kBKStep), idesc,
-                               (kb != 0 || c != 0 || k != 0) ? 1u : 0u);
+                               bd + (uint64_t)(c * (Cfg::kBHalf >> 4) + k * kBKStep), idesc, acc);
+              if constexpr (BN == 384)
+                tc_mma_bf16_pair(d_tmem + 192, ad + (uint64_t)(k * kAKStep), bd + (uint64_t)(kB2 + k * kBKStep),
+                                 idesc, acc);
+            }
           tc_commit_pair_mc(&empty[stage], (uint16_t)0x3);
           stage_off += kStageStep;
           if (++stage == S) {
@@ -906,7 +933,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
         }
         if (!ok) break;
         tc_commit_pair_mc(&tfull[buf], (uint16_t)0x3);
-        if (++buf == 2) {
+        if (++buf == Cfg::kBufs) {
           buf = 0;
           acc_phase ^= 1;
         }
@@ -954,7 +981,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty0 + (uint32_t)buf * 8u);
-      if (++buf == 2) {
+      if (++buf == Cfg::kBufs) {
         buf = 0;
         acc_phase ^= 1;
       }
@@ -3501,7 +3528,7 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
     if (std::strcmp(e, "256x1n") == 0) pair_force = 0;
     if (std::strcmp(e, "256x1") == 0) pair_force = 1;
     int pb = 0;
-    if (std::sscanf(e, "pair%d", &pb) == 1 && (pb == 128 || pb == 192 || pb == 256)) pair_bn = pb;
+    if (std::sscanf(e, "pair%d", &pb) == 1 && (pb == 128 || pb == 192 || pb == 256 || pb == 384)) pair_bn = pb;
     int bn_o = 0, mt_o = 0;
     const bool halo_ok = (s.W == 16 || s.W == 32 || s.W == 64) && s.H % (256 / s.W) == 0;
     if (std::sscanf(e, "halo%d", &bn_o) == 1 && halo_ok && (bn_o == 64 || bn_o == 128))
@@ -3576,13 +3603,25 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   const bool pair = pair_force >= 0 ? pair_force == 1
                                     : ((dgrad || prm.kchunks >= 4) && pair_tiles >= d.num_sms);
   if (pair_bn == 0 && pair && bn == 256 && ts.mt == 1) pair_bn = 256;
+  // 384 output channels whose 256-pixel x 384-channel pair tiles fill most of
+  // the GPU in one round, with a K of at least six 64-channel chunks: one tile
+  // per cluster, two N = 192 MMAs per K step.  Measured on GB300 (batch 64,
+  // 16x16): 896 -> 384 forward 79.6 -> 71.5 us, 384 -> 384 dgrad 40.8 -> 38.9
+  // us against 128 x 192 one-CTA tiles; 256 -> 384 (four chunks) and 16 pair
+  // tiles (8x8) ran slower.  CONV3X3_PAIR384=0 keeps the tile choice above.
+  const long long tiles384 = (g.P() + 2 * BM - 1) / (2 * BM);
+  bool p384 = pair_bn == 0 && pair_force != 0 && nout == 384 && tiles384 <= d.num_sms / 2 &&
+              tiles384 * 8 >= 3LL * d.num_sms && prm.kchunks >= 6;
+  if (const char* e = std::getenv("CONV3X3_PAIR384"))
+    if (std::strcmp(e, "0") == 0) p384 = false;
+  if (p384) pair_bn = 384;
   if (pair_bn && !s2) {
     // a pair tile is 256 pixels (128 per CTA) x pair_bn channels, each CTA
-    // loading pair_bn / 2 weight rows
+    // loading pair_bn / 2 weight rows (as two 96-row boxes at 384)
     prm.num_m_tiles = (int)((g.P() + 2 * BM - 1) / (2 * BM));
     prm.num_n_tiles = (nout + pair_bn - 1) / pair_bn;
     if (!dgrad) {  // (dgrad's map already has 64-row boxes)
-      rc = make_weight_map(&tb, w, s.Cin, s.Cout, pair_bn / 2);
+      rc = make_weight_map(&tb, w, s.Cin, s.Cout, pair_bn == 384 ? 96 : pair_bn / 2);
       if (rc) return rc;
     }
 #define C3_PAIR(BN_, KC_)                                                              \
@@ -3590,6 +3629,7 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
                : launch_igemm_pair<false, BN_, KC_>(ta, ta2, tb, prm, d, st)
     if (pair_bn == 128) C3_PAIR(128, 1);
     if (pair_bn == 192) C3_PAIR(192, 1);
+    if (pair_bn == 384) C3_PAIR(384, 1);
     // two 64-channel chunks per stage where K is a whole number of them;
     // CONV3X3_PAIR_KC=1 keeps one
     int pkc = prm.kchunks % 2 == 0 ? 2 : 1;
