@@ -62,6 +62,10 @@
  * channel tiles on two-CTA clusters.  CONV3X3_PAIR384=0 keeps 384-channel
  * outputs off the 384-wide two-CTA tile (unset: taken with at least six input
  * chunks and enough 256-pixel tiles to fill 3/8 of the GPU in one round).
+ * CONV3X3_KSPLIT=0|1 forces (or forbids) 128 x 256 tiles whose K is split over
+ * a two-CTA cluster and summed through distributed shared memory (outputs a
+ * multiple of 256 channels; unset: where such tiles fill a quarter to all of
+ * the GPU in pairs and the input has at least 1024 channels).
  * CONV3X3_PAIR=0|1 forces the two-CTA choice for 256-channel tiles (unset: dgrad
  * and forwards of at least 256 input channels, with two rounds of pair tiles).
  * CONV3X3_KC=1|2 forces the 64-channel chunks per pipeline stage of the im2col

@@ -195,6 +195,56 @@ def test_384_channel_tiles(shape, pair384, monkeypatch):
     assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
 
 
+KSPLIT_SHAPES = [
+    # N, Cin, Cout, H, W: 256-channel output tiles whose K is split over a CTA pair
+    (2, 128, 256, 8, 8),
+    (1, 72, 512, 5, 7),      # ragged chunk, ragged pixel tail, two channel tiles
+    (3, 512, 256, 8, 8),     # long K
+    (1, 64, 256, 3, 3),      # nine k-blocks: five and four per CTA
+]
+
+
+@pytest.mark.parametrize("ks", ["1", "0"], ids=["ksplit", "plain"])
+@pytest.mark.parametrize("shape", KSPLIT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_k_split_tiles(shape, ks, monkeypatch):
+    monkeypatch.setenv("CONV3X3_KSPLIT", ks)
+    t = _small(shape, seed=43)
+    x, w, b, dy = dev_tensors(t)
+    for act in (1, 2):
+        y32 = ops.fwd(x, w, b, act=act, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+        ybf = ops.fwd(x, w, b, act=act, path=L.PATH_TENSOR)
+        y32b = ops.fwd(x, w, b, act=act, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+        torch.cuda.synchronize()
+        assert rel_err(host(y32), oracle.conv3x3_fwd(t.x, t.w, t.bias, act)) <= TOL_BF16
+        assert np.array_equal(host(ybf), rne_bf16(host(y32)))
+        assert torch.equal(y32, y32b)  # the cross-CTA sum is deterministic
+    # dgrad needs Cin a multiple of 256 for this tile; the others take the plain kernels
+    dx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
+
+
+def test_k_split_fused_and_concat(monkeypatch):
+    # the fused activation backward and the concat-free calls on K-split tiles
+    monkeypatch.setenv("CONV3X3_KSPLIT", "1")
+    shape = (2, 192, 64, 256, 6, 7)  # N, Ca, Cb, Cout, H, W: a chunk pair across the split
+    N, Ca, Cb, Cout, H, W = shape
+    t, zin_h, _ = _cat_case(shape)
+    x, w, b, dy = dev_tensors(t)
+    xa, xb = x[..., :Ca].contiguous(), x[..., Ca:].contiguous()
+    y32 = ops.fwd_cat(xa, xb, w, b, act=1, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert rel_err(host(y32), oracle.conv3x3_fwd_cat(t.x[..., :Ca], t.x[..., Ca:], t.w, t.bias, 1)) <= TOL_BF16
+    zin = to_dev_bf16(zin_h)
+    za, zb = zin[..., :Ca].contiguous(), zin[..., Ca:].contiguous()
+    gxa, gxb = ops.dgrad_cat(dy, w, Ca, out_dtype=L.DT_F32, path=L.PATH_TENSOR, za_in=za, zb_in=zb,
+                             act_in=1)
+    torch.cuda.synchronize()
+    ref = oracle.conv3x3_dgrad_act(t.dy, t.w, zin_h, 1)
+    got = np.concatenate([host(gxa), host(gxb)], axis=-1)
+    assert rel_err(got, ref) <= TOL_BF16
+
+
 HALO_SHAPES = [
     (2, 64, 64, 16, 16),    # W = 16: one tile = one whole image
     (1, 72, 200, 8, 32),    # W = 32, ragged channel chunk and ragged N tile

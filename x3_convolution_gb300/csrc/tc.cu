@@ -995,6 +995,224 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
 }
 
 // ----------------------------------------------------------------------------
+// forward / dgrad with each tile's K split over a two-CTA cluster
+// ----------------------------------------------------------------------------
+// For grids that leave most of the GPU idle with 256-channel tiles (the 8x8
+// layers: 4096 pixels x 512 channels are 64 tiles of 128 x 256).  A cluster of
+// two CTAs owns one 128-pixel x 256-channel tile; rank r runs k-blocks
+// [r h, r h + h) of its K (h = half the 9 x chunks k-blocks) with one-CTA
+// N = 256 MMAs -- four per barrier round trip of the issuing thread where the
+// 128 x 128 tiles these grids otherwise take issue eight N = 128 MMAs -- into a
+// 256-column accumulator.  The two accumulators are then added through
+// distributed shared memory: each CTA writes the 128 columns the peer stores
+// into the peer's (then idle) stage memory, as [column / 4][pixel] float4s so
+// that a warp's 16-byte stores and loads are contiguous, and each CTA adds the
+// received half to its own and stores it.  Both CTAs add the same two fp32
+// values, so the result does not depend on which one stores a column.  Two
+// cluster barriers, passed by every thread on every path (an aborted role
+// still reaches them), order the exchange.
+constexpr int kKsBN = 256;
+constexpr uint32_t kKsStage = kABytes + kKsBN * 128;  // 128-pixel A box + 256 weight rows x 64 channels
+constexpr int kKsStages = 4;
+constexpr uint32_t kKsXchg = 128u * 128u * 4u;        // 128 pixels x 128 fp32 columns
+constexpr size_t kKsSmem = (size_t)kKsStages * kKsStage + 256 + 1024 + kGuardBytes;
+static_assert(kKsXchg <= (uint32_t)kKsStages * kKsStage, "the exchange reuses the stage memory");
+static_assert(kKsStages >= kProd, "stage-parallel producers need S >= kProd");
+
+template <bool kDgrad, bool kExt>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
+    k_igemm_ks(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+               const __grid_constant__ CUtensorMap tmB, const IgemmParams p) {
+  constexpr int S = kKsStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * kKsStage);
+  uint64_t* empty = full + S;
+  uint64_t* drain = empty + S;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  const uint32_t rank = cluster_ctarank();
+  const int tile = blockIdx.x >> 1;
+  const int mt = tile / p.num_n_tiles, nt = tile - mt * p.num_n_tiles;
+  const int HW = p.H * p.W;
+  const int kb_total = 9 * p.kchunks;
+  const int kb_half = (kb_total + 1) / 2;
+  const int kb0 = (int)rank * kb_half;
+  const int kb1 = min(kb_total, kb0 + kb_half);
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    if (p.kchunks_a < p.kchunks) tma_prefetch_desc(&tmA2);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, kKsBN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the previous kernel's writes are visible from here on
+
+  if (warp < kProd) {
+    // whole stages in turn: the A box and the weight tile (one 256-row box,
+    // or four 64-channel MN-major boxes for dgrad)
+    if (lane == 0) {
+      const int p0 = mt * BM;
+      const int n0 = p0 / HW, rem = p0 - n0 * HW;
+      const int h0 = rem / p.W;
+      const int cn = n0, ch = p.ustride * h0 - 1, cw = p.ustride * (rem - h0 * p.W) - 1;
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (issued % kProd == warp) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int tap = kb / p.kchunks, cc = kb - tap * p.kchunks;
+          uint8_t* sa = smem + (size_t)stage * kKsStage;
+          uint8_t* sb = sa + kABytes;
+          mbar_arrive_expect_tx(&full[stage], kKsStage);
+          const bool second = cc >= p.kchunks_a;
+          tma_load_im2col_4d(sa, second ? &tmA2 : &tmA, &full[stage], (second ? cc - p.kchunks_a : cc) * BKC, cw,
+                             ch, cn, (uint16_t)(tap % 3), (uint16_t)(tap / 3));
+          const int wtap = kDgrad ? 8 - tap : tap;
+          if (!kDgrad) {
+            tma_load_3d(sb, &tmB, &full[stage], cc * BKC, wtap, nt * kKsBN);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kKsBN / 64; ++j)
+              tma_load_3d(sb + j * 8192, &tmB, &full[stage], nt * kKsBN + j * 64, wtap, cc * BKC);
+          }
+        }
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) {
+        int n = issued < S ? issued : S;
+        for (int i = 0; i < n; ++i) {
+          if (--stage < 0) {
+            stage = S - 1;
+            phase ^= 1;
+          }
+          mbar_wait(&full[stage], phase, drain_wait_ns(p.wait_ns), nullptr, nullptr);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, kKsBN, 0, kDgrad ? 1 : 0);
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
+      const uint64_t b_desc0 = kDgrad ? smem_desc(sbase + kABytes, 8192, 1024, kSwizzle128B)
+                                      : smem_desc(sbase + kABytes, 16, 1024, kSwizzle128B);
+      constexpr uint32_t kStageStep = kKsStage >> 4;
+      constexpr uint32_t kBKStep = (kDgrad ? 2048u : 32u) >> 4;
+      constexpr uint32_t kAKStep = 32u >> 4;
+      int stage = 0;
+      uint32_t phase = 0, stage_off = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) break;
+        tc_fence_after();
+        const uint64_t ad = a_desc0 + stage_off, bd = b_desc0 + stage_off;
+#pragma unroll
+        for (int k = 0; k < BKC / 16; ++k)
+          tc_mma_bf16(tmem_base, ad + (uint64_t)(k * kAKStep), bd + (uint64_t)(k * kBKStep), idesc,
+                      (kb != kb0 || k != 0) ? 1u : 0u);
+        tc_commit(&empty[stage]);
+        stage_off += kStageStep;
+        if (++stage == S) {
+          stage = 0;
+          stage_off = 0;
+          phase ^= 1;
+        }
+      }
+      // every MMA has completed before the cluster barrier below
+      tc_commit(drain);
+      mbar_wait(drain, 0, p.wait_ns, nullptr, nullptr);
+    }
+    __syncwarp();
+  }
+
+  // both CTAs' accumulators are complete and their stage memory idle
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const int ew = warp - kEpiBase;
+  const int q = warp & 3;
+  const int hw = (ew >> 2) & 1;  // which 64 of the CTA's 128 exchanged / stored columns
+  const int row = q * 32 + lane;
+  const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+  const bool run = warp >= kEpiBase && !*abort_flag;
+  if (run) {
+    // send the peer's columns [128 (rank ^ 1) + 64 hw, +64) into its stage memory
+    const uint32_t peer_buf = cluster_addr(smem, rank ^ 1u);
+#pragma unroll 1
+    for (int j = 0; j < 2; ++j) {
+      const int cl = hw * 64 + j * 32;  // column within the peer's half
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(lane_addr + (uint32_t)(128 * (rank ^ 1u) + cl), v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        st_cluster_v4(peer_buf + (uint32_t)(((cl / 4 + g) * 128 + row) * 16), v[4 * g], v[4 * g + 1], v[4 * g + 2],
+                      v[4 * g + 3]);
+    }
+  }
+  // the received columns are visible once every thread passes here
+  __syncwarp();
+  cluster_sync();
+  if (run) {
+    const long long pix = (long long)mt * BM + row;
+    const bool valid = pix < p.P;
+    const uint4* recv = reinterpret_cast<const uint4*>(smem);
+#pragma unroll 1
+    for (int j = 0; j < 2; ++j) {
+      const int cl = hw * 64 + j * 32;  // column within this CTA's half
+      const int col0 = nt * kKsBN + 128 * (int)rank + cl;
+      const bool live = valid && col0 < p.nout;
+      float bv[32];
+      if (p.bias && live) load_bias(p, col0, bv);
+      uint4 zr[4] = {};
+      if (kExt && p.zin && live) load_zin(p, pix, col0, zr);
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(lane_addr + (uint32_t)(128 * rank + cl), v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const uint4 r = recv[(cl / 4 + g) * 128 + row];
+        v[4 * g] = __float_as_uint(__uint_as_float(v[4 * g]) + __uint_as_float(r.x));
+        v[4 * g + 1] = __float_as_uint(__uint_as_float(v[4 * g + 1]) + __uint_as_float(r.y));
+        v[4 * g + 2] = __float_as_uint(__uint_as_float(v[4 * g + 2]) + __uint_as_float(r.z));
+        v[4 * g + 3] = __float_as_uint(__uint_as_float(v[4 * g + 3]) + __uint_as_float(r.w));
+      }
+      if (live) store_chunk<kExt>(p, pix, col0, v, bv, zr);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem_base, kKsBN);
+}
+
+// ----------------------------------------------------------------------------
 // forward / dgrad implicit GEMM, halo variant (image widths 16, 32, 64)
 // ----------------------------------------------------------------------------
 // A CTA tile is R = 256 / W whole image rows (256 output pixels, two 128-row
@@ -3226,6 +3444,17 @@ int launch_igemm_pair(const CUtensorMap& a, const CUtensorMap& a2, const CUtenso
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
+template <bool kDgrad>
+int launch_igemm_ks(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
+                    const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
+  const bool ext = prm.zout || prm.zin || prm.out2;
+  auto kern = ext ? k_igemm_ks<kDgrad, true> : k_igemm_ks<kDgrad, false>;
+  if (set_smem(kern, kKsSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+  const int grid = 2 * prm.num_m_tiles * prm.num_n_tiles;  // one tile per cluster
+  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), kKsSmem, st, a, a2, b, prm);
+  return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
 template <int W_, int BN, bool kDgrad>
 int launch_halo(const CUtensorMap& a, const CUtensorMap& b, const IgemmParams& prm,
                 const DevCtx& d, cudaStream_t st) {
@@ -3615,6 +3844,28 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   if (const char* e = std::getenv("CONV3X3_PAIR384"))
     if (std::strcmp(e, "0") == 0) p384 = false;
   if (p384) pair_bn = 384;
+  // K split over two-CTA clusters (k_igemm_ks) where 128 x 256 tiles fill
+  // between a quarter and all of the GPU's SMs in pairs and K is long: the
+  // 8x8 layers with 1024 input channels.  Measured on GB300 (batch 64, 8x8):
+  // 1024 -> 512 forward 41.3 -> 39.2 us against 128 x 128 one-CTA tiles, but
+  // 512 -> 512 forward 25.4 -> 26.3 us (each CTA still streams 48 KB per
+  // k-block, and the fill and the exchange weigh more at short K).
+  // CONV3X3_KSPLIT=0|1 forces the choice (1 still needs a multiple of 256
+  // output channels).
+  const long long ks_tiles = (g.P() + BM - 1) / BM * ((nout + kKsBN - 1) / kKsBN);
+  bool ks = !s2 && !ts.halo && pair_bn == 0 && nout % kKsBN == 0 && 2 * ks_tiles <= d.num_sms &&
+            4 * ks_tiles >= d.num_sms && prm.kchunks >= 16;
+  if (const char* e = std::getenv("CONV3X3_KSPLIT"))
+    ks = std::strcmp(e, "0") != 0 && !s2 && !ts.halo && pair_bn == 0 && nout % kKsBN == 0;
+  if (ks) {
+    prm.num_m_tiles = (int)((g.P() + BM - 1) / BM);
+    prm.num_n_tiles = nout / kKsBN;
+    if (!dgrad) {  // one 256-row box per weight tile (dgrad's map has 64-row boxes)
+      rc = make_weight_map(&tb, w, s.Cin, s.Cout, kKsBN);
+      if (rc) return rc;
+    }
+    return dgrad ? launch_igemm_ks<true>(ta, ta2, tb, prm, d, st) : launch_igemm_ks<false>(ta, ta2, tb, prm, d, st);
+  }
   if (pair_bn && !s2) {
     // a pair tile is 256 pixels (128 per CTA) x pair_bn channels, each CTA
     // loading pair_bn / 2 weight rows (as two 96-row boxes at 384)
