@@ -3878,14 +3878,17 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
 #define C3_PAIR(BN_, KC_)                                                              \
   return dgrad ? launch_igemm_pair<true, BN_, KC_>(ta, ta2, tb, prm, d, st)            \
                : launch_igemm_pair<false, BN_, KC_>(ta, ta2, tb, prm, d, st)
-    if (pair_bn == 128) C3_PAIR(128, 1);
-    if (pair_bn == 192) C3_PAIR(192, 1);
-    if (pair_bn == 384) C3_PAIR(384, 1);
     // two 64-channel chunks per stage where K is a whole number of them;
     // CONV3X3_PAIR_KC=1 keeps one
     int pkc = prm.kchunks % 2 == 0 ? 2 : 1;
     if (const char* e = std::getenv("CONV3X3_PAIR_KC"))
       if (std::strcmp(e, "1") == 0) pkc = 1;
+    if (pair_bn == 128) {
+      if (pkc == 2) C3_PAIR(128, 2);
+      C3_PAIR(128, 1);
+    }
+    if (pair_bn == 192) C3_PAIR(192, 1);
+    if (pair_bn == 384) C3_PAIR(384, 1);
     if (pkc == 2) C3_PAIR(256, 2);
     C3_PAIR(256, 1);
 #undef C3_PAIR
