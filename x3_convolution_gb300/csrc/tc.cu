@@ -706,17 +706,17 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 // (1024 cycles of tensor work at N = 256) instead of four; the three 64 KB
 // stages are then filled box-parallel by all producers.
 //
-// BN = 384 (one accumulator, 384 of the 512 TMEM columns): two M = 256,
-// N = 192 MMAs per K step.  CTA r stages output channels [96 r, 96 r + 96) as
-// its weight rows 0-95 and [192 + 96 r, 192 + 96 r + 96) as rows 96-191, so
-// the first MMA (rows 0-95 of both CTAs) writes accumulator columns 0-191 and
-// the second (rows 96-191) columns 192-383: column = channel of the tile.  The
-// forward loads two 96-row K-major boxes, dgrad two pairs of 64-channel
-// MN-major boxes (the second of each pair half used).
+// BN = 384 (one accumulator, 384 of the 512 TMEM columns): an M = 256,
+// N = 256 and an M = 256, N = 128 MMA per K step.  CTA r stages output
+// channels [128 r, 128 r + 128) as its weight rows 0-127 and [256 + 64 r,
+// 256 + 64 r + 64) as rows 128-191, so the first MMA (rows 0-127 of both CTAs)
+// writes accumulator columns 0-255 and the second (rows 128-191) columns
+// 256-383: column = channel of the tile.  Both passes load three 64-row (or
+// 64-channel) boxes per CTA and k-block, every byte used.
 template <int BN, bool kDgrad, int KC = 1>
 struct PairCfg {
   static constexpr int kHalf = BN / 2;                  // weight rows (output channels) per CTA
-  static constexpr int kDgradBoxes = BN == 384 ? 4 : (kHalf + 63) / 64;  // dgrad: MN-major boxes
+  static constexpr int kDgradBoxes = (kHalf + 63) / 64;  // dgrad: 64-channel MN-major boxes
   static constexpr uint32_t kBHalf = kDgrad ? (uint32_t)kDgradBoxes * 8192u : (uint32_t)kHalf * 128u;
   static constexpr int kBufs = 2 * BN <= 512 ? 2 : 1;    // TMEM accumulators
   static constexpr uint32_t kStage = KC * (kABytes + kBHalf);  // per CTA: KC A boxes, then KC B halves
@@ -799,10 +799,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      constexpr int kBPer = kDgrad ? Cfg::kDgradBoxes : 1;  // weight boxes per chunk
+      constexpr int kBPer = (kDgrad || BN == 384) ? Cfg::kDgradBoxes : 1;  // weight boxes per chunk
       constexpr int kPer = 1 + kBPer;
       constexpr int kBoxes = KC * kPer;
-      constexpr uint32_t kBBox = kDgrad ? 8192u : Cfg::kBHalf;
+      constexpr uint32_t kBBox = (kDgrad || BN == 384) ? 8192u : Cfg::kBHalf;
       uint32_t my_bytes = 0;  // box-parallel: this producer's share of a stage
       for (int b = warp; b < kBoxes; b += kProd) my_bytes += b % kPer == 0 ? kABytes : kBBox;
       const int kgroups = p.kchunks / KC;
@@ -836,15 +836,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
                                         (second ? cc - p.kchunks_a : cc) * BKC, cw, ch, cn,
                                         (uint16_t)(tap % 3), (uint16_t)(tap / 3));
               } else if constexpr (BN == 384) {
-                // rows [96 rank, +96) then [192 + 96 rank, +96) of the tile's channels
-                const int cb = nt * kPairBN + (int)rank * 96;
-                if (!kDgrad) {
-                  tma_load_3d_pair(sb, &tmB, fb, cc * BKC, wtap, cb);
-                  tma_load_3d_pair(sb + 96 * 128, &tmB, fb, cc * BKC, wtap, cb + 192);
-                } else {
-                  const int j = r - 1;  // boxes at cb, cb + 64, cb + 192, cb + 256
-                  tma_load_3d_pair(sb + j * 8192, &tmB, fb, cb + (j >> 1) * 192 + (j & 1) * 64, wtap, cc * BKC);
-                }
+                // channels [128 rank, +128) then [256 + 64 rank, +64) of the tile, as
+                // three 64-row (forward) or 64-channel (dgrad) boxes
+                const int j = r - 1;
+                const int cb = nt * kPairBN + (j < 2 ? 128 * (int)rank + 64 * j : 256 + 64 * (int)rank);
+                if (!kDgrad)
+                  tma_load_3d_pair(sb + j * 8192, &tmB, fb, cc * BKC, wtap, cb);
+                else
+                  tma_load_3d_pair(sb + j * 8192, &tmB, fb, cb, wtap, cc * BKC);
               } else if (!kDgrad) {
                 tma_load_3d_pair(sb + c * Cfg::kBHalf, &tmB, fb, cc * BKC, wtap, c0);
               } else {
@@ -884,10 +883,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer (rank 0)
     if (rank == 0 && lane == 0) {
-      constexpr int kMmaN = BN == 384 ? 192 : kPairBN;  // two N = 192 MMAs per K step at BN = 384
+      constexpr int kMmaN = BN == 384 ? 256 : kPairBN;  // N = 256 + N = 128 per K step at BN = 384
       constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, kMmaN, 0, kDgrad ? 1 : 0);
-      // the second MMA's weight rows: 96 K-major rows on, or two 8 KB boxes on
-      constexpr uint32_t kB2 = (kDgrad ? 2u * 8192u : 96u * 128u) >> 4;
+      constexpr uint32_t idesc2 = idesc_bf16_f32(2 * BM, 128, 0, kDgrad ? 1 : 0);
+      // the second MMA's weight rows start after two 8 KB boxes (128 rows or channels)
+      constexpr uint32_t kB2 = (2u * 8192u) >> 4;
       const uint32_t sbase = smem_u32(smem);
       const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
       const uint64_t b_desc0 = kDgrad ? smem_desc(sbase + KC * kABytes, 8192, 1024, kSwizzle128B)
@@ -920,8 +920,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
               tc_mma_bf16_pair(d_tmem, ad + (uint64_t)(c * (kABytes >> 4) + k * kAKStep),
                                bd + (uint64_t)(c * (Cfg::kBHalf >> 4) + k * kBKStep), idesc, acc);
               if constexpr (BN == 384)
-                tc_mma_bf16_pair(d_tmem + 192, ad + (uint64_t)(k * kAKStep), bd + (uint64_t)(kB2 + k * kBKStep),
-                                 idesc, acc);
+                tc_mma_bf16_pair(d_tmem + 256, ad + (uint64_t)(k * kAKStep), bd + (uint64_t)(kB2 + k * kBKStep),
+                                 idesc2, acc);
             }
           tc_commit_pair_mc(&empty[stage], (uint16_t)0x3);
           stage_off += kStageStep;
@@ -3868,11 +3868,11 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   }
   if (pair_bn && !s2) {
     // a pair tile is 256 pixels (128 per CTA) x pair_bn channels, each CTA
-    // loading pair_bn / 2 weight rows (as two 96-row boxes at 384)
+    // loading pair_bn / 2 weight rows (as three 64-row boxes at 384)
     prm.num_m_tiles = (int)((g.P() + 2 * BM - 1) / (2 * BM));
     prm.num_n_tiles = (nout + pair_bn - 1) / pair_bn;
     if (!dgrad) {  // (dgrad's map already has 64-row boxes)
-      rc = make_weight_map(&tb, w, s.Cin, s.Cout, pair_bn == 384 ? 96 : pair_bn / 2);
+      rc = make_weight_map(&tb, w, s.Cin, s.Cout, pair_bn == 384 ? 64 : pair_bn / 2);
       if (rc) return rc;
     }
 #define C3_PAIR(BN_, KC_)                                                              \
