@@ -353,8 +353,8 @@ __device__ __forceinline__ float silu_f32(float z) { return __fdividef(z, 1.0f +
 // SiLU through tanh: z * sigmoid(z) = h + h * tanh(h) with h = z / 2, since
 // sigmoid(z) = (1 + tanh(z / 2)) / 2.  One special-function op (the hardware
 // tanh approximation, relative error near 2^-11) where silu_f32 takes two; the
-// 8-input-channel forward, whose epilogue is its bottleneck, uses it.  At
-// large |z| tanh saturates to +-1 and the result to z or -0.
+// tensor-core forward epilogues use it.  At large |z| tanh saturates to +-1
+// and the result to z or -0.
 __device__ __forceinline__ float silu_tanh_f32(float z) {
   const float h = 0.5f * z;
   float t;

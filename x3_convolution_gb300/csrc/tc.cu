@@ -68,6 +68,11 @@ constexpr int kProd = 4;
 #define C3_ONE_WEIGHT_BOX 1
 #endif
 
+// SiLU in the forward epilogues through tanh (one special-function op) when
+// 1, as z / (1 + e^-z) when 0
+#ifndef C3_SILU_TANH
+#define C3_SILU_TANH 1
+#endif
 constexpr bool kStageParallel = C3_STAGE_PARALLEL != 0;
 constexpr bool kOneWeightBox = C3_ONE_WEIGHT_BOX != 0;
 constexpr bool kWgStageParallel = false;  // the 3-stage wgrad ring is shared box-parallel
@@ -212,7 +217,7 @@ __device__ __forceinline__ void load_bias(const IgemmParams& p, int col0, float 
 // [* act'(z_in)] -> fp32 or bf16 store.  kExt = false compiles out the fused
 // extras (z store, z_in scaling, split output) for the plain calls; kTanh
 // takes SiLU through tanh (silu_tanh_f32).
-template <bool kExt, bool kTanh = false>
+template <bool kExt, bool kTanh = C3_SILU_TANH>
 __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix, int col0,
                                             const uint32_t (&v)[32], const float (&bv)[32],
                                             const uint4 (&zr)[4]) {
