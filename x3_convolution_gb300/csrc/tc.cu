@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
           }
           if (p.act == CONV3X3_ACT_SILU) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = silu_f32(f[i]);
+            for (int i = 0; i < 32; ++i) f[i] = C3_SILU_TANH ? silu_tanh_f32(f[i]) : silu_f32(f[i]);
           } else if (p.act == CONV3X3_ACT_LRELU) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = f[i] >= 0.0f ? f[i] : 0.2f * f[i];
