@@ -106,6 +106,11 @@ __device__ __forceinline__ void ufd_point(const UfdParams& p, int n, int oy, int
 template <int UP, int DOWN, int KH, int KW, int R>
 __global__ void __launch_bounds__(kUfdThreads)
     k_upfirdn2d(const __grid_constant__ UfdParams p) {
+  // Programmatic dependent launch: the next kernel in the stream may begin
+  // launching at once; nothing here reads memory before the previous kernel's
+  // writes are visible.
+  c3::pdl_trigger();
+  c3::pdl_wait();
   const int groups = p.C >> 3;
   const int item = blockIdx.x * kUfdThreads + (int)threadIdx.x;
   if (item >= p.Wo * groups) return;
@@ -166,6 +171,8 @@ __device__ __forceinline__ void store8(const UfdParams& p, size_t o, const float
 
 // Grid: x over (column block, channel group), y = row block, z = image.
 __global__ void __launch_bounds__(kUfdThreads) k_upfirdn2d_up2k4(const __grid_constant__ UfdParams p) {
+  c3::pdl_trigger();
+  c3::pdl_wait();
   const int groups = p.C >> 3;
   const int offx = (p.px0 + 1) & 1, offy = (p.py0 + 1) & 1;  // first block starts at -1 or 0
   const int nbx = (p.Wo + offx + 1) >> 1;
@@ -215,6 +222,8 @@ __global__ void __launch_bounds__(kUfdThreads) k_upfirdn2d_up2k4(const __grid_co
 // a = 2 dy + 3 - t when that lies in 0..3.  The window is walked row by row
 // (six 16-byte loads per row), every index compile-time.
 __global__ void __launch_bounds__(kUfdThreads) k_upfirdn2d_down2k4(const __grid_constant__ UfdParams p) {
+  c3::pdl_trigger();
+  c3::pdl_wait();
   const int groups = p.C >> 3;
   const int nbx = (p.Wo + 1) >> 1;
   const int item = blockIdx.x * kUfdThreads + (int)threadIdx.x;
@@ -327,6 +336,8 @@ int upfirdn2d(const void* x, const float* f, void* y, int N, int C, int H, int W
   const dim3 grid((unsigned)((row_items + kUfdThreads - 1) / kUfdThreads), (unsigned)((Ho + R - 1) / R),
                   (unsigned)N);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const dim3 blk(kUfdThreads);
+  cudaError_t e;
   const bool k4 = kh == 4 && kw == 4;
   const int groups = C / 8;
   if (k4 && up == 2 && down == 1) {
@@ -334,17 +345,17 @@ int upfirdn2d(const void* x, const float* f, void* y, int N, int C, int H, int W
     const long long items = (long long)((Wo + offx + 1) / 2) * groups;
     const dim3 g2((unsigned)((items + kUfdThreads - 1) / kUfdThreads), (unsigned)((Ho + offy + 1) / 2),
                   (unsigned)N);
-    k_upfirdn2d_up2k4<<<g2, kUfdThreads, 0, st>>>(p);
+    e = c3::launch_pdl(k_upfirdn2d_up2k4, g2, blk, 0, st, p);
   } else if (k4 && up == 1 && down == 2) {
     const long long items = (long long)((Wo + 1) / 2) * groups;
     const dim3 g2((unsigned)((items + kUfdThreads - 1) / kUfdThreads), (unsigned)((Ho + 1) / 2),
                   (unsigned)N);
-    k_upfirdn2d_down2k4<<<g2, kUfdThreads, 0, st>>>(p);
+    e = c3::launch_pdl(k_upfirdn2d_down2k4, g2, blk, 0, st, p);
   } else if (up == 1 && down == 1)
-    k_upfirdn2d<1, 1, 0, 0, R><<<grid, kUfdThreads, 0, st>>>(p);
+    e = c3::launch_pdl(k_upfirdn2d<1, 1, 0, 0, R>, grid, blk, 0, st, p);
   else
-    k_upfirdn2d<0, 0, 0, 0, R><<<grid, kUfdThreads, 0, st>>>(p);
-  return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+    e = c3::launch_pdl(k_upfirdn2d<0, 0, 0, 0, R>, grid, blk, 0, st, p);
+  return e == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
 }  // extern "C"
