@@ -501,23 +501,29 @@ __global__ void k_wgrad_reduce(const float* __restrict__ part, float* __restrict
 
 // The same sum for wide splits (a layer with few output tiles has up to
 // hundreds of splits of a small dw), in another fixed order: split group
-// g = 0..7 (in order) of the sums over s = g, g + 8, g + 16, ... (each in
-// increasing s).  A block covers 32 float4 columns with 8 warps, one per split
-// group, so the splits are read by eight warps at once instead of one thread
-// per column walking all of them; the result depends only on S, never on
-// timing, and is bit-identical run to run.  dbias rides along as Cout / 4 more
-// float4 columns over its Sdb partial rows stored after the S dw slices.
-constexpr int kRedGroups = 8;
+// g = 0..G-1 (in order) of the sums over s = g, g + G, g + 2G, ... (each in
+// increasing s).  A block of 256 threads covers 256 / G float4 columns with G
+// split groups, so the splits are read by G thread rows at once instead of one
+// thread per column walking all of them.  G is 8, or 32 when the columns are
+// too few to give every SM two blocks of 32 columns (a small dw such as the
+// 8-channel stem's: 32 groups of 8 columns, four times the blocks and a
+// quarter of the loads per thread).  The order depends only on the shape and
+// S, never on timing, and the result is bit-identical run to run.  dbias rides
+// along as Cout / 4 more float4 columns over its Sdb partial rows stored after
+// the S dw slices.
+constexpr int kRedThreads = 256;
 
-__global__ void __launch_bounds__(32 * kRedGroups)
+template <int G>
+__global__ void __launch_bounds__(kRedThreads)
     k_wgrad_reduce_wide(const float* __restrict__ part, float* __restrict__ dw, float* __restrict__ db,
                         long long dwsize, int Cout, int S, int Sdb) {
-  __shared__ float4 red[kRedGroups][32];
+  constexpr int CW = kRedThreads / G;  // float4 columns per block
+  __shared__ float4 red[G][CW];
   pdl_trigger();
   pdl_wait();  // the partials of the kernel before
   const int x = threadIdx.x, g = threadIdx.y;
   const long long n4 = dwsize / 4;
-  const long long col = blockIdx.x * 32LL + x;
+  const long long col = blockIdx.x * (long long)CW + x;
   const bool bias_col = col >= n4;
   const long long total = n4 + (db ? Cout / 4 : 0);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -526,7 +532,8 @@ __global__ void __launch_bounds__(32 * kRedGroups)
     const long long c = bias_col ? col - n4 : col;
     const long long stride = bias_col ? Cout / 4 : n4;
     const int n = bias_col ? Sdb : S;
-    for (int sp = g; sp < n; sp += kRedGroups) {
+#pragma unroll 4
+    for (int sp = g; sp < n; sp += G) {
       const float4 a = __ldg(src + (long long)sp * stride + c);
       acc.x += a.x;
       acc.y += a.y;
@@ -539,7 +546,7 @@ __global__ void __launch_bounds__(32 * kRedGroups)
   if (g == 0 && col < total) {
     float4 t = red[0][x];
 #pragma unroll
-    for (int i = 1; i < kRedGroups; ++i) {
+    for (int i = 1; i < G; ++i) {
       const float4 a = red[i][x];
       t.x += a.x;
       t.y += a.y;
@@ -607,8 +614,12 @@ int launch_wgrad_reduce(const float* part, float* dw, float* db, long long dwsiz
                         int Sdb, cudaStream_t st) {
   if (S >= kWideSplits) {
     const long long cols = dwsize / 4 + (db ? Cout / 4 : 0);
-    launch_pdl(k_wgrad_reduce_wide, dim3((unsigned)((cols + 31) / 32)), dim3(32, kRedGroups), 0, st,
-               part, dw, db, dwsize, Cout, S, Sdb);
+    if (cols < 2LL * kPlanSms * 32)
+      launch_pdl(k_wgrad_reduce_wide<32>, dim3((unsigned)((cols + 7) / 8)), dim3(8, 32), 0, st, part,
+                 dw, db, dwsize, Cout, S, Sdb);
+    else
+      launch_pdl(k_wgrad_reduce_wide<8>, dim3((unsigned)((cols + 31) / 32)), dim3(32, 8), 0, st, part,
+                 dw, db, dwsize, Cout, S, Sdb);
   } else {
     launch_pdl(k_wgrad_reduce, dim3(grid_for(dwsize / 4 + Cout)), dim3(kThreads), 0, st, part, dw, db,
                dwsize, Cout, S, Sdb);

@@ -2563,6 +2563,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // descriptors built once; stages and K steps move the start address only
       const uint32_t sbase = smem_u32(smem);
       const uint64_t a_desc0 = smem_desc(sbase, 8192, 1024, kSwizzle128B);
+      // row-shifted x: slot rows of stage 0 (addresses stay below 2^18, so
+      // adding offsets >> 4 to the start field never carries out of it)
+      const uint64_t x_desc0 = smem_desc(sbase + kWgABytes, Cfg::R * Cfg::kSlot, 1024, kSwizzle128B);
       constexpr uint32_t kStageStep = Cfg::kStageBytes >> 4;
       constexpr uint32_t kKStep = 2048u >> 4;
       int stage = 0;
@@ -2583,18 +2586,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the two channel halves Cfg::R slots apart.  The swizzle follows the
           // absolute shared-memory address, so a start that is s rows into a
           // 1 KB swizzle atom needs no base offset.
-          const uint32_t xbase = sbase + (uint32_t)stage * Cfg::kStageBytes + kWgABytes;
+          const uint64_t xd = x_desc0 + stage_off;
 #pragma unroll
           for (int k = 0; k < kWgPix / 16; ++k) {
             const uint32_t acc = k == 0 ? acc0 : 1u;
             constexpr int kW = kHW ? kHW : 16;  // (kHW = 0 never reaches here)
             const int i = (16 * k) / kW, w0 = (16 * k) % kW;
-            const uint32_t row0 = xbase + (uint32_t)i * Cfg::kSlot + (uint32_t)w0 * 128u;
+            const uint32_t row0 = (uint32_t)i * Cfg::kSlot + (uint32_t)w0 * 128u;
 #pragma unroll
             for (int t = 0; t < kWgTaps; ++t)
               tc_mma_bf16(tmem_base + (uint32_t)(t * 128), ad + (uint64_t)(k * kKStep),
-                          smem_desc(row0 + (uint32_t)t * 128u, Cfg::R * Cfg::kSlot, 1024, kSwizzle128B),
-                          t == 2 ? idesc_t2 : idesc128, acc);
+                          xd + (uint64_t)((row0 + (uint32_t)t * 128u) >> 4), t == 2 ? idesc_t2 : idesc128,
+                          acc);
           }
         } else {
           const uint64_t b_desc0 = smem_desc(sbase + kWgABytes, 8192, 1024, kSwizzle128B);
@@ -2932,6 +2935,7 @@ constexpr uint32_t kWc8BBytes = 12 * kWc8BlockBytes;           // 9 taps, zero, 
 constexpr uint32_t kWc8StageBytes = kWgABytes + kWc8BBytes;
 constexpr int kWc8Stages = 6;
 constexpr size_t kWc8Smem = (size_t)kWc8Stages * kWc8StageBytes + 256 + 1024;
+static_assert(kWc8StageBytes % 16 == 0, "stage offsets move descriptor start fields in 16-byte units");
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_wgrad_c8(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmX,
@@ -3038,8 +3042,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, 96, 1, 1);
+      // descriptors built once for stage 0 (addresses stay below 2^18: adding
+      // offsets >> 4 to the start field never carries out of it)
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t a_desc0 = smem_desc(sbase, 8192, 1024, kSwizzle128B);
+      const uint64_t b_desc0 = smem_desc(sbase + kWgABytes, 128, kWc8BlockBytes, kSwizzleNone);
+      constexpr uint32_t kStageStep = kWc8StageBytes >> 4;
       int stage = 0;
-      uint32_t phase = 0;
+      uint32_t phase = 0, stage_off = 0;
       bool ok = true;
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) {
@@ -3047,16 +3057,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a_base = smem_u32(smem + (size_t)stage * kWc8StageBytes);
-        const uint32_t b_base = a_base + kWgABytes;
 #pragma unroll
         for (int k = 0; k < kWgPix / 16; ++k)
-          tc_mma_bf16(tmem_base, smem_desc(a_base + k * 2048, 8192, 1024, kSwizzle128B),
-                      smem_desc(b_base + k * 256, 128, kWc8BlockBytes, kSwizzleNone), idesc,
-                      (kb != kb0 || k != 0) ? 1u : 0u);
+          tc_mma_bf16(tmem_base, a_desc0 + stage_off + (uint64_t)((k * 2048) >> 4),
+                      b_desc0 + stage_off + (uint64_t)((k * 256) >> 4), idesc, (kb != kb0 || k != 0) ? 1u : 0u);
         tc_commit(&empty[stage]);
+        stage_off += kStageStep;
         if (++stage == S) {
           stage = 0;
+          stage_off = 0;
           phase ^= 1;
         }
       }
@@ -3223,8 +3232,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, 32, 1, 1);
+      // descriptors built once for stage 0; stages, K steps and shifts move
+      // the start address only (addresses stay below 2^18: no carry)
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t a_desc0 = smem_desc(sbase, 8192, 1024, kSwizzle128B);
+      const uint64_t x_desc0 = smem_desc(sbase + kWhX + 16, 128, kWhRow, kSwizzleNone);
+      constexpr uint32_t kStageStep = kWhStage >> 4;
       int stage = 0;
-      uint32_t phase = 0;
+      uint32_t phase = 0, stage_off = 0;
       bool ok = true;
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) {
@@ -3232,20 +3247,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a_base = smem_u32(smem + (size_t)stage * kWhStage);
-        const uint32_t x_base = a_base + kWhX;
+        const uint64_t ad0 = a_desc0 + stage_off, xd0 = x_desc0 + stage_off;
 #pragma unroll
         for (int k = 0; k < kWgPix / 16; ++k) {
-          const uint64_t ad = smem_desc(a_base + k * 2048, 8192, 1024, kSwizzle128B);
+          const uint64_t ad = ad0 + (uint64_t)((k * 2048) >> 4);
 #pragma unroll
           for (int s = 0; s < 3; ++s)
-            tc_mma_bf16(tmem_base + (uint32_t)(32 * s), ad,
-                        smem_desc(x_base + (uint32_t)((s + 1) * 16 + k * 256), 128, kWhRow, kSwizzleNone),
-                        idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+            tc_mma_bf16(tmem_base + (uint32_t)(32 * s), ad, xd0 + (uint64_t)((s * 16 + k * 256) >> 4), idesc,
+                        (kb != kb0 || k != 0) ? 1u : 0u);
         }
         tc_commit(&empty[stage]);
+        stage_off += kStageStep;
         if (++stage == S) {
           stage = 0;
+          stage_off = 0;
           phase ^= 1;
         }
       }
