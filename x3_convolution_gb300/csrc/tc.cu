@@ -3117,25 +3117,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem_base, 128);
 }
 
-// Width 64, x staged as halo rows: x [N][H][64][8] viewed as [N][H][32][16]
-// (pixel pairs), one 4-D box per 64-pixel k-block (one image row h) brings
-// rows h - 1 .. h + 1 at pixels -2 .. 65 (34 pairs; outside the image reads
-// zero) as three contiguous 1088-byte rows, pixel p of row r at r * 1088 +
-// (p + 2) * 16.  In the MN-major no-swizzle layout (8-pixel x 16-byte core
-// matrices) the operand for column shift s starts (s + 1) * 16 bytes into the
-// rows, and its four 8-column blocks are rows 0, 1, 2 and a static ones block
-// one row further: per 16 pixels one M = 128, N = 32 MMA per shift s writes
-// accumulator columns 32 s + 8 r + c for tap (r, s), and column 24 (ones) is
-// dbias.  Three copies per k-block where the 512-byte row boxes take twenty.
-constexpr uint32_t kWhRow = 34 * 32;                          // one staged row of 68 pixels
-constexpr uint32_t kWhX = kWgABytes;                          // x rows after dy
-constexpr uint32_t kWhOnes = kWhX + 3 * kWhRow;               // the ones block, as row 3
-constexpr uint32_t kWhStage = (kWhOnes + kWhRow + 1023) / 1024 * 1024;
-constexpr uint32_t kWhLoad = kWgABytes + 3 * kWhRow;          // bytes copied per k-block
+// Width 64, x staged as three column-shifted copies of three halo rows.  x
+// [N][H][64][8] is viewed as flat rows [N][H][512]; per 64-pixel k-block (one
+// image row h) and column shift s = 0..2, two boxes of 256 elements x 3 rows
+// (pixels 32 hf + s - 1 .. + 31 of rows h - 1 .. h + 1; outside the image
+// reads zero) land at half hf's region + s * 1536, row r at + r * 512.  So in
+// each half the 8-pixel x 16-byte core matrices of tap (r, s) start (3 s + r)
+// * 512 bytes in: one uniform stride over the nine taps, and a static ones
+// block at position 9 (dbias).  Per 16 pixels one M = 128, N = 80 MMA covers
+// all nine taps where one copy per shift needed three N = 32 MMAs: measured on
+// the 64x64 stem, the twelve small MMAs per k-block ran at the DRAM's pace and
+// left no slack to drain the stages filled during the kernel's cold start.
+constexpr uint32_t kWhHalf = 5120;                            // 9 row blocks + ones block, per half
+constexpr uint32_t kWhX = kWgABytes;                          // x halves after dy
+constexpr uint32_t kWhOnes = 9 * 512;                         // ones block within a half
+constexpr uint32_t kWhStage = (kWhX + 2 * kWhHalf + 1023) / 1024 * 1024;
+constexpr uint32_t kWhLoad = kWgABytes + 6 * 3 * 512;         // bytes copied per k-block
 constexpr int kWhStages = 8;
 constexpr size_t kWhSmem = (size_t)kWhStages * kWhStage + 256 + 1024;
 static_assert(kWhStages >= kProd, "stage-parallel producers need S >= kProd");
-static_assert(kWhX % 128 == 0, "TMA destinations stay 128-byte aligned");
+static_assert(kWhX % 128 == 0 && kWhHalf % 16 == 0, "TMA destinations stay aligned");
+static_assert(kWhSmem <= 227 * 1024, "shared memory per CTA");
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_wgrad_c8h(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmX,
@@ -3174,13 +3176,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, 128);
     tmem_relinquish();
   }
-  if (warp >= kEpiBase) {  // every stage's ones block (bf16 1.0 = 0x3F80)
+  if (warp >= kEpiBase) {  // every stage's two ones blocks (bf16 1.0 = 0x3F80)
     const int t = threadIdx.x - 32 * kEpiBase;
-    for (int st = 0; st < S; ++st) {
-      uint4* b = reinterpret_cast<uint4*>(smem + (size_t)st * kWhStage + kWhOnes);
-      for (int i = t; i < (int)(kWhRow / 16); i += 32 * kWgEpiWarps)
-        b[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-    }
+    for (int st = 0; st < S; ++st)
+      for (int hf = 0; hf < 2; ++hf) {
+        uint4* b = reinterpret_cast<uint4*>(smem + (size_t)st * kWhStage + kWhX + hf * kWhHalf + kWhOnes);
+        for (int i = t; i < 512 / 16; i += 32 * kWgEpiWarps)
+          b[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+      }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   tc_fence_before();
@@ -3191,7 +3194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kProd) {
     // whole stages in turn: two dy boxes (64 pixels x 64 channels) and the
-    // three x rows of k-block kb (image row h0 of image n0)
+    // six x boxes of k-block kb (image row h0 of image n0)
     if (lane == 0) {
       int stage = 0, issued = 0;
       uint32_t phase = 0;
@@ -3208,7 +3211,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[stage], kWhLoad);
           tma_load_2d(sa, &tmDY, &full[stage], mb * 128, pk);
           tma_load_2d(sa + 8192, &tmDY, &full[stage], mb * 128 + 64, pk);
-          tma_load_4d(sa + kWhX, &tmX, &full[stage], 0, -1, h0 - 1, n0);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int sh = 0; sh < 3; ++sh)
+              tma_load_3d(sa + kWhX + hf * kWhHalf + sh * 1536, &tmX, &full[stage], 256 * hf + 8 * (sh - 1),
+                          h0 - 1, n0);
         }
         ++issued;
         if (++stage == S) {
@@ -3231,12 +3239,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, 32, 1, 1);
-      // descriptors built once for stage 0; stages, K steps and shifts move
-      // the start address only (addresses stay below 2^18: no carry)
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 80, 1, 1);
+      // descriptors built once for stage 0; stages and K steps move the start
+      // address only (addresses stay below 2^18: no carry)
       const uint32_t sbase = smem_u32(smem);
       const uint64_t a_desc0 = smem_desc(sbase, 8192, 1024, kSwizzle128B);
-      const uint64_t x_desc0 = smem_desc(sbase + kWhX + 16, 128, kWhRow, kSwizzleNone);
+      const uint64_t x_desc0 = smem_desc(sbase + kWhX, 128, 512, kSwizzleNone);
       constexpr uint32_t kStageStep = kWhStage >> 4;
       int stage = 0;
       uint32_t phase = 0, stage_off = 0;
@@ -3249,13 +3257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint64_t ad0 = a_desc0 + stage_off, xd0 = x_desc0 + stage_off;
 #pragma unroll
-        for (int k = 0; k < kWgPix / 16; ++k) {
-          const uint64_t ad = ad0 + (uint64_t)((k * 2048) >> 4);
-#pragma unroll
-          for (int s = 0; s < 3; ++s)
-            tc_mma_bf16(tmem_base + (uint32_t)(32 * s), ad, xd0 + (uint64_t)((s * 16 + k * 256) >> 4), idesc,
-                        (kb != kb0 || k != 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < kWgPix / 16; ++k)
+          tc_mma_bf16(tmem_base, ad0 + (uint64_t)((k * 2048) >> 4),
+                      xd0 + (uint64_t)(((k >> 1) * kWhHalf + (k & 1) * 256) >> 4), idesc,
+                      (kb != kb0 || k != 0) ? 1u : 0u);
         tc_commit(&empty[stage]);
         stage_off += kStageStep;
         if (++stage == S) {
@@ -3279,23 +3284,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
       float* o = p.part + (long long)split * dwsize + (long long)k * 72;
 #pragma unroll 1
-      for (int s = 0; s < 3; ++s) {
+      for (int c = 0; c < 3; ++c) {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(lane_addr + (uint32_t)(32 * s), v);
+        tmem_ld_32x32b_x32(lane_addr + (uint32_t)(32 * c), v);
         tmem_ld_wait();
         if (k < p.Cout) {
+          // column block j = 3 s + r (8 columns) holds tap (r, s)
 #pragma unroll
-          for (int r = 0; r < 3; ++r) {
-            const int tap = 3 * r + s;
-            reinterpret_cast<float4*>(o + tap * 8)[0] =
-                make_float4(__uint_as_float(v[8 * r]), __uint_as_float(v[8 * r + 1]),
-                            __uint_as_float(v[8 * r + 2]), __uint_as_float(v[8 * r + 3]));
-            reinterpret_cast<float4*>(o + tap * 8)[1] =
-                make_float4(__uint_as_float(v[8 * r + 4]), __uint_as_float(v[8 * r + 5]),
-                            __uint_as_float(v[8 * r + 6]), __uint_as_float(v[8 * r + 7]));
+          for (int g = 0; g < 4; ++g) {
+            const int j = 4 * c + g;
+            if (j < 9) {
+              const int tap = 3 * (j % 3) + j / 3;
+              reinterpret_cast<float4*>(o + tap * 8)[0] =
+                  make_float4(__uint_as_float(v[8 * g]), __uint_as_float(v[8 * g + 1]),
+                              __uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
+              reinterpret_cast<float4*>(o + tap * 8)[1] =
+                  make_float4(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]),
+                              __uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
+            }
           }
-          // column 24 of shift 0 is the first ones column: dbias
-          if (s == 0) p.part[(long long)p.S * dwsize + (long long)split * p.Cout + k] = __uint_as_float(v[24]);
+          // column 72 (block 9, the ones block) is dbias
+          if (c == 2) p.part[(long long)p.S * dwsize + (long long)split * p.Cout + k] = __uint_as_float(v[8]);
         }
       }
     }
@@ -3567,30 +3576,16 @@ int make_store_map(CUtensorMap* m, void* base, long long P, int C) {
 }
 
 // x [N][H][W][8] viewed as [N][H][W * 8]: boxes of `elems` consecutive
-// elements of one image row (no swizzle), for the row-staged 8-channel kernels.
-int make_row_map(CUtensorMap* m, const void* base, int N, int H, int W, int elems) {
+// elements of `rows` image rows (no swizzle), for the row-staged 8-channel
+// kernels.
+int make_row_map(CUtensorMap* m, const void* base, int N, int H, int W, int elems, int rows = 1) {
   PFN_encodeTiled enc = encode_tiled_fn();
   if (!enc) return CONV3X3_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)W * 8, (cuuint64_t)H, (cuuint64_t)N};
   cuuint64_t strides[2] = {(cuuint64_t)W * 16, (cuuint64_t)H * W * 16};
-  cuuint32_t box[3] = {(cuuint32_t)elems, 1, 1};
+  cuuint32_t box[3] = {(cuuint32_t)elems, (cuuint32_t)rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
-}
-
-// 8 channels viewed as pixel pairs, [N][H][W/2][16], for k_wgrad_c8h: one box
-// holds three image rows of W/2 + 2 pairs (a pair of zero pixels each side).
-int make_pair_row_map(CUtensorMap* m, const void* base, int N, int H, int W) {
-  PFN_encodeTiled enc = encode_tiled_fn();
-  if (!enc) return CONV3X3_ERR_CUDA;
-  cuuint64_t dims[4] = {16, (cuuint64_t)W / 2, (cuuint64_t)H, (cuuint64_t)N};
-  cuuint64_t strides[3] = {32, (cuuint64_t)W * 16, (cuuint64_t)H * W * 16};
-  cuuint32_t box[4] = {16, (cuuint32_t)W / 2 + 2, 3, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CONV3X3_OK : CONV3X3_ERR_CUDA;
@@ -4121,17 +4116,18 @@ int run_wgrad_c8(const void* x, const void* dy, float* dw, float* db, const Shap
                  const DevCtx& d, cudaStream_t st) {
   WgPlan pl = wg_plan_c8(s);
   // width 64 (each 64-pixel k-block is one image row): x staged as three
-  // halo rows per k-block, one copy; otherwise (or with CONV3X3_STEM_ROWS=0)
-  // as nine im2col boxes.  Measured on the 64x64 batch-64 stem: 28.7 us for
-  // the call against 33.3 us with two 512-byte row boxes per tap and 43 us
-  // with im2col boxes.
+  // column-shifted copies of three halo rows, six 3-row boxes per k-block;
+  // otherwise (or with CONV3X3_STEM_ROWS=0) as nine im2col boxes.  Measured
+  // on the 64x64 batch-64 stem (call, L2 flushed): 43 us with im2col boxes,
+  // 33.3 us with two 512-byte row boxes per tap, 28.7 us with one box of
+  // three pixel-pair rows and three N = 32 MMAs per K step.
   bool halo = s.W == 64;
   if (const char* e = std::getenv("CONV3X3_STEM_ROWS"))
     if (std::strcmp(e, "0") == 0) halo = false;
   CUtensorMap tdy, tx;
   int rc = make_rows_map(&tdy, dy, s.P(), s.Cout);
   if (rc) return rc;
-  rc = halo ? make_pair_row_map(&tx, x, s.N, s.H, s.W)
+  rc = halo ? make_row_map(&tx, x, s.N, s.H, s.W, 256, 3)
             : make_im2col_map(&tx, x, s.N, s.H, s.W, 8, kWgPix, 8, false);
   if (rc) return rc;
   WgradParams prm;
