@@ -1547,6 +1547,48 @@ struct StemCfg {
 // Byte offset in the A stage of K slot q (0..8: taps in the stage's order,
 // 9: the padding tap).  im2col: slot q holds tap q; row staging: slot q holds
 // tap (q % 3) * 3 + q / 3 (r = q % 3 rows into the slot of shift s = q / 3).
+// The stem's resident B operand: K slot q (0..8) holds one tap of every output
+// channel as a 16-byte row (rows at or past nout zero), slot 9 the bias split
+// into two bf16 halves (hi, lo) in channels 0-1.  Slot q holds tap q, or with
+// row staging (kRW) tap 3 (q % 3) + q / 3.  Run by the kEpiWarps epilogue
+// warps (t = 0 .. 32 kEpiWarps - 1): coalesced 16-byte loads in w's own order
+// [Cout][9][8], then one arrival per warp on `ready`.  Nine TMA boxes of
+// 16-byte rows took ~4,800 cycles to land at kernel start (the copy engine's
+// row rate); these loads take one global round trip.
+template <int BN, int kRW>
+__device__ __forceinline__ void stem_stage_weights(uint8_t* wsm, const __nv_bfloat16* __restrict__ w,
+                                                   const float* __restrict__ bias, int nout, int t,
+                                                   uint64_t* ready) {
+  constexpr int kT = 32 * kEpiWarps;
+  constexpr int kN = (9 * BN + kT - 1) / kT;
+  uint4 v[kN];
+#pragma unroll
+  for (int i = 0; i < kN; ++i) {
+    const int e = t + i * kT;  // 16-byte row e of w: channel e / 9, tap e % 9
+    v[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (e < 9 * BN && e / 9 < nout) v[i] = __ldg(reinterpret_cast<const uint4*>(w) + e);
+  }
+  for (int i = t; i < BN; i += kT) {
+    const float b = (bias && i < nout) ? __ldg(bias + i) : 0.0f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(b);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(b - __bfloat162float(hi));
+    *reinterpret_cast<uint4*>(wsm + 9 * BN * 16 + i * 16) =
+        make_uint4((uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(lo) << 16), 0, 0, 0);
+  }
+#pragma unroll
+  for (int i = 0; i < kN; ++i) {
+    const int e = t + i * kT;
+    if (e < 9 * BN) {
+      const int co = e / 9, tap = e - co * 9;
+      const int q = kRW ? 3 * (tap % 3) + tap / 3 : tap;
+      *reinterpret_cast<uint4*>(wsm + q * BN * 16 + co * 16) = v[i];
+    }
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+  if ((t & 31) == 0) mbar_arrive(ready);
+}
+
 template <int BN, bool kTS, int kRW>
 __host__ __device__ constexpr uint32_t stem_a_off(int q) {
   using Cfg = StemCfg<BN, kTS, kRW>;
@@ -1557,7 +1599,7 @@ __host__ __device__ constexpr uint32_t stem_a_off(int q) {
 
 template <int BN, bool kTS = false, int kRW = 0>
 __global__ void __launch_bounds__(kIgemmThreads, 1)
-    k_stem_fwd(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    k_stem_fwd(const __grid_constant__ CUtensorMap tmA, const __nv_bfloat16* __restrict__ w,
                const __grid_constant__ CUtensorMap tmY, const IgemmParams p) {
   using Cfg = StemCfg<BN, kTS, kRW>;
   constexpr int S = Cfg::kStages;
@@ -1589,11 +1631,10 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       mbar_init(&tempty[i], kEpiWarps);
     }
     mbar_init(drain, 1);
-    mbar_init(wfull, 1);
+    mbar_init(wfull, kEpiWarps);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
     if (kTS) tma_prefetch_desc(&tmY);
   }
   if (warp == kMmaWarp) {
@@ -1601,20 +1642,11 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     tmem_relinquish();
   }
   if (warp >= kEpiBase) {
-    // the tenth (padding) tap: ones in A channels 0-1 of every stage, the
-    // bias (hi, lo) in the weights' channels 0-1
-    pdl_wait();  // the bias is read below
+    // the tenth (padding) tap: ones in A channels 0-1 of every stage
     const int t = threadIdx.x - 32 * kEpiBase;
     for (int st = 0; st < S; ++st) {
       uint4* z = reinterpret_cast<uint4*>(smem + (size_t)st * Cfg::kStageBytes + Cfg::kPadOff);
       for (int i = t; i < (int)(Cfg::kTapBytes / 16); i += 32 * kEpiWarps) z[i] = make_uint4(0x3F803F80u, 0, 0, 0);
-    }
-    uint4* z = reinterpret_cast<uint4*>(wsm + 9 * Cfg::kBTap);
-    for (int i = t; i < BN; i += 32 * kEpiWarps) {
-      const float b = (p.bias && i < p.nout) ? __ldg(p.bias + i) : 0.0f;
-      const __nv_bfloat16 hi = __float2bfloat16_rn(b);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(b - __bfloat162float(hi));
-      z[i] = make_uint4((uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(lo) << 16), 0, 0, 0);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -1624,19 +1656,24 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // the previous kernel's writes are visible from here on
 
+  // resident weights and the bias tap, staged by the epilogue warps while the
+  // producers already stream x (the MMA waits on wfull)
+  if (warp >= kEpiBase)
+    stem_stage_weights<BN, kRW>(wsm, w, p.bias, p.nout, threadIdx.x - 32 * kEpiBase, wfull);
+
   if (warp < kProd) {
     if (lane == 0) {
-      if (warp == 0) {  // resident weights: nine boxes of BN rows x 8 channels, in K slot order
-        mbar_arrive_expect_tx(wfull, 9 * Cfg::kBTap);
-        for (int q = 0; q < 9; ++q)
-          tma_load_3d(wsm + q * Cfg::kBTap, &tmB, wfull, 0, kRW ? (q % 3) * 3 + q / 3 : q, 0);
-      }
-      // stage-parallel: this producer owns every kProd-th tile (one stage per tile)
+      // box-parallel: every producer takes every kProd-th box of each stage
+      // (producer 0 posts the stage's byte count), so the first stage lands
+      // after its own boxes instead of behind kProd stages' worth of boxes
+      // interleaved on the copy engine.  Measured on the 64x64 stem with one
+      // producer per stage: the first tile's data arrived ~4,900 cycles after
+      // its boxes were issued.
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        if (issued % kProd == warp) {
+        {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
             ok = false;
             break;
@@ -1647,16 +1684,17 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
           uint8_t* sa = smem + (size_t)stage * Cfg::kStageBytes;
           if constexpr (kRW != 0) {
             // slot s: image rows h0 - 1 .. h0 + R, columns s - 1 .. s - 2 + W
-            mbar_arrive_expect_tx(&full[stage], 3 * Cfg::kSlotBytes);
-            for (int sh = 0; sh < 3; ++sh)
-              for (int rho = 0; rho < Cfg::kRowsPerTile + 2; ++rho)
-#pragma unroll
-                for (int part = 0; part < Cfg::kRowParts; ++part)
-                  tma_load_3d(sa + sh * Cfg::kSlotBytes + rho * Cfg::kRowBytes + part * 2 * Cfg::kBoxElems,
-                              &tmA, &full[stage], (sh - 1) * 8 + part * Cfg::kBoxElems, h0 - 1 + rho, n0);
+            if (warp == 0) mbar_arrive_expect_tx(&full[stage], 3 * Cfg::kSlotBytes);
+            constexpr int kRows = Cfg::kRowsPerTile + 2;
+            for (int b = warp; b < 3 * kRows * Cfg::kRowParts; b += kProd) {
+              const int part = b % Cfg::kRowParts, rho = (b / Cfg::kRowParts) % kRows;
+              const int sh = b / (Cfg::kRowParts * kRows);
+              tma_load_3d(sa + sh * Cfg::kSlotBytes + rho * Cfg::kRowBytes + part * 2 * Cfg::kBoxElems, &tmA,
+                          &full[stage], (sh - 1) * 8 + part * Cfg::kBoxElems, h0 - 1 + rho, n0);
+            }
           } else {
-            mbar_arrive_expect_tx(&full[stage], 9 * Cfg::kTapBytes);
-            for (int t = 0; t < 9; ++t)
+            if (warp == 0) mbar_arrive_expect_tx(&full[stage], 9 * Cfg::kTapBytes);
+            for (int t = warp; t < 9; t += kProd)
               tma_load_im2col_4d(sa + t * Cfg::kTapBytes, &tmA, &full[stage], 0, w0 - 1, h0 - 1, n0,
                                  (uint16_t)(t % 3), (uint16_t)(t / 3));
           }
@@ -1677,7 +1715,6 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
           mbar_wait(&full[stage], phase, drain_wait_ns(p.wait_ns), nullptr, nullptr);
         }
       }
-      if (warp == 0) mbar_wait(wfull, 0, drain_wait_ns(p.wait_ns), nullptr, nullptr);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -1847,7 +1884,12 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 constexpr int kSdEpiWarps = 8;
 constexpr int kSdThreads = 32 * (kProd + 1 + kSdEpiWarps);
 constexpr int kSdN = 80;                  // MMA N: 72 used columns of T
-constexpr int kSdTPitch = 72;             // floats per staged T row
+// floats per staged T row (72 used): a pitch of 76 words puts the float4
+// stores of eight consecutive T pixels on eight distinct 4-bank groups, where
+// 72 (8 banks apart) wrote two pixels per group; the gather's reads stay
+// spread evenly.  Measured on the 64x64 stem: staging a tile's T took ~1300
+// cycles at pitch 72.
+constexpr int kSdTPitch = 76;
 constexpr uint32_t kSdChunkBytes = 256u * 128u;  // room for 256 dy pixels x 64 channels
 constexpr int kSdStages = 2;
 
@@ -1868,6 +1910,7 @@ __host__ __device__ constexpr size_t stem_dgrad_smem(int K) {
          + (size_t)256 * kSdTPitch * 4                   // staged T
          + 1024 + 256;                                   // alignment, barriers
 }
+static_assert(stem_dgrad_smem(128) <= 227 * 1024, "shared memory per CTA at 128 dy channels");
 
 __global__ void __launch_bounds__(kSdThreads, 1)
     k_stem_dgrad(const __grid_constant__ CUtensorMap tmDY, const __nv_bfloat16* __restrict__ w,
@@ -3550,13 +3593,13 @@ TileShape pick_tile(int nout, const Shape& sh, int num_sms) {
 }
 
 template <int BN, bool kTS = false, int kRW = 0>
-int launch_stem(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y,
+int launch_stem(const CUtensorMap& a, const __nv_bfloat16* w, const CUtensorMap& y,
                 const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
   using Cfg = StemCfg<BN, kTS, kRW>;
   auto kern = k_stem_fwd<BN, kTS, kRW>;
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int grid = prm.num_m_tiles < d.num_sms ? prm.num_m_tiles : d.num_sms;
-  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, b, y, prm);
+  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, w, y, prm);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
@@ -3605,12 +3648,11 @@ int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const
                  int out_f32, const EpiExtra& ex, const DevCtx& d, cudaStream_t st) {
   const int bn = s.Cout <= 64 ? 64 : s.Cout <= 128 ? 128 : 256;
   const int rw = stem_row_width(s);
-  CUtensorMap ta, tb;
+  CUtensorMap ta;
   int rc = rw ? make_row_map(&ta, x, s.N, s.H, s.W, rw * 8 < 256 ? rw * 8 : 256)
               : make_im2col_map(&ta, x, s.N, s.H, s.W, 8, BM, 8, false);
   if (rc) return rc;
-  rc = make_weight_map(&tb, w, 8, s.Cout, bn, 8, false);
-  if (rc) return rc;
+  const __nv_bfloat16* wp = static_cast<const __nv_bfloat16*>(w);
   IgemmParams prm;
   prm.out = y;
   prm.bias = bias;
@@ -3634,9 +3676,9 @@ int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const
   prm.wait_ns = d.wait_ns;
   prm.zout = static_cast<__nv_bfloat16*>(ex.zout);
 #define C3_STEM(BN_, TS_, Y_)                                                  \
-  return rw == 64   ? launch_stem<BN_, TS_, 64>(ta, tb, Y_, prm, d, st)          \
-         : rw == 32 ? launch_stem<BN_, TS_, 32>(ta, tb, Y_, prm, d, st)          \
-                    : launch_stem<BN_, TS_, 0>(ta, tb, Y_, prm, d, st)
+  return rw == 64   ? launch_stem<BN_, TS_, 64>(ta, wp, Y_, prm, d, st)          \
+         : rw == 32 ? launch_stem<BN_, TS_, 32>(ta, wp, Y_, prm, d, st)          \
+                    : launch_stem<BN_, TS_, 0>(ta, wp, Y_, prm, d, st)
   if (bn == 128 && !out_f32 && !ex.zout) {
     // bf16 output with no z store leaves through TMA stores
     CUtensorMap ty;
@@ -3644,9 +3686,10 @@ int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const
     if (rc) return rc;
     C3_STEM(128, true, ty);
   }
-  if (bn == 64) C3_STEM(64, false, tb);
-  if (bn == 128) C3_STEM(128, false, tb);
-  C3_STEM(256, false, tb);
+  // (without TMA stores the output map is unused: ta stands in)
+  if (bn == 64) C3_STEM(64, false, ta);
+  if (bn == 128) C3_STEM(128, false, ta);
+  C3_STEM(256, false, ta);
 #undef C3_STEM
 }
 
