@@ -1929,7 +1929,8 @@ __global__ void __launch_bounds__(kSdThreads, 1)
   uint64_t* tready = tempty + 2;  // every epilogue warp has staged its T rows
   uint64_t* tdone = tready + 1;   // every epilogue warp has finished reading them
   uint64_t* drain = tdone + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* wready = drain + 1;   // Wt is staged
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1949,6 +1950,7 @@ __global__ void __launch_bounds__(kSdThreads, 1)
     mbar_init(tready, kSdEpiWarps);
     mbar_init(tdone, kSdEpiWarps);
     mbar_init(drain, 1);
+    mbar_init(wready, kSdThreads / 32 - 1);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmDY);
@@ -1957,26 +1959,35 @@ __global__ void __launch_bounds__(kSdThreads, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  pdl_wait();  // w is read below
-  // Wt from w [K][3][3][8]: element (n = 8 t + c, k) at group k/8, row n, 2 (k % 8) bytes;
-  // rows 72..79 are zero
-  for (int e = threadIdx.x; e < (p.K / 8) * kSdN; e += kSdThreads) {
-    const int g = e / kSdN, n = e - g * kSdN;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (n < 72) {
-      __nv_bfloat16 h[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) h[i] = w[(size_t)(g * 8 + i) * 72 + n];
-      v = *reinterpret_cast<const uint4*>(h);
-    }
-    *reinterpret_cast<uint4*>(wsm + (size_t)g * wgroup_bytes + n * 16) = v;
-  }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // the previous kernel's writes are visible from here on
+
+  // Every warp but the producer stages Wt from w [K][3][3][8] while dy already
+  // streams in: element (n = 8 t + c, k) at group k / 8, row n, byte 2 (k % 8);
+  // rows 72..79 are zero.  One 16-byte load per (k, 8 consecutive n).  Staged
+  // before the copies by the whole CTA with 2-byte loads, it held the first dy
+  // box back ~3,700 cycles.
+  if (warp != 0) {
+    const int t = threadIdx.x - 32, nt = kSdThreads - 32;
+    for (int e = t; e < p.K * 9; e += nt) {
+      const int k = e / 9, n8 = e - k * 9;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(w + (size_t)k * 72) + n8);
+      const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&v);
+      uint8_t* dst = wsm + (size_t)(k >> 3) * wgroup_bytes + (size_t)(8 * n8) * 16 + 2 * (k & 7);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) *reinterpret_cast<__nv_bfloat16*>(dst + i * 16) = h[i];
+    }
+    for (int e = t; e < (p.K / 8) * (kSdN - 72); e += nt) {
+      const int g = e / (kSdN - 72), n = 72 + e - g * (kSdN - 72);
+      *reinterpret_cast<uint4*>(wsm + (size_t)g * wgroup_bytes + n * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(wready);
+  }
 
   if (warp < kProd) {
     // ------------------------------------------------------------ TMA producer (warp 0)
@@ -2020,7 +2031,7 @@ __global__ void __launch_bounds__(kSdThreads, 1)
       const uint32_t sbase = smem_u32(smem), wbase = smem_u32(wsm);
       int stage = 0, buf = 0;
       uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
+      bool ok = mbar_wait(wready, 0, p.wait_ns, p.status, abort_flag);
       for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
         if (!mbar_wait(&tempty[buf], acc_phase ^ 1, p.wait_ns, p.status, abort_flag)) break;
         if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) break;
