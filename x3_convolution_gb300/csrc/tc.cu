@@ -114,9 +114,13 @@ struct IgemmCfg {
   static constexpr bool kStagePar = kStageParallel && kStages >= kProd;
   static constexpr int kTmemCols = pow2_cols(2 * MT * BN);
   static_assert(2 * MT * BN <= 512, "double-buffered accumulators must fit in TMEM");
-  // + barriers, + alignment slack, + a 16 KB guard so that no descriptor
-  // arithmetic can ever address past the allocation
-  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 256 + 1024 + kGuardBytes;
+  // epilogue warps' bias slices (after the barriers): kEpiCols columns each
+  static constexpr int kEpiCols = MT == 2 ? BN : BN / 2;
+  static constexpr uint32_t kBiasBytes = (uint32_t)kEpiWarps * kEpiCols * 4;
+  // + barriers, + bias slices, + alignment slack, + a 16 KB guard so that no
+  // descriptor arithmetic can ever address past the allocation
+  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 256 + kBiasBytes + 1024 + kGuardBytes;
+  static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 };
 
 struct IgemmParams {
@@ -206,6 +210,30 @@ __device__ __forceinline__ void load_bias(const IgemmParams& p, int col0, float 
   for (int i = 0; i < 32; i += 4) {
     const float4 b = col0 + i < p.nout ? __ldg(reinterpret_cast<const float4*>(p.bias + col0 + i))
                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    bv[i] = b.x;
+    bv[i + 1] = b.y;
+    bv[i + 2] = b.z;
+    bv[i + 3] = b.w;
+  }
+}
+
+// The bias of one epilogue warp's kCols output columns c0 .. c0 + kCols - 1
+// (zero at or past nout), staged in the warp's own shared-memory slice before
+// it waits for the accumulator.  A tile's chunks then read it from shared
+// memory instead of each waiting on a global load: with one tile per CTA (the
+// 8x8 and 16x16 layers) nothing else hides that latency.
+template <int kCols>
+__device__ __forceinline__ void stage_bias_slice(const IgemmParams& p, int c0, float* sl, int lane) {
+  __syncwarp();  // every lane is done with the previous tile's slice
+#pragma unroll
+  for (int i = lane; i < kCols; i += 32) sl[i] = c0 + i < p.nout ? __ldg(p.bias + c0 + i) : 0.0f;
+  __syncwarp();
+}
+
+__device__ __forceinline__ void bias_from_slice(const float* sl, float (&bv)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    const float4 b = *reinterpret_cast<const float4*>(sl + i);  // one address for the warp
     bv[i] = b.x;
     bv[i + 1] = b.y;
     bv[i + 2] = b.z;
@@ -627,12 +655,13 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     // warp w may read TMEM lanes 32*(w%4) .. +31.  The two warps of a lane
     // quarter take one 128-pixel sub-tile each (MT = 2) or half the columns
     // of the single sub-tile (MT = 1).
-    constexpr int kCols = MT == 2 ? BN : BN / 2;
+    constexpr int kCols = Cfg::kEpiCols;
     const int q = warp & 3;
     const int half = (warp - kEpiBase) >> 2;
     const int sub = MT == 2 ? half : 0;
     const int col_off = MT == 2 ? 0 : half * kCols;
     const int row = q * 32 + lane;
+    float* bsl = reinterpret_cast<float*>(smem + (size_t)S * Cfg::kStageBytes + 256) + (warp - kEpiBase) * kCols;
     int buf = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -650,6 +679,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       }
       if (kExt && p.zin && valid && nt * BN + col_off < p.nout)
         prefetch_zin_row(p, pix, nt * BN + col_off, kCols);
+      if (p.bias) stage_bias_slice<kCols>(p, nt * BN + col_off, bsl, lane);
       if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
@@ -660,7 +690,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
         const bool live = valid && col0 < p.nout;
         // operands that do not depend on the accumulator are loaded first
         float bv[32];
-        if (p.bias && live) load_bias(p, col0, bv);
+        if (p.bias && live) bias_from_slice(bsl + j * 32, bv);
         uint4 zr[4] = {};
         if (kExt && p.zin && live) load_zin(p, pix, col0, zr);
         uint32_t v[32];
@@ -728,7 +758,10 @@ struct PairCfg {
   static constexpr int kStagesFit = (int)((200u * 1024u) / kStage);
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr bool kSP = kStages >= kProd;  // whole stages per producer, else boxes
-  static constexpr size_t kSmem = (size_t)kStages * kStage + 256 + 1024 + kGuardBytes;
+  // epilogue warps' bias slices (after the barriers): BN / 2 columns each
+  static constexpr uint32_t kBiasBytes = (uint32_t)kEpiWarps * kHalf * 4;
+  static constexpr size_t kSmem = (size_t)kStages * kStage + 256 + kBiasBytes + 1024 + kGuardBytes;
+  static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
   static_assert(BN == 128 || BN == 192 || BN == 256 || BN == 384, "pair tiles are 128 .. 384 channels wide");
   static_assert(BN != 384 || KC == 1, "384-channel pair tiles take one chunk per stage");
   static_assert(KC == 1 || KC == 2, "one or two chunks per stage");
@@ -958,6 +991,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
     const int half = (warp - kEpiBase) >> 2;
     const int col_off = half * kCols;
     const int row = q * 32 + lane;
+    float* bsl = reinterpret_cast<float*>(smem + (size_t)S * kPairStage + 256) + (warp - kEpiBase) * kCols;
     int buf = 0;
     uint32_t acc_phase = 0;
     for (int tile = pair; tile < num_tiles; tile += num_pairs) {
@@ -966,6 +1000,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
       const bool valid = pix < p.P;
       if (kExt && p.zin && valid && nt * kPairBN + col_off < p.nout)
         prefetch_zin_row(p, pix, nt * kPairBN + col_off, kCols);
+      if (p.bias) stage_bias_slice<kCols>(p, nt * kPairBN + col_off, bsl, lane);
       if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
       tc_fence_after();
       const uint32_t taddr =
@@ -975,7 +1010,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
         const int col0 = nt * kPairBN + col_off + j * 32;
         const bool live = valid && col0 < p.nout;
         float bv[32];
-        if (p.bias && live) load_bias(p, col0, bv);
+        if (p.bias && live) bias_from_slice(bsl + j * 32, bv);
         uint4 zr[4] = {};
         if (kExt && p.zin && live) load_zin(p, pix, col0, zr);
         uint32_t v[32];
@@ -1020,7 +1055,9 @@ constexpr int kKsBN = 256;
 constexpr uint32_t kKsStage = kABytes + kKsBN * 128;  // 128-pixel A box + 256 weight rows x 64 channels
 constexpr int kKsStages = 4;
 constexpr uint32_t kKsXchg = 128u * 128u * 4u;        // 128 pixels x 128 fp32 columns
-constexpr size_t kKsSmem = (size_t)kKsStages * kKsStage + 256 + 1024 + kGuardBytes;
+// + barriers, + the epilogue warps' bias slices (64 columns each), + slack
+constexpr size_t kKsSmem = (size_t)kKsStages * kKsStage + 256 + kEpiWarps * 64 * 4 + 1024 + kGuardBytes;
+static_assert(kKsSmem <= 227 * 1024, "shared memory per CTA");
 static_assert(kKsXchg <= (uint32_t)kKsStages * kKsStage, "the exchange reuses the stage memory");
 static_assert(kKsStages >= kProd, "stage-parallel producers need S >= kProd");
 
@@ -1069,6 +1106,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // the previous kernel's writes are visible from here on
+  // epilogue warp ew stores columns 128 rank + 64 ((ew >> 2) & 1) .. + 63:
+  // their bias is staged while the main loop runs
+  float* bsl = reinterpret_cast<float*>(smem + (size_t)S * kKsStage + 256) + (warp - kEpiBase) * 64;
+  if (warp >= kEpiBase && p.bias)
+    stage_bias_slice<64>(p, nt * kKsBN + 128 * (int)rank + 64 * (((warp - kEpiBase) >> 2) & 1), bsl, lane);
 
   if (warp < kProd) {
     // whole stages in turn: the A box and the weight tile (one 256-row box,
@@ -1194,7 +1236,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
       const int col0 = nt * kKsBN + 128 * (int)rank + cl;
       const bool live = valid && col0 < p.nout;
       float bv[32];
-      if (p.bias && live) load_bias(p, col0, bv);
+      if (p.bias && live) bias_from_slice(bsl + j * 32, bv);
       uint4 zr[4] = {};
       if (kExt && p.zin && live) load_zin(p, pix, col0, zr);
       uint32_t v[32];
