@@ -2522,12 +2522,57 @@ struct WgradParams {
   int num_mb, num_cb;  // 128-wide blocks of Cout and Cin
   unsigned* status;
   unsigned long long wait_ns;
+  int part_tma = 0;    // the dw partials leave through tmPart (see wg_store_partials)
 };
+
+// The dw partials of one wgrad CTA tile -- TMEM lanes = 128 output channels
+// from k0 = mb * 128, columns 128 t + c = tap 3 tr + t, input channel
+// cb * 128 + c -- written to part [S][Cout][9][Cin] through TMA tensor stores.
+// Warp q stages its 32 rows of each 32-column chunk (4 KB, 128-byte swizzle)
+// in four rotating buffers of the (idle) stage memory at `stg`, and lane 0
+// stores the box {32 channels, 1 tap, 32 rows, 1 split} of map tmPart
+// ([S][Cout][9][Cin] fp32; rows past Cout and channels past Cin are clipped).
+// Each thread storing its own row with 16-byte stores made every warp store
+// touch 32 lines: the partials then took ~19,000 cycles of a 73,000-cycle CTA
+// on the 384-channel 16x16 layer.
+__device__ __forceinline__ void wg_store_partials(const CUtensorMap* tmPart, uint8_t* stg, uint32_t lane_addr,
+                                                  int tr, int cb, int k0, int split, int Cin, int Cout,
+                                                  int q, int lane) {
+  uint8_t* wbuf = stg + (size_t)q * 4 * 4096;
+  int n = 0;
+#pragma unroll 1
+  for (int t = 0; t < kWgTaps; ++t) {
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j, ++n) {
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(lane_addr + (uint32_t)(t * 128 + j * 32), v);
+      tmem_ld_wait();
+      uint8_t* buf = wbuf + (n & 3) * 4096;
+      // the store issued from this buffer four chunks ago has read it
+      if (n >= 4 && lane == 0) bulk_wait_read<3>();
+      __syncwarp();
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        *reinterpret_cast<uint4*>(buf + lane * 128 + ((g ^ (lane & 7)) << 4)) =
+            make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int c0 = cb * 128 + j * 32, r0 = k0 + q * 32;
+        if (c0 < Cin && r0 < Cout) tma_store_4d(tmPart, buf, c0, tr * 3 + t, r0, split);
+        bulk_commit();  // one group per chunk, empty or not
+      }
+    }
+  }
+  if (lane == 0) bulk_wait<0>();
+  __syncwarp();
+}
 
 template <int kHW>
 __global__ void __launch_bounds__(kThreads, 1)
     k_wgrad(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmX,
-            const __grid_constant__ CUtensorMap tmX2, const WgradParams p) {
+            const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmPart,
+            const WgradParams p) {
   using Cfg = WgCfg<kHW>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -2731,8 +2776,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const long long dwsize = (long long)p.Cout * 9 * p.Cin;
       const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+      if (p.part_tma)
+        wg_store_partials(&tmPart, smem, lane_addr, tr, cb, mb * 128, split, p.Cin, p.Cout, q, lane);
 #pragma unroll 1
-      for (int t = 0; t < kWgTaps; ++t) {
+      for (int t = 0; t < (p.part_tma ? 0 : kWgTaps); ++t) {
         const int tap = tr * 3 + t;
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
@@ -4253,6 +4300,25 @@ int run_wgrad_c8(const void* x, const void* dy, float* dw, float* db, const Shap
   return launch_wgrad_reduce(prm.part, dw, db, (long long)s.Cout * 72, s.Cout, pl.S, pl.S, st);
 }
 
+// The wgrad partials part [S][Cout][9][Cin] fp32 as a 4-D map for TMA stores:
+// box {32 channels, 1 tap, 32 output channels, 1 split}, 128-byte swizzle
+// (the staging layout of wg_store_partials).  Taken for Cin >= 32 (a box
+// narrower than its tensor); CONV3X3_WGRAD_PART_TMA=0 keeps per-thread stores.
+bool make_part_map(CUtensorMap* m, float* part, int Cin, int Cout, int S) {
+  if (Cin < 32) return false;
+  if (const char* e = std::getenv("CONV3X3_WGRAD_PART_TMA"))
+    if (std::strcmp(e, "0") == 0) return false;
+  PFN_encodeTiled enc = encode_tiled_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)Cin, 9, (cuuint64_t)Cout, (cuuint64_t)S};
+  cuuint64_t strides[3] = {(cuuint64_t)Cin * 4, (cuuint64_t)Cin * 36, (cuuint64_t)Cout * Cin * 36};
+  cuuint32_t box[4] = {32, 1, 32, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, part, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s, void* ws,
              size_t ws_bytes, const CatSplit& cat, const DevCtx& d, cudaStream_t st) {
   if (!tc_supports_cat(s, cat)) return CONV3X3_ERR_UNSUPPORTED;
@@ -4316,12 +4382,14 @@ int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s
       tx2 = tx;
     }
   }
+  CUtensorMap tpart = tdy;  // (unused unless part_tma)
+  prm.part_tma = make_part_map(&tpart, prm.part, s.Cin, s.Cout, pl.S) ? 1 : 0;
 #define C3_WG(HW_)                                                                               \
   do {                                                                                           \
     using Cfg = WgCfg<HW_>;                                                                      \
     if (set_smem(k_wgrad<HW_>, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;     \
     launch_pdl(k_wgrad<HW_>, dim3(pl.tiles * pl.S), dim3(kThreads), Cfg::kSmem, st, tdy, tx, tx2, \
-               prm);                                                                             \
+               tpart, prm);                                                                      \
   } while (0)
   if (hw == 64)
     C3_WG(64);
