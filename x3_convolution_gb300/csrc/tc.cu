@@ -2526,8 +2526,9 @@ struct WgradParams {
 };
 
 // The dw partials of one wgrad CTA tile -- TMEM lanes = 128 output channels
-// from k0 = mb * 128, columns 128 t + c = tap 3 tr + t, input channel
-// cb * 128 + c -- written to part [S][Cout][9][Cin] through TMA tensor stores.
+// from k0, columns 128 t + c = tap 3 tr + t, input channel cb * 128 + c (tap
+// 2's columns 64.. sit `gap` columns later in the pair tile that owns dbias)
+// -- written to part [S][Cout][9][Cin] through TMA tensor stores.
 // Warp q stages its 32 rows of each 32-column chunk (4 KB, 128-byte swizzle)
 // in four rotating buffers of the (idle) stage memory at `stg`, and lane 0
 // stores the box {32 channels, 1 tap, 32 rows, 1 split} of map tmPart
@@ -2537,7 +2538,7 @@ struct WgradParams {
 // on the 384-channel 16x16 layer.
 __device__ __forceinline__ void wg_store_partials(const CUtensorMap* tmPart, uint8_t* stg, uint32_t lane_addr,
                                                   int tr, int cb, int k0, int split, int Cin, int Cout,
-                                                  int q, int lane) {
+                                                  int q, int lane, uint32_t gap = 0) {
   uint8_t* wbuf = stg + (size_t)q * 4 * 4096;
   int n = 0;
 #pragma unroll 1
@@ -2545,7 +2546,7 @@ __device__ __forceinline__ void wg_store_partials(const CUtensorMap* tmPart, uin
 #pragma unroll 1
     for (int j = 0; j < 4; ++j, ++n) {
       uint32_t v[32];
-      tmem_ld_32x32b_x32(lane_addr + (uint32_t)(t * 128 + j * 32), v);
+      tmem_ld_32x32b_x32(lane_addr + (uint32_t)(t * 128 + j * 32) + (t == 2 && j >= 2 ? gap : 0u), v);
       tmem_ld_wait();
       uint8_t* buf = wbuf + (n & 3) * 4096;
       // the store issued from this buffer four chunks ago has read it
@@ -2846,7 +2847,8 @@ static_assert(kWpStage % 1024 == 0 && kWpX2 % 1024 == 0, "swizzle atoms must sta
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_wgrad_pair(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmX,
-                 const __grid_constant__ CUtensorMap tmX2, const WgradParams p) {
+                 const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmPart,
+                 const WgradParams p) {
   constexpr int S = kWpStages;
   extern __shared__ uint8_t smem_raw[];
   // same offsets in both CTAs: the MMAs address the peer's operands at rank 0's
@@ -3023,8 +3025,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const long long dwsize = (long long)p.Cout * 9 * p.Cin;
       const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
       const uint32_t gap = do_bias ? 8u : 0u;  // the ones columns between tap 2's halves
+      if (p.part_tma)
+        wg_store_partials(&tmPart, smem, lane_addr, tr, cb, mb * 256 + (int)rank * 128, split, p.Cin, p.Cout, q,
+                          lane, gap);
 #pragma unroll 1
-      for (int t = 0; t < kWgTaps; ++t) {
+      for (int t = 0; t < (p.part_tma ? 0 : kWgTaps); ++t) {
         const int tap = tr * 3 + t;
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
@@ -4366,8 +4371,11 @@ int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s
     prm.S = pp.S;
     prm.num_mb = pp.num_mb;  // 256-channel pair blocks
     prm.num_cb = pp.num_cb;
+    CUtensorMap tpart = tdy;  // (unused unless part_tma)
+    prm.part_tma = make_part_map(&tpart, prm.part, s.Cin, s.Cout, pp.S) ? 1 : 0;
     if (set_smem(k_wgrad_pair, kWpSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
-    launch_pdl(k_wgrad_pair, dim3(2 * pp.tiles * pp.S), dim3(kThreads), kWpSmem, st, tdy, tx, tx2, prm);
+    launch_pdl(k_wgrad_pair, dim3(2 * pp.tiles * pp.S), dim3(kThreads), kWpSmem, st, tdy, tx, tx2, tpart,
+               prm);
     if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
     return launch_wgrad_reduce(prm.part, dw, db, (long long)s.Cout * 9 * s.Cin, s.Cout, pp.S, pp.S, st);
   }
