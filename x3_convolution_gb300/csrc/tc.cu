@@ -2511,6 +2511,7 @@ struct WgCfg {
   static_assert(kHW == 0 || kHW == 16 || kHW == 32 || kHW == 64, "row-shifted x for widths 16, 32, 64");
   static_assert(kStages >= 3, "wgrad stage ring too shallow");
   static_assert(kStageBytes % 1024 == 0 && kSlot % 1024 == 0, "swizzle atoms must stay 1 KB aligned");
+  static_assert(kStages * kStageBytes >= 2 * kWgEpiWarps * 4 * 4096, "partial staging fits in the stage ring");
 };
 
 struct WgradParams {
@@ -2528,29 +2529,30 @@ struct WgradParams {
 // The dw partials of one wgrad CTA tile -- TMEM lanes = 128 output channels
 // from k0, columns 128 t + c = tap 3 tr + t, input channel cb * 128 + c (tap
 // 2's columns 64.. sit `gap` columns later in the pair tile that owns dbias)
-// -- written to part [S][Cout][9][Cin] through TMA tensor stores.
-// Warp q stages its 32 rows of each 32-column chunk (4 KB, 128-byte swizzle)
-// in four rotating buffers of the (idle) stage memory at `stg`, and lane 0
-// stores the box {32 channels, 1 tap, 32 rows, 1 split} of map tmPart
-// ([S][Cout][9][Cin] fp32; rows past Cout and channels past Cin are clipped).
-// Each thread storing its own row with 16-byte stores made every warp store
-// touch 32 lines: the partials then took ~19,000 cycles of a 73,000-cycle CTA
-// on the 384-channel 16x16 layer.
+// -- written to part [S][Cout][9][Cin] through TMA tensor stores.  The
+// twelve 32-column chunks n = 4 t + j of lane quarter q are shared by two
+// warps (the epilogue warp takes n0 .. n1 = 0 .. 6, the idle producer warp of
+// the same quarter 6 .. 12).  A warp stages its 32 rows of a chunk (4 KB,
+// 128-byte swizzle) in four rotating buffers of its slot of the (idle) stage
+// memory at `stg`, and lane 0 stores the box {32 channels, 1 tap, 32 rows, 1
+// split} of map tmPart ([S][Cout][9][Cin] fp32; rows past Cout and channels
+// past Cin are clipped).  Each thread storing its own row with 16-byte stores
+// made every warp store touch 32 lines: the partials then took ~19,000 cycles
+// of a 73,000-cycle CTA on the 384-channel 16x16 layer.
 __device__ __forceinline__ void wg_store_partials(const CUtensorMap* tmPart, uint8_t* stg, uint32_t lane_addr,
                                                   int tr, int cb, int k0, int split, int Cin, int Cout,
-                                                  int q, int lane, uint32_t gap = 0) {
-  uint8_t* wbuf = stg + (size_t)q * 4 * 4096;
-  int n = 0;
+                                                  int q, int lane, uint32_t gap, int n0, int n1, int slot) {
+  uint8_t* wbuf = stg + (size_t)slot * 4 * 4096;
 #pragma unroll 1
-  for (int t = 0; t < kWgTaps; ++t) {
-#pragma unroll 1
-    for (int j = 0; j < 4; ++j, ++n) {
+  for (int n = n0; n < n1; ++n) {
+    const int t = n >> 2, j = n & 3;
+    {
       uint32_t v[32];
       tmem_ld_32x32b_x32(lane_addr + (uint32_t)(t * 128 + j * 32) + (t == 2 && j >= 2 ? gap : 0u), v);
       tmem_ld_wait();
-      uint8_t* buf = wbuf + (n & 3) * 4096;
+      uint8_t* buf = wbuf + ((n - n0) & 3) * 4096;
       // the store issued from this buffer four chunks ago has read it
-      if (n >= 4 && lane == 0) bulk_wait_read<3>();
+      if (n - n0 >= 4 && lane == 0) bulk_wait_read<3>();
       __syncwarp();
 #pragma unroll
       for (int g = 0; g < 8; ++g)
@@ -2696,6 +2698,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+    // this lane quarter's partial chunks 6 .. 11 (see wg_store_partials)
+    if (p.part_tma && mbar_wait(tfull, 0, p.wait_ns, p.status, abort_flag)) {
+      tc_fence_after();
+      wg_store_partials(&tmPart, smem, tmem_base + ((uint32_t)(warp * 32) << 16), tr, cb, mb * 128, split, p.Cin,
+                        p.Cout, warp, lane, 0u, 6, 12, kWgEpiWarps + warp);
+    }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idesc256 = idesc_bf16_f32(128, 256, 1, 1);
@@ -2778,7 +2786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long dwsize = (long long)p.Cout * 9 * p.Cin;
       const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
       if (p.part_tma)
-        wg_store_partials(&tmPart, smem, lane_addr, tr, cb, mb * 128, split, p.Cin, p.Cout, q, lane);
+        wg_store_partials(&tmPart, smem, lane_addr, tr, cb, mb * 128, split, p.Cin, p.Cout, q, lane, 0u, 0, 6, q);
 #pragma unroll 1
       for (int t = 0; t < (p.part_tma ? 0 : kWgTaps); ++t) {
         const int tap = tr * 3 + t;
@@ -2844,6 +2852,7 @@ constexpr int kWpStages = 4;
 constexpr size_t kWpSmem = (size_t)kWpStages * kWpStage + 256 + 1024 + 8 * 1024;
 static_assert(kWpStages >= kProd, "stage-parallel producers need S >= kProd");
 static_assert(kWpStage % 1024 == 0 && kWpX2 % 1024 == 0, "swizzle atoms must stay 1 KB aligned");
+static_assert(kWpStages * kWpStage >= 2 * kWgEpiWarps * 4 * 4096, "partial staging fits in the stage ring");
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_wgrad_pair(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmX,
@@ -2970,6 +2979,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+    // this lane quarter's partial chunks 6 .. 11 (see wg_store_partials)
+    if (p.part_tma && mbar_wait(tfull, 0, p.wait_ns, p.status, abort_flag)) {
+      tc_fence_after();
+      wg_store_partials(&tmPart, smem, tmem_base + ((uint32_t)(warp * 32) << 16), tr, cb,
+                        mb * 256 + (int)rank * 128, split, p.Cin, p.Cout, warp, lane, do_bias ? 8u : 0u, 6, 12,
+                        kWgEpiWarps + warp);
+    }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer (rank 0)
     if (rank == 0 && lane == 0) {
@@ -3027,7 +3043,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t gap = do_bias ? 8u : 0u;  // the ones columns between tap 2's halves
       if (p.part_tma)
         wg_store_partials(&tmPart, smem, lane_addr, tr, cb, mb * 256 + (int)rank * 128, split, p.Cin, p.Cout, q,
-                          lane, gap);
+                          lane, gap, 0, 6, q);
 #pragma unroll 1
       for (int t = 0; t < (p.part_tma ? 0 : kWgTaps); ++t) {
         const int tap = tr * 3 + t;
