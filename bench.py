@@ -360,29 +360,26 @@ def _wgrad(wl, i, sh, side=-1):
     return 2  # partial-sum kernel + fixed-order reduction
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one call of
-# each pass on the per-layer configs (stem, l1, l2, l3), from scoped ncu
-# captures -- one workload of one layer, the three calls of one step, DRAM
-# counters only -- and the SHA-256 of the kernel sources they were taken on: a
-# figure is reported only while those sources are unchanged.
-# DRAM bytes per call (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# scoped ncu capture per config: every launch of the call (the weight
-# gradient's kernel and its reduction), one pass each, caches flushed by ncu
-# before each launch -- so the reduction reads its split-K partials from DRAM
-# here, where in a step they are still in L2 -- and writes still in L2 when a
-# kernel ends are not counted.  Command: for each config, ncu --metrics
-# dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
-# --clock-control none -k regex:"k_(igemm|wgrad|stem)" -s 12 -c 4 on
-# bench.py --workload <config> --steps 1 --warmup 3 --no-e2e --no-cpu-baseline
-# --no-detail --no-gates --no-graph --wgrad-streams 1.
+# DRAM bytes per call (dram__bytes_read.sum + dram__bytes_write.sum) of each
+# pass on the per-layer configs (stem, l1, l2, l3), from one scoped ncu capture
+# per config -- every launch of the call (the weight gradient's kernel and its
+# reduction), DRAM counters only, one pass each, caches flushed by ncu before
+# each launch, so the reduction reads its split-K partials from DRAM here where
+# in a step they are still in L2, and writes still in L2 when a kernel ends are
+# not counted -- and the SHA-256 of the kernel sources they were taken on: a
+# figure is reported only while those sources are unchanged.  Command: for each
+# config, ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,
+# gpu__time_duration.sum --clock-control none -k regex:"k_(igemm|wgrad|stem)"
+# -s 12 -c 4 on bench.py --workload <config> --steps 1 --warmup 3 --no-e2e
+# --no-cpu-baseline --no-detail --no-gates --no-graph --wgrad-streams 1.
 RECORDED_TRAFFIC: dict = {   # {(config, pass): bytes per call}
-    ("stem", "fwd"): 10494208, ("stem", "dgrad"): 67160064, ("stem", "wgrad"): 77049856,
-    ("l1", "fwd"): 91642368, ("l1", "dgrad"): 87848960, ("l1", "wgrad"): 165497856,
-    ("l2", "fwd"): 34775040, ("l2", "dgrad"): 34772992, ("l2", "wgrad"): 95711232,
-    ("l3", "fwd"): 15265792, ("l3", "dgrad"): 15262720, ("l3", "wgrad"): 51855104,
+    ("stem", "fwd"): 10169344, ("stem", "dgrad"): 67188992, ("stem", "wgrad"): 77079552,
+    ("l1", "fwd"): 91368960, ("l1", "dgrad"): 86936320, ("l1", "wgrad"): 165451008,
+    ("l2", "fwd"): 34774016, ("l2", "dgrad"): 34783232, ("l2", "wgrad"): 95655680,
+    ("l3", "fwd"): 15267328, ("l3", "dgrad"): 15282688, ("l3", "wgrad"): 51757568,
 }
 TRAFFIC_SOURCES = ("tc.cu", "simt.cu", "ptx.cuh", "conv3x3_internal.h")
-TRAFFIC_SHA256 = "ae8554201ec5696c08dc979c81400610383498e8635fb6817eac4681c746bb3b"
+TRAFFIC_SHA256 = "a05c5366cb98e2ad44848838637bff16c236e4d0110ef74514532db3072e170d"
 
 
 def sources_sha256():
