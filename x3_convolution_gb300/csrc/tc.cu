@@ -148,6 +148,10 @@ struct IgemmParams {
   const __nv_bfloat16* zin = nullptr;
   const __nv_bfloat16* zin2 = nullptr;
   int zin_act = CONV3X3_ACT_NONE;
+  // bf16 output through TMA stores of {64 channels, 32 pixels} boxes (map
+  // tmY), staged in the idle stage ring: set only where every CTA (or pair)
+  // has one tile and the output is one plain bf16 tensor
+  int epi_tma = 0;
 };
 
 // Where output column col0 of pixel `pix` lives.  Columns [0, nsplit) are in
@@ -241,22 +245,9 @@ __device__ __forceinline__ void bias_from_slice(const float* sl, float (&bv)[32]
   }
 }
 
-// Epilogue of one 32-column chunk: (+ bias) -> [store z] -> activation ->
-// [* act'(z_in)] -> fp32 or bf16 store.  kExt = false compiles out the fused
-// extras (z store, z_in scaling, split output) for the plain calls; kTanh
-// takes SiLU through tanh (silu_tanh_f32).
-template <bool kExt, bool kTanh = C3_SILU_TANH>
-__device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix, int col0,
-                                            const uint32_t (&v)[32], const float (&bv)[32],
-                                            const uint4 (&zr)[4]) {
-  float f[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-  if (p.bias) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) f[i] += bv[i];
-  }
-  if (kExt && p.zout) store_bf16x32(p.zout + pix * p.nout + col0, p.nout - col0, f);
+// Activation, then the fused z_in scaling (act'(z_in)), on one chunk in fp32.
+template <bool kExt, bool kTanh>
+__device__ __forceinline__ void epi_act_zin(const IgemmParams& p, float (&f)[32], const uint4 (&zr)[4]) {
   if (p.act == CONV3X3_ACT_SILU) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) f[i] = kTanh ? silu_tanh_f32(f[i]) : silu_f32(f[i]);
@@ -276,6 +267,48 @@ __device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix,
       }
     }
   }
+}
+
+// One 32-column chunk of the TMA-store epilogue (epi_tma): bias, activation
+// and z_in scaling in fp32 as in store_chunk, one bf16 rounding, and the
+// thread's 64 bytes staged as 16-byte pieces c0 .. c0 + 3 of its 128-byte row
+// `row` of a {64 channels, 32 pixels} box, piece c at c ^ (lane % 8) (the
+// 128-byte swizzle: eight rows of a store phase cover all 32 banks).
+template <bool kExt, bool kTanh = C3_SILU_TANH>
+__device__ __forceinline__ void stage_chunk_bf16(const IgemmParams& p, const uint32_t (&v)[32],
+                                                 const float (&bv)[32], const uint4 (&zr)[4], uint8_t* row,
+                                                 int c0, int lane) {
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]) + (p.bias ? bv[i] : 0.0f);
+  epi_act_zin<kExt, kTanh>(p, f, zr);
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[8 * g + 2 * i], f[8 * g + 2 * i + 1]);
+    *reinterpret_cast<uint4*>(row + (((c0 + g) ^ (lane & 7)) << 4)) = u;
+  }
+}
+
+// Epilogue of one 32-column chunk: (+ bias) -> [store z] -> activation ->
+// [* act'(z_in)] -> fp32 or bf16 store.  kExt = false compiles out the fused
+// extras (z store, z_in scaling, split output) for the plain calls; kTanh
+// takes SiLU through tanh (silu_tanh_f32).
+template <bool kExt, bool kTanh = C3_SILU_TANH>
+__device__ __forceinline__ void store_chunk(const IgemmParams& p, long long pix, int col0,
+                                            const uint32_t (&v)[32], const float (&bv)[32],
+                                            const uint4 (&zr)[4]) {
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+  if (p.bias) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] += bv[i];
+  }
+  if (kExt && p.zout) store_bf16x32(p.zout + pix * p.nout + col0, p.nout - col0, f);
+  epi_act_zin<kExt, kTanh>(p, f, zr);
   const OutPos o = kExt ? out_pos(p, pix, col0) : OutPos{pix * p.nout + col0, p.nout - col0, false};
   void* base = (kExt && o.second) ? p.out2 : p.out;
   if (p.out_f32) {
@@ -352,7 +385,8 @@ __device__ __forceinline__ void s2_tap(int cls, int t, int& wtap, int& dj, int& 
 template <int BN, int MT, bool kDgrad, bool kExt, int KC, bool kT = false>
 __global__ void __launch_bounds__(kIgemmThreads, 1)
     k_igemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
-            const __grid_constant__ CUtensorMap tmB, const IgemmParams p) {
+            const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY,
+            const IgemmParams p) {
   static_assert(!kT || (MT == 2 && BN == BM && KC == 1), "transposed tiles are 128 channels x 256 pixels");
   using Cfg = IgemmCfg<BN, MT, KC>;
   constexpr int S = Cfg::kStages;
@@ -684,8 +718,39 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
                              (uint32_t)((buf * MT + sub) * BN + col_off);
+      if constexpr (kCols % 64 == 0) {
+        if (p.epi_tma) {
+          // one tile per CTA: the stage ring is idle; this warp's 32 pixels
+          // leave as kCols / 64 boxes of {64 channels, 32 pixels}
+          uint8_t* stg = smem + (size_t)(warp - kEpiBase) * (kCols / 64) * 4096u;
+          const long long wrow0 = (long long)mt * TM + sub * BM + q * 32;
 #pragma unroll 1
-      for (int j = 0; j < kCols / 32; ++j) {
+          for (int j = 0; j < kCols / 32; ++j) {
+            const int col0 = nt * BN + col_off + j * 32;
+            float bv[32];
+            if (p.bias) bias_from_slice(bsl + j * 32, bv);
+            uint4 zr[4] = {};
+            if (kExt && p.zin && valid && col0 < p.nout) load_zin(p, pix, col0, zr);
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
+            tmem_ld_wait();
+            uint8_t* box = stg + (j >> 1) * 4096u;
+            stage_chunk_bf16<kExt>(p, v, bv, zr, box + lane * 128, (j & 1) * 4, lane);
+            if (j & 1) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0 && col0 - 32 < p.nout && wrow0 < p.P) tma_store_2d(&tmY, box, col0 - 32, (int)wrow0);
+            }
+          }
+          if (lane == 0) {
+            bulk_commit();
+            bulk_wait<0>();
+          }
+          __syncwarp();
+        }
+      }
+#pragma unroll 1
+      for (int j = 0; j < (p.epi_tma && kCols % 64 == 0 ? 0 : kCols / 32); ++j) {
         const int col0 = nt * BN + col_off + j * 32;
         const bool live = valid && col0 < p.nout;
         // operands that do not depend on the accumulator are loaded first
@@ -772,7 +837,8 @@ struct PairCfg {
 template <bool kDgrad, bool kExt, int BN = 256, int KC = 1>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
     k_igemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
-                 const __grid_constant__ CUtensorMap tmB, const IgemmParams p) {
+                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY,
+                 const IgemmParams p) {
   using Cfg = PairCfg<BN, kDgrad, KC>;
   constexpr int S = Cfg::kStages;
   constexpr bool kSP = Cfg::kSP;
@@ -1005,8 +1071,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kPairBN + col_off);
+      if constexpr (kCols % 64 == 0) {
+        if (p.epi_tma) {
+          // one tile per pair: both stage rings are idle (every MMA of the
+          // tile has completed); this warp's 32 pixels leave as kCols / 64
+          // boxes of {64 channels, 32 pixels}
+          uint8_t* stg = smem + (size_t)(warp - kEpiBase) * (kCols / 64) * 4096u;
+          const long long wrow0 = (long long)mt * 2 * BM + rank * BM + q * 32;
 #pragma unroll 1
-      for (int j = 0; j < kCols / 32; ++j) {
+          for (int j = 0; j < kCols / 32; ++j) {
+            const int col0 = nt * kPairBN + col_off + j * 32;
+            float bv[32];
+            if (p.bias) bias_from_slice(bsl + j * 32, bv);
+            uint4 zr[4] = {};
+            if (kExt && p.zin && valid && col0 < p.nout) load_zin(p, pix, col0, zr);
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(taddr + (uint32_t)(j * 32), v);
+            tmem_ld_wait();
+            uint8_t* box = stg + (j >> 1) * 4096u;
+            stage_chunk_bf16<kExt>(p, v, bv, zr, box + lane * 128, (j & 1) * 4, lane);
+            if (j & 1) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0 && col0 - 32 < p.nout && wrow0 < p.P) tma_store_2d(&tmY, box, col0 - 32, (int)wrow0);
+            }
+          }
+          if (lane == 0) {
+            bulk_commit();
+            bulk_wait<0>();
+          }
+          __syncwarp();
+        }
+      }
+#pragma unroll 1
+      for (int j = 0; j < (p.epi_tma && kCols % 64 == 0 ? 0 : kCols / 32); ++j) {
         const int col0 = nt * kPairBN + col_off + j * 32;
         const bool live = valid && col0 < p.nout;
         float bv[32];
@@ -3579,6 +3677,19 @@ int set_smem(K kernel, size_t bytes, int device) {
   return CONV3X3_OK;
 }
 
+// The TMA-store epilogue (IgemmParams::epi_tma) where every CTA or pair has
+// one tile and the output is one plain bf16 tensor; `ty` then maps it.
+// CONV3X3_EPI_TMA=0 keeps the per-thread row stores.
+int make_store_map(CUtensorMap* m, void* base, long long P, int C);
+void epi_tma_setup(IgemmParams& p, int tiles, int slots, const CUtensorMap& dummy, CUtensorMap* ty) {
+  *ty = dummy;
+  p.epi_tma = 0;
+  if (tiles > slots || p.out_f32 || p.zout || p.out2 || p.s2 || p.nsplit != p.nout || p.nout % 8) return;
+  if (const char* e = std::getenv("CONV3X3_EPI_TMA"))
+    if (std::strcmp(e, "0") == 0) return;
+  p.epi_tma = make_store_map(ty, p.out, p.P, p.nout) == CONV3X3_OK ? 1 : 0;
+}
+
 template <int BN, int MT, bool kDgrad, int KC = 1, bool kT = false>
 int launch_igemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
                  const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
@@ -3589,7 +3700,10 @@ int launch_igemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap&
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int tiles = (prm.s2 ? 4 : 1) * prm.num_m_tiles * prm.num_n_tiles;
   const int grid = tiles < d.num_sms ? tiles : d.num_sms;
-  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, a2, b, prm);
+  IgemmParams p2 = prm;
+  CUtensorMap ty;
+  epi_tma_setup(p2, kT ? 0x7fffffff : tiles, grid, a, &ty);  // (the transposed tile has its own epilogue)
+  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, a2, b, ty, p2);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
@@ -3633,7 +3747,10 @@ int launch_igemm_pair(const CUtensorMap& a, const CUtensorMap& a2, const CUtenso
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
   const int pairs = pair_slots(kern, Cfg::kSmem, d);
   const int grid = 2 * (tiles < pairs ? tiles : pairs);
-  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, a2, b, prm);
+  IgemmParams p2 = prm;
+  CUtensorMap ty;
+  epi_tma_setup(p2, tiles, grid / 2, a, &ty);
+  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, a2, b, ty, p2);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
