@@ -79,10 +79,21 @@
  * for width 64 only.  CONV3X3_WGRAD_PAIR=0 keeps the weight gradient of Cout a
  * multiple of 256 on one-CTA tiles (by default, where x is staged as im2col
  * boxes, it runs on two-CTA clusters with 256-output-channel tiles; the
- * workspace size covers either).  CONV3X3_STEM_ROWS=0 makes the 8-input-channel forward
+ * workspace size covers either).  CONV3X3_WGRAD_HYBRID=0|1 forbids (or forces,
+ * wherever it applies) the split of a Cout above 256 that is not a multiple of
+ * 256 into two-CTA tiles over its first 256 k channels and one-CTA tiles over
+ * the rest, two launches with one workspace and one reduction (unset: where
+ * the one-CTA plan would leave over a quarter of the SMs idle).
+ * CONV3X3_WGRAD_PART_TMA=0 makes the weight gradient write its split partials
+ * with per-thread stores instead of TMA tensor stores (at least 32 input
+ * channels).  CONV3X3_EPI_TMA=0 makes forward and input-gradient tiles store
+ * their output from each thread instead of through TMA tensor stores (taken
+ * for one plain bf16 output where every CTA or CTA pair has one tile).
+ * CONV3X3_STEM_ROWS=0 makes the 8-input-channel forward
  * and weight gradient stage x as im2col boxes even where they would stage
- * whole image rows (forward: widths 32 and 64; weight gradient: width 64, one
- * box of three zero-padded image rows per 64-pixel k-block).
+ * whole image rows (forward: widths 32 and 64; weight gradient: width 64,
+ * three column-shifted copies of three zero-padded image rows per 64-pixel
+ * k-block).
  * CONV3X3_STEM_DGRAD=rows runs the 8-output-channel input gradient of width 64
  * as row bands instead of tiles.
  * CONV3X3_PDL=0 launches without programmatic dependent launch (by default a

@@ -501,6 +501,49 @@ def test_wgrad_pair_tiles(shape, pair, monkeypatch):
     assert torch.equal(dw, dw2) and torch.equal(db, db2)
 
 
+WGRAD_HYBRID_SHAPES = [
+    # N, Cin, Cout, H, W: Cout above 256 and not a multiple of it -- pair tiles
+    # over the first 256 k output channels, one-CTA tiles over the rest
+    (2, 128, 384, 8, 8),     # 256 + one 128-channel block
+    (1, 64, 320, 5, 7),      # 256 + half a block, ragged pixel tail
+    (1, 72, 448, 9, 9),      # 256 + one and a half blocks, ragged 64-channel box
+    (3, 256, 384, 16, 16),   # several channel blocks and splits
+    (1, 192, 640, 6, 6),     # 512 + 128: two pair blocks
+]
+
+
+@pytest.mark.parametrize("hybrid", ["1", "0"], ids=["hybrid", "one_cta"])
+@pytest.mark.parametrize("shape", WGRAD_HYBRID_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_wgrad_hybrid_tiles(shape, hybrid, monkeypatch):
+    # the two parts have split plans of their own; dw rows and dbias entries
+    # of each part are summed over that part's splits only
+    monkeypatch.setenv("CONV3X3_WGRAD_HYBRID", hybrid)
+    t = _small(shape, seed=29)
+    x, _, _, dy = dev_tensors(t)
+    dw, db = ops.wgrad(x, dy, path=L.PATH_TENSOR)
+    dw2, db2 = ops.wgrad(x, dy, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    rdw, rdb = oracle.conv3x3_wgrad(t.x, t.dy)
+    assert rel_err(host(dw), rdw) <= TOL_BF16
+    assert rel_err(host(db), rdb) <= TOL_BF16
+    assert torch.equal(dw, dw2) and torch.equal(db, db2)
+
+
+@pytest.mark.parametrize("splits", ["1", "5"])
+def test_wgrad_hybrid_forced_splits_and_concat(splits, monkeypatch):
+    # one split count forced on both parts, and x from two tensors
+    monkeypatch.setenv("CONV3X3_WGRAD_SPLITS", splits)
+    N, Ca, Cb, Cout, H, W = 1, 128, 64, 384, 8, 10
+    t = _small((N, Ca + Cb, Cout, H, W), seed=31)
+    x, _, _, dy = dev_tensors(t)
+    xa, xb = x[..., :Ca].contiguous(), x[..., Ca:].contiguous()
+    dw, db = ops.wgrad_cat(xa, xb, dy, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    rdw, rdb = oracle.conv3x3_wgrad(t.x, t.dy)
+    assert rel_err(host(dw), rdw) <= TOL_BF16
+    assert rel_err(host(db), rdb) <= TOL_BF16
+
+
 @pytest.mark.parametrize("splits", ["1", "3", "10"])
 def test_wgrad_pair_split_counts(splits, monkeypatch):
     # 624 pixels = 10 k-blocks, the last one 48 pixels: one split, splits of

@@ -459,20 +459,30 @@ __global__ void __launch_bounds__(kThreads) k_wgrad_bf16_c8_partial(
   }
 }
 
+// The split counts of one reduction: the partials hold Sreg slices of dw, then
+// Sreg rows of dbias; output channels below k1 (dw rows, and dbias entries)
+// have S1 valid splits, the others S2 (a weight gradient computed in two
+// parts with two split plans; k1 = Cout when there is one).
+struct RedSplits {
+  int Sreg, S1, S2, k1;
+};
+
 // dw[e] = sum_{s=0}^{S-1} part[s][e] in increasing s (four partials loaded at a
 // time, added strictly in order), four elements per thread; dbias likewise
-// over its Sdb partial rows stored after the S dw slices.  For layers whose
+// over its partial rows stored after the Sreg dw slices.  For layers whose
 // split count is small (a few partials of a large dw).
 __global__ void k_wgrad_reduce(const float* __restrict__ part, float* __restrict__ dw,
-                               float* __restrict__ db, long long dwsize, int Cout, int S, int Sdb) {
+                               float* __restrict__ db, long long dwsize, int Cout, RedSplits rs) {
   pdl_trigger();
   pdl_wait();  // the partials of the kernel before
   const long long n4 = dwsize / 4;
+  const long long n1 = (long long)rs.k1 * (dwsize / Cout) / 4;  // float4 columns of rows < k1
   const long long total = n4 + Cout;
   const float4* p4 = reinterpret_cast<const float4*>(part);
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
     if (e < n4) {
+      const int S = e < n1 ? rs.S1 : rs.S2;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       int s = 0;
       for (; s + 4 <= S; s += 4) {
@@ -492,8 +502,9 @@ __global__ void k_wgrad_reduce(const float* __restrict__ part, float* __restrict
       reinterpret_cast<float4*>(dw)[e] = acc;
     } else if (db) {
       const long long k = e - n4;
+      const int S = k < rs.k1 ? rs.S1 : rs.S2;
       float acc = 0.0f;
-      for (int s = 0; s < Sdb; ++s) acc += part[(long long)S * dwsize + (long long)s * Cout + k];
+      for (int s = 0; s < S; ++s) acc += part[(long long)rs.Sreg * dwsize + (long long)s * Cout + k];
       db[k] = acc;
     }
   }
@@ -516,22 +527,23 @@ constexpr int kRedThreads = 256;
 template <int G>
 __global__ void __launch_bounds__(kRedThreads)
     k_wgrad_reduce_wide(const float* __restrict__ part, float* __restrict__ dw, float* __restrict__ db,
-                        long long dwsize, int Cout, int S, int Sdb) {
+                        long long dwsize, int Cout, RedSplits rs) {
   constexpr int CW = kRedThreads / G;  // float4 columns per block
   __shared__ float4 red[G][CW];
   pdl_trigger();
   pdl_wait();  // the partials of the kernel before
   const int x = threadIdx.x, g = threadIdx.y;
   const long long n4 = dwsize / 4;
+  const long long n1 = (long long)rs.k1 * (dwsize / Cout) / 4;  // float4 columns of rows < k1
   const long long col = blockIdx.x * (long long)CW + x;
   const bool bias_col = col >= n4;
   const long long total = n4 + (db ? Cout / 4 : 0);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (col < total) {
-    const float4* src = reinterpret_cast<const float4*>(bias_col ? part + (long long)S * dwsize : part);
+    const float4* src = reinterpret_cast<const float4*>(bias_col ? part + (long long)rs.Sreg * dwsize : part);
     const long long c = bias_col ? col - n4 : col;
     const long long stride = bias_col ? Cout / 4 : n4;
-    const int n = bias_col ? Sdb : S;
+    const int n = (bias_col ? 4 * c < rs.k1 : c < n1) ? rs.S1 : rs.S2;
 #pragma unroll 4
     for (int sp = g; sp < n; sp += G) {
       const float4 a = __ldg(src + (long long)sp * stride + c);
@@ -610,21 +622,28 @@ WgradPlan wgrad_plan(const Shape& s) {
 // eight split groups per column from there on.
 constexpr int kWideSplits = 16;
 
-int launch_wgrad_reduce(const float* part, float* dw, float* db, long long dwsize, int Cout, int S,
-                        int Sdb, cudaStream_t st) {
-  if (S >= kWideSplits) {
+int launch_wgrad_reduce2(const float* part, float* dw, float* db, long long dwsize, int Cout, int Sreg,
+                         int S1, int S2, int k1, cudaStream_t st) {
+  const RedSplits rs{Sreg, S1, S2, k1};
+  if ((S1 > S2 ? S1 : S2) >= kWideSplits) {
     const long long cols = dwsize / 4 + (db ? Cout / 4 : 0);
     if (cols < 2LL * kPlanSms * 32)
       launch_pdl(k_wgrad_reduce_wide<32>, dim3((unsigned)((cols + 7) / 8)), dim3(8, 32), 0, st, part,
-                 dw, db, dwsize, Cout, S, Sdb);
+                 dw, db, dwsize, Cout, rs);
     else
       launch_pdl(k_wgrad_reduce_wide<8>, dim3((unsigned)((cols + 31) / 32)), dim3(32, 8), 0, st, part,
-                 dw, db, dwsize, Cout, S, Sdb);
+                 dw, db, dwsize, Cout, rs);
   } else {
     launch_pdl(k_wgrad_reduce, dim3(grid_for(dwsize / 4 + Cout)), dim3(kThreads), 0, st, part, dw, db,
-               dwsize, Cout, S, Sdb);
+               dwsize, Cout, rs);
   }
   return launch_status();
+}
+
+int launch_wgrad_reduce(const float* part, float* dw, float* db, long long dwsize, int Cout, int S,
+                        int Sdb, cudaStream_t st) {
+  (void)Sdb;  // dbias has as many partial rows as dw has slices
+  return launch_wgrad_reduce2(part, dw, db, dwsize, Cout, S, S, S, Cout, st);
 }
 
 // ---------------------------------------------------------------- launchers

@@ -47,6 +47,8 @@
 
 namespace c3 {
 
+int launch_wgrad_reduce2(const float* part, float* dw, float* db, long long dwsize, int Cout, int Sreg,
+                         int S1, int S2, int k1, cudaStream_t st);
 int launch_wgrad_reduce(const float* part, float* dw, float* db, long long dwsize, int Cout, int S,
                         int Sdb, cudaStream_t st);
 
@@ -744,7 +746,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
           }
           if (lane == 0) {
             bulk_commit();
-            bulk_wait<0>();
+            bulk_wait_read<0>();  // the stores' writes complete with the grid
           }
           __syncwarp();
         }
@@ -1098,7 +1100,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
           }
           if (lane == 0) {
             bulk_commit();
-            bulk_wait<0>();
+            bulk_wait_read<0>();  // the stores' writes complete with the grid
           }
           __syncwarp();
         }
@@ -1961,8 +1963,9 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
         acc_phase ^= 1;
       }
     }
-    // every store has completed before the CTA's shared memory goes away
-    if (lane == 0) bulk_wait<0>();
+    // every store has read its staging buffer before the CTA's shared memory
+    // goes away (the writes themselves complete with the grid)
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
   } else {
     // epilogue: as in k_igemm with one 128-pixel sub-tile (the two warps of a
@@ -2622,6 +2625,7 @@ struct WgradParams {
   unsigned* status;
   unsigned long long wait_ns;
   int part_tma = 0;    // the dw partials leave through tmPart (see wg_store_partials)
+  int mb0 = 0;         // first 128-channel block of Cout this launch covers (k_wgrad)
 };
 
 // The dw partials of one wgrad CTA tile -- TMEM lanes = 128 output channels
@@ -2665,7 +2669,7 @@ __device__ __forceinline__ void wg_store_partials(const CUtensorMap* tmPart, uin
       }
     }
   }
-  if (lane == 0) bulk_wait<0>();
+  if (lane == 0) bulk_wait_read<0>();  // the stores' writes complete with the grid
   __syncwarp();
 }
 
@@ -2691,7 +2695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_tiles = p.num_mb * 3 * p.num_cb;
   const int tile = blockIdx.x % num_tiles;
   const int split = blockIdx.x / num_tiles;
-  const int mb = tile % p.num_mb;
+  const int mb = p.mb0 + tile % p.num_mb;
   const int rest = tile / p.num_mb;
   const int cb = rest % p.num_cb;
   const int tr = rest / p.num_cb;  // kernel row r: taps 3r .. 3r+2
@@ -4268,6 +4272,28 @@ WgPlan wg_plan(const Shape& s) {
 // Two-CTA wgrad: Cout a multiple of 256 (pair tiles of 256 output channels).
 bool wg_pair_shape(const Shape& s) { return s.Cout % 256 == 0; }
 
+// Output channels [0, cpair) of a Cout above 256 that is not a multiple of
+// 256 run as pair tiles, the rest [cpair, Cout) on one-CTA tiles, in two
+// launches with a split plan each (one workspace, one reduction): 0 where
+// that is not taken.  Each part pays its own fill, partial write and launch,
+// so the hybrid is taken only where the one-CTA plan for all of Cout leaves
+// over a quarter of the SMs idle.  Measured on GB300 (batch 64, 16x16):
+// 768 -> 384 (108 of 152 SMs busy) 81 -> 69 us; 384 -> 384 (135 busy)
+// 42 -> 56 us and 256 -> 384 (144 busy) 31 -> 46 us, so both keep one-CTA
+// tiles.  CONV3X3_WGRAD_HYBRID=1 takes it wherever it applies, =0 nowhere.
+int wg_hybrid_cpair(const Shape& g) {
+  if (g.Cout <= 256 || wg_pair_shape(g)) return 0;
+  int mode = -1;
+  if (const char* e = std::getenv("CONV3X3_WGRAD_HYBRID")) mode = std::strcmp(e, "0") == 0 ? 0 : 1;
+  if (mode == 0) return 0;
+  if (mode < 0) {
+    const WgPlan pl = wg_plan(g);
+    if (4LL * pl.tiles * pl.S >= 3LL * kPlanSms) return 0;
+  }
+  return g.Cout / 256 * 256;
+}
+
+
 // Split plan of k_wgrad_pair: the same cost model over pair tiles and the
 // kPlanSms / 2 cluster slots.
 WgPlan wg_plan_pair(const Shape& s) {
@@ -4299,6 +4325,27 @@ WgPlan wg_plan_pair(const Shape& s) {
   pl.kb_per_split = (pl.kb_total + bestS - 1) / bestS;
   pl.S = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
   return pl;
+}
+
+// The two parts of a hybrid weight gradient (wg_hybrid_cpair): the pair plan
+// over output channels [0, cpair), the one-CTA plan over [cpair, Cout), and
+// the slices of their shared workspace (the larger split count).
+struct WgHybrid {
+  int cpair;
+  WgPlan pp, ps;
+  int Sreg;
+};
+
+WgHybrid wg_plan_hybrid(const Shape& g) {
+  WgHybrid h;
+  h.cpair = wg_hybrid_cpair(g);
+  Shape gp = g, gs = g;
+  gp.Cout = h.cpair;
+  gs.Cout = g.Cout - h.cpair;
+  h.pp = wg_plan_pair(gp);
+  h.ps = wg_plan(gs);
+  h.Sreg = h.pp.S > h.ps.S ? h.pp.S : h.ps.S;
+  return h;
 }
 
 }  // namespace
@@ -4388,6 +4435,10 @@ size_t tc_wgrad_workspace(const Shape& s, int /*num_sms*/) {
   if (wg_pair_shape(g)) {
     const int Sp = wg_plan_pair(g).S;
     if (Sp > S) S = Sp;
+  }
+  if (wg_hybrid_cpair(g)) {
+    const WgHybrid h = wg_plan_hybrid(g);
+    if (h.Sreg > S) S = h.Sreg;
   }
   long long dwsize = (long long)s.Cout * 9 * s.Cin;
   return (size_t)S * (size_t)(dwsize + s.Cout) * sizeof(float);
@@ -4494,9 +4545,10 @@ int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s
   const int hw = wg_row_width(s);
   // Two-CTA tiles for Cout a multiple of 256 with im2col x;
   // CONV3X3_WGRAD_PAIR=0 keeps the one-CTA kernel, =1 is the default.
-  bool pair = hw == 0 && wg_pair_shape(g);
+  bool pair_ok = true;
   if (const char* e = std::getenv("CONV3X3_WGRAD_PAIR"))
-    if (std::strcmp(e, "0") == 0) pair = false;
+    if (std::strcmp(e, "0") == 0) pair_ok = false;
+  const bool pair = hw == 0 && pair_ok && wg_pair_shape(g);
   if (pair) {
     const WgPlan pp = wg_plan_pair(g);
     prm.kb_total = pp.kb_total;
@@ -4511,6 +4563,40 @@ int tc_wgrad(const void* x, const void* dy, float* dw, float* db, const Shape& s
                prm);
     if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
     return launch_wgrad_reduce(prm.part, dw, db, (long long)s.Cout * 9 * s.Cin, s.Cout, pp.S, pp.S, st);
+  }
+  const int cpair = (hw == 0 && pair_ok) ? wg_hybrid_cpair(g) : 0;
+  if (cpair) {
+    // pair tiles over output channels [0, cpair), then one-CTA tiles over
+    // [cpair, Cout); both write the shared workspace (Sreg slices), and the
+    // reduction sums each part's own splits
+    const WgHybrid h = wg_plan_hybrid(g);
+    CUtensorMap tpart = tdy;  // (unused unless part_tma)
+    const int part_tma = make_part_map(&tpart, prm.part, s.Cin, s.Cout, h.Sreg) ? 1 : 0;
+    WgradParams pa = prm;
+    pa.kb_total = h.pp.kb_total;
+    pa.kb_per_split = h.pp.kb_per_split;
+    pa.S = h.Sreg;
+    pa.num_mb = h.pp.num_mb;
+    pa.num_cb = h.pp.num_cb;
+    pa.part_tma = part_tma;
+    if (set_smem(k_wgrad_pair, kWpSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+    launch_pdl(k_wgrad_pair, dim3(2 * h.pp.tiles * h.pp.S), dim3(kThreads), kWpSmem, st, tdy, tx, tx2, tpart,
+               pa);
+    if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
+    WgradParams pb = prm;
+    pb.kb_total = h.ps.kb_total;
+    pb.kb_per_split = h.ps.kb_per_split;
+    pb.S = h.Sreg;
+    pb.num_mb = h.ps.num_mb;
+    pb.num_cb = h.ps.num_cb;
+    pb.mb0 = cpair / 128;
+    pb.part_tma = part_tma;
+    if (set_smem(k_wgrad<0>, WgCfg<0>::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+    launch_pdl(k_wgrad<0>, dim3(h.ps.tiles * h.ps.S), dim3(kThreads), WgCfg<0>::kSmem, st, tdy, tx, tx2, tpart,
+               pb);
+    if (cudaGetLastError() != cudaSuccess) return CONV3X3_ERR_CUDA;
+    return launch_wgrad_reduce2(prm.part, dw, db, (long long)s.Cout * 9 * s.Cin, s.Cout, h.Sreg, h.pp.S, h.ps.S,
+                                cpair, st);
   }
   if (hw) {
     // row-shifted x: per image row one box of (W + 2) pixels x 64 channels
