@@ -1010,3 +1010,66 @@ def test_downsampling_layers_full_size_sampled(index):
     assert np.max(np.abs(dwh[iw] - rw)) / np.max(np.abs(rw)) <= TOL_BF16
     rdb = oracle.conv3x3_wgrad_strided_at(t.x, t.dy, 2, dwh.size + np.arange(Lr.Cout))
     assert rel_err(host(db), rdb) <= TOL_BF16
+
+
+# Store paths.  The output and the weight gradient's split partials leave
+# through TMA tensor stores where the library takes them; the per-thread store
+# path that replaces them (CONV3X3_EPI_TMA=0, CONV3X3_WGRAD_PART_TMA=0) holds
+# the same values, so both must give bit-identical tensors.
+EPI_STORE_SHAPES = [
+    # N, Cin, Cout, H, W: one tile per CTA (or CTA pair) for every tile kind
+    (2, 64, 128, 12, 12),     # 128x1 tiles, ragged pixel tail
+    (1, 256, 256, 16, 16),    # two-CTA 256-channel tiles
+    (2, 384, 384, 16, 16),    # two-CTA 384-channel tiles
+    (1, 128, 200, 9, 7),      # channels past the last 64-wide box are clipped
+    (2, 512, 512, 8, 8),      # the 8x8 layer's tiles
+]
+
+
+@pytest.mark.parametrize("shape", EPI_STORE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_output_tma_stores_match_thread_stores(shape, monkeypatch):
+    t = _small(shape, seed=37)
+    x, w, b, dy = dev_tensors(t)
+    zin = to_dev_bf16(synth.make_zin(t.layer, seed=37))  # laid out like dx
+
+    def run():
+        y = ops.fwd(x, w, b, act=1)
+        dx = ops.dgrad(dy, w)
+        gx = ops.dgrad(dy, w, z_in=zin, act_in=1)
+        torch.cuda.synchronize()
+        return y, dx, gx
+
+    a = run()
+    monkeypatch.setenv("CONV3X3_EPI_TMA", "0")
+    c = run()
+    for u, v in zip(a, c):
+        assert torch.equal(u, v)
+    y32 = ops.fwd(x, w, b, act=1, out_dtype=L.DT_F32)
+    torch.cuda.synchronize()
+    assert rel_err(host(y32), oracle.conv3x3_fwd(t.x, t.w, t.bias, 1)) <= TOL_BF16
+
+
+WGRAD_STORE_SHAPES = [
+    (2, 128, 128, 16, 16),    # one-CTA tiles, im2col x
+    (2, 128, 128, 8, 64),     # one-CTA tiles, row-shifted x (width 64)
+    (2, 128, 256, 8, 8),      # two-CTA tiles
+    (1, 72, 200, 9, 9),       # ragged channel boxes (clipped columns and rows)
+    (2, 128, 384, 8, 8),      # hybrid: two-CTA and one-CTA parts
+    (2, 8, 128, 3, 64),       # 8 input channels, width 64: the stem kernel
+    (1, 8, 136, 2, 64),       # the stem kernel with rows past Cout clipped
+]
+
+
+@pytest.mark.parametrize("shape", WGRAD_STORE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_wgrad_tma_partials_match_thread_stores(shape, monkeypatch):
+    monkeypatch.setenv("CONV3X3_WGRAD_HYBRID", "1")
+    t = _small(shape, seed=41)
+    x, _, _, dy = dev_tensors(t)
+    dw, db = ops.wgrad(x, dy, path=L.PATH_TENSOR)
+    monkeypatch.setenv("CONV3X3_WGRAD_PART_TMA", "0")
+    dw2, db2 = ops.wgrad(x, dy, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert torch.equal(dw, dw2) and torch.equal(db, db2)
+    rdw, rdb = oracle.conv3x3_wgrad(t.x, t.dy)
+    assert rel_err(host(dw), rdw) <= TOL_BF16
+    assert rel_err(host(db), rdb) <= TOL_BF16

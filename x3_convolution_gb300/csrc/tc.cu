@@ -3407,7 +3407,7 @@ static_assert(kWhSmem <= 227 * 1024, "shared memory per CTA");
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_wgrad_c8h(const __grid_constant__ CUtensorMap tmDY, const __grid_constant__ CUtensorMap tmX,
-                const WgradParams p) {
+                const __grid_constant__ CUtensorMap tmPart, const WgradParams p) {
   constexpr int S = kWhStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -3548,13 +3548,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const long long dwsize = (long long)p.Cout * 72;
       const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
-      float* o = p.part + (long long)split * dwsize + (long long)k * 72;
+      // the partial row of channel k: in global memory, or (part_tma) row
+      // `lane` of this warp's 32 x 72-float box in the idle stage memory,
+      // stored with one TMA tensor store (rows past Cout are clipped)
+      float* o = p.part_tma ? reinterpret_cast<float*>(smem + (size_t)q * 32 * 288) + lane * 72
+                            : p.part + (long long)split * dwsize + (long long)k * 72;
 #pragma unroll 1
       for (int c = 0; c < 3; ++c) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(lane_addr + (uint32_t)(32 * c), v);
         tmem_ld_wait();
-        if (k < p.Cout) {
+        if (p.part_tma || k < p.Cout) {
           // column block j = 3 s + r (8 columns) holds tap (r, s)
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -3570,8 +3574,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           // column 72 (block 9, the ones block) is dbias
-          if (c == 2) p.part[(long long)p.S * dwsize + (long long)split * p.Cout + k] = __uint_as_float(v[8]);
+          if (c == 2 && k < p.Cout)
+            p.part[(long long)p.S * dwsize + (long long)split * p.Cout + k] = __uint_as_float(v[8]);
         }
+      }
+      if (p.part_tma) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (mb * 128 + q * 32 < p.Cout)
+            tma_store_3d(&tmPart, smem + (size_t)q * 32 * 288, 0, mb * 128 + q * 32, split);
+          bulk_commit();
+          bulk_wait_read<0>();  // the store's writes complete with the grid
+        }
+        __syncwarp();
       }
     }
   }
@@ -4479,8 +4495,24 @@ int run_wgrad_c8(const void* x, const void* dy, float* dw, float* db, const Shap
   prm.status = d.status;
   prm.wait_ns = d.wait_ns;
   if (halo) {
+    // the partials [S][Cout][72] fp32 as a 3-D map for TMA stores: box {72, 32
+    // channels, 1 split} (CONV3X3_WGRAD_PART_TMA=0 keeps per-thread stores)
+    CUtensorMap tpart = tdy;  // (unused unless part_tma)
+    prm.part_tma = 0;
+    const char* pe = std::getenv("CONV3X3_WGRAD_PART_TMA");
+    if (!(pe && std::strcmp(pe, "0") == 0)) {
+      PFN_encodeTiled enc = encode_tiled_fn();
+      cuuint64_t dims[3] = {72, (cuuint64_t)s.Cout, (cuuint64_t)pl.S};
+      cuuint64_t strides[2] = {288, (cuuint64_t)s.Cout * 288};
+      cuuint32_t box[3] = {72, 32, 1};
+      cuuint32_t estr[3] = {1, 1, 1};
+      if (enc && enc(&tpart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, prm.part, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+        prm.part_tma = 1;
+    }
     if (set_smem(k_wgrad_c8h, kWhSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
-    launch_pdl(k_wgrad_c8h, dim3(pl.tiles * pl.S), dim3(kThreads), kWhSmem, st, tdy, tx, prm);
+    launch_pdl(k_wgrad_c8h, dim3(pl.tiles * pl.S), dim3(kThreads), kWhSmem, st, tdy, tx, tpart, prm);
   } else {
     if (set_smem(k_wgrad_c8, kWc8Smem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
     launch_pdl(k_wgrad_c8, dim3(pl.tiles * pl.S), dim3(kThreads), kWc8Smem, st, tdy, tx, prm);
