@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "conv3x3_internal.h"
@@ -146,6 +147,15 @@ __global__ void __launch_bounds__(kUfdThreads)
 // first row has ty even -- and likewise for columns -- is computed from one
 // 2x2 input block:  y[oy + dy][ox + dx] = sum_{u,v} f[dy + 2u][dx + 2v] *
 // x[ty/2 - u][tx/2 - v].  Four 16-byte loads serve four outputs.
+// 16-byte asynchronous copy global -> shared (L1-cached); src_bytes = 0
+// writes zeros without reading.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void unpack8(const uint4 v, float (&o)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -221,18 +231,38 @@ __global__ void __launch_bounds__(kUfdThreads) k_upfirdn2d_up2k4(const __grid_co
 // r0 = 2 oy0 - pad_y0: window row t serves output row dy with tap
 // a = 2 dy + 3 - t when that lies in 0..3.  The window is walked row by row
 // (six 16-byte loads per row), every index compile-time.
-__global__ void __launch_bounds__(kUfdThreads) k_upfirdn2d_down2k4(const __grid_constant__ UfdParams p) {
+constexpr int kDownThreads = 128;
+constexpr size_t kDownSmem = 36 * kDownThreads * sizeof(uint4);  // 73,728 bytes
+
+__global__ void __launch_bounds__(kDownThreads) k_upfirdn2d_down2k4(const __grid_constant__ UfdParams p) {
+  // the thread's 6x6 window, copied asynchronously into its 36 shared-memory
+  // slots [slot][thread] (zeros outside the image): one memory round trip per
+  // thread, where loads into registers went six rows deep in turn
+  extern __shared__ uint4 win[];
   c3::pdl_trigger();
   c3::pdl_wait();
   const int groups = p.C >> 3;
   const int nbx = (p.Wo + 1) >> 1;
-  const int item = blockIdx.x * kUfdThreads + (int)threadIdx.x;
+  const int item = blockIdx.x * kDownThreads + (int)threadIdx.x;
   if (item >= nbx * groups) return;
   const int bx = item / groups, cg = item - bx * groups;
   const int n = blockIdx.z;
   const int oy0 = 2 * (int)blockIdx.y, ox0 = 2 * bx;
   const int r0 = 2 * oy0 - p.py0, c0 = 2 * ox0 - p.px0;
   const __nv_bfloat16* xn = p.x + (size_t)n * p.H * p.W * p.C + (size_t)cg * 8;
+#pragma unroll
+  for (int t = 0; t < 6; ++t) {
+    const int r = r0 + t;
+    const bool row_ok = r >= 0 && r < p.H;
+#pragma unroll
+    for (int q = 0; q < 6; ++q) {
+      const int c = c0 + q;
+      const bool ok = row_ok && c >= 0 && c < p.W;
+      cp_async16(&win[(t * 6 + q) * kDownThreads + threadIdx.x],
+                 ok ? (const void*)(xn + ((size_t)r * p.W + c) * p.C) : (const void*)xn, ok ? 16 : 0);
+    }
+  }
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
   float acc[2][2][8];
 #pragma unroll
   for (int dy = 0; dy < 2; ++dy)
@@ -242,17 +272,9 @@ __global__ void __launch_bounds__(kUfdThreads) k_upfirdn2d_down2k4(const __grid_
       for (int i = 0; i < 8; ++i) acc[dy][dx][i] = 0.f;
 #pragma unroll
   for (int t = 0; t < 6; ++t) {
-    const int r = r0 + t;
-    const bool row_ok = r >= 0 && r < p.H;
     float xv[6][8];
 #pragma unroll
-    for (int q = 0; q < 6; ++q) {
-      const int c = c0 + q;
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (row_ok && c >= 0 && c < p.W)
-        w = __ldg(reinterpret_cast<const uint4*>(xn + ((size_t)r * p.W + c) * p.C));
-      unpack8(w, xv[q]);
-    }
+    for (int q = 0; q < 6; ++q) unpack8(win[(t * 6 + q) * kDownThreads + threadIdx.x], xv[q]);
 #pragma unroll
     for (int dy = 0; dy < 2; ++dy) {
       const int a = 2 * dy + 3 - t;
@@ -348,9 +370,19 @@ int upfirdn2d(const void* x, const float* f, void* y, int N, int C, int H, int W
     e = c3::launch_pdl(k_upfirdn2d_up2k4, g2, blk, 0, st, p);
   } else if (k4 && up == 1 && down == 2) {
     const long long items = (long long)((Wo + 1) / 2) * groups;
-    const dim3 g2((unsigned)((items + kUfdThreads - 1) / kUfdThreads), (unsigned)((Ho + 1) / 2),
+    const dim3 g2((unsigned)((items + kDownThreads - 1) / kDownThreads), (unsigned)((Ho + 1) / 2),
                   (unsigned)N);
-    e = c3::launch_pdl(k_upfirdn2d_down2k4, g2, blk, 0, st, p);
+    // the shared-memory attribute, once per device (devices up to 64)
+    static std::atomic<bool> smem_set[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CONV3X3_ERR_CUDA;
+    if (dev < 0 || dev >= 64 || !smem_set[dev].load()) {
+      if (cudaFuncSetAttribute(k_upfirdn2d_down2k4, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kDownSmem) != cudaSuccess)
+        return CONV3X3_ERR_CUDA;
+      if (dev >= 0 && dev < 64) smem_set[dev].store(true);
+    }
+    e = c3::launch_pdl(k_upfirdn2d_down2k4, g2, dim3(kDownThreads), kDownSmem, st, p);
   } else if (up == 1 && down == 1)
     e = c3::launch_pdl(k_upfirdn2d<1, 1, 0, 0, R>, grid, blk, 0, st, p);
   else
