@@ -378,16 +378,34 @@ RECORDED_TRAFFIC: dict = {   # {(config, pass): bytes per call}
     ("l2", "fwd"): 34780160, ("l2", "dgrad"): 34811904, ("l2", "wgrad"): 95643648,
     ("l3", "fwd"): 15272448, ("l3", "dgrad"): 15270400, ("l3", "wgrad"): 51770112,
 }
+# DRAM bytes of each pass of the UNet step (the pass's launches summed: 33
+# forwards, 33 input gradients, 33 weight gradients with their reductions),
+# from one scoped capture of a whole step's 133 launches -- one pass per
+# launch, caches flushed by ncu before each, writes still in L2 at a launch's
+# end not counted -- valid under the same source hash.  Command: ncu --metrics
+# dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
+# --clock-control none -k regex:"k_(igemm|wgrad|stem)" -s 399 -c 133 on
+# bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline --no-detail
+# --no-gates --no-graph --wgrad-streams 1.
+RECORDED_STEP_TRAFFIC: dict = {"fwd": 1543169024, "dgrad": 1469106432, "wgrad": 3210873856}
 TRAFFIC_SOURCES = ("tc.cu", "simt.cu", "ptx.cuh", "conv3x3_internal.h")
 TRAFFIC_SHA256 = "645a1ea9b9853408da0dea4db77b7babf5de325f99d58f328107eaffcae95050"
 
 
-def sources_sha256():
+# The six resampling ops of a step, the same way: ncu --metrics (as above)
+# -k regex:"k_upfirdn2d" -s 18 -c 6 on bench.py --workload upfirdn2d --steps 1
+# --warmup 3 --no-e2e --no-cpu-baseline.
+RECORDED_UFD_TRAFFIC = 235442176
+UFD_SOURCES = ("upfirdn2d.cu", "conv3x3_internal.h")
+UFD_SHA256 = "76b05b309ae5258121dd03bff3684fb85d605294f6da4de386dce5e1a5991dc1"
+
+
+def sources_sha256(files=None):
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "x3_convolution_gb300", "csrc")
     try:
-        for f in TRAFFIC_SOURCES:
+        for f in (files or TRAFFIC_SOURCES):
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(fh.read())
     except OSError:
@@ -845,9 +863,13 @@ def cuda_arm(args):
                          peaks["source"], "bf16 burst" if peak_key == "bf16_tflops" else
                          "bf16 sustained", "short timed region at full SM clock"
                          if peak_key == "bf16_tflops" else "long or throttled timed region"),
-                     "traffic": None,
-                     "traffic_note": "per-call DRAM bytes of the per-layer configs are in gates "
-                                     "(scoped ncu captures); the step's 33 layers are not captured"},
+                     "traffic": (RECORDED_STEP_TRAFFIC.get(dom)
+                                 if sources_sha256() == TRAFFIC_SHA256 else None),
+                     "traffic_note": "DRAM bytes of the pass's launches per step from one scoped "
+                                     "ncu capture of a whole step (one pass per launch, caches "
+                                     "flushed before each; writes still in L2 at a launch's end "
+                                     "not counted); per-call figures of the per-layer configs "
+                                     "are in gates"},
         "passes": fam,
         "gpu_launches": launches,
         "e2e": e2e,
@@ -980,7 +1002,12 @@ def upfirdn2d_arm(args):
         "roofline": {"bound": "hbm", "kernel": "k_upfirdn2d (all six ops)",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": None, "peak_source": peaks["source"] + " HBM copy"},
+                     "traffic": (RECORDED_UFD_TRAFFIC
+                                 if sources_sha256(UFD_SOURCES) == UFD_SHA256 else None),
+                     "traffic_note": "DRAM bytes of the six ops per step from one scoped ncu "
+                                     "capture (caches flushed before each op; outputs still in "
+                                     "L2 at an op's end not counted)",
+                     "peak_source": peaks["source"] + " HBM copy"},
         "ops_detail": detail, "slowest_op": dom["name"],
         "gpu_launches": len(ops_) * args.steps, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
     }
