@@ -671,6 +671,11 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
         if (kExt && p.zin && ch_ok) {
           const unsigned short* zp =
               reinterpret_cast<const unsigned short*>(second ? p.zin2 : p.zin) + pix0 * ostride + ocol;
+          // the next chunk's 32 pixels into L1 (one 64-byte run per lane)
+          // while this chunk is processed; this chunk's were fetched during
+          // the previous one (or, for the first, come from L2)
+          if (j + 1 < BM / 32 && pix0 + 32 + lane < p.P)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(zp - lane + (32 + lane) * ostride));
 #pragma unroll
           for (int i = 0; i < 32; ++i) zr[i] = i < npix ? __ldg(zp + i * ostride) : (unsigned short)0;
         }
