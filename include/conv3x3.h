@@ -88,7 +88,9 @@
  * with per-thread stores instead of TMA tensor stores (at least 32 input
  * channels).  CONV3X3_EPI_TMA=0 makes forward and input-gradient tiles store
  * their output from each thread instead of through TMA tensor stores (taken
- * for one plain bf16 output where every CTA or CTA pair has one tile).
+ * for one plain bf16 output: on every tile where every CTA or CTA pair has
+ * one, else on each CTA's or pair's last tile); CONV3X3_EPI_TMA=1 keeps them
+ * to one-tile launches.
  * CONV3X3_STEM_ROWS=0 makes the 8-input-channel forward
  * and weight gradient stage x as im2col boxes even where they would stage
  * whole image rows (forward: widths 32 and 64; weight gradient: width 64,

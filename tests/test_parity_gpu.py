@@ -1049,6 +1049,49 @@ def test_output_tma_stores_match_thread_stores(shape, monkeypatch):
     assert rel_err(host(y32), oracle.conv3x3_fwd(t.x, t.w, t.bias, 1)) <= TOL_BF16
 
 
+# Launches with more tiles than CTAs (or CTA pairs): each CTA's last tile
+# leaves through TMA stores, the others through per-thread stores.  Forced
+# tile kinds, ragged pixel tails and a ragged channel edge.
+MULTI_TILE_STORE_CASES = [
+    ("pair256", (10, 256, 256, 45, 45)),   # 80 two-CTA tiles over 76 pairs
+    ("pair384", (80, 384, 384, 16, 16)),   # 80 two-CTA 384-channel tiles
+    ("256x1n", (12, 256, 256, 45, 45)),    # 190 one-CTA 128 x 256 tiles
+    ("128x1", (12, 128, 200, 45, 45)),     # 380 tiles, 200 channels (clipped box)
+    ("128x2n", (20, 128, 128, 45, 45)),    # 159 untransposed 256 x 128 tiles
+    ("64x2", (20, 64, 64, 45, 45)),        # 159 256 x 64 tiles
+]
+
+
+@pytest.mark.parametrize("tile,shape", MULTI_TILE_STORE_CASES, ids=lambda v: v if isinstance(v, str) else "x".join(map(str, v)))
+def test_last_tile_tma_stores_match_thread_stores(tile, shape, monkeypatch):
+    t = _small(shape, seed=41)
+    x, w, b, dy = dev_tensors(t)
+    zin = to_dev_bf16(synth.make_zin(t.layer, seed=41))
+    monkeypatch.setenv("CONV3X3_TILE", tile)
+
+    def run():
+        y = ops.fwd(x, w, b, act=1)
+        dx = ops.dgrad(dy, w)
+        gx = ops.dgrad(dy, w, z_in=zin, act_in=1)
+        torch.cuda.synchronize()
+        return y, dx, gx
+
+    a = run()
+    monkeypatch.setenv("CONV3X3_EPI_TMA", "1")  # one-tile launches only: none here
+    c = run()
+    monkeypatch.setenv("CONV3X3_EPI_TMA", "0")
+    e = run()
+    for u, v, z in zip(a, c, e):
+        assert torch.equal(u, v)
+        assert torch.equal(u, z)
+    # every channel of a few pixels in the last tiles against the oracle
+    P, C = t.layer.N * t.layer.H * t.layer.W, t.layer.Cout
+    pix = np.array([0, P - 257, P - 130, P - 2, P - 1])
+    idx = (pix[:, None] * C + np.arange(C)[None, :]).reshape(-1)
+    ry = oracle.conv3x3_fwd_at(t.x, t.w, t.bias, 1, idx)
+    assert check_bf16_store(host(a[0]).reshape(-1)[idx], ry) == 0
+
+
 WGRAD_STORE_SHAPES = [
     (2, 128, 128, 16, 16),    # one-CTA tiles, im2col x
     (2, 128, 128, 8, 64),     # one-CTA tiles, row-shifted x (width 64)

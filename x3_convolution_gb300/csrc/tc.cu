@@ -758,10 +758,13 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
                              (uint32_t)((buf * MT + sub) * BN + col_off);
+      // the TMA-store path serves every tile of one-tile CTAs (epi_tma 1) or
+      // each CTA's last tile (epi_tma 2): there the stage ring is idle
+      const bool tma_here = p.epi_tma == 1 || (p.epi_tma == 2 && tile + (int)gridDim.x >= num_tiles);
       if constexpr (kCols % 64 == 0) {
-        if (p.epi_tma) {
-          // one tile per CTA: the stage ring is idle; this warp's 32 pixels
-          // leave as kCols / 64 boxes of {64 channels, 32 pixels}
+        if (tma_here) {
+          // every MMA of the tile has completed, so no stage is in use; this
+          // warp's 32 pixels leave as kCols / 64 boxes of {64 channels, 32 pixels}
           uint8_t* stg = smem + (size_t)(warp - kEpiBase) * (kCols / 64) * 4096u;
           const long long wrow0 = (long long)mt * TM + sub * BM + q * 32;
 #pragma unroll 1
@@ -790,7 +793,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
         }
       }
 #pragma unroll 1
-      for (int j = 0; j < (p.epi_tma && kCols % 64 == 0 ? 0 : kCols / 32); ++j) {
+      for (int j = 0; j < (tma_here && kCols % 64 == 0 ? 0 : kCols / 32); ++j) {
         const int col0 = nt * BN + col_off + j * 32;
         const bool live = valid && col0 < p.nout;
         // operands that do not depend on the accumulator are loaded first
@@ -1111,11 +1114,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kPairBN + col_off);
+      // every tile of one-tile pairs (epi_tma 1) or each pair's last tile
+      // (epi_tma 2) leaves through TMA stores staged in the idle stage rings
+      const bool tma_here = p.epi_tma == 1 || (p.epi_tma == 2 && tile + num_pairs >= num_tiles);
       if constexpr (kCols % 64 == 0) {
-        if (p.epi_tma) {
-          // one tile per pair: both stage rings are idle (every MMA of the
-          // tile has completed); this warp's 32 pixels leave as kCols / 64
-          // boxes of {64 channels, 32 pixels}
+        if (tma_here) {
+          // both stage rings are idle (every MMA of the tile has completed);
+          // this warp's 32 pixels leave as kCols / 64 boxes of {64 channels, 32 pixels}
           uint8_t* stg = smem + (size_t)(warp - kEpiBase) * (kCols / 64) * 4096u;
           const long long wrow0 = (long long)mt * 2 * BM + rank * BM + q * 32;
 #pragma unroll 1
@@ -1144,7 +1149,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
         }
       }
 #pragma unroll 1
-      for (int j = 0; j < (p.epi_tma && kCols % 64 == 0 ? 0 : kCols / 32); ++j) {
+      for (int j = 0; j < (tma_here && kCols % 64 == 0 ? 0 : kCols / 32); ++j) {
         const int col0 = nt * kPairBN + col_off + j * 32;
         const bool live = valid && col0 < p.nout;
         float bv[32];
@@ -3735,17 +3740,24 @@ int set_smem(K kernel, size_t bytes, int device) {
   return CONV3X3_OK;
 }
 
-// The TMA-store epilogue (IgemmParams::epi_tma) where every CTA or pair has
-// one tile and the output is one plain bf16 tensor; `ty` then maps it.
-// CONV3X3_EPI_TMA=0 keeps the per-thread row stores.
+// The TMA-store epilogue (IgemmParams::epi_tma) for a plain bf16 output:
+// every tile where every CTA or pair has one (1), else each CTA's or pair's
+// last tile (2), whose epilogue otherwise runs exposed at the end of the
+// launch; `ty` then maps the output.  CONV3X3_EPI_TMA=0 keeps the per-thread
+// row stores everywhere, CONV3X3_EPI_TMA=1 uses TMA stores on one-tile
+// launches only.
 int make_store_map(CUtensorMap* m, void* base, long long P, int C);
-void epi_tma_setup(IgemmParams& p, int tiles, int slots, const CUtensorMap& dummy, CUtensorMap* ty) {
+void epi_tma_setup(IgemmParams& p, bool allowed, int tiles, int slots, const CUtensorMap& dummy,
+                   CUtensorMap* ty) {
   *ty = dummy;
   p.epi_tma = 0;
-  if (tiles > slots || p.out_f32 || p.zout || p.out2 || p.s2 || p.nsplit != p.nout || p.nout % 8) return;
-  if (const char* e = std::getenv("CONV3X3_EPI_TMA"))
+  if (!allowed || p.out_f32 || p.zout || p.out2 || p.s2 || p.nsplit != p.nout || p.nout % 8) return;
+  const int mode = tiles > slots ? 2 : 1;
+  if (const char* e = std::getenv("CONV3X3_EPI_TMA")) {
     if (std::strcmp(e, "0") == 0) return;
-  p.epi_tma = make_store_map(ty, p.out, p.P, p.nout) == CONV3X3_OK ? 1 : 0;
+    if (std::strcmp(e, "1") == 0 && mode == 2) return;
+  }
+  if (make_store_map(ty, p.out, p.P, p.nout) == CONV3X3_OK) p.epi_tma = mode;
 }
 
 template <int BN, int MT, bool kDgrad, int KC = 1, bool kT = false>
@@ -3760,7 +3772,7 @@ int launch_igemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap&
   const int grid = tiles < d.num_sms ? tiles : d.num_sms;
   IgemmParams p2 = prm;
   CUtensorMap ty;
-  epi_tma_setup(p2, kT ? 0x7fffffff : tiles, grid, a, &ty);  // (the transposed tile has its own epilogue)
+  epi_tma_setup(p2, !kT, tiles, grid, a, &ty);  // (the transposed tile has its own epilogue)
   launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, a2, b, ty, p2);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
@@ -3807,7 +3819,7 @@ int launch_igemm_pair(const CUtensorMap& a, const CUtensorMap& a2, const CUtenso
   const int grid = 2 * (tiles < pairs ? tiles : pairs);
   IgemmParams p2 = prm;
   CUtensorMap ty;
-  epi_tma_setup(p2, tiles, grid / 2, a, &ty);
+  epi_tma_setup(p2, true, tiles, grid / 2, a, &ty);
   launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, a2, b, ty, p2);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
