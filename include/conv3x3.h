@@ -71,7 +71,10 @@
  * CONV3X3_KC=1|2 forces the 64-channel chunks per pipeline stage of the im2col
  * kernel (2 for 128x1 tiles unless set); CONV3X3_PAIR_KC=1 keeps one chunk per
  * stage in the 256-channel two-CTA tiles (unset: two where the input channels
- * are a whole number of 128).  CONV3X3_WGRAD_SPLITS=<S> forces the
+ * are a whole number of 128).  CONV3X3_PAIR_HALF=0 keeps whole 256-channel
+ * two-CTA tiles in a last round that fills at most half of the pairs (unset:
+ * that round's tiles run as two 128-channel halves each); =all splits every
+ * such tile (tests).  CONV3X3_WGRAD_SPLITS=<S> forces the
  * weight gradient's split count (set it before querying the workspace size).
  * CONV3X3_WGRAD_ROWS=0|1 chooses how the weight gradient stages x: im2col
  * boxes per tap (0), or one zero-padded box per image row that all three taps

@@ -170,6 +170,61 @@ def test_pair_chunks_per_stage(shape, kc, monkeypatch):
     assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
 
 
+@pytest.mark.parametrize("kc", ["2", "1"], ids=["two_chunks", "one_chunk"])
+@pytest.mark.parametrize("shape", [(1, 72, 200, 6, 11), (2, 256, 256, 8, 8), (3, 128, 256, 17, 13)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_pair_half_width_items(shape, kc, monkeypatch):
+    # every 256-channel pair tile as two 128-channel items (N = 128 MMAs over
+    # 64 weight rows per CTA): plain, bf16 through TMA stores, the forward's
+    # z store and the dgrad's z_in scaling; 200 and 72 output channels leave
+    # the second item partly or wholly past the last channel
+    monkeypatch.setenv("CONV3X3_TILE", "pair256")
+    monkeypatch.setenv("CONV3X3_PAIR_KC", kc)
+    monkeypatch.setenv("CONV3X3_PAIR_HALF", "all")
+    t = _small(shape, seed=43)
+    x, w, b, dy = dev_tensors(t)
+    zin_h = synth.make_zin(t.layer, seed=43)
+    N, Cin, Cout, H, W = shape
+    z = torch.empty((N, H, W, Cout), dtype=torch.bfloat16, device="cuda")
+    y32 = ops.fwd(x, w, b, act=1, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    ybf = ops.fwd(x, w, b, act=1, path=L.PATH_TENSOR)
+    ops.fwd(x, w, b, act=1, path=L.PATH_TENSOR, z_out=z)
+    dx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    gx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=L.PATH_TENSOR, z_in=to_dev_bf16(zin_h), act_in=1)
+    torch.cuda.synchronize()
+    ry = oracle.conv3x3_fwd(t.x, t.w, t.bias, 1)
+    assert rel_err(host(y32), ry) <= TOL_BF16
+    assert check_bf16_store(host(ybf), ry) == 0
+    assert check_bf16_store(host(z), oracle.conv3x3_fwd(t.x, t.w, t.bias, 0)) == 0
+    assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
+    assert rel_err(host(gx32), oracle.conv3x3_dgrad_act(t.dy, t.w, zin_h, 1)) <= TOL_BF16
+
+
+def test_pair_last_round_half_width_full_size(monkeypatch):
+    # 256 -> 256 channels at 32x32, batch 64: 256 pair tiles over the pairs
+    # that fit (76 on a 152-SM GPU) leave a last round of 28 tiles, which runs
+    # as 56 half-width items; against whole tiles and the oracle's last pixels
+    Lr = synth.L2
+    t = synth.make_tensors(Lr, seed=5)
+    x, w, b, dy = dev_tensors(t)
+    y = ops.fwd(x, w, b, act=1, out_dtype=L.DT_F32)
+    dx = ops.dgrad(dy, w, out_dtype=L.DT_F32)
+    monkeypatch.setenv("CONV3X3_PAIR_HALF", "0")
+    y0 = ops.fwd(x, w, b, act=1, out_dtype=L.DT_F32)
+    dx0 = ops.dgrad(dy, w, out_dtype=L.DT_F32)
+    torch.cuda.synchronize()
+    assert rel_err(host(y), host(y0)) <= 1e-6
+    assert rel_err(host(dx), host(dx0)) <= 1e-6
+    P = Lr.N * Lr.H * Lr.W
+    pix = np.array([P - 7 * 256 - 1, P - 256, P - 129, P - 1])
+    iy = (pix[:, None] * Lr.Cout + np.arange(Lr.Cout)[None, :]).reshape(-1)
+    ix = (pix[:, None] * Lr.Cin + np.arange(Lr.Cin)[None, :]).reshape(-1)
+    ry = oracle.conv3x3_fwd_at(t.x, t.w, t.bias, 1, iy)
+    rx = oracle.conv3x3_dgrad_at(t.dy, t.w, ix)
+    assert np.max(np.abs(host(y).reshape(-1)[iy] - ry)) / np.max(np.abs(ry)) <= TOL_BF16
+    assert np.max(np.abs(host(dx).reshape(-1)[ix] - rx)) / np.max(np.abs(rx)) <= TOL_BF16
+
+
 @pytest.mark.parametrize("pair384", ["auto", "0"], ids=["pair384", "one_cta"])
 @pytest.mark.parametrize("shape", [(2, 384, 384, 16, 16), (1, 256, 384, 16, 16), (3, 128, 384, 9, 13),
                                    (1, 896, 384, 8, 8)], ids=lambda s: "x".join(map(str, s)))

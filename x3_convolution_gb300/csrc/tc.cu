@@ -154,6 +154,10 @@ struct IgemmParams {
   // tmY), staged in the idle stage ring: set only where every CTA (or pair)
   // has one tile and the output is one plain bf16 tensor
   int epi_tma = 0;
+  // 256-channel pair tiles: work items from half_from on are half-width tiles
+  // of 128 channels, two per remaining tile (the last round's tiles split so
+  // that they spread over the pairs instead of leaving most of them idle)
+  int half_from = 0x7fffffff;
 };
 
 // Where output column col0 of pixel `pix` lives.  Columns [0, nsplit) are in
@@ -856,6 +860,22 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 // writes accumulator columns 0-255 and the second (rows 128-191) columns
 // 256-383: column = channel of the tile.  Both passes load three 64-row (or
 // 64-channel) boxes per CTA and k-block, every byte used.
+// Work item `it` of a 256-channel pair launch: tiles [0, half_from) whole,
+// then every remaining tile as two items of 128 channels each (N = 128 MMAs,
+// 64 weight rows per CTA), channel offset 0 or 128 within the tile.
+struct PairItem {
+  int tile, coff;
+  bool half;
+};
+__device__ __forceinline__ PairItem pair_item(const IgemmParams& p, int it) {
+  if (it < p.half_from) return PairItem{it, 0, false};
+  const int h = it - p.half_from;
+  return PairItem{p.half_from + (h >> 1), (h & 1) * 128, true};
+}
+__device__ __forceinline__ int pair_num_items(const IgemmParams& p, int num_tiles) {
+  return p.half_from < num_tiles ? 2 * num_tiles - p.half_from : num_tiles;
+}
+
 template <int BN, bool kDgrad, int KC = 1>
 struct PairCfg {
   static constexpr int kHalf = BN / 2;                  // weight rows (output channels) per CTA
@@ -880,8 +900,8 @@ struct PairCfg {
 template <bool kDgrad, bool kExt, int BN = 256, int KC = 1>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
     k_igemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
-                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY,
-                 const IgemmParams p) {
+                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
+                 const __grid_constant__ CUtensorMap tmY, const IgemmParams p) {
   using Cfg = PairCfg<BN, kDgrad, KC>;
   constexpr int S = Cfg::kStages;
   constexpr bool kSP = Cfg::kSP;
@@ -904,6 +924,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
   const uint32_t rank = cluster_ctarank();
   const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
   const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+  // half-width items exist only for 256-channel tiles
+  constexpr bool kHalves = BN == 256;
+  const int num_items = kHalves ? pair_num_items(p, num_tiles) : num_tiles;
   const int HW = p.H * p.W;
 
   if (warp == 0 && lane == 0) {
@@ -921,6 +944,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
     tma_prefetch_desc(&tmA);
     if (p.kchunks_a < p.kchunks) tma_prefetch_desc(&tmA2);
     tma_prefetch_desc(&tmB);
+    if (!kDgrad && kHalves && p.half_from < num_tiles) tma_prefetch_desc(&tmB2);
   }
   if (warp == kMmaWarp) {
     tmem_alloc_pair(tmem_slot, 512);
@@ -950,16 +974,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
       constexpr int kPer = 1 + kBPer;
       constexpr int kBoxes = KC * kPer;
       constexpr uint32_t kBBox = (kDgrad || BN == 384) ? 8192u : Cfg::kBHalf;
-      uint32_t my_bytes = 0;  // box-parallel: this producer's share of a stage
-      for (int b = warp; b < kBoxes; b += kProd) my_bytes += b % kPer == 0 ? kABytes : kBBox;
+      // box-parallel: this producer's share of a stage, of a whole tile's and of
+      // a half-width item's (half the forward's weight rows; the dgrad's first
+      // 64-channel box only)
+      uint32_t my_bytes = 0, my_bytes_h = 0;
+      for (int b = warp; b < kBoxes; b += kProd) {
+        my_bytes += b % kPer == 0 ? kABytes : kBBox;
+        my_bytes_h += b % kPer == 0 ? kABytes : kDgrad ? (b % kPer == 1 ? kBBox : 0u) : kBBox / 2;
+      }
+      constexpr uint32_t kPairStageH = KC * (kABytes + Cfg::kBHalf / 2);
       const int kgroups = p.kchunks / KC;
-      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
-        const int mt = tile / p.num_n_tiles, nt = tile - mt * p.num_n_tiles;
+      for (int it = pair; it < num_items && ok; it += num_pairs) {
+        const PairItem w = kHalves ? pair_item(p, it) : PairItem{it, 0, false};
+        const int mt = w.tile / p.num_n_tiles, nt = w.tile - mt * p.num_n_tiles;
         const int p0 = mt * 2 * BM + (int)rank * BM;  // this CTA's 128 pixels
         const int n0 = p0 / HW, rem = p0 - n0 * HW;
         const int h0 = rem / p.W;
         const int cn = n0, ch = p.ustride * h0 - 1, cw = p.ustride * (rem - h0 * p.W) - 1;
-        const int c0 = nt * kPairBN + (int)rank * Cfg::kHalf;  // this CTA's weight rows (output channels)
+        // this CTA's weight rows (output channels): half of the tile's, or of the item's 128
+        const int c0 = nt * kPairBN + w.coff + (int)rank * (w.half ? 64 : Cfg::kHalf);
         const int kblocks = 9 * kgroups;
         for (int kb = 0; kb < kblocks; ++kb) {
           const int tap = kb / kgroups, cg = (kb - tap * kgroups) * KC;
@@ -971,7 +1004,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
             uint8_t* sa = smem + (size_t)stage * kPairStage;
             uint8_t* sb = sa + KC * kABytes;
             const uint32_t fb = full0 + (uint32_t)stage * 8u;
-            if (rank == 0) mbar_arrive_expect_tx(&full[stage], kSP ? 2 * kPairStage : 2 * my_bytes);
+            if (rank == 0)
+              mbar_arrive_expect_tx(&full[stage], kSP ? 2 * (w.half ? kPairStageH : kPairStage)
+                                                      : 2 * (w.half ? my_bytes_h : my_bytes));
             const int wtap = kDgrad ? 8 - tap : tap;
 #pragma unroll
             for (int b = 0; b < kBoxes; ++b) {
@@ -992,9 +1027,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
                 else
                   tma_load_3d_pair(sb + j * 8192, &tmB, fb, cb, wtap, cc * BKC);
               } else if (!kDgrad) {
-                tma_load_3d_pair(sb + c * Cfg::kBHalf, &tmB, fb, cc * BKC, wtap, c0);
+                // a half-width item's 64 rows come through the 64-row box map
+                tma_load_3d_pair(sb + c * Cfg::kBHalf, w.half ? &tmB2 : &tmB, fb, cc * BKC, wtap, c0);
               } else {
                 const int j = r - 1;
+                if (w.half && j > 0) continue;  // a half-width item takes one 64-channel box
                 tma_load_3d_pair(sb + c * Cfg::kBHalf + j * 8192, &tmB, fb, c0 + j * 64, wtap, cc * BKC);
               }
             }
@@ -1032,7 +1069,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
     if (rank == 0 && lane == 0) {
       constexpr int kMmaN = BN == 384 ? 256 : kPairBN;  // N = 256 + N = 128 per K step at BN = 384
       constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, kMmaN, 0, kDgrad ? 1 : 0);
-      constexpr uint32_t idesc2 = idesc_bf16_f32(2 * BM, 128, 0, kDgrad ? 1 : 0);
+      constexpr uint32_t idesc2 = idesc_bf16_f32(2 * BM, 128, 0, kDgrad ? 1 : 0);  // also half-width items
       // the second MMA's weight rows start after two 8 KB boxes (128 rows or channels)
       constexpr uint32_t kB2 = (2u * 8192u) >> 4;
       const uint32_t sbase = smem_u32(smem);
@@ -1047,7 +1084,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
       int buf = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = pair; tile < num_tiles && ok; tile += num_pairs) {
+      for (int it = pair; it < num_items && ok; it += num_pairs) {
+        const uint32_t id = (kHalves && it >= p.half_from) ? idesc2 : idesc;
         if (!mbar_wait(&tempty[buf], acc_phase ^ 1, p.wait_ns, p.status, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kPairBN);
@@ -1065,7 +1103,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
             for (int k = 0; k < BKC / 16; ++k) {
               const uint32_t acc = (kb != 0 || c != 0 || k != 0) ? 1u : 0u;
               tc_mma_bf16_pair(d_tmem, ad + (uint64_t)(c * (kABytes >> 4) + k * kAKStep),
-                               bd + (uint64_t)(c * (Cfg::kBHalf >> 4) + k * kBKStep), idesc, acc);
+                               bd + (uint64_t)(c * (Cfg::kBHalf >> 4) + k * kBKStep), id, acc);
               if constexpr (BN == 384)
                 tc_mma_bf16_pair(d_tmem + 256, ad + (uint64_t)(k * kAKStep), bd + (uint64_t)(kB2 + k * kBKStep),
                                  idesc2, acc);
@@ -1093,39 +1131,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    // TMEM lane = this CTA's pixel, column = output channel of the 256-wide
-    // tile; the two warps of a lane quarter take 128 columns each.
+    // TMEM lane = this CTA's pixel, column = output channel of the tile (or
+    // of the half-width item); the two warps of a lane quarter take half the
+    // columns each.
     constexpr int kCols = kPairBN / 2;
     const int q = warp & 3;
     const int half = (warp - kEpiBase) >> 2;
-    const int col_off = half * kCols;
     const int row = q * 32 + lane;
     float* bsl = reinterpret_cast<float*>(smem + (size_t)S * kPairStage + 256) + (warp - kEpiBase) * kCols;
     int buf = 0;
     uint32_t acc_phase = 0;
-    for (int tile = pair; tile < num_tiles; tile += num_pairs) {
-      const int mt = tile / p.num_n_tiles, nt = tile - mt * p.num_n_tiles;
+    for (int it = pair; it < num_items; it += num_pairs) {
+      const PairItem w = kHalves ? pair_item(p, it) : PairItem{it, 0, false};
+      const int mt = w.tile / p.num_n_tiles, nt = w.tile - mt * p.num_n_tiles;
+      const int ncols = kHalves && w.half ? kCols / 2 : kCols;  // this warp's columns
+      const int cb = nt * kPairBN + w.coff + half * ncols;     // its first output channel
       const long long pix = (long long)mt * 2 * BM + rank * BM + row;
       const bool valid = pix < p.P;
-      if (kExt && kDgrad && p.zin && valid && nt * kPairBN + col_off < p.nout)
-        prefetch_zin_row(p, pix, nt * kPairBN + col_off, kCols);
-      if (!kDgrad && p.bias) stage_bias_slice<kCols>(p, nt * kPairBN + col_off, bsl, lane);
+      if (kExt && kDgrad && p.zin && valid && cb < p.nout) prefetch_zin_row(p, pix, cb, ncols);
+      if (!kDgrad && p.bias) stage_bias_slice<kCols>(p, cb, bsl, lane);
       if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
       tc_fence_after();
       const uint32_t taddr =
-          tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kPairBN + col_off);
-      // every tile of one-tile pairs (epi_tma 1) or each pair's last tile
+          tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * kPairBN + half * ncols);
+      // every item of one-item pairs (epi_tma 1) or each pair's last item
       // (epi_tma 2) leaves through TMA stores staged in the idle stage rings
-      const bool tma_here = p.epi_tma == 1 || (p.epi_tma == 2 && tile + num_pairs >= num_tiles);
+      const bool tma_here = p.epi_tma == 1 || (p.epi_tma == 2 && it + num_pairs >= num_items);
       if constexpr (kCols % 64 == 0) {
         if (tma_here) {
           // both stage rings are idle (every MMA of the tile has completed);
-          // this warp's 32 pixels leave as kCols / 64 boxes of {64 channels, 32 pixels}
+          // this warp's 32 pixels leave as ncols / 64 boxes of {64 channels, 32 pixels}
           uint8_t* stg = smem + (size_t)(warp - kEpiBase) * (kCols / 64) * 4096u;
           const long long wrow0 = (long long)mt * 2 * BM + rank * BM + q * 32;
 #pragma unroll 1
-          for (int j = 0; j < kCols / 32; ++j) {
-            const int col0 = nt * kPairBN + col_off + j * 32;
+          for (int j = 0; j < ncols / 32; ++j) {
+            const int col0 = cb + j * 32;
             float bv[32];
             if (!kDgrad && p.bias) bias_from_slice(bsl + j * 32, bv);
             uint4 zr[4] = {};
@@ -1149,8 +1189,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
         }
       }
 #pragma unroll 1
-      for (int j = 0; j < (tma_here && kCols % 64 == 0 ? 0 : kCols / 32); ++j) {
-        const int col0 = nt * kPairBN + col_off + j * 32;
+      for (int j = 0; j < (tma_here && kCols % 64 == 0 ? 0 : ncols / 32); ++j) {
+        const int col0 = cb + j * 32;
         const bool live = valid && col0 < p.nout;
         float bv[32];
         if (!kDgrad && p.bias && live) bias_from_slice(bsl + j * 32, bv);
@@ -3807,20 +3847,38 @@ int pair_slots(K kernel, size_t smem, const DevCtx& d) {
   return n;
 }
 
+// First work item of the half-width tiles of a 256-channel pair launch (see
+// IgemmParams::half_from), or INT_MAX for none.  Where the tiles leave a last
+// round that fills at most half of the pairs, that round's tiles run as two
+// 128-channel items each: they then spread over up to all of the pairs and
+// the round takes a half-width item's time.  CONV3X3_PAIR_HALF=0 keeps whole
+// tiles; CONV3X3_PAIR_HALF=all splits every tile (tests).
+int pair_half_from(int tiles, int pairs) {
+  int mode = -1;
+  if (const char* e = std::getenv("CONV3X3_PAIR_HALF")) mode = std::strcmp(e, "all") == 0 ? 1 : 0;
+  if (mode == 1) return 0;
+  if (mode == 0 || tiles <= pairs) return 0x7fffffff;
+  const int whole = tiles / pairs * pairs, left = tiles - whole;
+  return left > 0 && 2 * left <= pairs ? whole : 0x7fffffff;
+}
+
 template <bool kDgrad, int BN, int KC = 1>
 int launch_igemm_pair(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
-                      const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
+                      const CUtensorMap& b64, const IgemmParams& prm, const DevCtx& d,
+                      cudaStream_t st) {
   using Cfg = PairCfg<BN, kDgrad, KC>;
   const bool ext = prm.zout || prm.zin || prm.out2;
   auto kern = ext ? k_igemm_pair<kDgrad, true, BN, KC> : k_igemm_pair<kDgrad, false, BN, KC>;
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int tiles = prm.num_m_tiles * prm.num_n_tiles;
   const int pairs = pair_slots(kern, Cfg::kSmem, d);
-  const int grid = 2 * (tiles < pairs ? tiles : pairs);
   IgemmParams p2 = prm;
+  p2.half_from = BN == 256 ? pair_half_from(tiles, pairs) : 0x7fffffff;
+  const int items = p2.half_from < tiles ? 2 * tiles - p2.half_from : tiles;
+  const int grid = 2 * (items < pairs ? items : pairs);
   CUtensorMap ty;
-  epi_tma_setup(p2, true, tiles, grid / 2, a, &ty);
-  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, a2, b, ty, p2);
+  epi_tma_setup(p2, true, items, grid / 2, a, &ty);
+  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, a2, b, b64, ty, p2);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
@@ -4237,13 +4295,22 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
     // loading pair_bn / 2 weight rows (as three 64-row boxes at 384)
     prm.num_m_tiles = (int)((g.P() + 2 * BM - 1) / (2 * BM));
     prm.num_n_tiles = (nout + pair_bn - 1) / pair_bn;
-    if (!dgrad) {  // (dgrad's map already has 64-row boxes)
+    // the weight boxes: pair_bn / 2 rows, and 64 rows for half-width items
+    // (dgrad's map already has 64-channel boxes)
+    CUtensorMap tb64 = tb;
+    if (!dgrad) {
       rc = make_weight_map(&tb, w, s.Cin, s.Cout, pair_bn == 384 ? 64 : pair_bn / 2);
       if (rc) return rc;
+      if (pair_bn == 256) {
+        rc = make_weight_map(&tb64, w, s.Cin, s.Cout, 64);
+        if (rc) return rc;
+      } else {
+        tb64 = tb;
+      }
     }
 #define C3_PAIR(BN_, KC_)                                                              \
-  return dgrad ? launch_igemm_pair<true, BN_, KC_>(ta, ta2, tb, prm, d, st)            \
-               : launch_igemm_pair<false, BN_, KC_>(ta, ta2, tb, prm, d, st)
+  return dgrad ? launch_igemm_pair<true, BN_, KC_>(ta, ta2, tb, tb64, prm, d, st)      \
+               : launch_igemm_pair<false, BN_, KC_>(ta, ta2, tb, tb64, prm, d, st)
     // two 64-channel chunks per stage where K is a whole number of them;
     // CONV3X3_PAIR_KC=1 keeps one
     int pkc = prm.kchunks % 2 == 0 ? 2 : 1;
