@@ -48,7 +48,10 @@
  * returns CONV3X3_ERR_UNSUPPORTED.  Kernels that wait on the
  * hardware (mbarrier / TMA / tensor-core completion) give up after a bounded
  * time, record CONV3X3_ERR_TIMEOUT in the device status word and exit cleanly;
- * read it with conv3x3_device_status().
+ * read it with conv3x3_device_status().  The bound is 2 s per wait
+ * (CONV3X3_WAIT_LIMIT_NS, read once per process), timed on the global
+ * nanosecond timer and also required to have passed on the SM cycle counter
+ * (bound / 2 cycles).
  *
  * Tuning override: the environment variable CONV3X3_TILE forces the forward /
  * dgrad tensor-core tile: "<BN>x<MT>" (BN in {64,128,192,256}, MT in {1,2},

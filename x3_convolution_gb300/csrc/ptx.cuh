@@ -57,17 +57,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity to complete.  Returns false
 // (after recording CONV3X3_ERR_TIMEOUT in *status and raising *abort) when the
 // wait exceeds limit_ns, or as soon as another role of the CTA has aborted.
+// The bound is measured on the global nanosecond timer and must also have
+// passed on the SM's own cycle counter (limit_ns / 2 cycles: at least a
+// quarter of the bound at 2 GHz), so that a step of the global timer alone
+// cannot end a wait that is still making progress.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
                                           unsigned* status, volatile int* abort_flag) {
 #pragma unroll 1
   for (int i = 0; i < 32; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const long long c0 = clock64();
 #pragma unroll 1
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (abort_flag && *abort_flag) return false;
-    if (globaltimer_ns() - t0 > limit_ns) {
+    if (globaltimer_ns() - t0 > limit_ns && (uint64_t)(clock64() - c0) > (limit_ns >> 1)) {
       if (status) atomicExch(status, (unsigned)CONV3X3_ERR_TIMEOUT);
       if (abort_flag) *abort_flag = 1;
       return false;

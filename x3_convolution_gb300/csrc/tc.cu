@@ -4167,10 +4167,12 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   TileShape ts = pick_tile(nout, dgrad ? s : g, d.num_sms);
   // 128-channel x 256-pixel tiles run transposed (k_igemm kT) unless the
   // override names "128x2n".  256-channel tiles run on CTA pairs
-  // (k_igemm_pair) where that measured faster: dgrad, or a forward of at least
-  // four 64-channel chunks (256 -> 256 channels at 32x32: 61 instead of 65 us
-  // with two chunks per pair stage), and at least two rounds of pair tiles (a
-  // 256-pixel pair tile halves the tile count, so small grids lose).
+  // (k_igemm_pair) where that measured faster: a forward of at least two
+  // 64-channel chunks with at least two rounds of pair tiles (a 256-pixel pair
+  // tile halves the tile count, so small grids lose; 128 -> 256 channels at
+  // 32x32: 39.8 -> 37.5 us), or a dgrad whose pair tiles fill at least 4/5 of
+  // the SMs (1024 -> 512 at 8x8 and 256 -> 384 at 16x16, 64 pair tiles each:
+  // 33.7 -> 33.0 and 29.3 -> 27.5 us; 32 pair tiles ran slower).
   // CONV3X3_PAIR=0|1 or the override "256x1" / "256x1n" forces the choice.
   bool trans = true;
   int pair_force = -1, pair_bn = 0;
@@ -4254,17 +4256,19 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   }
   const long long pair_tiles = (g.P() + 2 * BM - 1) / (2 * BM) * prm.num_n_tiles;
   const bool pair = pair_force >= 0 ? pair_force == 1
-                                    : ((dgrad || prm.kchunks >= 4) && pair_tiles >= d.num_sms);
+                    : dgrad ? 10 * pair_tiles >= 4LL * d.num_sms
+                            : (prm.kchunks >= 2 && pair_tiles >= d.num_sms);
   if (pair_bn == 0 && pair && bn == 256 && ts.mt == 1) pair_bn = 256;
   // 384 output channels whose 256-pixel x 384-channel pair tiles fill most of
-  // the GPU in one round, with a K of at least six 64-channel chunks: one tile
-  // per cluster, two N = 192 MMAs per K step.  Measured on GB300 (batch 64,
+  // the GPU in one round, with a K of at least four 64-channel chunks: one tile
+  // per cluster, an N = 256 and an N = 128 MMA per K step.  Measured on GB300 (batch 64,
   // 16x16): 896 -> 384 forward 79.6 -> 71.5 us, 384 -> 384 dgrad 40.8 -> 38.9
-  // us against 128 x 192 one-CTA tiles; 256 -> 384 (four chunks) and 16 pair
-  // tiles (8x8) ran slower.  CONV3X3_PAIR384=0 keeps the tile choice above.
+  // us against 128 x 192 one-CTA tiles; 256 -> 384 (four chunks) 33.0 -> 29.9
+  // us once the one-tile epilogue stored through TMA; 16 pair tiles (8x8) ran
+  // slower.  CONV3X3_PAIR384=0 keeps the tile choice above.
   const long long tiles384 = (g.P() + 2 * BM - 1) / (2 * BM);
   bool p384 = pair_bn == 0 && pair_force != 0 && nout == 384 && tiles384 <= d.num_sms / 2 &&
-              tiles384 * 8 >= 3LL * d.num_sms && prm.kchunks >= 6;
+              tiles384 * 8 >= 3LL * d.num_sms && prm.kchunks >= 4;
   if (const char* e = std::getenv("CONV3X3_PAIR384"))
     if (std::strcmp(e, "0") == 0) p384 = false;
   if (p384) pair_bn = 384;
