@@ -373,10 +373,10 @@ def _wgrad(wl, i, sh, side=-1):
 # -s 12 -c 4 on bench.py --workload <config> --steps 1 --warmup 3 --no-e2e
 # --no-cpu-baseline --no-detail --no-gates --no-graph --wgrad-streams 1.
 RECORDED_TRAFFIC: dict = {   # {(config, pass): bytes per call}
-    ("stem", "fwd"): 10486016, ("stem", "dgrad"): 67167744, ("stem", "wgrad"): 77037824,
-    ("l1", "fwd"): 91748096, ("l1", "dgrad"): 86851328, ("l1", "wgrad"): 165413632,
-    ("l2", "fwd"): 34782208, ("l2", "dgrad"): 34769920, ("l2", "wgrad"): 95593984,
-    ("l3", "fwd"): 15272704, ("l3", "dgrad"): 15270400, ("l3", "wgrad"): 51758848,
+    ("stem", "fwd"): 10452992, ("stem", "dgrad"): 67167744, ("stem", "wgrad"): 77089536,
+    ("l1", "fwd"): 91382272, ("l1", "dgrad"): 86984704, ("l1", "wgrad"): 165376000,
+    ("l2", "fwd"): 34774784, ("l2", "dgrad"): 34778368, ("l2", "wgrad"): 95599616,
+    ("l3", "fwd"): 15273216, ("l3", "dgrad"): 15263488, ("l3", "wgrad"): 51759360,
 }
 # DRAM bytes of each pass of the UNet step (the pass's launches summed: 33
 # forwards, 33 input gradients, 33 weight gradients with their reductions),
@@ -387,9 +387,9 @@ RECORDED_TRAFFIC: dict = {   # {(config, pass): bytes per call}
 # --clock-control none -k regex:"k_(igemm|wgrad|stem)" -s 399 -c 133 on
 # bench.py --steps 1 --warmup 3 --no-e2e --no-cpu-baseline --no-detail
 # --no-gates --no-graph --wgrad-streams 1.
-RECORDED_STEP_TRAFFIC: dict = {"fwd": 1542156032, "dgrad": 1462373888, "wgrad": 3211929856}
+RECORDED_STEP_TRAFFIC: dict = {"fwd": 1542712064, "dgrad": 1464861440, "wgrad": 3211740160}
 TRAFFIC_SOURCES = ("tc.cu", "simt.cu", "ptx.cuh", "conv3x3_internal.h")
-TRAFFIC_SHA256 = "d46d007fa0ed446ca769146c6cc74e179a04143755808b718397049d02062bee"
+TRAFFIC_SHA256 = "6a359b4dc76d6f26f4f49c246af42284d38b837f71e7021dc455936341eb6938"
 
 
 # The six resampling ops of a step, the same way: ncu --metrics (as above)
