@@ -65,6 +65,13 @@
  * channel tiles on two-CTA clusters.  CONV3X3_PAIR384=0 keeps 384-channel
  * outputs off the 384-wide two-CTA tile (unset: taken with at least six input
  * chunks and enough 256-pixel tiles to fill 3/8 of the GPU in one round).
+ * CONV3X3_PKS=0|1 forbids (or, where the shape allows, forces) 256-pixel x
+ * 256-channel two-CTA tiles whose K is split over the two CTA pairs of a
+ * cluster of four and summed through distributed shared memory (outputs a
+ * multiple of 256, an even input chunk count of at least four; unset: taken
+ * with at least eight input chunks where whole pair tiles would fill under
+ * half of the GPU but such clusters fill at least half of it, as on 8x8
+ * layers of 512 channels).
  * CONV3X3_KSPLIT=0|1 forces (or forbids) 128 x 256 tiles whose K is split over
  * a two-CTA cluster and summed through distributed shared memory (outputs a
  * multiple of 256 channels; unset: where such tiles fill a quarter to all of

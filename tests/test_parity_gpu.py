@@ -225,6 +225,62 @@ def test_pair_last_round_half_width_full_size(monkeypatch):
     assert np.max(np.abs(host(dx).reshape(-1)[ix] - rx)) / np.max(np.abs(rx)) <= TOL_BF16
 
 
+PKS_SHAPES = [
+    # N, Cin, Cout, H, W: one 256 x 256 tile per cluster of four, K split over its two pairs
+    (2, 256, 256, 8, 8),      # one tile, the second CTA of each pair past the last pixel
+    (4, 512, 512, 8, 8),      # two tiles across the output channels
+    (5, 256, 512, 10, 11),    # six tiles, ragged pixel tail
+    (2, 384, 256, 9, 9),      # 27 k-blocks: halves of 14 and 13 (dgrad: 384 outputs, other tiles)
+]
+
+
+@pytest.mark.parametrize("shape", PKS_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_pair_tiles_with_k_split_over_two_pairs(shape, monkeypatch):
+    monkeypatch.setenv("CONV3X3_PKS", "1")
+    t = _small(shape, seed=47)
+    x, w, b, dy = dev_tensors(t)
+    zin_h = synth.make_zin(t.layer, seed=47)
+    N, Cin, Cout, H, W = shape
+    z = torch.empty((N, H, W, Cout), dtype=torch.bfloat16, device="cuda")
+    y32 = ops.fwd(x, w, b, act=1, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    ybf = ops.fwd(x, w, b, act=1, path=L.PATH_TENSOR, z_out=z)
+    dx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    gx32 = ops.dgrad(dy, w, out_dtype=L.DT_F32, path=L.PATH_TENSOR, z_in=to_dev_bf16(zin_h), act_in=1)
+    y32b = ops.fwd(x, w, b, act=1, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert torch.equal(y32, y32b)  # the two K halves are added in a fixed way
+    ry = oracle.conv3x3_fwd(t.x, t.w, t.bias, 1)
+    assert rel_err(host(y32), ry) <= TOL_BF16
+    assert check_bf16_store(host(ybf), ry) == 0
+    assert check_bf16_store(host(z), oracle.conv3x3_fwd(t.x, t.w, t.bias, 0)) == 0
+    assert rel_err(host(dx32), oracle.conv3x3_dgrad(t.dy, t.w)) <= TOL_BF16
+    assert rel_err(host(gx32), oracle.conv3x3_dgrad_act(t.dy, t.w, zin_h, 1)) <= TOL_BF16
+
+
+def test_pair_k_split_8x8_layer_full_size(monkeypatch):
+    # 512 -> 512 channels at 8x8, batch 64 (32 tiles, 128 CTAs), the AUTO path,
+    # against one-CTA tiles and the oracle's first and last pixels
+    Lr = synth.Layer("pks", 64, 512, 512, 8, 8, act=1)
+    t = synth.make_tensors(Lr, seed=9)
+    x, w, b, dy = dev_tensors(t)
+    y = ops.fwd(x, w, b, act=1, out_dtype=L.DT_F32)
+    dx = ops.dgrad(dy, w, out_dtype=L.DT_F32)
+    monkeypatch.setenv("CONV3X3_PKS", "0")
+    y0 = ops.fwd(x, w, b, act=1, out_dtype=L.DT_F32)
+    dx0 = ops.dgrad(dy, w, out_dtype=L.DT_F32)
+    torch.cuda.synchronize()
+    assert rel_err(host(y), host(y0)) <= 1e-5
+    assert rel_err(host(dx), host(dx0)) <= 1e-5
+    P = Lr.N * Lr.H * Lr.W
+    pix = np.array([0, 1, 129, 255, 256, P - 257, P - 1])
+    iy = (pix[:, None] * Lr.Cout + np.arange(Lr.Cout)[None, :]).reshape(-1)
+    ix = (pix[:, None] * Lr.Cin + np.arange(Lr.Cin)[None, :]).reshape(-1)
+    ry = oracle.conv3x3_fwd_at(t.x, t.w, t.bias, 1, iy)
+    rx = oracle.conv3x3_dgrad_at(t.dy, t.w, ix)
+    assert np.max(np.abs(host(y).reshape(-1)[iy] - ry)) / np.max(np.abs(ry)) <= TOL_BF16
+    assert np.max(np.abs(host(dx).reshape(-1)[ix] - rx)) / np.max(np.abs(rx)) <= TOL_BF16
+
+
 @pytest.mark.parametrize("pair384", ["auto", "0"], ids=["pair384", "one_cta"])
 @pytest.mark.parametrize("shape", [(2, 384, 384, 16, 16), (1, 256, 384, 16, 16), (3, 128, 384, 9, 13),
                                    (1, 896, 384, 8, 8)], ids=lambda s: "x".join(map(str, s)))

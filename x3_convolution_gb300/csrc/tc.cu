@@ -1443,6 +1443,267 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
 }
 
 // ----------------------------------------------------------------------------
+// forward / dgrad: 256-pixel x 256-channel pair tiles with K split over two
+// pairs (clusters of four CTAs)
+// ----------------------------------------------------------------------------
+// For grids too small for whole pair tiles (the 8x8 layers: 4096 pixels x 512
+// channels are 32 tiles of 256 x 256, 64 CTAs).  Ranks 0-1 and 2-3 of a
+// cluster are two CTA pairs (tcgen05 cta_group::2, peers differ in rank bit
+// 0); pair h = rank >> 1 runs the tile's k-blocks [h kh, h kh + kh) with the
+// M = 256, N = 256 MMAs of k_igemm_pair (two 64-channel chunks per stage: each
+// CTA streams 32 KB per 1024 cycles of tensor work), so the tile's 128 CTAs
+// fill most of the GPU.  Each CTA then holds its 128 pixels x 256 channels of
+// one K half.  The two CTAs with the same pixels (ranks r and r ^ 2) add them
+// through distributed shared memory as k_igemm_ks does: each writes the 128
+// columns the other stores into the other's (then idle) stage memory, then
+// adds the received half to its own and stores it; both add the same two fp32
+// values in the same order, so a column's sum does not depend on which CTA
+// stores it.  Every wait is bounded; the cluster barriers are reached by
+// every thread on every path.
+constexpr int kPksBN = 256;
+constexpr int kPksKC = 2;
+
+template <bool kDgrad, bool kExt>
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kIgemmThreads, 1)
+    k_igemm_pks(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                const __grid_constant__ CUtensorMap tmB, const IgemmParams p) {
+  using Cfg = PairCfg<kPksBN, kDgrad, kPksKC>;
+  constexpr int S = Cfg::kStages;
+  constexpr int KC = kPksKC;
+  constexpr uint32_t kStageBytes = Cfg::kStage;
+  static_assert((uint32_t)S * Cfg::kStage >= 128u * 128u * 4u, "the exchange reuses the stage memory");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * kStageBytes);
+  uint64_t* empty = full + S;
+  uint64_t* drain = empty + S;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t pr = rank & 1u;        // pixel half within the pair
+  const uint32_t h = rank >> 1;         // K half
+  const uint32_t leader = rank & ~1u;   // the pair's MMA-issuing CTA
+  const int tile = blockIdx.x >> 2;
+  const int mt = tile / p.num_n_tiles, nt = tile - mt * p.num_n_tiles;
+  const int HW = p.H * p.W;
+  const int kb_total = 9 * (p.kchunks / KC);
+  const int kb_half = (kb_total + 1) / 2;
+  const int kb0 = (int)h * kb_half;
+  const int kb1 = min(kb_total, kb0 + kb_half);
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], Cfg::kSP ? 1 : kProd);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    if (p.kchunks_a < p.kchunks) tma_prefetch_desc(&tmA2);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc_pair(tmem_slot, kPksBN);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the previous kernel's writes are visible from here on
+  const uint32_t full_l = cluster_addr(full, leader);
+  // epilogue warp ew stores columns 128 h + 64 ((ew >> 2) & 1) .. + 63: their
+  // bias is staged while the main loop runs
+  float* bsl = reinterpret_cast<float*>(smem + (size_t)S * kStageBytes + 256) + (warp - kEpiBase) * 64;
+  if (warp >= kEpiBase && !kDgrad && p.bias)
+    stage_bias_slice<64>(p, nt * kPksBN + 128 * (int)h + 64 * (((warp - kEpiBase) >> 2) & 1), bsl, lane);
+
+  if (warp < kProd) {
+    // as k_igemm_pair: per chunk this CTA's A box, then its 128 weight rows
+    // (one box forward, two 64-channel boxes dgrad); the leader's full barrier
+    // counts both CTAs' bytes
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      constexpr int kBPer = kDgrad ? Cfg::kDgradBoxes : 1;
+      constexpr int kPer = 1 + kBPer;
+      constexpr int kBoxes = KC * kPer;
+      constexpr uint32_t kBBox = kDgrad ? 8192u : Cfg::kBHalf;
+      uint32_t my_bytes = 0;
+      for (int b = warp; b < kBoxes; b += kProd) my_bytes += b % kPer == 0 ? kABytes : kBBox;
+      const int kgroups = p.kchunks / KC;
+      const int p0 = mt * 2 * BM + (int)pr * BM;  // this CTA's 128 pixels
+      const int n0 = p0 / HW, rem = p0 - n0 * HW;
+      const int h0 = rem / p.W;
+      const int cn = n0, ch = p.ustride * h0 - 1, cw = p.ustride * (rem - h0 * p.W) - 1;
+      const int c0 = nt * kPksBN + (int)pr * Cfg::kHalf;  // this CTA's weight rows
+      for (int kb = kb0; kb < kb1; ++kb) {
+        const int tap = kb / kgroups, cg = (kb - tap * kgroups) * KC;
+        if (!Cfg::kSP || issued % kProd == warp) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + (size_t)stage * kStageBytes;
+          uint8_t* sb = sa + KC * kABytes;
+          const uint32_t fb = full_l + (uint32_t)stage * 8u;
+          if (pr == 0) mbar_arrive_expect_tx(&full[stage], Cfg::kSP ? 2 * kStageBytes : 2 * my_bytes);
+          const int wtap = kDgrad ? 8 - tap : tap;
+#pragma unroll
+          for (int b = 0; b < kBoxes; ++b) {
+            if (!Cfg::kSP && b % kProd != warp) continue;
+            const int c = b / kPer, r = b - c * kPer, cc = cg + c;
+            if (r == 0) {
+              const bool second = cc >= p.kchunks_a;
+              tma_load_im2col_4d_pair(sa + c * kABytes, second ? &tmA2 : &tmA, fb,
+                                      (second ? cc - p.kchunks_a : cc) * BKC, cw, ch, cn, (uint16_t)(tap % 3),
+                                      (uint16_t)(tap / 3));
+            } else if (!kDgrad) {
+              tma_load_3d_pair(sb + c * Cfg::kBHalf, &tmB, fb, cc * BKC, wtap, c0);
+            } else {
+              const int j = r - 1;
+              tma_load_3d_pair(sb + c * Cfg::kBHalf + j * 8192, &tmB, fb, c0 + j * 64, wtap, cc * BKC);
+            }
+          }
+        }
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) {
+        if (pr == 0) {
+          // wait (bounded) for the loads still in flight
+          int n = issued < S ? issued : S;
+          int st = stage;
+          uint32_t ph = phase;
+          for (int i = 0; i < n; ++i) {
+            if (--st < 0) {
+              st = S - 1;
+              ph ^= 1;
+            }
+            mbar_wait(&full[st], ph, drain_wait_ns(p.wait_ns), nullptr, nullptr);
+          }
+        } else {
+          // the peer's loads complete on the leader's barriers: give them time to land
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer (the pair's leader)
+    if (pr == 0 && lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, kPksBN, 0, kDgrad ? 1 : 0);
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, kSwizzle128B);
+      const uint64_t b_desc0 = kDgrad ? smem_desc(sbase + KC * kABytes, 8192, 1024, kSwizzle128B)
+                                      : smem_desc(sbase + KC * kABytes, 16, 1024, kSwizzle128B);
+      constexpr uint32_t kStageStep = kStageBytes >> 4;
+      constexpr uint32_t kBKStep = (kDgrad ? 2048u : 32u) >> 4;
+      constexpr uint32_t kAKStep = 32u >> 4;
+      const uint16_t mask = (uint16_t)(0x3u << leader);  // both CTAs of this pair
+      int stage = 0;
+      uint32_t phase = 0, stage_off = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, abort_flag)) break;
+        tc_fence_after();
+        const uint64_t ad = a_desc0 + stage_off, bd = b_desc0 + stage_off;
+#pragma unroll
+        for (int c = 0; c < KC; ++c)
+#pragma unroll
+          for (int k = 0; k < BKC / 16; ++k)
+            tc_mma_bf16_pair(tmem_base, ad + (uint64_t)(c * (kABytes >> 4) + k * kAKStep),
+                             bd + (uint64_t)(c * (Cfg::kBHalf >> 4) + k * kBKStep), idesc,
+                             (kb != kb0 || c != 0 || k != 0) ? 1u : 0u);
+        tc_commit_pair_mc(&empty[stage], mask);
+        stage_off += kStageStep;
+        if (++stage == S) {
+          stage = 0;
+          stage_off = 0;
+          phase ^= 1;
+        }
+      }
+      // every issued MMA (which reads both CTAs' shared memory and writes both
+      // TMEMs) retires before the cluster barrier below
+      tc_commit_pair(drain);
+      mbar_wait(drain, 0, p.wait_ns, nullptr, nullptr);
+    }
+    __syncwarp();
+  }
+
+  // all four CTAs' accumulators are complete and their stage memory idle
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const int ew = warp - kEpiBase;
+  const int q = warp & 3;
+  const int hw = (ew >> 2) & 1;  // which 64 of the CTA's 128 exchanged / stored columns
+  const int row = q * 32 + lane;
+  const uint32_t lane_addr = tmem_base + ((uint32_t)(q * 32) << 16);
+  const bool run = warp >= kEpiBase && !*abort_flag;
+  if (run) {
+    // send the partner's columns [128 (h ^ 1) + 64 hw, +64) into its stage memory
+    const uint32_t peer_buf = cluster_addr(smem, rank ^ 2u);
+#pragma unroll 1
+    for (int j = 0; j < 2; ++j) {
+      const int cl = hw * 64 + j * 32;  // column within the partner's half
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(lane_addr + (uint32_t)(128 * (h ^ 1u) + cl), v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        st_cluster_v4(peer_buf + (uint32_t)(((cl / 4 + g) * 128 + row) * 16), v[4 * g], v[4 * g + 1], v[4 * g + 2],
+                      v[4 * g + 3]);
+    }
+  }
+  // the received columns are visible once every thread passes here
+  __syncwarp();
+  cluster_sync();
+  if (run) {
+    const long long pix = (long long)mt * 2 * BM + (long long)pr * BM + row;
+    const bool valid = pix < p.P;
+    const uint4* recv = reinterpret_cast<const uint4*>(smem);
+#pragma unroll 1
+    for (int j = 0; j < 2; ++j) {
+      const int cl = hw * 64 + j * 32;  // column within this CTA's half
+      const int col0 = nt * kPksBN + 128 * (int)h + cl;
+      const bool live = valid && col0 < p.nout;
+      float bv[32];
+      if (!kDgrad && p.bias && live) bias_from_slice(bsl + j * 32, bv);
+      uint4 zr[4] = {};
+      if (kExt && kDgrad && p.zin && live) load_zin(p, pix, col0, zr);
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(lane_addr + (uint32_t)(128 * h + cl), v);
+      tmem_ld_wait();
+      // own K half + the partner's (one fp32 addition per element: the same
+      // sum whichever CTA forms it)
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const uint4 r = recv[(cl / 4 + g) * 128 + row];
+        v[4 * g] = __float_as_uint(__uint_as_float(v[4 * g]) + __uint_as_float(r.x));
+        v[4 * g + 1] = __float_as_uint(__uint_as_float(v[4 * g + 1]) + __uint_as_float(r.y));
+        v[4 * g + 2] = __float_as_uint(__uint_as_float(v[4 * g + 2]) + __uint_as_float(r.z));
+        v[4 * g + 3] = __float_as_uint(__uint_as_float(v[4 * g + 3]) + __uint_as_float(r.w));
+      }
+      if (live) store_chunk<kExt, kDgrad ? 1 : 0>(p, pix, col0, v, bv, zr);
+    }
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc_pair(tmem_base, kPksBN);
+}
+
+// ----------------------------------------------------------------------------
 // forward / dgrad implicit GEMM, halo variant (image widths 16, 32, 64)
 // ----------------------------------------------------------------------------
 // A CTA tile is R = 256 / W whole image rows (256 output pixels, two 128-row
@@ -3817,10 +4078,11 @@ int launch_igemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap&
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
-// Resident two-CTA clusters of k_igemm_pair (a GPC with an odd number of free
-// SMs leaves one idle), cached per kernel and device.
+// Resident clusters of `csize` CTAs (two for k_igemm_pair, four for
+// k_igemm_pks; a GPC whose free SMs are not a multiple of the cluster size
+// leaves some idle), cached per kernel and device.
 template <typename K>
-int pair_slots(K kernel, size_t smem, const DevCtx& d) {
+int pair_slots(K kernel, size_t smem, const DevCtx& d, int csize = 2) {
   constexpr int kKeys = 16;
   static std::mutex mu;
   static int cache[kKeys][64] = {};
@@ -3832,13 +4094,13 @@ int pair_slots(K kernel, size_t smem, const DevCtx& d) {
   if (cacheable && keys[slot] == (const void*)kernel && cache[slot][d.device] > 0)
     return cache[slot][d.device];
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * (d.num_sms / 2), 1, 1);
+  cfg.gridDim = dim3(csize * (d.num_sms / csize), 1, 1);
   cfg.blockDim = dim3(kIgemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
     (void)cudaGetLastError();
-    n = d.num_sms / 2;
+    n = d.num_sms / csize;
   }
   if (cacheable) {
     keys[slot] = (const void*)kernel;
@@ -3890,6 +4152,22 @@ int launch_igemm_ks(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorM
   if (set_smem(kern, kKsSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int grid = 2 * prm.num_m_tiles * prm.num_n_tiles;  // one tile per cluster
   launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), kKsSmem, st, a, a2, b, prm);
+  return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
+}
+
+// K split over two pairs: one 256 x 256 tile per cluster of four.  Returns
+// CONV3X3_ERR_UNSUPPORTED (nothing launched) where the tiles' clusters do not
+// all fit on the GPU at once.
+template <bool kDgrad>
+int launch_igemm_pks(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b,
+                     const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
+  using Cfg = PairCfg<kPksBN, kDgrad, kPksKC>;
+  const bool ext = prm.zout || prm.zin || prm.out2;
+  auto kern = ext ? k_igemm_pks<kDgrad, true> : k_igemm_pks<kDgrad, false>;
+  if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
+  const int tiles = prm.num_m_tiles * prm.num_n_tiles;
+  if (tiles > pair_slots(kern, Cfg::kSmem, d, 4)) return CONV3X3_ERR_UNSUPPORTED;
+  launch_pdl(kern, dim3(4 * tiles), dim3(kIgemmThreads), Cfg::kSmem, st, a, a2, b, prm);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
@@ -4272,6 +4550,34 @@ int run_igemm(bool dgrad, const void* a_src, int a_ch, const void* w, const floa
   if (const char* e = std::getenv("CONV3X3_PAIR384"))
     if (std::strcmp(e, "0") == 0) p384 = false;
   if (p384) pair_bn = 384;
+  // K split over two pairs (k_igemm_pks) where 256 x 256 pair tiles would
+  // leave most pairs idle but their clusters of four fill at least half of
+  // the GPU at once, with an even input chunk count (two chunks per stage) of
+  // at least eight: the 8x8 layers of 512 output channels.  Measured on GB300
+  // (batch 64, 8x8, per call): 1024 -> 512 forward 39.4 -> 35.1 us against
+  // the one-CTA K split, 512 -> 512 dgrad 25.0 -> 24.5 us and forward equal
+  // against 128 x 128 tiles; 384 -> 512 (six chunks) 20.8 -> 22.8 us, so it
+  // keeps 128 x 128 tiles.  Not under a forced tile (CONV3X3_TILE);
+  // CONV3X3_PKS=0|1 forbids it, or takes it wherever the shape allows (at
+  // least four chunks) and the clusters fit.
+  const long long pks_tiles = (g.P() + 2 * BM - 1) / (2 * BM) * ((nout + kPksBN - 1) / kPksBN);
+  const bool pks_shape = !s2 && !ts.halo && pair_bn == 0 && nout % kPksBN == 0 && prm.kchunks % 2 == 0 &&
+                         prm.kchunks >= 4;
+  bool pks = pks_shape && prm.kchunks >= 8 && std::getenv("CONV3X3_TILE") == nullptr &&
+             4 * pks_tiles <= d.num_sms && 8 * pks_tiles >= d.num_sms;
+  if (const char* e = std::getenv("CONV3X3_PKS")) pks = std::strcmp(e, "0") != 0 && pks_shape;
+  if (pks) {
+    IgemmParams pq = prm;
+    pq.num_m_tiles = (int)((g.P() + 2 * BM - 1) / (2 * BM));
+    pq.num_n_tiles = nout / kPksBN;
+    CUtensorMap tq = tb;
+    if (!dgrad) {  // 128 weight rows per CTA in one box (dgrad's map has 64-channel boxes)
+      rc = make_weight_map(&tq, w, s.Cin, s.Cout, kPksBN / 2);
+      if (rc) return rc;
+    }
+    rc = dgrad ? launch_igemm_pks<true>(ta, ta2, tq, pq, d, st) : launch_igemm_pks<false>(ta, ta2, tq, pq, d, st);
+    if (rc != CONV3X3_ERR_UNSUPPORTED) return rc;  // (else the clusters do not fit: the tiles below)
+  }
   // K split over two-CTA clusters (k_igemm_ks) where 128 x 256 tiles fill
   // between a quarter and all of the GPU's SMs in pairs and K is long: the
   // 8x8 layers with 1024 input channels.  Measured on GB300 (batch 64, 8x8):
