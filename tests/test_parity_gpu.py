@@ -356,6 +356,32 @@ def test_k_split_fused_and_concat(monkeypatch):
     assert rel_err(got, ref) <= TOL_BF16
 
 
+def test_pks_fused_concat_and_strided(monkeypatch):
+    # the concat-free calls (a chunk pair across the split), the fused activation
+    # backward and a stride-2 forward on K-split pair tiles
+    monkeypatch.setenv("CONV3X3_PKS", "1")
+    shape = (2, 192, 64, 256, 6, 7)  # N, Ca, Cb, Cout, H, W
+    N, Ca, Cb, Cout, H, W = shape
+    t, zin_h, _ = _cat_case(shape)
+    x, w, b, dy = dev_tensors(t)
+    xa, xb = x[..., :Ca].contiguous(), x[..., Ca:].contiguous()
+    y32 = ops.fwd_cat(xa, xb, w, b, act=1, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert rel_err(host(y32), oracle.conv3x3_fwd_cat(t.x[..., :Ca], t.x[..., Ca:], t.w, t.bias, 1)) <= TOL_BF16
+    zin = to_dev_bf16(zin_h)
+    za, zb = zin[..., :Ca].contiguous(), zin[..., Ca:].contiguous()
+    gxa, gxb = ops.dgrad_cat(dy, w, Ca, out_dtype=L.DT_F32, path=L.PATH_TENSOR, za_in=za, zb_in=zb,
+                             act_in=1)
+    torch.cuda.synchronize()
+    got = np.concatenate([host(gxa), host(gxb)], axis=-1)
+    assert rel_err(got, oracle.conv3x3_dgrad_act(t.dy, t.w, zin_h, 1)) <= TOL_BF16
+    ts = _small((2, 256, 256, 9, 9), seed=53)
+    xs, ws, bs, _ = dev_tensors(ts)
+    ys = ops.fwd_strided(xs, ws, bs, stride=2, act=1, out_dtype=L.DT_F32, path=L.PATH_TENSOR)
+    torch.cuda.synchronize()
+    assert rel_err(host(ys), oracle.conv3x3_fwd_strided(ts.x, ts.w, ts.bias, 1, 2)) <= TOL_BF16
+
+
 HALO_SHAPES = [
     (2, 64, 64, 16, 16),    # W = 16: one tile = one whole image
     (1, 72, 200, 8, 32),    # W = 32, ragged channel chunk and ragged N tile
