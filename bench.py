@@ -421,6 +421,20 @@ def recorded_traffic(config, pas):
     return RECORDED_TRAFFIC[(config, pas)] if sources_sha256() == TRAFFIC_SHA256 else None
 
 
+def recorded_pass_traffic(workload, pas, fused_act=False, concat_free=False, path="auto"):
+    """DRAM bytes per step of pass `pas` for the bench line's roofline: the
+    recorded whole-step capture for the UNet step, the per-call capture for a
+    per-layer config; None for any other workload or variant (the fused or
+    concat-free calls and forced paths run other kernels than those captured)
+    and when the kernels changed since."""
+    if fused_act or concat_free or path != "auto" or TRAFFIC_SHA256 is None:
+        return None
+    if workload == "unet":
+        t = RECORDED_STEP_TRAFFIC.get(pas)
+        return t if t is not None and sources_sha256() == TRAFFIC_SHA256 else None
+    return recorded_traffic(workload, pas)
+
+
 def pick_peak(peaks, clocks, timed_s):
     """The tensor peak the step is held to: the burst figure (cuBLAS timed in
     isolation) when the timed region is short and the SM clock stayed near its
@@ -863,8 +877,8 @@ def cuda_arm(args):
                          peaks["source"], "bf16 burst" if peak_key == "bf16_tflops" else
                          "bf16 sustained", "short timed region at full SM clock"
                          if peak_key == "bf16_tflops" else "long or throttled timed region"),
-                     "traffic": (RECORDED_STEP_TRAFFIC.get(dom)
-                                 if sources_sha256() == TRAFFIC_SHA256 else None),
+                     "traffic": recorded_pass_traffic(args.workload, dom, args.fused_act,
+                                                      args.concat_free, args.path),
                      "traffic_note": "DRAM bytes of the pass's launches per step from one scoped "
                                      "ncu capture of a whole step (one pass per launch, caches "
                                      "flushed before each; writes still in L2 at a launch's end "

@@ -92,6 +92,22 @@ def test_recorded_traffic_guard(monkeypatch):
     assert bench.recorded_traffic("l1", "fwd") is None
 
 
+def test_recorded_pass_traffic_by_workload(monkeypatch):
+    monkeypatch.setattr(bench, "RECORDED_TRAFFIC", {("l1", "fwd"): 1.5e8})
+    monkeypatch.setattr(bench, "RECORDED_STEP_TRAFFIC", {"fwd": 1.5e9})
+    monkeypatch.setattr(bench, "TRAFFIC_SHA256", bench.sources_sha256())
+    assert bench.recorded_pass_traffic("unet", "fwd") == 1.5e9
+    assert bench.recorded_pass_traffic("l1", "fwd") == 1.5e8
+    # the step's figure never stands for another workload, nor the plain kernels' for variants
+    assert bench.recorded_pass_traffic("l2", "fwd") is None
+    assert bench.recorded_pass_traffic("stack", "fwd") is None
+    assert bench.recorded_pass_traffic("unet", "fwd", fused_act=True) is None
+    assert bench.recorded_pass_traffic("unet", "fwd", concat_free=True) is None
+    assert bench.recorded_pass_traffic("l1", "fwd", path="simt") is None
+    monkeypatch.setattr(bench, "TRAFFIC_SHA256", "0" * 64)
+    assert bench.recorded_pass_traffic("unet", "fwd") is None
+
+
 def test_peak_choice():
     peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
     full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0}
