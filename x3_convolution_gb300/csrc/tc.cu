@@ -82,6 +82,9 @@ constexpr int kMmaWarp = kProd;
 constexpr int kEpiBase = kProd + 1;
 constexpr int kEpiWarps = 8;         // igemm: two epilogue warps per TMEM lane quarter
 constexpr int kIgemmThreads = 32 * (kProd + 1 + kEpiWarps);
+// block size of k_igemm: the transposed tile with the fused extras runs
+// 2 + 1 + 12 warps
+constexpr int igemm_threads(bool wide_epilogue) { return wide_epilogue ? 32 * 15 : kIgemmThreads; }
 constexpr int kWgEpiWarps = 4;       // wgrad: one epilogue warp per lane quarter
 constexpr int kThreads = 32 * (kProd + 1 + kWgEpiWarps);
 constexpr uint32_t kABytes = BM * BKC * 2;
@@ -397,7 +400,7 @@ __device__ __forceinline__ void s2_tap(int cls, int t, int& wtap, int& dj, int& 
 // that channel's z_in the same way).  No stride-2 dgrad (the dispatch sends
 // it to the untransposed tile).
 template <int BN, int MT, bool kDgrad, bool kExt, int KC, bool kT = false>
-__global__ void __launch_bounds__(kIgemmThreads, 1)
+__global__ void __launch_bounds__(igemm_threads(kT && kExt), 1)
     k_igemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
             const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmY,
             const IgemmParams p) {
@@ -405,10 +408,20 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   using Cfg = IgemmCfg<BN, MT, KC>;
   constexpr int S = Cfg::kStages;
   constexpr int TM = BM * MT;  // pixels per CTA tile
+  // Warp roles: NP TMA producer warps, the MMA warp, NE epilogue warps.  The
+  // transposed tile with the fused extras, whose epilogue (one channel per
+  // thread, z loads or stores per element) outlasts its main loop, runs two
+  // producer warps and twelve epilogue warps (three per TMEM lane quarter):
+  // 128-channel 64x64 fused dgrad 88 -> 74 us.  The plain transposed tile
+  // keeps four producers and eight epilogue warps: with one producer its main
+  // loop, which sets its pace, ran 2.5 us longer.
+  constexpr bool kWide = kT && kExt;
+  constexpr int NP = kWide ? 2 : kProd, MW = NP, EB = NP + 1, NE = kWide ? 12 : kEpiWarps;
+  static_assert(32 * (NP + 1 + NE) == igemm_threads(kWide), "warp roles and block size");
   // A producer's parity wait on a stage is unambiguous only while no producer
-  // can run a whole ring ahead: stage-parallel mode needs S >= kProd.
-  constexpr bool kSP = Cfg::kStagePar;
-  static_assert(!kSP || S >= kProd, "stage-parallel producers need S >= kProd");
+  // can run a whole ring ahead: stage-parallel mode needs S >= NP.
+  constexpr bool kSP = kWide ? kStageParallel && S >= NP : Cfg::kStagePar;
+  static_assert(!kSP || S >= NP, "stage-parallel producers need S >= NP");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * Cfg::kStageBytes);
@@ -427,12 +440,12 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], kSP ? 1 : kProd);
+      mbar_init(&full[i], kSP ? 1 : NP);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], kEpiWarps);
+      mbar_init(&tempty[i], NE);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -441,7 +454,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     if (p.kchunks_a < p.kchunks) tma_prefetch_desc(&tmA2);
     tma_prefetch_desc(&tmB);
   }
-  if (warp == kMmaWarp) {
+  if (warp == MW) {
     tmem_alloc(tmem_slot, Cfg::kTmemCols);
     tmem_relinquish();
   }
@@ -451,11 +464,11 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // the previous kernel's writes are visible from here on
 
-  if (warp < kProd) {
+  if (warp < NP) {
     // ------------------------------------------------------------ TMA producers
     // Stage boxes: MT im2col A boxes (128 pixels x 64 channels) then BN/64
     // weight boxes (64 rows x 64 channels); producer `warp` issues box b when
-    // b % kProd == warp and registers its own byte count on the full barrier.
+    // b % NP == warp and registers its own byte count on the full barrier.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -488,8 +501,8 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
             off_h = tap / 3;
             wtap = kDgrad ? 8 - tap : tap;
           }
-          // stage-parallel mode: this producer owns every kProd-th stage
-          const bool mine = kSP ? (issued % kProd == warp) : true;
+          // stage-parallel mode: this producer owns every NP-th stage
+          const bool mine = kSP ? (issued % NP == warp) : true;
           if (mine) {
             if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
               ok = false;
@@ -507,11 +520,11 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
             uint32_t bytes = 0;
 #pragma unroll
             for (int b = 0; b < kBoxes; ++b)
-              if (kSP || b % kProd == warp) bytes += b % kPer < MT ? kABytes : kBBox;
+              if (kSP || b % NP == warp) bytes += b % kPer < MT ? kABytes : kBBox;
             mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
             for (int b = 0; b < kBoxes; ++b) {
-              if (!kSP && b % kProd != warp) continue;
+              if (!kSP && b % NP != warp) continue;
               // chunk cc of the stage (a chunk past the channels reads zeros)
               const int c = b / kPer, r = b - c * kPer, cc = cg + c;
               if (r < MT) {
@@ -552,7 +565,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+  } else if (warp == MW) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, kDgrad ? 1 : 0);
@@ -630,12 +643,13 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   } else if constexpr (kT) {
     // ------------------------------------------------------------ epilogue (transposed)
     // TMEM lane = output channel, column = pixel of the 256-pixel tile.  Warp
-    // w reads lanes 32*(w%4) .. +31 (32 channels); the two warps of a lane
-    // quarter take 128 pixels each.  A thread owns one channel, so a 32-pixel
-    // chunk leaves as 32 scalar stores, each a 64-byte (bf16) or 128-byte
-    // (fp32) contiguous run across the warp.
+    // w reads lanes 32*(w%4) .. +31 (32 channels); the NE / 4 warps of a lane
+    // quarter take the tile's eight 32-pixel chunks in turn (part, part +
+    // NE / 4, ...).  A thread owns one channel, so a chunk leaves as 32 scalar stores,
+    // each a 64-byte (bf16) or 128-byte (fp32) contiguous run across the warp.
+    constexpr int kParts = NE / 4, kChunks = TM / 32;
     const int q = warp & 3;
-    const int half = (warp - kEpiBase) >> 2;
+    const int part = (warp - EB) >> 2;
     int buf = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -649,23 +663,22 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       void* obase = second ? p.out2 : p.out;
       const long long ostride = !kExt ? p.nout : second ? p.nout - p.nsplit : p.nsplit;
       const int ocol = second ? ch - p.nsplit : ch;
-      const long long pix_base = (long long)ti.mt * TM + half * BM;
+      const long long pix_base = (long long)ti.mt * TM;
       if (kExt && p.zin && ch_ok) {
         // L2 prefetch of the z_in the warp reads for this tile (its 32
         // channels, one 64-byte run per pixel) while the MMAs still run
         const __nv_bfloat16* zq = (second ? p.zin2 : p.zin) + (ocol - lane);
-#pragma unroll
-        for (int k = 0; k < BM / 32; ++k) {
+#pragma unroll 1
+        for (int k = part; k < kChunks; k += kParts) {
           const long long px = pix_base + k * 32 + lane;
           if (px < p.P) asm volatile("prefetch.global.L2 [%0];" ::"l"(zq + px * ostride));
         }
       }
       if (!mbar_wait(&tfull[buf], acc_phase, p.wait_ns, p.status, abort_flag)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
-                             (uint32_t)(buf * MT * BN + half * BM);
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * MT * BN);
 #pragma unroll 1
-      for (int j = 0; j < BM / 32; ++j) {
+      for (int j = part; j < kChunks; j += kParts) {
         const long long pix0 = pix_base + j * 32;
         const int npix = p.P - pix0 < 32 ? (int)(p.P - pix0) : 32;  // <= 0 past the end
         // z_in of this channel at the chunk's 32 pixels (fused dgrad), loaded
@@ -675,11 +688,11 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
         if (kExt && p.zin && ch_ok) {
           const unsigned short* zp =
               reinterpret_cast<const unsigned short*>(second ? p.zin2 : p.zin) + pix0 * ostride + ocol;
-          // the next chunk's 32 pixels into L1 (one 64-byte run per lane)
-          // while this chunk is processed; this chunk's were fetched during
-          // the previous one (or, for the first, come from L2)
-          if (j + 1 < BM / 32 && pix0 + 32 + lane < p.P)
-            asm volatile("prefetch.global.L1 [%0];" ::"l"(zp - lane + (32 + lane) * ostride));
+          // this warp's next chunk's 32 pixels into L1 (one 64-byte run per
+          // lane) while this chunk is processed; this chunk's were fetched
+          // during the previous one (or, for the first, come from L2)
+          if (j + kParts < kChunks && pix0 + 32 * kParts + lane < p.P)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(zp - lane + (32 * kParts + lane) * ostride));
 #pragma unroll
           for (int i = 0; i < 32; ++i) zr[i] = i < npix ? __ldg(zp + i * ostride) : (unsigned short)0;
         }
@@ -735,11 +748,11 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
     // of the single sub-tile (MT = 1).
     constexpr int kCols = Cfg::kEpiCols;
     const int q = warp & 3;
-    const int half = (warp - kEpiBase) >> 2;
+    const int half = (warp - EB) >> 2;
     const int sub = MT == 2 ? half : 0;
     const int col_off = MT == 2 ? 0 : half * kCols;
     const int row = q * 32 + lane;
-    float* bsl = reinterpret_cast<float*>(smem + (size_t)S * Cfg::kStageBytes + 256) + (warp - kEpiBase) * kCols;
+    float* bsl = reinterpret_cast<float*>(smem + (size_t)S * Cfg::kStageBytes + 256) + (warp - EB) * kCols;
     int buf = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -769,7 +782,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
         if (tma_here) {
           // every MMA of the tile has completed, so no stage is in use; this
           // warp's 32 pixels leave as kCols / 64 boxes of {64 channels, 32 pixels}
-          uint8_t* stg = smem + (size_t)(warp - kEpiBase) * (kCols / 64) * 4096u;
+          uint8_t* stg = smem + (size_t)(warp - EB) * (kCols / 64) * 4096u;
           const long long wrow0 = (long long)mt * TM + sub * BM + q * 32;
 #pragma unroll 1
           for (int j = 0; j < kCols / 32; ++j) {
@@ -823,7 +836,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  if (warp == MW) tmem_dealloc(tmem_base, Cfg::kTmemCols);
 }
 
 // ----------------------------------------------------------------------------
@@ -4074,7 +4087,7 @@ int launch_igemm(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap&
   IgemmParams p2 = prm;
   CUtensorMap ty;
   epi_tma_setup(p2, !kT, tiles, grid, a, &ty);  // (the transposed tile has its own epilogue)
-  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, a2, b, ty, p2);
+  launch_pdl(kern, dim3(grid), dim3(igemm_threads(kT && ext)), Cfg::kSmem, st, a, a2, b, ty, p2);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
