@@ -1007,9 +1007,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kIgemmThreads, 1)
         // this CTA's weight rows (output channels): half of the tile's, or of the item's 128
         const int c0 = nt * kPairBN + w.coff + (int)rank * (w.half ? 64 : Cfg::kHalf);
         const int kblocks = 9 * kgroups;
+        // Box-parallel: rank 1's producers arrive on no barrier, so one with no
+        // box in this item's stages (the dgrad's second weight box of a
+        // half-width item, or a stage with fewer boxes than producers) gates
+        // nothing and could fall two phases behind on its empty barrier, then
+        // wait for a phase that never completes: it skips those stages.
+        const bool has_boxes = kSP || rank == 0 || (w.half ? my_bytes_h : my_bytes) > 0;
         for (int kb = 0; kb < kblocks; ++kb) {
           const int tap = kb / kgroups, cg = (kb - tap * kgroups) * KC;
-          if (!kSP || issued % kProd == warp) {
+          if ((!kSP || issued % kProd == warp) && has_boxes) {
             if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
               ok = false;
               break;
@@ -1556,9 +1562,11 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kIgemmThreads, 1)
       const int h0 = rem / p.W;
       const int cn = n0, ch = p.ustride * h0 - 1, cw = p.ustride * (rem - h0 * p.W) - 1;
       const int c0 = nt * kPksBN + (int)pr * Cfg::kHalf;  // this CTA's weight rows
+      // (as in k_igemm_pair: a second-rank producer without boxes skips the stages)
+      const bool has_boxes = Cfg::kSP || pr == 0 || my_bytes > 0;
       for (int kb = kb0; kb < kb1; ++kb) {
         const int tap = kb / kgroups, cg = (kb - tap * kgroups) * KC;
-        if (!Cfg::kSP || issued % kProd == warp) {
+        if ((!Cfg::kSP || issued % kProd == warp) && has_boxes) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns, p.status, abort_flag)) {
             ok = false;
             break;
