@@ -104,6 +104,9 @@
  * for one plain bf16 output: on every tile where every CTA or CTA pair has
  * one, else on each CTA's or pair's last tile); CONV3X3_EPI_TMA=1 keeps them
  * to one-tile launches.
+ * CONV3X3_STEM_ZTMA=0 makes the 8-input-channel forward that also stores z
+ * store y and z from each thread instead of through TMA tensor stores (taken
+ * with row staging, bf16 y and at most 128 output channels).
  * CONV3X3_STEM_ROWS=0 makes the 8-input-channel forward
  * and weight gradient stage x as im2col boxes even where they would stage
  * whole image rows (forward: widths 32 and 64; weight gradient: width 64,

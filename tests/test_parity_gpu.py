@@ -1229,6 +1229,35 @@ def test_last_tile_tma_stores_match_thread_stores(tile, shape, monkeypatch):
     assert check_bf16_store(host(a[0]).reshape(-1)[idx], ry) == 0
 
 
+STEM_Z_SHAPES = [
+    (2, 8, 128, 8, 64),    # width 64: 128-pixel tiles of two image rows
+    (3, 8, 128, 4, 32),    # width 32: four rows per tile
+    (2, 8, 72, 8, 64),     # channels past the last 64-wide box are clipped
+]
+
+
+@pytest.mark.parametrize("shape", STEM_Z_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_stem_forward_z_through_tma_stores(shape, monkeypatch):
+    # the 8-input-channel forward storing z (the fused training step): y and z
+    # through TMA tensor stores, against per-thread stores and the oracle
+    t = _small(shape, seed=59)
+    x, w, b, _ = dev_tensors(t)
+    N, Cin, Cout, H, W = shape
+
+    def run():
+        z = torch.empty((N, H, W, Cout), dtype=torch.bfloat16, device="cuda")
+        y = ops.fwd(x, w, b, act=1, path=L.PATH_TENSOR, z_out=z)
+        torch.cuda.synchronize()
+        return y, z
+
+    y, z = run()
+    monkeypatch.setenv("CONV3X3_STEM_ZTMA", "0")
+    y0, z0 = run()
+    assert torch.equal(y, y0) and torch.equal(z, z0)
+    assert check_bf16_store(host(z), oracle.conv3x3_fwd(t.x, t.w, t.bias, 0)) == 0
+    assert check_bf16_store(host(y), oracle.conv3x3_fwd(t.x, t.w, t.bias, 1)) == 0
+
+
 WGRAD_STORE_SHAPES = [
     (2, 128, 128, 16, 16),    # one-CTA tiles, im2col x
     (2, 128, 128, 8, 64),     # one-CTA tiles, row-shifted x (width 64)

@@ -2027,7 +2027,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
 // is then the 128 pixels that start r rows into slot s: 24 (W = 64) or 18
 // (W = 32) copy rows per tile instead of 1152.  The weights sit in the same
 // slot order.
-template <int BN, bool kTS = false, int kRW = 0>
+template <int BN, bool kTS = false, int kRW = 0, bool kZ = false>
 struct StemCfg {
   static constexpr uint32_t kTapBytes = BM * 16;           // 128 pixels x 8 channels
   static constexpr int kRowsPerTile = kRW ? BM / kRW : 0;  // image rows of a tile (kRW)
@@ -2040,13 +2040,17 @@ struct StemCfg {
   static constexpr uint32_t kStageBytes = kPadOff + kTapBytes;  // + padding tap
   static constexpr uint32_t kBTap = BN * 16;
   static constexpr uint32_t kBBytes = 10 * kBTap;
-  static constexpr int kStages = kTS ? (kRW ? 8 : 6) : 8;
+  // kZ (TMA-store epilogue only): z = conv + bias leaves through TMA stores
+  // too, from a second set of staging boxes, with four stages
+  static constexpr int kStages = kTS ? (kZ ? 4 : kRW ? 8 : 6) : 8;
   static constexpr uint32_t kStageOutBytes = 32 * 128;     // one warp's 32 x 64 bf16 box
-  static constexpr uint32_t kOutBytes = kTS ? 2 * kEpiWarps * kStageOutBytes : 0;
+  static constexpr uint32_t kOutBytes = kTS ? (kZ ? 2 : 1) * 2 * kEpiWarps * kStageOutBytes : 0;
   static constexpr int kTmemCols = pow2_cols(2 * BN);
   static constexpr size_t kSmem = (size_t)kStages * kStageBytes + kBBytes + kOutBytes + 512 + 1024;
   static_assert(kStages >= kProd, "stage-parallel producers need S >= kProd");
   static_assert(!kTS || BN == 128, "the TMA-store epilogue covers 128-channel tiles");
+  static_assert(!kZ || (kTS && kRW != 0), "z through TMA stores with row staging only");
+  static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
   static_assert(((size_t)kStages * kStageBytes + kBBytes) % 1024 == 0, "staging must be 1 KB aligned");
   static_assert(kRW == 0 || kRW == 32 || kRW == 64, "row staging for widths 32 and 64");
 };
@@ -2104,11 +2108,12 @@ __host__ __device__ constexpr uint32_t stem_a_off(int q) {
                       : (uint32_t)q * Cfg::kTapBytes;
 }
 
-template <int BN, bool kTS = false, int kRW = 0>
+template <int BN, bool kTS = false, int kRW = 0, bool kZ = false>
 __global__ void __launch_bounds__(kIgemmThreads, 1)
     k_stem_fwd(const __grid_constant__ CUtensorMap tmA, const __nv_bfloat16* __restrict__ w,
-               const __grid_constant__ CUtensorMap tmY, const IgemmParams p) {
-  using Cfg = StemCfg<BN, kTS, kRW>;
+               const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmZ,
+               const IgemmParams p) {
+  using Cfg = StemCfg<BN, kTS, kRW, kZ>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -2268,7 +2273,8 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
   } else if constexpr (kTS) {
     // epilogue, TMA-store path: warp (q, half) owns pixels 32q.. of the tile
     // and channels 64 half..; bias + activation in fp32, one bf16 rounding,
-    // staged swizzled, one TMA store per tile
+    // staged swizzled, one TMA store per tile (two with kZ: z, then y, in one
+    // bulk group)
     const int q = warp & 3;
     const int half = (warp - kEpiBase) >> 2;
     const int col_off = half * 64;
@@ -2282,6 +2288,8 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       if (lane == 0) bulk_wait_read<1>();
       __syncwarp();
       uint8_t* stg = osm + (size_t)(ew * 2 + sb) * Cfg::kStageOutBytes + lane * 128;
+      // z's boxes follow y's 2 x kEpiWarps boxes
+      uint8_t* stz = osm + (size_t)(2 * kEpiWarps + ew * 2 + sb) * Cfg::kStageOutBytes + lane * 128;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN + col_off);
       uint32_t v[2][32];
       tmem_ld_32x32b_x32(taddr, v[0]);
@@ -2291,12 +2299,14 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
       for (int j = 0; j < 2; ++j) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          uint4 u;
+          uint4 u, uz;
           __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+          __nv_bfloat162* hz = reinterpret_cast<__nv_bfloat162*>(&uz);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             float f0 = __uint_as_float(v[j][8 * g + 2 * i]);  // conv + bias
             float f1 = __uint_as_float(v[j][8 * g + 2 * i + 1]);
+            if (kZ) hz[i] = __floats2bfloat162_rn(f0, f1);
             if (p.act == CONV3X3_ACT_SILU) {
               f0 = silu_tanh_f32(f0);
               f1 = silu_tanh_f32(f1);
@@ -2308,6 +2318,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
           }
           const int chunk = (4 * j + g) ^ (lane & 7);
           *reinterpret_cast<uint4*>(stg + chunk * 16) = u;
+          if (kZ) *reinterpret_cast<uint4*>(stz + chunk * 16) = uz;
         }
       }
       tc_fence_before();
@@ -2318,8 +2329,12 @@ __global__ void __launch_bounds__(kIgemmThreads, 1)
         // one bulk group per tile (empty past the last pixel), so that
         // "all but the newest group" is always the store two tiles back
         const int row0 = tile * BM + q * 32;
-        if (row0 < p.P && col_off < p.nout)
+        if (row0 < p.P && col_off < p.nout) {
+          if (kZ)
+            tma_store_2d(&tmZ, osm + (size_t)(2 * kEpiWarps + ew * 2 + sb) * Cfg::kStageOutBytes, col_off,
+                         row0);
           tma_store_2d(&tmY, osm + (size_t)(ew * 2 + sb) * Cfg::kStageOutBytes, col_off, row0);
+        }
         bulk_commit();
       }
       sb ^= 1;
@@ -4257,14 +4272,14 @@ TileShape pick_tile(int nout, const Shape& sh, int num_sms) {
   return best;
 }
 
-template <int BN, bool kTS = false, int kRW = 0>
-int launch_stem(const CUtensorMap& a, const __nv_bfloat16* w, const CUtensorMap& y,
+template <int BN, bool kTS = false, int kRW = 0, bool kZ = false>
+int launch_stem(const CUtensorMap& a, const __nv_bfloat16* w, const CUtensorMap& y, const CUtensorMap& z,
                 const IgemmParams& prm, const DevCtx& d, cudaStream_t st) {
-  using Cfg = StemCfg<BN, kTS, kRW>;
-  auto kern = k_stem_fwd<BN, kTS, kRW>;
+  using Cfg = StemCfg<BN, kTS, kRW, kZ>;
+  auto kern = k_stem_fwd<BN, kTS, kRW, kZ>;
   if (set_smem(kern, Cfg::kSmem, d.device) != CONV3X3_OK) return CONV3X3_ERR_CUDA;
   const int grid = prm.num_m_tiles < d.num_sms ? prm.num_m_tiles : d.num_sms;
-  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, w, y, prm);
+  launch_pdl(kern, dim3(grid), dim3(kIgemmThreads), Cfg::kSmem, st, a, w, y, z, prm);
   return cudaGetLastError() == cudaSuccess ? CONV3X3_OK : CONV3X3_ERR_CUDA;
 }
 
@@ -4341,15 +4356,29 @@ int run_stem_fwd(const void* x, const void* w, const float* bias, void* y, const
   prm.wait_ns = d.wait_ns;
   prm.zout = static_cast<__nv_bfloat16*>(ex.zout);
 #define C3_STEM(BN_, TS_, Y_)                                                  \
-  return rw == 64   ? launch_stem<BN_, TS_, 64>(ta, wp, Y_, prm, d, st)          \
-         : rw == 32 ? launch_stem<BN_, TS_, 32>(ta, wp, Y_, prm, d, st)          \
-                    : launch_stem<BN_, TS_, 0>(ta, wp, Y_, prm, d, st)
+  return rw == 64   ? launch_stem<BN_, TS_, 64>(ta, wp, Y_, ta, prm, d, st)      \
+         : rw == 32 ? launch_stem<BN_, TS_, 32>(ta, wp, Y_, ta, prm, d, st)      \
+                    : launch_stem<BN_, TS_, 0>(ta, wp, Y_, ta, prm, d, st)
   if (bn == 128 && !out_f32 && !ex.zout) {
     // bf16 output with no z store leaves through TMA stores
     CUtensorMap ty;
     rc = make_store_map(&ty, y, s.P(), s.Cout);
     if (rc) return rc;
     C3_STEM(128, true, ty);
+  }
+  if (bn == 128 && !out_f32 && ex.zout && rw) {
+    // and with the z store (row staging): both through TMA stores.
+    // CONV3X3_STEM_ZTMA=0 keeps per-thread stores for both.
+    const char* e = std::getenv("CONV3X3_STEM_ZTMA");
+    if (!(e && std::strcmp(e, "0") == 0)) {
+      CUtensorMap ty, tz;
+      rc = make_store_map(&ty, y, s.P(), s.Cout);
+      if (rc) return rc;
+      rc = make_store_map(&tz, ex.zout, s.P(), s.Cout);
+      if (rc) return rc;
+      return rw == 64 ? launch_stem<128, true, 64, true>(ta, wp, ty, tz, prm, d, st)
+                      : launch_stem<128, true, 32, true>(ta, wp, ty, tz, prm, d, st);
+    }
   }
   // (without TMA stores the output map is unused: ta stands in)
   if (bn == 64) C3_STEM(64, false, ta);
